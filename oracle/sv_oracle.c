@@ -1,0 +1,593 @@
+/*
+ * sv_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, CPU oracle for the batched verify-and-accept step of
+ * speculative decoding (Leviathan rejection sampling as used by EAGLE /
+ * EAGLE-2 / EAGLE-3).  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load it.  It shares no code with the CUDA library.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [Lesson]  "Decodificação Especulativa e EAGLE-3" (ai-engineering.academy,
+ *             Phase 10 Lesson 15) and its Persian twin "دیکودینگ حدسی و
+ *             EAGLE-3" (nextadmin.net) -- same lesson, same sections.
+ *   [Blog]    "投机解码发展" (caijizhuo.github.io).  NOTE: the blog swaps the
+ *             letters (its p is the verifier, its q the draft).  This file uses
+ *             the lesson's notation throughout: p = draft, q = verifier.
+ *
+ * Precision.  Probabilities, ratios and the accept test are computed in
+ * double from logits widened exactly to double.  The inverse-CDF token
+ * choice (residual / bonus sampling) is a floating-point quantity deciding an
+ * integer; it is taken in the kernel's arithmetic, fully specified below
+ * (sample_repro): IEEE fp32 operations in a fixed order, an fp32 exponential
+ * built from Cody-Waite range reduction and a degree-7 Taylor polynomial, and
+ * exact 64-bit fixed-point sums, so that the order of summation cannot change
+ * the chosen token.  The tests pin that arithmetic against libm exp and
+ * against the double-precision residual law.
+ *
+ * Compile with -ffp-contract=off: every fused multiply-add below is explicit.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_DRAW_ACCEPT 0u
+#define ORC_DRAW_SAMPLE 1u
+#define ORC_DRAW_DRAFT 2u
+#define ORC_DRAW_TREE 3u
+
+#define ORC_ROW_NAN 1u
+#define ORC_ROW_BAD_TOKEN 2u
+#define ORC_ROW_RESID_ZERO 4u
+#define ORC_ROW_P_ZERO 8u
+#define ORC_ROW_BAD_TREE 16u
+
+/* ------------------------------------------------------------------------
+ * Philox4x32-10 counter-based generator.
+ * Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
+ * (SC'11), section on the Philox family: ten rounds of two 32x32->64
+ * multiplies (multipliers 0xD2511F53, 0xCD9E8D57), a word permutation with
+ * XOR of the high halves into the other words and the round key, and a Weyl
+ * key schedule (increments 0x9E3779B9, 0xBB67AE85) between rounds.
+ * ---------------------------------------------------------------------- */
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
+                       uint32_t out[4]) {
+  uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+    uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+    uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniform the pages call uniform() ([Lesson] Passo 1; [Blog] section 4,
+ * spec_decode / eagle_round pseudocode).  The pages leave the generator open;
+ * this build keys Philox on the seed and counts on (position, draw, sequence,
+ * step mod 2^32), and takes the top 24 bits of the first output word:
+ * u = u24 * 2^-24 in [0, 1 - 2^-24], exact in fp32 and fp64. */
+uint32_t orc_u24(uint64_t seed, uint64_t step, uint32_t seq, uint32_t pos,
+                 uint32_t draw) {
+  uint32_t ctr[4] = {pos, draw, seq, (uint32_t)step};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return out[0] >> 8;
+}
+
+/* ------------------------------------------------------------------------
+ * Double-precision softmax pieces.  The verifier returns q_1..q_{N+1} and the
+ * draft supplies p_1..p_N as full-vocabulary distributions ([Lesson] "O
+ * invariante"; [Blog] section 2, step 2 "verify").  Temperature scales the
+ * logits before the softmax (the pages name temperature as the knob that
+ * lowers acceptance: [Lesson] "Quando não recorrer"; [Blog] section 6).
+ * ---------------------------------------------------------------------- */
+
+/* 1 if the row is unusable: a NaN or +inf logit, or every logit -inf. */
+int orc_row_bad(const float *x, int V) {
+  int all_minf = 1;
+  for (int v = 0; v < V; ++v) {
+    float a = x[v];
+    if (isnan(a) || (isinf(a) && a > 0)) return 1;
+    if (!(isinf(a) && a < 0)) all_minf = 0;
+  }
+  return (V <= 0 || all_minf) ? 1 : 0;
+}
+
+/* max_v x_v / T and sum_v exp(x_v/T - max), sequential in index order. */
+void orc_row_stats(const float *x, int V, double T, double *m_out,
+                   double *s_out) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double z = (double)x[v] / T;
+    if (z > m) m = z;
+  }
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += exp((double)x[v] / T - m);
+  *m_out = m;
+  *s_out = s;
+}
+
+/* Full softmax row in double (used by the pins and the probability outputs). */
+void orc_softmax(const float *x, int V, double T, double *prob) {
+  double m, s;
+  orc_row_stats(x, V, T, &m, &s);
+  for (int v = 0; v < V; ++v) prob[v] = exp((double)x[v] / T - m) / s;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 1 of the lesson ("Passo 1: a regra de rejeição"): accept the draft
+ * token d with probability min(1, q(d)/p(d)); a draft probability <= 0 is
+ * accepted outright.  The test is u < min(1, q/p), strict.
+ * ---------------------------------------------------------------------- */
+int orc_accept(double q_prob, double p_prob, double u) {
+  if (p_prob <= 0.0) return 1;
+  double r = q_prob / p_prob;
+  return u < (r < 1.0 ? r : 1.0);
+}
+
+/* Step 2 of the lesson ("Passo 2: distribuição residual"): the residual is
+ * (q - p)_+ normalised by its L1 norm; when that norm is zero, q itself. */
+void orc_residual(const double *q, const double *p, int V, double *out) {
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double r = q[v] - p[v];
+    out[v] = r > 0.0 ? r : 0.0;
+    s += out[v];
+  }
+  if (s == 0.0) {
+    for (int v = 0; v < V; ++v) out[v] = q[v];
+    return;
+  }
+  for (int v = 0; v < V; ++v) out[v] /= s;
+}
+
+/* Inverse CDF in ascending token order: the smallest k whose cumulative
+ * weight exceeds t (the pages' sample() is unspecified; this is the plainest
+ * reading, and it is what Python's weighted choice does).  If rounding leaves
+ * no such k, the last k with positive weight. */
+int orc_invcdf_f64(const double *w, int V, double t) {
+  double c = 0.0;
+  int last_pos = -1;
+  for (int k = 0; k < V; ++k) {
+    c += w[k];
+    if (w[k] > 0.0) last_pos = k;
+    if (c > t) return k;
+  }
+  return last_pos;
+}
+
+/* ------------------------------------------------------------------------
+ * The sampling arithmetic (fp32 + exact fixed point), shared *by
+ * specification* with the GPU kernels (each side has its own code).
+ *
+ *   z_v   = fl32(x_v * invT),     invT = fl32(1 / T)
+ *   m     = max_v z_v             (exact)
+ *   e_v   = exp32(z_v - m)        (fl32 subtraction, then exp32 below)
+ *   S_e   = sum_v floor(e_v * 2^40)                     (exact uint64)
+ *   inv_s = fl32( 2^40 / fl64(S_e) )                    (fl64 divide)
+ *   q_v   = fl32(e_v * inv_s)
+ *   w_v   = max(0, fl32(q_v - p_v))   residual   |   w_v = q_v   bonus
+ *   W_v   = floor(w_v * 2^62);  S_W = sum_v W_v         (exact uint64)
+ *   if S_W == 0 (residual with q == p): W_v = floor(q_v * 2^62)
+ *   t     = floor(u24 * S_W / 2^24)                     (exact, 128-bit)
+ *   token = min { k : sum_{v<=k} W_v > t }
+ *
+ * exp32(a): 0 if a < -80; else n = rint(a*log2e) via the 1.5*2^23 shift,
+ * r = a - n*ln2 (Cody & Waite two-constant reduction, "Software Manual for the
+ * Elementary Functions", 1980), e^r by the Taylor series to degree 7 in
+ * Horner form with fused multiply-adds, scaled by 2^n.
+ * ---------------------------------------------------------------------- */
+static const float ORC_LOG2E = 0x1.715476p+0f;  /* fl32(1/ln 2) */
+static const float ORC_LN2_HI = 0x1.62e4p-1f;   /* ln 2 to 15 bits */
+static const float ORC_LN2_LO = 0x1.7f7d1cp-20f; /* fl32(ln 2 - LN2_HI) */
+static const float ORC_SHIFTER = 0x1.8p+23f;     /* 1.5 * 2^23 */
+
+float orc_exp32(float a) {
+  if (!(a >= -80.0f)) return 0.0f;
+  float t = fmaf(a, ORC_LOG2E, ORC_SHIFTER);
+  float n = t - ORC_SHIFTER;
+  float r = fmaf(-n, ORC_LN2_HI, a);
+  r = fmaf(-n, ORC_LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int ni = (int)n;
+  uint32_t bits = (uint32_t)(ni + 127) << 23;
+  float scale;
+  memcpy(&scale, &bits, sizeof scale);
+  return p * scale;
+}
+
+static float orc_zmax32(const float *x, int V, float invT) {
+  float m = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    float z = x[v] * invT;
+    if (z > m) m = z;
+  }
+  return m;
+}
+
+static float orc_inv_sum32(const float *x, int V, float invT, float m) {
+  uint64_t se = 0;
+  for (int v = 0; v < V; ++v) {
+    float e = orc_exp32(x[v] * invT - m);
+    se += (uint64_t)(e * 0x1p40f);
+  }
+  return (float)(0x1p40 / (double)se);
+}
+
+/* Residual (xp != NULL) or bonus (xp == NULL) sample in the arithmetic
+ * above.  Returns the token; *gap gets min(t - C_{k-1}, C_k - 1 - t) / S_W and
+ * *resid_zero is set when the residual mass was zero and q was used. */
+int orc_sample_repro(const float *xq, const float *xp, int V, float invT,
+                     uint32_t u24, double *gap, int *resid_zero) {
+  float mq = orc_zmax32(xq, V, invT);
+  float iq = orc_inv_sum32(xq, V, invT, mq);
+  float mp = 0.0f, ip = 0.0f;
+  if (xp) {
+    mp = orc_zmax32(xp, V, invT);
+    ip = orc_inv_sum32(xp, V, invT, mp);
+  }
+  uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
+  uint64_t S = 0;
+  int use_q = (xp == NULL);
+  *resid_zero = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    S = 0;
+    for (int v = 0; v < V; ++v) {
+      float q = orc_exp32(xq[v] * invT - mq) * iq;
+      float w;
+      if (use_q) {
+        w = q;
+      } else {
+        float p = orc_exp32(xp[v] * invT - mp) * ip;
+        float d = q - p;
+        w = d > 0.0f ? d : 0.0f;
+      }
+      W[v] = (uint64_t)(w * 0x1p62f);
+      S += W[v];
+    }
+    if (S != 0 || use_q) break;
+    use_q = 1; /* residual mass zero: fall back to q ([Lesson] Passo 2) */
+    *resid_zero = 1;
+  }
+  uint64_t t = (uint64_t)(((unsigned __int128)u24 * (unsigned __int128)S) >> 24);
+  uint64_t c = 0;
+  int k = -1;
+  for (int v = 0; v < V; ++v) {
+    uint64_t prev = c;
+    c += W[v];
+    if (c > t) {
+      uint64_t below = t - prev, above = c - 1 - t;
+      *gap = (double)(below < above ? below : above) / (double)S;
+      k = v;
+      break;
+    }
+  }
+  free(W);
+  return k;
+}
+
+/* ------------------------------------------------------------------------
+ * The verify walk ([Lesson] "O invariante" and Passo 3; [Blog] section 4,
+ * spec_decode pseudocode): walk positions left to right; at the first
+ * rejection j sample from residual(q_j, p_j) and stop; if every draft is
+ * accepted, sample a bonus token from q_{N+1}.  The bonus is emitted only on
+ * full acceptance (the blog's eagle_round listing appends it unconditionally,
+ * which contradicts its own worked example of 2 accepted + 1 correction = 3
+ * tokens in section 2; the lesson's reading is used).
+ *
+ * Generic over chain and tree: position i (0-based) is judged by verifier row
+ * path[i] and draft row path[i] of the sequence, and tests token tok[i]; the
+ * bonus row is verifier row path[npos].  A chain is path[i] = i.  The ratio
+ * q(d)/p(d) is evaluated as exp of its logarithm so that tiny probabilities do
+ * not underflow to 0/0; p(d) <= 0 means the draft logit is -inf.
+ *
+ * u_acc / u_samp (optional) replace the Philox uniforms, for enumeration.
+ * ---------------------------------------------------------------------- */
+int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
+               int64_t d_bstride, int B, int V, float T,
+               const int32_t *path, int path_stride, const int32_t *npos_arr,
+               const int32_t *tok, int tok_stride, uint64_t seed,
+               uint64_t step, const uint32_t *u_acc, int u_acc_stride,
+               const uint32_t *u_samp, int32_t *out_tokens, int out_stride,
+               int32_t *out_accept, double *out_q, double *out_p,
+               double *out_margin, int margin_stride, double *out_gap,
+               uint32_t *out_status) {
+  if (B < 0 || V <= 0 || !(T > 0.0f)) return -1;
+  float invT = 1.0f / T;
+  double Td = (double)T;
+  for (int b = 0; b < B; ++b) {
+    const float *vb = vlog + (int64_t)b * v_bstride;
+    const float *db = dlog + (int64_t)b * d_bstride;
+    int npos = npos_arr[b];
+    const int32_t *pb = path ? path + (int64_t)b * path_stride : NULL;
+    const int32_t *tb = tok + (int64_t)b * tok_stride;
+    uint32_t status = 0;
+    int32_t *ot = out_tokens + (int64_t)b * out_stride;
+    for (int i = 0; i < out_stride; ++i) ot[i] = -1;
+    for (int i = 0; i < margin_stride; ++i) {
+      if (out_q) out_q[(int64_t)b * margin_stride + i] = NAN;
+      if (out_p) out_p[(int64_t)b * margin_stride + i] = NAN;
+    }
+    if (out_margin)
+      for (int i = 0; i <= margin_stride; ++i)
+        out_margin[(int64_t)b * (margin_stride + 1) + i] = NAN;
+    /* row and token checks over every row / token the round could touch */
+    for (int i = 0; i <= npos; ++i) {
+      int r = pb ? pb[i] : i;
+      if (orc_row_bad(vb + (int64_t)r * V, V)) status |= ORC_ROW_NAN;
+      if (i < npos && orc_row_bad(db + (int64_t)r * V, V)) status |= ORC_ROW_NAN;
+      if (i < npos && (tb[i] < 0 || tb[i] >= V)) status |= ORC_ROW_BAD_TOKEN;
+    }
+    if (status) {
+      out_accept[b] = 0;
+      out_status[b] = status;
+      if (out_gap) out_gap[b] = NAN;
+      continue;
+    }
+    int a = 0, stopped = 0;
+    for (int i = 0; i < npos; ++i) {
+      int r = pb ? pb[i] : i;
+      const float *xq = vb + (int64_t)r * V, *xp = db + (int64_t)r * V;
+      int d = tb[i];
+      double mq, sq, mp, sp;
+      orc_row_stats(xq, V, Td, &mq, &sq);
+      orc_row_stats(xp, V, Td, &mp, &sp);
+      double zq = (double)xq[d] / Td, zp = (double)xp[d] / Td;
+      double qd = exp(zq - mq) / sq, pd = exp(zp - mp) / sp;
+      double ratio;
+      int p_zero = isinf(zp) && zp < 0;
+      if (p_zero)
+        ratio = INFINITY;
+      else if (isinf(zq) && zq < 0)
+        ratio = 0.0;
+      else
+        ratio = exp(((zq - mq) - (zp - mp)) + (log(sp) - log(sq)));
+      uint32_t u24 = u_acc ? u_acc[(int64_t)b * u_acc_stride + i]
+                           : orc_u24(seed, step, (uint32_t)b, (uint32_t)i,
+                                     ORC_DRAW_ACCEPT);
+      double u = (double)u24 * 0x1p-24;
+      if (out_q) out_q[(int64_t)b * margin_stride + i] = qd;
+      if (out_p) out_p[(int64_t)b * margin_stride + i] = pd;
+      double rc = ratio < 1.0 ? ratio : 1.0;
+      if (out_margin) out_margin[(int64_t)b * (margin_stride + 1) + i] = rc - u;
+      if (stopped) continue;
+      int acc = p_zero ? 1 : (u < rc);
+      if (p_zero && !stopped) status |= ORC_ROW_P_ZERO;
+      if (acc) {
+        ot[i] = d;
+        a = i + 1;
+      } else {
+        stopped = 1;
+      }
+    }
+    /* correction (residual at position a) or bonus (verifier row path[npos]) */
+    uint32_t us = u_samp ? u_samp[b]
+                         : orc_u24(seed, step, (uint32_t)b, (uint32_t)a,
+                                   ORC_DRAW_SAMPLE);
+    double gap = NAN;
+    int rz = 0, k;
+    if (a < npos) {
+      int r = pb ? pb[a] : a;
+      k = orc_sample_repro(vb + (int64_t)r * V, db + (int64_t)r * V, V, invT,
+                           us, &gap, &rz);
+    } else {
+      int r = pb ? pb[npos] : npos;
+      k = orc_sample_repro(vb + (int64_t)r * V, NULL, V, invT, us, &gap, &rz);
+    }
+    if (rz) status |= ORC_ROW_RESID_ZERO;
+    ot[a] = k;
+    out_accept[b] = a;
+    out_status[b] = status;
+    if (out_gap) out_gap[b] = gap;
+    if (out_margin)
+      out_margin[(int64_t)b * (margin_stride + 1) + margin_stride] = gap;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Tree helpers.  A flattened draft tree of T slots per sequence: parent[0] ==
+ * -1 is the root (the last committed token), parent[c] in [0, c) for a node,
+ * -2 for an unused slot.  [Blog] "为什么要树，以及树怎么一次验完": number the
+ * flattened nodes; each node sees only itself and its ancestors.
+ * ---------------------------------------------------------------------- */
+int orc_tree_valid(const int32_t *parent, const float *score, int T) {
+  if (T < 1 || parent[0] != -1) return 0;
+  for (int c = 1; c < T; ++c) {
+    if (parent[c] == -2) continue;
+    if (parent[c] < 0 || parent[c] >= c) return 0;
+    if (parent[parent[c]] == -2) return 0;
+    if (score && isnan(score[c])) return 0;
+  }
+  return 1;
+}
+
+/* Best-child walk ([Blog] section 4, eagle_round: "walk the tree along
+ * best_child").  best_child is not defined on the page; read as the child with
+ * the highest path score (the score the drafter attaches: parent score times
+ * draft probability, same listing), ties to the lower slot index, none at a
+ * leaf.  At most max_depth steps.  Returns the depth D; path[0..D]. */
+int orc_tree_best_path(const int32_t *parent, const float *score, int T,
+                       int max_depth, int32_t *path) {
+  int D = 0, cur = 0;
+  path[0] = 0;
+  while (D < max_depth) {
+    int best = -1;
+    for (int c = 1; c < T; ++c) {
+      if (parent[c] != cur) continue;
+      if (best < 0 || score[c] > score[best]) best = c;
+    }
+    if (best < 0) break;
+    path[++D] = best;
+    cur = best;
+  }
+  return D;
+}
+
+/* Tree verify: path from the best-child walk, then the verify walk with
+ * verifier row n_{k-1} judging token[n_k] (the parent's distribution is the
+ * one over the token that follows it; reading of the listing, whose p_all[child]
+ * indexes the node whose distribution predicts the *next* token). */
+int orc_verify_tree(const float *vlog, const float *dlog, const int32_t *parent,
+                    const int32_t *token, const float *score, int B, int T,
+                    int max_depth, int V, float temperature, uint64_t seed,
+                    uint64_t step, int32_t *out_path, int32_t *out_tokens,
+                    int32_t *out_accept, double *out_q, double *out_p,
+                    double *out_margin, double *out_gap, uint32_t *out_status) {
+  int P = max_depth + 1;
+  int32_t *path = (int32_t *)malloc(sizeof(int32_t) * (size_t)B * P);
+  int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)B * (P > 1 ? P - 1 : 1));
+  int32_t *npos = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+  uint8_t *bad = (uint8_t *)calloc((size_t)(B > 0 ? B : 1), 1);
+  for (int b = 0; b < B; ++b) {
+    const int32_t *pa = parent + (int64_t)b * T;
+    const float *sc = score + (int64_t)b * T;
+    int32_t *pth = path + (int64_t)b * P;
+    for (int i = 0; i < P; ++i) pth[i] = -1;
+    if (!orc_tree_valid(pa, sc, T)) {
+      bad[b] = 1;
+      npos[b] = 0;
+      pth[0] = 0;
+      continue;
+    }
+    int D = orc_tree_best_path(pa, sc, T, max_depth, pth);
+    npos[b] = D;
+    for (int i = 0; i < D; ++i) tok[(int64_t)b * (P - 1) + i] = token[(int64_t)b * T + pth[i + 1]];
+  }
+  int rc = orc_verify(vlog, (int64_t)T * V, dlog, (int64_t)T * V, B, V,
+                      temperature, path, P, npos, tok, P - 1, seed, step, NULL,
+                      0, NULL, out_tokens, P, out_accept, out_q, out_p,
+                      out_margin, P - 1, out_gap, out_status);
+  for (int b = 0; b < B; ++b) {
+    int32_t *op = out_path + (int64_t)b * P;
+    for (int i = 0; i < P; ++i) op[i] = -1;
+    op[0] = 0; /* the root (last committed token) is always kept */
+    if (bad[b]) {
+      out_status[b] = ORC_ROW_BAD_TREE;
+      out_accept[b] = 0;
+      for (int i = 0; i < P; ++i) out_tokens[(int64_t)b * P + i] = -1;
+      if (out_gap) out_gap[b] = NAN;
+      if (out_margin)
+        for (int i = 0; i < P; ++i) out_margin[(int64_t)b * P + i] = NAN;
+      if (out_q)
+        for (int i = 0; i < P - 1; ++i) out_q[(int64_t)b * (P - 1) + i] = NAN;
+      if (out_p)
+        for (int i = 0; i < P - 1; ++i) out_p[(int64_t)b * (P - 1) + i] = NAN;
+      continue;
+    }
+    if (out_status[b] & (ORC_ROW_NAN | ORC_ROW_BAD_TOKEN)) continue;
+    int a = out_accept[b];
+    for (int i = 0; i <= a; ++i) op[i] = path[(int64_t)b * P + i];
+  }
+  free(path);
+  free(tok);
+  free(npos);
+  free(bad);
+  return rc;
+}
+
+/* Ancestor mask: bit j of node n is set iff j == n or j is an ancestor of n;
+ * depth = number of ancestors.  Unused slots get an empty mask and depth -1. */
+void orc_tree_mask(const int32_t *parent, int B, int T, uint64_t *mask,
+                   int32_t *depth) {
+  int W = (T + 63) / 64;
+  for (int b = 0; b < B; ++b) {
+    const int32_t *pa = parent + (int64_t)b * T;
+    int ok = orc_tree_valid(pa, NULL, T);
+    for (int n = 0; n < T; ++n) {
+      uint64_t *mk = mask + ((int64_t)b * T + n) * W;
+      for (int w = 0; w < W; ++w) mk[w] = 0;
+      depth[(int64_t)b * T + n] = -1;
+      if (!ok || pa[n] == -2) continue;
+      int d = -1;
+      for (int j = n; j >= 0; j = pa[j]) {
+        mk[j / 64] |= (uint64_t)1 << (j % 64);
+        ++d;
+      }
+      depth[(int64_t)b * T + n] = d;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------
+ * KV rollback / compaction ([Lesson] "Reversão de KV cache" and Passo 4;
+ * [Blog] section 3 "copy the accepted path's KV rows together, drop the other
+ * branches" and the compact_kv step of eagle_round).  Cache layout
+ * [L][2][B][S][H][D] of elem_bytes each.  For every sequence, layer and K/V:
+ * dst row dst_base+k <- src row src_base+rows[k], k < n_rows, all reads
+ * before any write.  kv_len = dst_base + n_rows, or -1 (nothing moved) when a
+ * row is out of range, n_rows is out of [0, P], or an in-place call (src ==
+ * dst) has dst_base != src_base or rows not strictly increasing with
+ * rows[k] >= k.
+ * ---------------------------------------------------------------------- */
+void orc_kv_compact(const uint8_t *src, uint8_t *dst, int L, int B, int S_src,
+                    int S_dst, int H, int D, int elem_bytes,
+                    const int32_t *src_base, const int32_t *dst_base,
+                    const int32_t *rows, const int32_t *n_rows, int P,
+                    int32_t *out_kv_len) {
+  size_t rb = (size_t)H * D * elem_bytes;
+  int inplace = (src == dst);
+  uint8_t *tmp = (uint8_t *)malloc(rb * (size_t)(P > 0 ? P : 1));
+  for (int b = 0; b < B; ++b) {
+    int n = n_rows[b];
+    int ok = (n >= 0 && n <= P && src_base[b] >= 0 && dst_base[b] >= 0 &&
+              dst_base[b] + n <= S_dst);
+    if (inplace && src_base[b] != dst_base[b]) ok = 0;
+    for (int k = 0; ok && k < n; ++k) {
+      int r = rows[(int64_t)b * P + k];
+      if (r < 0 || src_base[b] + r >= S_src) ok = 0;
+      if (inplace && (r < k || (k > 0 && r <= rows[(int64_t)b * P + k - 1]))) ok = 0;
+    }
+    if (!ok) {
+      out_kv_len[b] = -1;
+      continue;
+    }
+    for (int l = 0; l < L; ++l) {
+      for (int kv = 0; kv < 2; ++kv) {
+        size_t slab = ((size_t)l * 2 + kv) * (size_t)B + (size_t)b;
+        const uint8_t *sb = src + slab * (size_t)S_src * rb;
+        uint8_t *db = dst + slab * (size_t)S_dst * rb;
+        for (int k = 0; k < n; ++k)
+          memcpy(tmp + (size_t)k * rb,
+                 sb + (size_t)(src_base[b] + rows[(int64_t)b * P + k]) * rb, rb);
+        for (int k = 0; k < n; ++k)
+          memcpy(db + (size_t)(dst_base[b] + k) * rb, tmp + (size_t)k * rb, rb);
+      }
+    }
+    out_kv_len[b] = dst_base[b] + n;
+  }
+  free(tmp);
+}
+
+/* ------------------------------------------------------------------------
+ * Speedup model ([Lesson] "O que determina a aceleração"): expected tokens
+ * per verifier pass (1 - a^(N+1)) / (1 - a); wall time per token
+ * (N c + 1) / E; speedup = E / (N c + 1).
+ * ---------------------------------------------------------------------- */
+double orc_expected_tokens(double alpha, int N) {
+  if (alpha == 1.0) return (double)(N + 1);
+  return (1.0 - pow(alpha, N + 1)) / (1.0 - alpha);
+}
+
+double orc_speedup(double alpha, int N, double c) {
+  return orc_expected_tokens(alpha, N) / ((double)N * c + 1.0);
+}

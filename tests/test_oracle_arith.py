@@ -1,0 +1,171 @@
+"""Pins for the oracle's softmax, accept rule, residual, inverse CDF and the
+fp32 sampling arithmetic -- each against closed forms, library routines or
+the mathematics, never against a retyped copy of the oracle's own formula."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+# ---------------------------------------------------------------- softmax
+def test_softmax_uniform_row_is_one_over_V():
+    for V in (1, 7, 1000):
+        p = oracle.softmax(np.full(V, 3.25, np.float32))
+        assert np.allclose(p, 1.0 / V, rtol=0, atol=1e-15)
+
+
+def test_softmax_two_level_closed_form():
+    # n_a tokens at logit a, n_b at b: p_a = e^a / (n_a e^a + n_b e^b)
+    a, b, na, nb = 2.0, -1.5, 3, 17
+    x = np.array([a] * na + [b] * nb, np.float32)
+    rng = np.random.default_rng(0)
+    rng.shuffle(x)
+    p = oracle.softmax(x)
+    den = na * math.exp(a) + nb * math.exp(b)
+    want = np.where(x == np.float32(a), math.exp(a) / den, math.exp(b) / den)
+    assert np.allclose(p, want, rtol=1e-14, atol=0)
+
+
+def test_softmax_temperature_and_shift_invariance():
+    x = np.random.default_rng(1).standard_normal(50).astype(np.float32) * 3
+    # T = 2 equals plain softmax of x/2 (x/2 exact in fp32)
+    assert np.allclose(oracle.softmax(x, 2.0), oracle.softmax(x / 2), atol=1e-15)
+    # against the library softmax (scipy) in double
+    from scipy.special import softmax as sp_softmax
+    assert np.allclose(oracle.softmax(x), sp_softmax(x.astype(np.float64)), atol=1e-15)
+    # -inf logits carry zero mass
+    y = x.copy(); y[::3] = -np.inf
+    p = oracle.softmax(y)
+    assert np.all(p[::3] == 0) and abs(p.sum() - 1) < 1e-14
+
+
+# ---------------------------------------------------------------- accept rule
+def test_accept_rule_edge_cases():
+    # a draft probability <= 0 is accepted whatever u is
+    for u in (0.0, 0.5, 1 - 2**-24):
+        assert oracle.accept(0.3, 0.0, u)
+        assert oracle.accept(0.0, 0.0, u)
+    # q >= p: ratio clipped to 1, always accepted for u < 1
+    assert oracle.accept(0.5, 0.25, 1 - 2**-24)
+    # strict comparison u < q/p
+    assert not oracle.accept(0.25, 0.5, 0.5)
+    assert oracle.accept(0.25, 0.5, 0.5 - 2**-24)
+    # q = 0, p > 0: never accepted
+    assert not oracle.accept(0.0, 0.4, 0.0)
+
+
+# ---------------------------------------------------------------- residual
+def test_residual_closed_form_and_zero_fallback():
+    q = np.array([0.5, 0.3, 0.2, 0.0])
+    p = np.array([0.2, 0.4, 0.1, 0.3])
+    r = oracle.residual(q, p)
+    assert np.allclose(r, [0.3 / 0.4, 0.0, 0.1 / 0.4, 0.0], atol=1e-15)
+    # q == p: zero residual mass falls back to q
+    assert np.array_equal(oracle.residual(q, q), q)
+    # Leviathan identity: min(p, q) + (1 - sum min) * residual == q
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        q = rng.dirichlet(np.ones(9)); p = rng.dirichlet(np.ones(9))
+        beta = np.minimum(p, q).sum()
+        assert np.allclose(np.minimum(p, q) + (1 - beta) * oracle.residual(q, p), q, atol=1e-14)
+
+
+# ---------------------------------------------------------------- inverse CDF
+def test_invcdf_matches_searchsorted():
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        V = int(rng.integers(1, 40))
+        w = rng.random(V) * (rng.random(V) < 0.6)
+        if w.sum() == 0:
+            w[rng.integers(V)] = 1.0
+        t = rng.random() * w.sum()
+        k = oracle.invcdf(w, t)
+        want = int(np.searchsorted(np.cumsum(w), t, side="right"))
+        assert k == min(want, V - 1) or (want == V and w[k] > 0)
+        assert w[k] > 0
+
+
+# ---------------------------------------------------------------- fp32 exp
+def test_exp32_error_bound_against_libm():
+    a = np.concatenate([np.linspace(-80, 0, 200001, dtype=np.float32),
+                        -np.logspace(-8, 0, 2001).astype(np.float32),
+                        np.float32([0.0, -1e-30, -0.34657359, -0.34657360, -79.999])])
+    got = np.array([oracle.exp32(x) for x in a], np.float64)
+    want = np.exp(a.astype(np.float64))
+    rel = np.abs(got - want) / want
+    # within 2 units in the last place of fp32 (2^-22 relative)
+    assert rel.max() < 2.0 ** -22, rel.max()
+    assert oracle.exp32(0.0) == 1.0
+    assert oracle.exp32(-80.001) == 0.0 and oracle.exp32(-np.inf) == 0.0
+
+
+def test_exp32_monotone_on_grid():
+    a = np.linspace(-30, 0, 30001, dtype=np.float32)
+    e = np.array([oracle.exp32(x) for x in a])
+    assert np.all(np.diff(e) >= 0)
+
+
+# ---------------------------------------------------------------- sampling arithmetic
+def _law_over_u_grid(xq, xp, G):
+    V = len(xq)
+    cnt = np.zeros(V)
+    for g in range(G):
+        u = int((g + 0.5) / G * 2**24)
+        k, _, _ = oracle.sample_repro(xq, xp, u)
+        cnt[k] += 1
+    return cnt / G
+
+
+def test_repro_bonus_law_matches_double_softmax():
+    rng = np.random.default_rng(5)
+    xq = (rng.standard_normal(12) * 1.5).astype(np.float32)
+    G = 20000
+    law = _law_over_u_grid(xq, None, G)
+    assert np.abs(law - oracle.softmax(xq)).max() <= 1.0 / G + 1e-6
+
+
+def test_repro_residual_law_matches_double_residual():
+    rng = np.random.default_rng(6)
+    xq = (rng.standard_normal(10) * 2).astype(np.float32)
+    xp = (xq + rng.standard_normal(10) * 0.8).astype(np.float32)
+    G = 20000
+    law = _law_over_u_grid(xq, xp, G)
+    want = oracle.residual(oracle.softmax(xq), oracle.softmax(xp))
+    assert np.abs(law - want).max() <= 1.0 / G + 1e-6
+    # tokens with q <= p are never chosen
+    assert np.all(law[oracle.softmax(xq) <= oracle.softmax(xp)] == 0)
+
+
+def test_repro_residual_zero_falls_back_to_q():
+    x = np.array([0.0, 1.0, -1.0, 2.0], np.float32)
+    k, gap, rz = oracle.sample_repro(x, x, 2**23)
+    assert rz
+    law = _law_over_u_grid(x, x, 4000)
+    assert np.abs(law - oracle.softmax(x)).max() <= 1 / 4000 + 1e-6
+
+
+def test_repro_extremes_of_u():
+    x = np.array([-np.inf, 0.0, 0.0, -np.inf, 0.0], np.float32)
+    assert oracle.sample_repro(x, None, 0)[0] == 1
+    assert oracle.sample_repro(x, None, 2**24 - 1)[0] == 4
+
+
+def test_repro_large_vocab_agrees_with_double_inverse_cdf():
+    # the fp32/fixed-point choice and a double inverse CDF differ only on
+    # near-ties; at V = 32000 those are rare
+    rng = np.random.default_rng(7)
+    V = 32000
+    xq = (rng.standard_normal(V) * 3).astype(np.float32)
+    xp = (xq + rng.standard_normal(V) * 0.4).astype(np.float32)
+    w = oracle.residual(oracle.softmax(xq), oracle.softmax(xp))
+    cdf = np.cumsum(w)
+    diff = 0
+    n = 300
+    for i in range(n):
+        u = int(rng.integers(0, 2**24))
+        k, _, _ = oracle.sample_repro(xq, xp, u)
+        kd = int(np.searchsorted(cdf, u / 2**24 * cdf[-1], side="right"))
+        diff += k != kd
+    assert diff <= 2
