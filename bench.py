@@ -1,0 +1,532 @@
+"""Benchmark of the verify-and-accept step on GB300.
+
+One step = one speculative round over a batch: the tree attention mask
+(sv_tree_build_mask), the tree verify (sv_verify_tree: best-child path, row
+statistics, accept walk, residual / bonus sampling) and the KV compaction of
+the accepted paths (sv_kv_compact, in place).  Default workload: the dynamic
+EAGLE-2 tree (B=128, 60-node budget, depth 6, top-k 10, V=128256, bf16 logits,
+KV shaped like a 70B model: 80 layers x 8 KV heads x 128).  `--config 3` runs
+the large-vocabulary chain (B=256, N=7) instead (verify + chain rollback).
+
+Prints one JSON line.  `value` = verified logit rows per second (B*T per tree
+round, B*(N+1) per chain round) with inputs resident in HBM; `e2e` = the same
+through host buffers (pinned host -> device copies and the device -> host read
+of the results inside the timed region); `roofline` = the row-statistics
+kernel's algorithmic bytes over its CUDA-event time against the measured HBM
+copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 5|3]
+    python bench.py --impl reference ...      # the CPU oracle alone
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s and accepted tokens/s at 1 GB300; achieved HBM GB/s vs ~8 TB/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pool", type=int, default=4, help="distinct rounds rotated in the timed loop")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=16, help="sequences the oracle times")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_batch(B, rank, world):
+    """Weak scaling: every rank runs the full per-GPU batch of B sequences;
+    sequence ids are offset so ranks draw distinct Philox streams."""
+    return rank * B, B
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def best_path_depth(parent, score, max_depth):
+    """Depth of the best-child walk per sequence (host, numpy), used only to
+    count the rows the verify step reads."""
+    B, T = parent.shape
+    out = np.zeros(B, np.int64)
+    for b in range(B):
+        cur, D = 0, 0
+        while D < max_depth:
+            kids = np.nonzero(parent[b] == cur)[0]
+            if kids.size == 0:
+                break
+            s = score[b, kids]
+            cur = int(kids[np.flatnonzero(s == s.max())[0]])
+            D += 1
+        out[b] = D
+    return out
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel, cfg_name):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current source of the kernel (source hash recorded)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{cfg_name}.txt")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not h:
+        return None
+    src = os.path.join(ROOT, "speculative_decoding_verification_vocab_gb300", "csrc")
+    cur = hashlib.sha256(b"".join(open(os.path.join(src, f), "rb").read()
+                                  for f in sorted(os.listdir(src)))).hexdigest()[:16]
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+# ------------------------------------------------------------------ workload
+class Workload:
+    def __init__(self, cfg, pool, device, seq_offset):
+        import torch
+        from speculative_decoding_verification_vocab_gb300 import synth
+        self.cfg = cfg
+        self.rounds = []
+        self.tree = cfg.kind.startswith("tree")
+        for r in range(pool):
+            if self.tree:
+                vq, dp, parent, token, score = synth.tree_inputs(cfg, seed=r + 1000 * seq_offset,
+                                                                 device=device)
+                depth = best_path_depth(parent.cpu().numpy(), score.cpu().numpy(), cfg.depth)
+                self.rounds.append(dict(vq=vq, dp=dp, parent=parent, token=token, score=score,
+                                        depth=depth))
+            else:
+                vq, dp, d = synth.chain_inputs(cfg, seed=r + 1000 * seq_offset, device=device)
+                self.rounds.append(dict(vq=vq, dp=dp, d=d,
+                                        depth=np.full(cfg.B, cfg.N, np.int64)))
+        torch.cuda.synchronize()
+        self.B = cfg.B
+        self.T = self.rounds[0]["vq"].shape[1]
+        self.V = cfg.V
+        self.esize = self.rounds[0]["vq"].element_size()
+        kv = cfg.kv
+        # KV window: the slots the round writes and compacts, for every sequence
+        # (the prefix of `kv.base` rows is never touched by the step)
+        self.S = self.T + 4
+        self.kv = synth.kv_cache(kv.L, cfg.B, self.S, kv.H, kv.D, device=device, seed=7)
+        self.kv_base = torch.zeros(cfg.B, dtype=torch.int32, device=device)
+        self.row_bytes = kv.H * kv.D * self.kv.element_size()
+
+    def rows_per_step(self):
+        return self.B * self.T
+
+    def stats_bytes(self, r):
+        d = self.rounds[r]["depth"]
+        return int(((2 * d + 1) * self.V * self.esize).sum())
+
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_vocab_gb300 as sv
+    from speculative_decoding_verification_vocab_gb300 import synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load_library()
+    cfg = synth.CONFIGS[args.config]
+    seq0, B = shard_batch(cfg.B, rank, world)
+    wl = Workload(cfg, args.pool, dev, rank)
+    K, W = args.steps, args.warmup
+    T, V = wl.T, wl.V
+    maxd = cfg.depth if wl.tree else cfg.N
+    P = maxd + 1
+    # per-step outputs land in slices of these buffers (no extra work per step)
+    o_path = torch.empty(K + W, B, P, dtype=torch.int32, device=dev)
+    o_tok = torch.empty(K + W, B, P, dtype=torch.int32, device=dev)
+    o_acc = torch.empty(K + W, B, dtype=torch.int32, device=dev)
+    o_st = torch.empty(K + W, B, dtype=torch.int32, device=dev)
+    o_kv = torch.empty(K + W, B, dtype=torch.int32, device=dev)
+    Wm = (T + 63) // 64
+    o_mask = torch.empty(B, T, Wm, dtype=torch.int64, device=dev)
+    o_depth = torch.empty(B, T, dtype=torch.int32, device=dev)
+    ws_bytes = (sv.sv_verify_tree_workspace(B, T, maxd, V) if wl.tree
+                else sv.sv_verify_chain_workspace(B, cfg.N, V))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, rd, seed_step):
+        if wl.tree:
+            sv.sv_tree_build_mask(rd["parent"], o_mask, o_depth, stream)
+            sv.sv_verify_tree(rd["vq"], rd["dp"], rd["parent"], rd["token"], rd["score"], maxd,
+                              cfg.temperature, 1234 + rank, seed_step, o_path[i], o_tok[i],
+                              o_acc[i], None, None, None, o_st[i], ws, stream)
+            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, o_path[i], o_acc[i], 1,
+                             o_kv[i], stream)
+        else:
+            sv.sv_verify_chain(rd["vq"], rd["dp"], rd["d"], cfg.temperature, 1234 + rank,
+                               seed_step, o_tok[i], o_acc[i], None, None, None, o_st[i], ws,
+                               stream)
+            # chain rollback: the accepted drafts' rows are already in place;
+            # only the logical length moves (rows NULL = identity)
+            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, None, o_acc[i], 1, o_kv[i],
+                             stream)
+
+    for i in range(W):
+        step(i, wl.rounds[i % args.pool], i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    n_launch0 = sv.sv_launch_count()
+    sv.sv_trace_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(K):
+            step(W + k, wl.rounds[k % args.pool], W + k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    sv.sv_trace_enable(False)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1)
+    launches = sv.sv_launch_count() - n_launch0
+    trace = sv.sv_trace_collect()
+    ms_max = max_over_ranks(ms, world)
+
+    acc = o_acc[W:].cpu().numpy()
+    st = o_st[W:].cpu().numpy()
+    paths = o_path[W:].cpu().numpy()
+    rows = wl.rows_per_step() * K
+    tokens = int((acc + 1).sum())
+    depth_used = np.stack([wl.rounds[k % args.pool]["depth"] for k in range(K)])
+    alpha_hat = float(acc.sum() / max(1, np.minimum(acc + 1, depth_used).sum()))
+    # algorithmic bytes
+    stats_bytes = sum(wl.stats_bytes(k % args.pool) for k in range(K))
+    kv_moved = 0
+    if wl.tree:
+        for k in range(K):
+            for b in range(B):
+                a = acc[k, b]
+                kv_moved += int(sum(1 for j in range(1, a + 1) if paths[k, b, j] != j))
+    kvb = cfg.kv
+    kv_bytes = kv_moved * 2 * kvb.L * 2 * wl.row_bytes
+    mask_bytes = K * B * T * (4 + 8 * Wm + 4) if wl.tree else 0
+    alg_bytes = stats_bytes + kv_bytes + mask_bytes
+    total_rows = sum_over_ranks(rows, world)
+    total_tokens = sum_over_ranks(tokens, world)
+    value = total_rows / (ms_max / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    rs_launches, rs_ms = trace.get("row_stats", (0, 0.0))
+    rs_bytes_per_launch = stats_bytes / K
+    rs_avg_ms = rs_ms / max(rs_launches, 1)
+    achieved = rs_bytes_per_launch / (rs_avg_ms / 1e3) / 1e9 if rs_launches else None
+    roofline = {"kernel": "row_stats", "bound": "hbm", "achieved": achieved, "peak": peak,
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "traffic": recorded_traffic("row_stats", cfg.name),
+                "alg_bytes_per_launch": rs_bytes_per_launch, "avg_launch_ms": rs_avg_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype.__repr__().endswith("bfloat16") else "f32",
+        "data": "synthetic",
+        "config": {"workload": f"config {cfg.index}: {cfg.name}", "B_per_gpu": B, "T": T, "V": V,
+                   "max_depth": maxd, "logits": str(cfg.dtype).replace("torch.", ""),
+                   "kv": f"{kvb.L} layers x {kvb.H} kv heads x {kvb.D}, bf16",
+                   "pool_rounds": args.pool,
+                   "l2": f"inputs larger than L2: each step reads {stats_bytes / K / 1e6:.0f} MB of "
+                         f"logit rows from a pool of {args.pool} distinct rounds "
+                         f"({args.pool * wl.rounds[0]['vq'].numel() * wl.esize * 2 / 1e9:.1f} GB)"},
+        "accepted_tokens_per_s": total_tokens / (ms_max / 1e3),
+        "mean_emitted_per_seq": tokens / (K * B), "alpha_hat": alpha_hat,
+        "hbm_gbs": alg_bytes / (ms_max / 1e3) / 1e9,
+        "hbm_frac_measured": alg_bytes / (ms_max / 1e3) / 1e9 / peak,
+        "hbm_frac_nominal_8tbs": alg_bytes / (ms_max / 1e3) / 1e9 / 8000.0,
+        "alg_bytes_per_step": {"row_stats": stats_bytes / K, "kv_compact": kv_bytes / K,
+                               "tree_mask": mask_bytes / K},
+        "kernels": {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in trace.items()},
+        "status_nonzero": int((st != 0).sum()),
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, wl, cfg)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
+    """Same step through host buffers: pinned host -> device copy of the
+    round's inputs, the three calls, device -> host read of the results."""
+    import torch
+    rd = wl.rounds[0]
+    names = ["vq", "dp", "parent", "token", "score"] if wl.tree else ["vq", "dp", "d"]
+    host = {n: rd[n].cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(rd[n]) for n in names}
+    P = maxd + 1
+    T, V = wl.T, wl.V
+    outs = dict(path=torch.empty(B, P, dtype=torch.int32, device=dev),
+                tok=torch.empty(B, P, dtype=torch.int32, device=dev),
+                acc=torch.empty(B, dtype=torch.int32, device=dev),
+                st=torch.empty(B, dtype=torch.int32, device=dev),
+                kv=torch.empty(B, dtype=torch.int32, device=dev))
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    ws = torch.empty(sv.sv_verify_tree_workspace(B, T, maxd, V) if wl.tree
+                     else sv.sv_verify_chain_workspace(B, cfg.N, V), dtype=torch.uint8, device=dev)
+    Wm = (T + 63) // 64
+    o_mask = torch.empty(B, T, Wm, dtype=torch.int64, device=dev)
+    o_depth = torch.empty(B, T, dtype=torch.int32, device=dev)
+    h2d = sum(h.numel() * h.element_size() for h in host.values())
+    d2h = sum(h.numel() * h.element_size() for h in hout.values())
+
+    def one(i):
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        if wl.tree:
+            sv.sv_tree_build_mask(devb["parent"], o_mask, o_depth, stream)
+            sv.sv_verify_tree(devb["vq"], devb["dp"], devb["parent"], devb["token"], devb["score"],
+                              maxd, cfg.temperature, 99, i, outs["path"], outs["tok"], outs["acc"],
+                              None, None, None, outs["st"], ws, stream)
+            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, outs["path"], outs["acc"], 1,
+                             outs["kv"], stream)
+        else:
+            sv.sv_verify_chain(devb["vq"], devb["dp"], devb["d"], cfg.temperature, 99, i,
+                               outs["tok"], outs["acc"], None, None, None, outs["st"], ws, stream)
+            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, None, outs["acc"], 1,
+                             outs["kv"], stream)
+        for k in outs:
+            hout[k].copy_(outs[k], non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    n = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(n):
+        one(i + 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1e3)
+    ms = max_over_ranks(ms, world)
+    rows = sum_over_ranks(wl.rows_per_step() * n, world)
+    return {"value": rows / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_round(cfg, rd, ids, step, kv=None):
+    """One round of the oracle on the sequences `ids` of a pooled round: the
+    tree (or chain) verify and, for trees, the in-place KV compaction of the
+    sampled sequences' window.  Returns (rows covered, seconds)."""
+    import oracle
+    import torch
+    tid = torch.as_tensor(ids)
+    vq = rd["vq"][tid].float().cpu().numpy()
+    dp = rd["dp"][tid].float().cpu().numpy()
+    t0 = time.perf_counter()
+    if "parent" in rd:
+        par = rd["parent"][tid].cpu().numpy()
+        o = oracle.verify_tree(vq, dp, par, rd["token"][tid].cpu().numpy(),
+                               rd["score"][tid].cpu().numpy(), cfg.depth, T=cfg.temperature,
+                               seed=1234, step=step, seq_ids=ids)
+        oracle.tree_mask(par)
+        if kv is not None:
+            L, H, D, S, buf = kv
+            nb = len(ids)
+            base = np.zeros(nb, np.int32)
+            oracle.kv_compact(buf, buf, L, nb, S, S, H, D, 2, base, base, o["path"],
+                              o["accept_len"] + 1)
+        rows = len(ids) * vq.shape[1]
+    else:
+        oracle.verify_chain(vq, dp, rd["d"][tid].cpu().numpy(), T=cfg.temperature, seed=1234,
+                            step=step, seq_ids=ids)
+        rows = len(ids) * vq.shape[1]
+    return rows, time.perf_counter() - t0
+
+
+def cpu_baseline(args, wl, cfg):
+    kv = None
+    k = min(args.cpu_sample, wl.B)
+    if wl.tree:
+        kvc = cfg.kv
+        buf = np.random.default_rng(0).integers(0, 256, (kvc.L, 2, k, wl.S, kvc.H, kvc.D * 2),
+                                                dtype=np.uint8)
+        kv = (kvc.L, kvc.H, kvc.D, wl.S, buf)
+    ids = np.arange(k)
+    rows, secs = _oracle_round(cfg, wl.rounds[0], ids, 0, kv)
+    return {"value": rows / secs, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{k} of {wl.B} sequences of one round of config {cfg.index} "
+                      f"({cfg.name}), single-threaded C oracle in double precision, "
+                      f"{secs:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle as it stands, timed on the host cores,
+    each step a bounded sample of the same workload."""
+    import torch
+    from speculative_decoding_verification_vocab_gb300 import synth
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[args.config]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    if cfg.kind.startswith("tree"):
+        vq, dp, parent, token, score = synth.tree_inputs(cfg, seed=1, device=dev)
+        rd = dict(vq=vq, dp=dp, parent=parent, token=token, score=score)
+    else:
+        vq, dp, d = synth.chain_inputs(cfg, seed=1, device=dev)
+        rd = dict(vq=vq, dp=dp, d=d)
+    k = max(1, min(args.cpu_sample // 4, cfg.B))
+    kv = None
+    T = vq.shape[1]
+    if cfg.kind.startswith("tree"):
+        kvc = cfg.kv
+        buf = np.random.default_rng(0).integers(0, 256, (kvc.L, 2, k, T + 4, kvc.H, kvc.D * 2),
+                                                dtype=np.uint8)
+        kv = (kvc.L, kvc.H, kvc.D, T + 4, buf)
+    for i in range(args.warmup):
+        _oracle_round(cfg, rd, np.arange(i * k, (i + 1) * k) % cfg.B, i, kv)
+    rows, secs = 0, 0.0
+    for i in range(args.steps):
+        ids = np.arange((args.warmup + i) * k, (args.warmup + i + 1) * k) % cfg.B
+        r, s = _oracle_round(cfg, rd, np.sort(ids), args.warmup + i, kv)
+        rows += r
+        secs += s
+    value = rows / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"config {cfg.index}: {cfg.name}", "B_per_gpu": cfg.B, "T": T,
+                       "V": cfg.V},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{k} sequences per step of config {cfg.index} "
+                                       f"({cfg.name}), single-threaded C oracle"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * sv.h -- C ABI of the GB300 (sm_103a) verify-and-accept library for
+ * speculative decoding: Leviathan rejection sampling along a draft chain or
+ * the best-scored path of an EAGLE-style draft tree, residual / bonus
+ * sampling, the tree's ancestor attention mask, and KV-cache rollback /
+ * compaction.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [Lesson] "Decodificação Especulativa e EAGLE-3" (ai-engineering.academy,
+ *            Phase 10 Lesson 15; the same lesson in Persian on nextadmin.net).
+ *   [Blog]   "投机解码发展" (caijizhuo.github.io).  The blog swaps the letters;
+ *            this header uses the lesson's: p = draft, q = verifier.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *    stated otherwise.  The library never allocates, frees or synchronises;
+ *    scratch memory is the caller's `workspace`, sized by the matching
+ *    *_workspace() query.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All work is enqueued asynchronously on it.
+ *  - Argument errors are detected on the host before anything is enqueued;
+ *    the call then returns a non-OK sv_status and sv_last_error() says why.
+ *    A failed kernel launch returns SV_ERR_CUDA.  No C++ exception crosses
+ *    the ABI.
+ *  - Data faults found on the device never abort: they set bits in the
+ *    per-sequence out_status word and produce the defined fallback outputs.
+ *  - Logit rows are row-major [rows][V], element type sv_dtype; rows need no
+ *    alignment beyond the element size (16-byte-aligned rows take the
+ *    vectorised path).
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed on `seed`,
+ *    counter (position, draw, sequence, step mod 2^32); u = (x0 >> 8) 2^-24.
+ *    draw 0 = accept test at a position, draw 1 = residual / bonus sample.
+ *    A round is a pure function of its inputs, seed and step.
+ */
+#ifndef SV_H
+#define SV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1, /* bad pointer, size, dtype or workspace */
+  SV_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits */
+  SV_ERR_CUDA = 3,        /* a CUDA call failed; sv_last_error() has it */
+  SV_ERR_TIMEOUT = 4      /* a bounded device wait gave up */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Bits of the per-sequence out_status word. */
+#define SV_ROW_NAN 1u        /* a used logit row holds NaN or +inf, or is all -inf */
+#define SV_ROW_BAD_TOKEN 2u  /* a draft token outside [0, V) */
+#define SV_ROW_RESID_ZERO 4u /* residual mass was 0; the correction came from q */
+#define SV_ROW_P_ZERO 8u     /* a tested draft token had p(d) = 0 (draft logit -inf) and was accepted */
+#define SV_ROW_BAD_TREE 16u  /* parent/score arrays do not describe a tree */
+
+/* Build limits. */
+#define SV_MAX_VOCAB (1 << 22)  /* fixed-point sampling sums stay below 2^63 */
+#define SV_MAX_POSITIONS 1024   /* N (chain) or max_depth (tree) */
+#define SV_MAX_TREE_NODES 1024  /* T */
+
+/* ---------------------------------------------------------------------------
+ * sv_verify_chain -- verify N drafted tokens per sequence in one call.
+ * [Lesson] "O invariante" (Leviathan rejection sampling; the chained form),
+ * Passo 1 (accept rule), Passo 2 (residual), Passo 3 (one speculative step);
+ * [Blog] section 2 (draft / verify / accept) and section 4 (spec_decode).
+ *
+ * For sequence b and position i = 0..N-1 the draft token d = draft_tokens[b][i]
+ * is judged by q_{i+1} = softmax(vlogits[b][i] / temperature) and
+ * p_{i+1} = softmax(dlogits[b][i] / temperature): accepted iff
+ * u < min(1, q(d)/p(d)) (or p(d) = 0), left to right.  At the first rejection
+ * a < N a correction token is drawn from (q_{a+1} - p_{a+1})_+ normalised (q
+ * itself if that mass is 0); if all N pass, a bonus token is drawn from
+ * q_{N+1} = softmax(vlogits[b][N]).
+ *
+ *   vlogits      [B][N+1][V] verifier logits (row i = distribution after input
+ *                position i, i.e. over the token that follows it)
+ *   dlogits      [B][N][V]   draft logits (may be NULL when N == 0)
+ *   draft_tokens [B][N] int32
+ *   temperature  > 0, finite.  Probabilities are softmax(logits / T).
+ * Outputs (device, caller-owned):
+ *   out_tokens     [B][N+1]  accepted drafts then the correction/bonus token;
+ *                            -1 after it.  emitted = out_accept_len + 1.
+ *   out_accept_len [B]       a, the number of accepted drafts.
+ *   out_q_prob     [B][N] or NULL: q_{i+1}(d_{i+1}) for every position.
+ *   out_p_prob     [B][N] or NULL: p_{i+1}(d_{i+1}).
+ *   out_margin     [B][N+1] or NULL: [i] = min(1, q/p) - u at position i;
+ *                  [N] = distance of the correction/bonus threshold to the
+ *                  nearest CDF boundary, as a fraction of the sampled mass.
+ *   out_status     [B]       SV_ROW_* bits.  On NAN / BAD_TOKEN the sequence
+ *                  emits nothing: accept_len 0, tokens all -1.
+ * The correction/bonus choice uses exact 64-bit fixed-point prefix sums of an
+ * fp32 distribution computed with a fixed sequence of IEEE operations, so the
+ * chosen token does not depend on how the sum is split across threads.
+ * --------------------------------------------------------------------------- */
+size_t sv_verify_chain_workspace(int B, int N, int V);
+sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
+                          const int32_t *draft_tokens, int B, int N, int V,
+                          float temperature, uint64_t seed, uint64_t step,
+                          int32_t *out_tokens, int32_t *out_accept_len,
+                          float *out_q_prob, float *out_p_prob,
+                          float *out_margin, uint32_t *out_status,
+                          void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* ---------------------------------------------------------------------------
+ * sv_verify_tree -- verify a flattened draft tree per sequence.
+ * [Blog] section 3 "为什么要树，以及树怎么一次验完" (flattened tree verified in
+ * one pass), section 4 eagle_round (walk along best_child with the same
+ * accept rule; residual on rejection; bonus at the end), section 5 (EAGLE-2
+ * path score = product of draft probabilities).
+ *
+ * Node 0 of each tree is the root = the last committed token.  parent[b][0] =
+ * -1; parent[b][c] in [0, c) for a node; -2 for an unused slot.  token[b][c]
+ * is the token of node c; score[b][c] its path score.  The walk starts at the
+ * root and repeatedly takes the child with the highest score (ties: the lower
+ * slot), at most max_depth steps; this gives path n_0 = 0, n_1..n_D.  Step
+ * k = 1..D tests token[n_k] with q = softmax(vlogits[b][n_{k-1}]) and
+ * p = softmax(dlogits[b][n_{k-1}]); the bonus comes from vlogits[b][n_D].
+ * Only the path's rows are read.
+ *
+ *   vlogits, dlogits [B][T][V]; parent, token int32 [B][T]; score f32 [B][T].
+ * Outputs: out_path_nodes [B][max_depth+1] = n_0..n_a then -1 (n_0 = 0 even
+ * for a faulty sequence: the root row is always kept); out_tokens
+ * [B][max_depth+1]; out_accept_len [B]; out_q_prob / out_p_prob [B][max_depth]
+ * or NULL; out_margin [B][max_depth+1] or NULL (gap at index max_depth);
+ * out_status [B] (SV_ROW_BAD_TREE: accept_len 0, tokens -1).
+ * A single-path tree gives bit-identical results to sv_verify_chain.
+ * --------------------------------------------------------------------------- */
+size_t sv_verify_tree_workspace(int B, int T, int max_depth, int V);
+sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv_dtype dt,
+                         const int32_t *parent, const int32_t *token,
+                         const float *score, int B, int T, int max_depth,
+                         int V, float temperature, uint64_t seed,
+                         uint64_t step, int32_t *out_path_nodes,
+                         int32_t *out_tokens, int32_t *out_accept_len,
+                         float *out_q_prob, float *out_p_prob,
+                         float *out_margin, uint32_t *out_status,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* ---------------------------------------------------------------------------
+ * sv_tree_build_mask -- the tree attention mask.
+ * [Blog] section 3 (each flattened node sees only itself and its ancestors,
+ * never its siblings); [Lesson] "Reversão de KV cache" (the verifier runs a
+ * non-causal mask that follows the tree).
+ *   parent  int32 [B][T] as for sv_verify_tree.
+ *   out_mask  uint64 [B][T][(T+63)/64]: bit j of word j/64 of node n is set
+ *             iff j == n or j is an ancestor of n.
+ *   out_depth int32  [B][T]: number of ancestors; -1 for unused slots.
+ * An invalid tree gets an all-zero mask and depth -1 everywhere.
+ * --------------------------------------------------------------------------- */
+sv_status sv_tree_build_mask(const int32_t *parent, int B, int T,
+                             uint64_t *out_mask, int32_t *out_depth,
+                             void *stream);
+
+/* ---------------------------------------------------------------------------
+ * sv_kv_compact -- KV rollback / compaction.
+ * [Lesson] "Reversão de KV cache" (scratch buffer committed on acceptance, or
+ * a physical cache with a logical length truncated on rejection) and Passo 4;
+ * [Blog] section 3 (copy the accepted path's KV rows together, drop the other
+ * branches) and compact_kv in section 4.
+ *
+ * Cache layout [L][2][B][S][H][D], elem_bytes per element; one token row is
+ * H*D*elem_bytes contiguous bytes.  For every sequence b, layer and K/V:
+ *   dst row dst_base[b]+k  <-  src row src_base[b]+rows[b][k],  k < n,
+ * with n = n_rows[b] + n_rows_add, all reads before any write.  rows == NULL
+ * means rows[b][k] = k.  out_kv_len[b] = dst_base[b] + n, or -1 with nothing
+ * moved when n is outside [0, P], a row is out of range, or an in-place call
+ * (src_kv == dst_kv) has dst_base != src_base or rows not strictly increasing
+ * with rows[k] >= k (an accepted tree path always satisfies both).  In place,
+ * rows with rows[k] == k are not copied.  src_kv and dst_kv must be the same
+ * buffer or not overlap.
+ * Typical uses: tree compaction with rows = out_path_nodes, n_rows =
+ * out_accept_len, n_rows_add = 1; chain rollback (rows NULL, in place: no
+ * bytes move, only the length); scratch commit (src = scratch, src_base 0).
+ * --------------------------------------------------------------------------- */
+sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int B,
+                        int S_src, int S_dst, int H, int D, int elem_bytes,
+                        const int32_t *src_base, const int32_t *dst_base,
+                        const int32_t *rows, const int32_t *n_rows,
+                        int n_rows_add, int P, int32_t *out_kv_len,
+                        void *stream);
+
+/* Thread-local message for the last non-OK status returned on this thread. */
+const char *sv_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Launch accounting and tracing (host-side; no device memory).
+ * sv_launch_count: kernels this library has launched since it was loaded.
+ * sv_trace_enable(1) starts recording a CUDA event pair around every kernel
+ * the library launches (on the launching stream); sv_trace_collect waits for
+ * the recorded events, writes up to `max` per-kernel aggregates and clears
+ * the record.  Returns the number of entries written, or -1 on a CUDA error.
+ * --------------------------------------------------------------------------- */
+typedef struct {
+  char name[40];
+  int64_t launches;
+  double total_ms;
+} sv_trace_entry;
+
+uint64_t sv_launch_count(void);
+sv_status sv_trace_enable(int on);
+int sv_trace_collect(sv_trace_entry *out, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_H */

@@ -81,7 +81,7 @@ def _declare(L):
     L.orc_verify.argtypes = [
         _f32p, C.c_int64, _f32p, C.c_int64, C.c_int, C.c_int, C.c_float,
         C.c_void_p, C.c_int, _i32p, _i32p, C.c_int, C.c_uint64, C.c_uint64,
-        C.c_void_p, C.c_int, C.c_void_p,
+        C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
         _i32p, C.c_int, _i32p, _f64p, _f64p, _f64p, C.c_int, _f64p, _u32p]
     L.orc_verify.restype = C.c_int
     L.orc_tree_valid.argtypes = [_i32p, C.c_void_p, C.c_int]
@@ -90,7 +90,7 @@ def _declare(L):
     L.orc_tree_best_path.restype = C.c_int
     L.orc_verify_tree.argtypes = [
         _f32p, _f32p, _i32p, _i32p, _f32p, C.c_int, C.c_int, C.c_int, C.c_int,
-        C.c_float, C.c_uint64, C.c_uint64, _i32p, _i32p, _i32p, _f64p, _f64p,
+        C.c_float, C.c_uint64, C.c_uint64, C.c_void_p, _i32p, _i32p, _i32p, _f64p, _f64p,
         _f64p, _f64p, _u32p]
     L.orc_verify_tree.restype = C.c_int
     L.orc_tree_mask.argtypes = [_i32p, C.c_int, C.c_int, _u64p, _i32p]
@@ -177,7 +177,7 @@ def sample_repro(xq, xp, u24_, T=1.0):
 # ---------------------------------------------------------------- verify
 def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
                  seed, step, u_acc=None, u_samp=None, v_bstride=None,
-                 d_bstride=None, B=None, maxpos=None):
+                 d_bstride=None, B=None, maxpos=None, seq_ids=None):
     vlog = _f32(vlog).reshape(-1)
     dlog = _f32(dlog).reshape(-1)
     npos = _i32(npos)
@@ -204,6 +204,10 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
     if u_samp is not None:
         us = np.ascontiguousarray(u_samp, np.uint32)
         keep.append(us)
+    sid = None
+    if seq_ids is not None:
+        sid = _i32(seq_ids)
+        keep.append(sid)
     rc = lib().orc_verify(
         vlog, v_bstride, dlog, d_bstride, B, V, T,
         pth.ctypes.data if pth is not None else None, path_stride, npos, tok,
@@ -211,6 +215,7 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
         ua.ctypes.data if ua is not None else None,
         ua.shape[-1] if ua is not None else 0,
         us.ctypes.data if us is not None else None,
+        sid.ctypes.data if sid is not None else None,
         out_tok, maxpos + 1, out_acc, out_q, out_p, out_m, maxpos, out_gap, out_st)
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
@@ -219,7 +224,7 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
 
 
 def verify_chain(vlogits, dlogits, draft_tokens, T=1.0, seed=0, step=0,
-                 u_acc=None, u_samp=None, shared_rows=False):
+                 u_acc=None, u_samp=None, shared_rows=False, seq_ids=None):
     """Chain verify.  vlogits [B][N+1][V], dlogits [B][N][V], draft_tokens [B][N].
 
     With ``shared_rows`` the logits are a single [N+1][V] / [N][V] set used by
@@ -236,11 +241,12 @@ def verify_chain(vlogits, dlogits, draft_tokens, T=1.0, seed=0, step=0,
         dl = _f32(dlogits)
     return _verify_core(vl, dl, V, T, None, 0, np.full(B, N, np.int32),
                         draft_tokens, N, seed, step, u_acc, u_samp,
-                        v_bstride=vstride, d_bstride=dstride, B=B, maxpos=N)
+                        v_bstride=vstride, d_bstride=dstride, B=B, maxpos=N,
+                        seq_ids=seq_ids)
 
 
 def verify_tree(vlogits, dlogits, parent, token, score, max_depth, T=1.0,
-                seed=0, step=0):
+                seed=0, step=0, seq_ids=None):
     """Tree verify.  vlogits/dlogits [B][T][V]; parent/token/score [B][T]."""
     vl = _f32(vlogits)
     dl = _f32(dlogits)
@@ -258,9 +264,11 @@ def verify_tree(vlogits, dlogits, parent, token, score, max_depth, T=1.0,
     out_m = np.empty((B, P), np.float64)
     out_gap = np.empty(B, np.float64)
     out_st = np.empty(B, np.uint32)
+    sid = _i32(seq_ids) if seq_ids is not None else None
     lib().orc_verify_tree(vl.reshape(-1), dl.reshape(-1), parent.reshape(-1),
                           token.reshape(-1), score.reshape(-1), B, Tn, max_depth,
-                          V, T, seed, step, out_path, out_tok, out_acc, out_q,
+                          V, T, seed, step, sid.ctypes.data if sid is not None else None,
+                          out_path, out_tok, out_acc, out_q,
                           out_p, out_m, out_gap, out_st)
     return dict(path=out_path, tokens=out_tok, accept_len=out_acc,
                 q_prob=out_q[:, :max_depth], p_prob=out_p[:, :max_depth],

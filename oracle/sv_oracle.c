@@ -300,14 +300,17 @@ int orc_sample_repro(const float *xq, const float *xp, int V, float invT,
  * q(d)/p(d) is evaluated as exp of its logarithm so that tiny probabilities do
  * not underflow to 0/0; p(d) <= 0 means the draft logit is -inf.
  *
- * u_acc / u_samp (optional) replace the Philox uniforms, for enumeration.
+ * u_acc / u_samp (optional) replace the Philox uniforms, for enumeration;
+ * seq_ids (optional) gives each row of the batch its sequence number in the
+ * Philox counter, so that a subset of a batch can be replayed.
  * ---------------------------------------------------------------------- */
 int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
                int64_t d_bstride, int B, int V, float T,
                const int32_t *path, int path_stride, const int32_t *npos_arr,
                const int32_t *tok, int tok_stride, uint64_t seed,
                uint64_t step, const uint32_t *u_acc, int u_acc_stride,
-               const uint32_t *u_samp, int32_t *out_tokens, int out_stride,
+               const uint32_t *u_samp, const int32_t *seq_ids,
+               int32_t *out_tokens, int out_stride,
                int32_t *out_accept, double *out_q, double *out_p,
                double *out_margin, int margin_stride, double *out_gap,
                uint32_t *out_status) {
@@ -315,6 +318,7 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
   float invT = 1.0f / T;
   double Td = (double)T;
   for (int b = 0; b < B; ++b) {
+    const uint32_t sid = seq_ids ? (uint32_t)seq_ids[b] : (uint32_t)b;
     const float *vb = vlog + (int64_t)b * v_bstride;
     const float *db = dlog + (int64_t)b * d_bstride;
     int npos = npos_arr[b];
@@ -362,8 +366,7 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
       else
         ratio = exp(((zq - mq) - (zp - mp)) + (log(sp) - log(sq)));
       uint32_t u24 = u_acc ? u_acc[(int64_t)b * u_acc_stride + i]
-                           : orc_u24(seed, step, (uint32_t)b, (uint32_t)i,
-                                     ORC_DRAW_ACCEPT);
+                           : orc_u24(seed, step, sid, (uint32_t)i, ORC_DRAW_ACCEPT);
       double u = (double)u24 * 0x1p-24;
       if (out_q) out_q[(int64_t)b * margin_stride + i] = qd;
       if (out_p) out_p[(int64_t)b * margin_stride + i] = pd;
@@ -381,8 +384,7 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
     }
     /* correction (residual at position a) or bonus (verifier row path[npos]) */
     uint32_t us = u_samp ? u_samp[b]
-                         : orc_u24(seed, step, (uint32_t)b, (uint32_t)a,
-                                   ORC_DRAW_SAMPLE);
+                         : orc_u24(seed, step, sid, (uint32_t)a, ORC_DRAW_SAMPLE);
     double gap = NAN;
     int rz = 0, k;
     if (a < npos) {
@@ -450,7 +452,8 @@ int orc_tree_best_path(const int32_t *parent, const float *score, int T,
 int orc_verify_tree(const float *vlog, const float *dlog, const int32_t *parent,
                     const int32_t *token, const float *score, int B, int T,
                     int max_depth, int V, float temperature, uint64_t seed,
-                    uint64_t step, int32_t *out_path, int32_t *out_tokens,
+                    uint64_t step, const int32_t *seq_ids, int32_t *out_path,
+                    int32_t *out_tokens,
                     int32_t *out_accept, double *out_q, double *out_p,
                     double *out_margin, double *out_gap, uint32_t *out_status) {
   int P = max_depth + 1;
@@ -475,7 +478,7 @@ int orc_verify_tree(const float *vlog, const float *dlog, const int32_t *parent,
   }
   int rc = orc_verify(vlog, (int64_t)T * V, dlog, (int64_t)T * V, B, V,
                       temperature, path, P, npos, tok, P - 1, seed, step, NULL,
-                      0, NULL, out_tokens, P, out_accept, out_q, out_p,
+                      0, NULL, seq_ids, out_tokens, P, out_accept, out_q, out_p,
                       out_margin, P - 1, out_gap, out_status);
   for (int b = 0; b < B; ++b) {
     int32_t *op = out_path + (int64_t)b * P;

@@ -1,0 +1,239 @@
+"""Python binding for libsv.so, the sm_103a verify-and-accept library.
+
+Argument marshalling only: every step runs in the CUDA kernels behind the C
+ABI declared in ``include/sv.h``.  The ``sv_*`` functions keep the C names and
+take torch tensors (device memory) instead of raw pointers; the lower-case
+helpers (``verify_chain`` ...) allocate the outputs and the workspace.  There
+is no CPU fallback: if the shared library is missing, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsv.so")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_TIMEOUT = 0, 1, 2, 3, 4
+SV_F32, SV_BF16 = 0, 1
+SV_ROW_NAN, SV_ROW_BAD_TOKEN, SV_ROW_RESID_ZERO, SV_ROW_P_ZERO, SV_ROW_BAD_TREE = 1, 2, 4, 8, 16
+SV_MAX_VOCAB, SV_MAX_POSITIONS, SV_MAX_TREE_NODES = 1 << 22, 1024, 1024
+
+EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain", "sv_verify_tree_workspace",
+           "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_last_error",
+           "sv_launch_count", "sv_trace_enable", "sv_trace_collect")
+
+
+class SvError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"sv status {status}: {msg}")
+        self.status = status
+
+
+class TraceEntry(C.Structure):
+    _fields_ = [("name", C.c_char * 40), ("launches", C.c_int64), ("total_ms", C.c_double)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libsv.so (no GPU needed) and declare every exported symbol."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with __graft_entry__.build() "
+                          "(nvcc, sm_103a); there is no CPU fallback")
+    L = C.CDLL(path)
+    vp, i32, u64, f32, sz = C.c_void_p, C.c_int, C.c_uint64, C.c_float, C.c_size_t
+    L.sv_verify_chain_workspace.argtypes = [i32, i32, i32]
+    L.sv_verify_chain_workspace.restype = sz
+    L.sv_verify_chain.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
+                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sv_verify_chain.restype = i32
+    L.sv_verify_tree_workspace.argtypes = [i32, i32, i32, i32]
+    L.sv_verify_tree_workspace.restype = sz
+    L.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
+                                 vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sv_verify_tree.restype = i32
+    L.sv_tree_build_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.sv_tree_build_mask.restype = i32
+    L.sv_kv_compact.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                i32, i32, vp, vp]
+    L.sv_kv_compact.restype = i32
+    L.sv_last_error.argtypes = []
+    L.sv_last_error.restype = C.c_char_p
+    L.sv_launch_count.argtypes = []
+    L.sv_launch_count.restype = C.c_uint64
+    L.sv_trace_enable.argtypes = [i32]
+    L.sv_trace_enable.restype = i32
+    L.sv_trace_collect.argtypes = [C.POINTER(TraceEntry), i32]
+    L.sv_trace_collect.restype = i32
+    _lib = L
+    return L
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("sv: tensors must live in device memory")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(st):
+    if st != SV_OK:
+        raise SvError(st, load_library().sv_last_error().decode())
+    return st
+
+
+def _dtype(t):
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise ValueError(f"unsupported logit dtype {t.dtype}")
+
+
+# ------------------------------------------------------------------ C names
+def sv_verify_chain_workspace(B, N, V):
+    return int(load_library().sv_verify_chain_workspace(B, N, V))
+
+
+def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out_tokens,
+                    out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, workspace,
+                    stream=None):
+    B, R, V = vlogits.shape
+    N = R - 1
+    return _check(load_library().sv_verify_chain(
+        _p(vlogits), _p(dlogits) if N > 0 else None, _dtype(vlogits),
+        _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
+        _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
+        _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def sv_verify_tree_workspace(B, T, max_depth, V):
+    return int(load_library().sv_verify_tree_workspace(B, T, max_depth, V))
+
+
+def sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
+                   out_path_nodes, out_tokens, out_accept_len, out_q_prob, out_p_prob,
+                   out_margin, out_status, workspace, stream=None):
+    B, T, V = vlogits.shape
+    return _check(load_library().sv_verify_tree(
+        _p(vlogits), _p(dlogits), _dtype(vlogits), _p(parent), _p(token), _p(score), B, T,
+        max_depth, V, float(temperature), int(seed), int(step), _p(out_path_nodes),
+        _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
+        _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def sv_tree_build_mask(parent, out_mask, out_depth, stream=None):
+    B, T = parent.shape
+    return _check(load_library().sv_tree_build_mask(_p(parent), B, T, _p(out_mask),
+                                                    _p(out_depth), _stream(stream)))
+
+
+def sv_kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add, out_kv_len,
+                  stream=None):
+    """src_kv [L][2][B][S_src][H][D], dst_kv [L][2][B][S_dst][H][D] (any dtype)."""
+    L, two, B, S_src, H, D = src_kv.shape
+    S_dst = dst_kv.shape[3]
+    P = rows.shape[1] if rows is not None else S_src
+    return _check(load_library().sv_kv_compact(
+        _p(src_kv), _p(dst_kv), L, B, S_src, S_dst, H, D, src_kv.element_size(),
+        _p(src_base), _p(dst_base), _p(rows), _p(n_rows), int(n_rows_add), P,
+        _p(out_kv_len), _stream(stream)))
+
+
+def sv_last_error():
+    return load_library().sv_last_error().decode()
+
+
+def sv_launch_count():
+    return int(load_library().sv_launch_count())
+
+
+def sv_trace_enable(on=True):
+    return _check(load_library().sv_trace_enable(1 if on else 0))
+
+
+def sv_trace_collect(max_entries=64):
+    buf = (TraceEntry * max_entries)()
+    n = load_library().sv_trace_collect(buf, max_entries)
+    if n < 0:
+        raise SvError(SV_ERR_CUDA, sv_last_error())
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n)}
+
+
+# ------------------------------------------------------------------ helpers
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0,
+                 workspace=None, stream=None, probs=True):
+    """Allocate outputs and run sv_verify_chain.  Returns a dict of tensors."""
+    B, R, V = vlogits.shape
+    N = R - 1
+    dev = vlogits.device
+    out = dict(
+        tokens=torch.empty(B, N + 1, dtype=torch.int32, device=dev),
+        accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+        q_prob=torch.empty(B, max(N, 1), dtype=torch.float32, device=dev) if probs else None,
+        p_prob=torch.empty(B, max(N, 1), dtype=torch.float32, device=dev) if probs else None,
+        margin=torch.empty(B, N + 1, dtype=torch.float32, device=dev) if probs else None,
+        status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = _ws(sv_verify_chain_workspace(B, N, V), dev)
+    sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out["tokens"],
+                    out["accept_len"], out["q_prob"], out["p_prob"], out["margin"],
+                    out["status"], workspace, stream)
+    return out
+
+
+def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1.0, seed=0,
+                step=0, workspace=None, stream=None, probs=True):
+    B, T, V = vlogits.shape
+    dev = vlogits.device
+    P = max_depth + 1
+    out = dict(
+        path=torch.empty(B, P, dtype=torch.int32, device=dev),
+        tokens=torch.empty(B, P, dtype=torch.int32, device=dev),
+        accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+        q_prob=torch.empty(B, max(max_depth, 1), dtype=torch.float32, device=dev) if probs else None,
+        p_prob=torch.empty(B, max(max_depth, 1), dtype=torch.float32, device=dev) if probs else None,
+        margin=torch.empty(B, P, dtype=torch.float32, device=dev) if probs else None,
+        status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = _ws(sv_verify_tree_workspace(B, T, max_depth, V), dev)
+    sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
+                   out["path"], out["tokens"], out["accept_len"], out["q_prob"], out["p_prob"],
+                   out["margin"], out["status"], workspace, stream)
+    return out
+
+
+def tree_build_mask(parent, stream=None):
+    B, T = parent.shape
+    W = (T + 63) // 64
+    mask = torch.empty(B, T, W, dtype=torch.int64, device=parent.device)
+    depth = torch.empty(B, T, dtype=torch.int32, device=parent.device)
+    sv_tree_build_mask(parent, mask, depth, stream)
+    return mask, depth
+
+
+def kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add=0, stream=None):
+    B = src_kv.shape[2]
+    kv_len = torch.empty(B, dtype=torch.int32, device=src_kv.device)
+    sv_kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add, kv_len, stream)
+    return kv_len

@@ -1,0 +1,134 @@
+// common.cuh -- device helpers and the host runtime hooks shared by the
+// library's translation units (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sv.h"
+
+namespace sv {
+
+// ----------------------------------------------------------------- host side
+// Error reporting (thread-local message) and launch bookkeeping.
+sv_status set_error(sv_status st, const char *fmt, ...);
+sv_status check_launch(const char *what);
+int num_sms();
+
+// Wraps every kernel launch: counts it and, while tracing is on, records an
+// event pair around it on the launching stream.
+struct LaunchScope {
+  int slot;
+  cudaStream_t stream;
+  LaunchScope(const char *name, cudaStream_t s);
+  ~LaunchScope();
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------- device side
+constexpr uint32_t kDrawAccept = 0u;
+constexpr uint32_t kDrawSample = 1u;
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 products with multipliers 0xD2511F53 / 0xCD9E8D57, a word
+// permutation XOR-ing the high halves into the other words and the round key,
+// and a Weyl key bump (0x9E3779B9, 0xBB67AE85) between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k.x += 0x9E3779B9u;
+      k.y += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+  }
+  return c;
+}
+
+// Top 24 bits of the first Philox word for counter (pos, draw, seq, step).
+__device__ __forceinline__ uint32_t uniform_u24(uint64_t seed, uint64_t step,
+                                                uint32_t seq, uint32_t pos,
+                                                uint32_t draw) {
+  const uint4 o = philox4x32_10(make_uint4(pos, draw, seq, (uint32_t)step),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  return o.x >> 8;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T> __device__ __forceinline__ float load_elem(const T *p);
+template <> __device__ __forceinline__ float load_elem<float>(const float *p) { return __ldg(p); }
+template <> __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t *p) {
+  return __uint_as_float((uint32_t)__ldg(p) << 16);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Online-softmax pair (m, s): s = sum exp2((x - m) * k).  Merge (m2, s2)
+// into (m, s).  A NaN sum (a NaN or +inf logit in the row) stays NaN.
+__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2,
+                                           float k) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) {
+    s = s + s2;
+    return;
+  }
+  s = s * ex2_approx((m - M) * k) + s2 * ex2_approx((m2 - M) * k);
+  m = M;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ----------------------------------------------------------------------------
+// The sampling arithmetic: an fp32 exponential from basic IEEE operations
+// only (explicit _rn intrinsics, so no contraction or fast-math can change a
+// bit): 0 below -80; n = nearest integer to a*log2(e) by the 1.5*2^23 shift;
+// Cody-Waite two-constant reduction r = a - n*ln2; e^r by the Taylor series to
+// degree 7 (coefficients 1/k! rounded to fp32) in Horner form with fused
+// multiply-adds; scaled by 2^n.  Max error about 2 ulp over [-80, 0].
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float exp32_repro(float a) {
+  if (!(a >= -80.0f)) return 0.0f;
+  const float t = __fmaf_rn(a, 0x1.715476p+0f, 0x1.8p+23f);
+  const float n = __fsub_rn(t, 0x1.8p+23f);
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, a);
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+  float p = 1.0f / 5040.0f;
+  p = __fmaf_rn(p, r, 1.0f / 720.0f);
+  p = __fmaf_rn(p, r, 1.0f / 120.0f);
+  p = __fmaf_rn(p, r, 1.0f / 24.0f);
+  p = __fmaf_rn(p, r, 1.0f / 6.0f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int ni = __float2int_rz(n);
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+}  // namespace sv

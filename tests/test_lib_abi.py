@@ -1,0 +1,74 @@
+"""CPU checks of the C ABI: the shared library loads, exports every entry point
+that include/sv.h declares, and rejects bad arguments on the host without
+touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_vocab_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_vocab_gb300 as sv
+    return sv.load_library()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "sv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("sv_verify_chain", "sv_verify_tree", "sv_kv_compact", "sv_tree_build_mask",
+                 "sv_verify_chain_workspace", "sv_verify_tree_workspace", "sv_last_error"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import speculative_decoding_verification_vocab_gb300 as sv
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in sv.EXPORTS or name.endswith("_workspace") or name.startswith("sv_")
+
+
+def test_binding_has_the_c_names():
+    import speculative_decoding_verification_vocab_gb300 as sv
+    for name in declared_symbols():
+        assert callable(getattr(sv, name)), name
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    null = None
+    # negative sizes, bad dtype, bad temperature: refused before any CUDA call
+    assert lib.sv_verify_chain(null, null, 0, null, -1, 2, 10, 1.0, 0, 0, null, null, null, null,
+                               null, null, null, 0, null) == 1
+    assert lib.sv_verify_chain(null, null, 7, null, 1, 2, 10, 1.0, 0, 0, null, null, null, null,
+                               null, null, null, 0, null) == 1
+    assert lib.sv_verify_chain(null, null, 0, null, 1, 2, 10, 0.0, 0, 0, null, null, null, null,
+                               null, null, null, 0, null) == 1
+    assert b"temperature" in lib.sv_last_error()
+    assert lib.sv_verify_chain(null, null, 0, null, 1, 2, (1 << 22) + 1, 1.0, 0, 0, null, null,
+                               null, null, null, null, null, 0, null) == 2
+    # B == 0 is a no-op
+    assert lib.sv_verify_chain(null, null, 0, null, 0, 2, 10, 1.0, 0, 0, null, null, null, null,
+                               null, null, null, 0, null) == 0
+    assert lib.sv_verify_tree(null, null, 1, null, null, null, 1, 20, 3, 10, 1.0, 0, 0, null,
+                              null, null, null, null, null, null, null, 0, null) == 1
+    assert lib.sv_tree_build_mask(null, 1, 2000, null, null, null) == 2
+    assert lib.sv_tree_build_mask(null, 1, 0, null, null, null) == 1
+    assert lib.sv_kv_compact(null, null, 0, 1, 4, 4, 1, 1, 2, null, null, null, null, 0, 1,
+                             null, null) == 1
+    assert lib.sv_launch_count() >= 0
+
+
+def test_workspace_queries(lib):
+    assert lib.sv_verify_chain_workspace(4, 3, 1000) > 0
+    assert lib.sv_verify_tree_workspace(4, 25, 5, 1000) > lib.sv_verify_chain_workspace(4, 0, 1000)
+    assert lib.sv_verify_chain_workspace(-1, 3, 1000) == 0
