@@ -265,7 +265,9 @@ def tree_inputs(cfg: Config, seed=None, device="cpu", **kw):
 
 
 def kv_cache(L, B, S, H, D, device="cpu", seed=0, dtype=torch.bfloat16):
-    """Random KV cache [L][2][B][S][H][D]."""
+    """Random KV cache [L][2][B][S][H][D] of `dtype` (random bytes)."""
     g = _gen(seed + 17, device)
-    return torch.randint(-2 ** 15, 2 ** 15, (L, 2, B, S, H, D), generator=g, device=device,
-                         dtype=torch.int16).view(dtype)
+    esize = torch.tensor([], dtype=dtype).element_size()
+    raw = torch.randint(0, 256, (L, 2, B, S, H, D * esize), generator=g, device=device,
+                        dtype=torch.uint8)
+    return raw.view(dtype)

@@ -183,7 +183,7 @@ def test_bad_trees_are_flagged():
     parent[0, 5] = 20            # parent after child
     parent[1, 0] = 0             # root with a parent
     score[2, 3] = float("nan")
-    parent[3, 7] = -2            # a padded slot that still has children
+    parent[3, 5] = -2            # a padded slot that still has children (13, 14, 15)
     g, o = run_tree(vq, dp, parent, token, score, c4.depth)
     assert np.all(to_np(g["status"]) == sv.SV_ROW_BAD_TREE)
     compare_verify(g, o, rows_per_seq=25, npos=np.zeros(4), label="bad trees")
