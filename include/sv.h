@@ -188,6 +188,38 @@ sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int B,
                         int n_rows_add, int P, int32_t *out_kv_len,
                         void *stream);
 
+/* ---------------------------------------------------------------------------
+ * sv_verify_chain_noalloc -- sv_verify_chain without a caller workspace.
+ * The pages have no counterpart to this call; it exists for callers that must
+ * not allocate device memory at all: a plugin inside a host program that owns
+ * every device allocation through its own pool, a caller whose memory budget
+ * is fixed once at start-up, or code that may run where an allocation would
+ * synchronise the device.  Such callers still pass every input and output.
+ *
+ * Scratch comes from one file-scope static device array of
+ * sv_verify_chain_noalloc_max_bytes() bytes (4 MiB), which every GPU that
+ * loads this library keeps until the process exits.  A call whose
+ * sv_verify_chain_workspace(B, N, V) exceeds it returns SV_ERR_UNSUPPORTED
+ * with a message and enqueues nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  Nothing here
+ * calls cudaMalloc, cudaFree or any allocating routine.
+ * All calls on a device share the one array, which keeps the previous call's
+ * contents; the kernels write every scratch word before reading it, so nothing
+ * has to start at zero.  Calls that overlap on the GPU (for example on two
+ * streams at once) race on the array: serialise them.
+ * Arguments, outputs and errors are otherwise those of sv_verify_chain.
+ * --------------------------------------------------------------------------- */
+size_t sv_verify_chain_noalloc_max_bytes(void);
+sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dlogits,
+                                  sv_dtype dt, const int32_t *draft_tokens,
+                                  int B, int N, int V, float temperature,
+                                  uint64_t seed, uint64_t step,
+                                  int32_t *out_tokens, int32_t *out_accept_len,
+                                  float *out_q_prob, float *out_p_prob,
+                                  float *out_margin, uint32_t *out_status,
+                                  void *stream);
+
 /* Thread-local message for the last non-OK status returned on this thread. */
 const char *sv_last_error(void);
 

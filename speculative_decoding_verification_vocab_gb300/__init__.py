@@ -21,7 +21,8 @@ SV_F32, SV_BF16 = 0, 1
 SV_ROW_NAN, SV_ROW_BAD_TOKEN, SV_ROW_RESID_ZERO, SV_ROW_P_ZERO, SV_ROW_BAD_TREE = 1, 2, 4, 8, 16
 SV_MAX_VOCAB, SV_MAX_POSITIONS, SV_MAX_TREE_NODES = 1 << 22, 1024, 1024
 
-EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain", "sv_verify_tree_workspace",
+EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain", "sv_verify_chain_noalloc",
+           "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
            "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_last_error",
            "sv_launch_count", "sv_trace_enable", "sv_trace_collect")
 
@@ -54,6 +55,11 @@ def load_library(path: str = LIB_PATH):
     L.sv_verify_chain.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
                                   vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.sv_verify_chain.restype = i32
+    L.sv_verify_chain_noalloc_max_bytes.argtypes = []
+    L.sv_verify_chain_noalloc_max_bytes.restype = sz
+    L.sv_verify_chain_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
+                                          vp, vp, vp, vp, vp, vp, vp]
+    L.sv_verify_chain_noalloc.restype = i32
     L.sv_verify_tree_workspace.argtypes = [i32, i32, i32, i32]
     L.sv_verify_tree_workspace.restype = sz
     L.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
@@ -120,6 +126,24 @@ def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out
         _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
         _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def sv_verify_chain_noalloc_max_bytes():
+    return int(load_library().sv_verify_chain_noalloc_max_bytes())
+
+
+def sv_verify_chain_noalloc(vlogits, dlogits, draft_tokens, temperature, seed, step, out_tokens,
+                            out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
+                            stream=None):
+    """sv_verify_chain for callers that cannot allocate: scratch is the
+    library's static device array (see include/sv.h)."""
+    B, R, V = vlogits.shape
+    N = R - 1
+    return _check(load_library().sv_verify_chain_noalloc(
+        _p(vlogits), _p(dlogits) if N > 0 else None, _dtype(vlogits),
+        _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
+        _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
+        _p(out_status), _stream(stream)))
 
 
 def sv_verify_tree_workspace(B, T, max_depth, V):

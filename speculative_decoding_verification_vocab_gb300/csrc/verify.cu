@@ -817,3 +817,73 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st)
                        : run_verify<float>(r, L, ws, seed, step, o, st);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free chain verify.  Its scratch is a file-scope device array of
+// kStaticScratchBytes that every GPU loading this library holds until exit.
+// Host code cannot hand the array's name to a kernel (on the host it names a
+// stand-in, not device memory), so the device address is looked up once per
+// device with cudaGetSymbolAddress, with that device current, on the first
+// call made on it.
+#include <mutex>
+
+namespace sv {
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+}  // namespace
+}  // namespace sv
+
+static __device__ __align__(256) unsigned char g_static_scratch[sv::kStaticScratchBytes];
+
+namespace sv {
+namespace {
+sv_status static_scratch_address(void **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(SV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(SV_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return set_error(SV_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s",
+                       cudaGetErrorString(e));
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return SV_OK;
+}
+}  // namespace
+}  // namespace sv
+
+extern "C" size_t sv_verify_chain_noalloc_max_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dlogits,
+                                             sv_dtype dt, const int32_t *draft_tokens, int B,
+                                             int N, int V, float temperature, uint64_t seed,
+                                             uint64_t step, int32_t *out_tokens,
+                                             int32_t *out_accept_len, float *out_q_prob,
+                                             float *out_p_prob, float *out_margin,
+                                             uint32_t *out_status, void *stream) {
+  if (B < 0 || N < 0 || V < 1)
+    return set_error(SV_ERR_INVALID_ARG, "need B >= 0, N >= 0, V >= 1");
+  if (B == 0) return SV_OK;
+  const size_t need = sv_verify_chain_workspace(B, N, V);
+  if (need > kStaticScratchBytes)
+    return set_error(SV_ERR_UNSUPPORTED,
+                     "sv_verify_chain_noalloc: B=%d N=%d V=%d needs %zu bytes of scratch, "
+                     "more than the %zu-byte static scratch; use sv_verify_chain with a "
+                     "caller-owned workspace",
+                     B, N, V, need, kStaticScratchBytes);
+  void *ws = nullptr;
+  sv_status s = static_scratch_address(&ws);
+  if (s != SV_OK) return s;
+  return sv_verify_chain(vlogits, dlogits, dt, draft_tokens, B, N, V, temperature, seed, step,
+                         out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,
+                         out_status, ws, kStaticScratchBytes, stream);
+}
