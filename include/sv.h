@@ -172,9 +172,10 @@ sv_status sv_tree_build_mask(const int32_t *parent, int B, int T,
  *   dst row dst_base[b]+k  <-  src row src_base[b]+rows[b][k],  k < n,
  * with n = n_rows[b] + n_rows_add, all reads before any write.  rows == NULL
  * means rows[b][k] = k.  out_kv_len[b] = dst_base[b] + n, or -1 with nothing
- * moved when n is outside [0, P], a row is out of range, or an in-place call
- * (src_kv == dst_kv) has dst_base != src_base or rows not strictly increasing
- * with rows[k] >= k (an accepted tree path always satisfies both).  In place,
+ * moved when n is outside [0, P] or above 4096, a row is out of range, or an
+ * in-place call (src_kv == dst_kv) has dst_base != src_base or rows not
+ * strictly increasing with rows[k] >= k (an accepted tree path always
+ * satisfies both).  In place,
  * rows with rows[k] == k are not copied.  src_kv and dst_kv must be the same
  * buffer or not overlap.
  * Typical uses: tree compaction with rows = out_path_nodes, n_rows =

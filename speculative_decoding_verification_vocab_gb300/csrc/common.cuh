@@ -80,17 +80,42 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   return v;
 }
 
-// Online-softmax pair (m, s): s = sum exp2((x - m) * k).  Merge (m2, s2)
-// into (m, s).  A NaN sum (a NaN or +inf logit in the row) stays NaN.
-__device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2,
-                                           float k) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) {
-    s = s + s2;
-    return;
-  }
-  s = s * ex2_approx((m - M) * k) + s2 * ex2_approx((m2 - M) * k);
-  m = M;
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): two IEEE round-to-nearest
+// operations per instruction, bit-identical to the scalar ones.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// max of two bf16 pairs (a NaN operand yields the other operand)
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -114,7 +139,6 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
 // multiply-adds; scaled by 2^n.  Max error about 2 ulp over [-80, 0].
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ float exp32_repro(float a) {
-  if (!(a >= -80.0f)) return 0.0f;
   const float t = __fmaf_rn(a, 0x1.715476p+0f, 0x1.8p+23f);
   const float n = __fsub_rn(t, 0x1.8p+23f);
   float r = __fmaf_rn(-n, 0x1.62e4p-1f, a);
@@ -127,8 +151,10 @@ __device__ __forceinline__ float exp32_repro(float a) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  const int ni = __float2int_rz(n);
-  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+  // t is 1.5*2^23 + n exactly (|n| < 2^22), so the integer n sits in its bits
+  const int ni = __float_as_int(t) - 0x4B400000;
+  const float e = __fmul_rn(p, __int_as_float((ni + 127) << 23));
+  return (a >= -80.0f) ? e : 0.0f;
 }
 
 }  // namespace sv

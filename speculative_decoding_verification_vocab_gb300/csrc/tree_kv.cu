@@ -12,7 +12,7 @@ namespace sv {
 namespace {
 
 constexpr int kMaskThreads = 256;
-constexpr int kKvThreads = 128;
+constexpr int kKvThreads = 256;
 constexpr int kKvGroup = 8;  // rows loaded before any is stored
 
 // ---------------------------------------------------------------------------
@@ -53,12 +53,16 @@ tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__r
 }
 
 // ---------------------------------------------------------------------------
-// KV compaction: one CTA per (sequence, layer, K/V).  Each thread owns a
-// column of 16-byte words (or bytes on the unaligned path) across the kept
-// rows; rows are moved in groups of kKvGroup: all loads of a group, then its
-// stores.  In place, rows[k] >= k and strictly increasing guarantee that a
-// later group never reads a slot an earlier group wrote, and a group's own
-// reads precede its writes.
+// KV compaction: one CTA per (sequence, group of kKvSlabs (layer, K/V) slabs).
+// Every warp validates the request on its own (no block barrier): lanes read
+// 32 row indices at a time and vote.  Then each thread owns (slab, 16-byte
+// column) units and moves the rows in groups of kKvGroup: all loads of a
+// group, then its stores, groups in increasing k.  In place, rows[k] >= k and
+// strictly increasing mean a later group never reads a slot an earlier group
+// wrote, and a group's reads precede its writes; rows[k] == k are skipped.
+constexpr int kKvSlabs = 8;
+constexpr int kKvMaxRows = 4096;
+
 struct KvArgs {
   const char *src;
   char *dst;
@@ -70,70 +74,73 @@ struct KvArgs {
   int inplace, vec;
 };
 
-__device__ __forceinline__ int kv_rows_ok(const KvArgs &a, int b, int &n) {
-  n = a.n_rows[b] + a.n_add;
-  const int sb = a.src_base[b], db = a.dst_base[b];
-  if (n < 0 || n > a.P || sb < 0 || db < 0 || (long)db + n > a.S_dst) return 0;
-  if (a.inplace && sb != db) return 0;
-  int prev = -1;
-  for (int k = 0; k < n; ++k) {
-    const int r = a.rows ? a.rows[(size_t)b * a.P + k] : k;
-    if (r < 0 || (long)sb + r >= a.S_src) return 0;
-    if (a.inplace && (r < k || r <= prev)) return 0;
-    prev = r;
-  }
-  return 1;
-}
-
 __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
   const int b = blockIdx.x;
-  const int slab_i = blockIdx.y;  // l * 2 + kv
-  __shared__ int s_ok, s_n;
-  if (threadIdx.x == 0) {
-    int n;
-    const int ok = kv_rows_ok(a, b, n);
-    s_ok = ok;
-    s_n = n;
-    if (slab_i == 0) a.kv_len[b] = ok ? a.dst_base[b] + n : -1;
-  }
-  __syncthreads();
-  if (!s_ok) return;
-  const int n = s_n;
-  const size_t slab = (size_t)slab_i * a.B + b;
-  const char *sbase = a.src + (slab * a.S_src + a.src_base[b]) * a.row_bytes;
-  char *dbase = a.dst + (slab * a.S_dst + a.dst_base[b]) * a.row_bytes;
+  const int lane = threadIdx.x & 31;
+  const unsigned FULL = 0xffffffffu;
+  const int n = a.n_rows[b] + a.n_add;
+  const int sb = a.src_base[b], db = a.dst_base[b];
+  bool ok = n >= 0 && n <= a.P && n <= kKvMaxRows && sb >= 0 && db >= 0 &&
+            (long)db + n <= a.S_dst && !(a.inplace && sb != db);
   const int32_t *rows = a.rows ? a.rows + (size_t)b * a.P : nullptr;
-  for (int k0 = 0; k0 < n; k0 += kKvGroup) {
-    const int kn = min(kKvGroup, n - k0);
-    int rr[kKvGroup];
+  int prev_last = -1;
+  for (int k0 = 0; ok && k0 < n; k0 += 32) {
+    const int k = k0 + lane;
+    const bool in = k < n;
+    const int r = in ? (rows ? rows[k] : k) : 0;
+    int prev = __shfl_up_sync(FULL, r, 1);
+    if (lane == 0) prev = prev_last;
+    bool bad = in && (r < 0 || (long)sb + r >= a.S_src);
+    if (a.inplace) bad = bad || (in && (r < k || r <= prev));
+    if (__any_sync(FULL, bad)) ok = false;
+    prev_last = __shfl_sync(FULL, r, 31);
+  }
+  if (blockIdx.y == 0 && threadIdx.x == 0) a.kv_len[b] = ok ? db + n : -1;
+  if (!ok || n == 0) return;
+  const int slab0 = blockIdx.y * kKvSlabs;
+  const int nslab = min(kKvSlabs, 2 * a.L - slab0);
+  const size_t ncol = a.vec ? a.row_bytes / 16 : a.row_bytes;
+  const size_t units = (size_t)nslab * ncol;
+  const size_t sbase_off = (size_t)sb * a.row_bytes, dbase_off = (size_t)db * a.row_bytes;
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    // this chunk's moves: lane j holds row k0 + j
+    const int kn = min(32, n - k0);
+    const int my_r = lane < kn ? (rows ? rows[k0 + lane] : k0 + lane) : 0;
+    for (int g0 = 0; g0 < kn; g0 += kKvGroup) {
+      int rr[kKvGroup];  // warp-uniform: broadcast before the divergent unit loop
 #pragma unroll
-    for (int j = 0; j < kKvGroup; ++j) rr[j] = (j < kn) ? (rows ? rows[k0 + j] : k0 + j) : 0;
-    if (a.vec) {
-      const size_t nw = a.row_bytes / 16;
-      for (size_t c = threadIdx.x; c < nw; c += kKvThreads) {
-        uint4 v[kKvGroup];
+      for (int j = 0; j < kKvGroup; ++j) rr[j] = __shfl_sync(FULL, my_r, (g0 + j) & 31);
+      for (size_t u = threadIdx.x; u < units; u += kKvThreads) {
+        const int sl = (int)(u / ncol);
+        const size_t c = u - (size_t)sl * ncol;
+        const size_t slab = (size_t)(slab0 + sl) * a.B + b;
+        const char *sp = a.src + slab * a.S_src * a.row_bytes + sbase_off;
+        char *dp = a.dst + slab * a.S_dst * a.row_bytes + dbase_off;
+        if (a.vec) {
+          uint4 v[kKvGroup];
 #pragma unroll
-        for (int j = 0; j < kKvGroup; ++j)
-          if (j < kn && !(a.inplace && rr[j] == k0 + j))
-            v[j] = ld_stream_v4(sbase + (size_t)rr[j] * a.row_bytes + c * 16);
+          for (int j = 0; j < kKvGroup; ++j) {
+            const int k = k0 + g0 + j;
+            if (g0 + j < kn && !(a.inplace && rr[j] == k))
+              v[j] = ld_stream_v4(sp + (size_t)rr[j] * a.row_bytes + c * 16);
+          }
 #pragma unroll
-        for (int j = 0; j < kKvGroup; ++j)
-          if (j < kn && !(a.inplace && rr[j] == k0 + j))
-            *(uint4 *)(dbase + (size_t)(k0 + j) * a.row_bytes + c * 16) = v[j];
-      }
-    } else {
-      for (size_t c = threadIdx.x; c < a.row_bytes; c += kKvThreads) {
-        char v[kKvGroup];
+          for (int j = 0; j < kKvGroup; ++j) {
+            const int k = k0 + g0 + j;
+            if (g0 + j < kn && !(a.inplace && rr[j] == k))
+              *(uint4 *)(dp + (size_t)k * a.row_bytes + c * 16) = v[j];
+          }
+        } else {
+          char v[kKvGroup];
 #pragma unroll
-        for (int j = 0; j < kKvGroup; ++j)
-          if (j < kn) v[j] = sbase[(size_t)rr[j] * a.row_bytes + c];
+          for (int j = 0; j < kKvGroup; ++j)
+            if (g0 + j < kn) v[j] = sp[(size_t)rr[j] * a.row_bytes + c];
 #pragma unroll
-        for (int j = 0; j < kKvGroup; ++j)
-          if (j < kn) dbase[(size_t)(k0 + j) * a.row_bytes + c] = v[j];
+          for (int j = 0; j < kKvGroup; ++j)
+            if (g0 + j < kn) dp[(size_t)(k0 + g0 + j) * a.row_bytes + c] = v[j];
+        }
       }
     }
-    // in place, the next group reads slots >= k0 + kKvGroup, which this
-    // group never writes; other threads touch other columns.
   }
 }
 
@@ -162,7 +169,7 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
                                    int P, int32_t *out_kv_len, void *stream) {
   if (L < 1 || B < 0 || S_src < 1 || S_dst < 1 || H < 1 || D < 1 || elem_bytes < 1 || P < 0)
     return set_error(SV_ERR_INVALID_ARG, "bad KV shape");
-  if (2L * L > 65535) return set_error(SV_ERR_UNSUPPORTED, "L > 32767");
+  if ((2L * L + kKvSlabs - 1) / kKvSlabs > 65535) return set_error(SV_ERR_UNSUPPORTED, "L too large");
   if (B == 0) return SV_OK;
   if (!src_kv || !dst_kv || !src_base || !dst_base || !n_rows || !out_kv_len)
     return set_error(SV_ERR_INVALID_ARG, "null pointer");
@@ -185,6 +192,6 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   a.vec = (a.row_bytes % 16 == 0) && ((uintptr_t)src_kv % 16 == 0) && ((uintptr_t)dst_kv % 16 == 0);
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("kv_compact", st);
-  kv_compact_kernel<<<dim3(B, 2 * L), kKvThreads, 0, st>>>(a);
+  kv_compact_kernel<<<dim3(B, (2 * L + kKvSlabs - 1) / kKvSlabs), kKvThreads, 0, st>>>(a);
   return check_launch("kv_compact");
 }

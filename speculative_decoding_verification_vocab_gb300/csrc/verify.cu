@@ -19,14 +19,17 @@
 
 #include "common.cuh"
 
+
 namespace sv {
 namespace {
 
-constexpr int kStatsThreads = 512;
 constexpr int kDecideWarps = 4;
-constexpr int kSampleThreads = 256;
-constexpr int kChunk = 2048;          // tokens per fixed-point chunk sum
-constexpr int kChunksPerSeg = 8;      // chunks per sampler CTA
+// sampler geometry: a CTA owns an 8192-element slice of a row; each of its
+// threads owns kSpRun consecutive elements of the slice
+constexpr int kSpThreads = 256;
+constexpr int kSpWarps = kSpThreads / 32;
+constexpr int kSpRun = 32;
+constexpr int kSpSlice = kSpThreads * kSpRun;  // 8192 elements per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Task {
@@ -39,52 +42,12 @@ struct Task {
   int pad;
 };
 
-struct Acc {  // exact fixed-point sums of one sampling task
-  unsigned long long se_q, se_p;  // sum floor(e * 2^40)
-  unsigned long long sw, sq;      // sum floor(w * 2^62), sum floor(q * 2^62)
-};
-
 struct Layout {
-  int maxpos, P, G, seg_len, nchunk, G3;
-  size_t partial, task, acc, chunks, path, npos, tok, tstat, total;
+  int maxpos, P, G, CS;
+  size_t ctr, rowlist, partial, task, norm, mass, run, path, npos, tok, tstat, total;
 };
 
-Layout plan(int B, int maxpos, int V, bool tree) {
-  Layout L;
-  L.maxpos = maxpos;
-  L.P = 2 * maxpos + 1;
-  const long nslots = (long)B * L.P;
-  const long target = (long)num_sms() * 16;
-  int g = (int)((target + nslots - 1) / (nslots > 0 ? nslots : 1));
-  const int gmax = V / 4096 > 1 ? V / 4096 : 1;
-  g = g < 1 ? 1 : (g > gmax ? gmax : g);
-  int len = (V + g - 1) / g;
-  len = (len + 63) / 64 * 64;
-  L.seg_len = len;
-  L.G = (V + len - 1) / len;
-  L.nchunk = (V + kChunk - 1) / kChunk;
-  L.G3 = (L.nchunk + kChunksPerSeg - 1) / kChunksPerSeg;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t o = off;
-    off = align_up(off + bytes, 256);
-    return o;
-  };
-  L.partial = take(sizeof(float2) * (size_t)nslots * L.G);
-  L.task = take(sizeof(Task) * (size_t)B);
-  L.acc = take(sizeof(Acc) * (size_t)B);
-  L.chunks = take(sizeof(ulonglong2) * (size_t)B * L.nchunk);
-  if (tree) {
-    L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
-    L.npos = take(sizeof(int32_t) * (size_t)B);
-    L.tok = take(sizeof(int32_t) * (size_t)B * (maxpos > 0 ? maxpos : 1));
-    L.tstat = take(sizeof(uint32_t) * (size_t)B);
-  } else {
-    L.path = L.npos = L.tok = L.tstat = 0;
-  }
-  L.total = off + 256;
-  return L;
-}
+Layout plan(int B, int maxpos, int V, bool tree);
 
 // ---------------------------------------------------------------------------
 // Shared view of one round: how position i of sequence b maps to rows.
@@ -108,132 +71,243 @@ __device__ __forceinline__ int round_node(const Round &r, int b, int i) {
 }
 
 // ---------------------------------------------------------------------------
-// row_stats: work item = (slot, segment).  Slot j of a sequence is the
-// verifier row of position j (j <= maxpos) or the draft row of position
-// j - maxpos - 1.  Writes (max x, sum exp2((x - max) * k)) of its segment.
-template <typename E>
-__device__ __forceinline__ void accum8(uint4 v, float &m, float &s0, float &s1, float k);
+// row_stats: online softmax statistics of every used logit row.
+// One CTA per unit = one kSegElems-element segment of one row (tree: the
+// units of the rows on the best paths, listed by tree_path).  Each thread
+// keeps kRsUnroll 16-byte loads in flight and folds them into an online
+// (max, log2-reference, sum) triple; bf16 maxima are taken on packed pairs and
+// the reference moves only when a larger value appears.  The CTA combines the
+// triples and writes (max x, mk, sum exp2(fma(x, k, -mk))) for the segment.
+// Ragged head / tail elements (outside the 16-byte-aligned body) are read
+// one by one.  Row slot j of a sequence is the verifier row of position j
+// (j <= maxpos) or the draft row of position j - maxpos - 1.
+constexpr int kSegElems = 16384;
+constexpr int kRsThreads = 256;
+constexpr int kRsUnroll = 8;
 
-template <>
-__device__ __forceinline__ void accum8<uint16_t>(uint4 v, float &m, float &s0, float &s1,
-                                                 float k) {
-  const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
-  const float x4 = bf16_lo(v.z), x5 = bf16_hi(v.z), x6 = bf16_lo(v.w), x7 = bf16_hi(v.w);
-  const float cm = fmaxf(fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), fmaxf(fmaxf(x4, x5), fmaxf(x6, x7)));
-  if (cm > m) {
-    const float f = ex2_approx((m - cm) * k);
-    s0 *= f;
-    s1 *= f;
-    m = cm;
-  }
-  const float mm = (m == -INFINITY) ? 0.0f : m;
-  s0 += ex2_approx((x0 - mm) * k) + ex2_approx((x1 - mm) * k);
-  s1 += ex2_approx((x2 - mm) * k) + ex2_approx((x3 - mm) * k);
-  s0 += ex2_approx((x4 - mm) * k) + ex2_approx((x5 - mm) * k);
-  s1 += ex2_approx((x6 - mm) * k) + ex2_approx((x7 - mm) * k);
+// Per-thread online statistics.  mx = running max of raw logits (exact);
+// mk = fl(mx * k), the log2-domain reference of the sum; s = sum of
+// exp2(fma(x, k, -mk)) over the elements seen.  Each exponent is one fused
+// multiply-add, rounded once, and the output pair (mk, s) states the
+// reference the sum was taken against, so no rounding of mk enters q.
+struct StatState {
+  float mx, mk;
+  float s0, s1;
+};
+
+__device__ __forceinline__ void stat_raise(StatState &st, float cm, float k) {
+  // cm > st.mx: move the reference up and rescale the sums
+  const float nk = cm * k;
+  const float f = (st.mx == -INFINITY) ? 0.0f : ex2_approx(st.mk - nk);
+  st.s0 *= f;
+  st.s1 *= f;
+  st.mx = cm;
+  st.mk = nk;
 }
 
-template <>
-__device__ __forceinline__ void accum8<float>(uint4 v, float &m, float &s0, float &s1, float k) {
+// the reference used inside the exponent (a row that so far holds only -inf
+// or NaN uses 0, so -inf contributes 0 and NaN stays NaN)
+__device__ __forceinline__ float stat_ref(const StatState &st) {
+  return st.mx == -INFINITY ? 0.0f : st.mk;
+}
+
+// 8 bf16 logits in one 16-byte word
+__device__ __forceinline__ void stat8_bf16(uint4 v, StatState &st, uint32_t &mx2, float k) {
+  const uint32_t t = bf2_max(bf2_max(v.x, v.y), bf2_max(v.z, v.w));
+  if (bf2_max(t, mx2) != mx2) {  // some element above the running max (rare)
+    const float cm = fmaxf(bf16_lo(t), bf16_hi(t));
+    if (cm > st.mx) {
+      stat_raise(st, cm, k);
+      const uint32_t hb = __float_as_uint(cm) >> 16;
+      mx2 = (hb << 16) | hb;
+    }
+  }
+  const float r = stat_ref(st);
+  st.s0 += ex2_approx(fmaf(bf16_lo(v.x), k, -r));
+  st.s1 += ex2_approx(fmaf(bf16_hi(v.x), k, -r));
+  st.s0 += ex2_approx(fmaf(bf16_lo(v.y), k, -r));
+  st.s1 += ex2_approx(fmaf(bf16_hi(v.y), k, -r));
+  st.s0 += ex2_approx(fmaf(bf16_lo(v.z), k, -r));
+  st.s1 += ex2_approx(fmaf(bf16_hi(v.z), k, -r));
+  st.s0 += ex2_approx(fmaf(bf16_lo(v.w), k, -r));
+  st.s1 += ex2_approx(fmaf(bf16_hi(v.w), k, -r));
+}
+
+// 4 fp32 logits in one 16-byte word
+__device__ __forceinline__ void stat4_f32(uint4 v, StatState &st, float k) {
   const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
   const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
   const float cm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-  if (cm > m) {
-    const float f = ex2_approx((m - cm) * k);
-    s0 *= f;
-    s1 *= f;
-    m = cm;
-  }
-  const float mm = (m == -INFINITY) ? 0.0f : m;
-  s0 += ex2_approx((x0 - mm) * k) + ex2_approx((x1 - mm) * k);
-  s1 += ex2_approx((x2 - mm) * k) + ex2_approx((x3 - mm) * k);
-}
-
-// One scalar element (ragged head / tail of a segment).  Rescales both
-// partial sums when the running max moves.
-__device__ __forceinline__ void accum1(float x, float &m, float &s0, float &s1, bool to0,
-                                       float k) {
-  if (x > m) {
-    const float f = ex2_approx((m - x) * k);
-    s0 *= f;
-    s1 *= f;
-    m = x;
-  }
-  const float mm = (m == -INFINITY) ? 0.0f : m;
-  const float e = ex2_approx((x - mm) * k);
-  if (to0)
-    s0 += e;
-  else
-    s1 += e;
+  if (cm > st.mx) stat_raise(st, cm, k);
+  const float r = stat_ref(st);
+  st.s0 += ex2_approx(fmaf(x0, k, -r));
+  st.s1 += ex2_approx(fmaf(x1, k, -r));
+  st.s0 += ex2_approx(fmaf(x2, k, -r));
+  st.s1 += ex2_approx(fmaf(x3, k, -r));
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kStatsThreads)
-row_stats_kernel(Round r, int G, int seg_len, float2 *__restrict__ partial) {
-  const int w = blockIdx.x;
-  const int slot = w / G, seg = w - slot * G;
-  const int b = slot / r.P, j = slot - b * r.P;
-  const int npos = round_npos(r, b);
+__device__ __forceinline__ void stat_vec(uint4 v, StatState &st, uint32_t &mx2, float k);
+template <>
+__device__ __forceinline__ void stat_vec<uint16_t>(uint4 v, StatState &st, uint32_t &mx2,
+                                                   float k) {
+  stat8_bf16(v, st, mx2, k);
+}
+template <>
+__device__ __forceinline__ void stat_vec<float>(uint4 v, StatState &st, uint32_t &, float k) {
+  stat4_f32(v, st, k);
+}
+
+__device__ __forceinline__ void stat1(float x, StatState &st, uint32_t &mx2, float k) {
+  if (x > st.mx) {
+    stat_raise(st, x, k);
+    const uint32_t hb = __float_as_uint(x) >> 16;
+    mx2 = (hb << 16) | hb;
+  }
+  st.s0 += ex2_approx(fmaf(x, k, -stat_ref(st)));
+}
+
+// Merge (mx2, mk2, s2) into (mx, mk, s): log2-domain references, -inf refs
+// contribute nothing, NaN sums stay NaN.
+__device__ __forceinline__ void st_combine(float &mx, float &mk, float &s, float mx2, float mk2,
+                                           float s2) {
+  const float a = (mx == -INFINITY) ? -INFINITY : mk;
+  const float b = (mx2 == -INFINITY) ? -INFINITY : mk2;
+  const float M = fmaxf(a, b);
+  if (M == -INFINITY) {
+    s = s + s2;
+  } else {
+    s = s * ex2_approx(a - M) + s2 * ex2_approx(b - M);
+  }
+  mx = fmaxf(mx, mx2);
+  mk = M;
+}
+
+// Row slot of active row `a` of sequence b (tree: a <= npos verifier, then draft)
+__device__ __forceinline__ int slot_of_active(int a, int npos, int maxpos) {
+  return a <= npos ? a : maxpos + 1 + (a - npos - 1);
+}
+
+struct SegInfo {
+  const char *row;   // row base
+  int v0, v1;        // element range of the segment
+  uintptr_t ab, ae;  // 16-byte-aligned body [ab, ae)
+  size_t out;        // partial index
+};
+
+template <typename E>
+__device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t *rowlist,
+                                            long u) {
+  const long row_i = u / G;
+  const int seg = (int)(u - row_i * G);
+  int b, j;
+  if (rowlist) {
+    const int e = rowlist[row_i];
+    b = e >> 12;
+    j = slot_of_active(e & 0xfff, round_npos(r, b), r.maxpos);
+  } else {
+    b = (int)(row_i / r.P);
+    j = (int)(row_i - (long)b * r.P);
+  }
   const bool is_v = j <= r.maxpos;
   const int i = is_v ? j : j - r.maxpos - 1;
-  if (is_v ? (i > npos) : (i >= npos)) return;
   const int node = round_node(r, b, i);
+  SegInfo si;
   const E *row = (const E *)(is_v ? r.vlog : r.dlog) +
                  ((size_t)b * (is_v ? r.v_rows : r.d_rows) + node) * (size_t)r.V;
-  const int v0 = seg * seg_len;
-  const int v1 = min(r.V, v0 + seg_len);
+  si.row = (const char *)row;
+  si.v0 = seg * kSegElems;
+  si.v1 = min(r.V, si.v0 + kSegElems);
+  const uintptr_t pb = (uintptr_t)(row + si.v0), pe = (uintptr_t)(row + si.v1);
+  si.ab = (pb + 15) & ~(uintptr_t)15;
+  si.ae = pe & ~(uintptr_t)15;
+  if (si.ab > si.ae) si.ab = si.ae = pe;
+  si.out = ((size_t)b * r.P + j) * G + seg;
+  return si;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kRsThreads)
+row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+                 const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+  const long u = blockIdx.x;
+  if (rowlist && u >= (long)*rowcount * G) return;  // beyond the tree's active rows
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const SegInfo si = seg_info<E>(r, G, rowlist, u);
+  const E *row = (const E *)si.row;
   const float k = r.k;
-
-  float m = -INFINITY, s0 = 0.0f, s1 = 0.0f;
-  const uintptr_t pb = (uintptr_t)(row + v0), pe = (uintptr_t)(row + v1);
-  uintptr_t ab = (pb + 15) & ~(uintptr_t)15, ae = pe & ~(uintptr_t)15;
-  if (ab > ae) ab = ae = pe;
-  const int nhead = (int)((ab - pb) / sizeof(E));
-  const int ntail = (int)((pe - ae) / sizeof(E));
-  const int tid = threadIdx.x;
-  if (tid < nhead) accum1(load_elem<E>(row + v0 + tid), m, s0, s1, true, k);
-  if (tid < ntail) accum1(load_elem<E>((const E *)ae + tid), m, s0, s1, false, k);
-  const uint4 *body = (const uint4 *)ab;
-  const long nvec = (long)((ae - ab) / 16);
-  long vi = tid;
-  for (; vi + 3L * kStatsThreads < nvec; vi += 4L * kStatsThreads) {
-    const uint4 a0 = ld_stream_v4(body + vi);
-    const uint4 a1 = ld_stream_v4(body + vi + kStatsThreads);
-    const uint4 a2 = ld_stream_v4(body + vi + 2 * kStatsThreads);
-    const uint4 a3 = ld_stream_v4(body + vi + 3 * kStatsThreads);
-    accum8<E>(a0, m, s0, s1, k);
-    accum8<E>(a1, m, s0, s1, k);
-    accum8<E>(a2, m, s0, s1, k);
-    accum8<E>(a3, m, s0, s1, k);
+  StatState st{-INFINITY, 0.0f, 0.0f, 0.0f};
+  uint32_t mx2 = 0xff80ff80u;  // (-inf, -inf) as bf16x2
+  const int nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
+  const int ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
+  if (tid < nhead) stat1(load_elem<E>(row + si.v0 + tid), st, mx2, k);
+  if (tid < ntail) stat1(load_elem<E>((const E *)si.ae + tid), st, mx2, k);
+  const uint4 *body = (const uint4 *)si.ab;
+  const int nv = (int)((si.ae - si.ab) / 16);
+  int i = tid;
+  for (; i + (kRsUnroll - 1) * kRsThreads < nv; i += kRsUnroll * kRsThreads) {
+    uint4 buf[kRsUnroll];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) stat_vec<E>(buf[j], st, mx2, k);
   }
-  for (; vi < nvec; vi += kStatsThreads) accum8<E>(ld_stream_v4(body + vi), m, s0, s1, k);
-  float s = s0 + s1;
+  for (; i < nv; i += kRsThreads) stat_vec<E>(ld_stream_v4(body + i), st, mx2, k);
 
-  // warp, then block combine of (m, s)
+  float mx = st.mx, mk = st.mk, s = st.s0 + st.s1;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    ms_combine(m, s, m2, s2, k);
+    const float mxo = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float mko = __shfl_xor_sync(0xffffffffu, mk, o);
+    const float so = __shfl_xor_sync(0xffffffffu, s, o);
+    st_combine(mx, mk, s, mxo, mko, so);
   }
-  __shared__ float sm[kStatsThreads / 32], ss[kStatsThreads / 32];
-  const int wid = tid >> 5, lane = tid & 31;
-  if (lane == 0) {
-    sm[wid] = m;
-    ss[wid] = s;
-  }
+  __shared__ float4 red[kRsThreads / 32];
+  if (lane == 0) red[warp] = make_float4(mx, mk, s, 0.0f);
   __syncthreads();
-  if (wid == 0) {
-    m = lane < kStatsThreads / 32 ? sm[lane] : -INFINITY;
-    s = lane < kStatsThreads / 32 ? ss[lane] : 0.0f;
+  if (warp == 0) {
+    float4 v = lane < kRsThreads / 32 ? red[lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      ms_combine(m, s, m2, s2, k);
+      const float mxo = __shfl_xor_sync(0xffffffffu, v.x, o);
+      const float mko = __shfl_xor_sync(0xffffffffu, v.y, o);
+      const float so = __shfl_xor_sync(0xffffffffu, v.z, o);
+      st_combine(v.x, v.y, v.z, mxo, mko, so);
     }
-    if (lane == 0) partial[w] = make_float2(m, s);
+    if (lane == 0) partial[si.out] = v;
   }
+}
+
+Layout plan(int B, int maxpos, int V, bool tree) {
+  Layout L;
+  L.maxpos = maxpos;
+  L.P = 2 * maxpos + 1;
+  L.G = (V + kSegElems - 1) / kSegElems;
+  const size_t nslots = (size_t)B * L.P;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.ctr = take(sizeof(int));  // active row count (tree)
+  L.rowlist = tree ? take(sizeof(int32_t) * nslots) : 0;
+  L.partial = take(sizeof(float4) * nslots * L.G);
+  L.task = take(sizeof(Task) * (size_t)B);
+  L.CS = (V + kSpSlice - 1) / kSpSlice;
+  L.norm = take(sizeof(ulonglong2) * (size_t)B * L.CS);
+  L.mass = take(sizeof(unsigned long long) * (size_t)B * L.CS);
+  L.run = take(sizeof(unsigned long long) * (size_t)B * L.CS * kSpThreads);
+  if (tree) {
+    L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
+    L.npos = take(sizeof(int32_t) * (size_t)B);
+    L.tok = take(sizeof(int32_t) * (size_t)B * (maxpos > 0 ? maxpos : 1));
+    L.tstat = take(sizeof(uint32_t) * (size_t)B);
+  } else {
+    L.path = L.npos = L.tok = L.tstat = 0;
+  }
+  L.total = off + 256;
+  return L;
 }
 
 // ---------------------------------------------------------------------------
@@ -247,44 +321,46 @@ struct DecideOut {
   int32_t *path_out;     // [B][maxpos+1] or null (tree)
 };
 
-template <typename E>
-__device__ __forceinline__ void merge_slot(const float2 *part, int G, float k, float &m,
+// Merge the G segment partials of one row: raw max mx, log2 reference mk and
+// the sum s = sum_v exp2(fma(x_v, k, -mk)).
+__device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx, float &mk,
                                            float &s) {
-  m = -INFINITY;
+  mx = -INFINITY;
+  mk = 0.0f;
   s = 0.0f;
   for (int g = 0; g < G; ++g) {
-    const float2 v = part[g];
-    ms_combine(m, s, v.x, v.y, k);
+    const float4 v = part[g];
+    st_combine(mx, mk, s, v.x, v.y, v.z);
   }
 }
 
 template <typename E>
 __global__ void __launch_bounds__(kDecideWarps * 32)
-decide_kernel(Round r, int G, const float2 *__restrict__ partial, uint64_t seed,
-              uint64_t step, DecideOut o, Task *__restrict__ tasks, Acc *__restrict__ acc) {
+decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
+              uint64_t step, DecideOut o, Task *__restrict__ tasks) {
   const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= r.B) return;
   const unsigned FULL = 0xffffffffu;
   const int npos = round_npos(r, b);
   const uint32_t tree_bad = r.tstat ? r.tstat[b] : 0u;
-  const float2 *pb = partial + (size_t)b * r.P * G;
-  const float k = r.k, invT = r.invT;
+  const float4 *pb = partial + (size_t)b * r.P * G;
+  const float k = r.k;
 
   uint32_t bad = 0, pzero_bits = 0, acc_bits = 0;
   // bonus row (verifier row of position npos) is checked by lane 0
   if (lane == 0 && !tree_bad) {
-    float m, s;
-    merge_slot<E>(pb + (size_t)npos * G, G, k, m, s);
+    float mx, mk, s;
+    merge_slot(pb + (size_t)npos * G, G, mx, mk, s);
     if (!(s > 0.0f)) bad |= SV_ROW_NAN;
   }
   const int nchunks = (npos + 31) / 32;
   for (int c = 0; c < nchunks && !tree_bad; ++c) {
     const int i = c * 32 + lane;
     if (i >= npos) break;
-    float mq, sq, mp, sp;
-    merge_slot<E>(pb + (size_t)i * G, G, k, mq, sq);
-    merge_slot<E>(pb + (size_t)(r.maxpos + 1 + i) * G, G, k, mp, sp);
+    float mxq, mkq, sq, mxp, mkp, sp;
+    merge_slot(pb + (size_t)i * G, G, mxq, mkq, sq);
+    merge_slot(pb + (size_t)(r.maxpos + 1 + i) * G, G, mxp, mkp, sp);
     if (!(sq > 0.0f) || !(sp > 0.0f)) bad |= SV_ROW_NAN;
     const int d = r.tok[(size_t)b * r.tok_stride + i];
     if (d < 0 || d >= r.V) {
@@ -295,8 +371,9 @@ decide_kernel(Round r, int G, const float2 *__restrict__ partial, uint64_t seed,
     const E *vrow = (const E *)r.vlog + ((size_t)b * r.v_rows + node) * (size_t)r.V;
     const E *drow = (const E *)r.dlog + ((size_t)b * r.d_rows + node) * (size_t)r.V;
     const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
-    const float lq = (xq - mq) * invT, lp = (xp - mp) * invT;  // log q(d) + log sq, ...
-    const float qd = expf(lq) / sq, pd = expf(lp) / sp;
+    // log2 q(d) + log2 sq and log2 p(d) + log2 sp, against the row references
+    const float lq = fmaf(xq, k, -mkq), lp = fmaf(xp, k, -mkp);
+    const float qd = exp2f(lq) / sq, pd = exp2f(lp) / sp;
     const bool p_zero = (xp == -INFINITY);
     float ratio;
     if (p_zero)
@@ -304,7 +381,7 @@ decide_kernel(Round r, int G, const float2 *__restrict__ partial, uint64_t seed,
     else if (xq == -INFINITY)
       ratio = 0.0f;
     else
-      ratio = exp2f((lq - lp) * kLog2e + (log2f(sp) - log2f(sq)));
+      ratio = exp2f((lq - lp) + (log2f(sp) - log2f(sq)));
     const float rc = fminf(ratio, 1.0f);
     const uint32_t u24 = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawAccept);
     const float u = (float)u24 * 0x1p-24f;
@@ -360,133 +437,259 @@ decide_kernel(Round r, int G, const float2 *__restrict__ partial, uint64_t seed,
     const int vi = a < npos ? a : npos;
     t.vrow = b * r.v_rows + round_node(r, b, vi);
     t.drow = a < npos ? b * r.d_rows + round_node(r, b, a) : -1;
-    float m, s;
-    merge_slot<E>(pb + (size_t)vi * G, G, k, m, s);
-    t.mq = m;
+    float mx, mk, s;
+    merge_slot(pb + (size_t)vi * G, G, mx, mk, s);
+    t.mq = mx;
     t.mp = 0.0f;
     if (a < npos) {
-      merge_slot<E>(pb + (size_t)(r.maxpos + 1 + a) * G, G, k, m, s);
-      t.mp = m;
+      merge_slot(pb + (size_t)(r.maxpos + 1 + a) * G, G, mx, mk, s);
+      t.mp = mx;
     }
     t.u24 = uniform_u24(seed, step, (uint32_t)b, (uint32_t)a, kDrawSample);
     tasks[b] = t;
-    acc[b] = Acc{0ull, 0ull, 0ull, 0ull};
   }
 }
 
 // ---------------------------------------------------------------------------
 // The sampling arithmetic (fixed sequence of IEEE fp32 operations + exact
-// 64-bit fixed point):
+// 64-bit fixed point), shared by specification with the CPU oracle:
 //   z = fl(x * invT); e = exp32_repro(fl(z - max z)); S_e = sum floor(e 2^40)
 //   inv_s = fl32(2^40 / fl64(S_e)); q = fl(e * inv_s)
 //   w = max(0, fl(q - p)) (residual) or q (bonus); W = floor(w 2^62)
 //   t = floor(u24 * sum W / 2^24); token = min{k : sum_{v<=k} W_v > t}
-template <typename E>
-__device__ __forceinline__ float e_of(const E *row, int v, float invT, float mz) {
-  return exp32_repro(__fsub_rn(__fmul_rn(load_elem<E>(row + v), invT), mz));
-}
+// Only scalar _rn intrinsics are used where a product feeds a sum, so no
+// multiply can be fused into a later add.
+//
+// Exact sums without 64-bit conversions (slow on this GPU): a value v in
+// [0, 1] splits exactly into parts on fixed grids -- a = v truncated to a
+// multiple of 2^-16 (an add rounding toward zero onto 2^7, minus 2^7), then
+// the remainder truncated to 2^-32, and so on.  Parts of up to 128 values sum
+// exactly in fp32 (each part fits 17 bits, 7 more bits of headroom); the
+// per-thread part sums become integers once and meet in uint64.  The result is
+// sum floor(v 2^40) (three parts) or sum floor(v 2^62) (four parts) exactly.
+//
+// Three kernels per round.  A CTA owns one kSpSlice-element slice of one
+// sequence's q row (and p row for a residual); thread t owns the kSpRun
+// consecutive elements [t * kSpRun, (t + 1) * kSpRun) of the slice:
+//   sample_norm  partial sums of floor(e 2^40) of the slice
+//   sample_mass  S_e from the partials, then W of every element; the sum of
+//                each thread's run is stored (the prefix search's blocks)
+//   sample_pick  one warp per sequence: the threshold, the slice, the run,
+//                then a warp scan of the run's 32 elements
 
+struct Parts40 {
+  float a, b, c;  // multiples of 2^-16, 2^-32, 2^-40
+};
+struct Parts62 {
+  float a, b, c, d;  // multiples of 2^-16, 2^-32, 2^-48, 2^-62
+};
+__device__ __forceinline__ float trunc_to(float v, float grid_top) {
+  // v truncated to the grid of spacing ulp(grid_top) (v < grid_top)
+  return __fsub_rn(__fadd_rz(v, grid_top), grid_top);
+}
+__device__ __forceinline__ void add40(Parts40 &P, float e) {
+  const float a = trunc_to(e, 0x1p7f);
+  const float r1 = __fsub_rn(e, a);
+  const float b = trunc_to(r1, 0x1p-9f);
+  const float r2 = __fsub_rn(r1, b);
+  const float c = trunc_to(r2, 0x1p-17f);
+  P.a = __fadd_rn(P.a, a);
+  P.b = __fadd_rn(P.b, b);
+  P.c = __fadd_rn(P.c, c);
+}
+__device__ __forceinline__ unsigned long long fix_of(const Parts40 &P) {
+  return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 24) +
+         (unsigned long long)__float2uint_rn(__fmul_rn(P.b, 0x1p32f)) * (1ull << 8) +
+         (unsigned long long)__float2uint_rn(__fmul_rn(P.c, 0x1p40f));
+}
+__device__ __forceinline__ void add62(Parts62 &P, float w) {
+  const float a = trunc_to(w, 0x1p7f);
+  const float r1 = __fsub_rn(w, a);
+  const float b = trunc_to(r1, 0x1p-9f);
+  const float r2 = __fsub_rn(r1, b);
+  const float c = trunc_to(r2, 0x1p-25f);
+  const float r3 = __fsub_rn(r2, c);
+  const float d = trunc_to(r3, 0x1p-39f);
+  P.a = __fadd_rn(P.a, a);
+  P.b = __fadd_rn(P.b, b);
+  P.c = __fadd_rn(P.c, c);
+  P.d = __fadd_rn(P.d, d);
+}
+__device__ __forceinline__ unsigned long long fix_of(const Parts62 &P) {
+  return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 46) +
+         (unsigned long long)__float2uint_rn(__fmul_rn(P.b, 0x1p32f)) * (1ull << 30) +
+         (unsigned long long)__float2uint_rn(__fmul_rn(P.c, 0x1p48f)) * (1ull << 14) +
+         (unsigned long long)__float2uint_rn(__fmul_rn(P.d, 0x1p62f));
+}
+// single values (the final scan only)
+__device__ __forceinline__ unsigned long long fix62(float w) {
+  return __float2ull_rz(__fmul_rn(w, 0x1p62f));
+}
 __device__ __forceinline__ float inv_sum(unsigned long long se) {
   return __double2float_rn(__ddiv_rn(0x1p40, __ull2double_rn(se)));
 }
 
-__device__ __forceinline__ unsigned long long fix40(float e) {
-  return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+// The logits of elements [v, v + kSpRun) as fp32 (0 past V).
+template <typename E>
+__device__ __forceinline__ void load_run(const E *row, int v, int V, bool vec,
+                                         float x[kSpRun]);
+template <>
+__device__ __forceinline__ void load_run<uint16_t>(const uint16_t *row, int v, int V, bool vec,
+                                                   float x[kSpRun]) {
+  if (vec && v + kSpRun <= V) {
+    const uint4 *p = (const uint4 *)(row + v);
+#pragma unroll
+    for (int j = 0; j < kSpRun / 8; ++j) {
+      const uint4 w = __ldg(p + j);
+      x[8 * j + 0] = bf16_lo(w.x);
+      x[8 * j + 1] = bf16_hi(w.x);
+      x[8 * j + 2] = bf16_lo(w.y);
+      x[8 * j + 3] = bf16_hi(w.y);
+      x[8 * j + 4] = bf16_lo(w.z);
+      x[8 * j + 5] = bf16_hi(w.z);
+      x[8 * j + 6] = bf16_lo(w.w);
+      x[8 * j + 7] = bf16_hi(w.w);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < kSpRun; ++j) x[j] = (v + j < V) ? load_elem<uint16_t>(row + v + j) : 0.0f;
 }
-__device__ __forceinline__ unsigned long long fix62(float w) {
-  return __float2ull_rz(__fmul_rn(w, 0x1p62f));
+template <>
+__device__ __forceinline__ void load_run<float>(const float *row, int v, int V, bool vec,
+                                                float x[kSpRun]) {
+  if (vec && v + kSpRun <= V) {
+    const float4 *p = (const float4 *)(row + v);
+#pragma unroll
+    for (int j = 0; j < kSpRun / 4; ++j) {
+      const float4 f = __ldg(p + j);
+      x[4 * j + 0] = f.x;
+      x[4 * j + 1] = f.y;
+      x[4 * j + 2] = f.z;
+      x[4 * j + 3] = f.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < kSpRun; ++j) x[j] = (v + j < V) ? __ldg(row + v + j) : 0.0f;
 }
 
-template <typename T>
-__device__ __forceinline__ T block_sum(T v, T *red) {
-  v = (T)warp_sum_u64((unsigned long long)v);
-  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ float e1(float x, float invT, float mz, bool unit_t) {
+  const float z = unit_t ? x : __fmul_rn(x, invT);
+  return exp32_repro(__fsub_rn(z, mz));
+}
+
+struct SampleWs {
+  ulonglong2 *norm;          // [B][CS] partial (sum floor(e_q 2^40), sum floor(e_p 2^40))
+  unsigned long long *mass;  // [B][CS] slice sum W
+  unsigned long long *run;   // [B][CS][kSpThreads] run sums of W
+  int CS;                    // slices per row
+};
+
+struct RowPair {
+  const void *rq, *rp;
+  float mzq, mzp;
+  bool resid, vec, unit_t;
+};
+
+template <typename E>
+__device__ __forceinline__ RowPair row_pair(const Round &r, const Task &t) {
+  RowPair p;
+  p.resid = t.drow >= 0;
+  const E *rq = (const E *)r.vlog + (size_t)t.vrow * r.V;
+  const E *rp = p.resid ? (const E *)r.dlog + (size_t)t.drow * r.V : rq;
+  p.rq = rq;
+  p.rp = rp;
+  p.mzq = __fmul_rn(t.mq, r.invT);
+  p.mzp = __fmul_rn(t.mp, r.invT);
+  p.vec = ((((uintptr_t)rq) | ((uintptr_t)rp)) & 15) == 0;
+  p.unit_t = r.invT == 1.0f;
+  return p;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
+                                                            unsigned long long *red) {
+  v = warp_sum_u64(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (lane == 0) red[wid] = v;
-  __syncthreads();
-  T tot = 0;
+  unsigned long long tot = 0;
   if (threadIdx.x == 0)
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+    for (int i = 0; i < kSpWarps; ++i) tot += red[i];
+  __syncthreads();
   return tot;  // valid on thread 0
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSampleThreads)
-sample_sum_kernel(Round r, const Task *__restrict__ tasks, Acc *__restrict__ acc) {
-  const int b = blockIdx.x, g = blockIdx.y;
+__global__ void __launch_bounds__(kSpThreads)
+sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
+  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
   const Task t = tasks[b];
   if (!t.active) return;
-  const int v0 = g * kChunk * kChunksPerSeg;
-  const int v1 = min(r.V, v0 + kChunk * kChunksPerSeg);
-  const E *rq = (const E *)r.vlog + (size_t)t.vrow * r.V;
-  const float mzq = __fmul_rn(t.mq, r.invT);
-  unsigned long long sq = 0, sp = 0;
-  for (int v = v0 + threadIdx.x; v < v1; v += kSampleThreads) sq += fix40(e_of(rq, v, r.invT, mzq));
-  if (t.drow >= 0) {
-    const E *rp = (const E *)r.dlog + (size_t)t.drow * r.V;
-    const float mzp = __fmul_rn(t.mp, r.invT);
-    for (int v = v0 + threadIdx.x; v < v1; v += kSampleThreads) sp += fix40(e_of(rp, v, r.invT, mzp));
+  const RowPair p = row_pair<E>(r, t);
+  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
+  float x[kSpRun];
+  Parts40 Pq{0.0f, 0.0f, 0.0f}, Pp{0.0f, 0.0f, 0.0f};
+  load_run<E>((const E *)p.rq, v, r.V, p.vec, x);
+#pragma unroll
+  for (int j = 0; j < kSpRun; ++j)
+    if (v + j < r.V) add40(Pq, e1(x[j], r.invT, p.mzq, p.unit_t));
+  if (p.resid) {
+    load_run<E>((const E *)p.rp, v, r.V, p.vec, x);
+#pragma unroll
+    for (int j = 0; j < kSpRun; ++j)
+      if (v + j < r.V) add40(Pp, e1(x[j], r.invT, p.mzp, p.unit_t));
   }
-  __shared__ unsigned long long red[kSampleThreads / 32];
-  sq = block_sum(sq, red);
-  if (threadIdx.x == 0) atomicAdd(&acc[b].se_q, sq);
-  if (t.drow >= 0) {
-    sp = block_sum(sp, red);
-    if (threadIdx.x == 0) atomicAdd(&acc[b].se_p, sp);
+  __shared__ unsigned long long red[kSpWarps];
+  const unsigned long long sq = block_sum_u64(fix_of(Pq), red);
+  const unsigned long long sp = block_sum_u64(fix_of(Pp), red);
+  if (threadIdx.x == 0) sw.norm[blockIdx.x] = make_ulonglong2(sq, sp);
+}
+
+// S_e of the q and p rows of sequence b -> 1 / sum, by one thread
+__device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, float &iq,
+                                         float &ip) {
+  unsigned long long Sq = 0, Sp = 0;
+  for (int c = 0; c < sw.CS; ++c) {
+    const ulonglong2 n = sw.norm[(size_t)b * sw.CS + c];
+    Sq += n.x;
+    Sp += n.y;
   }
+  iq = inv_sum(Sq);
+  ip = resid ? inv_sum(Sp) : 0.0f;
 }
 
 template <typename E>
-__device__ __forceinline__ void wmass(const Round &r, const E *rq, const E *rp, int v, float mzq,
-                                      float iq, float mzp, float ip, unsigned long long &W,
-                                      unsigned long long &Wq) {
-  const float q = __fmul_rn(e_of(rq, v, r.invT, mzq), iq);
-  Wq = fix62(q);
-  if (rp) {
-    const float p = __fmul_rn(e_of(rp, v, r.invT, mzp), ip);
-    const float d = __fsub_rn(q, p);
-    W = fix62(d > 0.0f ? d : 0.0f);
-  } else {
-    W = Wq;
-  }
-}
-
-template <typename E>
-__global__ void __launch_bounds__(kSampleThreads)
-sample_chunk_kernel(Round r, const Task *__restrict__ tasks, Acc *__restrict__ acc,
-                    ulonglong2 *__restrict__ chunks, int nchunk) {
-  const int b = blockIdx.x, g = blockIdx.y;
+__global__ void __launch_bounds__(kSpThreads)
+sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
+  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
   const Task t = tasks[b];
   if (!t.active) return;
-  const E *rq = (const E *)r.vlog + (size_t)t.vrow * r.V;
-  const E *rp = t.drow >= 0 ? (const E *)r.dlog + (size_t)t.drow * r.V : nullptr;
-  const float mzq = __fmul_rn(t.mq, r.invT), iq = inv_sum(acc[b].se_q);
-  const float mzp = rp ? __fmul_rn(t.mp, r.invT) : 0.0f;
-  const float ip = rp ? inv_sum(acc[b].se_p) : 0.0f;
-  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long tw = 0, tq = 0;
-  for (int c = g * kChunksPerSeg + wid; c < min(nchunk, (g + 1) * kChunksPerSeg);
-       c += kSampleThreads / 32) {
-    const int v0 = c * kChunk, v1 = min(r.V, v0 + kChunk);
-    unsigned long long sw = 0, sq = 0;
-    for (int v = v0 + lane; v < v1; v += 32) {
-      unsigned long long W, Wq;
-      wmass(r, rq, rp, v, mzq, iq, mzp, ip, W, Wq);
-      sw += W;
-      sq += Wq;
+  const RowPair p = row_pair<E>(r, t);
+  __shared__ float s_inv[2];
+  if (threadIdx.x == 0) inv_sums(sw, b, p.resid, s_inv[0], s_inv[1]);
+  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
+  float xq[kSpRun], xp[kSpRun];
+  load_run<E>((const E *)p.rq, v, r.V, p.vec, xq);
+  if (p.resid) load_run<E>((const E *)p.rp, v, r.V, p.vec, xp);
+  __syncthreads();
+  const float iq = s_inv[0], ip = s_inv[1];
+  Parts62 P{0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int j = 0; j < kSpRun; ++j) {
+    if (v + j >= r.V) continue;
+    const float q = __fmul_rn(e1(xq[j], r.invT, p.mzq, p.unit_t), iq);
+    float w = q;
+    if (p.resid) {
+      const float d = __fsub_rn(q, __fmul_rn(e1(xp[j], r.invT, p.mzp, p.unit_t), ip));
+      w = d > 0.0f ? d : 0.0f;
     }
-    sw = warp_sum_u64(sw);
-    sq = warp_sum_u64(sq);
-    if (lane == 0) {
-      chunks[(size_t)b * nchunk + c] = make_ulonglong2(sw, sq);
-      tw += sw;
-      tq += sq;
-    }
+    add62(P, w);
   }
-  if (lane == 0) {
-    atomicAdd(&acc[b].sw, tw);
-    atomicAdd(&acc[b].sq, tq);
-  }
+  const unsigned long long mine = fix_of(P);
+  sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
+  __shared__ unsigned long long red[kSpWarps];
+  const unsigned long long tot = block_sum_u64(mine, red);
+  if (threadIdx.x == 0) sw.mass[blockIdx.x] = tot;
 }
 
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
@@ -499,82 +702,99 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return v;
 }
 
-template <typename E>
-__global__ void __launch_bounds__(32)
-sample_pick_kernel(Round r, const Task *__restrict__ tasks, const Acc *__restrict__ acc,
-                   const ulonglong2 *__restrict__ chunks, int nchunk, DecideOut o) {
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const Task t = tasks[b];
-  if (!t.active) return;
-  const Acc A = acc[b];
-  const bool resid = t.drow >= 0;
-  bool use_q = !resid;
-  unsigned long long S = resid ? A.sw : A.sq;
-  bool rz = false;
-  if (resid && S == 0ull) {
-    S = A.sq;
-    use_q = true;
-    rz = true;
-  }
-  const unsigned long long hi = __umul64hi((unsigned long long)t.u24, S);
-  const unsigned long long lo = (unsigned long long)t.u24 * S;
-  const unsigned long long thr = (hi << 40) | (lo >> 24);
-
-  // chunk search
-  unsigned long long base = 0;
-  int cfound = -1;
-  for (int c0 = 0; c0 < nchunk && cfound < 0; c0 += 32) {
-    const int c = c0 + lane;
-    unsigned long long v = 0;
-    if (c < nchunk) {
-      const ulonglong2 cv = chunks[(size_t)b * nchunk + c];
-      v = use_q ? cv.y : cv.x;
-    }
+// first index i in [0, n) where the running sum of get(i) exceeds thr;
+// `base` gets the sum before it.  One warp, uniform result.
+template <typename F>
+__device__ __forceinline__ int warp_find(int n, unsigned long long thr, F get,
+                                         unsigned long long &base) {
+  base = 0;
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const int c = c0 + (threadIdx.x & 31);
+    const unsigned long long v = c < n ? get(c) : 0ull;
     const unsigned long long inc = warp_incl_scan_u64(v) + base;
-    const unsigned hit = __ballot_sync(0xffffffffu, c < nchunk && inc > thr);
+    const unsigned hit = __ballot_sync(0xffffffffu, c < n && inc > thr);
     if (hit) {
       const int l = __ffs(hit) - 1;
-      cfound = c0 + l;
       base = __shfl_sync(0xffffffffu, inc - v, l);
-    } else {
-      base = __shfl_sync(0xffffffffu, inc, 31);
-    }
-  }
-  if (cfound < 0) cfound = nchunk - 1;  // unreachable: thr < S
-  // token search inside the chunk
-  const E *rq = (const E *)r.vlog + (size_t)t.vrow * r.V;
-  const E *rp = resid ? (const E *)r.dlog + (size_t)t.drow * r.V : nullptr;
-  const float mzq = __fmul_rn(t.mq, r.invT), iq = inv_sum(A.se_q);
-  const float mzp = rp ? __fmul_rn(t.mp, r.invT) : 0.0f;
-  const float ip = rp ? inv_sum(A.se_p) : 0.0f;
-  const int v0 = cfound * kChunk, v1 = min(r.V, v0 + kChunk);
-  int token = -1;
-  unsigned long long below = 0, above = 0;
-  for (int vb = v0; vb < v1; vb += 32) {
-    const int v = vb + lane;
-    unsigned long long W = 0, Wq = 0;
-    if (v < v1) wmass(r, rq, rp, v, mzq, iq, mzp, ip, W, Wq);
-    const unsigned long long w = use_q ? Wq : W;
-    const unsigned long long inc = warp_incl_scan_u64(w) + base;
-    const unsigned hit = __ballot_sync(0xffffffffu, v < v1 && inc > thr);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      token = vb + l;
-      const unsigned long long c_hi = __shfl_sync(0xffffffffu, inc, l);
-      const unsigned long long c_lo = __shfl_sync(0xffffffffu, inc - w, l);
-      below = thr - c_lo;
-      above = c_hi - 1ull - thr;
-      break;
+      return c0 + l;
     }
     base = __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (lane == 0) {
-    const int W = r.maxpos + 1;
-    o.tokens[(size_t)b * W + t.a] = token;
+  return n - 1;  // not reached when thr < total
+}
+
+// W (or the q mass) of one element
+template <typename E>
+__device__ __forceinline__ unsigned long long w_elem(const Round &r, const RowPair &p, int v,
+                                                     float iq, float ip, bool use_q) {
+  if (v >= r.V) return 0ull;
+  const float q = __fmul_rn(e1(load_elem<E>((const E *)p.rq + v), r.invT, p.mzq, p.unit_t), iq);
+  if (use_q) return fix62(q);
+  const float d = __fsub_rn(
+      q, __fmul_rn(e1(load_elem<E>((const E *)p.rp + v), r.invT, p.mzp, p.unit_t), ip));
+  return fix62(d > 0.0f ? d : 0.0f);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(32)
+sample_pick_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const Task t = tasks[b];
+  if (!t.active) return;
+  const RowPair p = row_pair<E>(r, t);
+  float iq, ip;
+  inv_sums(sw, b, p.resid, iq, ip);
+  const unsigned long long *mass = sw.mass + (size_t)b * sw.CS;
+  unsigned long long Sw = 0;
+  for (int c = 0; c < sw.CS; ++c) Sw += mass[c];
+  // residual mass 0 (q == p to the last bit): fall back to q; its masses are
+  // recomputed here (a warp per slice / run), which only this case needs
+  const bool use_q = !p.resid || Sw == 0ull;
+  const bool fallback = p.resid && use_q;
+  auto run_mass = [&](int c, int th) -> unsigned long long {  // one lane, one run
+    unsigned long long m = 0;
+    const int v0 = c * kSpSlice + kSpRun * th;
+    for (int j = 0; j < kSpRun; ++j) m += w_elem<E>(r, p, v0 + j, iq, ip, true);
+    return m;
+  };
+  auto slice_mass = [&](int c) -> unsigned long long {  // one lane, one slice
+    unsigned long long m = 0;
+    for (int th = 0; th < kSpThreads; ++th) m += run_mass(c, th);
+    return m;
+  };
+  unsigned long long S = Sw;
+  if (fallback) {
+    S = 0;
+    for (int c0 = 0; c0 < sw.CS; c0 += 32) {
+      const unsigned long long m = (c0 + lane < sw.CS) ? slice_mass(c0 + lane) : 0ull;
+      S += warp_sum_u64(m);
+    }
+  }
+  const unsigned long long thr =
+      (__umul64hi((unsigned long long)t.u24, S) << 40) | (((unsigned long long)t.u24 * S) >> 24);
+  unsigned long long base_s, base_r;
+  const int cs = warp_find(sw.CS, thr, [&](int c) { return fallback ? slice_mass(c) : mass[c]; },
+                           base_s);
+  const unsigned long long *run = sw.run + ((size_t)b * sw.CS + cs) * kSpThreads;
+  const unsigned long long tl = thr - base_s;
+  const int ri = warp_find(kSpThreads, tl,
+                           [&](int th) { return fallback ? run_mass(cs, th) : run[th]; }, base_r);
+  // the run's 32 elements, one per lane
+  const int v = cs * kSpSlice + kSpRun * ri + lane;
+  const unsigned long long w = w_elem<E>(r, p, v, iq, ip, use_q);
+  const unsigned long long tb = tl - base_r;
+  const unsigned long long inc = warp_incl_scan_u64(w);
+  const unsigned hit = __ballot_sync(0xffffffffu, inc > tb);
+  const int l = __ffs(hit) - 1;
+  if (lane == l) {
+    const unsigned long long c = inc - w;
+    const unsigned long long b_lo = tb - c, b_hi = c + w - 1ull - tb;
+    const int Wd = r.maxpos + 1;
+    o.tokens[(size_t)b * Wd + t.a] = v;
     if (o.margin)
-      o.margin[(size_t)b * W + r.maxpos] =
-          (float)((double)(below < above ? below : above) / (double)S);
-    if (rz) o.status[b] |= SV_ROW_RESID_ZERO;
+      o.margin[(size_t)b * Wd + r.maxpos] =
+          (float)((double)(b_lo < b_hi ? b_lo : b_hi) / (double)S);
+    if (fallback) o.status[b] |= SV_ROW_RESID_ZERO;
   }
 }
 
@@ -585,7 +805,8 @@ __global__ void __launch_bounds__(32)
 tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__ token,
                  const float *__restrict__ score, int B, int T, int max_depth,
                  int32_t *__restrict__ path, int32_t *__restrict__ npos,
-                 int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat) {
+                 int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
+                 int32_t *__restrict__ rowlist, int *__restrict__ rowcount) {
   const int b = blockIdx.x, lane = threadIdx.x;
   const int32_t *pa = parent + (size_t)b * T;
   const float *sc = score + (size_t)b * T;
@@ -607,6 +828,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
       pth[0] = 0;
       npos[b] = 0;
       tstat[b] = SV_ROW_BAD_TREE;
+      rowlist[atomicAdd(rowcount, 1)] = b << 12;  // the root row only
     }
     return;
   }
@@ -644,47 +866,57 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
       tok[(size_t)b * tok_stride + D - 1] = token[(size_t)b * T + bi];
     }
   }
+  int base = 0;
   if (lane == 0) {
     npos[b] = D;
     tstat[b] = 0u;
+    base = atomicAdd(rowcount, 2 * D + 1);
   }
+  base = __shfl_sync(0xffffffffu, base, 0);
+  for (int a = lane; a < 2 * D + 1; a += 32) rowlist[base + a] = (b << 12) | a;
 }
 
 // ---------------------------------------------------------------------------
 template <typename E>
 sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, uint64_t step,
                      const DecideOut &o, cudaStream_t st) {
-  float2 *partial = (float2 *)(ws + L.partial);
+  float4 *partial = (float4 *)(ws + L.partial);
   Task *tasks = (Task *)(ws + L.task);
-  Acc *acc = (Acc *)(ws + L.acc);
-  ulonglong2 *chunks = (ulonglong2 *)(ws + L.chunks);
   sv_status s;
   {
-    const long nitems = (long)r.B * r.P * L.G;
+    const long units = (long)r.B * r.P * L.G;  // tree: an upper bound, extra CTAs exit
+    const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
     LaunchScope ls("row_stats", st);
-    row_stats_kernel<E><<<(unsigned)nitems, kStatsThreads, 0, st>>>(r, L.G, L.seg_len, partial);
+    row_stats_kernel<E><<<(unsigned)units, kRsThreads, 0, st>>>(r, L.G, rowlist,
+                                                                (const int *)(ws + L.ctr),
+                                                                partial);
     if ((s = check_launch("row_stats")) != SV_OK) return s;
   }
   {
     LaunchScope ls("decide", st);
     decide_kernel<E><<<(r.B + kDecideWarps - 1) / kDecideWarps, kDecideWarps * 32, 0, st>>>(
-        r, L.G, partial, seed, step, o, tasks, acc);
+        r, L.G, partial, seed, step, o, tasks);
     if ((s = check_launch("decide")) != SV_OK) return s;
   }
+  SampleWs sw;
+  sw.norm = (ulonglong2 *)(ws + L.norm);
+  sw.mass = (unsigned long long *)(ws + L.mass);
+  sw.run = (unsigned long long *)(ws + L.run);
+  sw.CS = L.CS;
+  const unsigned grid = (unsigned)((long)r.B * L.CS);
   {
-    LaunchScope ls("sample_sum", st);
-    sample_sum_kernel<E><<<dim3(r.B, L.G3), kSampleThreads, 0, st>>>(r, tasks, acc);
-    if ((s = check_launch("sample_sum")) != SV_OK) return s;
+    LaunchScope ls("sample_norm", st);
+    sample_norm_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw);
+    if ((s = check_launch("sample_norm")) != SV_OK) return s;
   }
   {
-    LaunchScope ls("sample_chunk", st);
-    sample_chunk_kernel<E><<<dim3(r.B, L.G3), kSampleThreads, 0, st>>>(r, tasks, acc, chunks,
-                                                                        L.nchunk);
-    if ((s = check_launch("sample_chunk")) != SV_OK) return s;
+    LaunchScope ls("sample_mass", st);
+    sample_mass_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw);
+    if ((s = check_launch("sample_mass")) != SV_OK) return s;
   }
   {
     LaunchScope ls("sample_pick", st);
-    sample_pick_kernel<E><<<r.B, 32, 0, st>>>(r, tasks, acc, chunks, L.nchunk, o);
+    sample_pick_kernel<E><<<r.B, 32, 0, st>>>(r, tasks, sw, o);
     if ((s = check_launch("sample_pick")) != SV_OK) return s;
   }
   return SV_OK;
@@ -778,6 +1010,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   if (T > SV_MAX_TREE_NODES) return set_error(SV_ERR_UNSUPPORTED, "T > %d", SV_MAX_TREE_NODES);
   if (max_depth < 0) return set_error(SV_ERR_INVALID_ARG, "max_depth must be >= 0");
   if (max_depth > SV_MAX_POSITIONS) return set_error(SV_ERR_UNSUPPORTED, "max_depth > %d", SV_MAX_POSITIONS);
+  if (B > (1 << 19)) return set_error(SV_ERR_UNSUPPORTED, "B > %d for trees", 1 << 19);
   if (!dlogits || !parent || !token || !score || !out_path_nodes)
     return set_error(SV_ERR_INVALID_ARG, "null pointer argument");
   const Layout L = plan(B, max_depth, V, true);
@@ -790,10 +1023,13 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   int32_t *tok = (int32_t *)(ws + L.tok);
   uint32_t *tstat = (uint32_t *)(ws + L.tstat);
   cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws + L.ctr, 0, sizeof(int), st) != cudaSuccess)
+    return check_launch("row counter reset");
   {
     LaunchScope ls("tree_path", st);
     tree_path_kernel<<<B, 32, 0, st>>>(parent, token, score, B, T, max_depth, path, npos, tok,
-                                       max_depth > 0 ? max_depth : 1, tstat);
+                                       max_depth > 0 ? max_depth : 1, tstat,
+                                       (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr));
     if ((s = check_launch("tree_path")) != SV_OK) return s;
   }
   Round r;

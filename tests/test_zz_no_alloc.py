@@ -60,7 +60,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     import speculative_decoding_verification_vocab_gb300 as sv
     lib = sv.load_library()
     cap = lib.sv_verify_chain_noalloc_max_bytes()
-    B, N, V = 4096, 7, 128256
+    B, N, V = 16384, 7, 128256
     assert lib.sv_verify_chain_workspace(B, N, V) > cap
     st = lib.sv_verify_chain_noalloc(None, None, sv.SV_BF16, None, B, N, V, 1.0, 0, 0, None,
                                      None, None, None, None, None, None)
