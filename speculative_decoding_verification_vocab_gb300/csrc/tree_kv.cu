@@ -13,7 +13,6 @@ namespace {
 
 constexpr int kMaskThreads = 256;
 constexpr int kKvThreads = 256;
-constexpr int kKvGroup = 8;  // rows loaded before any is stored
 
 // ---------------------------------------------------------------------------
 // ancestor mask: one CTA per sequence; node n walks its parent chain and sets
@@ -22,7 +21,9 @@ __global__ void __launch_bounds__(kMaskThreads)
 tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__restrict__ mask,
                  int32_t *__restrict__ depth) {
   const int b = blockIdx.x;
-  const int32_t *pa = parent + (size_t)b * T;
+  __shared__ int32_t pa[SV_MAX_TREE_NODES];
+  for (int c = threadIdx.x; c < T; c += kMaskThreads) pa[c] = parent[(size_t)b * T + c];
+  __syncthreads();
   int ok = 1;
   for (int c = threadIdx.x; c < T; c += kMaskThreads) {
     const int p = pa[c];
@@ -35,6 +36,18 @@ tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__r
   for (int n = threadIdx.x; n < T; n += kMaskThreads) {
     uint64_t *mk = mask + ((size_t)b * T + n) * W;
     const bool used = ok && pa[n] != -2;
+    if (W == 1) {  // one word: a single walk up the chain
+      uint64_t bits = 0;
+      int d = -1;
+      if (used)
+        for (int j = n; j >= 0; j = pa[j]) {
+          bits |= 1ull << j;
+          ++d;
+        }
+      mk[0] = bits;
+      depth[(size_t)b * T + n] = used ? d : -1;
+      continue;
+    }
     int d = -1;
     for (int w = 0; w < W; ++w) {
       uint64_t bits = 0;
@@ -54,14 +67,17 @@ tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__r
 
 // ---------------------------------------------------------------------------
 // KV compaction: one CTA per (sequence, group of kKvSlabs (layer, K/V) slabs).
-// Every warp validates the request on its own (no block barrier): lanes read
-// 32 row indices at a time and vote.  Then each thread owns (slab, 16-byte
-// column) units and moves the rows in groups of kKvGroup: all loads of a
-// group, then its stores, groups in increasing k.  In place, rows[k] >= k and
-// strictly increasing mean a later group never reads a slot an earlier group
-// wrote, and a group's reads precede its writes; rows[k] == k are skipped.
+// Warp 0 validates the request (lanes read 32 row indices at a time and vote)
+// and lists the rows that actually move (in place, rows[k] == k stays) in
+// shared memory, in increasing k.  Each thread then owns kUnits (slab, 16-byte
+// column) units and walks its (unit, move) pairs unit by unit, in batches of
+// kKvBatch: all loads of a batch, then its stores.  In place, rows[k] >= k and
+// strictly increasing mean a later batch never reads a slot an earlier one
+// wrote (a unit's moves go in increasing k), and a batch's reads precede its
+// writes; different threads touch different columns or slabs.
 constexpr int kKvSlabs = 8;
 constexpr int kKvMaxRows = 4096;
+constexpr int kKvBatch = 8;
 
 struct KvArgs {
   const char *src;
@@ -71,75 +87,97 @@ struct KvArgs {
   const int32_t *src_base, *dst_base, *rows, *n_rows;
   int n_add, P;
   int32_t *kv_len;
-  int inplace, vec;
+  int inplace, vec, copy;
 };
 
 __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
-  const int n = a.n_rows[b] + a.n_add;
-  const int sb = a.src_base[b], db = a.dst_base[b];
-  bool ok = n >= 0 && n <= a.P && n <= kKvMaxRows && sb >= 0 && db >= 0 &&
-            (long)db + n <= a.S_dst && !(a.inplace && sb != db);
-  const int32_t *rows = a.rows ? a.rows + (size_t)b * a.P : nullptr;
-  int prev_last = -1;
-  for (int k0 = 0; ok && k0 < n; k0 += 32) {
-    const int k = k0 + lane;
-    const bool in = k < n;
-    const int r = in ? (rows ? rows[k] : k) : 0;
-    int prev = __shfl_up_sync(FULL, r, 1);
-    if (lane == 0) prev = prev_last;
-    bool bad = in && (r < 0 || (long)sb + r >= a.S_src);
-    if (a.inplace) bad = bad || (in && (r < k || r <= prev));
-    if (__any_sync(FULL, bad)) ok = false;
-    prev_last = __shfl_sync(FULL, r, 31);
+  __shared__ int s_ok, s_nm;
+  __shared__ int s_src[kKvMaxRows], s_dst[kKvMaxRows];
+  if (threadIdx.x < 32) {
+    const int n = a.n_rows[b] + a.n_add;
+    const int sb = a.src_base[b], db = a.dst_base[b];
+    bool ok = n >= 0 && n <= a.P && n <= kKvMaxRows && sb >= 0 && db >= 0 &&
+              (long)db + n <= a.S_dst && !(a.inplace && sb != db);
+    const int32_t *rows = a.rows ? a.rows + (size_t)b * a.P : nullptr;
+    int nm = 0, prev_last = -1;
+    for (int k0 = 0; ok && k0 < n; k0 += 32) {
+      const int k = k0 + lane;
+      const bool in = k < n;
+      const int r = in ? (rows ? rows[k] : k) : 0;
+      int prev = __shfl_up_sync(FULL, r, 1);
+      if (lane == 0) prev = prev_last;
+      bool bad = in && (r < 0 || (long)sb + r >= a.S_src);
+      if (a.inplace) bad = bad || (in && (r < k || r <= prev));
+      if (__any_sync(FULL, bad)) ok = false;
+      const bool moves = in && !(a.inplace && r == k);
+      const unsigned mm = __ballot_sync(FULL, moves);
+      if (moves) {
+        const int pos = nm + __popc(mm & ((1u << lane) - 1u));
+        s_src[pos] = r;
+        s_dst[pos] = k;
+      }
+      nm += __popc(mm);
+      prev_last = __shfl_sync(FULL, r, 31);
+    }
+    if (lane == 0) {
+      s_ok = ok;
+      s_nm = nm;
+      if (blockIdx.y == 0) a.kv_len[b] = ok ? db + n : -1;
+    }
   }
-  if (blockIdx.y == 0 && threadIdx.x == 0) a.kv_len[b] = ok ? db + n : -1;
-  if (!ok || n == 0) return;
+  __syncthreads();
+  if (!s_ok || !a.copy) return;
+  const int nm = s_nm;
+  if (nm == 0) return;
   const int slab0 = blockIdx.y * kKvSlabs;
   const int nslab = min(kKvSlabs, 2 * a.L - slab0);
+  const size_t sb_off = (size_t)a.src_base[b] * a.row_bytes;
+  const size_t db_off = (size_t)a.dst_base[b] * a.row_bytes;
   const size_t ncol = a.vec ? a.row_bytes / 16 : a.row_bytes;
-  const size_t units = (size_t)nslab * ncol;
-  const size_t sbase_off = (size_t)sb * a.row_bytes, dbase_off = (size_t)db * a.row_bytes;
-  for (int k0 = 0; k0 < n; k0 += 32) {
-    // this chunk's moves: lane j holds row k0 + j
-    const int kn = min(32, n - k0);
-    const int my_r = lane < kn ? (rows ? rows[k0 + lane] : k0 + lane) : 0;
-    for (int g0 = 0; g0 < kn; g0 += kKvGroup) {
-      int rr[kKvGroup];  // warp-uniform: broadcast before the divergent unit loop
+  const long units = (long)nslab * (long)ncol;
+  const long my_units = units > threadIdx.x ? (units - 1 - threadIdx.x) / kKvThreads + 1 : 0;
+  const long items = my_units * nm;
+  long uu = 0;  // (unit, move) cursor, unit-major
+  int mv = 0;
+  for (long i0 = 0; i0 < items; i0 += kKvBatch) {
+    const char *srcp[kKvBatch];
+    char *dstp[kKvBatch];
+    const int cnt = (int)min((long)kKvBatch, items - i0);
 #pragma unroll
-      for (int j = 0; j < kKvGroup; ++j) rr[j] = __shfl_sync(FULL, my_r, (g0 + j) & 31);
-      for (size_t u = threadIdx.x; u < units; u += kKvThreads) {
-        const int sl = (int)(u / ncol);
-        const size_t c = u - (size_t)sl * ncol;
+    for (int j = 0; j < kKvBatch; ++j) {
+      if (j < cnt) {
+        const long u = threadIdx.x + uu * kKvThreads;
+        const int sl = (int)(u / (long)ncol);
+        const size_t c = (size_t)(u - (long)sl * (long)ncol);
         const size_t slab = (size_t)(slab0 + sl) * a.B + b;
-        const char *sp = a.src + slab * a.S_src * a.row_bytes + sbase_off;
-        char *dp = a.dst + slab * a.S_dst * a.row_bytes + dbase_off;
-        if (a.vec) {
-          uint4 v[kKvGroup];
-#pragma unroll
-          for (int j = 0; j < kKvGroup; ++j) {
-            const int k = k0 + g0 + j;
-            if (g0 + j < kn && !(a.inplace && rr[j] == k))
-              v[j] = ld_stream_v4(sp + (size_t)rr[j] * a.row_bytes + c * 16);
-          }
-#pragma unroll
-          for (int j = 0; j < kKvGroup; ++j) {
-            const int k = k0 + g0 + j;
-            if (g0 + j < kn && !(a.inplace && rr[j] == k))
-              *(uint4 *)(dp + (size_t)k * a.row_bytes + c * 16) = v[j];
-          }
-        } else {
-          char v[kKvGroup];
-#pragma unroll
-          for (int j = 0; j < kKvGroup; ++j)
-            if (g0 + j < kn) v[j] = sp[(size_t)rr[j] * a.row_bytes + c];
-#pragma unroll
-          for (int j = 0; j < kKvGroup; ++j)
-            if (g0 + j < kn) dp[(size_t)(k0 + g0 + j) * a.row_bytes + c] = v[j];
+        const size_t col = a.vec ? c * 16 : c;
+        srcp[j] = a.src + slab * a.S_src * a.row_bytes + sb_off + (size_t)s_src[mv] * a.row_bytes + col;
+        dstp[j] = a.dst + slab * a.S_dst * a.row_bytes + db_off + (size_t)s_dst[mv] * a.row_bytes + col;
+        if (++mv == nm) {
+          mv = 0;
+          ++uu;
         }
       }
+    }
+    if (a.vec) {
+      uint4 v[kKvBatch];
+#pragma unroll
+      for (int j = 0; j < kKvBatch; ++j)
+        if (j < cnt) v[j] = ld_stream_v4(srcp[j]);
+#pragma unroll
+      for (int j = 0; j < kKvBatch; ++j)
+        if (j < cnt) *(uint4 *)dstp[j] = v[j];
+    } else {
+      char v[kKvBatch];
+#pragma unroll
+      for (int j = 0; j < kKvBatch; ++j)
+        if (j < cnt) v[j] = *srcp[j];
+#pragma unroll
+      for (int j = 0; j < kKvBatch; ++j)
+        if (j < cnt) *dstp[j] = v[j];
     }
   }
 }
@@ -190,8 +228,12 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   a.kv_len = out_kv_len;
   a.inplace = (src_kv == dst_kv);
   a.vec = (a.row_bytes % 16 == 0) && ((uintptr_t)src_kv % 16 == 0) && ((uintptr_t)dst_kv % 16 == 0);
+  // rows == NULL in place moves no byte (every row stays): validate and set
+  // the lengths with one CTA per sequence
+  a.copy = !(rows == nullptr && a.inplace);
+  const unsigned gy = a.copy ? (unsigned)((2 * L + kKvSlabs - 1) / kKvSlabs) : 1u;
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("kv_compact", st);
-  kv_compact_kernel<<<dim3(B, (2 * L + kKvSlabs - 1) / kKvSlabs), kKvThreads, 0, st>>>(a);
+  kv_compact_kernel<<<dim3(B, gy), kKvThreads, 0, st>>>(a);
   return check_launch("kv_compact");
 }

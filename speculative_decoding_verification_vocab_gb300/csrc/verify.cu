@@ -7,9 +7,9 @@
 //                streams the whole input; HBM-bound
 //   decide       one warp per sequence: q(d)/p(d), Philox uniforms, the left-
 //                to-right accept walk, outputs, and the sampling task
-//   sample_sum   exact fixed-point normaliser of the 1-2 sampled rows
-//   sample_chunk fixed-point residual / bonus masses per 2048-token chunk
-//   sample_pick  inverse CDF: chunk search, then a warp scan in the chunk
+//   sample_norm  exact fixed-point normaliser partials of the 1-2 sampled rows
+//   sample_mass  fixed-point residual / bonus masses per slice and per run;
+//                the last slice CTA of a sequence does the inverse-CDF pick
 //
 // Pages: "Decodificação Especulativa e EAGLE-3" (lesson; "O invariante",
 // Passo 1-3) and "投机解码发展" (blog; section 2 steps, section 4 spec_decode /
@@ -44,7 +44,7 @@ struct Task {
 
 struct Layout {
   int maxpos, P, G, CS;
-  size_t ctr, rowlist, partial, task, norm, mass, run, path, npos, tok, tstat, total;
+  size_t ctr, rowlist, partial, task, norm, mass, run, done, path, npos, tok, tstat, total;
 };
 
 Layout plan(int B, int maxpos, int V, bool tree);
@@ -298,6 +298,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   L.norm = take(sizeof(ulonglong2) * (size_t)B * L.CS);
   L.mass = take(sizeof(unsigned long long) * (size_t)B * L.CS);
   L.run = take(sizeof(unsigned long long) * (size_t)B * L.CS * kSpThreads);
+  L.done = take(sizeof(unsigned) * (size_t)B);
   if (tree) {
     L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
     L.npos = take(sizeof(int32_t) * (size_t)B);
@@ -337,7 +338,8 @@ __device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx,
 template <typename E>
 __global__ void __launch_bounds__(kDecideWarps * 32)
 decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
-              uint64_t step, DecideOut o, Task *__restrict__ tasks) {
+              uint64_t step, DecideOut o, Task *__restrict__ tasks,
+              unsigned *__restrict__ done) {
   const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= r.B) return;
@@ -346,6 +348,12 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   const uint32_t tree_bad = r.tstat ? r.tstat[b] : 0u;
   const float4 *pb = partial + (size_t)b * r.P * G;
   const float k = r.k;
+  // per position: raw max of the verifier / draft row and the sample uniform,
+  // kept for the task so that lane 0 needs no further global reads
+  extern __shared__ float dsm[];
+  float *mxv = dsm + (threadIdx.x >> 5) * 3 * (r.maxpos + 1);
+  float *mxd = mxv + (r.maxpos + 1);
+  uint32_t *usm = (uint32_t *)(mxd + (r.maxpos + 1));
 
   uint32_t bad = 0, pzero_bits = 0, acc_bits = 0;
   // bonus row (verifier row of position npos) is checked by lane 0
@@ -353,21 +361,26 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     float mx, mk, s;
     merge_slot(pb + (size_t)npos * G, G, mx, mk, s);
     if (!(s > 0.0f)) bad |= SV_ROW_NAN;
+    mxv[npos] = mx;
+    usm[npos] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)npos, kDrawSample);
   }
   const int nchunks = (npos + 31) / 32;
   for (int c = 0; c < nchunks && !tree_bad; ++c) {
     const int i = c * 32 + lane;
     if (i >= npos) break;
+    const int d = r.tok[(size_t)b * r.tok_stride + i];  // issued first: x_d depends on it
+    const int node = round_node(r, b, i);
     float mxq, mkq, sq, mxp, mkp, sp;
     merge_slot(pb + (size_t)i * G, G, mxq, mkq, sq);
     merge_slot(pb + (size_t)(r.maxpos + 1 + i) * G, G, mxp, mkp, sp);
+    mxv[i] = mxq;
+    mxd[i] = mxp;
+    usm[i] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawSample);
     if (!(sq > 0.0f) || !(sp > 0.0f)) bad |= SV_ROW_NAN;
-    const int d = r.tok[(size_t)b * r.tok_stride + i];
     if (d < 0 || d >= r.V) {
       bad |= SV_ROW_BAD_TOKEN;
       continue;
     }
-    const int node = round_node(r, b, i);
     const E *vrow = (const E *)r.vlog + ((size_t)b * r.v_rows + node) * (size_t)r.V;
     const E *drow = (const E *)r.dlog + ((size_t)b * r.d_rows + node) * (size_t)r.V;
     const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
@@ -427,6 +440,7 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
       if (o.margin) o.margin[(size_t)b * W + i] = NAN;
     }
   }
+  __syncwarp();
   if (lane == 0) {
     o.accept_len[b] = a;
     o.status[b] = bad ? bad : (pz ? SV_ROW_P_ZERO : 0u);
@@ -437,16 +451,11 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     const int vi = a < npos ? a : npos;
     t.vrow = b * r.v_rows + round_node(r, b, vi);
     t.drow = a < npos ? b * r.d_rows + round_node(r, b, a) : -1;
-    float mx, mk, s;
-    merge_slot(pb + (size_t)vi * G, G, mx, mk, s);
-    t.mq = mx;
-    t.mp = 0.0f;
-    if (a < npos) {
-      merge_slot(pb + (size_t)(r.maxpos + 1 + a) * G, G, mx, mk, s);
-      t.mp = mx;
-    }
-    t.u24 = uniform_u24(seed, step, (uint32_t)b, (uint32_t)a, kDrawSample);
+    t.mq = bad ? 0.0f : mxv[vi];
+    t.mp = (!bad && a < npos) ? mxd[a] : 0.0f;
+    t.u24 = bad ? 0u : usm[vi];
     tasks[b] = t;
+    done[b] = 0u;  // the sampler's per-sequence completion count
   }
 }
 
@@ -468,14 +477,15 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
 // per-thread part sums become integers once and meet in uint64.  The result is
 // sum floor(v 2^40) (three parts) or sum floor(v 2^62) (four parts) exactly.
 //
-// Three kernels per round.  A CTA owns one kSpSlice-element slice of one
+// Two kernels per round.  A CTA owns one kSpSlice-element slice of one
 // sequence's q row (and p row for a residual); thread t owns the kSpRun
 // consecutive elements [t * kSpRun, (t + 1) * kSpRun) of the slice:
 //   sample_norm  partial sums of floor(e 2^40) of the slice
 //   sample_mass  S_e from the partials, then W of every element; the sum of
 //                each thread's run is stored (the prefix search's blocks)
-//   sample_pick  one warp per sequence: the threshold, the slice, the run,
-//                then a warp scan of the run's 32 elements
+//   (pick)       in the CTA that finishes a sequence's masses last, one warp:
+//                the threshold, the slice, the run, then a warp scan of the
+//                run's 32 elements
 
 struct Parts40 {
   float a, b, c;  // multiples of 2^-16, 2^-32, 2^-40
@@ -583,6 +593,7 @@ struct SampleWs {
   ulonglong2 *norm;          // [B][CS] partial (sum floor(e_q 2^40), sum floor(e_p 2^40))
   unsigned long long *mass;  // [B][CS] slice sum W
   unsigned long long *run;   // [B][CS][kSpThreads] run sums of W
+  unsigned *done;            // [B] slice CTAs of sample_mass finished (zeroed by decide)
   int CS;                    // slices per row
 };
 
@@ -658,40 +669,6 @@ __device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, 
   ip = resid ? inv_sum(Sp) : 0.0f;
 }
 
-template <typename E>
-__global__ void __launch_bounds__(kSpThreads)
-sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
-  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
-  const Task t = tasks[b];
-  if (!t.active) return;
-  const RowPair p = row_pair<E>(r, t);
-  __shared__ float s_inv[2];
-  if (threadIdx.x == 0) inv_sums(sw, b, p.resid, s_inv[0], s_inv[1]);
-  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
-  float xq[kSpRun], xp[kSpRun];
-  load_run<E>((const E *)p.rq, v, r.V, p.vec, xq);
-  if (p.resid) load_run<E>((const E *)p.rp, v, r.V, p.vec, xp);
-  __syncthreads();
-  const float iq = s_inv[0], ip = s_inv[1];
-  Parts62 P{0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-  for (int j = 0; j < kSpRun; ++j) {
-    if (v + j >= r.V) continue;
-    const float q = __fmul_rn(e1(xq[j], r.invT, p.mzq, p.unit_t), iq);
-    float w = q;
-    if (p.resid) {
-      const float d = __fsub_rn(q, __fmul_rn(e1(xp[j], r.invT, p.mzp, p.unit_t), ip));
-      w = d > 0.0f ? d : 0.0f;
-    }
-    add62(P, w);
-  }
-  const unsigned long long mine = fix_of(P);
-  sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
-  __shared__ unsigned long long red[kSpWarps];
-  const unsigned long long tot = block_sum_u64(mine, red);
-  if (threadIdx.x == 0) sw.mass[blockIdx.x] = tot;
-}
-
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -735,18 +712,18 @@ __device__ __forceinline__ unsigned long long w_elem(const Round &r, const RowPa
   return fix62(d > 0.0f ? d : 0.0f);
 }
 
+
+// The inverse-CDF pick of sequence b, by one warp (the last sample_mass CTA
+// of the sequence; the other CTAs' masses are read through L2).
 template <typename E>
-__global__ void __launch_bounds__(32)
-sample_pick_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
-  const int b = blockIdx.x, lane = threadIdx.x;
-  const Task t = tasks[b];
-  if (!t.active) return;
-  const RowPair p = row_pair<E>(r, t);
+__device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, const RowPair &p,
+                                              const SampleWs &sw, const DecideOut &o, int b) {
+  const int lane = threadIdx.x & 31;
   float iq, ip;
   inv_sums(sw, b, p.resid, iq, ip);
   const unsigned long long *mass = sw.mass + (size_t)b * sw.CS;
   unsigned long long Sw = 0;
-  for (int c = 0; c < sw.CS; ++c) Sw += mass[c];
+  for (int c = 0; c < sw.CS; ++c) Sw += __ldcg(mass + c);
   // residual mass 0 (q == p to the last bit): fall back to q; its masses are
   // recomputed here (a warp per slice / run), which only this case needs
   const bool use_q = !p.resid || Sw == 0ull;
@@ -773,12 +750,14 @@ sample_pick_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideO
   const unsigned long long thr =
       (__umul64hi((unsigned long long)t.u24, S) << 40) | (((unsigned long long)t.u24 * S) >> 24);
   unsigned long long base_s, base_r;
-  const int cs = warp_find(sw.CS, thr, [&](int c) { return fallback ? slice_mass(c) : mass[c]; },
+  const int cs = warp_find(sw.CS, thr,
+                           [&](int c) { return fallback ? slice_mass(c) : __ldcg(mass + c); },
                            base_s);
   const unsigned long long *run = sw.run + ((size_t)b * sw.CS + cs) * kSpThreads;
   const unsigned long long tl = thr - base_s;
   const int ri = warp_find(kSpThreads, tl,
-                           [&](int th) { return fallback ? run_mass(cs, th) : run[th]; }, base_r);
+                           [&](int th) { return fallback ? run_mass(cs, th) : __ldcg(run + th); },
+                           base_r);
   // the run's 32 elements, one per lane
   const int v = cs * kSpSlice + kSpRun * ri + lane;
   const unsigned long long w = w_elem<E>(r, p, v, iq, ip, use_q);
@@ -798,6 +777,49 @@ sample_pick_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideO
   }
 }
 
+template <typename E>
+__global__ void __launch_bounds__(kSpThreads)
+sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
+  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
+  const Task t = tasks[b];
+  if (!t.active) return;
+  const RowPair p = row_pair<E>(r, t);
+  __shared__ float s_inv[2];
+  if (threadIdx.x == 0) inv_sums(sw, b, p.resid, s_inv[0], s_inv[1]);
+  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
+  float xq[kSpRun], xp[kSpRun];
+  load_run<E>((const E *)p.rq, v, r.V, p.vec, xq);
+  if (p.resid) load_run<E>((const E *)p.rp, v, r.V, p.vec, xp);
+  __syncthreads();
+  const float iq = s_inv[0], ip = s_inv[1];
+  Parts62 P{0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int j = 0; j < kSpRun; ++j) {
+    if (v + j >= r.V) continue;
+    const float q = __fmul_rn(e1(xq[j], r.invT, p.mzq, p.unit_t), iq);
+    float w = q;
+    if (p.resid) {
+      const float d = __fsub_rn(q, __fmul_rn(e1(xp[j], r.invT, p.mzp, p.unit_t), ip));
+      w = d > 0.0f ? d : 0.0f;
+    }
+    add62(P, w);
+  }
+  const unsigned long long mine = fix_of(P);
+  sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
+  __threadfence();
+  __shared__ unsigned long long red[kSpWarps];
+  const unsigned long long tot = block_sum_u64(mine, red);
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    sw.mass[blockIdx.x] = tot;
+    __threadfence();
+    s_last = atomicAdd(sw.done + b, 1u) == (unsigned)(sw.CS - 1);
+  }
+  __syncthreads();
+  // the last slice CTA of the sequence picks the token
+  if (s_last && threadIdx.x < 32) pick_sequence<E>(r, t, p, sw, o, b);
+}
+
 // ---------------------------------------------------------------------------
 // tree_path: one warp per sequence.  Validates the tree, walks best children
 // (highest score; ties to the lower slot) at most max_depth steps.
@@ -808,8 +830,13 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
                  int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
                  int32_t *__restrict__ rowlist, int *__restrict__ rowcount) {
   const int b = blockIdx.x, lane = threadIdx.x;
-  const int32_t *pa = parent + (size_t)b * T;
-  const float *sc = score + (size_t)b * T;
+  __shared__ int32_t pa[SV_MAX_TREE_NODES];
+  __shared__ float sc[SV_MAX_TREE_NODES];
+  for (int c = lane; c < T; c += 32) {  // one coalesced pass over the tree
+    pa[c] = parent[(size_t)b * T + c];
+    sc[c] = score[(size_t)b * T + c];
+  }
+  __syncwarp();
   bool ok = true;
   for (int c = lane; c < T; c += 32) {
     const int p = pa[c];
@@ -840,10 +867,10 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     int bi = 0x7fffffff;
     for (int c = 1 + lane; c < T; c += 32) {
       if (pa[c] != cur) continue;
-      const float s = sc[c];
-      if (!have || s > bs || (s == bs && c < bi)) {
+      const float sv = sc[c];
+      if (!have || sv > bs || (sv == bs && c < bi)) {
         have = true;
-        bs = s;
+        bs = sv;
         bi = c;
       }
     }
@@ -861,11 +888,11 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     if (!have) break;
     ++D;
     cur = bi;
-    if (lane == 0) {
-      pth[D] = bi;
-      tok[(size_t)b * tok_stride + D - 1] = token[(size_t)b * T + bi];
-    }
+    if (lane == 0) pth[D] = bi;
   }
+  __syncwarp();
+  // tested tokens token[n_1..n_D], gathered in parallel
+  for (int i = lane; i < D; i += 32) tok[(size_t)b * tok_stride + i] = token[(size_t)b * T + pth[i + 1]];
   int base = 0;
   if (lane == 0) {
     npos[b] = D;
@@ -893,15 +920,22 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     if ((s = check_launch("row_stats")) != SV_OK) return s;
   }
   {
+    // per warp: raw maxima of both rows and the sample uniform per position
+    const size_t dsm = (size_t)kDecideWarps * 3 * (r.maxpos + 1) * sizeof(float);
+    if (dsm > 48 * 1024 &&
+        cudaFuncSetAttribute(decide_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)dsm) != cudaSuccess)
+      return set_error(SV_ERR_CUDA, "decide: shared memory attribute");
     LaunchScope ls("decide", st);
-    decide_kernel<E><<<(r.B + kDecideWarps - 1) / kDecideWarps, kDecideWarps * 32, 0, st>>>(
-        r, L.G, partial, seed, step, o, tasks);
+    decide_kernel<E><<<(r.B + kDecideWarps - 1) / kDecideWarps, kDecideWarps * 32, dsm, st>>>(
+        r, L.G, partial, seed, step, o, tasks, (unsigned *)(ws + L.done));
     if ((s = check_launch("decide")) != SV_OK) return s;
   }
   SampleWs sw;
   sw.norm = (ulonglong2 *)(ws + L.norm);
   sw.mass = (unsigned long long *)(ws + L.mass);
   sw.run = (unsigned long long *)(ws + L.run);
+  sw.done = (unsigned *)(ws + L.done);
   sw.CS = L.CS;
   const unsigned grid = (unsigned)((long)r.B * L.CS);
   {
@@ -911,13 +945,8 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   }
   {
     LaunchScope ls("sample_mass", st);
-    sample_mass_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw);
+    sample_mass_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw, o);
     if ((s = check_launch("sample_mass")) != SV_OK) return s;
-  }
-  {
-    LaunchScope ls("sample_pick", st);
-    sample_pick_kernel<E><<<r.B, 32, 0, st>>>(r, tasks, sw, o);
-    if ((s = check_launch("sample_pick")) != SV_OK) return s;
   }
   return SV_OK;
 }
