@@ -15,6 +15,12 @@ of the results inside the timed region); `roofline` = the row-statistics
 kernel's algorithmic bytes over its CUDA-event time against the measured HBM
 copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded sample.
 
+The timed region runs K steps with no event between launches (the library
+chains its kernels by programmatic dependent launch).  Per-kernel durations
+come from a second pass over the same K steps with an event pair around every
+launch; those events serialise the launches, so that pass reports its own
+`traced_ms_per_step` and is not the step time.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 5|3]
     python bench.py --impl reference ...      # the CPU oracle alone
 """
@@ -279,8 +285,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
+    # timed region: K steps back to back (kernels chained by programmatic
+    # dependent launch; no event between them)
     n_launch0 = sv.sv_launch_count()
-    sv.sv_trace_enable(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         torch.cuda.synchronize()
@@ -289,13 +296,24 @@ def run_ours(args):
             step(W + k, wl.rounds[k % args.pool], W + k)
         e1.record(stream)
         torch.cuda.synchronize()
-    sv.sv_trace_enable(False)
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
     launches = sv.sv_launch_count() - n_launch0
-    trace = sv.sv_trace_collect()
     ms_max = max_over_ranks(ms, world)
+    # the same K steps again with an event pair around every launch: per-kernel
+    # durations (the events serialise the launches, so this pass is slower and
+    # is not the step time)
+    sv.sv_trace_enable(True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        step(W + k, wl.rounds[k % args.pool], W + k)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sv.sv_trace_enable(False)
+    trace = sv.sv_trace_collect()
+    traced_ms = t0.elapsed_time(t1)
 
     acc = o_acc[W:].cpu().numpy()
     st = o_st[W:].cpu().numpy()
@@ -351,6 +369,7 @@ def run_ours(args):
         "alg_bytes_per_step": {"row_stats": stats_bytes / K, "kv_compact": kv_bytes / K,
                                "tree_mask": mask_bytes / K},
         "kernels": {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in trace.items()},
+        "traced_ms_per_step": traced_ms / K,
         "status_nonzero": int((st != 0).sum()),
         "gpu_launches": int(launches),
         "roofline": roofline,

@@ -13,7 +13,30 @@ namespace sv {
 // Error reporting (thread-local message) and launch bookkeeping.
 sv_status set_error(sv_status st, const char *fmt, ...);
 sv_status check_launch(const char *what);
+sv_status check_launch(const char *what, cudaError_t launched);
 int num_sms();
+
+// Every kernel of the library is launched with programmatic stream
+// serialisation allowed: the next kernel of the stream may be launched while
+// this one drains.  Each kernel therefore waits for the grids before it
+// (griddepcontrol.wait, below) before it touches global memory, so results
+// are ordered as on a plain stream while launch latency and CTA rasterisation
+// overlap the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Wraps every kernel launch: counts it and, while tracing is on, records an
 // event pair around it on the launching stream.
@@ -27,6 +50,13 @@ struct LaunchScope {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ----------------------------------------------------------------- device side
+// Start of every kernel: wait until the grids this one depends on have
+// completed and their writes are visible, then allow the stream's next grid
+// to begin launching (its CTAs wait in turn at their own start).
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 constexpr uint32_t kDrawAccept = 0u;
 constexpr uint32_t kDrawSample = 1u;
 

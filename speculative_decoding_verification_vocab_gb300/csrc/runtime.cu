@@ -28,6 +28,14 @@ sv_status check_launch(const char *what) {
   return SV_OK;
 }
 
+sv_status check_launch(const char *what, cudaError_t launched) {
+  if (launched != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky copy of a launch error
+    return set_error(SV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(launched));
+  }
+  return check_launch(what);
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;

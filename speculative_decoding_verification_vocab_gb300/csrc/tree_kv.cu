@@ -20,6 +20,7 @@ constexpr int kKvThreads = 256;
 __global__ void __launch_bounds__(kMaskThreads)
 tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__restrict__ mask,
                  int32_t *__restrict__ depth) {
+  grid_dep_sync();
   const int b = blockIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
   for (int c = threadIdx.x; c < T; c += kMaskThreads) pa[c] = parent[(size_t)b * T + c];
@@ -91,6 +92,7 @@ struct KvArgs {
 };
 
 __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
+  grid_dep_sync();
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
@@ -196,8 +198,8 @@ extern "C" sv_status sv_tree_build_mask(const int32_t *parent, int B, int T, uin
   if ((uintptr_t)out_mask % 8) return set_error(SV_ERR_INVALID_ARG, "out_mask misaligned");
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("tree_mask", st);
-  tree_mask_kernel<<<B, kMaskThreads, 0, st>>>(parent, T, (T + 63) / 64, out_mask, out_depth);
-  return check_launch("tree_mask");
+  return check_launch("tree_mask", launch_pdl(tree_mask_kernel, dim3(B), dim3(kMaskThreads), 0, st,
+                                              parent, T, (T + 63) / 64, out_mask, out_depth));
 }
 
 extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int B, int S_src,
@@ -234,6 +236,6 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   const unsigned gy = a.copy ? (unsigned)((2 * L + kKvSlabs - 1) / kKvSlabs) : 1u;
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("kv_compact", st);
-  kv_compact_kernel<<<dim3(B, gy), kKvThreads, 0, st>>>(a);
-  return check_launch("kv_compact");
+  return check_launch("kv_compact",
+                      launch_pdl(kv_compact_kernel, dim3(B, gy), dim3(kKvThreads), 0, st, a));
 }

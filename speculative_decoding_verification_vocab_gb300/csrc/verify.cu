@@ -230,6 +230,7 @@ template <typename E>
 __global__ void __launch_bounds__(kRsThreads)
 row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+  grid_dep_sync();
   const long u = blockIdx.x;
   if (rowlist && u >= (long)*rowcount * G) return;  // beyond the tree's active rows
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
 decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
               uint64_t step, DecideOut o, Task *__restrict__ tasks,
               unsigned *__restrict__ done) {
+  grid_dep_sync();
   const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= r.B) return;
@@ -633,6 +635,7 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 template <typename E>
 __global__ void __launch_bounds__(kSpThreads)
 sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
+  grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
   const Task t = tasks[b];
   if (!t.active) return;
@@ -780,6 +783,7 @@ __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, con
 template <typename E>
 __global__ void __launch_bounds__(kSpThreads)
 sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
+  grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
   const Task t = tasks[b];
   if (!t.active) return;
@@ -829,6 +833,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
                  int32_t *__restrict__ path, int32_t *__restrict__ npos,
                  int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
                  int32_t *__restrict__ rowlist, int *__restrict__ rowcount) {
+  grid_dep_sync();
   const int b = blockIdx.x, lane = threadIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
   __shared__ float sc[SV_MAX_TREE_NODES];
@@ -914,10 +919,10 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     const long units = (long)r.B * r.P * L.G;  // tree: an upper bound, extra CTAs exit
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
     LaunchScope ls("row_stats", st);
-    row_stats_kernel<E><<<(unsigned)units, kRsThreads, 0, st>>>(r, L.G, rowlist,
-                                                                (const int *)(ws + L.ctr),
-                                                                partial);
-    if ((s = check_launch("row_stats")) != SV_OK) return s;
+    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3((unsigned)units),
+                                             dim3(kRsThreads), 0, st, r, L.G, rowlist,
+                                             (const int *)(ws + L.ctr), partial));
+    if (s != SV_OK) return s;
   }
   {
     // per warp: raw maxima of both rows and the sample uniform per position
@@ -927,9 +932,11 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
                              (int)dsm) != cudaSuccess)
       return set_error(SV_ERR_CUDA, "decide: shared memory attribute");
     LaunchScope ls("decide", st);
-    decide_kernel<E><<<(r.B + kDecideWarps - 1) / kDecideWarps, kDecideWarps * 32, dsm, st>>>(
-        r, L.G, partial, seed, step, o, tasks, (unsigned *)(ws + L.done));
-    if ((s = check_launch("decide")) != SV_OK) return s;
+    s = check_launch("decide", launch_pdl(decide_kernel<E>,
+                                          dim3((r.B + kDecideWarps - 1) / kDecideWarps),
+                                          dim3(kDecideWarps * 32), dsm, st, r, L.G, partial, seed,
+                                          step, o, tasks, (unsigned *)(ws + L.done)));
+    if (s != SV_OK) return s;
   }
   SampleWs sw;
   sw.norm = (ulonglong2 *)(ws + L.norm);
@@ -940,13 +947,15 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   const unsigned grid = (unsigned)((long)r.B * L.CS);
   {
     LaunchScope ls("sample_norm", st);
-    sample_norm_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw);
-    if ((s = check_launch("sample_norm")) != SV_OK) return s;
+    s = check_launch("sample_norm", launch_pdl(sample_norm_kernel<E>, dim3(grid),
+                                               dim3(kSpThreads), 0, st, r, tasks, sw));
+    if (s != SV_OK) return s;
   }
   {
     LaunchScope ls("sample_mass", st);
-    sample_mass_kernel<E><<<grid, kSpThreads, 0, st>>>(r, tasks, sw, o);
-    if ((s = check_launch("sample_mass")) != SV_OK) return s;
+    s = check_launch("sample_mass", launch_pdl(sample_mass_kernel<E>, dim3(grid),
+                                               dim3(kSpThreads), 0, st, r, tasks, sw, o));
+    if (s != SV_OK) return s;
   }
   return SV_OK;
 }
@@ -1056,10 +1065,11 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
     return check_launch("row counter reset");
   {
     LaunchScope ls("tree_path", st);
-    tree_path_kernel<<<B, 32, 0, st>>>(parent, token, score, B, T, max_depth, path, npos, tok,
-                                       max_depth > 0 ? max_depth : 1, tstat,
-                                       (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr));
-    if ((s = check_launch("tree_path")) != SV_OK) return s;
+    s = check_launch("tree_path",
+                     launch_pdl(tree_path_kernel, dim3(B), dim3(32), 0, st, parent, token, score,
+                                B, T, max_depth, path, npos, tok, max_depth > 0 ? max_depth : 1,
+                                tstat, (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr)));
+    if (s != SV_OK) return s;
   }
   Round r;
   r.vlog = vlogits;
