@@ -69,29 +69,47 @@ def dist_env():
 
 
 def shard_batch(B, rank, world):
-    """Weak scaling: every rank runs the full per-GPU batch of B sequences;
-    sequence ids are offset so ranks draw distinct Philox streams."""
+    """Weak scaling: every rank verifies its own batch of B sequences (the
+    per-GPU batch of the workload), so the job covers world * B sequences.
+    Returns (first global sequence index of this rank, B)."""
     return rank * B, B
+
+
+def rank_seed(base, rank):
+    """Philox key of a rank: ranks draw independent uniforms (the kernel's
+    counter carries the in-batch sequence index, the key the rank)."""
+    return base + rank
+
+
+def _reduce(x, op):
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
+    return float(t.item())
 
 
 def max_over_ranks(x, world):
     if world == 1:
         return x
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    return _reduce(x, dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(x, world):
     if world == 1:
         return x
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(x, dist.ReduceOp.SUM)
+
+
+def aggregate(units, ms, world):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time.  Returns (total units, max ms, units per second)."""
+    ms_max = max_over_ranks(ms, world)
+    total = sum_over_ranks(units, world)
+    return total, ms_max, total / (ms_max / 1e3)
 
 
 def best_path_depth(parent, score, max_depth):
@@ -243,7 +261,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     sv.load_library()
     cfg = synth.CONFIGS[args.config]
-    seq0, B = shard_batch(cfg.B, rank, world)
+    _, B = shard_batch(cfg.B, rank, world)
     wl = Workload(cfg, args.pool, dev, rank)
     K, W = args.steps, args.warmup
     T, V = wl.T, wl.V
@@ -267,12 +285,12 @@ def run_ours(args):
         if wl.tree:
             sv.sv_tree_build_mask(rd["parent"], o_mask, o_depth, stream)
             sv.sv_verify_tree(rd["vq"], rd["dp"], rd["parent"], rd["token"], rd["score"], maxd,
-                              cfg.temperature, 1234 + rank, seed_step, o_path[i], o_tok[i],
+                              cfg.temperature, rank_seed(1234, rank), seed_step, o_path[i], o_tok[i],
                               o_acc[i], None, None, None, o_st[i], ws, stream)
             sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, o_path[i], o_acc[i], 1,
                              o_kv[i], stream)
         else:
-            sv.sv_verify_chain(rd["vq"], rd["dp"], rd["d"], cfg.temperature, 1234 + rank,
+            sv.sv_verify_chain(rd["vq"], rd["dp"], rd["d"], cfg.temperature, rank_seed(1234, rank),
                                seed_step, o_tok[i], o_acc[i], None, None, None, o_st[i], ws,
                                stream)
             # chain rollback: the accepted drafts' rows are already in place;
@@ -300,7 +318,6 @@ def run_ours(args):
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
     launches = sv.sv_launch_count() - n_launch0
-    ms_max = max_over_ranks(ms, world)
     # the same K steps again with an event pair around every launch: per-kernel
     # durations (the events serialise the launches, so this pass is slower and
     # is not the step time)
@@ -334,9 +351,8 @@ def run_ours(args):
     kv_bytes = kv_moved * 2 * kvb.L * 2 * wl.row_bytes
     mask_bytes = K * B * T * (4 + 8 * Wm + 4) if wl.tree else 0
     alg_bytes = stats_bytes + kv_bytes + mask_bytes
-    total_rows = sum_over_ranks(rows, world)
+    total_rows, ms_max, value = aggregate(rows, ms, world)
     total_tokens = sum_over_ranks(tokens, world)
-    value = total_rows / (ms_max / 1e3)
 
     peak, peak_kind = measured_peaks()
     rs_launches, rs_ms = trace.get("row_stats", (0, 0.0))
@@ -439,9 +455,8 @@ def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1e3)
-    ms = max_over_ranks(ms, world)
-    rows = sum_over_ranks(wl.rows_per_step() * n, world)
-    return {"value": rows / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+    rows, ms, value = aggregate(wl.rows_per_step() * n, ms, world)
+    return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n}
 
 
