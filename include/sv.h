@@ -13,10 +13,16 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every pointer argument is a DEVICE pointer owned by the caller, unless
- *    stated otherwise.  The library never allocates, frees or synchronises;
- *    scratch memory is the caller's `workspace`, sized by the matching
- *    *_workspace() query.
+ *  - Every pointer argument is owned by the caller and points to memory the
+ *    current device can address: its own device (or managed) memory, or
+ *    page-locked host memory (cudaHostAlloc / cudaHostRegister).  Host
+ *    buffers are read and written in place by the kernels over the host link
+ *    (on GB300, NVLink-C2C), so a round whose logits sit in host memory moves
+ *    only the rows it actually reads.  Pageable host memory and another
+ *    device's memory are refused with SV_ERR_INVALID_ARG before anything is
+ *    enqueued.  The library never allocates, frees or synchronises; scratch
+ *    memory is the caller's `workspace`, sized by the matching *_workspace()
+ *    query (device memory is the fast choice).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  All work is enqueued asynchronously on it.
  *  - Argument errors are detected on the host before anything is enqueued;

@@ -2,7 +2,8 @@
 
 Argument marshalling only: every step runs in the CUDA kernels behind the C
 ABI declared in ``include/sv.h``.  The ``sv_*`` functions keep the C names and
-take torch tensors (device memory) instead of raw pointers; the lower-case
+take torch tensors (device memory, or page-locked host memory that the kernels
+read in place) instead of raw pointers; the lower-case
 helpers (``verify_chain`` ...) allocate the outputs and the workspace.  There
 is no CPU fallback: if the shared library is missing, loading fails loudly.
 """
@@ -85,8 +86,8 @@ def load_library(path: str = LIB_PATH):
 def _p(t):
     if t is None:
         return None
-    if not t.is_cuda:
-        raise ValueError("sv: tensors must live in device memory")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("sv: tensors must be in device memory or page-locked host memory")
     return C.c_void_p(t.data_ptr())
 
 
@@ -205,12 +206,18 @@ def _ws(nbytes, device):
     return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
 
 
+def _out_dev(t):
+    """Outputs and workspace go to device memory: the input's device, or the
+    current device when the input sits in page-locked host memory."""
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0,
                  workspace=None, stream=None, probs=True):
     """Allocate outputs and run sv_verify_chain.  Returns a dict of tensors."""
     B, R, V = vlogits.shape
     N = R - 1
-    dev = vlogits.device
+    dev = _out_dev(vlogits)
     out = dict(
         tokens=torch.empty(B, N + 1, dtype=torch.int32, device=dev),
         accept_len=torch.empty(B, dtype=torch.int32, device=dev),
@@ -229,7 +236,7 @@ def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0
 def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1.0, seed=0,
                 step=0, workspace=None, stream=None, probs=True):
     B, T, V = vlogits.shape
-    dev = vlogits.device
+    dev = _out_dev(vlogits)
     P = max_depth + 1
     out = dict(
         path=torch.empty(B, P, dtype=torch.int32, device=dev),
@@ -250,14 +257,14 @@ def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1
 def tree_build_mask(parent, stream=None):
     B, T = parent.shape
     W = (T + 63) // 64
-    mask = torch.empty(B, T, W, dtype=torch.int64, device=parent.device)
-    depth = torch.empty(B, T, dtype=torch.int32, device=parent.device)
+    mask = torch.empty(B, T, W, dtype=torch.int64, device=_out_dev(parent))
+    depth = torch.empty(B, T, dtype=torch.int32, device=_out_dev(parent))
     sv_tree_build_mask(parent, mask, depth, stream)
     return mask, depth
 
 
 def kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add=0, stream=None):
     B = src_kv.shape[2]
-    kv_len = torch.empty(B, dtype=torch.int32, device=src_kv.device)
+    kv_len = torch.empty(B, dtype=torch.int32, device=_out_dev(src_kv))
     sv_kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add, kv_len, stream)
     return kv_len

@@ -16,6 +16,20 @@ sv_status check_launch(const char *what);
 sv_status check_launch(const char *what, cudaError_t launched);
 int num_sms();
 
+// Pointer arguments: device or managed memory of the current device is used
+// as is; page-locked host memory (cudaHostAlloc, cudaHostRegister) through its
+// device mapping, so the kernels read or write it in place over the host link;
+// pageable host memory and other devices' memory are refused with
+// SV_ERR_INVALID_ARG (a kernel would fault on them).  NULL stays NULL.
+sv_status map_ptr(const void **p, const char *what);
+template <typename T>
+sv_status map_arg(T *&p, const char *what) {
+  const void *q = p;
+  const sv_status s = map_ptr(&q, what);
+  p = (T *)q;
+  return s;
+}
+
 // Every kernel of the library is launched with programmatic stream
 // serialisation allowed: the next kernel of the stream may be launched while
 // this one drains.  Each kernel therefore waits for the grids before it

@@ -36,6 +36,37 @@ sv_status check_launch(const char *what, cudaError_t launched) {
   return check_launch(what);
 }
 
+sv_status map_ptr(const void **p, const char *what) {
+  if (!*p) return SV_OK;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, *p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(SV_ERR_INVALID_ARG, "%s: pointer not usable by CUDA (%s)", what,
+                     cudaGetErrorString(e));
+  }
+  int dev = -1;
+  cudaGetDevice(&dev);
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      if (a.device != dev)
+        return set_error(SV_ERR_INVALID_ARG, "%s: memory of device %d, current device %d", what,
+                         a.device, dev);
+      return SV_OK;
+    case cudaMemoryTypeManaged:
+      return SV_OK;
+    case cudaMemoryTypeHost:
+      if (!a.devicePointer)
+        return set_error(SV_ERR_INVALID_ARG, "%s: page-locked host memory with no device mapping",
+                         what);
+      *p = a.devicePointer;
+      return SV_OK;
+    default:
+      return set_error(SV_ERR_INVALID_ARG,
+                       "%s: pageable host memory (page-lock it or copy it to the device)", what);
+  }
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;

@@ -196,6 +196,10 @@ extern "C" sv_status sv_tree_build_mask(const int32_t *parent, int B, int T, uin
   if (B == 0) return SV_OK;
   if (!parent || !out_mask || !out_depth) return set_error(SV_ERR_INVALID_ARG, "null pointer");
   if ((uintptr_t)out_mask % 8) return set_error(SV_ERR_INVALID_ARG, "out_mask misaligned");
+  sv_status s;
+  if ((s = map_arg(parent, "parent")) != SV_OK || (s = map_arg(out_mask, "out_mask")) != SV_OK ||
+      (s = map_arg(out_depth, "out_depth")) != SV_OK)
+    return s;
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("tree_mask", st);
   return check_launch("tree_mask", launch_pdl(tree_mask_kernel, dim3(B), dim3(kMaskThreads), 0, st,
@@ -213,6 +217,12 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   if (B == 0) return SV_OK;
   if (!src_kv || !dst_kv || !src_base || !dst_base || !n_rows || !out_kv_len)
     return set_error(SV_ERR_INVALID_ARG, "null pointer");
+  sv_status s;
+  if ((s = map_arg(src_kv, "src_kv")) != SV_OK || (s = map_arg(dst_kv, "dst_kv")) != SV_OK ||
+      (s = map_arg(src_base, "src_base")) != SV_OK ||
+      (s = map_arg(dst_base, "dst_base")) != SV_OK || (s = map_arg(rows, "rows")) != SV_OK ||
+      (s = map_arg(n_rows, "n_rows")) != SV_OK || (s = map_arg(out_kv_len, "out_kv_len")) != SV_OK)
+    return s;
   KvArgs a;
   a.src = (const char *)src_kv;
   a.dst = (char *)dst_kv;

@@ -977,6 +977,21 @@ sv_status check_common(const void *vlogits, sv_dtype dt, int B, int V, float tem
   return SV_OK;
 }
 
+sv_status map_chain_args(const void *&vlogits, const void *&dlogits, const int32_t *&tokens,
+                         int32_t *&out_tokens, int32_t *&out_accept_len, float *&out_q_prob,
+                         float *&out_p_prob, float *&out_margin, uint32_t *&out_status) {
+  sv_status s;
+  if ((s = map_arg(vlogits, "vlogits")) != SV_OK || (s = map_arg(dlogits, "dlogits")) != SV_OK ||
+      (s = map_arg(tokens, "tokens")) != SV_OK || (s = map_arg(out_tokens, "out_tokens")) != SV_OK ||
+      (s = map_arg(out_accept_len, "out_accept_len")) != SV_OK ||
+      (s = map_arg(out_q_prob, "out_q_prob")) != SV_OK ||
+      (s = map_arg(out_p_prob, "out_p_prob")) != SV_OK ||
+      (s = map_arg(out_margin, "out_margin")) != SV_OK ||
+      (s = map_arg(out_status, "out_status")) != SV_OK)
+    return s;
+  return SV_OK;
+}
+
 }  // namespace
 }  // namespace sv
 
@@ -1005,6 +1020,10 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   if (workspace_bytes < L.total)
     return set_error(SV_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                      L.total);
+  if ((s = map_chain_args(vlogits, dlogits, draft_tokens, out_tokens, out_accept_len, out_q_prob,
+                          out_p_prob, out_margin, out_status)) != SV_OK ||
+      (s = map_arg(workspace, "workspace")) != SV_OK)
+    return s;
   char *ws = (char *)align_up((uintptr_t)workspace, 256);
   Round r;
   r.vlog = vlogits;
@@ -1055,6 +1074,12 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   if (workspace_bytes < L.total)
     return set_error(SV_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                      L.total);
+  if ((s = map_chain_args(vlogits, dlogits, token, out_tokens, out_accept_len, out_q_prob,
+                          out_p_prob, out_margin, out_status)) != SV_OK ||
+      (s = map_arg(parent, "parent")) != SV_OK || (s = map_arg(score, "score")) != SV_OK ||
+      (s = map_arg(out_path_nodes, "out_path_nodes")) != SV_OK ||
+      (s = map_arg(workspace, "workspace")) != SV_OK)
+    return s;
   char *ws = (char *)align_up((uintptr_t)workspace, 256);
   int32_t *path = (int32_t *)(ws + L.path);
   int32_t *npos = (int32_t *)(ws + L.npos);

@@ -370,3 +370,66 @@ def test_trace_and_launch_count():
     assert sv.sv_launch_count() - n0 == 4
     assert set(tr) == {"row_stats", "decide", "sample_norm", "sample_mass"}
     assert all(v[0] == 1 and v[1] > 0 for v in tr.values())
+
+
+# ------------------------------------------------------------ host-resident inputs
+def _same(a, b):
+    for k in a:
+        if a[k] is None:
+            continue
+        x, y = a[k].cpu(), b[k].cpu()
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                           y.view(torch.int32) if y.dtype == torch.float32 else y), k
+
+
+def test_host_resident_tree_inputs():
+    """Logits and tree arrays in page-locked host memory, read in place by the
+    kernels: results bit-identical to the same call on device copies."""
+    cfg = synth.CONFIGS[5]
+    vq, dp, parent, token, score = synth.tree_inputs(cfg, seed=21, B=12, V=5003)
+    dev_args = [x.to(DEV) for x in (vq, dp, parent, token, score)]
+    host_args = [x.pin_memory() for x in (vq, dp, parent, token, score)]
+    gd = sv.verify_tree(*dev_args, max_depth=cfg.depth, temperature=cfg.temperature, seed=5,
+                        step=2)
+    gh = sv.verify_tree(*host_args, max_depth=cfg.depth, temperature=cfg.temperature, seed=5,
+                        step=2)
+    torch.cuda.synchronize()
+    _same(gd, gh)
+    md, dd = sv.tree_build_mask(dev_args[2])
+    mh, dh = sv.tree_build_mask(host_args[2])
+    torch.cuda.synchronize()
+    assert torch.equal(md.cpu(), mh.cpu()) and torch.equal(dd.cpu(), dh.cpu())
+
+
+def test_host_resident_chain_outputs():
+    """Chain inputs and outputs both in page-locked host memory."""
+    cfg = _cfg(torch.bfloat16, sigma_noise=0.4)
+    vq, dp, d = synth.chain_inputs(cfg, seed=8, B=6, V=4097, N=5)
+    gd = sv.verify_chain(vq.to(DEV), dp.to(DEV), d.to(DEV), seed=3, step=1)
+    hv, hd, ht = vq.pin_memory(), dp.pin_memory(), d.pin_memory()
+    B, N = 6, 5
+    out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in gd.items()}
+    ws = torch.empty(sv.sv_verify_chain_workspace(B, N, 4097), dtype=torch.uint8, device=DEV)
+    sv.sv_verify_chain(hv, hd, ht, 1.0, 3, 1, out["tokens"], out["accept_len"], out["q_prob"],
+                       out["p_prob"], out["margin"], out["status"], ws)
+    torch.cuda.synchronize()
+    _same(gd, out)
+
+
+def test_pageable_host_memory_refused():
+    """A pageable host buffer is refused on the host before any launch."""
+    import ctypes as C
+    lib = sv.load_library()
+    B, N, V = 2, 1, 64
+    host = np.zeros((B, N + 1, V), np.float32)  # pageable
+    dev = lambda shape, dt: torch.zeros(shape, dtype=dt, device=DEV)
+    dl, dt_ = dev((B, N, V), torch.float32), dev((B, N), torch.int32)
+    tok, acc, st = dev((B, N + 1), torch.int32), dev((B,), torch.int32), dev((B,), torch.int32)
+    ws = dev((sv.sv_verify_chain_workspace(B, N, V),), torch.uint8)
+    n0 = sv.sv_launch_count()
+    p = lambda t: C.c_void_p(t.data_ptr())
+    rc = lib.sv_verify_chain(C.c_void_p(host.ctypes.data), p(dl), 0, p(dt_), B, N, V, 1.0, 0, 0,
+                             p(tok), p(acc), None, None, None, p(st), p(ws), ws.numel(), None)
+    assert rc == sv.SV_ERR_INVALID_ARG
+    assert "pageable" in sv.sv_last_error()
+    assert sv.sv_launch_count() == n0
