@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences the oracle times")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="per-GPU batch override (smaller cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -263,6 +265,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     sv.load_library()
     cfg = synth.CONFIGS[args.config]
+    if args.batch:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, B=args.batch)
     _, B = shard_batch(cfg.B, rank, world)
     wl = Workload(cfg, args.pool, dev, rank)
     K, W = args.steps, args.warmup

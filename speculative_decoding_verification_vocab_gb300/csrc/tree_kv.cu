@@ -89,7 +89,26 @@ struct KvArgs {
   int n_add, P;
   int32_t *kv_len;
   int inplace, vec, copy;
+  int ncol;             // units per row: 16-byte words (vec) or bytes
+  int step_sl, step_c;  // kKvThreads units = step_sl rows + step_c units
 };
+
+struct KvCursor {
+  int sl, c;  // slab (relative to the CTA's first) and column of the unit
+  int mv;     // move index
+};
+// next (unit, move) pair: the next move, or the first move of the next unit
+__device__ __forceinline__ void kv_step(KvCursor &q, int nm, int step_sl, int step_c, int ncol) {
+  if (++q.mv == nm) {
+    q.mv = 0;
+    q.c += step_c;
+    q.sl += step_sl;
+    if (q.c >= ncol) {
+      q.c -= ncol;
+      ++q.sl;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
   grid_dep_sync();
@@ -136,50 +155,58 @@ __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
   if (nm == 0) return;
   const int slab0 = blockIdx.y * kKvSlabs;
   const int nslab = min(kKvSlabs, 2 * a.L - slab0);
-  const size_t sb_off = (size_t)a.src_base[b] * a.row_bytes;
-  const size_t db_off = (size_t)a.dst_base[b] * a.row_bytes;
-  const size_t ncol = a.vec ? a.row_bytes / 16 : a.row_bytes;
-  const long units = (long)nslab * (long)ncol;
+  const size_t rb = a.row_bytes;
+  // row 0 of this sequence's window in slab 0: [L][2][B][S][row_bytes]
+  const char *src0 = a.src + ((size_t)b * a.S_src + a.src_base[b]) * rb;
+  char *dst0 = a.dst + ((size_t)b * a.S_dst + a.dst_base[b]) * rb;
+  const size_t src_slab = (size_t)a.B * a.S_src * rb, dst_slab = (size_t)a.B * a.S_dst * rb;
+  const int ncol = a.ncol;  // units per row: 16-byte words, or bytes
+  const long units = (long)nslab * ncol;
   const long my_units = units > threadIdx.x ? (units - 1 - threadIdx.x) / kKvThreads + 1 : 0;
   const long items = my_units * nm;
-  long uu = 0;  // (unit, move) cursor, unit-major
-  int mv = 0;
+  // (unit, move) cursor, unit-major: unit = threadIdx.x + uu * kKvThreads
+  // sits in slab slab0 + sl at column c; stepping a unit adds kKvThreads
+  KvCursor cur{(int)(threadIdx.x / ncol), (int)(threadIdx.x % ncol), 0};
+  const size_t colw = a.vec ? 16 : 1;
   for (long i0 = 0; i0 < items; i0 += kKvBatch) {
-    const char *srcp[kKvBatch];
-    char *dstp[kKvBatch];
     const int cnt = (int)min((long)kKvBatch, items - i0);
-#pragma unroll
-    for (int j = 0; j < kKvBatch; ++j) {
-      if (j < cnt) {
-        const long u = threadIdx.x + uu * kKvThreads;
-        const int sl = (int)(u / (long)ncol);
-        const size_t c = (size_t)(u - (long)sl * (long)ncol);
-        const size_t slab = (size_t)(slab0 + sl) * a.B + b;
-        const size_t col = a.vec ? c * 16 : c;
-        srcp[j] = a.src + slab * a.S_src * a.row_bytes + sb_off + (size_t)s_src[mv] * a.row_bytes + col;
-        dstp[j] = a.dst + slab * a.S_dst * a.row_bytes + db_off + (size_t)s_dst[mv] * a.row_bytes + col;
-        if (++mv == nm) {
-          mv = 0;
-          ++uu;
-        }
-      }
-    }
+    const KvCursor start = cur;
+    auto src_of = [&](const KvCursor &q) {
+      return src0 + (size_t)(slab0 + q.sl) * src_slab + (size_t)s_src[q.mv] * rb + q.c * colw;
+    };
+    auto dst_of = [&](const KvCursor &q) {
+      return dst0 + (size_t)(slab0 + q.sl) * dst_slab + (size_t)s_dst[q.mv] * rb + q.c * colw;
+    };
     if (a.vec) {
       uint4 v[kKvBatch];
 #pragma unroll
       for (int j = 0; j < kKvBatch; ++j)
-        if (j < cnt) v[j] = ld_stream_v4(srcp[j]);
+        if (j < cnt) {
+          v[j] = ld_stream_v4(src_of(cur));
+          kv_step(cur, nm, a.step_sl, a.step_c, ncol);
+        }
+      cur = start;
 #pragma unroll
       for (int j = 0; j < kKvBatch; ++j)
-        if (j < cnt) *(uint4 *)dstp[j] = v[j];
+        if (j < cnt) {
+          *(uint4 *)dst_of(cur) = v[j];
+          kv_step(cur, nm, a.step_sl, a.step_c, ncol);
+        }
     } else {
       char v[kKvBatch];
 #pragma unroll
       for (int j = 0; j < kKvBatch; ++j)
-        if (j < cnt) v[j] = *srcp[j];
+        if (j < cnt) {
+          v[j] = *src_of(cur);
+          kv_step(cur, nm, a.step_sl, a.step_c, ncol);
+        }
+      cur = start;
 #pragma unroll
       for (int j = 0; j < kKvBatch; ++j)
-        if (j < cnt) *dstp[j] = v[j];
+        if (j < cnt) {
+          *dst_of(cur) = v[j];
+          kv_step(cur, nm, a.step_sl, a.step_c, ncol);
+        }
     }
   }
 }
@@ -243,6 +270,11 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   // rows == NULL in place moves no byte (every row stays): validate and set
   // the lengths with one CTA per sequence
   a.copy = !(rows == nullptr && a.inplace);
+  if (a.row_bytes / (a.vec ? 16 : 1) > 0x7fffffff)
+    return set_error(SV_ERR_UNSUPPORTED, "KV row too long");
+  a.ncol = (int)(a.row_bytes / (a.vec ? 16 : 1));
+  a.step_sl = kKvThreads / a.ncol;
+  a.step_c = kKvThreads % a.ncol;
   const unsigned gy = a.copy ? (unsigned)((2 * L + kKvSlabs - 1) / kKvSlabs) : 1u;
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("kv_compact", st);

@@ -72,38 +72,30 @@ __device__ __forceinline__ int round_node(const Round &r, int b, int i) {
 
 // ---------------------------------------------------------------------------
 // row_stats: online softmax statistics of every used logit row.
-// One CTA per unit = one kSegElems-element segment of one row (tree: the
-// units of the rows on the best paths, listed by tree_path).  Each thread
-// keeps kRsUnroll 16-byte loads in flight and folds them into an online
-// (max, log2-reference, sum) triple; bf16 maxima are taken on packed pairs and
-// the reference moves only when a larger value appears.  The CTA combines the
-// triples and writes (max x, mk, sum exp2(fma(x, k, -mk))) for the segment.
-// Ragged head / tail elements (outside the 16-byte-aligned body) are read
-// one by one.  Row slot j of a sequence is the verifier row of position j
-// (j <= maxpos) or the draft row of position j - maxpos - 1.
+// One CTA per (row, kSegElems-element segment); grid x = row (tree: the rows
+// on the best paths, listed by tree_path), y = segment.  Each thread loads
+// kRsUnroll 16-byte words at once, takes the batch maximum on packed pairs,
+// moves its log2-domain reference only when that maximum exceeds the running
+// one, and folds the batch into a sum of exp2(fma(x, k, -ref)) with packed
+// fp32 pair arithmetic (one ex2 per element).  The CTA combines the
+// per-thread triples and writes (max x, mk, sum exp2(fma(x, k, -mk))) for the
+// segment.  Ragged head / tail elements (outside the 16-byte-aligned body)
+// are read one by one.  Row slot j of a sequence is the verifier row of
+// position j (j <= maxpos) or the draft row of position j - maxpos - 1.
 constexpr int kSegElems = 16384;
 constexpr int kRsThreads = 256;
 constexpr int kRsUnroll = 8;
 
 // Per-thread online statistics.  mx = running max of raw logits (exact);
 // mk = fl(mx * k), the log2-domain reference of the sum; s = sum of
-// exp2(fma(x, k, -mk)) over the elements seen.  Each exponent is one fused
-// multiply-add, rounded once, and the output pair (mk, s) states the
-// reference the sum was taken against, so no rounding of mk enters q.
+// exp2(fma(x, k, -mk)) over the elements seen, kept as two packed pairs.
+// Each exponent is one fused multiply-add, rounded once, and the output pair
+// (mk, s) states the reference the sum was taken against, so no rounding of
+// mk enters q.
 struct StatState {
   float mx, mk;
-  float s0, s1;
+  unsigned long long s01, s23;  // packed partial sums
 };
-
-__device__ __forceinline__ void stat_raise(StatState &st, float cm, float k) {
-  // cm > st.mx: move the reference up and rescale the sums
-  const float nk = cm * k;
-  const float f = (st.mx == -INFINITY) ? 0.0f : ex2_approx(st.mk - nk);
-  st.s0 *= f;
-  st.s1 *= f;
-  st.mx = cm;
-  st.mk = nk;
-}
 
 // the reference used inside the exponent (a row that so far holds only -inf
 // or NaN uses 0, so -inf contributes 0 and NaN stays NaN)
@@ -111,60 +103,104 @@ __device__ __forceinline__ float stat_ref(const StatState &st) {
   return st.mx == -INFINITY ? 0.0f : st.mk;
 }
 
-// 8 bf16 logits in one 16-byte word
-__device__ __forceinline__ void stat8_bf16(uint4 v, StatState &st, uint32_t &mx2, float k) {
-  const uint32_t t = bf2_max(bf2_max(v.x, v.y), bf2_max(v.z, v.w));
-  if (bf2_max(t, mx2) != mx2) {  // some element above the running max (rare)
-    const float cm = fmaxf(bf16_lo(t), bf16_hi(t));
-    if (cm > st.mx) {
-      stat_raise(st, cm, k);
-      const uint32_t hb = __float_as_uint(cm) >> 16;
-      mx2 = (hb << 16) | hb;
-    }
-  }
-  const float r = stat_ref(st);
-  st.s0 += ex2_approx(fmaf(bf16_lo(v.x), k, -r));
-  st.s1 += ex2_approx(fmaf(bf16_hi(v.x), k, -r));
-  st.s0 += ex2_approx(fmaf(bf16_lo(v.y), k, -r));
-  st.s1 += ex2_approx(fmaf(bf16_hi(v.y), k, -r));
-  st.s0 += ex2_approx(fmaf(bf16_lo(v.z), k, -r));
-  st.s1 += ex2_approx(fmaf(bf16_hi(v.z), k, -r));
-  st.s0 += ex2_approx(fmaf(bf16_lo(v.w), k, -r));
-  st.s1 += ex2_approx(fmaf(bf16_hi(v.w), k, -r));
+__device__ __forceinline__ void stat_raise(StatState &st, float cm, float k) {
+  // cm > st.mx: move the reference up and rescale the sums
+  const float nk = cm * k;
+  const float f = (st.mx == -INFINITY) ? 0.0f : ex2_approx(st.mk - nk);
+  const unsigned long long f2 = f2_pack(f, f);
+  st.s01 = f2_mul(st.s01, f2);
+  st.s23 = f2_mul(st.s23, f2);
+  st.mx = cm;
+  st.mk = nk;
 }
 
-// 4 fp32 logits in one 16-byte word
-__device__ __forceinline__ void stat4_f32(uint4 v, StatState &st, float k) {
-  const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
-  const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
-  const float cm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-  if (cm > st.mx) stat_raise(st, cm, k);
-  const float r = stat_ref(st);
-  st.s0 += ex2_approx(fmaf(x0, k, -r));
-  st.s1 += ex2_approx(fmaf(x1, k, -r));
-  st.s0 += ex2_approx(fmaf(x2, k, -r));
-  st.s1 += ex2_approx(fmaf(x3, k, -r));
+// exp2 of a packed pair, accumulated
+__device__ __forceinline__ unsigned long long ex2_acc(unsigned long long acc,
+                                                      unsigned long long y2) {
+  float y0, y1;
+  f2_unpack(y2, y0, y1);
+  return f2_add(acc, f2_pack(ex2_approx(y0), ex2_approx(y1)));
 }
 
 template <typename E>
-__device__ __forceinline__ void stat_vec(uint4 v, StatState &st, uint32_t &mx2, float k);
+__device__ __forceinline__ void stat_batch(const uint4 (&w)[kRsUnroll], StatState &st, float k);
+
+// kRsUnroll words of 8 bf16 logits
 template <>
-__device__ __forceinline__ void stat_vec<uint16_t>(uint4 v, StatState &st, uint32_t &mx2,
-                                                   float k) {
-  stat8_bf16(v, st, mx2, k);
-}
-template <>
-__device__ __forceinline__ void stat_vec<float>(uint4 v, StatState &st, uint32_t &, float k) {
-  stat4_f32(v, st, k);
+__device__ __forceinline__ void stat_batch<uint16_t>(const uint4 (&w)[kRsUnroll], StatState &st,
+                                                     float k) {
+  uint32_t m[kRsUnroll];
+#pragma unroll
+  for (int j = 0; j < kRsUnroll; ++j) m[j] = bf2_max(bf2_max(w[j].x, w[j].y), bf2_max(w[j].z, w[j].w));
+#pragma unroll
+  for (int h = kRsUnroll / 2; h; h >>= 1)
+#pragma unroll
+    for (int j = 0; j < h; ++j) m[j] = bf2_max(m[j], m[j + h]);
+  const float cm = fmaxf(bf16_lo(m[0]), bf16_hi(m[0]));
+  if (cm > st.mx) stat_raise(st, cm, k);
+  const float r = stat_ref(st);
+  const unsigned long long k2 = f2_pack(k, k), nr2 = f2_pack(-r, -r);
+#pragma unroll
+  for (int j = 0; j < kRsUnroll; ++j) {
+    const uint32_t q[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const unsigned long long y2 = f2_fma(f2_pack(bf16_lo(q[h]), bf16_hi(q[h])), k2, nr2);
+      if (h & 1)
+        st.s23 = ex2_acc(st.s23, y2);
+      else
+        st.s01 = ex2_acc(st.s01, y2);
+    }
+  }
 }
 
-__device__ __forceinline__ void stat1(float x, StatState &st, uint32_t &mx2, float k) {
-  if (x > st.mx) {
-    stat_raise(st, x, k);
-    const uint32_t hb = __float_as_uint(x) >> 16;
-    mx2 = (hb << 16) | hb;
+// kRsUnroll words of 4 fp32 logits
+template <>
+__device__ __forceinline__ void stat_batch<float>(const uint4 (&w)[kRsUnroll], StatState &st,
+                                                  float k) {
+  float m[kRsUnroll];
+#pragma unroll
+  for (int j = 0; j < kRsUnroll; ++j)
+    m[j] = fmaxf(fmaxf(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
+                 fmaxf(__uint_as_float(w[j].z), __uint_as_float(w[j].w)));
+#pragma unroll
+  for (int h = kRsUnroll / 2; h; h >>= 1)
+#pragma unroll
+    for (int j = 0; j < h; ++j) m[j] = fmaxf(m[j], m[j + h]);
+  if (m[0] > st.mx) stat_raise(st, m[0], k);
+  const float r = stat_ref(st);
+  const unsigned long long k2 = f2_pack(k, k), nr2 = f2_pack(-r, -r);
+#pragma unroll
+  for (int j = 0; j < kRsUnroll; ++j) {
+    st.s01 = ex2_acc(st.s01, f2_fma(f2_pack(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
+                                    k2, nr2));
+    st.s23 = ex2_acc(st.s23, f2_fma(f2_pack(__uint_as_float(w[j].z), __uint_as_float(w[j].w)),
+                                    k2, nr2));
   }
-  st.s0 += ex2_approx(fmaf(x, k, -stat_ref(st)));
+}
+
+// one logit (ragged head / tail, and the short remainder of a segment)
+__device__ __forceinline__ void stat1(float x, StatState &st, float k) {
+  if (x > st.mx) stat_raise(st, x, k);
+  st.s01 = f2_add(st.s01, f2_pack(ex2_approx(fmaf(x, k, -stat_ref(st))), 0.0f));
+}
+template <typename E>
+__device__ __forceinline__ void stat_word(uint4 v, StatState &st, float k);
+template <>
+__device__ __forceinline__ void stat_word<uint16_t>(uint4 v, StatState &st, float k) {
+  const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    stat1(bf16_lo(q[h]), st, k);
+    stat1(bf16_hi(q[h]), st, k);
+  }
+}
+template <>
+__device__ __forceinline__ void stat_word<float>(uint4 v, StatState &st, float k) {
+  stat1(__uint_as_float(v.x), st, k);
+  stat1(__uint_as_float(v.y), st, k);
+  stat1(__uint_as_float(v.z), st, k);
+  stat1(__uint_as_float(v.w), st, k);
 }
 
 // Merge (mx2, mk2, s2) into (mx, mk, s): log2-domain references, -inf refs
@@ -183,6 +219,22 @@ __device__ __forceinline__ void st_combine(float &mx, float &mk, float &s, float
   mk = M;
 }
 
+// Combine the triples of the lanes of a warp: the largest reference wins,
+// every lane rescales its sum to it once, then max and sum reductions.
+__device__ __forceinline__ void warp_stat_combine(float &mx, float &mk, float &s) {
+  const float a = (mx == -INFINITY) ? -INFINITY : mk;
+  float M = a;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M != -INFINITY) s = s * ex2_approx(a - M);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  mk = M;
+}
+
 // Row slot of active row `a` of sequence b (tree: a <= npos verifier, then draft)
 __device__ __forceinline__ int slot_of_active(int a, int npos, int maxpos) {
   return a <= npos ? a : maxpos + 1 + (a - npos - 1);
@@ -197,17 +249,15 @@ struct SegInfo {
 
 template <typename E>
 __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t *rowlist,
-                                            long u) {
-  const long row_i = u / G;
-  const int seg = (int)(u - row_i * G);
+                                            int row_i, int seg) {
   int b, j;
   if (rowlist) {
     const int e = rowlist[row_i];
     b = e >> 12;
     j = slot_of_active(e & 0xfff, round_npos(r, b), r.maxpos);
   } else {
-    b = (int)(row_i / r.P);
-    j = (int)(row_i - (long)b * r.P);
+    b = row_i / r.P;
+    j = row_i - b * r.P;
   }
   const bool is_v = j <= r.maxpos;
   const int i = is_v ? j : j - r.maxpos - 1;
@@ -226,23 +276,20 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
   return si;
 }
 
+// statistics of segment blockIdx.y of listed row row_i, by the whole CTA
 template <typename E>
-__global__ void __launch_bounds__(kRsThreads)
-row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
-                 const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
-  grid_dep_sync();
-  const long u = blockIdx.x;
-  if (rowlist && u >= (long)*rowcount * G) return;  // beyond the tree's active rows
+__device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_t *rowlist,
+                                             int row_i, float4 *partial) {
+  const int seg = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SegInfo si = seg_info<E>(r, G, rowlist, u);
+  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg);
   const E *row = (const E *)si.row;
   const float k = r.k;
-  StatState st{-INFINITY, 0.0f, 0.0f, 0.0f};
-  uint32_t mx2 = 0xff80ff80u;  // (-inf, -inf) as bf16x2
+  StatState st{-INFINITY, 0.0f, 0ull, 0ull};
   const int nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
   const int ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
-  if (tid < nhead) stat1(load_elem<E>(row + si.v0 + tid), st, mx2, k);
-  if (tid < ntail) stat1(load_elem<E>((const E *)si.ae + tid), st, mx2, k);
+  if (tid < nhead) stat1(load_elem<E>(row + si.v0 + tid), st, k);
+  if (tid < ntail) stat1(load_elem<E>((const E *)si.ae + tid), st, k);
   const uint4 *body = (const uint4 *)si.ab;
   const int nv = (int)((si.ae - si.ab) / 16);
   int i = tid;
@@ -250,33 +297,36 @@ row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
     uint4 buf[kRsUnroll];
 #pragma unroll
     for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) stat_vec<E>(buf[j], st, mx2, k);
+    stat_batch<E>(buf, st, k);
   }
-  for (; i < nv; i += kRsThreads) stat_vec<E>(ld_stream_v4(body + i), st, mx2, k);
+  for (; i < nv; i += kRsThreads) stat_word<E>(ld_stream_v4(body + i), st, k);
 
-  float mx = st.mx, mk = st.mk, s = st.s0 + st.s1;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float mxo = __shfl_xor_sync(0xffffffffu, mx, o);
-    const float mko = __shfl_xor_sync(0xffffffffu, mk, o);
-    const float so = __shfl_xor_sync(0xffffffffu, s, o);
-    st_combine(mx, mk, s, mxo, mko, so);
-  }
+  float a0, a1, a2, a3;
+  f2_unpack(st.s01, a0, a1);
+  f2_unpack(st.s23, a2, a3);
+  float mx = st.mx, mk = st.mk, s = (a0 + a1) + (a2 + a3);
+  warp_stat_combine(mx, mk, s);
   __shared__ float4 red[kRsThreads / 32];
   if (lane == 0) red[warp] = make_float4(mx, mk, s, 0.0f);
   __syncthreads();
   if (warp == 0) {
     float4 v = lane < kRsThreads / 32 ? red[lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float mxo = __shfl_xor_sync(0xffffffffu, v.x, o);
-      const float mko = __shfl_xor_sync(0xffffffffu, v.y, o);
-      const float so = __shfl_xor_sync(0xffffffffu, v.z, o);
-      st_combine(v.x, v.y, v.z, mxo, mko, so);
-    }
+    warp_stat_combine(v.x, v.y, v.z);
     if (lane == 0) partial[si.out] = v;
   }
+  __syncthreads();  // red[] is reused by the CTA's next row
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+                 const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+  grid_dep_sync();
+  // chain: one row per CTA (exact grid); tree: the grid covers half the row
+  // slots and a CTA takes a second listed row when the paths are deep
+  const int nrows = rowlist ? *rowcount : (int)gridDim.x;
+  for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
+    stat_segment<E>(r, G, rowlist, row_i, partial);
 }
 
 Layout plan(int B, int maxpos, int V, bool tree) {
@@ -916,10 +966,12 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   Task *tasks = (Task *)(ws + L.task);
   sv_status s;
   {
-    const long units = (long)r.B * r.P * L.G;  // tree: an upper bound, extra CTAs exit
+    // tree: B * P row slots bound the listed rows; half as many CTAs per
+    // segment, each taking a second row when the paths are deep
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
+    const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
     LaunchScope ls("row_stats", st);
-    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3((unsigned)units),
+    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3(gx, (unsigned)L.G),
                                              dim3(kRsThreads), 0, st, r, L.G, rowlist,
                                              (const int *)(ws + L.ctr), partial));
     if (s != SV_OK) return s;
@@ -977,6 +1029,13 @@ sv_status check_common(const void *vlogits, sv_dtype dt, int B, int V, float tem
   return SV_OK;
 }
 
+// grid sizes of the round's kernels must fit a 32-bit grid dimension
+sv_status check_grid(int B, const Layout &L) {
+  if ((long long)B * L.P > 0x7fffffffLL || (long long)B * L.CS > 0x7fffffffLL)
+    return set_error(SV_ERR_UNSUPPORTED, "batch too large: B=%d", B);
+  return SV_OK;
+}
+
 sv_status map_chain_args(const void *&vlogits, const void *&dlogits, const int32_t *&tokens,
                          int32_t *&out_tokens, int32_t *&out_accept_len, float *&out_q_prob,
                          float *&out_p_prob, float *&out_margin, uint32_t *&out_status) {
@@ -1017,6 +1076,7 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   if (N > 0 && (!dlogits || !draft_tokens))
     return set_error(SV_ERR_INVALID_ARG, "dlogits and draft_tokens are required when N > 0");
   const Layout L = plan(B, N, V, false);
+  if ((s = check_grid(B, L)) != SV_OK) return s;
   if (workspace_bytes < L.total)
     return set_error(SV_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                      L.total);
@@ -1071,6 +1131,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   if (!dlogits || !parent || !token || !score || !out_path_nodes)
     return set_error(SV_ERR_INVALID_ARG, "null pointer argument");
   const Layout L = plan(B, max_depth, V, true);
+  if ((s = check_grid(B, L)) != SV_OK) return s;
   if (workspace_bytes < L.total)
     return set_error(SV_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                      L.total);
