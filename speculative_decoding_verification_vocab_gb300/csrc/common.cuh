@@ -195,10 +195,44 @@ __device__ __forceinline__ float exp32_repro(float a) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  // t is 1.5*2^23 + n exactly (|n| < 2^22), so the integer n sits in its bits
+  // t is 1.5*2^23 + n exactly (|n| < 2^22), so the integer n sits in its bits;
+  // p * 2^n is exact for a >= -80 (p in [0.7, 1.5], the product is a normal
+  // number), so adding n to p's exponent field gives its bits without a
+  // multiply
   const int ni = __float_as_int(t) - 0x4B400000;
-  const float e = __fmul_rn(p, __int_as_float((ni + 127) << 23));
+  const float e = __int_as_float(__float_as_int(p) + (ni << 23));
   return (a >= -80.0f) ? e : 0.0f;
+}
+
+// exp32_repro of both lanes of a packed pair, bit for bit: the same fp32
+// operations as packed pair instructions (fused multiply-adds and one
+// subtraction; no multiply feeds an addition, so none can be contracted).
+__device__ __forceinline__ unsigned long long f2_add_rz(unsigned long long a,
+                                                        unsigned long long b) {
+  unsigned long long r;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_splat(float a) { return f2_pack(a, a); }
+__device__ __forceinline__ unsigned long long exp32x2(unsigned long long a2) {
+  const unsigned long long t2 = f2_fma(a2, f2_splat(0x1.715476p+0f), f2_splat(0x1.8p+23f));
+  const unsigned long long n2 = f2_sub(t2, f2_splat(0x1.8p+23f));
+  unsigned long long r2 = f2_fma(n2, f2_splat(-0x1.62e4p-1f), a2);
+  r2 = f2_fma(n2, f2_splat(-0x1.7f7d1cp-20f), r2);
+  unsigned long long p2 = f2_fma(f2_splat(1.0f / 5040.0f), r2, f2_splat(1.0f / 720.0f));
+  p2 = f2_fma(p2, r2, f2_splat(1.0f / 120.0f));
+  p2 = f2_fma(p2, r2, f2_splat(1.0f / 24.0f));
+  p2 = f2_fma(p2, r2, f2_splat(1.0f / 6.0f));
+  p2 = f2_fma(p2, r2, f2_splat(0.5f));
+  p2 = f2_fma(p2, r2, f2_splat(1.0f));
+  p2 = f2_fma(p2, r2, f2_splat(1.0f));
+  float t0, t1, q0, q1, a0, a1;
+  f2_unpack(t2, t0, t1);
+  f2_unpack(p2, q0, q1);
+  f2_unpack(a2, a0, a1);
+  const float e0 = __int_as_float(__float_as_int(q0) + ((__float_as_int(t0) - 0x4B400000) << 23));
+  const float e1 = __int_as_float(__float_as_int(q1) + ((__float_as_int(t1) - 0x4B400000) << 23));
+  return f2_pack(a0 >= -80.0f ? e0 : 0.0f, a1 >= -80.0f ? e1 : 0.0f);
 }
 
 }  // namespace sv

@@ -545,37 +545,10 @@ struct Parts40 {
 struct Parts62 {
   float a, b, c, d;  // multiples of 2^-16, 2^-32, 2^-48, 2^-62
 };
-__device__ __forceinline__ float trunc_to(float v, float grid_top) {
-  // v truncated to the grid of spacing ulp(grid_top) (v < grid_top)
-  return __fsub_rn(__fadd_rz(v, grid_top), grid_top);
-}
-__device__ __forceinline__ void add40(Parts40 &P, float e) {
-  const float a = trunc_to(e, 0x1p7f);
-  const float r1 = __fsub_rn(e, a);
-  const float b = trunc_to(r1, 0x1p-9f);
-  const float r2 = __fsub_rn(r1, b);
-  const float c = trunc_to(r2, 0x1p-17f);
-  P.a = __fadd_rn(P.a, a);
-  P.b = __fadd_rn(P.b, b);
-  P.c = __fadd_rn(P.c, c);
-}
 __device__ __forceinline__ unsigned long long fix_of(const Parts40 &P) {
   return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 24) +
          (unsigned long long)__float2uint_rn(__fmul_rn(P.b, 0x1p32f)) * (1ull << 8) +
          (unsigned long long)__float2uint_rn(__fmul_rn(P.c, 0x1p40f));
-}
-__device__ __forceinline__ void add62(Parts62 &P, float w) {
-  const float a = trunc_to(w, 0x1p7f);
-  const float r1 = __fsub_rn(w, a);
-  const float b = trunc_to(r1, 0x1p-9f);
-  const float r2 = __fsub_rn(r1, b);
-  const float c = trunc_to(r2, 0x1p-25f);
-  const float r3 = __fsub_rn(r2, c);
-  const float d = trunc_to(r3, 0x1p-39f);
-  P.a = __fadd_rn(P.a, a);
-  P.b = __fadd_rn(P.b, b);
-  P.c = __fadd_rn(P.c, c);
-  P.d = __fadd_rn(P.d, d);
 }
 __device__ __forceinline__ unsigned long long fix_of(const Parts62 &P) {
   return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 46) +
@@ -591,49 +564,120 @@ __device__ __forceinline__ float inv_sum(unsigned long long se) {
   return __double2float_rn(__ddiv_rn(0x1p40, __ull2double_rn(se)));
 }
 
-// The logits of elements [v, v + kSpRun) as fp32 (0 past V).
+// A thread's run of kSpRun consecutive logits of one row, kept as the raw
+// 16-byte words (bf16 pairs or fp32) and converted element by element when
+// used.  Elements past the row's end read as -inf, whose exponential is 0.
 template <typename E>
-__device__ __forceinline__ void load_run(const E *row, int v, int V, bool vec,
-                                         float x[kSpRun]);
+struct Run;
 template <>
-__device__ __forceinline__ void load_run<uint16_t>(const uint16_t *row, int v, int V, bool vec,
-                                                   float x[kSpRun]) {
+struct Run<uint16_t> {
+  uint4 w[kSpRun / 8];
+  __device__ __forceinline__ float operator[](int j) const {
+    const uint4 &q = w[j >> 3];
+    const int c = (j >> 1) & 3;
+    const uint32_t x = c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
+    return (j & 1) ? bf16_hi(x) : bf16_lo(x);
+  }
+};
+template <>
+struct Run<float> {
+  uint4 w[kSpRun / 4];
+  __device__ __forceinline__ float operator[](int j) const {
+    const uint4 &q = w[j >> 2];
+    const int c = j & 3;
+    return __uint_as_float(c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w);
+  }
+};
+
+template <typename E>
+__device__ __forceinline__ void load_run(Run<E> &run, const E *row, int v, int V, bool vec) {
+  constexpr int kPer = 16 / sizeof(E);  // elements per word
   if (vec && v + kSpRun <= V) {
     const uint4 *p = (const uint4 *)(row + v);
 #pragma unroll
-    for (int j = 0; j < kSpRun / 8; ++j) {
-      const uint4 w = __ldg(p + j);
-      x[8 * j + 0] = bf16_lo(w.x);
-      x[8 * j + 1] = bf16_hi(w.x);
-      x[8 * j + 2] = bf16_lo(w.y);
-      x[8 * j + 3] = bf16_hi(w.y);
-      x[8 * j + 4] = bf16_lo(w.z);
-      x[8 * j + 5] = bf16_hi(w.z);
-      x[8 * j + 6] = bf16_lo(w.w);
-      x[8 * j + 7] = bf16_hi(w.w);
-    }
+    for (int k = 0; k < kSpRun / kPer; ++k) run.w[k] = __ldg(p + k);
     return;
   }
+  // ragged or unaligned run: element by element
+  uint32_t bits[kSpRun];
 #pragma unroll
-  for (int j = 0; j < kSpRun; ++j) x[j] = (v + j < V) ? load_elem<uint16_t>(row + v + j) : 0.0f;
+  for (int j = 0; j < kSpRun; ++j) {
+    const bool in = v + j < V;
+    if (sizeof(E) == 2)
+      bits[j] = in ? (uint32_t)__ldg((const unsigned short *)row + v + j) : 0xff80u;
+    else
+      bits[j] = in ? __float_as_uint(__ldg((const float *)row + v + j)) : 0xff800000u;
+  }
+#pragma unroll
+  for (int k = 0; k < kSpRun / kPer; ++k) {
+    uint32_t q[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      q[c] = sizeof(E) == 2 ? (bits[8 * k + 2 * c] | (bits[8 * k + 2 * c + 1] << 16))
+                            : bits[4 * k + c];
+    run.w[k] = make_uint4(q[0], q[1], q[2], q[3]);
+  }
 }
-template <>
-__device__ __forceinline__ void load_run<float>(const float *row, int v, int V, bool vec,
-                                                float x[kSpRun]) {
-  if (vec && v + kSpRun <= V) {
-    const float4 *p = (const float4 *)(row + v);
-#pragma unroll
-    for (int j = 0; j < kSpRun / 4; ++j) {
-      const float4 f = __ldg(p + j);
-      x[4 * j + 0] = f.x;
-      x[4 * j + 1] = f.y;
-      x[4 * j + 2] = f.z;
-      x[4 * j + 3] = f.w;
-    }
-    return;
-  }
-#pragma unroll
-  for (int j = 0; j < kSpRun; ++j) x[j] = (v + j < V) ? __ldg(row + v + j) : 0.0f;
+
+// packed exponent arguments fl(fl(x * invT) - mz) of two elements (the
+// multiply is skipped at T = 1; scalar where a multiply is involved)
+__device__ __forceinline__ unsigned long long arg2(float x0, float x1, float m0, float m1,
+                                                   float invT, bool unit_t) {
+  if (unit_t) return f2_sub(f2_pack(x0, x1), f2_pack(m0, m1));
+  return f2_pack(__fsub_rn(__fmul_rn(x0, invT), m0), __fsub_rn(__fmul_rn(x1, invT), m1));
+}
+
+// split-part accumulation of a packed pair (each lane as add40 / add62)
+struct Parts40x2 {
+  unsigned long long a, b, c;
+};
+struct Parts62x2 {
+  unsigned long long a, b, c, d;
+};
+__device__ __forceinline__ unsigned long long trunc2(unsigned long long v, float grid_top) {
+  const unsigned long long g = f2_splat(grid_top);
+  return f2_sub(f2_add_rz(v, g), g);
+}
+__device__ __forceinline__ void add40x2(Parts40x2 &P, unsigned long long e) {
+  const unsigned long long a = trunc2(e, 0x1p7f);
+  const unsigned long long r1 = f2_sub(e, a);
+  const unsigned long long b = trunc2(r1, 0x1p-9f);
+  const unsigned long long r2 = f2_sub(r1, b);
+  const unsigned long long c = trunc2(r2, 0x1p-17f);
+  P.a = f2_add(P.a, a);
+  P.b = f2_add(P.b, b);
+  P.c = f2_add(P.c, c);
+}
+__device__ __forceinline__ void add62x2(Parts62x2 &P, unsigned long long w) {
+  const unsigned long long a = trunc2(w, 0x1p7f);
+  const unsigned long long r1 = f2_sub(w, a);
+  const unsigned long long b = trunc2(r1, 0x1p-9f);
+  const unsigned long long r2 = f2_sub(r1, b);
+  const unsigned long long c = trunc2(r2, 0x1p-25f);
+  const unsigned long long r3 = f2_sub(r2, c);
+  const unsigned long long d = trunc2(r3, 0x1p-39f);
+  P.a = f2_add(P.a, a);
+  P.b = f2_add(P.b, b);
+  P.c = f2_add(P.c, c);
+  P.d = f2_add(P.d, d);
+}
+// the two lanes' exact sums
+__device__ __forceinline__ void fix_lanes(const Parts40x2 &P, unsigned long long &s0,
+                                          unsigned long long &s1) {
+  Parts40 l0, l1;
+  f2_unpack(P.a, l0.a, l1.a);
+  f2_unpack(P.b, l0.b, l1.b);
+  f2_unpack(P.c, l0.c, l1.c);
+  s0 = fix_of(l0);
+  s1 = fix_of(l1);
+}
+__device__ __forceinline__ unsigned long long fix_sum(const Parts62x2 &P) {
+  Parts62 l0, l1;
+  f2_unpack(P.a, l0.a, l1.a);
+  f2_unpack(P.b, l0.b, l1.b);
+  f2_unpack(P.c, l0.c, l1.c);
+  f2_unpack(P.d, l0.d, l1.d);
+  return fix_of(l0) + fix_of(l1);
 }
 
 __device__ __forceinline__ float e1(float x, float invT, float mz, bool unit_t) {
@@ -683,7 +727,7 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads)
+__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 4 : 2)
 sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
   grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
@@ -691,21 +735,29 @@ sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
   if (!t.active) return;
   const RowPair p = row_pair<E>(r, t);
   const int v = cs * kSpSlice + kSpRun * threadIdx.x;
-  float x[kSpRun];
-  Parts40 Pq{0.0f, 0.0f, 0.0f}, Pp{0.0f, 0.0f, 0.0f};
-  load_run<E>((const E *)p.rq, v, r.V, p.vec, x);
-#pragma unroll
-  for (int j = 0; j < kSpRun; ++j)
-    if (v + j < r.V) add40(Pq, e1(x[j], r.invT, p.mzq, p.unit_t));
-  if (p.resid) {
-    load_run<E>((const E *)p.rp, v, r.V, p.vec, x);
+  Run<E> rq;
+  load_run<E>(rq, (const E *)p.rq, v, r.V, p.vec);
+  Parts40x2 P{0ull, 0ull, 0ull};
+  unsigned long long fq, fp;
+  if (p.resid) {  // lanes (q row, p row) of the same element
+    Run<E> rp;
+    load_run<E>(rp, (const E *)p.rp, v, r.V, p.vec);
 #pragma unroll
     for (int j = 0; j < kSpRun; ++j)
-      if (v + j < r.V) add40(Pp, e1(x[j], r.invT, p.mzp, p.unit_t));
+      add40x2(P, exp32x2(arg2(rq[j], rp[j], p.mzq, p.mzp, r.invT, p.unit_t)));
+    fix_lanes(P, fq, fp);
+  } else {  // lanes (element j, element j + 1) of the q row
+#pragma unroll
+    for (int j = 0; j < kSpRun; j += 2)
+      add40x2(P, exp32x2(arg2(rq[j], rq[j + 1], p.mzq, p.mzq, r.invT, p.unit_t)));
+    unsigned long long f1;
+    fix_lanes(P, fq, f1);
+    fq += f1;
+    fp = 0ull;
   }
   __shared__ unsigned long long red[kSpWarps];
-  const unsigned long long sq = block_sum_u64(fix_of(Pq), red);
-  const unsigned long long sp = block_sum_u64(fix_of(Pp), red);
+  const unsigned long long sq = block_sum_u64(fq, red);
+  const unsigned long long sp = block_sum_u64(fp, red);
   if (threadIdx.x == 0) sw.norm[blockIdx.x] = make_ulonglong2(sq, sp);
 }
 
@@ -831,7 +883,7 @@ __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, con
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads)
+__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 4 : 2)
 sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
   grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
@@ -841,24 +893,32 @@ sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideO
   __shared__ float s_inv[2];
   if (threadIdx.x == 0) inv_sums(sw, b, p.resid, s_inv[0], s_inv[1]);
   const int v = cs * kSpSlice + kSpRun * threadIdx.x;
-  float xq[kSpRun], xp[kSpRun];
-  load_run<E>((const E *)p.rq, v, r.V, p.vec, xq);
-  if (p.resid) load_run<E>((const E *)p.rp, v, r.V, p.vec, xp);
+  Run<E> rq, rp;
+  load_run<E>(rq, (const E *)p.rq, v, r.V, p.vec);
+  if (p.resid) load_run<E>(rp, (const E *)p.rp, v, r.V, p.vec);
   __syncthreads();
   const float iq = s_inv[0], ip = s_inv[1];
-  Parts62 P{0.0f, 0.0f, 0.0f, 0.0f};
+  Parts62x2 P{0ull, 0ull, 0ull, 0ull};
+  if (p.resid) {
 #pragma unroll
-  for (int j = 0; j < kSpRun; ++j) {
-    if (v + j >= r.V) continue;
-    const float q = __fmul_rn(e1(xq[j], r.invT, p.mzq, p.unit_t), iq);
-    float w = q;
-    if (p.resid) {
-      const float d = __fsub_rn(q, __fmul_rn(e1(xp[j], r.invT, p.mzp, p.unit_t), ip));
-      w = d > 0.0f ? d : 0.0f;
+    for (int j = 0; j < kSpRun; j += 2) {
+      float q0, p0, q1, p1;
+      f2_unpack(exp32x2(arg2(rq[j], rp[j], p.mzq, p.mzp, r.invT, p.unit_t)), q0, p0);
+      f2_unpack(exp32x2(arg2(rq[j + 1], rp[j + 1], p.mzq, p.mzp, r.invT, p.unit_t)), q1, p1);
+      const float d0 = __fsub_rn(__fmul_rn(q0, iq), __fmul_rn(p0, ip));
+      const float d1 = __fsub_rn(__fmul_rn(q1, iq), __fmul_rn(p1, ip));
+      add62x2(P, f2_pack(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)));
     }
-    add62(P, w);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kSpRun; j += 2) {
+      float e0, e1;
+      f2_unpack(exp32x2(arg2(rq[j], rq[j + 1], p.mzq, p.mzq, r.invT, p.unit_t)), e0, e1);
+      // q >= 0; the max keeps the product out of the split's addition
+      add62x2(P, f2_pack(fmaxf(__fmul_rn(e0, iq), 0.0f), fmaxf(__fmul_rn(e1, iq), 0.0f)));
+    }
   }
-  const unsigned long long mine = fix_of(P);
+  const unsigned long long mine = fix_sum(P);
   sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
   __threadfence();
   __shared__ unsigned long long red[kSpWarps];
