@@ -3,7 +3,9 @@
 One step = one speculative round over a batch: the tree attention mask
 (sv_tree_build_mask), the tree verify (sv_verify_tree: best-child path, row
 statistics, accept walk, residual / bonus sampling) and the KV compaction of
-the accepted paths (sv_kv_compact, in place).  Default workload: the dynamic
+the accepted paths (sv_kv_compact, in place).  The mask and the compaction run
+on a second stream: the mask needs only the tree, and the compaction starts
+at the verify call's accept event, overlapping the residual / bonus sampling.  Default workload: the dynamic
 EAGLE-2 tree (B=128, 60-node budget, depth 6, top-k 10, V=128256, bf16 logits,
 KV shaped like a 70B model: 80 layers x 8 KV heads x 128).  `--config 3` runs
 the large-vocabulary chain (B=256, N=7) instead (verify + chain rollback).
@@ -252,6 +254,36 @@ class Workload:
         return int(((2 * d + 1) * self.V * self.esize).sum())
 
 
+def run_round(sv, wl, cfg, maxd, src, out, i, seed, step_no, ws, stream, side, ev_fork, ev_acc):
+    """One speculative round, the way a serving loop would issue it: the main
+    stream verifies; a side stream builds the tree mask (it needs only the
+    tree) and, once the accept walk's event fires, compacts the KV cache while
+    the main stream still samples the correction / bonus tokens.  The main
+    stream joins the side stream at the end, so the round is complete there.
+    `out` holds per-round output views: path, tok, acc, st, kv, mask, depth."""
+    ev_fork.record(stream)
+    side.wait_event(ev_fork)
+    if wl.tree:
+        sv.sv_tree_build_mask(src["parent"], out["mask"], out["depth"], side)
+        sv.sv_verify_tree(src["vq"], src["dp"], src["parent"], src["token"], src["score"], maxd,
+                          cfg.temperature, seed, step_no, out["path"][i], out["tok"][i],
+                          out["acc"][i], None, None, None, out["st"][i], ws, stream,
+                          accept_event=ev_acc)
+        side.wait_event(ev_acc)
+        sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, out["path"][i], out["acc"][i], 1,
+                         out["kv"][i], side)
+    else:
+        sv.sv_verify_chain(src["vq"], src["dp"], src["d"], cfg.temperature, seed, step_no,
+                           out["tok"][i], out["acc"][i], None, None, None, out["st"][i], ws,
+                           stream, accept_event=ev_acc)
+        side.wait_event(ev_acc)
+        # chain rollback: the accepted drafts' rows are already in place;
+        # only the logical length moves (rows NULL = identity)
+        sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, None, out["acc"][i], 1,
+                         out["kv"][i], side)
+    stream.wait_stream(side)
+
+
 def run_ours(args):
     import torch
     import speculative_decoding_verification_vocab_gb300 as sv
@@ -287,23 +319,13 @@ def run_ours(args):
                 else sv.sv_verify_chain_workspace(B, cfg.N, V))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    ev_fork, ev_acc = torch.cuda.Event(), torch.cuda.Event()
+    outs = dict(path=o_path, tok=o_tok, acc=o_acc, st=o_st, kv=o_kv, mask=o_mask, depth=o_depth)
 
     def step(i, rd, seed_step):
-        if wl.tree:
-            sv.sv_tree_build_mask(rd["parent"], o_mask, o_depth, stream)
-            sv.sv_verify_tree(rd["vq"], rd["dp"], rd["parent"], rd["token"], rd["score"], maxd,
-                              cfg.temperature, rank_seed(1234, rank), seed_step, o_path[i], o_tok[i],
-                              o_acc[i], None, None, None, o_st[i], ws, stream)
-            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, o_path[i], o_acc[i], 1,
-                             o_kv[i], stream)
-        else:
-            sv.sv_verify_chain(rd["vq"], rd["dp"], rd["d"], cfg.temperature, rank_seed(1234, rank),
-                               seed_step, o_tok[i], o_acc[i], None, None, None, o_st[i], ws,
-                               stream)
-            # chain rollback: the accepted drafts' rows are already in place;
-            # only the logical length moves (rows NULL = identity)
-            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, None, o_acc[i], 1, o_kv[i],
-                             stream)
+        run_round(sv, wl, cfg, maxd, rd, outs, i, rank_seed(1234, rank), seed_step, ws, stream,
+                  side, ev_fork, ev_acc)
 
     for i in range(W):
         step(i, wl.rounds[i % args.pool], i)
@@ -437,19 +459,13 @@ def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
     o_depth = torch.empty(B, T, dtype=torch.int32, device=dev)
     d2h = sum(h.numel() * h.element_size() for h in hout.values())
 
+    side = torch.cuda.Stream(device=dev)
+    ev_fork, ev_acc = torch.cuda.Event(), torch.cuda.Event()
+    o1 = {k: v[None] for k, v in outs.items()}
+    o1.update(mask=o_mask, depth=o_depth)
+
     def calls(src, i):
-        if wl.tree:
-            sv.sv_tree_build_mask(src["parent"], o_mask, o_depth, stream)
-            sv.sv_verify_tree(src["vq"], src["dp"], src["parent"], src["token"], src["score"],
-                              maxd, cfg.temperature, 99, i, outs["path"], outs["tok"], outs["acc"],
-                              None, None, None, outs["st"], ws, stream)
-            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, outs["path"], outs["acc"], 1,
-                             outs["kv"], stream)
-        else:
-            sv.sv_verify_chain(src["vq"], src["dp"], src["d"], cfg.temperature, 99, i,
-                               outs["tok"], outs["acc"], None, None, None, outs["st"], ws, stream)
-            sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, None, outs["acc"], 1,
-                             outs["kv"], stream)
+        run_round(sv, wl, cfg, maxd, src, o1, 0, 99, i, ws, stream, side, ev_fork, ev_acc)
         for k in outs:
             hout[k].copy_(outs[k], non_blocking=True)
 

@@ -25,6 +25,13 @@
  *    query (device memory is the fast choice).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  All work is enqueued asynchronously on it.
+ *  - `accept_event` (verify calls; a cudaEvent_t as void*, or NULL): when
+ *    given, it is recorded on `stream` as soon as the accept walk is done --
+ *    out_accept_len, out_path_nodes and the accepted tokens are final -- and
+ *    before the correction / bonus sampling runs.  Work that needs only the
+ *    accepted prefix (the KV compaction) can wait on it from another stream
+ *    and overlap the sampling.  out_tokens[a], out_margin's gap and the
+ *    SV_ROW_RESID_ZERO bit are written after it.
  *  - Argument errors are detected on the host before anything is enqueued;
  *    the call then returns a non-OK sv_status and sv_last_error() says why.
  *    A failed kernel launch returns SV_ERR_CUDA.  No C++ exception crosses
@@ -113,7 +120,7 @@ sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
                           float *out_q_prob, float *out_p_prob,
                           float *out_margin, uint32_t *out_status,
                           void *workspace, size_t workspace_bytes,
-                          void *stream);
+                          void *stream, void *accept_event);
 
 /* ---------------------------------------------------------------------------
  * sv_verify_tree -- verify a flattened draft tree per sequence.
@@ -149,7 +156,7 @@ sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv_dtype dt,
                          float *out_q_prob, float *out_p_prob,
                          float *out_margin, uint32_t *out_status,
                          void *workspace, size_t workspace_bytes,
-                         void *stream);
+                         void *stream, void *accept_event);
 
 /* ---------------------------------------------------------------------------
  * sv_tree_build_mask -- the tree attention mask.
@@ -225,7 +232,7 @@ sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dlogits,
                                   int32_t *out_tokens, int32_t *out_accept_len,
                                   float *out_q_prob, float *out_p_prob,
                                   float *out_margin, uint32_t *out_status,
-                                  void *stream);
+                                  void *stream, void *accept_event);
 
 /* Thread-local message for the last non-OK status returned on this thread. */
 const char *sv_last_error(void);

@@ -54,17 +54,17 @@ def load_library(path: str = LIB_PATH):
     L.sv_verify_chain_workspace.argtypes = [i32, i32, i32]
     L.sv_verify_chain_workspace.restype = sz
     L.sv_verify_chain.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
-                                  vp, vp, vp, vp, vp, vp, vp, sz, vp]
+                                  vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.sv_verify_chain.restype = i32
     L.sv_verify_chain_noalloc_max_bytes.argtypes = []
     L.sv_verify_chain_noalloc_max_bytes.restype = sz
     L.sv_verify_chain_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
-                                          vp, vp, vp, vp, vp, vp, vp]
+                                          vp, vp, vp, vp, vp, vp, vp, vp]
     L.sv_verify_chain_noalloc.restype = i32
     L.sv_verify_tree_workspace.argtypes = [i32, i32, i32, i32]
     L.sv_verify_tree_workspace.restype = sz
     L.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
-                                 vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+                                 vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.sv_verify_tree.restype = i32
     L.sv_tree_build_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     L.sv_tree_build_mask.restype = i32
@@ -97,6 +97,16 @@ def _stream(stream):
     return C.c_void_p(stream.cuda_stream)
 
 
+def _event(ev):
+    """A torch.cuda.Event (or None) as a cudaEvent_t.  torch creates the
+    underlying event on its first record, so an unused one is recorded once."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record()
+    return C.c_void_p(ev.cuda_event)
+
+
 def _check(st):
     if st != SV_OK:
         raise SvError(st, load_library().sv_last_error().decode())
@@ -118,7 +128,7 @@ def sv_verify_chain_workspace(B, N, V):
 
 def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out_tokens,
                     out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, workspace,
-                    stream=None):
+                    stream=None, accept_event=None):
     B, R, V = vlogits.shape
     N = R - 1
     return _check(load_library().sv_verify_chain(
@@ -126,7 +136,7 @@ def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out
         _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
         _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
         _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        _stream(stream), _event(accept_event)))
 
 
 def sv_verify_chain_noalloc_max_bytes():
@@ -135,7 +145,7 @@ def sv_verify_chain_noalloc_max_bytes():
 
 def sv_verify_chain_noalloc(vlogits, dlogits, draft_tokens, temperature, seed, step, out_tokens,
                             out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
-                            stream=None):
+                            stream=None, accept_event=None):
     """sv_verify_chain for callers that cannot allocate: scratch is the
     library's static device array (see include/sv.h)."""
     B, R, V = vlogits.shape
@@ -144,7 +154,7 @@ def sv_verify_chain_noalloc(vlogits, dlogits, draft_tokens, temperature, seed, s
         _p(vlogits), _p(dlogits) if N > 0 else None, _dtype(vlogits),
         _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
         _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
-        _p(out_status), _stream(stream)))
+        _p(out_status), _stream(stream), _event(accept_event)))
 
 
 def sv_verify_tree_workspace(B, T, max_depth, V):
@@ -153,14 +163,14 @@ def sv_verify_tree_workspace(B, T, max_depth, V):
 
 def sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
                    out_path_nodes, out_tokens, out_accept_len, out_q_prob, out_p_prob,
-                   out_margin, out_status, workspace, stream=None):
+                   out_margin, out_status, workspace, stream=None, accept_event=None):
     B, T, V = vlogits.shape
     return _check(load_library().sv_verify_tree(
         _p(vlogits), _p(dlogits), _dtype(vlogits), _p(parent), _p(token), _p(score), B, T,
         max_depth, V, float(temperature), int(seed), int(step), _p(out_path_nodes),
         _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
         _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        _stream(stream), _event(accept_event)))
 
 
 def sv_tree_build_mask(parent, out_mask, out_depth, stream=None):
@@ -213,7 +223,7 @@ def _out_dev(t):
 
 
 def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0,
-                 workspace=None, stream=None, probs=True):
+                 workspace=None, stream=None, probs=True, accept_event=None):
     """Allocate outputs and run sv_verify_chain.  Returns a dict of tensors."""
     B, R, V = vlogits.shape
     N = R - 1
@@ -229,12 +239,12 @@ def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0
         workspace = _ws(sv_verify_chain_workspace(B, N, V), dev)
     sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out["tokens"],
                     out["accept_len"], out["q_prob"], out["p_prob"], out["margin"],
-                    out["status"], workspace, stream)
+                    out["status"], workspace, stream, accept_event)
     return out
 
 
 def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1.0, seed=0,
-                step=0, workspace=None, stream=None, probs=True):
+                step=0, workspace=None, stream=None, probs=True, accept_event=None):
     B, T, V = vlogits.shape
     dev = _out_dev(vlogits)
     P = max_depth + 1
@@ -250,7 +260,7 @@ def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1
         workspace = _ws(sv_verify_tree_workspace(B, T, max_depth, V), dev)
     sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
                    out["path"], out["tokens"], out["accept_len"], out["q_prob"], out["p_prob"],
-                   out["margin"], out["status"], workspace, stream)
+                   out["margin"], out["status"], workspace, stream, accept_event)
     return out
 
 

@@ -1021,7 +1021,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
 // ---------------------------------------------------------------------------
 template <typename E>
 sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, uint64_t step,
-                     const DecideOut &o, cudaStream_t st) {
+                     const DecideOut &o, cudaStream_t st, cudaEvent_t accept_event) {
   float4 *partial = (float4 *)(ws + L.partial);
   Task *tasks = (Task *)(ws + L.task);
   sv_status s;
@@ -1049,6 +1049,10 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
                                           dim3(kDecideWarps * 32), dsm, st, r, L.G, partial, seed,
                                           step, o, tasks, (unsigned *)(ws + L.done)));
     if (s != SV_OK) return s;
+  }
+  if (accept_event) {
+    const cudaError_t e = cudaEventRecord(accept_event, st);
+    if (e != cudaSuccess) return set_error(SV_ERR_CUDA, "accept_event: %s", cudaGetErrorString(e));
   }
   SampleWs sw;
   sw.norm = (ulonglong2 *)(ws + L.norm);
@@ -1127,7 +1131,8 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
                                      int32_t *out_tokens, int32_t *out_accept_len,
                                      float *out_q_prob, float *out_p_prob, float *out_margin,
                                      uint32_t *out_status, void *workspace,
-                                     size_t workspace_bytes, void *stream) {
+                                     size_t workspace_bytes, void *stream,
+                                     void *accept_event) {
   sv_status s = check_common(vlogits, dt, B, V, temperature, out_tokens, out_accept_len,
                              out_status, workspace);
   if (s != SV_OK || B == 0) return s;
@@ -1163,8 +1168,8 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   r.k = r.invT * kLog2e;
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
-  return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st)
-                       : run_verify<float>(r, L, ws, seed, step, o, st);
+  return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
+                       : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event);
 }
 
 extern "C" size_t sv_verify_tree_workspace(int B, int T, int max_depth, int V) {
@@ -1179,7 +1184,8 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
                                     int32_t *out_path_nodes, int32_t *out_tokens,
                                     int32_t *out_accept_len, float *out_q_prob,
                                     float *out_p_prob, float *out_margin, uint32_t *out_status,
-                                    void *workspace, size_t workspace_bytes, void *stream) {
+                                    void *workspace, size_t workspace_bytes, void *stream,
+                                    void *accept_event) {
   sv_status s = check_common(vlogits, dt, B, V, temperature, out_tokens, out_accept_len,
                              out_status, workspace);
   if (s != SV_OK || B == 0) return s;
@@ -1235,8 +1241,8 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   r.k = r.invT * kLog2e;
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
               out_path_nodes};
-  return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st)
-                       : run_verify<float>(r, L, ws, seed, step, o, st);
+  return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
+                       : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event);
 }
 
 // ---------------------------------------------------------------------------
@@ -1290,7 +1296,8 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dl
                                              uint64_t step, int32_t *out_tokens,
                                              int32_t *out_accept_len, float *out_q_prob,
                                              float *out_p_prob, float *out_margin,
-                                             uint32_t *out_status, void *stream) {
+                                             uint32_t *out_status, void *stream,
+                                             void *accept_event) {
   if (B < 0 || N < 0 || V < 1)
     return set_error(SV_ERR_INVALID_ARG, "need B >= 0, N >= 0, V >= 1");
   if (B == 0) return SV_OK;
@@ -1306,5 +1313,5 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dl
   if (s != SV_OK) return s;
   return sv_verify_chain(vlogits, dlogits, dt, draft_tokens, B, N, V, temperature, seed, step,
                          out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,
-                         out_status, ws, kStaticScratchBytes, stream);
+                         out_status, ws, kStaticScratchBytes, stream, accept_event);
 }

@@ -429,7 +429,45 @@ def test_pageable_host_memory_refused():
     n0 = sv.sv_launch_count()
     p = lambda t: C.c_void_p(t.data_ptr())
     rc = lib.sv_verify_chain(C.c_void_p(host.ctypes.data), p(dl), 0, p(dt_), B, N, V, 1.0, 0, 0,
-                             p(tok), p(acc), None, None, None, p(st), p(ws), ws.numel(), None)
+                             p(tok), p(acc), None, None, None, p(st), p(ws), ws.numel(), None,
+                             None)
     assert rc == sv.SV_ERR_INVALID_ARG
     assert "pageable" in sv.sv_last_error()
     assert sv.sv_launch_count() == n0
+
+
+def test_accept_event_marks_final_accept_outputs():
+    """The accept event: once it has fired, accept lengths and paths are
+    final, so a second stream can compact the KV cache while the sampling
+    still runs; both streams' results match a plain single-stream call."""
+    cfg = synth.CONFIGS[5]
+    B, V = 16, 20000
+    vq, dp, parent, token, score = (x.to(DEV) for x in synth.tree_inputs(cfg, seed=4, B=B, V=V))
+    ref = sv.verify_tree(vq, dp, parent, token, score, cfg.depth, seed=9, step=3)
+    torch.cuda.synchronize()
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    L, S, H, D = 2, parent.shape[1] + 4, 2, 16
+    kv = synth.kv_cache(L, B, S, H, D, device=DEV, seed=3)
+    kv_ref = kv.clone()
+    base = torch.zeros(B, dtype=torch.int32, device=DEV)
+    main.wait_stream(torch.cuda.current_stream())
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(main):
+        out = sv.verify_tree(vq, dp, parent, token, score, cfg.depth, seed=9, step=3,
+                             stream=main, accept_event=ev)
+    side.wait_event(ev)
+    with torch.cuda.stream(side):
+        acc_at_event = out["accept_len"].clone()
+        path_at_event = out["path"].clone()
+        kl = sv.kv_compact(kv, kv, base, base, out["path"], out["accept_len"], 1, stream=side)
+    torch.cuda.synchronize()
+    assert torch.equal(acc_at_event, ref["accept_len"])
+    assert torch.equal(path_at_event, ref["path"])
+    for k in ("tokens", "accept_len", "path", "status"):
+        assert torch.equal(out[k], ref[k]), k
+    kl_ref = sv.kv_compact(kv_ref, kv_ref, base, base, ref["path"], ref["accept_len"], 1)
+    torch.cuda.synchronize()
+    # random KV bytes hold NaN patterns: compare the bytes
+    assert torch.equal(kl, kl_ref)
+    assert torch.equal(kv.view(torch.int16), kv_ref.view(torch.int16))

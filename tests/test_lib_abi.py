@@ -48,19 +48,19 @@ def test_host_argument_checks_need_no_gpu(lib):
     null = None
     # negative sizes, bad dtype, bad temperature: refused before any CUDA call
     assert lib.sv_verify_chain(null, null, 0, null, -1, 2, 10, 1.0, 0, 0, null, null, null, null,
-                               null, null, null, 0, null) == 1
+                               null, null, null, 0, null, null) == 1
     assert lib.sv_verify_chain(null, null, 7, null, 1, 2, 10, 1.0, 0, 0, null, null, null, null,
-                               null, null, null, 0, null) == 1
+                               null, null, null, 0, null, null) == 1
     assert lib.sv_verify_chain(null, null, 0, null, 1, 2, 10, 0.0, 0, 0, null, null, null, null,
-                               null, null, null, 0, null) == 1
+                               null, null, null, 0, null, null) == 1
     assert b"temperature" in lib.sv_last_error()
     assert lib.sv_verify_chain(null, null, 0, null, 1, 2, (1 << 22) + 1, 1.0, 0, 0, null, null,
-                               null, null, null, null, null, 0, null) == 2
+                               null, null, null, null, null, 0, null, null) == 2
     # B == 0 is a no-op
     assert lib.sv_verify_chain(null, null, 0, null, 0, 2, 10, 1.0, 0, 0, null, null, null, null,
-                               null, null, null, 0, null) == 0
+                               null, null, null, 0, null, null) == 0
     assert lib.sv_verify_tree(null, null, 1, null, null, null, 1, 20, 3, 10, 1.0, 0, 0, null,
-                              null, null, null, null, null, null, null, 0, null) == 1
+                              null, null, null, null, null, null, null, 0, null, null) == 1
     assert lib.sv_tree_build_mask(null, 1, 2000, null, null, null) == 2
     assert lib.sv_tree_build_mask(null, 1, 0, null, null, null) == 1
     assert lib.sv_kv_compact(null, null, 0, 1, 4, 4, 1, 1, 2, null, null, null, null, 0, 1,

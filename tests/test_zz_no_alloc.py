@@ -45,7 +45,7 @@ def test_noalloc_matches_workspace_entry_point():
                 _ptr(vq), _ptr(dp), sv.SV_BF16 if dtype == torch.bfloat16 else sv.SV_F32,
                 _ptr(d), B, N, V, T, 5, call, _ptr(out["tokens"]), _ptr(out["accept_len"]),
                 _ptr(out["q_prob"]), _ptr(out["p_prob"]), _ptr(out["margin"]),
-                _ptr(out["status"]), stream)
+                _ptr(out["status"]), stream, None)
             assert st == sv.SV_OK, lib.sv_last_error()
             torch.cuda.synchronize()
             for k in ("tokens", "accept_len", "status"):
@@ -63,7 +63,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     B, N, V = 16384, 7, 128256
     assert lib.sv_verify_chain_workspace(B, N, V) > cap
     st = lib.sv_verify_chain_noalloc(None, None, sv.SV_BF16, None, B, N, V, 1.0, 0, 0, None,
-                                     None, None, None, None, None, None)
+                                     None, None, None, None, None, None, None)
     assert st == sv.SV_ERR_UNSUPPORTED
     msg = lib.sv_last_error().decode()
     assert "static scratch" in msg and str(cap) in msg
