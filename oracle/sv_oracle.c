@@ -457,9 +457,9 @@ int orc_verify_tree(const float *vlog, const float *dlog, const int32_t *parent,
                     int32_t *out_accept, double *out_q, double *out_p,
                     double *out_margin, double *out_gap, uint32_t *out_status) {
   int P = max_depth + 1;
-  int32_t *path = (int32_t *)malloc(sizeof(int32_t) * (size_t)B * P);
-  int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)B * (P > 1 ? P - 1 : 1));
-  int32_t *npos = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+  int32_t *path = (int32_t *)calloc((size_t)B * P + 1, sizeof(int32_t));
+  int32_t *tok = (int32_t *)calloc((size_t)B * (P > 1 ? P - 1 : 1) + 1, sizeof(int32_t));
+  int32_t *npos = (int32_t *)calloc((size_t)(B > 0 ? B : 1), sizeof(int32_t));
   uint8_t *bad = (uint8_t *)calloc((size_t)(B > 0 ? B : 1), 1);
   for (int b = 0; b < B; ++b) {
     const int32_t *pa = parent + (int64_t)b * T;

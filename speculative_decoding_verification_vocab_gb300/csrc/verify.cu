@@ -7,7 +7,8 @@
 //                streams the whole input; HBM-bound
 //   decide       one warp per sequence: q(d)/p(d), Philox uniforms, the left-
 //                to-right accept walk, outputs, and the sampling task
-//   sample_norm  exact fixed-point normaliser partials of the 1-2 sampled rows
+//   sample_norm  exact fixed-point normaliser partials of the 1-2 sampled rows;
+//                the last slice CTA of a sequence turns them into 1/S_e
 //   sample_mass  fixed-point residual / bonus masses per slice and per run;
 //                the last slice CTA of a sequence does the inverse-CDF pick
 //
@@ -44,7 +45,7 @@ struct Task {
 
 struct Layout {
   int maxpos, P, G, CS;
-  size_t ctr, rowlist, partial, task, norm, mass, run, done, path, npos, tok, tstat, total;
+  size_t ctr, rowlist, partial, task, norm, mass, run, done, inv, path, npos, tok, tstat, total;
 };
 
 Layout plan(int B, int maxpos, int V, bool tree);
@@ -349,7 +350,8 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   L.norm = take(sizeof(ulonglong2) * (size_t)B * L.CS);
   L.mass = take(sizeof(unsigned long long) * (size_t)B * L.CS);
   L.run = take(sizeof(unsigned long long) * (size_t)B * L.CS * kSpThreads);
-  L.done = take(sizeof(unsigned) * (size_t)B);
+  L.done = take(sizeof(unsigned) * 2 * (size_t)B);
+  L.inv = take(sizeof(float2) * (size_t)B);
   if (tree) {
     L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
     L.npos = take(sizeof(int32_t) * (size_t)B);
@@ -507,7 +509,8 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     t.mp = (!bad && a < npos) ? mxd[a] : 0.0f;
     t.u24 = bad ? 0u : usm[vi];
     tasks[b] = t;
-    done[b] = 0u;  // the sampler's per-sequence completion count
+    done[b] = 0u;        // the sampler's per-sequence completion counts:
+    done[r.B + b] = 0u;  // slice CTAs of sample_mass, of sample_norm
   }
 }
 
@@ -532,9 +535,14 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
 // Two kernels per round.  A CTA owns one kSpSlice-element slice of one
 // sequence's q row (and p row for a residual); thread t owns the kSpRun
 // consecutive elements [t * kSpRun, (t + 1) * kSpRun) of the slice:
-//   sample_norm  partial sums of floor(e 2^40) of the slice
-//   sample_mass  S_e from the partials, then W of every element; the sum of
-//                each thread's run is stored (the prefix search's blocks)
+//   sample_norm  partial sums of floor(e 2^40) of the slice; the CTA that
+//                completes a sequence's slices last (a per-sequence count)
+//                computes 1/S_e of the q and p rows once
+//   sample_mass  W of every element; the sum of each thread's run is stored
+//                (the prefix search's blocks)
+// Both evaluate the exponentials and the splits on packed fp32 pairs: the q
+// and p element of one position (residual), or two neighbouring q elements
+// (bonus), one per lane.
 //   (pick)       in the CTA that finishes a sequence's masses last, one warp:
 //                the threshold, the slice, the run, then a warp scan of the
 //                run's 32 elements
@@ -689,8 +697,11 @@ struct SampleWs {
   ulonglong2 *norm;          // [B][CS] partial (sum floor(e_q 2^40), sum floor(e_p 2^40))
   unsigned long long *mass;  // [B][CS] slice sum W
   unsigned long long *run;   // [B][CS][kSpThreads] run sums of W
-  unsigned *done;            // [B] slice CTAs of sample_mass finished (zeroed by decide)
+  unsigned *done;            // [2][B] slice CTAs of sample_mass / sample_norm finished
+                             // (zeroed by decide)
+  float2 *inv;               // [B] (1/S_e of q, of p) from the last sample_norm CTA
   int CS;                    // slices per row
+  int B;
 };
 
 struct RowPair {
@@ -726,6 +737,19 @@ __device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v
   return tot;  // valid on thread 0
 }
 
+// S_e of the q and p rows of sequence b -> 1 / sum, by one thread
+__device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, float &iq,
+                                         float &ip) {
+  unsigned long long Sq = 0, Sp = 0;
+  for (int c = 0; c < sw.CS; ++c) {
+    const ulonglong2 n = __ldcg(sw.norm + (size_t)b * sw.CS + c);  // other CTAs' sums
+    Sq += n.x;
+    Sp += n.y;
+  }
+  iq = inv_sum(Sq);
+  ip = resid ? inv_sum(Sp) : 0.0f;
+}
+
 template <typename E>
 __global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 4 : 2)
 sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
@@ -758,21 +782,19 @@ sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
   __shared__ unsigned long long red[kSpWarps];
   const unsigned long long sq = block_sum_u64(fq, red);
   const unsigned long long sp = block_sum_u64(fp, red);
-  if (threadIdx.x == 0) sw.norm[blockIdx.x] = make_ulonglong2(sq, sp);
+  if (threadIdx.x == 0) {
+    // the last slice CTA of the sequence turns the slice sums into 1/S_e
+    sw.norm[blockIdx.x] = make_ulonglong2(sq, sp);
+    __threadfence();
+    if (atomicAdd(sw.done + sw.B + b, 1u) == (unsigned)(sw.CS - 1)) {
+      __threadfence();
+      float iq, ip;
+      inv_sums(sw, b, p.resid, iq, ip);
+      sw.inv[b] = make_float2(iq, ip);
+    }
+  }
 }
 
-// S_e of the q and p rows of sequence b -> 1 / sum, by one thread
-__device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, float &iq,
-                                         float &ip) {
-  unsigned long long Sq = 0, Sp = 0;
-  for (int c = 0; c < sw.CS; ++c) {
-    const ulonglong2 n = sw.norm[(size_t)b * sw.CS + c];
-    Sq += n.x;
-    Sp += n.y;
-  }
-  iq = inv_sum(Sq);
-  ip = resid ? inv_sum(Sp) : 0.0f;
-}
 
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
@@ -824,8 +846,8 @@ template <typename E>
 __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, const RowPair &p,
                                               const SampleWs &sw, const DecideOut &o, int b) {
   const int lane = threadIdx.x & 31;
-  float iq, ip;
-  inv_sums(sw, b, p.resid, iq, ip);
+  const float2 iv = sw.inv[b];
+  const float iq = iv.x, ip = iv.y;
   const unsigned long long *mass = sw.mass + (size_t)b * sw.CS;
   unsigned long long Sw = 0;
   for (int c = 0; c < sw.CS; ++c) Sw += __ldcg(mass + c);
@@ -890,14 +912,12 @@ sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideO
   const Task t = tasks[b];
   if (!t.active) return;
   const RowPair p = row_pair<E>(r, t);
-  __shared__ float s_inv[2];
-  if (threadIdx.x == 0) inv_sums(sw, b, p.resid, s_inv[0], s_inv[1]);
   const int v = cs * kSpSlice + kSpRun * threadIdx.x;
   Run<E> rq, rp;
   load_run<E>(rq, (const E *)p.rq, v, r.V, p.vec);
   if (p.resid) load_run<E>(rp, (const E *)p.rp, v, r.V, p.vec);
-  __syncthreads();
-  const float iq = s_inv[0], ip = s_inv[1];
+  const float2 iv = sw.inv[b];  // written by sample_norm
+  const float iq = iv.x, ip = iv.y;
   Parts62x2 P{0ull, 0ull, 0ull, 0ull};
   if (p.resid) {
 #pragma unroll
@@ -920,11 +940,13 @@ sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideO
   }
   const unsigned long long mine = fix_sum(P);
   sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
-  __threadfence();
   __shared__ unsigned long long red[kSpWarps];
-  const unsigned long long tot = block_sum_u64(mine, red);
+  const unsigned long long tot = block_sum_u64(mine, red);  // also a CTA barrier
   __shared__ int s_last;
   if (threadIdx.x == 0) {
+    // the barrier above orders every thread's run store before this
+    // thread's device-scope fence, which orders them (cumulatively) before
+    // the count that the last CTA of the sequence observes
     sw.mass[blockIdx.x] = tot;
     __threadfence();
     s_last = atomicAdd(sw.done + b, 1u) == (unsigned)(sw.CS - 1);
@@ -1059,7 +1081,9 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   sw.mass = (unsigned long long *)(ws + L.mass);
   sw.run = (unsigned long long *)(ws + L.run);
   sw.done = (unsigned *)(ws + L.done);
+  sw.inv = (float2 *)(ws + L.inv);
   sw.CS = L.CS;
+  sw.B = r.B;
   const unsigned grid = (unsigned)((long)r.B * L.CS);
   {
     LaunchScope ls("sample_norm", st);
