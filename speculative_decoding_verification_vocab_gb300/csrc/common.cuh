@@ -22,6 +22,8 @@ int num_sms();
 // pageable host memory and other devices' memory are refused with
 // SV_ERR_INVALID_ARG (a kernel would fault on them).  NULL stays NULL.
 sv_status map_ptr(const void **p, const char *what);
+// 1 when p is memory of the current device (not host memory mapped into it)
+int is_device_memory(const void *p);
 template <typename T>
 sv_status map_arg(T *&p, const char *what) {
   const void *q = p;
@@ -114,6 +116,18 @@ template <typename T> __device__ __forceinline__ float load_elem(const T *p);
 template <> __device__ __forceinline__ float load_elem<float>(const float *p) { return __ldg(p); }
 template <> __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t *p) {
   return __uint_as_float((uint32_t)__ldg(p) << 16);
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), and its completion
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {

@@ -62,6 +62,8 @@ struct Round {
   int tok_stride;
   const uint32_t *tstat;    // [B] tree status or null
   float invT, k;            // 1/T and log2(e)/T
+  int stage;                // logits in device memory: row_stats may stage through
+                            // shared memory with asynchronous copies
 };
 
 __device__ __forceinline__ int round_npos(const Round &r, int b) {
@@ -83,9 +85,17 @@ __device__ __forceinline__ int round_node(const Round &r, int b, int i) {
 // segment.  Ragged head / tail elements (outside the 16-byte-aligned body)
 // are read one by one.  Row slot j of a sequence is the verifier row of
 // position j (j <= maxpos) or the draft row of position j - maxpos - 1.
-constexpr int kSegElems = 16384;
+constexpr int kSegElems = 16384;  // smallest segment (fp32); sizes the workspace
 constexpr int kRsThreads = 256;
 constexpr int kRsUnroll = 8;
+// A thread owns 2 * kRsUnroll 16-byte words of a segment: the first
+// kRsUnroll go to registers, the second are staged into shared memory by
+// asynchronous copies issued first, so a CTA keeps 64 KB of loads in flight
+// while holding only 32 words of registers per thread.
+template <typename E>
+__host__ __device__ constexpr int seg_elems() {
+  return kRsThreads * 2 * kRsUnroll * 16 / (int)sizeof(E);
+}
 
 // Per-thread online statistics.  mx = running max of raw logits (exact);
 // mk = fl(mx * k), the log2-domain reference of the sum; s = sum of
@@ -267,8 +277,8 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
   const E *row = (const E *)(is_v ? r.vlog : r.dlog) +
                  ((size_t)b * (is_v ? r.v_rows : r.d_rows) + node) * (size_t)r.V;
   si.row = (const char *)row;
-  si.v0 = seg * kSegElems;
-  si.v1 = min(r.V, si.v0 + kSegElems);
+  si.v0 = seg * seg_elems<E>();
+  si.v1 = min(r.V, si.v0 + seg_elems<E>());
   const uintptr_t pb = (uintptr_t)(row + si.v0), pe = (uintptr_t)(row + si.v1);
   si.ab = (pb + 15) & ~(uintptr_t)15;
   si.ae = pe & ~(uintptr_t)15;
@@ -294,6 +304,24 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
   const uint4 *body = (const uint4 *)si.ab;
   const int nv = (int)((si.ae - si.ab) / 16);
   int i = tid;
+  if (r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
+    // full pattern: the second half through shared memory (each thread reads
+    // back only the slots it copied, so its own wait is the only sync needed)
+    __shared__ uint4 sbuf[kRsUnroll][kRsThreads];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j)
+      cp_async16(&sbuf[j][tid], body + i + (kRsUnroll + j) * kRsThreads);
+    cp_async_commit();
+    uint4 buf[kRsUnroll];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
+    stat_batch<E>(buf, st, k);
+    cp_async_wait_all();
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = sbuf[j][tid];
+    stat_batch<E>(buf, st, k);
+    i += 2 * kRsUnroll * kRsThreads;
+  }
   for (; i + (kRsUnroll - 1) * kRsThreads < nv; i += kRsUnroll * kRsThreads) {
     uint4 buf[kRsUnroll];
 #pragma unroll
@@ -1047,14 +1075,16 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   float4 *partial = (float4 *)(ws + L.partial);
   Task *tasks = (Task *)(ws + L.task);
   sv_status s;
+  // segments per row for this element type (the workspace holds L.G >= G)
+  const int G = (r.V + seg_elems<E>() - 1) / seg_elems<E>();
   {
     // tree: B * P row slots bound the listed rows; half as many CTAs per
     // segment, each taking a second row when the paths are deep
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
     const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
     LaunchScope ls("row_stats", st);
-    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3(gx, (unsigned)L.G),
-                                             dim3(kRsThreads), 0, st, r, L.G, rowlist,
+    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3(gx, (unsigned)G),
+                                             dim3(kRsThreads), 0, st, r, G, rowlist,
                                              (const int *)(ws + L.ctr), partial));
     if (s != SV_OK) return s;
   }
@@ -1068,7 +1098,7 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     LaunchScope ls("decide", st);
     s = check_launch("decide", launch_pdl(decide_kernel<E>,
                                           dim3((r.B + kDecideWarps - 1) / kDecideWarps),
-                                          dim3(kDecideWarps * 32), dsm, st, r, L.G, partial, seed,
+                                          dim3(kDecideWarps * 32), dsm, st, r, G, partial, seed,
                                           step, o, tasks, (unsigned *)(ws + L.done)));
     if (s != SV_OK) return s;
   }
@@ -1190,6 +1220,7 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   r.tstat = nullptr;
   r.invT = 1.0f / temperature;
   r.k = r.invT * kLog2e;
+  r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
@@ -1263,6 +1294,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   r.tstat = tstat;
   r.invT = 1.0f / temperature;
   r.k = r.invT * kLog2e;
+  r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
               out_path_nodes};
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
