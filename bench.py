@@ -452,8 +452,10 @@ def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
                 st=torch.empty(B, dtype=torch.int32, device=dev),
                 kv=torch.empty(B, dtype=torch.int32, device=dev))
     hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
-    ws = torch.empty(sv.sv_verify_tree_workspace(B, T, maxd, V) if wl.tree
-                     else sv.sv_verify_chain_workspace(B, cfg.N, V), dtype=torch.uint8, device=dev)
+    # the host-size workspace: each host row read crosses the link once
+    ws = torch.empty(sv.sv_verify_tree_workspace_host(B, T, maxd, V, rd["vq"].dtype) if wl.tree
+                     else sv.sv_verify_chain_workspace_host(B, cfg.N, V, rd["vq"].dtype),
+                     dtype=torch.uint8, device=dev)
     Wm = (T + 63) // 64
     o_mask = torch.empty(B, T, Wm, dtype=torch.int64, device=dev)
     o_depth = torch.empty(B, T, dtype=torch.int32, device=dev)
@@ -485,13 +487,10 @@ def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
 
     n = max(1, args.e2e_steps)
     rows, ms, value = timed(lambda i: calls(host, i), n)
-    # host bytes the kernels read: the stats rows, the sampled rows (two
-    # passes; two rows for a residual, one for a bonus), the tree arrays
-    acc = hout["acc"].numpy().astype(np.int64)
-    depth = rd["depth"]
-    esize = wl.esize
-    sampled_rows = np.where(acc < depth, 2, 1)
-    h2d = (wl.stats_bytes(0) + int(2 * sampled_rows.sum()) * V * esize
+    # host bytes the kernels read: the stats rows (copied to the device as
+    # they are read; the accept walk and the sampler use the copies) and the
+    # tree arrays
+    h2d = (wl.stats_bytes(0)
            + sum(host[k].numel() * host[k].element_size() for k in names if k not in ("vq", "dp")))
     in_bytes = sum(h.numel() * h.element_size() for h in host.values())
 

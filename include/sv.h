@@ -61,7 +61,7 @@ typedef enum {
   SV_ERR_INVALID_ARG = 1, /* bad pointer, size, dtype or workspace */
   SV_ERR_UNSUPPORTED = 2, /* valid but beyond this build's limits */
   SV_ERR_CUDA = 3,        /* a CUDA call failed; sv_last_error() has it */
-  SV_ERR_TIMEOUT = 4      /* a bounded device wait gave up */
+  SV_ERR_TIMEOUT = 4      /* reserved: no call of this build waits on the device */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -113,6 +113,11 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  * chosen token does not depend on how the sum is split across threads.
  * --------------------------------------------------------------------------- */
 size_t sv_verify_chain_workspace(int B, int N, int V);
+/* A larger workspace for logits in page-locked host memory: with it, every
+ * logit row the round reads crosses the host link once (the row statistics
+ * keep a device copy that the accept walk and the sampler read); with the
+ * plain size those steps read the host rows again.  Returns 0 on bad sizes. */
+size_t sv_verify_chain_workspace_host(int B, int N, int V, sv_dtype dt);
 sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
                           const int32_t *draft_tokens, int B, int N, int V,
                           float temperature, uint64_t seed, uint64_t step,
@@ -147,6 +152,8 @@ sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
  * A single-path tree gives bit-identical results to sv_verify_chain.
  * --------------------------------------------------------------------------- */
 size_t sv_verify_tree_workspace(int B, int T, int max_depth, int V);
+/* As sv_verify_chain_workspace_host, for trees. */
+size_t sv_verify_tree_workspace_host(int B, int T, int max_depth, int V, sv_dtype dt);
 sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv_dtype dt,
                          const int32_t *parent, const int32_t *token,
                          const float *score, int B, int T, int max_depth,

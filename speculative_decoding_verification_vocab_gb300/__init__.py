@@ -22,7 +22,8 @@ SV_F32, SV_BF16 = 0, 1
 SV_ROW_NAN, SV_ROW_BAD_TOKEN, SV_ROW_RESID_ZERO, SV_ROW_P_ZERO, SV_ROW_BAD_TREE = 1, 2, 4, 8, 16
 SV_MAX_VOCAB, SV_MAX_POSITIONS, SV_MAX_TREE_NODES = 1 << 22, 1024, 1024
 
-EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain", "sv_verify_chain_noalloc",
+EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_verify_chain",
+           "sv_verify_chain_noalloc", "sv_verify_tree_workspace_host",
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
            "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_last_error",
            "sv_launch_count", "sv_trace_enable", "sv_trace_collect")
@@ -63,6 +64,10 @@ def load_library(path: str = LIB_PATH):
     L.sv_verify_chain_noalloc.restype = i32
     L.sv_verify_tree_workspace.argtypes = [i32, i32, i32, i32]
     L.sv_verify_tree_workspace.restype = sz
+    L.sv_verify_tree_workspace_host.argtypes = [i32, i32, i32, i32, i32]
+    L.sv_verify_tree_workspace_host.restype = sz
+    L.sv_verify_chain_workspace_host.argtypes = [i32, i32, i32, i32]
+    L.sv_verify_chain_workspace_host.restype = sz
     L.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                  vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.sv_verify_tree.restype = i32
@@ -126,6 +131,13 @@ def sv_verify_chain_workspace(B, N, V):
     return int(load_library().sv_verify_chain_workspace(B, N, V))
 
 
+def sv_verify_chain_workspace_host(B, N, V, dtype):
+    """Workspace bytes with room for a device copy of the rows read (for
+    logits in page-locked host memory); dtype: a torch dtype."""
+    return int(load_library().sv_verify_chain_workspace_host(
+        B, N, V, SV_BF16 if dtype == torch.bfloat16 else SV_F32))
+
+
 def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out_tokens,
                     out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, workspace,
                     stream=None, accept_event=None):
@@ -159,6 +171,12 @@ def sv_verify_chain_noalloc(vlogits, dlogits, draft_tokens, temperature, seed, s
 
 def sv_verify_tree_workspace(B, T, max_depth, V):
     return int(load_library().sv_verify_tree_workspace(B, T, max_depth, V))
+
+
+def sv_verify_tree_workspace_host(B, T, max_depth, V, dtype):
+    """As sv_verify_chain_workspace_host, for trees."""
+    return int(load_library().sv_verify_tree_workspace_host(
+        B, T, max_depth, V, SV_BF16 if dtype == torch.bfloat16 else SV_F32))
 
 
 def sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
@@ -236,7 +254,8 @@ def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0
         margin=torch.empty(B, N + 1, dtype=torch.float32, device=dev) if probs else None,
         status=torch.empty(B, dtype=torch.int32, device=dev))
     if workspace is None:
-        workspace = _ws(sv_verify_chain_workspace(B, N, V), dev)
+        workspace = _ws(sv_verify_chain_workspace(B, N, V) if vlogits.is_cuda
+                        else sv_verify_chain_workspace_host(B, N, V, vlogits.dtype), dev)
     sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out["tokens"],
                     out["accept_len"], out["q_prob"], out["p_prob"], out["margin"],
                     out["status"], workspace, stream, accept_event)
@@ -257,7 +276,8 @@ def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1
         margin=torch.empty(B, P, dtype=torch.float32, device=dev) if probs else None,
         status=torch.empty(B, dtype=torch.int32, device=dev))
     if workspace is None:
-        workspace = _ws(sv_verify_tree_workspace(B, T, max_depth, V), dev)
+        workspace = _ws(sv_verify_tree_workspace(B, T, max_depth, V) if vlogits.is_cuda
+                        else sv_verify_tree_workspace_host(B, T, max_depth, V, vlogits.dtype), dev)
     sv_verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature, seed, step,
                    out["path"], out["tokens"], out["accept_len"], out["q_prob"], out["p_prob"],
                    out["margin"], out["status"], workspace, stream, accept_event)

@@ -112,6 +112,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+__device__ __forceinline__ float elem_to_f32(float x) { return x; }
+__device__ __forceinline__ float elem_to_f32(uint16_t x) {
+  return __uint_as_float((uint32_t)x << 16);
+}
+
 template <typename T> __device__ __forceinline__ float load_elem(const T *p);
 template <> __device__ __forceinline__ float load_elem<float>(const float *p) { return __ldg(p); }
 template <> __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t *p) {

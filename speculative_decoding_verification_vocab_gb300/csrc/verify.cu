@@ -34,18 +34,20 @@ constexpr int kSpSlice = kSpThreads * kSpRun;  // 8192 elements per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Task {
-  int active;  // 1: a correction / bonus token is to be drawn
-  int a;       // accept length = output slot of the drawn token
-  int vrow;    // absolute verifier row (rows of V elements)
-  int drow;    // absolute draft row, -1 for a bonus draw
-  float mq, mp;  // raw-logit maxima of those rows
+  const void *rq;  // the verifier row to sample from (its device copy for host logits)
+  const void *rp;  // the draft row of a residual draw, null for a bonus draw
+  int active;      // 1: a correction / bonus token is to be drawn
+  int a;           // accept length = output slot of the drawn token
+  float mq, mp;    // raw-logit maxima of those rows
   uint32_t u24;
   int pad;
 };
 
 struct Layout {
   int maxpos, P, G, CS;
-  size_t ctr, rowlist, partial, task, norm, mass, run, done, inv, path, npos, tok, tstat, total;
+  size_t ctr, rowlist, partial, task, norm, mass, run, done, inv, path, npos, tok, tstat;
+  size_t end;    // end of the regions (256-aligned); an optional row copy follows
+  size_t total;  // bytes to request: the regions plus base-pointer alignment
 };
 
 Layout plan(int B, int maxpos, int V, bool tree);
@@ -64,6 +66,8 @@ struct Round {
   float invT, k;            // 1/T and log2(e)/T
   int stage;                // logits in device memory: row_stats may stage through
                             // shared memory with asynchronous copies
+  char *copy;               // host-resident logits: device copy of every row slot
+  size_t pitch;             // that row_stats reads (bytes per slot), or null
 };
 
 __device__ __forceinline__ int round_npos(const Round &r, int b) {
@@ -71,6 +75,24 @@ __device__ __forceinline__ int round_npos(const Round &r, int b) {
 }
 __device__ __forceinline__ int round_node(const Round &r, int b, int i) {
   return r.path ? r.path[(size_t)b * (r.maxpos + 1) + i] : i;
+}
+
+// Row slot j of sequence b: the verifier row of position j (j <= maxpos) or
+// the draft row of position j - maxpos - 1, in the caller's logits ...
+template <typename E>
+__device__ __forceinline__ const E *src_row(const Round &r, int b, int j) {
+  const bool is_v = j <= r.maxpos;
+  const int node = round_node(r, b, is_v ? j : j - r.maxpos - 1);
+  return (const E *)(is_v ? r.vlog : r.dlog) +
+         ((size_t)b * (is_v ? r.v_rows : r.d_rows) + node) * (size_t)r.V;
+}
+// ... and where the steps after row_stats read it: the device copy when the
+// logits are host-resident (same offset within 16 bytes as the source row,
+// so the vector paths line up), else the source row itself
+template <typename E>
+__device__ __forceinline__ const E *used_row(const Round &r, int b, int j, const E *src) {
+  if (!r.copy) return src;
+  return (const E *)(r.copy + ((size_t)b * r.P + j) * r.pitch + ((uintptr_t)src & 15));
 }
 
 // ---------------------------------------------------------------------------
@@ -253,6 +275,7 @@ __device__ __forceinline__ int slot_of_active(int a, int npos, int maxpos) {
 
 struct SegInfo {
   const char *row;   // row base
+  char *copy;        // its device copy (host-resident logits), or null
   int v0, v1;        // element range of the segment
   uintptr_t ab, ae;  // 16-byte-aligned body [ab, ae)
   size_t out;        // partial index
@@ -270,13 +293,10 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
     b = row_i / r.P;
     j = row_i - b * r.P;
   }
-  const bool is_v = j <= r.maxpos;
-  const int i = is_v ? j : j - r.maxpos - 1;
-  const int node = round_node(r, b, i);
   SegInfo si;
-  const E *row = (const E *)(is_v ? r.vlog : r.dlog) +
-                 ((size_t)b * (is_v ? r.v_rows : r.d_rows) + node) * (size_t)r.V;
+  const E *row = src_row<E>(r, b, j);
   si.row = (const char *)row;
+  si.copy = r.copy ? (char *)used_row<E>(r, b, j, row) : nullptr;
   si.v0 = seg * seg_elems<E>();
   si.v1 = min(r.V, si.v0 + seg_elems<E>());
   const uintptr_t pb = (uintptr_t)(row + si.v0), pe = (uintptr_t)(row + si.v1);
@@ -288,7 +308,7 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
 }
 
 // statistics of segment blockIdx.y of listed row row_i, by the whole CTA
-template <typename E>
+template <typename E, bool kCopy>
 __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_t *rowlist,
                                              int row_i, float4 *partial) {
   const int seg = blockIdx.y;
@@ -299,12 +319,25 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
   StatState st{-INFINITY, 0.0f, 0ull, 0ull};
   const int nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
   const int ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
-  if (tid < nhead) stat1(load_elem<E>(row + si.v0 + tid), st, k);
-  if (tid < ntail) stat1(load_elem<E>((const E *)si.ae + tid), st, k);
+  // host-resident logits: every element read is also written to the row's
+  // device copy, which the accept walk and the sampler read instead
+  E *crow = kCopy ? (E *)si.copy : nullptr;
+  uint4 *cbody = kCopy ? (uint4 *)(si.copy + (si.ab - (uintptr_t)si.row)) : nullptr;
+  if (tid < nhead) {
+    const E x = __ldg(row + si.v0 + tid);
+    if (kCopy) crow[si.v0 + tid] = x;
+    stat1(elem_to_f32(x), st, k);
+  }
+  if (tid < ntail) {
+    const int v = (int)((si.ae - (uintptr_t)row) / sizeof(E)) + tid;
+    const E x = __ldg(row + v);
+    if (kCopy) crow[v] = x;
+    stat1(elem_to_f32(x), st, k);
+  }
   const uint4 *body = (const uint4 *)si.ab;
   const int nv = (int)((si.ae - si.ab) / 16);
   int i = tid;
-  if (r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
+  if (!kCopy && r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
     // full pattern: the second half through shared memory (each thread reads
     // back only the slots it copied, so its own wait is the only sync needed)
     __shared__ uint4 sbuf[kRsUnroll][kRsThreads];
@@ -326,9 +359,16 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
     uint4 buf[kRsUnroll];
 #pragma unroll
     for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
+    if (kCopy)
+#pragma unroll
+      for (int j = 0; j < kRsUnroll; ++j) cbody[i + j * kRsThreads] = buf[j];
     stat_batch<E>(buf, st, k);
   }
-  for (; i < nv; i += kRsThreads) stat_word<E>(ld_stream_v4(body + i), st, k);
+  for (; i < nv; i += kRsThreads) {
+    const uint4 w = ld_stream_v4(body + i);
+    if (kCopy) cbody[i] = w;
+    stat_word<E>(w, st, k);
+  }
 
   float a0, a1, a2, a3;
   f2_unpack(st.s01, a0, a1);
@@ -346,7 +386,7 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
   __syncthreads();  // red[] is reused by the CTA's next row
 }
 
-template <typename E>
+template <typename E, bool kCopy>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
 row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
@@ -355,7 +395,7 @@ row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
   // slots and a CTA takes a second listed row when the paths are deep
   const int nrows = rowlist ? *rowcount : (int)gridDim.x;
   for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
-    stat_segment<E>(r, G, rowlist, row_i, partial);
+    stat_segment<E, kCopy>(r, G, rowlist, row_i, partial);
 }
 
 Layout plan(int B, int maxpos, int V, bool tree) {
@@ -388,6 +428,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   } else {
     L.path = L.npos = L.tok = L.tstat = 0;
   }
+  L.end = off;
   L.total = off + 256;
   return L;
 }
@@ -451,7 +492,6 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     const int i = c * 32 + lane;
     if (i >= npos) break;
     const int d = r.tok[(size_t)b * r.tok_stride + i];  // issued first: x_d depends on it
-    const int node = round_node(r, b, i);
     float mxq, mkq, sq, mxp, mkp, sp;
     merge_slot(pb + (size_t)i * G, G, mxq, mkq, sq);
     merge_slot(pb + (size_t)(r.maxpos + 1 + i) * G, G, mxp, mkp, sp);
@@ -463,8 +503,8 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
       bad |= SV_ROW_BAD_TOKEN;
       continue;
     }
-    const E *vrow = (const E *)r.vlog + ((size_t)b * r.v_rows + node) * (size_t)r.V;
-    const E *drow = (const E *)r.dlog + ((size_t)b * r.d_rows + node) * (size_t)r.V;
+    const E *vrow = used_row<E>(r, b, i, src_row<E>(r, b, i));
+    const E *drow = used_row<E>(r, b, r.maxpos + 1 + i, src_row<E>(r, b, r.maxpos + 1 + i));
     const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
     // log2 q(d) + log2 sq and log2 p(d) + log2 sp, against the row references
     const float lq = fmaf(xq, k, -mkq), lp = fmaf(xp, k, -mkp);
@@ -531,8 +571,9 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     t.a = a;
     t.pad = 0;
     const int vi = a < npos ? a : npos;
-    t.vrow = b * r.v_rows + round_node(r, b, vi);
-    t.drow = a < npos ? b * r.d_rows + round_node(r, b, a) : -1;
+    t.rq = used_row<E>(r, b, vi, src_row<E>(r, b, vi));
+    t.rp = a < npos ? used_row<E>(r, b, r.maxpos + 1 + a, src_row<E>(r, b, r.maxpos + 1 + a))
+                    : nullptr;
     t.mq = bad ? 0.0f : mxv[vi];
     t.mp = (!bad && a < npos) ? mxd[a] : 0.0f;
     t.u24 = bad ? 0u : usm[vi];
@@ -741,9 +782,9 @@ struct RowPair {
 template <typename E>
 __device__ __forceinline__ RowPair row_pair(const Round &r, const Task &t) {
   RowPair p;
-  p.resid = t.drow >= 0;
-  const E *rq = (const E *)r.vlog + (size_t)t.vrow * r.V;
-  const E *rp = p.resid ? (const E *)r.dlog + (size_t)t.drow * r.V : rq;
+  p.resid = t.rp != nullptr;
+  const E *rq = (const E *)t.rq;
+  const E *rp = p.resid ? (const E *)t.rp : rq;
   p.rq = rq;
   p.rp = rp;
   p.mzq = __fmul_rn(t.mq, r.invT);
@@ -1083,7 +1124,9 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
     const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
     LaunchScope ls("row_stats", st);
-    s = check_launch("row_stats", launch_pdl(row_stats_kernel<E>, dim3(gx, (unsigned)G),
+    s = check_launch("row_stats", launch_pdl(r.copy ? row_stats_kernel<E, true>
+                                                    : row_stats_kernel<E, false>,
+                                             dim3(gx, (unsigned)G),
                                              dim3(kRsThreads), 0, st, r, G, rowlist,
                                              (const int *)(ws + L.ctr), partial));
     if (s != SV_OK) return s;
@@ -1154,6 +1197,27 @@ sv_status check_grid(int B, const Layout &L) {
   return SV_OK;
 }
 
+// Host-resident logits and a workspace with room for it: row_stats copies
+// every row slot it reads into the workspace (one slot per (sequence, slot),
+// pitch = the row rounded up to 16 bytes plus 16 for the source's offset
+// within 16 bytes), and the accept walk and the sampler read the copies, so
+// each row crosses the host link once.
+size_t row_copy_pitch(int V, sv_dtype dt) {
+  return align_up((size_t)V * (dt == SV_F32 ? 4 : 2), 16) + 16;
+}
+size_t row_copy_bytes(int B, const Layout &L, int V, sv_dtype dt) {
+  return (size_t)B * L.P * row_copy_pitch(V, dt);
+}
+void set_row_copy(Round &r, const Layout &L, char *ws, size_t workspace_bytes, int B,
+                  sv_dtype dt) {
+  r.copy = nullptr;
+  r.pitch = 0;
+  if (!r.stage && workspace_bytes >= L.total + row_copy_bytes(B, L, r.V, dt)) {
+    r.copy = ws + L.end;
+    r.pitch = row_copy_pitch(r.V, dt);
+  }
+}
+
 sv_status map_chain_args(const void *&vlogits, const void *&dlogits, const int32_t *&tokens,
                          int32_t *&out_tokens, int32_t *&out_accept_len, float *&out_q_prob,
                          float *&out_p_prob, float *&out_margin, uint32_t *&out_status) {
@@ -1177,6 +1241,12 @@ using namespace sv;
 extern "C" size_t sv_verify_chain_workspace(int B, int N, int V) {
   if (B < 0 || N < 0 || V < 1) return 0;
   return plan(B, N, V, false).total;
+}
+
+extern "C" size_t sv_verify_chain_workspace_host(int B, int N, int V, sv_dtype dt) {
+  if (B < 0 || N < 0 || V < 1 || (dt != SV_F32 && dt != SV_BF16)) return 0;
+  const Layout L = plan(B, N, V, false);
+  return L.total + row_copy_bytes(B, L, V, dt);
 }
 
 extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
@@ -1221,6 +1291,7 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   r.invT = 1.0f / temperature;
   r.k = r.invT * kLog2e;
   r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
+  set_row_copy(r, L, ws, workspace_bytes, B, dt);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
@@ -1230,6 +1301,13 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
 extern "C" size_t sv_verify_tree_workspace(int B, int T, int max_depth, int V) {
   if (B < 0 || T < 1 || max_depth < 0 || V < 1) return 0;
   return plan(B, max_depth, V, true).total;
+}
+
+extern "C" size_t sv_verify_tree_workspace_host(int B, int T, int max_depth, int V,
+                                                sv_dtype dt) {
+  if (B < 0 || T < 1 || max_depth < 0 || V < 1 || (dt != SV_F32 && dt != SV_BF16)) return 0;
+  const Layout L = plan(B, max_depth, V, true);
+  return L.total + row_copy_bytes(B, L, V, dt);
 }
 
 extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv_dtype dt,
@@ -1295,6 +1373,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   r.invT = 1.0f / temperature;
   r.k = r.invT * kLog2e;
   r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
+  set_row_copy(r, L, ws, workspace_bytes, B, dt);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
               out_path_nodes};
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)

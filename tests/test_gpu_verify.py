@@ -391,10 +391,19 @@ def test_host_resident_tree_inputs():
     host_args = [x.pin_memory() for x in (vq, dp, parent, token, score)]
     gd = sv.verify_tree(*dev_args, max_depth=cfg.depth, temperature=cfg.temperature, seed=5,
                         step=2)
+    # with the host-size workspace (rows copied to the device once) ...
     gh = sv.verify_tree(*host_args, max_depth=cfg.depth, temperature=cfg.temperature, seed=5,
                         step=2)
+    # ... and with the plain one (every step reads the host rows)
+    B, T, V = vq.shape
+    ws = torch.empty(sv.sv_verify_tree_workspace(B, T, cfg.depth, V), dtype=torch.uint8,
+                     device=DEV)
+    gp = sv.verify_tree(*host_args, max_depth=cfg.depth, temperature=cfg.temperature, seed=5,
+                        step=2, workspace=ws)
     torch.cuda.synchronize()
+    assert sv.sv_verify_tree_workspace_host(B, T, cfg.depth, V, vq.dtype) > ws.numel()
     _same(gd, gh)
+    _same(gd, gp)
     md, dd = sv.tree_build_mask(dev_args[2])
     mh, dh = sv.tree_build_mask(host_args[2])
     torch.cuda.synchronize()
@@ -408,12 +417,14 @@ def test_host_resident_chain_outputs():
     gd = sv.verify_chain(vq.to(DEV), dp.to(DEV), d.to(DEV), seed=3, step=1)
     hv, hd, ht = vq.pin_memory(), dp.pin_memory(), d.pin_memory()
     B, N = 6, 5
-    out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in gd.items()}
-    ws = torch.empty(sv.sv_verify_chain_workspace(B, N, 4097), dtype=torch.uint8, device=DEV)
-    sv.sv_verify_chain(hv, hd, ht, 1.0, 3, 1, out["tokens"], out["accept_len"], out["q_prob"],
-                       out["p_prob"], out["margin"], out["status"], ws)
-    torch.cuda.synchronize()
-    _same(gd, out)
+    for ws_bytes in (sv.sv_verify_chain_workspace(B, N, 4097),
+                     sv.sv_verify_chain_workspace_host(B, N, 4097, vq.dtype)):
+        out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in gd.items()}
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+        sv.sv_verify_chain(hv, hd, ht, 1.0, 3, 1, out["tokens"], out["accept_len"],
+                           out["q_prob"], out["p_prob"], out["margin"], out["status"], ws)
+        torch.cuda.synchronize()
+        _same(gd, out)
 
 
 def test_pageable_host_memory_refused():
