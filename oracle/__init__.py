@@ -73,6 +73,8 @@ def _declare(L):
     L.orc_residual.restype = None
     L.orc_invcdf_f64.argtypes = [_f64p, C.c_int, C.c_double]
     L.orc_invcdf_f64.restype = C.c_int
+    L.orc_argmax.argtypes = [_f32p, C.c_int]
+    L.orc_argmax.restype = C.c_int
     L.orc_exp32.argtypes = [C.c_float]
     L.orc_exp32.restype = C.c_float
     L.orc_sample_repro.argtypes = [_f32p, C.c_void_p, C.c_int, C.c_float, C.c_uint32,
@@ -153,6 +155,12 @@ def residual(q, p):
 def invcdf(w, t):
     w = np.ascontiguousarray(w, np.float64)
     return int(lib().orc_invcdf_f64(w, w.size, t))
+
+
+def argmax(x):
+    """Arg max of a row, ties to the lowest index (greedy verification)."""
+    x = _f32(x)
+    return int(lib().orc_argmax(x, x.size))
 
 
 def exp32(a):

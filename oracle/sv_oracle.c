@@ -304,6 +304,72 @@ int orc_sample_repro(const float *xq, const float *xp, int V, float invT,
  * seq_ids (optional) gives each row of the batch its sequence number in the
  * Philox counter, so that a subset of a batch can be replayed.
  * ---------------------------------------------------------------------- */
+/* ------------------------------------------------------------------------
+ * Greedy verification: the temperature -> 0 limit of the rule above.  Every
+ * softmax becomes the point mass at the row's arg max (ties: the lowest
+ * token id), so min(1, q(d)/p(d)) is 1 when d is the verifier's arg max and
+ * 0 otherwise, the residual (q - p)+ is the point mass at the verifier's arg
+ * max, and so is the bonus.  Only verifier rows are read: a draft token is
+ * accepted iff it equals the verifier row's arg max; the first mismatch
+ * emits that arg max and stops; full acceptance emits the arg max of the last
+ * verifier row.  q_prob = 1 or 0 (the limit of q(d)); p_prob, margins and
+ * gap are NaN (not defined in the limit).
+ * ---------------------------------------------------------------------- */
+int orc_argmax(const float *x, int V) {
+  int k = 0;
+  for (int v = 1; v < V; ++v)
+    if (x[v] > x[k]) k = v;
+  return k;
+}
+
+static int orc_verify_greedy(const float *vlog, int64_t v_bstride, int B, int V,
+                             const int32_t *path, int path_stride, const int32_t *npos_arr,
+                             const int32_t *tok, int tok_stride, int32_t *out_tokens,
+                             int out_stride, int32_t *out_accept, double *out_q, double *out_p,
+                             double *out_margin, int margin_stride, double *out_gap,
+                             uint32_t *out_status) {
+  for (int b = 0; b < B; ++b) {
+    const float *vb = vlog + (int64_t)b * v_bstride;
+    int npos = npos_arr[b];
+    const int32_t *pb = path ? path + (int64_t)b * path_stride : NULL;
+    const int32_t *tb = tok + (int64_t)b * tok_stride;
+    uint32_t status = 0;
+    int32_t *ot = out_tokens + (int64_t)b * out_stride;
+    for (int i = 0; i < out_stride; ++i) ot[i] = -1;
+    for (int i = 0; i < margin_stride; ++i) {
+      if (out_q) out_q[(int64_t)b * margin_stride + i] = NAN;
+      if (out_p) out_p[(int64_t)b * margin_stride + i] = NAN;
+    }
+    if (out_margin)
+      for (int i = 0; i <= margin_stride; ++i)
+        out_margin[(int64_t)b * (margin_stride + 1) + i] = NAN;
+    if (out_gap) out_gap[b] = NAN;
+    for (int i = 0; i <= npos; ++i) {
+      int r = pb ? pb[i] : i;
+      if (orc_row_bad(vb + (int64_t)r * V, V)) status |= ORC_ROW_NAN;
+      if (i < npos && (tb[i] < 0 || tb[i] >= V)) status |= ORC_ROW_BAD_TOKEN;
+    }
+    if (status) {
+      out_accept[b] = 0;
+      out_status[b] = status;
+      continue;
+    }
+    int a = npos;
+    for (int i = 0; i < npos; ++i) {
+      int r = pb ? pb[i] : i;
+      int k = orc_argmax(vb + (int64_t)r * V, V);
+      if (out_q) out_q[(int64_t)b * margin_stride + i] = (tb[i] == k) ? 1.0 : 0.0;
+      if (a == npos && tb[i] != k) a = i;
+    }
+    for (int i = 0; i < a; ++i) ot[i] = tb[i];
+    int r = pb ? pb[a] : a;
+    ot[a] = orc_argmax(vb + (int64_t)r * V, V);
+    out_accept[b] = a;
+    out_status[b] = 0;
+  }
+  return 0;
+}
+
 int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
                int64_t d_bstride, int B, int V, float T,
                const int32_t *path, int path_stride, const int32_t *npos_arr,
@@ -314,7 +380,11 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
                int32_t *out_accept, double *out_q, double *out_p,
                double *out_margin, int margin_stride, double *out_gap,
                uint32_t *out_status) {
-  if (B < 0 || V <= 0 || !(T > 0.0f)) return -1;
+  if (B < 0 || V <= 0 || !(T >= 0.0f)) return -1;
+  if (T == 0.0f)
+    return orc_verify_greedy(vlog, v_bstride, B, V, path, path_stride, npos_arr, tok,
+                             tok_stride, out_tokens, out_stride, out_accept, out_q, out_p,
+                             out_margin, margin_stride, out_gap, out_status);
   float invT = 1.0f / T;
   double Td = (double)T;
   for (int b = 0; b < B; ++b) {

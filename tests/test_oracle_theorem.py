@@ -160,3 +160,89 @@ def test_data_faults_set_status_and_stop():
     pz = xp.copy(); pz[0, 0, 4] = -np.inf
     r = oracle.verify_chain(xq, pz, np.array([[4, 1]]), seed=3)
     assert r["status"][0] & oracle.ROW_P_ZERO and r["accept_len"][0] >= 1
+
+
+# ---------------------------------------------------------------- greedy (T = 0)
+def _bf16_rows(rng, shape, sigma=3.0):
+    x = (rng.standard_normal(shape) * sigma).astype(np.float32)
+    return (x.view(np.uint32) & 0xFFFF0000).view(np.float32)  # exact bf16 values
+
+
+def test_greedy_matches_argmax_walk():
+    """Greedy verification = accept while the draft token is the verifier
+    row's arg max (numpy's first-occurrence arg max), then emit the arg max
+    of the row where the walk stopped."""
+    rng = np.random.default_rng(5)
+    B, N, V = 64, 5, 37
+    vq = _bf16_rows(rng, (B, N + 1, V))
+    dp = _bf16_rows(rng, (B, N, V))
+    am = vq.argmax(axis=-1)
+    # half of the drafts copy the verifier's arg max, so walks run long
+    d = np.where(rng.random((B, N)) < 0.7, am[:, :N], rng.integers(0, V, (B, N)))
+    o = oracle.verify_chain(vq, dp, d, T=0.0, seed=1, step=2)
+    for b in range(B):
+        a = next((i for i in range(N) if d[b, i] != am[b, i]), N)
+        assert o["accept_len"][b] == a
+        assert list(o["tokens"][b, :a]) == list(d[b, :a])
+        assert o["tokens"][b, a] == am[b, a]
+        assert np.all(o["tokens"][b, a + 1:] == -1)
+        assert np.array_equal(o["q_prob"][b], (d[b] == am[b, :N]).astype(float))
+        assert o["status"][b] == 0
+
+
+def test_greedy_is_the_low_temperature_limit():
+    """Drafts drawn at T -> 0 are the draft rows' arg maxes.  At T = 1e-3 with
+    a top-2 logit gap >= 1, every softmax is a point mass (exp(-1000)
+    underflows): p(d) = 1, so min(1, q(d)/p(d)) is 1 iff d is the verifier's
+    arg max, and the residual and the bonus are the verifier's arg max — the
+    stochastic rule reduces exactly to the greedy walk."""
+    rng = np.random.default_rng(6)
+    B, N, V = 48, 4, 29
+    vq = _bf16_rows(rng, (B, N + 1, V))
+    dp = _bf16_rows(rng, (B, N, V))
+    am = vq.argmax(axis=-1)
+    # 60% of the draft rows share the verifier's arg max
+    share = rng.random((B, N)) < 0.6
+    top = np.where(share, am[:, :N], dp.argmax(axis=-1))
+    np.put_along_axis(dp, top[..., None], dp.max(axis=-1, keepdims=True) + 2.0, -1)
+    k = vq.argmax(axis=-1)
+    np.put_along_axis(vq, k[..., None], vq.max(axis=-1, keepdims=True) + 2.0, -1)
+    d = dp.argmax(axis=-1).astype(np.int32)
+    g = oracle.verify_chain(vq, dp, d, T=0.0)
+    s = oracle.verify_chain(vq, dp, d, T=1e-3, seed=3, step=9)
+    assert np.array_equal(g["accept_len"], s["accept_len"])
+    assert np.array_equal(g["tokens"], s["tokens"])
+
+
+def test_greedy_ties_and_faults():
+    V = 8
+    vq = np.zeros((3, 2, V), np.float32)
+    vq[:, :, 5] = 1.0
+    vq[:, :, 2] = 1.0  # tie: the lowest token id wins
+    vq[1, 0, 3] = np.nan
+    d = np.array([[2], [2], [V]], np.int32)
+    o = oracle.verify_chain(vq, np.zeros((3, 1, V), np.float32), d, T=0.0)
+    assert o["accept_len"][0] == 1 and list(o["tokens"][0]) == [2, 2]
+    assert o["status"][1] == 1 and o["accept_len"][1] == 0  # NaN row
+    assert o["status"][2] == 2 and o["accept_len"][2] == 0  # token out of range
+    assert oracle.argmax(vq[0, 0]) == 2
+
+
+def test_greedy_tree_follows_best_path():
+    """Tree mode at T = 0: the walk along the best-scored path accepts while
+    each node's token is the arg max of its parent's verifier row."""
+    rng = np.random.default_rng(7)
+    T, V = 7, 19
+    parent = np.array([-1, 0, 0, 1, 1, 2, 3], np.int32)
+    score = np.array([1.0, 0.6, 0.3, 0.5, 0.1, 0.2, 0.4], np.float32)
+    path = [0, 1, 3, 6]
+    vq = _bf16_rows(rng, (1, T, V))
+    dp = _bf16_rows(rng, (1, T, V))
+    token = rng.integers(0, V, (1, T)).astype(np.int32)
+    token[0, 1] = vq[0, 0].argmax()  # node 1 accepted
+    token[0, 3] = vq[0, 1].argmax()  # node 3 accepted
+    token[0, 6] = (vq[0, 3].argmax() + 1) % V  # node 6 rejected
+    o = oracle.verify_tree(vq, dp, parent[None], token, score[None], 3, T=0.0)
+    assert list(o["path"][0]) == [0, 1, 3, -1]
+    assert o["accept_len"][0] == 2
+    assert list(o["tokens"][0]) == [token[0, 1], token[0, 3], vq[0, 3].argmax(), -1]
