@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences the oracle times")
+    ap.add_argument("--greedy", action="store_true",
+                    help="temperature 0: greedy verification (verifier rows only, no sampling)")
     ap.add_argument("--batch", type=int, default=0,
                     help="per-GPU batch override (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -220,6 +222,7 @@ class Workload:
         import torch
         from speculative_decoding_verification_vocab_gb300 import synth
         self.cfg = cfg
+        self.greedy = False
         self.rounds = []
         self.tree = cfg.kind.startswith("tree")
         for r in range(pool):
@@ -250,8 +253,11 @@ class Workload:
         return self.B * self.T
 
     def stats_bytes(self, r):
+        """Logit bytes the row pass reads: verifier and draft rows along the
+        path (2D+1 per sequence), or the verifier rows alone when greedy."""
         d = self.rounds[r]["depth"]
-        return int(((2 * d + 1) * self.V * self.esize).sum())
+        rows = d + 1 if self.greedy else 2 * d + 1
+        return int((rows * self.V * self.esize).sum())
 
 
 def run_round(sv, wl, cfg, maxd, src, out, i, seed, step_no, ws, stream, side, ev_fork, ev_acc):
@@ -297,11 +303,14 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     sv.load_library()
     cfg = synth.CONFIGS[args.config]
+    import dataclasses
     if args.batch:
-        import dataclasses
         cfg = dataclasses.replace(cfg, B=args.batch)
     _, B = shard_batch(cfg.B, rank, world)
-    wl = Workload(cfg, args.pool, dev, rank)
+    wl = Workload(cfg, args.pool, dev, rank)  # inputs drawn at the configuration's T
+    if args.greedy:  # then verified at T = 0
+        cfg = dataclasses.replace(cfg, temperature=0.0)
+        wl.greedy = True
     K, W = args.steps, args.warmup
     T, V = wl.T, wl.V
     maxd = cfg.depth if wl.tree else cfg.N
@@ -384,14 +393,15 @@ def run_ours(args):
     total_tokens = sum_over_ranks(tokens, world)
 
     peak, peak_kind = measured_peaks()
-    rs_launches, rs_ms = trace.get("row_stats", (0, 0.0))
+    rs_name = "row_argmax" if cfg.temperature == 0.0 else "row_stats"
+    rs_launches, rs_ms = trace.get(rs_name, (0, 0.0))
     rs_bytes_per_launch = stats_bytes / K
     rs_avg_ms = rs_ms / max(rs_launches, 1)
     achieved = rs_bytes_per_launch / (rs_avg_ms / 1e3) / 1e9 if rs_launches else None
-    roofline = {"kernel": "row_stats", "bound": "hbm", "achieved": achieved, "peak": peak,
+    roofline = {"kernel": rs_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                 "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
-                "traffic": recorded_traffic("row_stats", cfg.name),
+                "traffic": recorded_traffic(rs_name, cfg.name),
                 "alg_bytes_per_launch": rs_bytes_per_launch, "avg_launch_ms": rs_avg_ms}
 
     line = {
@@ -399,7 +409,7 @@ def run_ours(args):
         "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype.__repr__().endswith("bfloat16") else "f32",
         "data": "synthetic",
-        "config": {"workload": f"config {cfg.index}: {cfg.name}", "B_per_gpu": B, "T": T, "V": V,
+        "config": {"workload": f"config {cfg.index}: {cfg.name}" + (" (greedy, T=0)" if wl.greedy else ""), "B_per_gpu": B, "T": T, "V": V,
                    "max_depth": maxd, "logits": str(cfg.dtype).replace("torch.", ""),
                    "kv": f"{kvb.L} layers x {kvb.H} kv heads x {kvb.D}, bf16",
                    "pool_rounds": args.pool,

@@ -96,7 +96,15 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *                position i, i.e. over the token that follows it)
  *   dlogits      [B][N][V]   draft logits (may be NULL when N == 0)
  *   draft_tokens [B][N] int32
- *   temperature  > 0, finite.  Probabilities are softmax(logits / T).
+ *   temperature  >= 0, finite.  Probabilities are softmax(logits / T).
+ *                T = 0 is greedy verification, the T -> 0 limit of the rule
+ *                (every softmax a point mass at the row's arg max, ties to
+ *                the lowest token id): a draft token is accepted iff it is
+ *                the verifier row's arg max, the first mismatch emits that
+ *                arg max, full acceptance emits the last row's arg max.  Only
+ *                verifier rows are read and nothing is sampled; out_q_prob
+ *                holds 1 or 0, out_p_prob and out_margin NaN.  The same
+ *                holds for sv_verify_tree along the best path.
  * Outputs (device, caller-owned):
  *   out_tokens     [B][N+1]  accepted drafts then the correction/bonus token;
  *                            -1 after it.  emitted = out_accept_len + 1.

@@ -181,6 +181,13 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
   return r;
 }
 
+// max of two bf16 pairs, NaN-propagating
+__device__ __forceinline__ uint32_t bf2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

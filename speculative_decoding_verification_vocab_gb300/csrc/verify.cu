@@ -584,6 +584,229 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
 }
 
 // ---------------------------------------------------------------------------
+// Greedy verification (temperature 0): the T -> 0 limit of the accept rule.
+// row_argmax: per (verifier row, segment) the maximum, its lowest index and
+// fault flags; decide_greedy: one warp per sequence accepts while the draft
+// token is the row's arg max and emits the arg max where the walk stops.
+// Only verifier rows are read; nothing is sampled.
+constexpr uint32_t kArgNan = 1u;   // a NaN or +inf logit
+constexpr uint32_t kArgSeen = 2u;  // a logit above -inf
+
+struct ArgState {
+  float best;  // running maximum (NaN ignored)
+  int idx;     // lowest index holding it
+  uint32_t flags;
+};
+
+__device__ __forceinline__ void arg1(ArgState &a, float x, int v) {
+  if (x > a.best) {
+    a.best = x;
+    a.idx = v;
+  }
+  if (x != x || x == INFINITY) a.flags |= kArgNan;
+  if (x > -INFINITY) a.flags |= kArgSeen;
+}
+// (best, idx) pairs: larger value wins, equal values go to the lower index
+__device__ __forceinline__ void arg_merge(ArgState &a, float best, int idx, uint32_t flags) {
+  if (best > a.best || (best == a.best && idx < a.idx)) {
+    a.best = best;
+    a.idx = idx;
+  }
+  a.flags |= flags;
+}
+
+// one 16-byte word of logits starting at element v; the word's maximum is
+// taken on packed pairs first and the elements are scanned only when it
+// beats the running maximum (in index order, so the lowest index is kept)
+template <typename E>
+__device__ __forceinline__ void arg_word(ArgState &a, uint4 w, int v);
+template <>
+__device__ __forceinline__ void arg_word<uint16_t>(ArgState &a, uint4 w, int v) {
+  const uint32_t m = bf2_max(bf2_max(w.x, w.y), bf2_max(w.z, w.w));
+  const uint32_t mn = bf2_max_nan(bf2_max_nan(w.x, w.y), bf2_max_nan(w.z, w.w));
+  const float wm = fmaxf(bf16_lo(m), bf16_hi(m));
+  const float n0 = bf16_lo(mn), n1 = bf16_hi(mn);  // NaN in either half: a NaN element
+  if (n0 != n0 || n1 != n1 || wm == INFINITY) a.flags |= kArgNan;
+  if (wm > -INFINITY) a.flags |= kArgSeen;
+  if (wm > a.best) {
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    int k = 7;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      const float x = (j & 1) ? bf16_hi(q[j >> 1]) : bf16_lo(q[j >> 1]);
+      if (x == wm) k = j;
+    }
+    a.best = wm;
+    a.idx = v + k;
+  }
+}
+template <>
+__device__ __forceinline__ void arg_word<float>(ArgState &a, uint4 w, int v) {
+  const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                      __uint_as_float(w.w)};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) arg1(a, x[j], v + j);
+}
+
+template <typename E>
+__device__ __forceinline__ void argmax_segment(const Round &r, int G, const int32_t *rowlist,
+                                               int row_i, float4 *partial) {
+  const int seg = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg);
+  const E *row = (const E *)si.row;
+  ArgState a{-INFINITY, 0x7fffffff, 0u};
+  const int nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
+  const int ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
+  const int vbody = si.v0 + nhead;  // element index of the body's first word
+  if (tid < nhead) arg1(a, load_elem<E>(row + si.v0 + tid), si.v0 + tid);
+  const uint4 *body = (const uint4 *)si.ab;
+  const int nv = (int)((si.ae - si.ab) / 16);
+  constexpr int kPer = 16 / (int)sizeof(E);
+  int i = tid;
+  if (r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
+    // as row_stats: the second half of the thread's words through shared
+    // memory; words are still taken in increasing index order
+    __shared__ uint4 sbuf[kRsUnroll][kRsThreads];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j)
+      cp_async16(&sbuf[j][tid], body + i + (kRsUnroll + j) * kRsThreads);
+    cp_async_commit();
+    uint4 buf[kRsUnroll];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) arg_word<E>(a, buf[j], vbody + (i + j * kRsThreads) * kPer);
+    cp_async_wait_all();
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j)
+      arg_word<E>(a, sbuf[j][tid], vbody + (i + (kRsUnroll + j) * kRsThreads) * kPer);
+    i += 2 * kRsUnroll * kRsThreads;
+  }
+  for (; i + (kRsUnroll - 1) * kRsThreads < nv; i += kRsUnroll * kRsThreads) {
+    uint4 buf[kRsUnroll];
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j) arg_word<E>(a, buf[j], vbody + (i + j * kRsThreads) * kPer);
+  }
+  for (; i < nv; i += kRsThreads) arg_word<E>(a, ld_stream_v4(body + i), vbody + i * kPer);
+  if (tid < ntail) arg1(a, load_elem<E>((const E *)si.ae + tid), vbody + nv * kPer + tid);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, a.best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, a.idx, o);
+    const uint32_t of = __shfl_xor_sync(0xffffffffu, a.flags, o);
+    arg_merge(a, ob, oi, of);
+  }
+  __shared__ float4 red[kRsThreads / 32];
+  if (lane == 0) red[warp] = make_float4(a.best, __int_as_float(a.idx), __uint_as_float(a.flags), 0.f);
+  __syncthreads();
+  if (warp == 0) {
+    const float4 v = lane < kRsThreads / 32 ? red[lane]
+                                            : make_float4(-INFINITY, __int_as_float(0x7fffffff),
+                                                          0.0f, 0.0f);
+    ArgState c{v.x, __float_as_int(v.y), __float_as_uint(v.z)};
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, c.best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, c.idx, o);
+      const uint32_t of = __shfl_xor_sync(0xffffffffu, c.flags, o);
+      arg_merge(c, ob, oi, of);
+    }
+    if (lane == 0)
+      partial[si.out] = make_float4(c.best, __int_as_float(c.idx), __uint_as_float(c.flags), 0.f);
+  }
+  __syncthreads();  // red[] is reused by the CTA's next row
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+row_argmax_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+  grid_dep_sync();
+  const int nrows = rowlist ? *rowcount : (int)gridDim.x;
+  for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
+    argmax_segment<E>(r, G, rowlist, row_i, partial);
+}
+
+// arg max of verifier row slot j of sequence b from its G segment partials
+__device__ __forceinline__ ArgState merge_arg(const float4 *part, int G) {
+  ArgState a{-INFINITY, 0x7fffffff, 0u};
+  for (int g = 0; g < G; ++g) {
+    const float4 v = part[g];
+    arg_merge(a, v.x, __float_as_int(v.y), __float_as_uint(v.z));
+  }
+  return a;
+}
+__device__ __forceinline__ bool arg_bad(const ArgState &a) {
+  return (a.flags & kArgNan) || !(a.flags & kArgSeen);
+}
+
+__global__ void __launch_bounds__(kDecideWarps * 32)
+decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideOut o) {
+  grid_dep_sync();
+  const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= r.B) return;
+  const unsigned FULL = 0xffffffffu;
+  const int npos = round_npos(r, b);
+  const uint32_t tree_bad = r.tstat ? r.tstat[b] : 0u;
+  const float4 *pb = partial + (size_t)b * r.P * G;
+  extern __shared__ int am_sm[];  // per warp: arg max of row slot j, j <= maxpos
+  int *am = am_sm + (threadIdx.x >> 5) * (r.maxpos + 1);
+  uint32_t bad = 0, rej_bits = 0;
+  if (lane == 0 && !tree_bad) {
+    const ArgState a = merge_arg(pb + (size_t)npos * G, G);
+    if (arg_bad(a)) bad |= SV_ROW_NAN;
+    am[npos] = a.idx;
+  }
+  const int nchunks = (npos + 31) / 32;
+  for (int c = 0; c < nchunks && !tree_bad; ++c) {
+    const int i = c * 32 + lane;
+    if (i >= npos) break;
+    const int d = r.tok[(size_t)b * r.tok_stride + i];
+    const ArgState a = merge_arg(pb + (size_t)i * G, G);
+    am[i] = a.idx;
+    if (arg_bad(a)) bad |= SV_ROW_NAN;
+    if (d < 0 || d >= r.V) bad |= SV_ROW_BAD_TOKEN;
+    if (d != a.idx) rej_bits |= 1u << c;
+    if (o.q_prob) o.q_prob[(size_t)b * r.maxpos + i] = (d == a.idx) ? 1.0f : 0.0f;
+  }
+  bad = __reduce_or_sync(FULL, bad);
+  if (tree_bad) bad = SV_ROW_BAD_TREE;
+  int a = npos;
+  for (int c = 0; c < nchunks; ++c) {
+    const int i = c * 32 + lane;
+    const unsigned rej = __ballot_sync(FULL, i < npos && ((rej_bits >> c) & 1u));
+    if (rej) {
+      a = c * 32 + __ffs(rej) - 1;
+      break;
+    }
+  }
+  if (bad) a = 0;
+  __syncwarp();
+  const int W = r.maxpos + 1;
+  for (int i = lane; i < W; i += 32) {
+    int32_t t = -1;
+    if (!bad && i < a) t = r.tok[(size_t)b * r.tok_stride + i];
+    if (!bad && i == a) t = am[a];
+    o.tokens[(size_t)b * W + i] = t;
+    if (o.path_out)
+      o.path_out[(size_t)b * W + i] = (i == 0) ? 0 : ((!bad && i <= a) ? round_node(r, b, i) : -1);
+    if (i < r.maxpos) {
+      if (o.p_prob) o.p_prob[(size_t)b * r.maxpos + i] = NAN;
+      if (o.q_prob && (i >= npos || bad)) o.q_prob[(size_t)b * r.maxpos + i] = NAN;
+    }
+    if (o.margin) o.margin[(size_t)b * W + i] = NAN;
+  }
+  if (lane == 0) {
+    o.accept_len[b] = a;
+    o.status[b] = bad;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The sampling arithmetic (fixed sequence of IEEE fp32 operations + exact
 // 64-bit fixed point), shared by specification with the CPU oracle:
 //   z = fl(x * invT); e = exp32_repro(fl(z - max z)); S_e = sum floor(e 2^40)
@@ -1033,7 +1256,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
                  const float *__restrict__ score, int B, int T, int max_depth,
                  int32_t *__restrict__ path, int32_t *__restrict__ npos,
                  int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
-                 int32_t *__restrict__ rowlist, int *__restrict__ rowcount) {
+                 int32_t *__restrict__ rowlist, int *__restrict__ rowcount, int greedy) {
   grid_dep_sync();
   const int b = blockIdx.x, lane = threadIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
@@ -1103,10 +1326,12 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   if (lane == 0) {
     npos[b] = D;
     tstat[b] = 0u;
-    base = atomicAdd(rowcount, 2 * D + 1);
+    base = atomicAdd(rowcount, greedy ? D + 1 : 2 * D + 1);
   }
   base = __shfl_sync(0xffffffffu, base, 0);
-  for (int a = lane; a < 2 * D + 1; a += 32) rowlist[base + a] = (b << 12) | a;
+  // the verifier rows n_0..n_D, then (stochastic rule) the draft rows
+  const int nrow = greedy ? D + 1 : 2 * D + 1;
+  for (int a = lane; a < nrow; a += 32) rowlist[base + a] = (b << 12) | a;
 }
 
 // ---------------------------------------------------------------------------
@@ -1173,6 +1398,36 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   return SV_OK;
 }
 
+template <typename E>
+sv_status run_verify_greedy(const Round &r, const Layout &L, char *ws, const DecideOut &o,
+                            cudaStream_t st, cudaEvent_t accept_event) {
+  float4 *partial = (float4 *)(ws + L.partial);
+  const int G = (r.V + seg_elems<E>() - 1) / seg_elems<E>();
+  sv_status s;
+  {
+    const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
+    const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
+    LaunchScope ls("row_argmax", st);
+    s = check_launch("row_argmax", launch_pdl(row_argmax_kernel<E>, dim3(gx, (unsigned)G),
+                                              dim3(kRsThreads), 0, st, r, G, rowlist,
+                                              (const int *)(ws + L.ctr), partial));
+    if (s != SV_OK) return s;
+  }
+  {
+    const size_t dsm = (size_t)kDecideWarps * (r.maxpos + 1) * sizeof(int);
+    LaunchScope ls("decide_greedy", st);
+    s = check_launch("decide_greedy",
+                     launch_pdl(decide_greedy_kernel, dim3((r.B + kDecideWarps - 1) / kDecideWarps),
+                                dim3(kDecideWarps * 32), dsm, st, r, G, partial, o));
+    if (s != SV_OK) return s;
+  }
+  if (accept_event) {
+    const cudaError_t e = cudaEventRecord(accept_event, st);
+    if (e != cudaSuccess) return set_error(SV_ERR_CUDA, "accept_event: %s", cudaGetErrorString(e));
+  }
+  return SV_OK;
+}
+
 sv_status check_common(const void *vlogits, sv_dtype dt, int B, int V, float temperature,
                        const void *out_tokens, const void *out_accept, const void *out_status,
                        const void *workspace) {
@@ -1180,8 +1435,8 @@ sv_status check_common(const void *vlogits, sv_dtype dt, int B, int V, float tem
   if (V < 1) return set_error(SV_ERR_INVALID_ARG, "V must be >= 1 (got %d)", V);
   if (V > SV_MAX_VOCAB) return set_error(SV_ERR_UNSUPPORTED, "V > %d", SV_MAX_VOCAB);
   if (dt != SV_F32 && dt != SV_BF16) return set_error(SV_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
-  if (!(temperature > 0.0f) || !isfinite(temperature))
-    return set_error(SV_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (!(temperature >= 0.0f) || !isfinite(temperature))
+    return set_error(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0 (0 = greedy)");
   if (B == 0) return SV_OK;
   if (!vlogits || !out_tokens || !out_accept || !out_status || !workspace)
     return set_error(SV_ERR_INVALID_ARG, "null pointer argument");
@@ -1288,12 +1543,18 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
   r.tok = draft_tokens;
   r.tok_stride = N;
   r.tstat = nullptr;
-  r.invT = 1.0f / temperature;
+  r.invT = temperature > 0.0f ? 1.0f / temperature : 0.0f;
   r.k = r.invT * kLog2e;
   r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
   set_row_copy(r, L, ws, workspace_bytes, B, dt);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
+  if (temperature == 0.0f) {  // greedy: verifier rows only, nothing sampled
+    r.P = N + 1;
+    r.copy = nullptr;
+    return dt == SV_BF16 ? run_verify_greedy<uint16_t>(r, L, ws, o, st, (cudaEvent_t)accept_event)
+                         : run_verify_greedy<float>(r, L, ws, o, st, (cudaEvent_t)accept_event);
+  }
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
                        : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event);
 }
@@ -1353,7 +1614,8 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
     s = check_launch("tree_path",
                      launch_pdl(tree_path_kernel, dim3(B), dim3(32), 0, st, parent, token, score,
                                 B, T, max_depth, path, npos, tok, max_depth > 0 ? max_depth : 1,
-                                tstat, (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr)));
+                                tstat, (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr),
+                                temperature == 0.0f ? 1 : 0));
     if (s != SV_OK) return s;
   }
   Round r;
@@ -1370,12 +1632,18 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   r.tok = tok;
   r.tok_stride = max_depth > 0 ? max_depth : 1;
   r.tstat = tstat;
-  r.invT = 1.0f / temperature;
+  r.invT = temperature > 0.0f ? 1.0f / temperature : 0.0f;
   r.k = r.invT * kLog2e;
   r.stage = is_device_memory(r.vlog) && is_device_memory(r.dlog);
   set_row_copy(r, L, ws, workspace_bytes, B, dt);
   DecideOut o{out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin, out_status,
               out_path_nodes};
+  if (temperature == 0.0f) {  // greedy: the path's verifier rows only, nothing sampled
+    r.P = max_depth + 1;
+    r.copy = nullptr;
+    return dt == SV_BF16 ? run_verify_greedy<uint16_t>(r, L, ws, o, st, (cudaEvent_t)accept_event)
+                         : run_verify_greedy<float>(r, L, ws, o, st, (cudaEvent_t)accept_event);
+  }
   return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
                        : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event);
 }

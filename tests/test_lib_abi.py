@@ -51,7 +51,7 @@ def test_host_argument_checks_need_no_gpu(lib):
                                null, null, null, 0, null, null) == 1
     assert lib.sv_verify_chain(null, null, 7, null, 1, 2, 10, 1.0, 0, 0, null, null, null, null,
                                null, null, null, 0, null, null) == 1
-    assert lib.sv_verify_chain(null, null, 0, null, 1, 2, 10, 0.0, 0, 0, null, null, null, null,
+    assert lib.sv_verify_chain(null, null, 0, null, 1, 2, 10, -0.5, 0, 0, null, null, null, null,
                                null, null, null, 0, null, null) == 1
     assert b"temperature" in lib.sv_last_error()
     assert lib.sv_verify_chain(null, null, 0, null, 1, 2, (1 << 22) + 1, 1.0, 0, 0, null, null,
