@@ -73,6 +73,11 @@ def _declare(L):
     L.orc_residual.restype = None
     L.orc_invcdf_f64.argtypes = [_f64p, C.c_int, C.c_double]
     L.orc_invcdf_f64.restype = C.c_int
+    L.orc_tree_expand.argtypes = [_f32p, C.c_int, C.c_int, C.c_float, _f32p, C.c_int,
+                                  _i32p, _f64p]
+    L.orc_tree_select.argtypes = [_f32p, _i32p, C.c_int, C.c_int, C.c_int, _i32p]
+    L.orc_tree_finalize.argtypes = [_i32p, _i32p, _f32p, _i32p, C.c_int, C.c_int, C.c_int,
+                                    _i32p, _i32p, _f32p]
     L.orc_argmax.argtypes = [_f32p, C.c_int]
     L.orc_argmax.restype = C.c_int
     L.orc_exp32.argtypes = [C.c_float]
@@ -155,6 +160,45 @@ def residual(q, p):
 def invcdf(w, t):
     w = np.ascontiguousarray(w, np.float64)
     return int(lib().orc_invcdf_f64(w, w.size, t))
+
+
+def tree_expand(dlogits, fscore, K, T=1.0):
+    """Per frontier row ([..., V] logits, [...] path scores): the K tokens with
+    the largest logits (ties to the lower id) and their child scores.
+    Returns (tokens [..., K] int32, scores [..., K] float64)."""
+    x = _f32(dlogits)
+    V = x.shape[-1]
+    lead = x.shape[:-1]
+    R = int(np.prod(lead)) if lead else 1
+    fs = _f32(fscore).reshape(-1)
+    tok = np.empty(R * K, np.int32)
+    sc = np.empty(R * K, np.float64)
+    rc = lib().orc_tree_expand(x.reshape(-1), R, V, float(T), fs, K, tok, sc)
+    assert rc == 0
+    return tok.reshape(lead + (K,)), sc.reshape(lead + (K,))
+
+
+def tree_select(score, token, K):
+    """Per sequence ([B][C]) the indices of the K best candidates."""
+    s, t = _f32(score), _i32(token)
+    B, Cn = s.shape
+    out = np.empty((B, K), np.int32)
+    assert lib().orc_tree_select(s.reshape(-1), t.reshape(-1), B, Cn, K, out.reshape(-1)) == 0
+    return out
+
+
+def tree_finalize(cparent, ctoken, cscore, clevel, Tn):
+    """Per sequence ([B][C] candidates) the Tn-slot tree: parent, token, score."""
+    cp, ct, cl = _i32(cparent), _i32(ctoken), _i32(clevel)
+    cs = _f32(cscore)
+    B, Cn = cp.shape
+    parent = np.empty((B, Tn), np.int32)
+    token = np.empty((B, Tn), np.int32)
+    score = np.empty((B, Tn), np.float32)
+    assert lib().orc_tree_finalize(cp.reshape(-1), ct.reshape(-1), cs.reshape(-1),
+                                   cl.reshape(-1), B, Cn, Tn, parent.reshape(-1),
+                                   token.reshape(-1), score.reshape(-1)) == 0
+    return parent, token, score
 
 
 def argmax(x):

@@ -665,3 +665,148 @@ double orc_expected_tokens(double alpha, int N) {
 double orc_speedup(double alpha, int N, double c) {
   return orc_expected_tokens(alpha, N) / ((double)N * c + 1.0);
 }
+
+/* ------------------------------------------------------------------------
+ * Dynamic draft tree (EAGLE-2; [Blog] section 5, "三代之间的变化": the tree
+ * grows where the draft is confident -- a node's score is the product of the
+ * draft probabilities along its path, the best-scored nodes are expanded,
+ * and the tree is pruned to a node budget).  Three steps, called per level
+ * by the caller that runs the draft model:
+ *
+ * expand:   for each frontier row (a draft logit row and the path score of
+ *           the node it belongs to) the K tokens with the largest logits
+ *           (equal logits in ascending token id) and their child scores
+ *           = frontier score * softmax(x / T)[token] (T = 0: 1 for the
+ *           first arg max, 0 for the others).  A row with a NaN or +inf
+ *           logit, or all -inf, proposes nothing: tokens -1, scores -inf.
+ * select:   per sequence the K best candidates of a level, by score, equal
+ *           scores in ascending candidate index; candidates with token -1
+ *           are never chosen; missing picks are -1.
+ * finalize: per sequence the T best candidates overall (score descending,
+ *           then level ascending, then index ascending; candidate 0 is the
+ *           root), numbered level by level (score descending, index
+ *           ascending within a level); a kept node's parent is the slot of
+ *           its parent candidate (-1 for the root; -2 if that candidate was
+ *           not kept, which cannot happen when child scores never exceed
+ *           their parent's); unused slots get parent -2, token -1, score 0.
+ * ---------------------------------------------------------------------- */
+int orc_tree_expand(const float *dlog, int R, int V, float T, const float *fscore, int K,
+                    int32_t *out_tok, double *out_score) {
+  if (R < 0 || V < 1 || K < 1 || K > V || !(T >= 0.0f)) return -1;
+  double *prob = (double *)malloc(sizeof(double) * (size_t)V);
+  uint8_t *taken = (uint8_t *)malloc((size_t)V);
+  for (int r = 0; r < R; ++r) {
+    const float *x = dlog + (int64_t)r * V;
+    int32_t *ot = out_tok + (int64_t)r * K;
+    double *os = out_score + (int64_t)r * K;
+    if (orc_row_bad(x, V)) {
+      for (int k = 0; k < K; ++k) {
+        ot[k] = -1;
+        os[k] = -INFINITY;
+      }
+      continue;
+    }
+    int am = orc_argmax(x, V);
+    if (T > 0.0f) orc_softmax(x, V, (double)T, prob);
+    memset(taken, 0, (size_t)V);
+    for (int k = 0; k < K; ++k) {
+      int best = -1;
+      for (int v = 0; v < V; ++v)
+        if (!taken[v] && (best < 0 || x[v] > x[best])) best = v;
+      taken[best] = 1;
+      ot[k] = best;
+      double p = T > 0.0f ? prob[best] : (best == am ? 1.0 : 0.0);
+      os[k] = (double)fscore[r] * p;
+    }
+  }
+  free(prob);
+  free(taken);
+  return 0;
+}
+
+int orc_tree_select(const float *score, const int32_t *token, int B, int C, int K,
+                    int32_t *out_idx) {
+  if (B < 0 || C < 1 || K < 1) return -1;
+  uint8_t *taken = (uint8_t *)malloc((size_t)C);
+  for (int b = 0; b < B; ++b) {
+    const float *s = score + (int64_t)b * C;
+    const int32_t *t = token + (int64_t)b * C;
+    memset(taken, 0, (size_t)C);
+    for (int k = 0; k < K; ++k) {
+      int best = -1;
+      for (int c = 0; c < C; ++c)
+        if (!taken[c] && t[c] >= 0 && (best < 0 || s[c] > s[best])) best = c;
+      out_idx[(int64_t)b * K + k] = best;
+      if (best >= 0) taken[best] = 1;
+    }
+  }
+  free(taken);
+  return 0;
+}
+
+/* a before b in the keep order: score desc, level asc, index asc */
+static int orc_keep_before(const float *s, const int32_t *lv, int a, int b) {
+  if (s[a] != s[b]) return s[a] > s[b];
+  if (lv[a] != lv[b]) return lv[a] < lv[b];
+  return a < b;
+}
+/* a before b in the slot order: level asc, score desc, index asc */
+static int orc_slot_before(const float *s, const int32_t *lv, int a, int b) {
+  if (lv[a] != lv[b]) return lv[a] < lv[b];
+  if (s[a] != s[b]) return s[a] > s[b];
+  return a < b;
+}
+
+int orc_tree_finalize(const int32_t *cparent, const int32_t *ctoken, const float *cscore,
+                      const int32_t *clevel, int B, int C, int Tn, int32_t *parent,
+                      int32_t *token, float *score) {
+  if (B < 0 || C < 1 || Tn < 1) return -1;
+  int *keep = (int *)malloc(sizeof(int) * (size_t)Tn);
+  int *slot = (int *)malloc(sizeof(int) * (size_t)C);
+  uint8_t *taken = (uint8_t *)malloc((size_t)C);
+  for (int b = 0; b < B; ++b) {
+    const int32_t *cp = cparent + (int64_t)b * C, *ct = ctoken + (int64_t)b * C;
+    const int32_t *cl = clevel + (int64_t)b * C;
+    const float *cs = cscore + (int64_t)b * C;
+    memset(taken, 0, (size_t)C);
+    int n = 0;
+    for (; n < Tn; ++n) { /* selection of the keep set, one pick at a time */
+      int best = -1;
+      for (int c = 0; c < C; ++c)
+        if (!taken[c] && (c == 0 || ct[c] >= 0) && (best < 0 || orc_keep_before(cs, cl, c, best)))
+          best = c;
+      if (best < 0) break;
+      taken[best] = 1;
+      keep[n] = best;
+    }
+    /* slot order among the kept: insertion sort */
+    for (int i = 1; i < n; ++i) {
+      int v = keep[i], j = i - 1;
+      while (j >= 0 && orc_slot_before(cs, cl, v, keep[j])) {
+        keep[j + 1] = keep[j];
+        --j;
+      }
+      keep[j + 1] = v;
+    }
+    for (int c = 0; c < C; ++c) slot[c] = -1;
+    for (int i = 0; i < n; ++i) slot[keep[i]] = i;
+    int32_t *op = parent + (int64_t)b * Tn, *otk = token + (int64_t)b * Tn;
+    float *os = score + (int64_t)b * Tn;
+    for (int i = 0; i < Tn; ++i) {
+      if (i >= n) {
+        op[i] = -2;
+        otk[i] = -1;
+        os[i] = 0.0f;
+        continue;
+      }
+      int c = keep[i];
+      op[i] = cp[c] < 0 ? -1 : (slot[cp[c]] >= 0 ? slot[cp[c]] : -2);
+      otk[i] = ct[c];
+      os[i] = cs[c];
+    }
+  }
+  free(keep);
+  free(slot);
+  free(taken);
+  return 0;
+}
