@@ -249,6 +249,50 @@ sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dlogits,
                                   float *out_margin, uint32_t *out_status,
                                   void *stream, void *accept_event);
 
+/* ---------------------------------------------------------------------------
+ * Dynamic draft tree (EAGLE-2).  [Blog] section 5 (三代之间的变化): the tree
+ * grows where the draft is confident; a node's score is the product of the
+ * draft probabilities along its path; the best-scored nodes are expanded and
+ * the tree is pruned to a node budget.  The caller runs the draft model level
+ * by level and calls, per level, sv_tree_expand on the frontier's draft rows
+ * and sv_tree_select on the level's candidates; sv_tree_finalize turns all
+ * candidates into the [B][T] parent / token / score arrays of sv_verify_tree.
+ *
+ * sv_tree_expand -- per frontier row (dlogits [B][F][V], sv_dtype dt; the
+ * path score of the node it belongs to in frontier_score [B][F]) the K
+ * tokens with the largest logits, equal logits in ascending token id
+ * (out_token [B][F][K], descending), and their child scores
+ * frontier_score * softmax(x / T)[token] (out_score [B][F][K], fp32).
+ * T = 0: probability 1 for the first arg max, 0 for the others.  A row with
+ * a NaN or +inf logit, or all -inf, or a NaN frontier score (an empty
+ * frontier entry) proposes nothing: tokens -1, scores -inf.  1 <= K <= 16 and K <= V (else SV_ERR_INVALID_ARG / UNSUPPORTED).
+ * --------------------------------------------------------------------------- */
+sv_status sv_tree_expand(const void *dlogits, sv_dtype dt, int B, int F, int V,
+                         float temperature, const float *frontier_score, int K,
+                         int32_t *out_token, float *out_score, void *stream);
+
+/* sv_tree_select -- per sequence, the indices (out_index [B][K]) of the K
+ * best of C candidates (cand_score / cand_token [B][C]): score descending,
+ * equal scores in ascending index; a candidate with token -1 is never chosen;
+ * missing picks are -1.  C <= 4096. */
+sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int B,
+                         int C, int K, int32_t *out_index, void *stream);
+
+/* sv_tree_finalize -- per sequence, the T-slot tree from C candidates
+ * (cand_parent: index of the parent candidate, -1 for candidate 0 = the
+ * root; cand_token; cand_score; cand_level, all [B][C]).  The kept nodes are
+ * the T first in (score descending, level ascending, index ascending) among
+ * the root and the candidates with a token; slots number them in (level
+ * ascending, score descending, index ascending).  out_parent [B][T] = slot of
+ * the parent candidate (-1 for the root; -2 if it was not kept, which cannot
+ * happen when child scores never exceed their parent's); out_token,
+ * out_score [B][T]; unused slots: parent -2, token -1, score 0.  C <= 4096,
+ * T <= SV_MAX_TREE_NODES. */
+sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token,
+                           const float *cand_score, const int32_t *cand_level, int B,
+                           int C, int T, int32_t *out_parent, int32_t *out_token,
+                           float *out_score, void *stream);
+
 /* Thread-local message for the last non-OK status returned on this thread. */
 const char *sv_last_error(void);
 

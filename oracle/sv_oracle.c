@@ -678,7 +678,8 @@ double orc_speedup(double alpha, int N, double c) {
  *           (equal logits in ascending token id) and their child scores
  *           = frontier score * softmax(x / T)[token] (T = 0: 1 for the
  *           first arg max, 0 for the others).  A row with a NaN or +inf
- *           logit, or all -inf, proposes nothing: tokens -1, scores -inf.
+ *           logit, or all -inf, or a NaN frontier score (an empty frontier
+ *           entry), proposes nothing: tokens -1, scores -inf.
  * select:   per sequence the K best candidates of a level, by score, equal
  *           scores in ascending candidate index; candidates with token -1
  *           are never chosen; missing picks are -1.
@@ -699,7 +700,7 @@ int orc_tree_expand(const float *dlog, int R, int V, float T, const float *fscor
     const float *x = dlog + (int64_t)r * V;
     int32_t *ot = out_tok + (int64_t)r * K;
     double *os = out_score + (int64_t)r * K;
-    if (orc_row_bad(x, V)) {
+    if (orc_row_bad(x, V) || isnan(fscore[r])) {
       for (int k = 0; k < K; ++k) {
         ot[k] = -1;
         os[k] = -INFINITY;

@@ -26,7 +26,8 @@ EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_ve
            "sv_verify_chain_noalloc", "sv_verify_tree_workspace_host",
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
            "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_last_error",
-           "sv_launch_count", "sv_trace_enable", "sv_trace_collect")
+           "sv_launch_count", "sv_trace_enable", "sv_trace_collect", "sv_tree_expand",
+           "sv_tree_select", "sv_tree_finalize")
 
 
 class SvError(RuntimeError):
@@ -71,6 +72,12 @@ def load_library(path: str = LIB_PATH):
     L.sv_verify_tree.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, u64, u64,
                                  vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.sv_verify_tree.restype = i32
+    L.sv_tree_expand.argtypes = [vp, i32, i32, i32, i32, f32, vp, i32, vp, vp, vp]
+    L.sv_tree_expand.restype = i32
+    L.sv_tree_select.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+    L.sv_tree_select.restype = i32
+    L.sv_tree_finalize.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
+    L.sv_tree_finalize.restype = i32
     L.sv_tree_build_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     L.sv_tree_build_mask.restype = i32
     L.sv_kv_compact.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
@@ -209,6 +216,29 @@ def sv_kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add, 
         _p(out_kv_len), _stream(stream)))
 
 
+def sv_tree_expand(dlogits, frontier_score, K, out_token, out_score, temperature=1.0,
+                   stream=None):
+    """dlogits [B][F][V]; frontier_score [B][F]; out_token / out_score [B][F][K]."""
+    B, F, V = dlogits.shape
+    return _check(load_library().sv_tree_expand(
+        _p(dlogits), _dtype(dlogits), B, F, V, float(temperature), _p(frontier_score), int(K),
+        _p(out_token), _p(out_score), _stream(stream)))
+
+
+def sv_tree_select(cand_score, cand_token, K, out_index, stream=None):
+    B, Cn = cand_score.shape
+    return _check(load_library().sv_tree_select(_p(cand_score), _p(cand_token), B, Cn, int(K),
+                                                _p(out_index), _stream(stream)))
+
+
+def sv_tree_finalize(cand_parent, cand_token, cand_score, cand_level, T, out_parent, out_token,
+                     out_score, stream=None):
+    B, Cn = cand_parent.shape
+    return _check(load_library().sv_tree_finalize(
+        _p(cand_parent), _p(cand_token), _p(cand_score), _p(cand_level), B, Cn, int(T),
+        _p(out_parent), _p(out_token), _p(out_score), _stream(stream)))
+
+
 def sv_last_error():
     return load_library().sv_last_error().decode()
 
@@ -282,6 +312,74 @@ def verify_tree(vlogits, dlogits, parent, token, score, max_depth, temperature=1
                    out["path"], out["tokens"], out["accept_len"], out["q_prob"], out["p_prob"],
                    out["margin"], out["status"], workspace, stream, accept_event)
     return out
+
+
+def tree_expand(dlogits, frontier_score, K, temperature=1.0, stream=None):
+    B, F, V = dlogits.shape
+    dev = _out_dev(dlogits)
+    tok = torch.empty(B, F, K, dtype=torch.int32, device=dev)
+    sc = torch.empty(B, F, K, dtype=torch.float32, device=dev)
+    sv_tree_expand(dlogits, frontier_score, K, tok, sc, temperature, stream)
+    return tok, sc
+
+
+def tree_select(cand_score, cand_token, K, stream=None):
+    out = torch.empty(cand_score.shape[0], K, dtype=torch.int32, device=_out_dev(cand_score))
+    sv_tree_select(cand_score, cand_token, K, out, stream)
+    return out
+
+
+def tree_finalize(cand_parent, cand_token, cand_score, cand_level, T, stream=None):
+    B = cand_parent.shape[0]
+    dev = _out_dev(cand_parent)
+    parent = torch.empty(B, T, dtype=torch.int32, device=dev)
+    token = torch.empty(B, T, dtype=torch.int32, device=dev)
+    score = torch.empty(B, T, dtype=torch.float32, device=dev)
+    sv_tree_finalize(cand_parent, cand_token, cand_score, cand_level, T, parent, token, score,
+                     stream)
+    return parent, token, score
+
+
+def build_tree(level_rows, K, T, temperature=1.0, stream=None, return_candidates=False):
+    """EAGLE-2 dynamic tree from the draft rows of each level.  level_rows(l,
+    frontier) -> [B][F][V] draft logits of the frontier's nodes (frontier:
+    [B][F] candidate ids; level 1's frontier is the root).  Every level's
+    expansion and frontier selection and the final pruning run in the
+    library's kernels; this loop only concatenates candidate lists.
+    Returns (parent, token, score) [B][T] for sv_verify_tree."""
+    frontier = None
+    valid = None  # frontier entries that hold a node (a pick could come up empty)
+    cp, ct, cs, cl = [], [], [], []
+    depth = 0
+    while True:
+        rows = level_rows(depth + 1, frontier)
+        if rows is None:
+            break
+        B, F, _ = rows.shape
+        dev = rows.device
+        if frontier is None:
+            frontier = torch.zeros(B, 1, dtype=torch.int64, device=dev)
+            cp.append(torch.full((B, 1), -1, dtype=torch.int32, device=dev))
+            ct.append(torch.zeros(B, 1, dtype=torch.int32, device=dev))
+            cs.append(torch.ones(B, 1, dtype=torch.float32, device=dev))
+            cl.append(torch.zeros(B, 1, dtype=torch.int32, device=dev))
+        depth += 1
+        n0 = sum(c.shape[1] for c in ct)
+        fscore = torch.gather(torch.cat(cs, 1), 1, frontier)
+        if valid is not None:  # an empty entry (NaN score) proposes nothing
+            fscore = fscore.masked_fill(~valid, float("nan"))
+        fscore = fscore.contiguous()
+        tok, sc = tree_expand(rows, fscore, K, temperature, stream)
+        cp.append(frontier.repeat_interleave(K, dim=1).to(torch.int32))
+        ct.append(tok.reshape(B, F * K))
+        cs.append(sc.reshape(B, F * K))
+        cl.append(torch.full((B, F * K), depth, dtype=torch.int32, device=dev))
+        sel = tree_select(cs[-1].contiguous(), ct[-1].contiguous(), K, stream).to(torch.int64)
+        valid = sel >= 0
+        frontier = torch.where(valid, sel + n0, torch.zeros_like(sel))
+    cands = tuple(torch.cat(a, 1).contiguous() for a in (cp, ct, cs, cl))
+    tree = tree_finalize(*cands, T, stream=stream)
+    return (tree, cands) if return_candidates else tree
 
 
 def tree_build_mask(parent, stream=None):
