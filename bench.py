@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences the oracle times")
+    ap.add_argument("--tree-build", action="store_true",
+                    help="time the GPU dynamic-tree builder instead of the verify step")
     ap.add_argument("--greedy", action="store_true",
                     help="temperature 0: greedy verification (verifier rows only, no sampling)")
     ap.add_argument("--batch", type=int, default=0,
@@ -642,10 +644,86 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_tree_build(args):
+    """--tree-build: the EAGLE-2 dynamic tree of config 5 (B=128, depth 6,
+    top-k 10, budget 60, V=128256 bf16) built on the GPU, one build per step:
+    per level sv_tree_expand over the frontier's draft rows and sv_tree_select,
+    then sv_tree_finalize.  The draft rows of every level are pre-generated
+    (the draft model is out of scope), 4 distinct pools rotated."""
+    import torch
+    import speculative_decoding_verification_vocab_gb300 as sv
+    from speculative_decoding_verification_vocab_gb300 import synth
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load_library()
+    cfg = synth.CONFIGS[5]
+    B, V, K, depth, Tn = cfg.B, cfg.V, cfg.topk, cfg.depth, cfg.T
+    pools = []
+    for r in range(args.pool):
+        g = torch.Generator(device=dev).manual_seed(1000 + r)
+        pools.append([(torch.randn((B, 1 if lvl == 1 else K, V), generator=g, device=dev) *
+                       cfg.sigma_q).to(cfg.dtype) for lvl in range(1, depth + 1)])
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        rows = pools[i % args.pool]
+        return sv.build_tree(lambda lvl, f: rows[lvl - 1] if lvl <= depth else None, K, Tn,
+                             cfg.temperature, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    n0 = sv.sv_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = sv.sv_launch_count() - n0
+    sv.sv_trace_enable(True)
+    for k in range(args.steps):
+        step(k)
+    torch.cuda.synchronize()
+    sv.sv_trace_enable(False)
+    trace = sv.sv_trace_collect()
+    rows_per_build = B * (1 + K * (depth - 1))
+    bytes_per_build = rows_per_build * V * 2
+    ex_n, ex_ms = trace.get("tree_expand", (0, 0.0))
+    per_level_bytes = bytes_per_build / depth
+    peak, peak_kind = measured_peaks()
+    ach = per_level_bytes / (ex_ms / max(ex_n, 1) / 1e3) / 1e9 if ex_n else None
+    line = {
+        "metric": "dynamic-tree builds/s (draft rows expanded per second)", "value":
+        args.steps / (ms / 1e3), "unit": "builds/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "config 5 tree build: B=128, depth 6, top-k 10, budget 60, "
+                               "V=128256 bf16", "draft_rows_per_build": rows_per_build,
+                   "l2": f"draft rows rotate over {args.pool} pools of "
+                         f"{bytes_per_build / 1e9:.2f} GB"},
+        "draft_rows_per_s": rows_per_build * args.steps / (ms / 1e3),
+        "kernels": {k: {"launches": v[0], "avg_us": 1e3 * v[1] / max(v[0], 1)}
+                    for k, v in trace.items()},
+        "gpu_launches": int(launches),
+        "roofline": {"kernel": "tree_expand", "bound": "hbm", "achieved": ach, "peak": peak,
+                     "unit": "GB/s", "frac": ach / peak if ach else None,
+                     "peak_kind": f"{peak_kind} copy bandwidth",
+                     "alg_bytes_per_launch": per_level_bytes, "traffic": None},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.tree_build:
+        run_tree_build(args)
     else:
         run_ours(args)
 

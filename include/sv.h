@@ -274,7 +274,7 @@ sv_status sv_tree_expand(const void *dlogits, sv_dtype dt, int B, int F, int V,
 /* sv_tree_select -- per sequence, the indices (out_index [B][K]) of the K
  * best of C candidates (cand_score / cand_token [B][C]): score descending,
  * equal scores in ascending index; a candidate with token -1 is never chosen;
- * missing picks are -1.  C <= 4096. */
+ * missing picks are -1.  C <= 2048. */
 sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int B,
                          int C, int K, int32_t *out_index, void *stream);
 
@@ -286,7 +286,7 @@ sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int
  * ascending, score descending, index ascending).  out_parent [B][T] = slot of
  * the parent candidate (-1 for the root; -2 if it was not kept, which cannot
  * happen when child scores never exceed their parent's); out_token,
- * out_score [B][T]; unused slots: parent -2, token -1, score 0.  C <= 4096,
+ * out_score [B][T]; unused slots: parent -2, token -1, score 0.  C <= 2048,
  * T <= SV_MAX_TREE_NODES. */
 sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token,
                            const float *cand_score, const int32_t *cand_level, int B,

@@ -7,6 +7,7 @@
 // probabilities along its path; the best-scored nodes are expanded and the
 // tree is pruned to a budget.
 #include "common.cuh"
+#include "rowstat.cuh"
 
 namespace sv {
 namespace {
@@ -15,79 +16,160 @@ constexpr int kExThreads = 256;
 constexpr int kExWarps = kExThreads / 32;
 constexpr int kExUnroll = 8;
 constexpr int kMaxK = 16;
-constexpr int kMaxCand = 4096;
-constexpr int kSelWarps = 4;
+constexpr int kMaxCand = 2048;
 
 // ---------------------------------------------------------------------------
-// expand: one CTA per frontier row.  Each thread scans its 16-byte words in
-// index order keeping (a) online softmax statistics in the log2 domain and
-// (b) its own top-K list in shared memory (value descending, index
-// ascending); a word whose packed maximum does not beat the thread's K-th
-// value is skipped.  The CTA merges the lists with K rounds of a block-wide
-// arg max and writes the K tokens and their child scores.
-struct ExStat {
-  float mx, mk, s;  // raw max, fl(mx * k), sum exp2(fma(x, k, -mk))
-  uint32_t flags;   // 1: NaN or +inf seen, 2: a logit above -inf seen
+// expand: one CTA per frontier row.  Each thread streams its 16-byte words
+// (online softmax statistics in the log2 domain, as the verify step's row
+// pass), and each warp keeps a top-K list spread over its lanes (lane j
+// holds entry j; value descending, index ascending).  A word is looked at
+// only when its packed maximum reaches the list's K-th value; its elements
+// are then offered one at a time to the whole warp, which inserts an element
+// that precedes the K-th entry by shifting the lanes after its rank.  The
+// CTA merges the eight warp lists and writes the K tokens and their child
+// scores.
+struct WarpTopK {
+  float v;  // this lane's entry (lane < K), -inf when empty
+  int i;    // its token id, INT_MAX when empty
+  float tv; // the K-th entry, uniform over the warp
+  int ti;
 };
 
-__device__ __forceinline__ void ex_stat(ExStat &st, float x, float k) {
-  if (x > st.mx) {
-    const float nk = x * k;
-    st.s = (st.mx == -INFINITY) ? 0.0f : st.s * ex2_approx(st.mk - nk);
-    st.mx = x;
-    st.mk = nk;
-  }
-  st.s += ex2_approx(fmaf(x, k, -(st.mx == -INFINITY ? 0.0f : st.mk)));
-  if (x != x || x == INFINITY) st.flags |= 1u;
-  if (x > -INFINITY) st.flags |= 2u;
+// (va, ia) precedes (vb, ib): larger value, or equal value and lower id
+__device__ __forceinline__ bool tk_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
 }
 
-// the thread's list: val/idx[j][tid], j < n, sorted (value desc, index asc);
-// elements arrive in increasing index, so an equal value goes after
-struct TopK {
-  float (*val)[kExThreads];
-  int (*idx)[kExThreads];
-  int n, K;
-  float thr;  // value of the K-th entry once full, else -inf
-};
-
-__device__ __forceinline__ void topk_offer(TopK &t, float x, int v) {
-  const int tid = threadIdx.x;
-  if (!(t.n < t.K ? x == x : x > t.thr)) return;
-  int j = t.n < t.K ? t.n : t.K - 1;  // the slot freed (or the last one)
-  while (j > 0 && t.val[j - 1][tid] < x) {
-    t.val[j][tid] = t.val[j - 1][tid];
-    t.idx[j][tid] = t.idx[j - 1][tid];
-    --j;
+__device__ __forceinline__ void warp_offer(WarpTopK &w, float x, int idx, int K) {
+  // uniform: every lane holds the same (x, idx)
+  if (!tk_before(x, idx, w.tv, w.ti)) return;
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int pos = __popc(__ballot_sync(FULL, lane < K && tk_before(w.v, w.i, x, idx)));
+  const float pv = __shfl_up_sync(FULL, w.v, 1);
+  const int pi = __shfl_up_sync(FULL, w.i, 1);
+  if (lane > pos && lane < K) {
+    w.v = pv;
+    w.i = pi;
   }
-  t.val[j][tid] = x;
-  t.idx[j][tid] = v;
-  if (t.n < t.K) ++t.n;
-  t.thr = t.n == t.K ? t.val[t.K - 1][tid] : -INFINITY;
+  if (lane == pos) {
+    w.v = x;
+    w.i = idx;
+  }
+  w.tv = __shfl_sync(FULL, w.v, K - 1);
+  w.ti = __shfl_sync(FULL, w.i, K - 1);
 }
 
 template <typename E>
-__device__ __forceinline__ void ex_word(ExStat &st, TopK &t, uint4 w, int v, float k);
+__device__ __forceinline__ float word_max(uint4 w);
 template <>
-__device__ __forceinline__ void ex_word<uint16_t>(ExStat &st, TopK &t, uint4 w, int v, float k) {
-  const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) ex_stat(st, (j & 1) ? bf16_hi(q[j >> 1]) : bf16_lo(q[j >> 1]), k);
+__device__ __forceinline__ float word_max<uint16_t>(uint4 w) {
   const uint32_t m = bf2_max(bf2_max(w.x, w.y), bf2_max(w.z, w.w));
-  if (t.n < t.K || fmaxf(bf16_lo(m), bf16_hi(m)) > t.thr)
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      topk_offer(t, (j & 1) ? bf16_hi(q[j >> 1]) : bf16_lo(q[j >> 1]), v + j);
+  return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 template <>
-__device__ __forceinline__ void ex_word<float>(ExStat &st, TopK &t, uint4 w, int v, float k) {
-  const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                      __uint_as_float(w.w)};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    ex_stat(st, x[j], k);
-    topk_offer(t, x[j], v + j);
+__device__ __forceinline__ float word_max<float>(uint4 w) {
+  return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+               fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+template <typename E>
+__device__ __forceinline__ float word_elem(uint4 w, int j) {
+  if (sizeof(E) == 2) {
+    const uint32_t c = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+    return (j & 1) ? bf16_hi(c) : bf16_lo(c);
   }
+  return __uint_as_float(j == 0 ? w.x : j == 1 ? w.y : j == 2 ? w.z : w.w);
+}
+
+// every lane's word (element ids v, v+1, ...): the lanes whose word can
+// reach the list offer their elements, lane by lane; `skip` is an element id
+// of the lane already in the list (-1: none)
+template <typename E>
+__device__ __forceinline__ void warp_offer_words(WarpTopK &w, uint4 word, int v, bool in, int K,
+                                                 int skip = -1) {
+  constexpr int kPer = 16 / (int)sizeof(E);
+  const unsigned FULL = 0xffffffffu;
+  const float m = in ? word_max<E>(word) : -INFINITY;
+  // the lane marks the elements of its word that can reach the list
+  unsigned emask = 0u;
+  if (in && m >= w.tv) {
+#pragma unroll 1
+    for (int j = 0; j < kPer; ++j) {
+      const float x = word_elem<E>(word, j);
+      if (x >= w.tv && v + j != skip) emask |= 1u << j;  // NaN fails the compare
+    }
+  }
+  unsigned cand = __ballot_sync(FULL, emask != 0u);
+  while (cand) {
+    const int src = __ffs(cand) - 1;
+    cand &= cand - 1;
+    const uint4 q = make_uint4(__shfl_sync(FULL, word.x, src), __shfl_sync(FULL, word.y, src),
+                               __shfl_sync(FULL, word.z, src), __shfl_sync(FULL, word.w, src));
+    const int v0 = __shfl_sync(FULL, v, src);
+    unsigned em = __shfl_sync(FULL, emask, src);
+    while (em) {
+      const int j = __ffs(em) - 1;
+      em &= em - 1;
+      warp_offer(w, word_elem<E>(q, j), v0 + j, K);
+    }
+  }
+}
+
+// Seed an empty warp list from a full batch: every lane's best element of
+// its batch (value desc, id asc) is sorted across the warp (bitonic, by
+// shuffles) and the first K become the list, so the gate is tight from the
+// start.  Returns the id the lane contributed, or -1 if it was not kept.
+template <typename E>
+__device__ __forceinline__ int warp_seed(WarpTopK &w, const uint4 (&buf)[kRsUnroll], int v0,
+                                         int stride_elems, int K) {
+  constexpr int kPer = 16 / (int)sizeof(E);
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < kRsUnroll; ++j) {
+    const float m = word_max<E>(buf[j]);
+    if (m > bv) {  // words come in increasing id: strict keeps the lowest id
+#pragma unroll 1
+      for (int e = 0; e < kPer; ++e)
+        if (word_elem<E>(buf[j], e) == m) {
+          bv = m;
+          bi = v0 + j * stride_elems + e;
+          break;
+        }
+    }
+  }
+  float sv = bv;
+  int si = bi;
+  // bitonic sort, descending in (value, then ascending id)
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float ov = __shfl_xor_sync(FULL, sv, stride);
+      const int oi = __shfl_xor_sync(FULL, si, stride);
+      const bool up = ((lane & size) == 0);       // this block sorts descending
+      const bool lower = (lane & stride) == 0;    // the lane keeps the "first" of the pair
+      const bool other_first = tk_before(ov, oi, sv, si);
+      if ((up == lower) == other_first) {
+        sv = ov;
+        si = oi;
+      }
+    }
+  const bool ok = sv == sv && si != 0x7fffffff;
+  w.v = (lane < K && ok) ? sv : -INFINITY;
+  w.i = (lane < K && ok) ? si : 0x7fffffff;
+  w.tv = __shfl_sync(FULL, w.v, K - 1);
+  w.ti = __shfl_sync(FULL, w.i, K - 1);
+  // did my own best element land in the list?
+  const unsigned kept = __ballot_sync(FULL, lane < K && ok);
+  int mine = -1;
+  for (int j = 0; j < K; ++j) {
+    const int id = __shfl_sync(FULL, w.i, j);
+    if (((kept >> j) & 1u) && id == bi) mine = bi;
+  }
+  return mine;
 }
 
 template <typename E>
@@ -99,10 +181,8 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   const size_t rowi = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const E *row = dlog + rowi * (size_t)V;
-  __shared__ float s_val[kMaxK][kExThreads];
-  __shared__ int s_idx[kMaxK][kExThreads];
-  TopK t{s_val, s_idx, 0, K, -INFINITY};
-  ExStat st{-INFINITY, 0.0f, 0.0f, 0u};
+  WarpTopK w{-INFINITY, 0x7fffffff, -INFINITY, 0x7fffffff};
+  StatState st{-INFINITY, 0.0f, 0ull, 0ull};
   const uintptr_t pb = (uintptr_t)row, pe = (uintptr_t)(row + V);
   uintptr_t ab = (pb + 15) & ~(uintptr_t)15, ae = pe & ~(uintptr_t)15;
   if (ab > ae) ab = ae = pe;
@@ -110,167 +190,124 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   constexpr int kPer = 16 / (int)sizeof(E);
   const uint4 *body = (const uint4 *)ab;
   const int nv = (int)((ae - ab) / 16);
-  // head elements first (lowest indices), then the body, then the tail
-  if (tid == 0)
-    for (int j = 0; j < nhead; ++j) {
-      const float x = load_elem<E>(row + j);
-      ex_stat(st, x, k);
-      topk_offer(t, x, j);
-    }
-  int i = tid;
-  for (; i + (kExUnroll - 1) * kExThreads < nv; i += kExUnroll * kExThreads) {
-    uint4 buf[kExUnroll];
-#pragma unroll
-    for (int j = 0; j < kExUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kExThreads);
-#pragma unroll
-    for (int j = 0; j < kExUnroll; ++j)
-      ex_word<E>(st, t, buf[j], nhead + (i + j * kExThreads) * kPer, k);
-  }
-  for (; i < nv; i += kExThreads) ex_word<E>(st, t, ld_stream_v4(body + i), nhead + i * kPer, k);
-  if (tid == kExThreads - 1)
-    for (int v = nhead + nv * kPer; v < V; ++v) {
+  const int ntail = (int)((pe - ae) / sizeof(E));
+  // ragged head and tail elements (fewer than 8 each), by warp 0
+  if (warp == 0) {
+    for (int j = 0; j < nhead + ntail; ++j) {
+      const int v = j < nhead ? j : nhead + nv * kPer + (j - nhead);
       const float x = load_elem<E>(row + v);
-      ex_stat(st, x, k);
-      topk_offer(t, x, v);
+      if (lane == 0) stat1(x, st, k);
+      if (x == x) warp_offer(w, x, v, K);
     }
-  // statistics: max of references, one rescale per thread, sums
-  __shared__ float s_red[3][kExWarps];
-  __shared__ uint32_t s_flags[kExWarps];
-  {
-    float a = (st.mx == -INFINITY) ? -INFINITY : st.mk, M = a, mx = st.mx;
-    uint32_t fl = st.flags;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      fl |= __shfl_xor_sync(0xffffffffu, fl, o);
-    }
-    if (lane == 0) {
-      s_red[0][warp] = M;
-      s_red[1][warp] = mx;
-      s_flags[warp] = fl;
-    }
-    __syncthreads();
-    float MM = -INFINITY;
-    uint32_t FF = 0u;
-    for (int w = 0; w < kExWarps; ++w) {
-      MM = fmaxf(MM, s_red[0][w]);
-      FF |= s_flags[w];
-    }
-    float s = (MM == -INFINITY || a == -INFINITY) ? 0.0f : st.s * ex2_approx(a - MM);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    __syncthreads();
-    if (lane == 0) s_red[2][warp] = s;
-    __syncthreads();
-    st.mk = MM;
-    st.flags = FF;
-    st.s = 0.0f;
-    for (int w = 0; w < kExWarps; ++w) st.s += s_red[2][w];
-    st.mx = 0.0f;
-    for (int w = 0; w < kExWarps; ++w) st.mx = fmaxf(st.mx, s_red[1][w]);
   }
-  // a faulty row, or a frontier entry with a NaN score (no node), proposes nothing
-  const bool bad = (st.flags & 1u) || !(st.flags & 2u) || fscore[rowi] != fscore[rowi];
-  // K rounds of a block-wide arg max over the heads of the thread lists
-  __shared__ float s_hv[kExWarps];
-  __shared__ int s_hi[kExWarps];
-  int head = 0;
-  for (int r = 0; r < K; ++r) {
-    float hv = head < t.n ? s_val[head][tid] : -INFINITY;
-    int hi = head < t.n ? s_idx[head][tid] : 0x7fffffff;
+  int i = tid;
+  bool seeded = false;
+  // warp-uniform trip count (the warp's offers are warp-wide collectives):
+  // a batch is taken only when every lane of the warp has its full batch
+  for (; (i - lane) + 31 + (kRsUnroll - 1) * kExThreads < nv; i += kRsUnroll * kExThreads) {
+    uint4 buf[kRsUnroll];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, hv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, hi, o);
-      if (ov > hv || (ov == hv && oi < hi)) {
-        hv = ov;
-        hi = oi;
-      }
+    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kExThreads);
+    stat_batch<E>(buf, st, k);
+    int skip = -1;
+    if (!seeded && w.ti == 0x7fffffff) {  // list still empty: seed it from this batch
+      skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
+      seeded = true;
     }
-    if (lane == 0) {
-      s_hv[warp] = hv;
-      s_hi[warp] = hi;
+#pragma unroll
+    for (int j = 0; j < kRsUnroll; ++j)
+      warp_offer_words<E>(w, buf[j], nhead + (i + j * kExThreads) * kPer, true, K, skip);
+  }
+  // the remainder: words are loaded warp-uniformly so every lane joins the ballots
+  for (int i0 = i - lane; i0 < nv; i0 += kExThreads) {
+    const int ii = i0 + lane;
+    const bool in = ii < nv;
+    const uint4 wd = in ? ld_stream_v4(body + ii) : make_uint4(0u, 0u, 0u, 0u);
+    if (in) stat_word<E>(wd, st, k);
+    warp_offer_words<E>(w, wd, nhead + ii * kPer, in, K);
+  }
+  // the row's statistics, as the verify step's row pass combines them
+  float a0, a1, a2, a3;
+  f2_unpack(st.s01, a0, a1);
+  f2_unpack(st.s23, a2, a3);
+  float mx = st.mx, mk = st.mk, ssum = (a0 + a1) + (a2 + a3);
+  warp_stat_combine(mx, mk, ssum);
+  __shared__ float4 s_red[kExWarps];
+  __shared__ float s_tv[kExWarps][kMaxK];
+  __shared__ int s_ti[kExWarps][kMaxK];
+  if (lane == 0) s_red[warp] = make_float4(mx, mk, ssum, 0.0f);
+  if (lane < K) {
+    s_tv[warp][lane] = w.v;
+    s_ti[warp][lane] = w.i;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float4 rs = lane < kExWarps ? s_red[lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+  warp_stat_combine(rs.x, rs.y, rs.z);
+  const float MK = rs.y, S = rs.z;
+  // a faulty row (NaN or +inf: the sum is NaN; all -inf: the sum is 0), or a
+  // frontier entry with a NaN score (no node), proposes nothing
+  const bool bad = !(S > 0.0f) || fscore[rowi] != fscore[rowi];
+  // merge: the eight warp lists through warp 0's list
+  WarpTopK m{-INFINITY, 0x7fffffff, -INFINITY, 0x7fffffff};
+  for (int wi = 0; wi < kExWarps; ++wi)
+    for (int j = 0; j < K; ++j) {
+      const float x = s_tv[wi][j];
+      if (x == x && s_ti[wi][j] != 0x7fffffff) warp_offer(m, x, s_ti[wi][j], K);
     }
-    __syncthreads();
-    float bv = s_hv[0];
-    int bi = s_hi[0];
-    for (int w = 1; w < kExWarps; ++w)
-      if (s_hv[w] > bv || (s_hv[w] == bv && s_hi[w] < bi)) {
-        bv = s_hv[w];
-        bi = s_hi[w];
-      }
-    __syncthreads();
-    if (head < t.n && s_idx[head][tid] == bi) ++head;  // indices are unique
-    if (tid == 0) {
-      const size_t o = rowi * (size_t)K + r;
-      if (bad || bi == 0x7fffffff) {
-        out_tok[o] = -1;
-        out_score[o] = -INFINITY;
-      } else {
-        float p;
-        if (greedy)
-          p = (r == 0) ? 1.0f : 0.0f;
-        else
-          p = ex2_approx(fmaf(bv, k, -st.mk)) / st.s;
-        out_tok[o] = bi;
-        out_score[o] = fscore[rowi] * p;
-      }
+  if (lane < K) {
+    const size_t o = rowi * (size_t)K + lane;
+    if (bad || m.i == 0x7fffffff) {
+      out_tok[o] = -1;
+      out_score[o] = -INFINITY;
+    } else {
+      const float p = greedy ? (lane == 0 ? 1.0f : 0.0f) : ex2_approx(fmaf(m.v, k, -MK)) / S;
+      out_tok[o] = m.i;
+      out_score[o] = fscore[rowi] * p;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// select: one warp per sequence, K rounds of a warp arg max (score
-// descending, index ascending) over the not-yet-taken candidates with a
-// token; a shared-memory bitmap marks the taken ones.
-__global__ void __launch_bounds__(kSelWarps * 32)
-tree_select_kernel(const float *__restrict__ score, const int32_t *__restrict__ token, int B,
-                   int C, int K, int32_t *__restrict__ out) {
+// select: one CTA per sequence.  A candidate's pick order is its rank among
+// the candidates with a token (score descending, index ascending); every
+// thread ranks its candidates against all others staged in shared memory,
+// and a candidate of rank r < K is pick r.
+__global__ void __launch_bounds__(kExThreads)
+tree_select_kernel(const float *__restrict__ score, const int32_t *__restrict__ token, int C,
+                   int K, int32_t *__restrict__ out) {
   grid_dep_sync();
-  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kSelWarps + wi;
-  __shared__ uint32_t taken[kSelWarps][kMaxCand / 32];
-  for (int j = lane; j < (C + 31) / 32; j += 32) taken[wi][j] = 0u;
-  __syncwarp();
-  if (b >= B) return;
-  const float *s = score + (size_t)b * C;
-  const int32_t *tk = token + (size_t)b * C;
-  for (int r = 0; r < K; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = lane; c < C; c += 32) {
-      if ((taken[wi][c >> 5] >> (c & 31)) & 1u) continue;
-      if (tk[c] < 0) continue;
-      const float v = s[c];
-      if (bi == 0x7fffffff || v > bv) {  // lane-local candidates in index order
-        bv = v;
-        bi = c;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      out[(size_t)b * K + r] = bi == 0x7fffffff ? -1 : bi;
-      if (bi != 0x7fffffff) taken[wi][bi >> 5] |= 1u << (bi & 31);
-    }
-    __syncwarp();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ float sv_[kMaxCand];
+  __shared__ int ok_[kMaxCand];
+  __shared__ int s_nvalid;
+  if (tid == 0) s_nvalid = 0;
+  __syncthreads();
+  int nv = 0;
+  for (int c = tid; c < C; c += kExThreads) {
+    sv_[c] = score[(size_t)b * C + c];
+    ok_[c] = token[(size_t)b * C + c] >= 0;
+    nv += ok_[c];
   }
+  atomicAdd(&s_nvalid, nv);
+  __syncthreads();
+  for (int c = tid; c < C; c += kExThreads) {
+    if (!ok_[c]) continue;
+    const float v = sv_[c];
+    int rank = 0;
+    for (int d = 0; d < C; ++d)
+      rank += ok_[d] && (sv_[d] > v || (sv_[d] == v && d < c));
+    if (rank < K) out[(size_t)b * K + rank] = c;
+  }
+  for (int r = s_nvalid + tid; r < K; r += kExThreads) out[(size_t)b * K + r] = -1;
 }
 
 // ---------------------------------------------------------------------------
-// finalize: one CTA per sequence.  T rounds of a block-wide pick in keep
-// order (score descending, level ascending, index ascending) build the kept
-// set; each kept node's slot is its rank in (level ascending, score
-// descending, index ascending); parents map through the candidate -> slot
-// table.
+// finalize: one CTA per sequence.  A candidate (the root, or one with a
+// token) is kept when its rank in keep order (score descending, level
+// ascending, index ascending) is below T; a kept node's slot is its rank
+// among the kept in (level ascending, score descending, index ascending);
+// parents map through the candidate -> slot table.
 __device__ __forceinline__ bool keep_before(float sa, int la, int a, float sb, int lb, int b) {
   if (sa != sb) return sa > sb;
   if (la != lb) return la < lb;
@@ -283,78 +320,42 @@ tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restr
                      int Tn, int32_t *__restrict__ parent, int32_t *__restrict__ token,
                      float *__restrict__ score) {
   grid_dep_sync();
-  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, tid = threadIdx.x;
   const int32_t *cp = cparent + (size_t)b * C, *ct = ctoken + (size_t)b * C;
-  const int32_t *cl = clevel + (size_t)b * C;
-  const float *cs = cscore + (size_t)b * C;
+  __shared__ float sc_[kMaxCand];
+  __shared__ int lv_[kMaxCand];  // level, or -1: not a node
   __shared__ int slot_of[kMaxCand];
   __shared__ int keep[SV_MAX_TREE_NODES];
-  __shared__ float w_v[kExWarps];
-  __shared__ int w_l[kExWarps], w_i[kExWarps];
   __shared__ int s_n;
-  for (int c = tid; c < C; c += kExThreads) slot_of[c] = -1;  // -1: not kept (yet)
-  __syncthreads();
-  int n = 0;
-  for (; n < Tn; ++n) {
-    float bv = 0.0f;
-    int bl = 0, bi = 0x7fffffff;
-    for (int c = tid; c < C; c += kExThreads) {
-      if (slot_of[c] != -1) continue;
-      if (c != 0 && ct[c] < 0) continue;
-      const float v = cs[c];
-      const int l = cl[c];
-      if (bi == 0x7fffffff || keep_before(v, l, c, bv, bl, bi)) {
-        bv = v;
-        bl = l;
-        bi = c;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || keep_before(ov, ol, oi, bv, bl, bi))) {
-        bv = ov;
-        bl = ol;
-        bi = oi;
-      }
-    }
-    if (lane == 0) {
-      w_v[warp] = bv;
-      w_l[warp] = bl;
-      w_i[warp] = bi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float v = w_v[0];
-      int l = w_l[0], i = w_i[0];
-      for (int w = 1; w < kExWarps; ++w)
-        if (w_i[w] != 0x7fffffff && (i == 0x7fffffff || keep_before(w_v[w], w_l[w], w_i[w], v, l, i))) {
-          v = w_v[w];
-          l = w_l[w];
-          i = w_i[w];
-        }
-      s_n = i;
-      if (i != 0x7fffffff) {
-        keep[n] = i;
-        slot_of[i] = -3;  // kept; its slot is set below
-      }
-    }
-    __syncthreads();
-    if (s_n == 0x7fffffff) break;
+  if (tid == 0) s_n = 0;
+  for (int c = tid; c < C; c += kExThreads) {
+    sc_[c] = cscore[(size_t)b * C + c];
+    lv_[c] = (c == 0 || ct[c] >= 0) ? clevel[(size_t)b * C + c] : -1;
+    slot_of[c] = -1;
   }
-  // slots: rank in (level asc, score desc, index asc) among the kept
+  __syncthreads();
+  for (int c = tid; c < C; c += kExThreads) {
+    if (lv_[c] < 0) continue;
+    const float v = sc_[c];
+    const int l = lv_[c];
+    int rank = 0;
+    for (int d = 0; d < C && rank < Tn; ++d)
+      rank += lv_[d] >= 0 && keep_before(sc_[d], lv_[d], d, v, l, c);
+    if (rank < Tn) {
+      keep[rank] = c;
+      atomicAdd(&s_n, 1);
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
   for (int i = tid; i < n; i += kExThreads) {
     const int c = keep[i];
-    const int l = cl[c];
-    const float v = cs[c];
+    const int l = lv_[c];
+    const float v = sc_[c];
     int rank = 0;
     for (int j = 0; j < n; ++j) {
       const int d = keep[j];
-      const int ld = cl[d];
-      const float vd = cs[d];
-      rank += (ld < l) || (ld == l && (vd > v || (vd == v && d < c)));
+      rank += (lv_[d] < l) || (lv_[d] == l && (sc_[d] > v || (sc_[d] == v && d < c)));
     }
     slot_of[c] = rank;
   }
@@ -364,7 +365,7 @@ tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restr
     const int pc = cp[c];
     parent[(size_t)b * Tn + sl] = pc < 0 ? -1 : (slot_of[pc] >= 0 ? slot_of[pc] : -2);
     token[(size_t)b * Tn + sl] = ct[c];
-    score[(size_t)b * Tn + sl] = cs[c];
+    score[(size_t)b * Tn + sl] = sc_[c];
   }
   for (int i = n + tid; i < Tn; i += kExThreads) {
     parent[(size_t)b * Tn + i] = -2;
@@ -428,9 +429,8 @@ extern "C" sv_status sv_tree_select(const float *cand_score, const int32_t *cand
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("tree_select", st);
   return check_launch("tree_select",
-                      launch_pdl(tree_select_kernel, dim3((B + kSelWarps - 1) / kSelWarps),
-                                 dim3(kSelWarps * 32), 0, st, cand_score, cand_token, B, C, K,
-                                 out_index));
+                      launch_pdl(tree_select_kernel, dim3(B), dim3(kExThreads), 0, st,
+                                 cand_score, cand_token, C, K, out_index));
 }
 
 extern "C" sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token,
