@@ -76,6 +76,10 @@ def _declare(L):
     L.orc_tree_expand.argtypes = [_f32p, C.c_int, C.c_int, C.c_float, _f32p, C.c_int,
                                   _i32p, _f64p]
     L.orc_tree_select.argtypes = [_f32p, _i32p, C.c_int, C.c_int, C.c_int, _i32p]
+    L.orc_tree_attention.argtypes = [_f32p, _f32p, _i32p, _u64p, C.c_int, C.c_int, C.c_int,
+                                     C.c_int, C.c_int, C.c_int, C.c_double, C.c_void_p,
+                                     C.c_int, _f64p, _f64p]
+    L.orc_tree_attention.restype = C.c_int
     L.orc_tree_finalize.argtypes = [_i32p, _i32p, _f32p, _i32p, C.c_int, C.c_int, C.c_int,
                                     _i32p, _i32p, _f32p]
     L.orc_argmax.argtypes = [_f32p, C.c_int]
@@ -366,6 +370,34 @@ def kv_compact(src, dst, L, B, S_src, S_dst, H, D, elem_bytes, src_base,
     lib().orc_kv_compact(src, dst, L, B, S_src, S_dst, H, D, elem_bytes,
                          _i32(src_base), _i32(dst_base), rows, _i32(n_rows), P, out)
     return out
+
+
+def tree_attention(q, kv, base, mask, scale, sel=None):
+    """Tree-masked attention of one layer in double precision.
+
+    q [B][T][Hq][D] and kv [2][B][S][Hkv][D] (float32 arrays holding the
+    bf16 values exactly), base [B], mask [B][T][W] uint64.  With ``sel``
+    (an [n][3] array of (b, node, head)) only those rows are computed.
+    Returns (out, lse): [B][T][Hq][D] and [B][T][Hq], or [n][D] and [n]."""
+    q, kv = _f32(q), _f32(kv)
+    B, T, Hq, D = q.shape
+    _, B2, S, Hkv, D2 = kv.shape
+    assert B2 == B and D2 == D
+    mask = np.ascontiguousarray(mask, np.uint64)
+    if sel is None:
+        out = np.empty((B, T, Hq, D), np.float64)
+        lse = np.empty((B, T, Hq), np.float64)
+        sp, ns = None, 0
+    else:
+        sel = _i32(sel).reshape(-1, 3)
+        out = np.empty((sel.shape[0], D), np.float64)
+        lse = np.empty(sel.shape[0], np.float64)
+        sp, ns = sel.ctypes.data, sel.shape[0]
+    rc = lib().orc_tree_attention(q.reshape(-1), kv.reshape(-1), _i32(base), mask.reshape(-1),
+                                  B, T, Hq, Hkv, D, S, float(scale), sp, ns,
+                                  out.reshape(-1), lse.reshape(-1))
+    assert rc == 0, rc
+    return out, lse
 
 
 def expected_tokens(alpha, N):

@@ -811,3 +811,96 @@ int orc_tree_finalize(const int32_t *cparent, const int32_t *ctoken, const float
   free(taken);
   return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Tree-masked verifier attention, one layer.  [Blog] section 3: the verifier
+ * scores the whole flattened draft tree in one forward pass, and the
+ * attention mask lets every node see the committed context, itself and its
+ * ancestors, never a sibling or another branch; [Lesson] "Reversão de KV
+ * cache": the verifier pass over a tree runs a non-causal mask that follows
+ * the tree.  Grouped-query heads: query head h reads KV head h / (Hq / Hkv).
+ *
+ *   q    [B][T][Hq][D]        queries of the T tree nodes (node 0 = root)
+ *   kv   [2][B][S][Hkv][D]    this layer's cache, K then V; node n's own
+ *                             K/V row is slot base[b] + n
+ *   mask [B][T][(T+63)/64]    ancestor bitmask (orc_tree_mask)
+ *
+ * Row (b, n, h) sees key slots j < base[b] and j = base[b] + m for every
+ * m < T whose bit is set in node n's mask.  Scores s_j = scale * <q, k_j>;
+ * out = sum_j exp(s_j - M) v_j / sum_j exp(s_j - M) with M = max_j s_j, and
+ * lse = M + log(sum_j exp(s_j - M)).  No visible key: out 0, lse -inf.
+ * base[b] < 0 or base[b] + T > S: out and lse NaN.
+ * sel lists n_sel (b, n, h) triples to compute (sel == NULL: every row in
+ * [B][T][Hq] order); out is [rows][D], lse [rows] (lse may be NULL).
+ * Plain double arithmetic, keys in slot order.
+ * ---------------------------------------------------------------------- */
+int orc_tree_attention(const float *q, const float *kv, const int32_t *base,
+                       const uint64_t *mask, int B, int T, int Hq, int Hkv,
+                       int D, int S, double scale, const int32_t *sel,
+                       int n_sel, double *out, double *lse) {
+  if (B < 1 || T < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || D < 1 || S < 1)
+    return -1;
+  const int G = Hq / Hkv, W = (T + 63) / 64;
+  const int64_t rows = sel ? n_sel : (int64_t)B * T * Hq;
+  int32_t *vis = (int32_t *)malloc(sizeof(int32_t) * ((size_t)S + 1));
+  double *s = (double *)malloc(sizeof(double) * ((size_t)S + 1));
+  if (!vis || !s) {
+    free(vis);
+    free(s);
+    return -2;
+  }
+  for (int64_t r = 0; r < rows; ++r) {
+    int b, n, h;
+    if (sel) {
+      b = sel[3 * r];
+      n = sel[3 * r + 1];
+      h = sel[3 * r + 2];
+    } else {
+      b = (int)(r / ((int64_t)T * Hq));
+      n = (int)(r / Hq % T);
+      h = (int)(r % Hq);
+    }
+    double *o = out + r * D;
+    const int bs = base[b];
+    if (bs < 0 || (int64_t)bs + T > S) {
+      for (int d = 0; d < D; ++d) o[d] = NAN;
+      if (lse) lse[r] = NAN;
+      continue;
+    }
+    const float *qr = q + (((int64_t)b * T + n) * Hq + h) * D;
+    const int kh = h / G;
+    const float *K = kv + (int64_t)b * S * Hkv * D;
+    const float *V = kv + ((int64_t)B + b) * S * Hkv * D;
+    const uint64_t *mk = mask + ((int64_t)b * T + n) * W;
+    int nv = 0;
+    for (int j = 0; j < bs; ++j) vis[nv++] = j;
+    for (int m = 0; m < T; ++m)
+      if ((mk[m / 64] >> (m % 64)) & 1) vis[nv++] = bs + m;
+    if (nv == 0) {
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (lse) lse[r] = -INFINITY;
+      continue;
+    }
+    double M = -INFINITY;
+    for (int i = 0; i < nv; ++i) {
+      const float *kr = K + ((int64_t)vis[i] * Hkv + kh) * D;
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d) acc += (double)qr[d] * (double)kr[d];
+      s[i] = scale * acc;
+      if (s[i] > M) M = s[i];
+    }
+    double l = 0.0;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int i = 0; i < nv; ++i) {
+      const double w = exp(s[i] - M);
+      const float *vr = V + ((int64_t)vis[i] * Hkv + kh) * D;
+      l += w;
+      for (int d = 0; d < D; ++d) o[d] += w * (double)vr[d];
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    if (lse) lse[r] = M + log(l);
+  }
+  free(vis);
+  free(s);
+  return 0;
+}

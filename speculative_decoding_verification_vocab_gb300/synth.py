@@ -271,3 +271,45 @@ def kv_cache(L, B, S, H, D, device="cpu", seed=0, dtype=torch.bfloat16):
     raw = torch.randint(0, 256, (L, 2, B, S, H, D * esize), generator=g, device=device,
                         dtype=torch.uint8)
     return raw.view(dtype)
+
+
+def level_tree_parents(B, T, depth, seed=0, device="cpu"):
+    """Random draft trees shaped like the dynamic tree: T slots (root included)
+    numbered level by level over `depth` levels of near-equal size; the parent
+    of each node is drawn uniformly from the level above.  int32 [B][T]."""
+    g = _gen(seed + 29, "cpu")
+    n = T - 1
+    sizes = [n // depth + (1 if lv < n % depth else 0) for lv in range(depth)] if depth else []
+    parent = torch.full((B, T), -1, dtype=torch.int32)
+    prev_lo, prev_hi, nxt = 0, 1, 1
+    for sz in sizes:
+        if sz == 0:
+            break
+        parent[:, nxt:nxt + sz] = torch.randint(prev_lo, prev_hi, (B, sz), generator=g,
+                                                dtype=torch.int32)
+        prev_lo, prev_hi, nxt = nxt, nxt + sz, nxt + sz
+    return parent.to(device)
+
+
+BF16_NAN = 0x7FC0
+
+
+def attention_inputs(B, T, Hq, Hkv, D, S, base, seed=0, device="cpu", sigma=1.0,
+                     poison_tail=True):
+    """Tree-attention inputs: queries q [B][T][Hq][D] and one layer of the
+    cache kv [2][B][S][Hkv][D] (K then V), bf16, iid N(0, sigma^2).  `base`
+    (int or [B]) is each sequence's committed length; tree node n's K/V row is
+    slot base + n.  With poison_tail the slots from base + T on hold NaN, which
+    no output may depend on.  Returns (q, kv, base int32 [B])."""
+    g = _gen(seed + 31, device)
+    if isinstance(base, int):
+        base = [base] * B
+    base_t = torch.tensor(base, dtype=torch.int32)
+    q = (torch.randn((B, T, Hq, D), generator=g, device=device) * sigma).to(torch.bfloat16)
+    kv = (torch.randn((2, B, S, Hkv, D), generator=g, device=device) * sigma).to(torch.bfloat16)
+    if poison_tail:
+        nan = torch.tensor(BF16_NAN, dtype=torch.int16).view(torch.bfloat16).item()
+        for b, bs in enumerate(base):
+            if 0 <= bs and bs + T < S:
+                kv[:, b, bs + T:] = nan
+    return q, kv, base_t.to(device)
