@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences the oracle times")
     ap.add_argument("--tree-build", action="store_true",
                     help="time the GPU dynamic-tree builder instead of the verify step")
+    ap.add_argument("--attention", action="store_true",
+                    help="time the tree-masked verifier attention (one layer) instead")
     ap.add_argument("--greedy", action="store_true",
                     help="temperature 0: greedy verification (verifier rows only, no sampling)")
     ap.add_argument("--batch", type=int, default=0,
@@ -718,12 +720,87 @@ def run_tree_build(args):
     print(json.dumps(line))
 
 
+def run_attention(args):
+    """--attention: the tree-masked verifier attention of one layer for the
+    dynamic-tree workload (B=128 trees of 60 nodes built over 6 levels, a
+    70B-shaped layer: 64 query heads on 8 KV heads of 128, bf16, context 4096),
+    one sv_tree_attention launch per step.  Every launch reads the 2.2 GB of
+    keys and values (larger than L2)."""
+    import torch
+    import speculative_decoding_verification_vocab_gb300 as sv
+    from speculative_decoding_verification_vocab_gb300 import synth
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load_library()
+    B, T, Hq, Hkv, D, ctx = args.batch or 128, 60, 64, 8, 128, 4096
+    S = ctx + 64
+    q, kv, base = synth.attention_inputs(B, T, Hq, Hkv, D, S, ctx, seed=rank_seed(3, rank),
+                                         device=dev)
+    parent = synth.level_tree_parents(B, T, 6, seed=rank_seed(3, rank)).to(dev)
+    mask, depth = sv.tree_build_mask(parent)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, T, Hq, dtype=torch.float32, device=dev)
+    status = torch.zeros(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    scale = D ** -0.5
+
+    def step():
+        sv.sv_tree_attention(q, kv, base, mask, scale, out, lse, status, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    n0 = sv.sv_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    launches = sv.sv_launch_count() - n0
+    assert int(torch.count_nonzero(status)) == 0
+    # algorithmic work: every (node, query head) row against its visible keys
+    vis = (base.double()[:, None] + depth.double() + 1.0).sum().item() * Hq
+    flops = 4.0 * D * vis
+    kv_bytes = 2.0 * (base.double() + T).sum().item() * Hkv * D * 2
+    io_bytes = kv_bytes + 2.0 * q.numel() * 2 + lse.numel() * 4
+    d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    peak, kind = (float(d["bf16_tflops"]), "measured") if d else (1900.0, "fallback")
+    hbm, _ = measured_peaks()
+    ach = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "tree-attention verifier rows/s (one layer)", "value":
+        B * T * Hq / (ms / 1e3), "unit": "query rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "tree attention, dynamic-tree shape: B=%d, T=60 (6 levels), "
+                               "Hq=64, Hkv=8, D=128, context 4096, bf16" % B,
+                   "l2": "inputs larger than L2: %.2f GB of keys and values per launch"
+                         % (kv_bytes / 1e9)},
+        "tflops": ach, "hbm_gbs": io_bytes / (ms / 1e3) / 1e9,
+        "hbm_frac_measured": io_bytes / (ms / 1e3) / 1e9 / hbm,
+        "gpu_launches": int(launches),
+        "roofline": {"kernel": "tree_attention", "bound": "tensor", "achieved": ach,
+                     "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                     "peak_kind": f"{kind} bf16 dense (burst)",
+                     "alg_flops_per_launch": flops, "traffic": None},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.tree_build:
         run_tree_build(args)
+    elif args.attention:
+        run_attention(args)
     else:
         run_ours(args)
 

@@ -72,6 +72,8 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_ROW_RESID_ZERO 4u /* residual mass was 0; the correction came from q */
 #define SV_ROW_P_ZERO 8u     /* a tested draft token had p(d) = 0 (draft logit -inf) and was accepted */
 #define SV_ROW_BAD_TREE 16u  /* parent/score arrays do not describe a tree */
+#define SV_ROW_BAD_BASE 32u  /* sv_tree_attention: base < 0 or base + T > S */
+#define SV_ROW_TIMEOUT 64u   /* sv_tree_attention: a wait on the device ran out */
 
 /* Build limits. */
 #define SV_MAX_VOCAB (1 << 22)  /* fixed-point sampling sums stay below 2^63 */
@@ -292,6 +294,42 @@ sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token
                            const float *cand_score, const int32_t *cand_level, int B,
                            int C, int T, int32_t *out_parent, int32_t *out_token,
                            float *out_score, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * sv_tree_attention -- tree-masked verifier attention, one layer.
+ * [Blog] section 3 (the flattened draft tree is scored in one verifier pass;
+ * each node attends to the committed context and to itself and its ancestors,
+ * never to a sibling or another branch); [Lesson] "Reversão de KV cache" (the
+ * tree pass runs a non-causal mask that follows the tree).  Grouped-query
+ * heads: query head h reads KV head h / (Hq / Hkv).
+ *
+ *   q     bf16 [B][T][Hq][D]      queries of the T tree nodes (node 0 = root)
+ *   kv    bf16 [2][B][S][Hkv][D]  this layer of the cache, K then V (one layer
+ *                                 of the [L][2][B][S][H][D] layout that
+ *                                 sv_kv_compact moves); node n's own K/V row
+ *                                 is slot base[b] + n
+ *   base  int32 [B]               committed length of each sequence
+ *   mask  uint64 [B][T][(T+63)/64] ancestor bitmask (sv_tree_build_mask)
+ *   scale > 0, finite             softmax scale (usually 1/sqrt(D))
+ *   out   bf16 [B][T][Hq][D]      softmax(scale * q K^T) V over the visible
+ *                                 keys
+ *   out_lse   fp32 [B][T][Hq] or NULL: natural log of sum exp(scale * q.k)
+ *   out_status uint32 [B] or NULL: SV_ROW_BAD_BASE / SV_ROW_TIMEOUT bits are
+ *                                 OR-ed in (zero it before the call)
+ * Row (b, n, h) sees key slots j < base[b] and base[b] + m for each m < T
+ * whose bit is set in node n's mask.  A row with no visible key gets 0 and
+ * lse -inf; a sequence with base < 0 or base + T > S gets NaN rows and
+ * SV_ROW_BAD_BASE.  Slots at or past base + T are never read into a result
+ * (they may hold anything); slots below it must be finite.
+ * D = 128 only, Hq / Hkv must divide 128 (else SV_ERR_UNSUPPORTED).  q and kv
+ * must be device memory (they are read by tensor-map copies) and q, kv, out
+ * 16-byte aligned.  The kernel keeps every wait bounded (2 s); a wait that
+ * runs out sets SV_ROW_TIMEOUT and the sequence's rows are left unwritten.
+ * --------------------------------------------------------------------------- */
+sv_status sv_tree_attention(const void *q, const void *kv, const int32_t *base,
+                            const uint64_t *mask, int B, int T, int Hq, int Hkv,
+                            int D, int S, float scale, void *out, float *out_lse,
+                            uint32_t *out_status, void *stream);
 
 /* Thread-local message for the last non-OK status returned on this thread. */
 const char *sv_last_error(void);

@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_PKG, "libsv.so")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_TIMEOUT = 0, 1, 2, 3, 4
 SV_F32, SV_BF16 = 0, 1
 SV_ROW_NAN, SV_ROW_BAD_TOKEN, SV_ROW_RESID_ZERO, SV_ROW_P_ZERO, SV_ROW_BAD_TREE = 1, 2, 4, 8, 16
+SV_ROW_BAD_BASE, SV_ROW_TIMEOUT = 32, 64
 SV_MAX_VOCAB, SV_MAX_POSITIONS, SV_MAX_TREE_NODES = 1 << 22, 1024, 1024
 
 EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_verify_chain",
            "sv_verify_chain_noalloc", "sv_verify_tree_workspace_host",
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
-           "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_last_error",
+           "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_tree_attention", "sv_last_error",
            "sv_launch_count", "sv_trace_enable", "sv_trace_collect", "sv_tree_expand",
            "sv_tree_select", "sv_tree_finalize")
 
@@ -83,6 +84,9 @@ def load_library(path: str = LIB_PATH):
     L.sv_kv_compact.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                 i32, i32, vp, vp]
     L.sv_kv_compact.restype = i32
+    L.sv_tree_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp,
+                                    vp, vp]
+    L.sv_tree_attention.restype = i32
     L.sv_last_error.argtypes = []
     L.sv_last_error.restype = C.c_char_p
     L.sv_launch_count.argtypes = []
@@ -214,6 +218,17 @@ def sv_kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add, 
         _p(src_kv), _p(dst_kv), L, B, S_src, S_dst, H, D, src_kv.element_size(),
         _p(src_base), _p(dst_base), _p(rows), _p(n_rows), int(n_rows_add), P,
         _p(out_kv_len), _stream(stream)))
+
+
+def sv_tree_attention(q, kv, base, mask, scale, out, out_lse=None, out_status=None,
+                      stream=None):
+    """q [B][T][Hq][D] bf16, kv [2][B][S][Hkv][D] bf16 (one layer), base [B] int32,
+    mask [B][T][W] (64-bit words), out like q."""
+    B, T, Hq, D = q.shape
+    S, Hkv = kv.shape[2], kv.shape[3]
+    return _check(load_library().sv_tree_attention(
+        _p(q), _p(kv), _p(base), _p(mask), B, T, Hq, Hkv, D, S, float(scale), _p(out),
+        _p(out_lse), _p(out_status), _stream(stream)))
 
 
 def sv_tree_expand(dlogits, frontier_score, K, out_token, out_score, temperature=1.0,
@@ -389,6 +404,20 @@ def tree_build_mask(parent, stream=None):
     depth = torch.empty(B, T, dtype=torch.int32, device=_out_dev(parent))
     sv_tree_build_mask(parent, mask, depth, stream)
     return mask, depth
+
+
+def tree_attention(q, kv, base, mask, scale=None, return_lse=False, stream=None):
+    """Tree-masked attention of one layer: returns out (like q), and with
+    return_lse the log-sum-exp [B][T][Hq] and the status words [B]."""
+    B, T, Hq, D = q.shape
+    if scale is None:
+        scale = D ** -0.5
+    dev = _out_dev(q)
+    out = torch.empty_like(q, device=dev)
+    lse = torch.empty(B, T, Hq, dtype=torch.float32, device=dev) if return_lse else None
+    status = torch.zeros(B, dtype=torch.int32, device=dev) if return_lse else None
+    sv_tree_attention(q, kv, base, mask, scale, out, lse, status, stream)
+    return (out, lse, status) if return_lse else out
 
 
 def kv_compact(src_kv, dst_kv, src_base, dst_base, rows, n_rows, n_rows_add=0, stream=None):

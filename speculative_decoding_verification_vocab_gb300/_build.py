@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["runtime.cu", "verify.cu", "tree_kv.cu", "tree_build.cu"]
+SOURCES = ["runtime.cu", "verify.cu", "tree_kv.cu", "tree_build.cu", "tree_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

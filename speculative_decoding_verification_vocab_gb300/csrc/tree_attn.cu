@@ -1,0 +1,637 @@
+// tree_attn.cu -- tree-masked verifier attention on the 5th-generation tensor
+// cores (sm_103a): TMA tile loads, tcgen05.mma with accumulators in tensor
+// memory, online softmax in registers.
+//
+// [Blog] "投机解码发展", section 3: the verifier scores the flattened draft tree
+// in one forward pass in which each node attends to the committed context and
+// to itself and its ancestors only (never to a sibling or another branch);
+// [Lesson] "Decodificação Especulativa e EAGLE-3", "Reversão de KV cache": the
+// tree pass runs a non-causal mask that follows the tree.  This is the
+// attention of that pass for one layer, with grouped-query heads.
+//
+// One CTA owns 128 query rows of one (sequence, KV head): the G = Hq / Hkv
+// query heads sharing that KV head times 128 / G consecutive tree nodes, row
+// r = node_local * G + head_local.  It walks the sequence's keys (context,
+// then the T tree rows) in tiles of 128:
+//   warp 0      TMA producer: the query tile once, then K and V tiles into a
+//               two-stage ring (128B-swizzled boxes of 64 columns);
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two S buffers in tensor
+//               memory, O += P_{j-1} V_{j-1} into the O accumulator;
+//   warps 2..5  softmax: S_j from tensor memory to registers (one row per
+//               thread), ancestor mask, running max with a lazy rescale of O
+//               (only when the max grows by more than 2^8), P_j = exp2(...)
+//               as bf16 into shared memory in the MMA's operand layout, then
+//               the epilogue O / l.
+// Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
+// out sets SV_ROW_TIMEOUT for the sequence and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kHd = 128;               // head dimension
+constexpr int kRows = 128;             // query rows per CTA = tensor-memory lanes
+constexpr int kKeys = 128;             // keys per tile
+constexpr int kAttnThreads = 192;      // 6 warps
+constexpr uint32_t kTile = 32768;      // one 128 x 128 bf16 operand tile
+constexpr uint32_t kHalfTile = 16384;  // one 128-byte-wide swizzled box of it
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTile;      // 2 stages
+constexpr uint32_t kOffV = kOffK + 2 * kTile;  // 2 stages
+constexpr uint32_t kOffP = kOffV + 2 * kTile;  // 2 buffers
+constexpr uint32_t kOffBar = kOffP + 2 * kTile;
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;
+constexpr size_t kAttnSmem = kOffMisc + 64 + 1024;  // + alignment slack
+// barrier indices
+constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarS = 5, kBarP = 7, kBarPV = 9;
+// tensor-memory columns: S buffers at 0 and 128, O at 256
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (log2 units)
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+struct AttnArgs {
+  const int32_t *base;
+  const uint64_t *mask;
+  uint16_t *out;
+  float *lse;
+  uint32_t *status;
+  int B, T, Hq, Hkv, S, G, W, npt;  // npt = tree nodes per CTA = 128 / G
+  float scale_log2;                 // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Gives up after kWaitNs
+// or as soon as another role of the CTA has given up (*abort != 0).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 4-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load4(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                          int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of tcgen05: start, leading and stride byte
+// offsets (16-byte units), the fixed 0b001 at bits 46-48, swizzle mode at
+// bits 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), N >> 3 at bit 17, M >> 4 at bit 24; bit 16 =
+// B is MN-major (the V tile: keys x head dim, head dim contiguous).
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKeys >> 3) << 17) |
+                             ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                             ((uint32_t)(kHd >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Bits [pos, pos + 32) of a node's ancestor mask (pos >= 0; words past W read 0).
+__device__ __forceinline__ uint32_t mask_bits32(const uint64_t *mrow, int W, int pos) {
+  const int w = pos >> 6, sh = pos & 63;
+  const uint64_t lo = w < W ? __ldg(mrow + w) : 0ull;
+  const uint64_t hi = (sh && w + 1 < W) ? __ldg(mrow + w + 1) : 0ull;
+  return (uint32_t)(sh ? (lo >> sh) | (hi << (64 - sh)) : lo);
+}
+
+// Visibility of keys base + rel + i, i = 0..31: context keys (rel + i < 0)
+// are visible, tree key m = rel + i < T iff bit m of the node's mask, keys at
+// or past base + T never.  mrow == nullptr (a padding row): context only.
+__device__ __forceinline__ uint32_t visible32(const uint64_t *mrow, int W, int T, int rel) {
+  const uint32_t pre = rel >= 0 ? 0u : (rel <= -32 ? 0xFFFFFFFFu : ((1u << (-rel)) - 1u));
+  if (rel <= -32 || rel >= T || mrow == nullptr) return pre;
+  uint32_t tree;
+  int nvalid;
+  if (rel >= 0) {
+    tree = mask_bits32(mrow, W, rel);
+    nvalid = T - rel;
+  } else {
+    tree = mask_bits32(mrow, W, 0) << (-rel);
+    nvalid = T - rel;
+  }
+  if (nvalid < 32) tree &= (1u << nvalid) - 1u;
+  return pre | tree;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    tree_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
+                     AttnArgs a) {
+  grid_dep_sync();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int mt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bs = a.base[b];
+  const int node0 = mt * a.npt;
+  // the softmax warps' row: warp w reads tensor-memory lanes 32 * (w % 4) + lane
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;
+  const int node = node0 + r / a.G;
+  const int head = kvh * a.G + r % a.G;
+  const bool row_ok = node < a.T;
+  const size_t orow = ((size_t)b * a.T + node) * a.Hq + head;
+
+  if (bs < 0 || (long long)bs + a.T > a.S) {
+    // base out of range: NaN rows, nothing read
+    if (warp >= 2 && row_ok) {
+      uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd);
+      for (int c = 0; c < kHd / 8; ++c) o[c] = nan4;
+      if (a.lse) a.lse[orow] = __int_as_float(0x7FC00000);
+    }
+    if (threadIdx.x == 0 && a.status && mt == 0 && kvh == 0) atomicOr(a.status + b, SV_ROW_BAD_BASE);
+    return;
+  }
+  const int n_keys = bs + a.T;
+  const int n_tiles = (n_keys + kKeys - 1) / kKeys;
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+  volatile int *abort = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  const uint32_t bar0 = smem_addr(bars);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  const uint32_t sQ = smem_addr(sm + kOffQ), sK = smem_addr(sm + kOffK),
+                 sV = smem_addr(sm + kOffV), sP = smem_addr(sm + kOffP);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarK + s), 1);
+      mbar_init(bar(kBarV + s), 1);
+      mbar_init(bar(kBarS + s), 1);
+      mbar_init(bar(kBarP + s), 4);
+      mbar_init(bar(kBarPV + s), 1);
+    }
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      mbar_expect_tx(bar(kBarQ), kTile);
+      tma_load4(sQ, &tq, 0, kvh * a.G, node0, b, bar(kBarQ));
+      tma_load4(sQ + kHalfTile, &tq, 64, kvh * a.G, node0, b, bar(kBarQ));
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(bar(kBarPV + st), ((j - 2) >> 1) & 1, abort)) break;
+        const int key0 = j * kKeys;
+        mbar_expect_tx(bar(kBarK + st), kTile);
+        tma_load4(sK + st * kTile, &tkv, 0, kvh, key0, b, bar(kBarK + st));
+        tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, kvh, key0, b, bar(kBarK + st));
+        mbar_expect_tx(bar(kBarV + st), kTile);
+        tma_load4(sV + st * kTile, &tkv, 0, kvh, key0, a.B + b, bar(kBarV + st));
+        tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, key0, a.B + b, bar(kBarV + st));
+        issued = j + 1;
+      }
+      // every copy issued has landed before the CTA exits (immediate unless a
+      // consumer gave up early); the last two tiles are the last phases of
+      // their stage barriers, so the parity test cannot alias
+      volatile int no_abort = 0;
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) {
+        mbar_wait(bar(kBarK + (j & 1)), (j >> 1) & 1, &no_abort);
+        mbar_wait(bar(kBarV + (j & 1)), (j >> 1) & 1, &no_abort);
+      }
+      mbar_wait(bar(kBarQ), 0, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    bool ok = mbar_wait(bar(kBarQ), 0, abort);
+    int s_issued = 0, pv_issued = 0;  // S and PV tiles committed so far
+    tc_fence_after();
+    for (int j = 0; ok && j <= n_tiles; ++j) {
+      if (j < n_tiles) {
+        const int st = j & 1;
+        ok = mbar_wait(bar(kBarK + st), (j >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < kHd / 16; ++ks) {
+            const uint32_t koff = (ks >> 2) * kHalfTile + (ks & 3) * 32;
+            mma_bf16(tmem + st * kKeys, sdesc(sQ + koff, 16, 1024),
+                     sdesc(sK + st * kTile + koff, 16, 1024), kIdescS, ks > 0);
+          }
+          mma_commit(bar(kBarS + st));
+        }
+        __syncwarp();
+        s_issued = j + 1;
+      }
+      if (j >= 1) {
+        const int i = j - 1, sp = i & 1;
+        ok = mbar_wait(bar(kBarP + sp), (i >> 1) & 1, abort) &&
+             mbar_wait(bar(kBarV + sp), (i >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (i == n_tiles - 1) {
+          // value rows past the last key may hold anything (NaN included):
+          // zero them so that P = 0 there contributes exactly 0
+          const int rem = n_keys - i * kKeys;
+          uint8_t *vt = sm + kOffV + sp * kTile;
+          const int nz = (kKeys - rem) * 8;  // 16-byte chunks per half
+          for (int c = lane; c < 2 * nz; c += 32) {
+            const int h = c / nz, k = c % nz;
+            *reinterpret_cast<uint4 *>(vt + h * kHalfTile + rem * 128 + k * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint32_t poff = (ks >> 2) * kHalfTile + (ks & 3) * 32;
+            mma_bf16(tmem + kColO, sdesc(sP + sp * kTile + poff, 16, 1024),
+                     sdesc(sV + sp * kTile + ks * 16 * 128, kHalfTile, 1024), kIdescO,
+                     (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarPV + sp));
+        }
+        __syncwarp();
+        pv_issued = j;
+      }
+    }
+    if (!ok) {
+      // retire the MMAs in flight before tensor memory is released: the last
+      // S and the last PV commit are the newest phases of their barriers
+      volatile int no_abort = 0;
+      if (s_issued > 0) {
+        const int i = s_issued - 1;
+        mbar_wait(bar(kBarS + (i & 1)), (i >> 1) & 1, &no_abort);
+      }
+      if (pv_issued > 0) {
+        const int i = pv_issued - 1;
+        mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, &no_abort);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const uint64_t *mrow = row_ok ? a.mask + ((size_t)b * a.T + node) * a.W : nullptr;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const float NEG_INF = -INFINITY;
+    float m_ref = NEG_INF;  // reference max (log2 domain, scaled)
+    float l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      ok = mbar_wait(bar(kBarS + st), (j >> 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 32) tm_ld32(tmem + lane_off + st * kKeys + c, s + c);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      const int key0 = j * kKeys;
+      if (key0 + kKeys > bs) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t vis = visible32(mrow, a.W, a.T, key0 + 32 * c4 - bs);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (!((vis >> c) & 1u)) s[32 * c4 + c] = NEG_INF;
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
+      mx *= a.scale_log2;  // scale > 0: max commutes with it
+      const bool grow = mx > m_ref + kRescaleLog2;
+      const float m_new = grow ? mx : m_ref;
+      const float factor = (grow && m_ref != NEG_INF) ? ex2(m_ref - m_new) : 1.0f;
+      if (__any_sync(0xffffffffu, factor != 1.0f)) {
+        // O holds tiles 0..j-1: wait for the last of them, then rescale it
+        const int i = j - 1;
+        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kHd; c += 32) {
+          float o[32];
+          tm_ld32(tmem + lane_off + kColO + c, o);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] *= factor;
+          tm_st32(tmem + lane_off + kColO + c, o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      l *= factor;
+      m_ref = m_new;
+      const float mneg = m_ref == NEG_INF ? 0.0f : -m_ref;
+      if (j >= 2) {
+        // P buffer st was last read by the PV of tile j - 2
+        ok = mbar_wait(bar(kBarPV + st), ((j - 2) >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      uint8_t *prow = sm + kOffP + st * kTile + r * 128;
+      float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) p[k] = ex2(fmaf(s[8 * c8 + k], a.scale_log2, mneg));
+        l0 += (p[0] + p[2]) + (p[4] + p[6]);
+        l1 += (p[1] + p[3]) + (p[5] + p[7]);
+        const uint4 w = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                                   pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
+        const int h = c8 >> 3, ch = c8 & 7;
+        *reinterpret_cast<uint4 *>(prow + h * kHalfTile + ((ch ^ (r & 7)) << 4)) = w;
+      }
+      l += l0 + l1;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarP + st));
+    }
+    if (ok) {
+      const int i = n_tiles - 1;
+      ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd);
+#pragma unroll
+      for (int c = 0; c < kHd; c += 32) {
+        float v[32];
+        tm_ld32(tmem + lane_off + kColO + c, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (row_ok) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 8)
+            o[(c + k) / 8] = make_uint4(pack_bf16(v[k] * inv, v[k + 1] * inv),
+                                        pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
+                                        pack_bf16(v[k + 4] * inv, v[k + 5] * inv),
+                                        pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
+        }
+      }
+      if (row_ok && a.lse)
+        a.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0 && a.status) atomicOr(a.status + b, SV_ROW_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (the library
+// does not link libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// 4-D bf16 map with 128-byte swizzle; dims innermost first, strides in bytes
+// for dims 1..3, box {64, b1, b2, 1}.
+sv_status encode4(CUtensorMap *m, const void *base, const cuuint64_t dims[4],
+                  const cuuint64_t strides[3], cuuint32_t b1, cuuint32_t b2, const char *what) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(SV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const cuuint32_t box[4] = {64, b1, b2, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(SV_ERR_CUDA, "tensor map for %s: error %d", what, (int)r);
+  return SV_OK;
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int32_t *base,
+                                       const uint64_t *mask, int B, int T, int Hq, int Hkv, int D,
+                                       int S, float scale, void *out, float *out_lse,
+                                       uint32_t *out_status, void *stream) {
+  if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || S < 1)
+    return set_error(SV_ERR_INVALID_ARG, "need B >= 0, T >= 1, Hq >= 1, Hkv >= 1, S >= 1");
+  if (T > SV_MAX_TREE_NODES) return set_error(SV_ERR_UNSUPPORTED, "T > %d", SV_MAX_TREE_NODES);
+  if (D != kHd) return set_error(SV_ERR_UNSUPPORTED, "head dimension %d (only 128)", D);
+  if (Hq % Hkv) return set_error(SV_ERR_INVALID_ARG, "Hq must be a multiple of Hkv");
+  const int G = Hq / Hkv;
+  if (G > kRows || (kRows % G)) return set_error(SV_ERR_UNSUPPORTED, "Hq / Hkv must divide 128");
+  if (!(scale > 0.0f) || !isfinite(scale)) return set_error(SV_ERR_INVALID_ARG, "scale must be > 0");
+  if (Hkv > 65535 || B > 65535) return set_error(SV_ERR_UNSUPPORTED, "Hkv or B above 65535");
+  if (B == 0) return SV_OK;
+  if (!q || !kv || !base || !mask || !out) return set_error(SV_ERR_INVALID_ARG, "null pointer");
+  if (!is_device_memory(q) || !is_device_memory(kv))
+    return set_error(SV_ERR_INVALID_ARG, "q and kv must be device memory (tensor-map loads)");
+  if ((uintptr_t)q % 16 || (uintptr_t)kv % 16 || (uintptr_t)out % 16 || (uintptr_t)mask % 8)
+    return set_error(SV_ERR_INVALID_ARG, "q, kv, out need 16-byte and mask 8-byte alignment");
+  sv_status s;
+  if ((s = map_arg(base, "base")) != SV_OK || (s = map_arg(mask, "mask")) != SV_OK ||
+      (s = map_arg(out, "out")) != SV_OK || (s = map_arg(out_lse, "out_lse")) != SV_OK ||
+      (s = map_arg(out_status, "out_status")) != SV_OK)
+    return s;
+  const int npt = kRows / G;
+  CUtensorMap tq, tkv;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hq, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t str[3] = {(cuuint64_t)kHd * 2, (cuuint64_t)Hq * kHd * 2,
+                               (cuuint64_t)T * Hq * kHd * 2};
+    if ((s = encode4(&tq, q, dims, str, (cuuint32_t)G, (cuuint32_t)npt, "q")) != SV_OK) return s;
+  }
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hkv, (cuuint64_t)S,
+                                (cuuint64_t)2 * B};
+    const cuuint64_t str[3] = {(cuuint64_t)kHd * 2, (cuuint64_t)Hkv * kHd * 2,
+                               (cuuint64_t)S * Hkv * kHd * 2};
+    if ((s = encode4(&tkv, kv, dims, str, 1, (cuuint32_t)kKeys, "kv")) != SV_OK) return s;
+  }
+  static int smem_set_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem_set_dev != dev) {
+    const cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kAttnSmem);
+    if (e != cudaSuccess) return check_launch("tree_attention", e);
+    smem_set_dev = dev;
+  }
+  AttnArgs a;
+  a.base = base;
+  a.mask = mask;
+  a.out = (uint16_t *)out;
+  a.lse = out_lse;
+  a.status = out_status;
+  a.B = B;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.S = S;
+  a.G = G;
+  a.W = (T + 63) / 64;
+  a.npt = npt;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int mtiles = (T + npt - 1) / npt;
+  cudaStream_t st = (cudaStream_t)stream;
+  LaunchScope ls("tree_attention", st);
+  return check_launch("tree_attention",
+                      launch_pdl(tree_attn_kernel, dim3(mtiles, Hkv, B), dim3(kAttnThreads),
+                                 kAttnSmem, st, tq, tkv, a));
+}
