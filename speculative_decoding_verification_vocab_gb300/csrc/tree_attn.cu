@@ -17,11 +17,13 @@
 //               two-stage ring (128B-swizzled boxes of 64 columns);
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two S buffers in tensor
 //               memory, O += P_{j-1} V_{j-1} into the O accumulator;
-//   warps 2..5  softmax: S_j from tensor memory to registers (one row per
-//               thread), ancestor mask, running max with a lazy rescale of O
-//               (only when the max grows by more than 2^8), P_j = exp2(...)
-//               as bf16 into shared memory in the MMA's operand layout, then
-//               the epilogue O / l.
+//   warps 2..9  softmax, two warps per tensor-memory lane quarter (one row
+//               per thread, half of the key columns each): S_j from tensor
+//               memory to registers, ancestor mask, row max shared by the
+//               pair, running max with a lazy rescale of O (only when the max
+//               grows by more than 2^8), P_j = exp2(...) as bf16 into the
+//               single shared-memory P buffer in the MMA's operand layout,
+//               then the epilogue O / l.
 // Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
 // out sets SV_ROW_TIMEOUT for the sequence and the CTA drains and exits.
 #include <cuda.h>
@@ -37,18 +39,19 @@ namespace {
 constexpr int kHd = 128;               // head dimension
 constexpr int kRows = 128;             // query rows per CTA = tensor-memory lanes
 constexpr int kKeys = 128;             // keys per tile
-constexpr int kAttnThreads = 192;      // 6 warps
+constexpr int kAttnThreads = 320;      // 10 warps
 constexpr uint32_t kTile = 32768;      // one 128 x 128 bf16 operand tile
 constexpr uint32_t kHalfTile = 16384;  // one 128-byte-wide swizzled box of it
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTile;      // 2 stages
 constexpr uint32_t kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTile;  // 2 buffers
-constexpr uint32_t kOffBar = kOffP + 2 * kTile;
-constexpr uint32_t kOffMisc = kOffBar + 16 * 8;
-constexpr size_t kAttnSmem = kOffMisc + 64 + 1024;  // + alignment slack
-// barrier indices
-constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarS = 5, kBarP = 7, kBarPV = 9;
+constexpr uint32_t kOffP = kOffV + 2 * kTile;  // 1 buffer
+constexpr uint32_t kOffBar = kOffP + kTile;
+constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
+constexpr uint32_t kOffXchg = kOffMisc + 64;   // float [2 parity][2 half][128 rows]
+constexpr size_t kAttnSmem = kOffXchg + 2048 + 1024;  // + alignment slack
+// barrier indices; kBarX + 2 * quarter + parity: the softmax pair's exchange
+constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarS = 5, kBarP = 7, kBarPV = 9, kBarX = 11;
 // tensor-memory columns: S buffers at 0 and 128, O at 256
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -88,8 +91,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase of `parity` to complete.  Gives up after kWaitNs
 // or as soon as another role of the CTA has given up (*abort != 0).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
@@ -101,6 +103,10 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bs = a.base[b];
   const int node0 = mt * a.npt;
-  // the softmax warps' row: warp w reads tensor-memory lanes 32 * (w % 4) + lane
+  // a softmax warp's row: warp w reads tensor-memory lanes 32 * (w % 4) + lane
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;
   const int node = node0 + r / a.G;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (bs < 0 || (long long)bs + a.T > a.S) {
     // base out of range: NaN rows, nothing read
-    if (warp >= 2 && row_ok) {
+    if (warp >= 2 && warp < 6 && row_ok) {
       uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
       uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd);
       for (int c = 0; c < kHd / 8; ++c) o[c] = nan4;
@@ -283,9 +289,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(kBarK + s), 1);
       mbar_init(bar(kBarV + s), 1);
       mbar_init(bar(kBarS + s), 1);
-      mbar_init(bar(kBarP + s), 4);
+      mbar_init(bar(kBarP + s), 8);
       mbar_init(bar(kBarPV + s), 1);
     }
+    for (int x = 0; x < 8; ++x) mbar_init(bar(kBarX + x), 2);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -307,27 +314,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_expect_tx(bar(kBarQ), kTile);
       tma_load4(sQ, &tq, 0, kvh * a.G, node0, b, bar(kBarQ));
       tma_load4(sQ + kHalfTile, &tq, 64, kvh * a.G, node0, b, bar(kBarQ));
-      int issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
+      // K_j may overwrite its stage once S_{j-2} has retired, V_j once PV_{j-2}
+      // has; the MMA warp retires them in the order S_0, S_1, PV_0, S_2, PV_1,
+      // S_3, ..., so the loads follow it: K_{i+3} after S_{i+1}, then V_{i+2}
+      // after PV_i.
+      auto load_k = [&](int j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(bar(kBarPV + st), ((j - 2) >> 1) & 1, abort)) break;
-        const int key0 = j * kKeys;
         mbar_expect_tx(bar(kBarK + st), kTile);
-        tma_load4(sK + st * kTile, &tkv, 0, kvh, key0, b, bar(kBarK + st));
-        tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, kvh, key0, b, bar(kBarK + st));
+        tma_load4(sK + st * kTile, &tkv, 0, kvh, j * kKeys, b, bar(kBarK + st));
+        tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, b, bar(kBarK + st));
+      };
+      auto load_v = [&](int j) {
+        const int st = j & 1;
         mbar_expect_tx(bar(kBarV + st), kTile);
-        tma_load4(sV + st * kTile, &tkv, 0, kvh, key0, a.B + b, bar(kBarV + st));
-        tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, key0, a.B + b, bar(kBarV + st));
-        issued = j + 1;
+        tma_load4(sV + st * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + st));
+        tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + st));
+      };
+      int kn = 0, vn = 0;  // K and V tiles issued
+      for (; kn < 2 && kn < n_tiles; ++kn, ++vn) {
+        load_k(kn);
+        load_v(kn);
+      }
+      if (n_tiles > 2 && mbar_wait(bar(kBarS), 0, abort)) load_k(kn++);
+      for (int i = 0; !*abort && (kn < n_tiles || vn < n_tiles); ++i) {
+        if (kn < n_tiles) {
+          if (!mbar_wait(bar(kBarS + ((i + 1) & 1)), ((i + 1) >> 1) & 1, abort)) break;
+          load_k(kn++);
+        }
+        if (vn < n_tiles) {
+          if (!mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort)) break;
+          load_v(vn++);
+        }
       }
       // every copy issued has landed before the CTA exits (immediate unless a
-      // consumer gave up early); the last two tiles are the last phases of
-      // their stage barriers, so the parity test cannot alias
+      // consumer gave up early); the last two tiles of each ring are the last
+      // phases of their stage barriers, so the parity test cannot alias
       volatile int no_abort = 0;
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) {
+      for (int j = kn > 2 ? kn - 2 : 0; j < kn; ++j)
         mbar_wait(bar(kBarK + (j & 1)), (j >> 1) & 1, &no_abort);
+      for (int j = vn > 2 ? vn - 2 : 0; j < vn; ++j)
         mbar_wait(bar(kBarV + (j & 1)), (j >> 1) & 1, &no_abort);
-      }
       mbar_wait(bar(kBarQ), 0, &no_abort);
     }
   } else if (warp == 1) {
@@ -379,7 +405,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kKeys / 16; ++ks) {
             const uint32_t poff = (ks >> 2) * kHalfTile + (ks & 3) * 32;
-            mma_bf16(tmem + kColO, sdesc(sP + sp * kTile + poff, 16, 1024),
+            mma_bf16(tmem + kColO, sdesc(sP + poff, 16, 1024),
                      sdesc(sV + sp * kTile + ks * 16 * 128, kHalfTile, 1024), kIdescO,
                      (i > 0 || ks > 0) ? 1u : 0u);
           }
@@ -404,11 +430,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax
+    // warps w and w + 4 share tensor-memory lane quarter w % 4 (the same 32
+    // rows); the first takes key columns 0..63 of each tile and head-dim
+    // columns 0..63 of O, the second the upper 64.  The pair exchanges its
+    // partial row maxima (and at the end the partial sums) through shared
+    // memory and a two-arrival mbarrier per tile parity.
+    const int half = (warp - 2) >> 2;
     const uint64_t *mrow = row_ok ? a.mask + ((size_t)b * a.T + node) * a.W : nullptr;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float *xchg = reinterpret_cast<float *>(sm + kOffXchg);
     const float NEG_INF = -INFINITY;
     float m_ref = NEG_INF;  // reference max (log2 domain, scaled)
-    float l = 0.0f;
+    float l = 0.0f;         // partial sum over this warp's key columns
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
@@ -416,69 +449,90 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[kKeys];
-#pragma unroll
-      for (int c = 0; c < kKeys; c += 32) tm_ld32(tmem + lane_off + st * kKeys + c, s + c);
+      float s[64];
+      tm_ld32(tmem + lane_off + st * kKeys + 64 * half, s);
+      tm_ld32(tmem + lane_off + st * kKeys + 64 * half + 32, s + 32);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int key0 = j * kKeys;
-      if (key0 + kKeys > bs) {
+      const int key0 = j * kKeys + 64 * half;
+      if (key0 + 64 > bs) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c4 = 0; c4 < 2; ++c4) {
           const uint32_t vis = visible32(mrow, a.W, a.T, key0 + 32 * c4 - bs);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (!((vis >> c) & 1u)) s[32 * c4 + c] = NEG_INF;
         }
       }
-      float mx = s[0];
+      float pm[8];
 #pragma unroll
-      for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
-      mx *= a.scale_log2;  // scale > 0: max commutes with it
+      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+      for (int c = 16; c < 64; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[c + k]);
+      const float mine = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      float *xs = xchg + st * 256;
+      xs[half * 128 + r] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + st));
+      ok = mbar_wait(bar(kBarX + 2 * quarter + st), (j >> 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const float mx = fmaxf(mine, xs[(half ^ 1) * 128 + r]) * a.scale_log2;  // scale > 0
       const bool grow = mx > m_ref + kRescaleLog2;
       const float m_new = grow ? mx : m_ref;
       const float factor = (grow && m_ref != NEG_INF) ? ex2(m_ref - m_new) : 1.0f;
+      bool o_ready = j == 0;  // the PV of tile j - 1 has retired
       if (__any_sync(0xffffffffu, factor != 1.0f)) {
-        // O holds tiles 0..j-1: wait for the last of them, then rescale it
+        // O holds tiles 0..j-1: wait for the last of them, then rescale this
+        // warp's half of it
         const int i = j - 1;
         ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        o_ready = true;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kHd; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           float o[32];
-          tm_ld32(tmem + lane_off + kColO + c, o);
+          tm_ld32(tmem + lane_off + kColO + 64 * half + c, o);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] *= factor;
-          tm_st32(tmem + lane_off + kColO + c, o);
+          tm_st32(tmem + lane_off + kColO + 64 * half + c, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       l *= factor;
       m_ref = m_new;
       const float mneg = m_ref == NEG_INF ? 0.0f : -m_ref;
-      if (j >= 2) {
-        // P buffer st was last read by the PV of tile j - 2
-        ok = mbar_wait(bar(kBarPV + st), ((j - 2) >> 1) & 1, abort);
+      uint32_t pk[32];
+      float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float p0 = ex2(fmaf(s[c], a.scale_log2, mneg));
+        const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, mneg));
+        const float p2 = ex2(fmaf(s[c + 2], a.scale_log2, mneg));
+        const float p3 = ex2(fmaf(s[c + 3], a.scale_log2, mneg));
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        pk[c / 2] = pack_bf16(p0, p1);
+        pk[c / 2 + 1] = pack_bf16(p2, p3);
+      }
+      l += l0 + l1;
+      if (!o_ready) {
+        // the single P buffer was last read by the PV of tile j - 1
+        const int i = j - 1;
+        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
-      uint8_t *prow = sm + kOffP + st * kTile + r * 128;
-      float l0 = 0.0f, l1 = 0.0f;
+      uint8_t *prow = sm + kOffP + half * kHalfTile + r * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < kKeys / 8; ++c8) {
-        float p[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) p[k] = ex2(fmaf(s[8 * c8 + k], a.scale_log2, mneg));
-        l0 += (p[0] + p[2]) + (p[4] + p[6]);
-        l1 += (p[1] + p[3]) + (p[5] + p[7]);
-        const uint4 w = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                   pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-        const int h = c8 >> 3, ch = c8 & 7;
-        *reinterpret_cast<uint4 *>(prow + h * kHalfTile + ((ch ^ (r & 7)) << 4)) = w;
-      }
-      l += l0 + l1;
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -490,25 +544,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd);
+      // total row sum: the partner's partial through the exchange slot of the
+      // parity after the last tile (free: both passed the last exchange)
+      const int px = n_tiles & 1;
+      float *xs = xchg + px * 256;
+      xs[half * 128 + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + px));
+      ok = mbar_wait(bar(kBarX + 2 * quarter + px), (n_tiles >> 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        const float lt = l + xs[(half ^ 1) * 128 + r];
+        tc_fence_after();
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+        uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd + 64 * half);
 #pragma unroll
-      for (int c = 0; c < kHd; c += 32) {
-        float v[32];
-        tm_ld32(tmem + lane_off + kColO + c, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (row_ok) {
+        for (int c = 0; c < 64; c += 32) {
+          float v[32];
+          tm_ld32(tmem + lane_off + kColO + 64 * half + c, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (row_ok) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 8)
-            o[(c + k) / 8] = make_uint4(pack_bf16(v[k] * inv, v[k + 1] * inv),
-                                        pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
-                                        pack_bf16(v[k + 4] * inv, v[k + 5] * inv),
-                                        pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
+            for (int k = 0; k < 32; k += 8)
+              o[(c + k) / 8] = make_uint4(pack_bf16(v[k] * inv, v[k + 1] * inv),
+                                          pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
+                                          pack_bf16(v[k + 4] * inv, v[k + 5] * inv),
+                                          pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
+          }
         }
+        if (row_ok && half == 0 && a.lse)
+          a.lse[orow] = lt > 0.0f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : NEG_INF;
       }
-      if (row_ok && a.lse)
-        a.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * 0.69314718055994531f : NEG_INF;
     }
   }
   tc_fence_before();
