@@ -15,15 +15,16 @@
 // then the T tree rows) in tiles of 128:
 //   warp 0      TMA producer: the query tile once, then K and V tiles into a
 //               two-stage ring (128B-swizzled boxes of 64 columns);
-//   warp 1      MMA issuer: S_j = Q K_j^T into one of two S buffers in tensor
-//               memory, O += P_{j-1} V_{j-1} into the O accumulator;
-//   warps 2..9  softmax, two warps per tensor-memory lane quarter (one row
-//               per thread, half of the key columns each): S_j from tensor
-//               memory to registers, ancestor mask, row max shared by the
-//               pair, running max with a lazy rescale of O (only when the max
-//               grows by more than 2^8), P_j = exp2(...) as bf16 into the
-//               single shared-memory P buffer in the MMA's operand layout,
-//               then the epilogue O / l.
+//   warp 1      MMA issuer: S_j = Q K_j^T into S buffer j mod 2 in tensor
+//               memory, O_{j mod 2} += P_j V_j;
+//   warps 2..9  softmax, two warpgroups: warpgroup g takes the key tiles
+//               j = g mod 2 (one row per thread), with its own S buffer, P
+//               buffer and O accumulator: S_j from tensor memory to
+//               registers, ancestor mask, running max with a lazy rescale of
+//               O_g (only when the max grows by more than 2^8), P_j =
+//               exp2(...) as bf16 into shared memory in the MMA's operand
+//               layout.  At the end the two partial results (m, l, O_g) of a
+//               row are merged and normalised.
 // Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
 // out sets SV_ROW_TIMEOUT for the sequence and the CTA drains and exits.
 #include <cuda.h>
@@ -42,23 +43,27 @@ constexpr int kKeys = 128;             // keys per tile
 constexpr int kAttnThreads = 320;      // 10 warps
 constexpr uint32_t kTile = 32768;      // one 128 x 128 bf16 operand tile
 constexpr uint32_t kHalfTile = 16384;  // one 128-byte-wide swizzled box of it
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTile;      // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kTile;  // 1 buffer
-constexpr uint32_t kOffBar = kOffP + kTile;
+constexpr int kStages = 3;             // K and V ring depth
+constexpr uint32_t kOffK = 0;                        // kStages K tiles
+constexpr uint32_t kOffV = kOffK + kStages * kTile;  // kStages V tiles
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
-constexpr uint32_t kOffXchg = kOffMisc + 64;   // float [2 parity][2 half][128 rows]
+constexpr uint32_t kOffXchg = kOffMisc + 64;  // float [2 parity][2 half][128 rows]
 constexpr size_t kAttnSmem = kOffXchg + 2048 + 1024;  // + alignment slack
-// barrier indices; kBarX + 2 * quarter + parity: the softmax pair's exchange
-constexpr int kBarQ = 0, kBarK = 1, kBarV = 3, kBarS = 5, kBarP = 7, kBarPV = 9, kBarX = 11;
-// tensor-memory columns: S buffers at 0 and 128, O at 256
-constexpr uint32_t kColO = 256;
+// barrier indices: K/V landed and stage free (per stage), S ready / read out,
+// P ready and PV retired (per parity), the pair exchanges (2 per quarter)
+constexpr int kBarQ = 0, kBarK = 1, kBarV = kBarK + kStages, kBarKF = kBarV + kStages,
+              kBarVF = kBarKF + kStages, kBarS = kBarVF + kStages, kBarSF = kBarS + 2,
+              kBarP = kBarSF + 2, kBarPV = kBarP + 2, kBarX = kBarPV + 2;
+// tensor-memory columns: S buffers at 0 and 128, O at 256, Q (bf16 pairs) at
+// 384, P (bf16 pairs) at 448
+constexpr uint32_t kColO = 256, kColQ = 384, kColP = 448;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (log2 units)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
 
 struct AttnArgs {
+  const uint16_t *q;
   const int32_t *base;
   const uint64_t *mask;
   uint16_t *out;
@@ -109,6 +114,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
 }
 
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One lane of the (converged) warp: true there, false elsewhere.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -148,12 +174,15 @@ constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kK
 constexpr uint32_t kIdescO = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                              ((uint32_t)(kHd >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t acc) {
+// D (+)= A * B with the A operand in tensor memory (rows on lanes, K as bf16
+// pairs, the even element in the low half: one K16 slice = 8 columns) and B
+// in shared memory.
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -204,6 +233,10 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const float *v) {
       : "memory");
 }
 
+__device__ __forceinline__ void tm_st32u(uint32_t taddr, const uint32_t *v) {
+  tm_st32(taddr, reinterpret_cast<const float *>(v));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -244,8 +277,7 @@ __device__ __forceinline__ uint32_t visible32(const uint64_t *mrow, int W, int T
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    tree_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
-                     AttnArgs a) {
+    tree_attn_kernel(const __grid_constant__ CUtensorMap tkv, AttnArgs a) {
   grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -280,15 +312,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int *abort = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  const uint32_t sQ = smem_addr(sm + kOffQ), sK = smem_addr(sm + kOffK),
-                 sV = smem_addr(sm + kOffV), sP = smem_addr(sm + kOffP);
+  const uint32_t sK = smem_addr(sm + kOffK), sV = smem_addr(sm + kOffV);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(bar(kBarQ), 8);
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarK + s), 1);
       mbar_init(bar(kBarV + s), 1);
+      mbar_init(bar(kBarKF + s), 1);
+      mbar_init(bar(kBarVF + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarS + s), 1);
+      mbar_init(bar(kBarSF + s), 8);
       mbar_init(bar(kBarP + s), 8);
       mbar_init(bar(kBarPV + s), 1);
     }
@@ -311,109 +347,148 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      mbar_expect_tx(bar(kBarQ), kTile);
-      tma_load4(sQ, &tq, 0, kvh * a.G, node0, b, bar(kBarQ));
-      tma_load4(sQ + kHalfTile, &tq, 64, kvh * a.G, node0, b, bar(kBarQ));
-      // K_j may overwrite its stage once S_{j-2} has retired, V_j once PV_{j-2}
-      // has; the MMA warp retires them in the order S_0, S_1, PV_0, S_2, PV_1,
-      // S_3, ..., so the loads follow it: K_{i+3} after S_{i+1}, then V_{i+2}
-      // after PV_i.
+      // K_j goes to stage j % kStages once S_{j-kStages} has read that stage
+      // (kBarKF), V_j once PV_{j-kStages} has (kBarVF).  Each condition is a
+      // phase of a barrier whose earlier phases this thread has already seen
+      // and whose next phase needs the tile about to be loaded, so the parity
+      // test cannot alias.  The two rings are polled and V never runs ahead
+      // of K.
       auto load_k = [&](int j) {
-        const int st = j & 1;
+        const int st = j % kStages;
         mbar_expect_tx(bar(kBarK + st), kTile);
         tma_load4(sK + st * kTile, &tkv, 0, kvh, j * kKeys, b, bar(kBarK + st));
         tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, b, bar(kBarK + st));
       };
       auto load_v = [&](int j) {
-        const int st = j & 1;
+        const int st = j % kStages;
         mbar_expect_tx(bar(kBarV + st), kTile);
         tma_load4(sV + st * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + st));
         tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + st));
       };
       int kn = 0, vn = 0;  // K and V tiles issued
-      for (; kn < 2 && kn < n_tiles; ++kn, ++vn) {
-        load_k(kn);
-        load_v(kn);
-      }
-      if (n_tiles > 2 && mbar_wait(bar(kBarS), 0, abort)) load_k(kn++);
-      for (int i = 0; !*abort && (kn < n_tiles || vn < n_tiles); ++i) {
-        if (kn < n_tiles) {
-          if (!mbar_wait(bar(kBarS + ((i + 1) & 1)), ((i + 1) >> 1) & 1, abort)) break;
+      unsigned long long t_last = global_ns();
+      while (kn < n_tiles || vn < n_tiles) {
+        bool did = false;
+        if (kn < n_tiles &&
+            (kn < kStages ||
+             mbar_test(bar(kBarKF + kn % kStages), ((kn - kStages) / kStages) & 1))) {
           load_k(kn++);
+          did = true;
         }
-        if (vn < n_tiles) {
-          if (!mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort)) break;
+        if (vn < kn &&
+            (vn < kStages ||
+             mbar_test(bar(kBarVF + vn % kStages), ((vn - kStages) / kStages) & 1))) {
           load_v(vn++);
+          did = true;
         }
+        if (did) {
+          t_last = global_ns();
+          continue;
+        }
+        if (*abort) break;
+        if (global_ns() - t_last > kWaitNs) {
+          *abort = 1;
+          break;
+        }
+        __nanosleep(64);
       }
       // every copy issued has landed before the CTA exits (immediate unless a
-      // consumer gave up early); the last two tiles of each ring are the last
-      // phases of their stage barriers, so the parity test cannot alias
+      // consumer gave up early): the newest phase of each stage barrier
       volatile int no_abort = 0;
-      for (int j = kn > 2 ? kn - 2 : 0; j < kn; ++j)
-        mbar_wait(bar(kBarK + (j & 1)), (j >> 1) & 1, &no_abort);
-      for (int j = vn > 2 ? vn - 2 : 0; j < vn; ++j)
-        mbar_wait(bar(kBarV + (j & 1)), (j >> 1) & 1, &no_abort);
-      mbar_wait(bar(kBarQ), 0, &no_abort);
+      for (int j = kn > kStages ? kn - kStages : 0; j < kn; ++j)
+        mbar_wait(bar(kBarK + j % kStages), (j / kStages) & 1, &no_abort);
+      for (int j = vn > kStages ? vn - kStages : 0; j < vn; ++j)
+        mbar_wait(bar(kBarV + j % kStages), (j / kStages) & 1, &no_abort);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
+    // Both products take their A operand from tensor memory (Q, then P) and
+    // only K or V from shared memory.  The K16 steps of two independent
+    // products are interleaved -- S_{i+2} (into the S buffer that S_i has
+    // left) with PV_i, once P_i is ready; S_0 and S_1 go first on their own.
+    // The whole warp runs the loop converged and elect.sync picks the lane
+    // that issues: a lone diverged lane issues far more slowly while the
+    // softmax warps keep the sub-partition busy.  Descriptors are a stage
+    // base plus a constant step (the start address is the low 14 bits).
+    int s_issued = 0, pv_issued = 0;
     bool ok = mbar_wait(bar(kBarQ), 0, abort);
-    int s_issued = 0, pv_issued = 0;  // S and PV tiles committed so far
+    ok = __all_sync(0xffffffffu, ok);
+    const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, kHalfTile, 1024);
+    constexpr uint64_t kStageStep = kTile >> 4;
     tc_fence_after();
-    for (int j = 0; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles) {
-        const int st = j & 1;
-        ok = mbar_wait(bar(kBarK + st), (j >> 1) & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
+    int sk = 0;  // stage of the next K tile to consume
+    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarK + sk), 0, abort));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dk = dK0 + sk * kStageStep;
 #pragma unroll
-          for (int ks = 0; ks < kHd / 16; ++ks) {
-            const uint32_t koff = (ks >> 2) * kHalfTile + (ks & 3) * 32;
-            mma_bf16(tmem + st * kKeys, sdesc(sQ + koff, 16, 1024),
-                     sdesc(sK + st * kTile + koff, 16, 1024), kIdescS, ks > 0);
-          }
-          mma_commit(bar(kBarS + st));
-        }
-        __syncwarp();
-        s_issued = j + 1;
+        for (int ks = 0; ks < kHd / 16; ++ks)
+          mma_ts(tmem + j * kKeys, tmem + kColQ + ks * 8,
+                 dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
+        mma_commit(bar(kBarS + j));
+        mma_commit(bar(kBarKF + sk));
       }
-      if (j >= 1) {
-        const int i = j - 1, sp = i & 1;
-        ok = mbar_wait(bar(kBarP + sp), (i >> 1) & 1, abort) &&
-             mbar_wait(bar(kBarV + sp), (i >> 1) & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        if (i == n_tiles - 1) {
-          // value rows past the last key may hold anything (NaN included):
-          // zero them so that P = 0 there contributes exactly 0
-          const int rem = n_keys - i * kKeys;
-          uint8_t *vt = sm + kOffV + sp * kTile;
-          const int nz = (kKeys - rem) * 8;  // 16-byte chunks per half
-          for (int c = lane; c < 2 * nz; c += 32) {
-            const int h = c / nz, k = c % nz;
-            *reinterpret_cast<uint4 *>(vt + h * kHalfTile + rem * 128 + k * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
+      __syncwarp();
+      s_issued = j + 1;
+      sk = sk + 1 == kStages ? 0 : sk + 1;
+    }
+    int sv = 0;  // stage of the next V tile
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const bool with_s = i + 2 < n_tiles;
+      bool w = true;
+      if (with_s)
+        w = mbar_wait(bar(kBarSF + (i & 1)), (i >> 1) & 1, abort) &&
+            mbar_wait(bar(kBarK + sk), ((i + 2) / kStages) & 1, abort);
+      w = w && mbar_wait(bar(kBarP + (i & 1)), (i >> 1) & 1, abort) &&
+          mbar_wait(bar(kBarV + sv), (i / kStages) & 1, abort);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      if (i == n_tiles - 1) {
+        // value rows past the last key may hold anything (NaN included):
+        // zero them so that P = 0 there contributes exactly 0
+        const int rem = n_keys - i * kKeys;
+        uint8_t *vt = sm + kOffV + sv * kTile;
+        const int nz = (kKeys - rem) * 8;  // 16-byte chunks per half
+        for (int c = lane; c < 2 * nz; c += 32) {
+          const int h = c / nz, k = c % nz;
+          *reinterpret_cast<uint4 *>(vt + h * kHalfTile + rem * 128 + k * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
         }
-        tc_fence_after();
-        if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dk = dK0 + sk * kStageStep, dv = dV0 + sv * kStageStep;
+        const uint32_t dS = tmem + (i & 1) * kKeys;
+        if (with_s) {
 #pragma unroll
-          for (int ks = 0; ks < kKeys / 16; ++ks) {
-            const uint32_t poff = (ks >> 2) * kHalfTile + (ks & 3) * 32;
-            mma_bf16(tmem + kColO, sdesc(sP + poff, 16, 1024),
-                     sdesc(sV + sp * kTile + ks * 16 * 128, kHalfTile, 1024), kIdescO,
-                     (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) {
+            mma_ts(dS, tmem + kColQ + ks * 8,
+                   dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
+            mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
+                   (i > 0 || ks > 0) ? 1u : 0u);
           }
-          mma_commit(bar(kBarPV + sp));
+          mma_commit(bar(kBarS + (i & 1)));
+          mma_commit(bar(kBarKF + sk));
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
+                   (i > 0 || ks > 0) ? 1u : 0u);
         }
-        __syncwarp();
-        pv_issued = j;
+        mma_commit(bar(kBarPV + (i & 1)));
+        mma_commit(bar(kBarVF + sv));
       }
+      __syncwarp();
+      if (with_s) {
+        s_issued = i + 3;
+        sk = sk + 1 == kStages ? 0 : sk + 1;
+      }
+      pv_issued = i + 1;
+      sv = sv + 1 == kStages ? 0 : sv + 1;
     }
     if (!ok) {
       // retire the MMAs in flight before tensor memory is released: the last
@@ -431,28 +506,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else {
     // ---------------------------------------------------------------- softmax
     // warps w and w + 4 share tensor-memory lane quarter w % 4 (the same 32
-    // rows); the first takes key columns 0..63 of each tile and head-dim
-    // columns 0..63 of O, the second the upper 64.  The pair exchanges its
-    // partial row maxima (and at the end the partial sums) through shared
-    // memory and a two-arrival mbarrier per tile parity.
+    // rows); warp `half` takes key columns 64 half .. 64 half + 63 of every
+    // tile, and head-dim columns 64 half .. of Q and O.  The pair exchanges
+    // its partial row maxima (and at the end the partial sums) through
+    // shared memory and a two-arrival barrier per tile parity.
     const int half = (warp - 2) >> 2;
     const uint64_t *mrow = row_ok ? a.mask + ((size_t)b * a.T + node) * a.W : nullptr;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float *xchg = reinterpret_cast<float *>(sm + kOffXchg);
     const float NEG_INF = -INFINITY;
+    {
+      // this row's query (head-dim half) into tensor memory, bf16 pairs
+      uint32_t qv[32];
+      const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + orow * kHd + 64 * half);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = row_ok ? __ldg(qs + c) : make_uint4(0u, 0u, 0u, 0u);
+        qv[4 * c] = w.x;
+        qv[4 * c + 1] = w.y;
+        qv[4 * c + 2] = w.z;
+        qv[4 * c + 3] = w.w;
+      }
+      tm_st32u(tmem + lane_off + kColQ + 32 * half, qv);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarQ));
+    }
     float m_ref = NEG_INF;  // reference max (log2 domain, scaled)
     float l = 0.0f;         // partial sum over this warp's key columns
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      ok = mbar_wait(bar(kBarS + st), (j >> 1) & 1, abort);
+      const int sb = j & 1;
+      ok = mbar_wait(bar(kBarS + sb), (j >> 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       float s[64];
-      tm_ld32(tmem + lane_off + st * kKeys + 64 * half, s);
-      tm_ld32(tmem + lane_off + st * kKeys + 64 * half + 32, s + 32);
+      tm_ld32(tmem + lane_off + sb * kKeys + 64 * half, s);
+      tm_ld32(tmem + lane_off + sb * kKeys + 64 * half + 32, s + 32);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSF + sb));  // S buffer sb read out
       const int key0 = j * kKeys + 64 * half;
       if (key0 + 64 > bs) {
 #pragma unroll
@@ -472,38 +568,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[c + k]);
       const float mine = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      float *xs = xchg + st * 256;
+      float *xs = xchg + sb * 256;
       xs[half * 128 + r] = mine;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + st));
-      ok = mbar_wait(bar(kBarX + 2 * quarter + st), (j >> 1) & 1, abort);
+      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + sb));
+      ok = mbar_wait(bar(kBarX + 2 * quarter + sb), (j >> 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const float mx = fmaxf(mine, xs[(half ^ 1) * 128 + r]) * a.scale_log2;  // scale > 0
       const bool grow = mx > m_ref + kRescaleLog2;
       const float m_new = grow ? mx : m_ref;
       const float factor = (grow && m_ref != NEG_INF) ? ex2(m_ref - m_new) : 1.0f;
-      bool o_ready = j == 0;  // the PV of tile j - 1 has retired
-      if (__any_sync(0xffffffffu, factor != 1.0f)) {
-        // O holds tiles 0..j-1: wait for the last of them, then rescale this
-        // warp's half of it
-        const int i = j - 1;
-        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        o_ready = true;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          float o[32];
-          tm_ld32(tmem + lane_off + kColO + 64 * half + c, o);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] *= factor;
-          tm_st32(tmem + lane_off + kColO + 64 * half + c, o);
-        }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      }
       l *= factor;
       m_ref = m_new;
       const float mneg = m_ref == NEG_INF ? 0.0f : -m_ref;
@@ -521,22 +596,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         pk[c / 2 + 1] = pack_bf16(p2, p3);
       }
       l += l0 + l1;
-      if (!o_ready) {
-        // the single P buffer was last read by the PV of tile j - 1
+      if (j >= 1) {
+        // PV_{j-1} has retired: the P columns are free and O covers tiles < j
         const int i = j - 1;
         ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        tc_fence_after();
       }
-      uint8_t *prow = sm + kOffP + half * kHalfTile + r * 128;
+      if (__any_sync(0xffffffffu, factor != 1.0f)) {
+        // the max grew: bring this warp's half of O to the new reference
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int c = 0; c < 64; c += 32) {
+          float o[32];
+          tm_ld32(tmem + lane_off + kColO + 64 * half + c, o);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] *= factor;
+          tm_st32(tmem + lane_off + kColO + 64 * half + c, o);
+        }
+      }
+      tm_st32u(tmem + lane_off + kColP + 32 * half, pk);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + st));
+      if (lane == 0) mbar_arrive(bar(kBarP + sb));
     }
     if (ok) {
       const int i = n_tiles - 1;
@@ -655,13 +739,7 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
       (s = map_arg(out_status, "out_status")) != SV_OK)
     return s;
   const int npt = kRows / G;
-  CUtensorMap tq, tkv;
-  {
-    const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hq, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t str[3] = {(cuuint64_t)kHd * 2, (cuuint64_t)Hq * kHd * 2,
-                               (cuuint64_t)T * Hq * kHd * 2};
-    if ((s = encode4(&tq, q, dims, str, (cuuint32_t)G, (cuuint32_t)npt, "q")) != SV_OK) return s;
-  }
+  CUtensorMap tkv;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hkv, (cuuint64_t)S,
                                 (cuuint64_t)2 * B};
@@ -680,6 +758,7 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
     smem_set_dev = dev;
   }
   AttnArgs a;
+  a.q = (const uint16_t *)q;
   a.base = base;
   a.mask = mask;
   a.out = (uint16_t *)out;
@@ -699,5 +778,5 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
   LaunchScope ls("tree_attention", st);
   return check_launch("tree_attention",
                       launch_pdl(tree_attn_kernel, dim3(mtiles, Hkv, B), dim3(kAttnThreads),
-                                 kAttnSmem, st, tq, tkv, a));
+                                 kAttnSmem, st, tkv, a));
 }
