@@ -48,13 +48,12 @@ constexpr uint32_t kOffK = 0;                        // kStages K tiles
 constexpr uint32_t kOffV = kOffK + kStages * kTile;  // kStages V tiles
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
-constexpr uint32_t kOffXchg = kOffMisc + 64;  // float [2 parity][2 half][128 rows]
-constexpr size_t kAttnSmem = kOffXchg + 2048 + 1024;  // + alignment slack
+constexpr size_t kAttnSmem = kOffMisc + 64 + 1024;  // + alignment slack
 // barrier indices: K/V landed and stage free (per stage), S ready / read out,
-// P ready and PV retired (per parity), the pair exchanges (2 per quarter)
+// P ready and PV retired (per parity)
 constexpr int kBarQ = 0, kBarK = 1, kBarV = kBarK + kStages, kBarKF = kBarV + kStages,
               kBarVF = kBarKF + kStages, kBarS = kBarVF + kStages, kBarSF = kBarS + 2,
-              kBarP = kBarSF + 2, kBarPV = kBarP + 2, kBarX = kBarPV + 2;
+              kBarP = kBarSF + 2, kBarPV = kBarP + 2;
 // tensor-memory columns: S buffers at 0 and 128, O at 256, Q (bf16 pairs) at
 // 384, P (bf16 pairs) at 448
 constexpr uint32_t kColO = 256, kColQ = 384, kColP = 448;
@@ -199,22 +198,7 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tm_ld32(uint32_t taddr, float *v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
-
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane (32x32b).
 __device__ __forceinline__ void tm_st32(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -230,6 +214,56 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const float *v) {
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// 16x256b shape, 8 repetitions (64 columns): thread t gets rows t/4 and
+// t/4 + 8 of the 16-lane window, columns 8c + 2 (t % 4) + {0, 1}:
+// v[4c + 0, 1] = first row, v[4c + 2, 3] = second row.
+__device__ __forceinline__ void tm_ld16x256_x8(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tm_st16x256_x8(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// 16x128b shape, 16 repetitions (64 columns): thread t writes column
+// 4c + t % 4 of rows t/4 (v[2c]) and t/4 + 8 (v[2c + 1]).
+__device__ __forceinline__ void tm_st16x128_x16(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x128b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -328,7 +362,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(kBarP + s), 8);
       mbar_init(bar(kBarPV + s), 1);
     }
-    for (int x = 0; x < 8; ++x) mbar_init(bar(kBarX + x), 2);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -403,9 +436,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     // Both products take their A operand from tensor memory (Q, then P) and
-    // only K or V from shared memory.  The K16 steps of two independent
-    // products are interleaved -- S_{i+2} (into the S buffer that S_i has
-    // left) with PV_i, once P_i is ready; S_0 and S_1 go first on their own.
+    // only K or V from shared memory.  Once P_i is ready, PV_i is issued and
+    // then S_{i+2} (into the S buffer that S_i has left): PV_i retires first,
+    // which is what the softmax of tile i + 1 waits for; S_0 and S_1 go
+    // first on their own.
     // The whole warp runs the loop converged and elect.sync picks the lane
     // that issues: a lone diverged lane issues far more slowly while the
     // softmax warps keep the sub-partition busy.  Descriptors are a stage
@@ -465,12 +499,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t dS = tmem + (i & 1) * kKeys;
         if (with_s) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            mma_ts(dS, tmem + kColQ + ks * 8,
-                   dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
+          for (int ks = 0; ks < 8; ++ks)
             mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
                    (i > 0 || ks > 0) ? 1u : 0u);
-          }
+          mma_commit(bar(kBarPV + (i & 1)));
+          mma_commit(bar(kBarVF + sv));
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(dS, tmem + kColQ + ks * 8,
+                   dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
           mma_commit(bar(kBarS + (i & 1)));
           mma_commit(bar(kBarKF + sk));
         } else {
@@ -478,9 +515,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
                    (i > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar(kBarPV + (i & 1)));
+          mma_commit(bar(kBarVF + sv));
         }
-        mma_commit(bar(kBarPV + (i & 1)));
-        mma_commit(bar(kBarVF + sv));
       }
       __syncwarp();
       if (with_s) {
@@ -505,18 +542,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    // warps w and w + 4 share tensor-memory lane quarter w % 4 (the same 32
-    // rows); warp `half` takes key columns 64 half .. 64 half + 63 of every
-    // tile, and head-dim columns 64 half .. of Q and O.  The pair exchanges
-    // its partial row maxima (and at the end the partial sums) through
-    // shared memory and a two-arrival barrier per tile parity.
+    // Warp w reads tensor-memory lanes of quarter w % 4; the pair (w, w + 4)
+    // splits them into two 16-lane halves.  With the 16x256b / 16x128b
+    // shapes thread t holds rows h16 + t/4 and h16 + t/4 + 8 of its half and,
+    // in every 8-column chunk, columns 2 (t % 4) and 2 (t % 4) + 1: a row is
+    // spread over the four threads of a quad, so row maxima and sums are two
+    // shuffles and no warp waits for another.  The P store (16x128b) writes
+    // bf16 pair column 4 c + t % 4, exactly the two keys the thread holds.
     const int half = (warp - 2) >> 2;
-    const uint64_t *mrow = row_ok ? a.mask + ((size_t)b * a.T + node) * a.W : nullptr;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float *xchg = reinterpret_cast<float *>(sm + kOffXchg);
+    const int q4 = lane & 3;
+    const uint32_t lane16 = (uint32_t)(quarter * 32 + half * 16) << 16;
+    const int rowA = quarter * 32 + half * 16 + (lane >> 2);  // and rowA + 8
     const float NEG_INF = -INFINITY;
     {
-      // this row's query (head-dim half) into tensor memory, bf16 pairs
+      // this warp's query columns (head-dim half) for all 32 lanes of the
+      // quarter into tensor memory, bf16 pairs (32x32b: lane = row)
       uint32_t qv[32];
       const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + orow * kHd + 64 * half);
 #pragma unroll
@@ -527,14 +567,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         qv[4 * c + 2] = w.z;
         qv[4 * c + 3] = w.w;
       }
-      tm_st32u(tmem + lane_off + kColQ + 32 * half, qv);
+      tm_st32u(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 32 * half, qv);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarQ));
     }
-    float m_ref = NEG_INF;  // reference max (log2 domain, scaled)
-    float l = 0.0f;         // partial sum over this warp's key columns
+    // the two rows of this thread
+    int rnode[2];
+    size_t rrow[2];
+    bool rok[2];
+    const uint64_t *rmask[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int rr = rowA + 8 * e;
+      rnode[e] = node0 + rr / a.G;
+      rok[e] = rnode[e] < a.T;
+      rrow[e] = ((size_t)b * a.T + rnode[e]) * a.Hq + kvh * a.G + rr % a.G;
+      rmask[e] = rok[e] ? a.mask + ((size_t)b * a.T + rnode[e]) * a.W : nullptr;
+    }
+    float m_ref[2] = {NEG_INF, NEG_INF};  // reference max (log2 domain, scaled)
+    float l[2] = {0.0f, 0.0f};            // partial sums over this thread's columns
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
@@ -542,60 +595,73 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // s[4c + 0, 1]: row A, keys 8c + 2 q4 + {0, 1}; s[4c + 2, 3]: row B
       float s[64];
-      tm_ld32(tmem + lane_off + sb * kKeys + 64 * half, s);
-      tm_ld32(tmem + lane_off + sb * kKeys + 64 * half + 32, s + 32);
+      tm_ld16x256_x8(tmem + lane16 + sb * kKeys, s);
+      tm_ld16x256_x8(tmem + lane16 + sb * kKeys + 64, s + 32);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSF + sb));  // S buffer sb read out
-      const int key0 = j * kKeys + 64 * half;
-      if (key0 + 64 > bs) {
+      const int key0 = j * kKeys;
+      if (key0 + kKeys > bs) {
 #pragma unroll
-        for (int c4 = 0; c4 < 2; ++c4) {
-          const uint32_t vis = visible32(mrow, a.W, a.T, key0 + 32 * c4 - bs);
+        for (int e = 0; e < 2; ++e) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (!((vis >> c) & 1u)) s[32 * c4 + c] = NEG_INF;
+          for (int g = 0; g < 4; ++g) {
+            // keys key0 + 32 g .. +31: chunks c = 4 g .. 4 g + 3
+            const uint32_t vis = visible32(rmask[e], a.W, a.T, key0 + 32 * g - bs);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c = 4 * g + cc, bit = 8 * cc + 2 * q4;
+              if (!((vis >> bit) & 1u)) s[4 * c + 2 * e] = NEG_INF;
+              if (!((vis >> (bit + 1)) & 1u)) s[4 * c + 2 * e + 1] = NEG_INF;
+            }
+          }
         }
       }
-      float pm[8];
+      float factor[2], mneg[2];
+      bool any_grow = false;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(s[k], s[k + 8]);
+      for (int e = 0; e < 2; ++e) {
+        // four independent chains over the 32 values of row e (chunks 0..15)
+        float pm[4] = {s[2 * e], s[2 * e + 1], s[4 + 2 * e], s[4 + 2 * e + 1]};
 #pragma unroll
-      for (int c = 16; c < 64; c += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[c + k]);
-      const float mine = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      float *xs = xchg + sb * 256;
-      xs[half * 128 + r] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + sb));
-      ok = mbar_wait(bar(kBarX + 2 * quarter + sb), (j >> 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const float mx = fmaxf(mine, xs[(half ^ 1) * 128 + r]) * a.scale_log2;  // scale > 0
-      const bool grow = mx > m_ref + kRescaleLog2;
-      const float m_new = grow ? mx : m_ref;
-      const float factor = (grow && m_ref != NEG_INF) ? ex2(m_ref - m_new) : 1.0f;
-      l *= factor;
-      m_ref = m_new;
-      const float mneg = m_ref == NEG_INF ? 0.0f : -m_ref;
-      uint32_t pk[32];
-      float l0 = 0.0f, l1 = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float p0 = ex2(fmaf(s[c], a.scale_log2, mneg));
-        const float p1 = ex2(fmaf(s[c + 1], a.scale_log2, mneg));
-        const float p2 = ex2(fmaf(s[c + 2], a.scale_log2, mneg));
-        const float p3 = ex2(fmaf(s[c + 3], a.scale_log2, mneg));
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        pk[c / 2] = pack_bf16(p0, p1);
-        pk[c / 2 + 1] = pack_bf16(p2, p3);
+        for (int c = 2; c < 16; c += 2) {
+          pm[0] = fmaxf(pm[0], s[4 * c + 2 * e]);
+          pm[1] = fmaxf(pm[1], s[4 * c + 2 * e + 1]);
+          pm[2] = fmaxf(pm[2], s[4 * c + 4 + 2 * e]);
+          pm[3] = fmaxf(pm[3], s[4 * c + 4 + 2 * e + 1]);
+        }
+        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx *= a.scale_log2;  // scale > 0: max commutes with it
+        const bool grow = mx > m_ref[e] + kRescaleLog2;
+        const float m_new = grow ? mx : m_ref[e];
+        factor[e] = (grow && m_ref[e] != NEG_INF) ? ex2(m_ref[e] - m_new) : 1.0f;
+        any_grow |= factor[e] != 1.0f;
+        l[e] *= factor[e];
+        m_ref[e] = m_new;
+        mneg[e] = m_new == NEG_INF ? 0.0f : -m_new;
       }
-      l += l0 + l1;
+      uint32_t pk[32];
+      float la0 = 0.0f, la1 = 0.0f, lb0 = 0.0f, lb1 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float p0 = ex2(fmaf(s[4 * c], a.scale_log2, mneg[0]));
+        const float p1 = ex2(fmaf(s[4 * c + 1], a.scale_log2, mneg[0]));
+        const float p2 = ex2(fmaf(s[4 * c + 2], a.scale_log2, mneg[1]));
+        const float p3 = ex2(fmaf(s[4 * c + 3], a.scale_log2, mneg[1]));
+        la0 += p0;
+        la1 += p1;
+        lb0 += p2;
+        lb1 += p3;
+        pk[2 * c] = pack_bf16(p0, p1);      // row A, pair column 4c + q4
+        pk[2 * c + 1] = pack_bf16(p2, p3);  // row B
+      }
+      l[0] += la0 + la1;
+      l[1] += lb0 + lb1;
       if (j >= 1) {
         // PV_{j-1} has retired: the P columns are free and O covers tiles < j
         const int i = j - 1;
@@ -604,19 +670,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, factor != 1.0f)) {
-        // the max grew: bring this warp's half of O to the new reference
+      if (__any_sync(0xffffffffu, any_grow)) {
+        // the max grew: bring these rows of O to the new reference
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kHd; c += 64) {
           float o[32];
-          tm_ld32(tmem + lane_off + kColO + 64 * half + c, o);
+          tm_ld16x256_x8(tmem + lane16 + kColO + c, o);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] *= factor;
-          tm_st32(tmem + lane_off + kColO + 64 * half + c, o);
+          for (int k = 0; k < 32; ++k) o[k] *= factor[(k >> 1) & 1];
+          tm_st16x256_x8(tmem + lane16 + kColO + c, o);
         }
       }
-      tm_st32u(tmem + lane_off + kColP + 32 * half, pk);
+      tm_st16x128_x16(tmem + lane16 + kColP, pk);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -628,36 +694,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
-      // total row sum: the partner's partial through the exchange slot of the
-      // parity after the last tile (free: both passed the last exchange)
-      const int px = n_tiles & 1;
-      float *xs = xchg + px * 256;
-      xs[half * 128 + r] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarX + 2 * quarter + px));
-      ok = mbar_wait(bar(kBarX + 2 * quarter + px), (n_tiles >> 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        const float lt = l + xs[(half ^ 1) * 128 + r];
-        tc_fence_after();
-        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-        uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd + 64 * half);
+      tc_fence_after();
+      float inv[2], lt[2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          float v[32];
-          tm_ld32(tmem + lane_off + kColO + 64 * half + c, v);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          if (row_ok) {
+      for (int e = 0; e < 2; ++e) {
+        float v = l[e];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        lt[e] = v;
+        inv[e] = v > 0.0f ? 1.0f / v : 0.0f;
+      }
 #pragma unroll
-            for (int k = 0; k < 32; k += 8)
-              o[(c + k) / 8] = make_uint4(pack_bf16(v[k] * inv, v[k + 1] * inv),
-                                          pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
-                                          pack_bf16(v[k + 4] * inv, v[k + 5] * inv),
-                                          pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
-          }
+      for (int c = 0; c < kHd; c += 64) {
+        float o[32];
+        tm_ld16x256_x8(tmem + lane16 + kColO + c, o);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        // o[4k + 0, 1]: row A, columns c + 8k + 2 q4 + {0, 1}; o[4k + 2, 3]: row B
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (!rok[e]) continue;
+          uint32_t *orow32 = reinterpret_cast<uint32_t *>(a.out + rrow[e] * kHd + c + 2 * q4);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            orow32[4 * k] = pack_bf16(o[4 * k + 2 * e] * inv[e], o[4 * k + 2 * e + 1] * inv[e]);
         }
-        if (row_ok && half == 0 && a.lse)
-          a.lse[orow] = lt > 0.0f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : NEG_INF;
+      }
+      if (q4 == 0 && a.lse) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (rok[e])
+            a.lse[rrow[e]] =
+                lt[e] > 0.0f ? (m_ref[e] + __log2f(lt[e])) * 0.69314718055994531f : NEG_INF;
       }
     }
   }
