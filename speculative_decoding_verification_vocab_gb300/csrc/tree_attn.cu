@@ -277,6 +277,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ex2 of a packed pair on the MUFU (ex2.approx.ftz: -inf gives +0).
+__device__ __forceinline__ unsigned long long ex2_2(unsigned long long x) {
+  float a, b;
+  f2_unpack(x, a, b);
+  return f2_pack(ex2(a), ex2(b));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -364,6 +371,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the first K/V tiles need nothing but the barriers just initialised:
+    // start them before the rest of the CTA is set up
+    for (int j = 0; j < kStages && j < n_tiles; ++j) {
+      mbar_expect_tx(bar(kBarK + j), kTile);
+      tma_load4(sK + j * kTile, &tkv, 0, kvh, j * kKeys, b, bar(kBarK + j));
+      tma_load4(sK + j * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, b, bar(kBarK + j));
+      mbar_expect_tx(bar(kBarV + j), kTile);
+      tma_load4(sV + j * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + j));
+      tma_load4(sV + j * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + j));
+    }
+  }
+  // softmax warps: this row's query words (head-dim half), fetched now and
+  // written to tensor memory once it is allocated
+  uint32_t qv[32];
+  if (warp >= 2) {
+    const int half = (warp - 2) >> 2;
+    const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + orow * kHd + 64 * half);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 w = row_ok ? __ldg(qs + c) : make_uint4(0u, 0u, 0u, 0u);
+      qv[4 * c] = w.x;
+      qv[4 * c + 1] = w.y;
+      qv[4 * c + 2] = w.z;
+      qv[4 * c + 3] = w.w;
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -398,7 +430,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load4(sV + st * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + st));
         tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + st));
       };
-      int kn = 0, vn = 0;  // K and V tiles issued
+      int kn = n_tiles < kStages ? n_tiles : kStages, vn = kn;  // tiles issued
       unsigned long long t_last = global_ns();
       while (kn < n_tiles || vn < n_tiles) {
         bool did = false;
@@ -479,15 +511,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mbar_wait(bar(kBarV + sv), (i / kStages) & 1, abort);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
-      if (i == n_tiles - 1) {
-        // value rows past the last key may hold anything (NaN included):
-        // zero them so that P = 0 there contributes exactly 0
-        const int rem = n_keys - i * kKeys;
+      // the last tile's PV runs only the K16 steps holding keys below
+      // n_keys; value rows past the last key inside the last step may hold
+      // anything (NaN included) and are zeroed, so that P = 0 there adds 0
+      const int rem = n_keys - i * kKeys;
+      const int pv_steps = (i == n_tiles - 1) ? (rem + 15) >> 4 : 8;
+      if (i == n_tiles - 1 && (rem & 15)) {
         uint8_t *vt = sm + kOffV + sv * kTile;
-        const int nz = (kKeys - rem) * 8;  // 16-byte chunks per half
-        for (int c = lane; c < 2 * nz; c += 32) {
-          const int h = c / nz, k = c % nz;
-          *reinterpret_cast<uint4 *>(vt + h * kHalfTile + rem * 128 + k * 16) =
+        const int nrow = 16 * pv_steps - rem;  // < 16 rows, 16 chunks each
+        for (int c = lane; c < nrow * 16; c += 32) {
+          const int row = rem + (c >> 4), ch = c & 15;
+          *reinterpret_cast<uint4 *>(vt + (ch >> 3) * kHalfTile + row * 128 + (ch & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -511,8 +545,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_commit(bar(kBarS + (i & 1)));
           mma_commit(bar(kBarKF + sk));
         } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
+          for (int ks = 0; ks < pv_steps; ++ks)
             mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
                    (i > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar(kBarPV + (i & 1)));
@@ -557,16 +590,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     {
       // this warp's query columns (head-dim half) for all 32 lanes of the
       // quarter into tensor memory, bf16 pairs (32x32b: lane = row)
-      uint32_t qv[32];
-      const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + orow * kHd + 64 * half);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w = row_ok ? __ldg(qs + c) : make_uint4(0u, 0u, 0u, 0u);
-        qv[4 * c] = w.x;
-        qv[4 * c + 1] = w.y;
-        qv[4 * c + 2] = w.z;
-        qv[4 * c + 3] = w.w;
-      }
       tm_st32u(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 32 * half, qv);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -645,23 +668,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         m_ref[e] = m_new;
         mneg[e] = m_new == NEG_INF ? 0.0f : -m_new;
       }
+      // p = 2^(scale*log2e*s - m): scaling and sums on packed fp32 pairs,
+      // the exponentials on the MUFU (moving a share of them to a polynomial
+      // on the FMA pipe measured slower: the warps are bound by issue slots)
       uint32_t pk[32];
-      float la0 = 0.0f, la1 = 0.0f, lb0 = 0.0f, lb1 = 0.0f;
+      unsigned long long la2 = 0ull, lb2 = 0ull;
+      const unsigned long long sc2 = f2_splat(a.scale_log2);
+      const unsigned long long ma2 = f2_splat(mneg[0]), mb2 = f2_splat(mneg[1]);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float p0 = ex2(fmaf(s[4 * c], a.scale_log2, mneg[0]));
-        const float p1 = ex2(fmaf(s[4 * c + 1], a.scale_log2, mneg[0]));
-        const float p2 = ex2(fmaf(s[4 * c + 2], a.scale_log2, mneg[1]));
-        const float p3 = ex2(fmaf(s[4 * c + 3], a.scale_log2, mneg[1]));
-        la0 += p0;
-        la1 += p1;
-        lb0 += p2;
-        lb1 += p3;
+        const unsigned long long xa = f2_fma(f2_pack(s[4 * c], s[4 * c + 1]), sc2, ma2);
+        const unsigned long long xb = f2_fma(f2_pack(s[4 * c + 2], s[4 * c + 3]), sc2, mb2);
+        const unsigned long long pa = ex2_2(xa);
+        const unsigned long long pb = ex2_2(xb);
+        la2 = f2_add(la2, pa);
+        lb2 = f2_add(lb2, pb);
+        float p0, p1, p2, p3;
+        f2_unpack(pa, p0, p1);
+        f2_unpack(pb, p2, p3);
         pk[2 * c] = pack_bf16(p0, p1);      // row A, pair column 4c + q4
         pk[2 * c + 1] = pack_bf16(p2, p3);  // row B
       }
-      l[0] += la0 + la1;
-      l[1] += lb0 + lb1;
+      {
+        float u0, u1, v0, v1;
+        f2_unpack(la2, u0, u1);
+        f2_unpack(lb2, v0, v1);
+        l[0] += u0 + u1;
+        l[1] += v0 + v1;
+      }
       if (j >= 1) {
         // PV_{j-1} has retired: the P columns are free and O covers tiles < j
         const int i = j - 1;

@@ -2,11 +2,11 @@
 through the C ABI against the oracle (double precision).
 
 Tolerance, derived from the kernel's arithmetic: scores are fp32 sums of
-exact bf16 products; the softmax weights are rounded to bf16 (relative error
-<= 2^-9) before the P.V product, and the output is rounded to bf16 (<= 2^-9 of
-|out|).  Both errors are bounded by 2^-9 max|v| over the visible value rows,
-so |out - ref| <= 2^-8 max|v| (plus fp32 terms three orders smaller: 1%
-margin).  The lse bound is computed from the data: the fp32 score error
+exact bf16 products; the softmax weights come from ex2.approx (relative error
+about 2^-22), are rounded to bf16 (relative error <= 2^-9) before the P.V
+product, and the output is rounded to bf16 (<= 2^-9 of |out|).  The two roundings are bounded by 2^-9
+max|v| each over the visible value rows, so |out - ref| <= 2^-8 max|v| plus
+terms below 1e-5 max|v| (covered by a 1% margin).  The lse bound is computed from the data: the fp32 score error
 gamma_128 * scale * sum_d |q_d k_d|, plus the fp32 sum of n weights
 (n * 2^-24) and the ex2 approximation (2^-21 relative).
 """
