@@ -46,14 +46,16 @@ constexpr uint32_t kHalfTile = 16384;  // one 128-byte-wide swizzled box of it
 constexpr int kStages = 3;             // K and V ring depth
 constexpr uint32_t kOffK = 0;                        // kStages K tiles
 constexpr uint32_t kOffV = kOffK + kStages * kTile;  // kStages V tiles
-constexpr uint32_t kOffBar = kOffV + kStages * kTile;
+constexpr uint32_t kOffQ = kOffV + kStages * kTile;  // the next item's query tile
+constexpr uint32_t kOffBar = kOffQ + kTile;
 constexpr uint32_t kOffMisc = kOffBar + 32 * 8;
 constexpr size_t kAttnSmem = kOffMisc + 64 + 1024;  // + alignment slack
-// barrier indices: K/V landed and stage free (per stage), S ready / read out,
-// P ready and PV retired (per parity)
+// barrier indices: query in tensor memory (kBarQ), K/V landed and stage free
+// (per stage), S ready / read out, P ready and PV retired (per parity), query
+// tile landed in / read out of shared memory (kBarQS / kBarQF)
 constexpr int kBarQ = 0, kBarK = 1, kBarV = kBarK + kStages, kBarKF = kBarV + kStages,
               kBarVF = kBarKF + kStages, kBarS = kBarVF + kStages, kBarSF = kBarS + 2,
-              kBarP = kBarSF + 2, kBarPV = kBarP + 2;
+              kBarP = kBarSF + 2, kBarPV = kBarP + 2, kBarQS = kBarPV + 2, kBarQF = kBarQS + 1;
 // tensor-memory columns: S buffers at 0 and 128, O at 256, Q (bf16 pairs) at
 // 384, P (bf16 pairs) at 448
 constexpr uint32_t kColO = 256, kColQ = 384, kColP = 448;
@@ -68,7 +70,8 @@ struct AttnArgs {
   uint16_t *out;
   float *lse;
   uint32_t *status;
-  int B, T, Hq, Hkv, S, G, W, npt;  // npt = tree nodes per CTA = 128 / G
+  int B, T, Hq, Hkv, S, G, W, npt;  // npt = tree nodes per item = 128 / G
+  int mtiles, n_items;              // query tiles per (sequence, KV head); items
   float scale_log2;                 // softmax scale * log2(e)
 };
 
@@ -290,73 +293,86 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Bits [pos, pos + 32) of a node's ancestor mask (pos >= 0; words past W read 0).
-__device__ __forceinline__ uint32_t mask_bits32(const uint64_t *mrow, int W, int pos) {
+// Word w of a node's ancestor mask: words 0 and 1 prefetched (m01), later
+// ones from memory, words past W zero.
+__device__ __forceinline__ uint64_t mask_word(const uint64_t *mrow, int W, uint64_t m0,
+                                              uint64_t m1, int w) {
+  return w == 0 ? m0 : (w == 1 ? m1 : (w < W ? __ldg(mrow + w) : 0ull));
+}
+
+// Bits [pos, pos + 32) of a node's ancestor mask (pos >= 0).
+__device__ __forceinline__ uint32_t mask_bits32(const uint64_t *mrow, int W, uint64_t m0,
+                                                uint64_t m1, int pos) {
   const int w = pos >> 6, sh = pos & 63;
-  const uint64_t lo = w < W ? __ldg(mrow + w) : 0ull;
-  const uint64_t hi = (sh && w + 1 < W) ? __ldg(mrow + w + 1) : 0ull;
+  const uint64_t lo = mask_word(mrow, W, m0, m1, w);
+  const uint64_t hi = sh ? mask_word(mrow, W, m0, m1, w + 1) : 0ull;
   return (uint32_t)(sh ? (lo >> sh) | (hi << (64 - sh)) : lo);
 }
 
 // Visibility of keys base + rel + i, i = 0..31: context keys (rel + i < 0)
 // are visible, tree key m = rel + i < T iff bit m of the node's mask, keys at
 // or past base + T never.  mrow == nullptr (a padding row): context only.
-__device__ __forceinline__ uint32_t visible32(const uint64_t *mrow, int W, int T, int rel) {
+__device__ __forceinline__ uint32_t visible32(const uint64_t *mrow, int W, uint64_t m0,
+                                              uint64_t m1, int T, int rel) {
   const uint32_t pre = rel >= 0 ? 0u : (rel <= -32 ? 0xFFFFFFFFu : ((1u << (-rel)) - 1u));
   if (rel <= -32 || rel >= T || mrow == nullptr) return pre;
   uint32_t tree;
   int nvalid;
   if (rel >= 0) {
-    tree = mask_bits32(mrow, W, rel);
+    tree = mask_bits32(mrow, W, m0, m1, rel);
     nvalid = T - rel;
   } else {
-    tree = mask_bits32(mrow, W, 0) << (-rel);
+    tree = mask_bits32(mrow, W, m0, m1, 0) << (-rel);
     nvalid = T - rel;
   }
   if (nvalid < 32) tree &= (1u << nvalid) - 1u;
   return pre | tree;
 }
 
+// One work item: 128 query rows (query tile mt) of one (sequence, KV head).
+struct Item {
+  int mt, kvh, b, bs, n_keys, n_tiles;
+  bool bad;
+};
+
+__device__ __forceinline__ Item decode_item(const AttnArgs &a, int it) {
+  Item x;
+  x.mt = it % a.mtiles;
+  const int rest = it / a.mtiles;
+  x.kvh = rest % a.Hkv;
+  x.b = rest / a.Hkv;
+  x.bs = a.base[x.b];
+  x.bad = x.bs < 0 || (long long)x.bs + a.T > a.S;
+  x.n_keys = x.bs + a.T;
+  x.n_tiles = x.bad ? 0 : (x.n_keys + kKeys - 1) / kKeys;
+  return x;
+}
+
+// Persistent: CTA c takes items c, c + gridDim.x, ...  Every role walks the
+// same item sequence; ring stages, S buffers and barrier phases follow
+// CTA-wide tile counters, so the producer runs ahead into the next item while
+// the current one drains and the per-CTA setup happens once.
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    tree_attn_kernel(const __grid_constant__ CUtensorMap tkv, AttnArgs a) {
+    tree_attn_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tkv,
+                     AttnArgs a) {
   grid_dep_sync();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int mt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bs = a.base[b];
-  const int node0 = mt * a.npt;
-  // a softmax warp's row: warp w reads tensor-memory lanes 32 * (w % 4) + lane
   const int quarter = warp & 3;
-  const int r = quarter * 32 + lane;
-  const int node = node0 + r / a.G;
-  const int head = kvh * a.G + r % a.G;
-  const bool row_ok = node < a.T;
-  const size_t orow = ((size_t)b * a.T + node) * a.Hq + head;
-
-  if (bs < 0 || (long long)bs + a.T > a.S) {
-    // base out of range: NaN rows, nothing read
-    if (warp >= 2 && warp < 6 && row_ok) {
-      uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-      uint4 *o = reinterpret_cast<uint4 *>(a.out + orow * kHd);
-      for (int c = 0; c < kHd / 8; ++c) o[c] = nan4;
-      if (a.lse) a.lse[orow] = __int_as_float(0x7FC00000);
-    }
-    if (threadIdx.x == 0 && a.status && mt == 0 && kvh == 0) atomicOr(a.status + b, SV_ROW_BAD_BASE);
-    return;
-  }
-  const int n_keys = bs + a.T;
-  const int n_tiles = (n_keys + kKeys - 1) / kKeys;
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
   volatile int *abort = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+  volatile int *abort_item = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
   const uint32_t bar0 = smem_addr(bars);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  const uint32_t sK = smem_addr(sm + kOffK), sV = smem_addr(sm + kOffV);
+  const uint32_t sK = smem_addr(sm + kOffK), sV = smem_addr(sm + kOffV), sQ = smem_addr(sm + kOffQ);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 8);
+    mbar_init(bar(kBarQS), 1);
+    mbar_init(bar(kBarQF), 8);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarK + s), 1);
       mbar_init(bar(kBarV + s), 1);
@@ -370,32 +386,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(bar(kBarPV + s), 1);
     }
     *abort = 0;
+    *abort_item = a.n_items;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the first K/V tiles need nothing but the barriers just initialised:
-    // start them before the rest of the CTA is set up
-    for (int j = 0; j < kStages && j < n_tiles; ++j) {
-      mbar_expect_tx(bar(kBarK + j), kTile);
-      tma_load4(sK + j * kTile, &tkv, 0, kvh, j * kKeys, b, bar(kBarK + j));
-      tma_load4(sK + j * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, b, bar(kBarK + j));
-      mbar_expect_tx(bar(kBarV + j), kTile);
-      tma_load4(sV + j * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + j));
-      tma_load4(sV + j * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + j));
-    }
-  }
-  // softmax warps: this row's query words (head-dim half), fetched now and
-  // written to tensor memory once it is allocated
-  uint32_t qv[32];
-  if (warp >= 2) {
-    const int half = (warp - 2) >> 2;
-    const uint4 *qs = reinterpret_cast<const uint4 *>(a.q + orow * kHd + 64 * half);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 w = row_ok ? __ldg(qs + c) : make_uint4(0u, 0u, 0u, 0u);
-      qv[4 * c] = w.x;
-      qv[4 * c + 1] = w.y;
-      qv[4 * c + 2] = w.z;
-      qv[4 * c + 3] = w.w;
-    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -412,166 +404,169 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      // K_j goes to stage j % kStages once S_{j-kStages} has read that stage
-      // (kBarKF), V_j once PV_{j-kStages} has (kBarVF).  Each condition is a
-      // phase of a barrier whose earlier phases this thread has already seen
-      // and whose next phase needs the tile about to be loaded, so the parity
-      // test cannot alias.  The two rings are polled and V never runs ahead
-      // of K.
-      auto load_k = [&](int j) {
-        const int st = j % kStages;
-        mbar_expect_tx(bar(kBarK + st), kTile);
-        tma_load4(sK + st * kTile, &tkv, 0, kvh, j * kKeys, b, bar(kBarK + st));
-        tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, b, bar(kBarK + st));
-      };
-      auto load_v = [&](int j) {
-        const int st = j % kStages;
-        mbar_expect_tx(bar(kBarV + st), kTile);
-        tma_load4(sV + st * kTile, &tkv, 0, kvh, j * kKeys, a.B + b, bar(kBarV + st));
-        tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, kvh, j * kKeys, a.B + b, bar(kBarV + st));
-      };
-      int kn = n_tiles < kStages ? n_tiles : kStages, vn = kn;  // tiles issued
+      // K tile g (CTA-wide count) goes to stage g % kStages once S_{g-kStages}
+      // has read that stage (kBarKF), V tile g once PV_{g-kStages} has
+      // (kBarVF).  Each condition is a phase of a barrier whose earlier
+      // phases this thread has already seen and whose next phase needs the
+      // tile about to be loaded, so the parity test cannot alias.  The two
+      // rings are polled; V never runs ahead of K.
+      int gk = 0, gv = 0, nq = 0;
       unsigned long long t_last = global_ns();
-      while (kn < n_tiles || vn < n_tiles) {
-        bool did = false;
-        if (kn < n_tiles &&
-            (kn < kStages ||
-             mbar_test(bar(kBarKF + kn % kStages), ((kn - kStages) / kStages) & 1))) {
-          load_k(kn++);
-          did = true;
-        }
-        if (vn < kn &&
-            (vn < kStages ||
-             mbar_test(bar(kBarVF + vn % kStages), ((vn - kStages) / kStages) & 1))) {
-          load_v(vn++);
-          did = true;
-        }
-        if (did) {
+      bool stop = false;
+      for (int it = blockIdx.x; it < a.n_items && !stop; it += gridDim.x) {
+        const Item x = decode_item(a, it);
+        if (x.n_tiles > 0) {
+          // the item's query tile, once the softmax warps have read the last
+          // one (the previous phase of kBarQF, already seen by this thread)
+          if (nq > 0 && !mbar_wait(bar(kBarQF), (nq - 1) & 1, abort)) {
+            atomicMin(const_cast<int *>(abort_item), it);
+            break;
+          }
+          mbar_expect_tx(bar(kBarQS), kTile);
+          tma_load4(sQ, &tq, 0, x.kvh * a.G, x.mt * a.npt, x.b, bar(kBarQS));
+          tma_load4(sQ + kHalfTile, &tq, 64, x.kvh * a.G, x.mt * a.npt, x.b, bar(kBarQS));
+          ++nq;
           t_last = global_ns();
-          continue;
         }
-        if (*abort) break;
-        if (global_ns() - t_last > kWaitNs) {
-          *abort = 1;
-          break;
+        int kn = 0, vn = 0;
+        while (kn < x.n_tiles || vn < x.n_tiles) {
+          bool did = false;
+          if (kn < x.n_tiles &&
+              (gk < kStages ||
+               mbar_test(bar(kBarKF + gk % kStages), ((gk - kStages) / kStages) & 1))) {
+            const int st = gk % kStages;
+            mbar_expect_tx(bar(kBarK + st), kTile);
+            tma_load4(sK + st * kTile, &tkv, 0, x.kvh, kn * kKeys, x.b, bar(kBarK + st));
+            tma_load4(sK + st * kTile + kHalfTile, &tkv, 64, x.kvh, kn * kKeys, x.b,
+                      bar(kBarK + st));
+            ++kn;
+            ++gk;
+            did = true;
+          }
+          if (vn < kn &&
+              (gv < kStages ||
+               mbar_test(bar(kBarVF + gv % kStages), ((gv - kStages) / kStages) & 1))) {
+            const int st = gv % kStages;
+            mbar_expect_tx(bar(kBarV + st), kTile);
+            tma_load4(sV + st * kTile, &tkv, 0, x.kvh, vn * kKeys, a.B + x.b, bar(kBarV + st));
+            tma_load4(sV + st * kTile + kHalfTile, &tkv, 64, x.kvh, vn * kKeys, a.B + x.b,
+                      bar(kBarV + st));
+            ++vn;
+            ++gv;
+            did = true;
+          }
+          if (did) {
+            t_last = global_ns();
+            continue;
+          }
+          if (*abort || global_ns() - t_last > kWaitNs) {
+            *abort = 1;
+            atomicMin(const_cast<int *>(abort_item), it);
+            stop = true;
+            break;
+          }
+          __nanosleep(64);
         }
-        __nanosleep(64);
       }
       // every copy issued has landed before the CTA exits (immediate unless a
       // consumer gave up early): the newest phase of each stage barrier
       volatile int no_abort = 0;
-      for (int j = kn > kStages ? kn - kStages : 0; j < kn; ++j)
-        mbar_wait(bar(kBarK + j % kStages), (j / kStages) & 1, &no_abort);
-      for (int j = vn > kStages ? vn - kStages : 0; j < vn; ++j)
-        mbar_wait(bar(kBarV + j % kStages), (j / kStages) & 1, &no_abort);
+      for (int g = gk > kStages ? gk - kStages : 0; g < gk; ++g)
+        mbar_wait(bar(kBarK + g % kStages), (g / kStages) & 1, &no_abort);
+      for (int g = gv > kStages ? gv - kStages : 0; g < gv; ++g)
+        mbar_wait(bar(kBarV + g % kStages), (g / kStages) & 1, &no_abort);
+      if (nq > 0) mbar_wait(bar(kBarQS), (nq - 1) & 1, &no_abort);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     // Both products take their A operand from tensor memory (Q, then P) and
-    // only K or V from shared memory.  Once P_i is ready, PV_i is issued and
-    // then S_{i+2} (into the S buffer that S_i has left): PV_i retires first,
-    // which is what the softmax of tile i + 1 waits for; S_0 and S_1 go
-    // first on their own.
-    // The whole warp runs the loop converged and elect.sync picks the lane
-    // that issues: a lone diverged lane issues far more slowly while the
-    // softmax warps keep the sub-partition busy.  Descriptors are a stage
-    // base plus a constant step (the start address is the low 14 bits).
-    int s_issued = 0, pv_issued = 0;
-    bool ok = mbar_wait(bar(kBarQ), 0, abort);
-    ok = __all_sync(0xffffffffu, ok);
+    // only K or V from shared memory.  Per item: S of the first two tiles,
+    // then for each tile i, once P_i is ready, PV_i and then S_{i+2} (into
+    // the S buffer that S_i has left): PV_i retires first, which is what the
+    // softmax of tile i + 1 waits for.  The whole warp runs the loop
+    // converged and elect.sync picks the issuing lane: a lone diverged lane
+    // issues far more slowly while the softmax warps keep the sub-partition
+    // busy.  Descriptors are a stage base plus a constant step (the start
+    // address is the low 14 bits).  gS / gP count S and PV tiles CTA-wide.
+    int gS = 0, gP = 0, nq = 0;
+    bool ok = true;
     const uint64_t dK0 = sdesc(sK, 16, 1024), dV0 = sdesc(sV, kHalfTile, 1024);
     constexpr uint64_t kStageStep = kTile >> 4;
-    tc_fence_after();
-    int sk = 0;  // stage of the next K tile to consume
-    for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarK + sk), 0, abort));
+    auto issue_s = [&](int g) {
+      const uint64_t dk = dK0 + (g % kStages) * kStageStep;
+#pragma unroll
+      for (int ks = 0; ks < kHd / 16; ++ks)
+        mma_ts(tmem + (g & 1) * kKeys, tmem + kColQ + ks * 8,
+               dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
+      mma_commit(bar(kBarS + (g & 1)));
+      mma_commit(bar(kBarKF + g % kStages));
+    };
+    auto wait_s_ready = [&](int g) -> bool {  // K_g landed, S buffer g % 2 read out
+      return (g < 2 || mbar_wait(bar(kBarSF + (g & 1)), ((g - 2) >> 1) & 1, abort)) &&
+             mbar_wait(bar(kBarK + g % kStages), (g / kStages) & 1, abort);
+    };
+    int it = blockIdx.x;
+    for (; ok && it < a.n_items; it += gridDim.x) {
+      const Item x = decode_item(a, it);
+      if (x.n_tiles == 0) continue;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQ), nq & 1, abort));  // this item's Q
+      ++nq;
       if (!ok) break;
       tc_fence_after();
-      if (elect_one()) {
-        const uint64_t dk = dK0 + sk * kStageStep;
-#pragma unroll
-        for (int ks = 0; ks < kHd / 16; ++ks)
-          mma_ts(tmem + j * kKeys, tmem + kColQ + ks * 8,
-                 dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
-        mma_commit(bar(kBarS + j));
-        mma_commit(bar(kBarKF + sk));
-      }
-      __syncwarp();
-      s_issued = j + 1;
-      sk = sk + 1 == kStages ? 0 : sk + 1;
-    }
-    int sv = 0;  // stage of the next V tile
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const bool with_s = i + 2 < n_tiles;
-      bool w = true;
-      if (with_s)
-        w = mbar_wait(bar(kBarSF + (i & 1)), (i >> 1) & 1, abort) &&
-            mbar_wait(bar(kBarK + sk), ((i + 2) / kStages) & 1, abort);
-      w = w && mbar_wait(bar(kBarP + (i & 1)), (i >> 1) & 1, abort) &&
-          mbar_wait(bar(kBarV + sv), (i / kStages) & 1, abort);
-      ok = __all_sync(0xffffffffu, w);
-      if (!ok) break;
-      // the last tile's PV runs only the K16 steps holding keys below
-      // n_keys; value rows past the last key inside the last step may hold
-      // anything (NaN included) and are zeroed, so that P = 0 there adds 0
-      const int rem = n_keys - i * kKeys;
-      const int pv_steps = (i == n_tiles - 1) ? (rem + 15) >> 4 : 8;
-      if (i == n_tiles - 1 && (rem & 15)) {
-        uint8_t *vt = sm + kOffV + sv * kTile;
-        const int nrow = 16 * pv_steps - rem;  // < 16 rows, 16 chunks each
-        for (int c = lane; c < nrow * 16; c += 32) {
-          const int row = rem + (c >> 4), ch = c & 15;
-          *reinterpret_cast<uint4 *>(vt + (ch >> 3) * kHalfTile + row * 128 + (ch & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int j = 0; ok && j < 2 && j < x.n_tiles; ++j) {
+        ok = __all_sync(0xffffffffu, wait_s_ready(gS));
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) issue_s(gS);
         __syncwarp();
+        ++gS;
       }
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t dk = dK0 + sk * kStageStep, dv = dV0 + sv * kStageStep;
-        const uint32_t dS = tmem + (i & 1) * kKeys;
-        if (with_s) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
-                   (i > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(kBarPV + (i & 1)));
-          mma_commit(bar(kBarVF + sv));
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(dS, tmem + kColQ + ks * 8,
-                   dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
-          mma_commit(bar(kBarS + (i & 1)));
-          mma_commit(bar(kBarKF + sk));
-        } else {
+      for (int i = 0; ok && i < x.n_tiles; ++i) {
+        const bool with_s = i + 2 < x.n_tiles;
+        bool w = (!with_s || wait_s_ready(gS)) &&
+                 mbar_wait(bar(kBarP + (gP & 1)), (gP >> 1) & 1, abort) &&
+                 mbar_wait(bar(kBarV + gP % kStages), (gP / kStages) & 1, abort);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        // the last tile's PV runs only the K16 steps holding keys below
+        // n_keys; value rows past the last key inside the last step may hold
+        // anything (NaN included) and are zeroed, so that P = 0 there adds 0
+        const int sv = gP % kStages;
+        const int rem = x.n_keys - i * kKeys;
+        const int pv_steps = (i == x.n_tiles - 1) ? (rem + 15) >> 4 : 8;
+        if (i == x.n_tiles - 1 && (rem & 15)) {
+          uint8_t *vt = sm + kOffV + sv * kTile;
+          const int nrow = 16 * pv_steps - rem;  // < 16 rows, 16 chunks each
+          for (int c = lane; c < nrow * 16; c += 32) {
+            const int row = rem + (c >> 4), ch = c & 15;
+            *reinterpret_cast<uint4 *>(vt + (ch >> 3) * kHalfTile + row * 128 + (ch & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dv = dV0 + sv * kStageStep;
           for (int ks = 0; ks < pv_steps; ++ks)
             mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
                    (i > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar(kBarPV + (i & 1)));
+          mma_commit(bar(kBarPV + (gP & 1)));
           mma_commit(bar(kBarVF + sv));
+          if (with_s) issue_s(gS);
         }
+        __syncwarp();
+        ++gP;
+        if (with_s) ++gS;
       }
-      __syncwarp();
-      if (with_s) {
-        s_issued = i + 3;
-        sk = sk + 1 == kStages ? 0 : sk + 1;
-      }
-      pv_issued = i + 1;
-      sv = sv + 1 == kStages ? 0 : sv + 1;
     }
     if (!ok) {
+      if (lane == 0) atomicMin(const_cast<int *>(abort_item), it);
       // retire the MMAs in flight before tensor memory is released: the last
       // S and the last PV commit are the newest phases of their barriers
       volatile int no_abort = 0;
-      if (s_issued > 0) {
-        const int i = s_issued - 1;
-        mbar_wait(bar(kBarS + (i & 1)), (i >> 1) & 1, &no_abort);
-      }
-      if (pv_issued > 0) {
-        const int i = pv_issued - 1;
-        mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, &no_abort);
-      }
+      if (gS > 0) mbar_wait(bar(kBarS + ((gS - 1) & 1)), ((gS - 1) >> 1) & 1, &no_abort);
+      if (gP > 0) mbar_wait(bar(kBarPV + ((gP - 1) & 1)), ((gP - 1) >> 1) & 1, &no_abort);
     }
   } else {
     // ---------------------------------------------------------------- softmax
@@ -582,189 +577,241 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // spread over the four threads of a quad, so row maxima and sums are two
     // shuffles and no warp waits for another.  The P store (16x128b) writes
     // bf16 pair column 4 c + t % 4, exactly the two keys the thread holds.
+    // gT counts tiles CTA-wide (S buffers, P and PV barriers follow it).
     const int half = (warp - 2) >> 2;
     const int q4 = lane & 3;
     const uint32_t lane16 = (uint32_t)(quarter * 32 + half * 16) << 16;
     const int rowA = quarter * 32 + half * 16 + (lane >> 2);  // and rowA + 8
     const float NEG_INF = -INFINITY;
-    {
-      // this warp's query columns (head-dim half) for all 32 lanes of the
-      // quarter into tensor memory, bf16 pairs (32x32b: lane = row)
-      tm_st32u(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 32 * half, qv);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQ));
-    }
-    // the two rows of this thread
-    int rnode[2];
-    size_t rrow[2];
-    bool rok[2];
-    const uint64_t *rmask[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int rr = rowA + 8 * e;
-      rnode[e] = node0 + rr / a.G;
-      rok[e] = rnode[e] < a.T;
-      rrow[e] = ((size_t)b * a.T + rnode[e]) * a.Hq + kvh * a.G + rr % a.G;
-      rmask[e] = rok[e] ? a.mask + ((size_t)b * a.T + rnode[e]) * a.W : nullptr;
-    }
-    float m_ref[2] = {NEG_INF, NEG_INF};  // reference max (log2 domain, scaled)
-    float l[2] = {0.0f, 0.0f};            // partial sums over this thread's columns
+    int gT = 0, it = blockIdx.x, nq = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(bar(kBarS + sb), (j >> 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      // s[4c + 0, 1]: row A, keys 8c + 2 q4 + {0, 1}; s[4c + 2, 3]: row B
-      float s[64];
-      tm_ld16x256_x8(tmem + lane16 + sb * kKeys, s);
-      tm_ld16x256_x8(tmem + lane16 + sb * kKeys + 64, s + 32);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSF + sb));  // S buffer sb read out
-      const int key0 = j * kKeys;
-      if (key0 + kKeys > bs) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            // keys key0 + 32 g .. +31: chunks c = 4 g .. 4 g + 3
-            const uint32_t vis = visible32(rmask[e], a.W, a.T, key0 + 32 * g - bs);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const int c = 4 * g + cc, bit = 8 * cc + 2 * q4;
-              if (!((vis >> bit) & 1u)) s[4 * c + 2 * e] = NEG_INF;
-              if (!((vis >> (bit + 1)) & 1u)) s[4 * c + 2 * e + 1] = NEG_INF;
-            }
-          }
+    for (; ok && it < a.n_items; it += gridDim.x) {
+      const Item x = decode_item(a, it);
+      const int node0 = x.mt * a.npt;
+      // the 32x32b row of this thread (query copy, rows of a bad sequence)
+      const int r32 = quarter * 32 + lane;
+      const int node32 = node0 + r32 / a.G;
+      const bool ok32 = node32 < a.T;
+      const size_t orow32 = ((size_t)x.b * a.T + node32) * a.Hq + x.kvh * a.G + r32 % a.G;
+      if (x.bad) {
+        // base out of range: NaN rows, nothing read
+        if (half == 0 && ok32) {
+          const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+          uint4 *o = reinterpret_cast<uint4 *>(a.out + orow32 * kHd);
+          for (int c = 0; c < kHd / 8; ++c) o[c] = nan4;
+          if (a.lse) a.lse[orow32] = __int_as_float(0x7FC00000);
         }
-      }
-      float factor[2], mneg[2];
-      bool any_grow = false;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        // four independent chains over the 32 values of row e (chunks 0..15)
-        float pm[4] = {s[2 * e], s[2 * e + 1], s[4 + 2 * e], s[4 + 2 * e + 1]};
-#pragma unroll
-        for (int c = 2; c < 16; c += 2) {
-          pm[0] = fmaxf(pm[0], s[4 * c + 2 * e]);
-          pm[1] = fmaxf(pm[1], s[4 * c + 2 * e + 1]);
-          pm[2] = fmaxf(pm[2], s[4 * c + 4 + 2 * e]);
-          pm[3] = fmaxf(pm[3], s[4 * c + 4 + 2 * e + 1]);
-        }
-        float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx *= a.scale_log2;  // scale > 0: max commutes with it
-        const bool grow = mx > m_ref[e] + kRescaleLog2;
-        const float m_new = grow ? mx : m_ref[e];
-        factor[e] = (grow && m_ref[e] != NEG_INF) ? ex2(m_ref[e] - m_new) : 1.0f;
-        any_grow |= factor[e] != 1.0f;
-        l[e] *= factor[e];
-        m_ref[e] = m_new;
-        mneg[e] = m_new == NEG_INF ? 0.0f : -m_new;
-      }
-      // p = 2^(scale*log2e*s - m): scaling and sums on packed fp32 pairs,
-      // the exponentials on the MUFU (moving a share of them to a polynomial
-      // on the FMA pipe measured slower: the warps are bound by issue slots)
-      uint32_t pk[32];
-      unsigned long long la2 = 0ull, lb2 = 0ull;
-      const unsigned long long sc2 = f2_splat(a.scale_log2);
-      const unsigned long long ma2 = f2_splat(mneg[0]), mb2 = f2_splat(mneg[1]);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const unsigned long long xa = f2_fma(f2_pack(s[4 * c], s[4 * c + 1]), sc2, ma2);
-        const unsigned long long xb = f2_fma(f2_pack(s[4 * c + 2], s[4 * c + 3]), sc2, mb2);
-        const unsigned long long pa = ex2_2(xa);
-        const unsigned long long pb = ex2_2(xb);
-        la2 = f2_add(la2, pa);
-        lb2 = f2_add(lb2, pb);
-        float p0, p1, p2, p3;
-        f2_unpack(pa, p0, p1);
-        f2_unpack(pb, p2, p3);
-        pk[2 * c] = pack_bf16(p0, p1);      // row A, pair column 4c + q4
-        pk[2 * c + 1] = pack_bf16(p2, p3);  // row B
+        if (threadIdx.x == 64 && a.status && x.mt == 0 && x.kvh == 0)
+          atomicOr(a.status + x.b, SV_ROW_BAD_BASE);
+        continue;
       }
       {
-        float u0, u1, v0, v1;
-        f2_unpack(la2, u0, u1);
-        f2_unpack(lb2, v0, v1);
-        l[0] += u0 + u1;
-        l[1] += v0 + v1;
+        // this warp's query columns (head-dim half) for all 32 lanes of the
+        // quarter, from the tile the producer staged in shared memory (128-byte
+        // swizzled: row r32, chunk c at (c ^ (r32 & 7)) * 16; rows past T are
+        // the copy's zero fill), into tensor memory as bf16 pairs (32x32b:
+        // lane = row); the item's S products wait for all eight warps
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQS), nq & 1, abort));
+        ++nq;
+        if (!ok) break;
+        uint32_t qv[32];
+        const uint8_t *qrow = sm + kOffQ + half * kHalfTile + r32 * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (r32 & 7)) << 4));
+          qv[4 * c] = w.x;
+          qv[4 * c + 1] = w.y;
+          qv[4 * c + 2] = w.z;
+          qv[4 * c + 3] = w.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQF));  // this warp is done with the tile
+        tm_st32u(tmem + ((uint32_t)(quarter * 32) << 16) + kColQ + 32 * half, qv);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQ));
       }
-      if (j >= 1) {
-        // PV_{j-1} has retired: the P columns are free and O covers tiles < j
-        const int i = j - 1;
-        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+      // the two rows of this thread
+      int rnode[2];
+      size_t rrow[2];
+      bool rok[2];
+      const uint64_t *rmask[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rr = rowA + 8 * e;
+        rnode[e] = node0 + rr / a.G;
+        rok[e] = rnode[e] < a.T;
+        rrow[e] = ((size_t)x.b * a.T + rnode[e]) * a.Hq + x.kvh * a.G + rr % a.G;
+        rmask[e] = rok[e] ? a.mask + ((size_t)x.b * a.T + rnode[e]) * a.W : nullptr;
+      }
+      // the first two mask words of both rows, fetched now for the tiles that
+      // reach the tree (the last one or two of the item)
+      uint64_t mw[2][2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int w = 0; w < 2; ++w) mw[e][w] = (rmask[e] && w < a.W) ? __ldg(rmask[e] + w) : 0ull;
+      float m_ref[2] = {NEG_INF, NEG_INF};  // reference max (log2 domain, scaled)
+      float l[2] = {0.0f, 0.0f};            // partial sums over this thread's columns
+      for (int j = 0; j < x.n_tiles; ++j) {
+        const int g = gT + j, sb = g & 1;
+        ok = mbar_wait(bar(kBarS + sb), (g >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        // s[4c + 0, 1]: row A, keys 8c + 2 q4 + {0, 1}; s[4c + 2, 3]: row B
+        float s[64];
+        tm_ld16x256_x8(tmem + lane16 + sb * kKeys, s);
+        tm_ld16x256_x8(tmem + lane16 + sb * kKeys + 64, s + 32);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSF + sb));  // S buffer sb read out
+        const int key0 = j * kKeys;
+        if (key0 + kKeys > x.bs) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+#pragma unroll
+            for (int gg = 0; gg < 4; ++gg) {
+              // keys key0 + 32 gg .. +31: chunks c = 4 gg .. 4 gg + 3
+              const uint32_t vis = visible32(rmask[e], a.W, mw[e][0], mw[e][1], a.T, key0 + 32 * gg - x.bs);
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const int c = 4 * gg + cc, bit = 8 * cc + 2 * q4;
+                if (!((vis >> bit) & 1u)) s[4 * c + 2 * e] = NEG_INF;
+                if (!((vis >> (bit + 1)) & 1u)) s[4 * c + 2 * e + 1] = NEG_INF;
+              }
+            }
+          }
+        }
+        float factor[2], mneg[2];
+        bool any_grow = false;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          // four independent chains over the 32 values of row e (chunks 0..15)
+          float pm[4] = {s[2 * e], s[2 * e + 1], s[4 + 2 * e], s[4 + 2 * e + 1]};
+#pragma unroll
+          for (int c = 2; c < 16; c += 2) {
+            pm[0] = fmaxf(pm[0], s[4 * c + 2 * e]);
+            pm[1] = fmaxf(pm[1], s[4 * c + 2 * e + 1]);
+            pm[2] = fmaxf(pm[2], s[4 * c + 4 + 2 * e]);
+            pm[3] = fmaxf(pm[3], s[4 * c + 4 + 2 * e + 1]);
+          }
+          float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx *= a.scale_log2;  // scale > 0: max commutes with it
+          const bool grow = mx > m_ref[e] + kRescaleLog2;
+          const float m_new = grow ? mx : m_ref[e];
+          factor[e] = (grow && m_ref[e] != NEG_INF) ? ex2(m_ref[e] - m_new) : 1.0f;
+          any_grow |= factor[e] != 1.0f;
+          l[e] *= factor[e];
+          m_ref[e] = m_new;
+          mneg[e] = m_new == NEG_INF ? 0.0f : -m_new;
+        }
+        // p = 2^(scale*log2e*s - m): scaling and sums on packed fp32 pairs,
+        // the exponentials on the MUFU (moving a share of them to a polynomial
+        // on the FMA pipe measured slower: the warps are bound by issue slots)
+        uint32_t pk[32];
+        unsigned long long la2 = 0ull, lb2 = 0ull;
+        const unsigned long long sc2 = f2_splat(a.scale_log2);
+        const unsigned long long ma2 = f2_splat(mneg[0]), mb2 = f2_splat(mneg[1]);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const unsigned long long xa = f2_fma(f2_pack(s[4 * c], s[4 * c + 1]), sc2, ma2);
+          const unsigned long long xb = f2_fma(f2_pack(s[4 * c + 2], s[4 * c + 3]), sc2, mb2);
+          const unsigned long long pa = ex2_2(xa);
+          const unsigned long long pb = ex2_2(xb);
+          la2 = f2_add(la2, pa);
+          lb2 = f2_add(lb2, pb);
+          float p0, p1, p2, p3;
+          f2_unpack(pa, p0, p1);
+          f2_unpack(pb, p2, p3);
+          pk[2 * c] = pack_bf16(p0, p1);      // row A, pair column 4c + q4
+          pk[2 * c + 1] = pack_bf16(p2, p3);  // row B
+        }
+        {
+          float u0, u1, v0, v1;
+          f2_unpack(la2, u0, u1);
+          f2_unpack(lb2, v0, v1);
+          l[0] += u0 + u1;
+          l[1] += v0 + v1;
+        }
+        if (j >= 1) {
+          // PV_{g-1} has retired: the P columns are free and O covers tiles < j
+          const int i = g - 1;
+          ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, any_grow)) {
+          // the max grew: bring these rows of O to the new reference
+#pragma unroll
+          for (int c = 0; c < kHd; c += 64) {
+            float o[32];
+            tm_ld16x256_x8(tmem + lane16 + kColO + c, o);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= factor[(k >> 1) & 1];
+            tm_st16x256_x8(tmem + lane16 + kColO + c, o);
+          }
+        }
+        tm_st16x128_x16(tmem + lane16 + kColP, pk);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarP + sb));
       }
-      if (__any_sync(0xffffffffu, any_grow)) {
-        // the max grew: bring these rows of O to the new reference
+      if (ok) {
+        const int i = gT + x.n_tiles - 1;
+        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        tc_fence_after();
+        float inv[2], lt[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = l[e];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          lt[e] = v;
+          inv[e] = v > 0.0f ? 1.0f / v : 0.0f;
+        }
 #pragma unroll
         for (int c = 0; c < kHd; c += 64) {
           float o[32];
           tm_ld16x256_x8(tmem + lane16 + kColO + c, o);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          // o[4k + 0, 1]: row A, columns c + 8k + 2 q4 + {0, 1}; o[4k + 2, 3]: row B
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] *= factor[(k >> 1) & 1];
-          tm_st16x256_x8(tmem + lane16 + kColO + c, o);
+          for (int e = 0; e < 2; ++e) {
+            if (!rok[e]) continue;
+            uint32_t *orow32 = reinterpret_cast<uint32_t *>(a.out + rrow[e] * kHd + c + 2 * q4);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              orow32[4 * k] = pack_bf16(o[4 * k + 2 * e] * inv[e], o[4 * k + 2 * e + 1] * inv[e]);
+          }
+        }
+        if (q4 == 0 && a.lse) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (rok[e])
+              a.lse[rrow[e]] =
+                  lt[e] > 0.0f ? (m_ref[e] + __log2f(lt[e])) * 0.69314718055994531f : NEG_INF;
         }
       }
-      tm_st16x128_x16(tmem + lane16 + kColP, pk);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + sb));
+      gT += x.n_tiles;
     }
-    if (ok) {
-      const int i = n_tiles - 1;
-      ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      float inv[2], lt[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = l[e];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        lt[e] = v;
-        inv[e] = v > 0.0f ? 1.0f / v : 0.0f;
-      }
-#pragma unroll
-      for (int c = 0; c < kHd; c += 64) {
-        float o[32];
-        tm_ld16x256_x8(tmem + lane16 + kColO + c, o);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        // o[4k + 0, 1]: row A, columns c + 8k + 2 q4 + {0, 1}; o[4k + 2, 3]: row B
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          if (!rok[e]) continue;
-          uint32_t *orow32 = reinterpret_cast<uint32_t *>(a.out + rrow[e] * kHd + c + 2 * q4);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            orow32[4 * k] = pack_bf16(o[4 * k + 2 * e] * inv[e], o[4 * k + 2 * e + 1] * inv[e]);
-        }
-      }
-      if (q4 == 0 && a.lse) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (rok[e])
-            a.lse[rrow[e]] =
-                lt[e] > 0.0f ? (m_ref[e] + __log2f(lt[e])) * 0.69314718055994531f : NEG_INF;
-      }
-    }
+    if (!ok) atomicMin(const_cast<int *>(abort_item), it);
   }
   tc_fence_before();
   __syncthreads();
-  if (*abort && threadIdx.x == 0 && a.status) atomicOr(a.status + b, SV_ROW_TIMEOUT);
+  if (*abort && threadIdx.x == 0 && a.status)
+    for (int it = *abort_item; it < a.n_items; it += gridDim.x)
+      if (it % (int)gridDim.x == (int)blockIdx.x) atomicOr(a.status + decode_item(a, it).b, SV_ROW_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -840,7 +887,14 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
       (s = map_arg(out_status, "out_status")) != SV_OK)
     return s;
   const int npt = kRows / G;
-  CUtensorMap tkv;
+  CUtensorMap tq, tkv;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hq, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t str[3] = {(cuuint64_t)kHd * 2, (cuuint64_t)Hq * kHd * 2,
+                               (cuuint64_t)T * Hq * kHd * 2};
+    if ((s = encode4(&tq, q, dims, str, (cuuint32_t)G, (cuuint32_t)(kRows / G), "q")) != SV_OK)
+      return s;
+  }
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kHd, (cuuint64_t)Hkv, (cuuint64_t)S,
                                 (cuuint64_t)2 * B};
@@ -875,9 +929,14 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
   a.npt = npt;
   a.scale_log2 = scale * 1.4426950408889634f;
   const int mtiles = (T + npt - 1) / npt;
+  const long long n_items = (long long)mtiles * Hkv * B;
+  if (n_items > 0x7fffffffLL) return set_error(SV_ERR_UNSUPPORTED, "too many query tiles");
+  a.mtiles = mtiles;
+  a.n_items = (int)n_items;
+  const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("tree_attention", st);
   return check_launch("tree_attention",
-                      launch_pdl(tree_attn_kernel, dim3(mtiles, Hkv, B), dim3(kAttnThreads),
-                                 kAttnSmem, st, tkv, a));
+                      launch_pdl(tree_attn_kernel, dim3(grid), dim3(kAttnThreads),
+                                 kAttnSmem, st, tq, tkv, a));
 }
