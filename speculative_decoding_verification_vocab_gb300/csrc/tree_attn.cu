@@ -9,24 +9,26 @@
 // tree pass runs a non-causal mask that follows the tree.  This is the
 // attention of that pass for one layer, with grouped-query heads.
 //
-// One CTA owns 128 query rows of one (sequence, KV head): the G = Hq / Hkv
+// Work item: 128 query rows of one (sequence, KV head) -- the G = Hq / Hkv
 // query heads sharing that KV head times 128 / G consecutive tree nodes, row
-// r = node_local * G + head_local.  It walks the sequence's keys (context,
-// then the T tree rows) in tiles of 128:
-//   warp 0      TMA producer: the query tile once, then K and V tiles into a
-//               two-stage ring (128B-swizzled boxes of 64 columns);
-//   warp 1      MMA issuer: S_j = Q K_j^T into S buffer j mod 2 in tensor
-//               memory, O_{j mod 2} += P_j V_j;
-//   warps 2..9  softmax, two warpgroups: warpgroup g takes the key tiles
-//               j = g mod 2 (one row per thread), with its own S buffer, P
-//               buffer and O accumulator: S_j from tensor memory to
-//               registers, ancestor mask, running max with a lazy rescale of
-//               O_g (only when the max grows by more than 2^8), P_j =
-//               exp2(...) as bf16 into shared memory in the MMA's operand
-//               layout.  At the end the two partial results (m, l, O_g) of a
-//               row are merged and normalised.
+// r = node_local * G + head_local.  The kernel is persistent: one CTA per SM
+// walks items c, c + gridDim.x, ... and, per item, the sequence's keys
+// (context, then the T tree rows) in tiles of 128:
+//   warp 0      TMA producer: each item's query tile into shared memory, K
+//               and V tiles into three-stage rings (128B-swizzled boxes of 64
+//               columns), each load issued as soon as its stage is free;
+//   warp 1      MMA issuer (converged warp, elect.sync): S_j = Q K_j^T into
+//               the S buffer of tensor memory as soon as the softmax warps
+//               have read S_{j-1} out of it, O += P_j V_j once P_j is ready;
+//               both with the A operand (Q, P) in tensor memory;
+//   warps 2..9  softmax: query tile from shared memory to tensor memory;
+//               per tile S_j to registers (16-lane shapes: a row over a quad
+//               of threads), ancestor mask, running max with a lazy rescale
+//               of O (only when the max grows by more than 2^8), P_j =
+//               exp2(...) as bf16 into one of two P buffers in tensor memory;
+//               at the end of the item O / l to global memory.
 // Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
-// out sets SV_ROW_TIMEOUT for the sequence and the CTA drains and exits.
+// out sets SV_ROW_TIMEOUT for the sequences left and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -56,9 +58,9 @@ constexpr size_t kAttnSmem = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr int kBarQ = 0, kBarK = 1, kBarV = kBarK + kStages, kBarKF = kBarV + kStages,
               kBarVF = kBarKF + kStages, kBarS = kBarVF + kStages, kBarSF = kBarS + 2,
               kBarP = kBarSF + 2, kBarPV = kBarP + 2, kBarQS = kBarPV + 2, kBarQF = kBarQS + 1;
-// tensor-memory columns: S buffers at 0 and 128, O at 256, Q (bf16 pairs) at
-// 384, P (bf16 pairs) at 448
-constexpr uint32_t kColO = 256, kColQ = 384, kColP = 448;
+// tensor-memory columns: S at 0, O at 128, Q (bf16 pairs) at 256, two P
+// buffers (bf16 pairs) at 320 and 384
+constexpr uint32_t kColS = 0, kColO = 128, kColQ = 256, kColP = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (log2 units)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
@@ -480,10 +482,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     // Both products take their A operand from tensor memory (Q, then P) and
-    // only K or V from shared memory.  Per item: S of the first two tiles,
-    // then for each tile i, once P_i is ready, PV_i and then S_{i+2} (into
-    // the S buffer that S_i has left): PV_i retires first, which is what the
-    // softmax of tile i + 1 waits for.  The whole warp runs the loop
+    // only K or V from shared memory.  One S buffer: S_{i+1} is issued as soon
+    // as the softmax warps have read S_i out of it (early in their tile i),
+    // so it is ready when they finish tile i; PV_i follows once P_i is ready,
+    // reading P buffer i % 2 (the softmax writes P_{i+1} into the other one
+    // meanwhile).  The whole warp runs the loop
     // converged and elect.sync picks the issuing lane: a lone diverged lane
     // issues far more slowly while the softmax warps keep the sub-partition
     // busy.  Descriptors are a stage base plus a constant step (the start
@@ -496,13 +499,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t dk = dK0 + (g % kStages) * kStageStep;
 #pragma unroll
       for (int ks = 0; ks < kHd / 16; ++ks)
-        mma_ts(tmem + (g & 1) * kKeys, tmem + kColQ + ks * 8,
+        mma_ts(tmem + kColS, tmem + kColQ + ks * 8,
                dk + (uint64_t)(((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4), kIdescS, ks > 0);
-      mma_commit(bar(kBarS + (g & 1)));
+      mma_commit(bar(kBarS));
       mma_commit(bar(kBarKF + g % kStages));
     };
-    auto wait_s_ready = [&](int g) -> bool {  // K_g landed, S buffer g % 2 read out
-      return (g < 2 || mbar_wait(bar(kBarSF + (g & 1)), ((g - 2) >> 1) & 1, abort)) &&
+    auto wait_s_ready = [&](int g) -> bool {  // K_g landed, S_{g-1} read out
+      return (g < 1 || mbar_wait(bar(kBarSF), (g - 1) & 1, abort)) &&
              mbar_wait(bar(kBarK + g % kStages), (g / kStages) & 1, abort);
     };
     int it = blockIdx.x;
@@ -513,20 +516,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ++nq;
       if (!ok) break;
       tc_fence_after();
-      for (int j = 0; ok && j < 2 && j < x.n_tiles; ++j) {
-        ok = __all_sync(0xffffffffu, wait_s_ready(gS));
-        if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) issue_s(gS);
-        __syncwarp();
-        ++gS;
-      }
+      ok = __all_sync(0xffffffffu, wait_s_ready(gS));
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) issue_s(gS);
+      __syncwarp();
+      ++gS;
       for (int i = 0; ok && i < x.n_tiles; ++i) {
-        const bool with_s = i + 2 < x.n_tiles;
-        bool w = (!with_s || wait_s_ready(gS)) &&
-                 mbar_wait(bar(kBarP + (gP & 1)), (gP >> 1) & 1, abort) &&
-                 mbar_wait(bar(kBarV + gP % kStages), (gP / kStages) & 1, abort);
-        ok = __all_sync(0xffffffffu, w);
+        if (i + 1 < x.n_tiles) {
+          ok = __all_sync(0xffffffffu, wait_s_ready(gS));
+          if (!ok) break;
+          tc_fence_after();
+          if (elect_one()) issue_s(gS);
+          __syncwarp();
+          ++gS;
+        }
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(kBarP + (gP & 1)), (gP >> 1) & 1, abort) &&
+                            mbar_wait(bar(kBarV + gP % kStages), (gP / kStages) & 1, abort));
         if (!ok) break;
         // the last tile's PV runs only the K16 steps holding keys below
         // n_keys; value rows past the last key inside the last step may hold
@@ -548,16 +555,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         if (elect_one()) {
           const uint64_t dv = dV0 + sv * kStageStep;
+          const uint32_t pa = tmem + kColP + (gP & 1) * 64;
           for (int ks = 0; ks < pv_steps; ++ks)
-            mma_ts(tmem + kColO, tmem + kColP + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
+            mma_ts(tmem + kColO, pa + ks * 8, dv + (uint64_t)(ks * 128), kIdescO,
                    (i > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar(kBarPV + (gP & 1)));
           mma_commit(bar(kBarVF + sv));
-          if (with_s) issue_s(gS);
         }
         __syncwarp();
         ++gP;
-        if (with_s) ++gS;
       }
     }
     if (!ok) {
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // retire the MMAs in flight before tensor memory is released: the last
       // S and the last PV commit are the newest phases of their barriers
       volatile int no_abort = 0;
-      if (gS > 0) mbar_wait(bar(kBarS + ((gS - 1) & 1)), ((gS - 1) >> 1) & 1, &no_abort);
+      if (gS > 0) mbar_wait(bar(kBarS), (gS - 1) & 1, &no_abort);
       if (gP > 0) mbar_wait(bar(kBarPV + ((gP - 1) & 1)), ((gP - 1) >> 1) & 1, &no_abort);
     }
   } else {
@@ -655,19 +661,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float m_ref[2] = {NEG_INF, NEG_INF};  // reference max (log2 domain, scaled)
       float l[2] = {0.0f, 0.0f};            // partial sums over this thread's columns
       for (int j = 0; j < x.n_tiles; ++j) {
-        const int g = gT + j, sb = g & 1;
-        ok = mbar_wait(bar(kBarS + sb), (g >> 1) & 1, abort);
+        const int g = gT + j, pb = g & 1;
+        ok = mbar_wait(bar(kBarS), g & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
         // s[4c + 0, 1]: row A, keys 8c + 2 q4 + {0, 1}; s[4c + 2, 3]: row B
         float s[64];
-        tm_ld16x256_x8(tmem + lane16 + sb * kKeys, s);
-        tm_ld16x256_x8(tmem + lane16 + sb * kKeys + 64, s + 32);
+        tm_ld16x256_x8(tmem + lane16 + kColS, s);
+        tm_ld16x256_x8(tmem + lane16 + kColS + 64, s + 32);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarSF + sb));  // S buffer sb read out
+        if (lane == 0) mbar_arrive(bar(kBarSF));  // the S buffer is free for S_{g+1}
         const int key0 = j * kKeys;
         if (key0 + kKeys > x.bs) {
 #pragma unroll
@@ -738,16 +744,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           l[0] += u0 + u1;
           l[1] += v0 + v1;
         }
-        if (j >= 1) {
-          // PV_{g-1} has retired: the P columns are free and O covers tiles < j
-          const int i = g - 1;
+        if (g >= 2) {
+          // PV_{g-2} has retired: P buffer pb is free (this warp has seen
+          // every earlier phase of its barrier)
+          const int i = g - 2;
           ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          tc_fence_after();
         }
         if (__any_sync(0xffffffffu, any_grow)) {
-          // the max grew: bring these rows of O to the new reference
+          // the max grew: once O covers tiles < j (PV_{g-1} retired), bring
+          // these rows of it to the new reference
+          if (j >= 1) {
+            const int i = g - 1;
+            ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < kHd; c += 64) {
             float o[32];
@@ -758,11 +772,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tm_st16x256_x8(tmem + lane16 + kColO + c, o);
           }
         }
-        tm_st16x128_x16(tmem + lane16 + kColP, pk);
+        tm_st16x128_x16(tmem + lane16 + kColP + pb * 64, pk);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarP + sb));
+        if (lane == 0) mbar_arrive(bar(kBarP + pb));
       }
       if (ok) {
         const int i = gT + x.n_tiles - 1;
