@@ -203,9 +203,25 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# the sources each profiled kernel is built from (its counters stay valid while
+# these files are unchanged)
+KERNEL_SOURCES = {
+    "row_stats": ("common.cuh", "rowstat.cuh", "verify.cu"),
+    "sampler_kv": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
+    "launches": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
+    "tree_attention": ("common.cuh", "tree_attn.cu"),
+}
+
+
+def source_hash(kernel):
+    src = os.path.join(ROOT, "speculative_decoding_verification_vocab_gb300", "csrc")
+    return hashlib.sha256(b"".join(open(os.path.join(src, f), "rb").read()
+                                   for f in KERNEL_SOURCES[kernel])).hexdigest()[:16]
+
+
 def recorded_traffic(kernel, cfg_name):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
-    was taken on the current source of the kernel (source hash recorded)."""
+    was taken on the current sources of the kernel (source hash recorded)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{cfg_name}.txt")
     if not os.path.exists(p):
         return None
@@ -214,10 +230,7 @@ def recorded_traffic(kernel, cfg_name):
     h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
     if not m or not h:
         return None
-    src = os.path.join(ROOT, "speculative_decoding_verification_vocab_gb300", "csrc")
-    cur = hashlib.sha256(b"".join(open(os.path.join(src, f), "rb").read()
-                                  for f in sorted(os.listdir(src)))).hexdigest()[:16]
-    return float(m.group(1)) if cur == h.group(1) else None
+    return float(m.group(1)) if source_hash(kernel) == h.group(1) else None
 
 
 # ------------------------------------------------------------------ workload
@@ -787,7 +800,8 @@ def run_attention(args):
         "roofline": {"kernel": "tree_attention", "bound": "tensor", "achieved": ach,
                      "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                      "peak_kind": f"{kind} bf16 dense (burst)",
-                     "alg_flops_per_launch": flops, "traffic": None},
+                     "alg_flops_per_launch": flops,
+                     "traffic": recorded_traffic("tree_attention", "dynamic_eagle2_tree")},
         "clocks": clk.summary(),
     }
     print(json.dumps(line))

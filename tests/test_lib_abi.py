@@ -72,3 +72,24 @@ def test_workspace_queries(lib):
     assert lib.sv_verify_chain_workspace(4, 3, 1000) > 0
     assert lib.sv_verify_tree_workspace(4, 25, 5, 1000) > lib.sv_verify_chain_workspace(4, 0, 1000)
     assert lib.sv_verify_chain_workspace(-1, 3, 1000) == 0
+
+
+def test_tree_attention_host_checks_need_no_gpu(lib):
+    """sv_tree_attention refuses bad shapes and scales before any CUDA call."""
+    f = lib.sv_tree_attention
+    null = None
+    # (q, kv, base, mask, B, T, Hq, Hkv, D, S, scale, out, lse, status, stream)
+    assert f(null, null, null, null, 1, 4, 8, 2, 64, 16, 1.0, null, null, null, null) == 2
+    assert b"head dimension" in lib.sv_last_error()
+    assert f(null, null, null, null, 1, 4, 9, 3, 128, 16, 1.0, null, null, null, null) == 2
+    assert f(null, null, null, null, 1, 4, 8, 3, 128, 16, 1.0, null, null, null, null) == 1
+    assert f(null, null, null, null, 1, 4, 8, 2, 128, 16, 0.0, null, null, null, null) == 1
+    assert f(null, null, null, null, 1, 4, 8, 2, 128, 16, float("nan"), null, null, null,
+             null) == 1
+    assert f(null, null, null, null, 1, 0, 8, 2, 128, 16, 1.0, null, null, null, null) == 1
+    assert f(null, null, null, null, 1, 2000, 8, 2, 128, 4096, 1.0, null, null, null,
+             null) == 2
+    # B == 0 is a no-op; null pointers with B > 0 are refused
+    assert f(null, null, null, null, 0, 4, 8, 2, 128, 16, 1.0, null, null, null, null) == 0
+    assert f(null, null, null, null, 1, 4, 8, 2, 128, 16, 1.0, null, null, null, null) == 1
+    assert b"null" in lib.sv_last_error()
