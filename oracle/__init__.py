@@ -95,6 +95,8 @@ def _declare(L):
         C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
         _i32p, C.c_int, _i32p, _f64p, _f64p, _f64p, C.c_int, _f64p, _u32p]
     L.orc_verify.restype = C.c_int
+    L.orc_verify_ex.argtypes = L.orc_verify.argtypes + [C.c_int]
+    L.orc_verify_ex.restype = C.c_int
     L.orc_tree_valid.argtypes = [_i32p, C.c_void_p, C.c_int]
     L.orc_tree_valid.restype = C.c_int
     L.orc_tree_best_path.argtypes = [_i32p, _f32p, C.c_int, C.c_int, _i32p]
@@ -233,7 +235,7 @@ def sample_repro(xq, xp, u24_, T=1.0):
 # ---------------------------------------------------------------- verify
 def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
                  seed, step, u_acc=None, u_samp=None, v_bstride=None,
-                 d_bstride=None, B=None, maxpos=None, seq_ids=None):
+                 d_bstride=None, B=None, maxpos=None, seq_ids=None, early_exit=False):
     vlog = _f32(vlog).reshape(-1)
     dlog = _f32(dlog).reshape(-1)
     npos = _i32(npos)
@@ -264,7 +266,7 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
     if seq_ids is not None:
         sid = _i32(seq_ids)
         keep.append(sid)
-    rc = lib().orc_verify(
+    rc = lib().orc_verify_ex(
         vlog, v_bstride, dlog, d_bstride, B, V, T,
         pth.ctypes.data if pth is not None else None, path_stride, npos, tok,
         tok_stride, seed, step,
@@ -272,7 +274,8 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
         ua.shape[-1] if ua is not None else 0,
         us.ctypes.data if us is not None else None,
         sid.ctypes.data if sid is not None else None,
-        out_tok, maxpos + 1, out_acc, out_q, out_p, out_m, maxpos, out_gap, out_st)
+        out_tok, maxpos + 1, out_acc, out_q, out_p, out_m, maxpos, out_gap, out_st,
+        1 if early_exit else 0)
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dict(tokens=out_tok, accept_len=out_acc, q_prob=out_q[:, :maxpos],
@@ -280,11 +283,15 @@ def _verify_core(vlog, dlog, V, T, path, path_stride, npos, tok, tok_stride,
 
 
 def verify_chain(vlogits, dlogits, draft_tokens, T=1.0, seed=0, step=0,
-                 u_acc=None, u_samp=None, shared_rows=False, seq_ids=None):
+                 u_acc=None, u_samp=None, shared_rows=False, seq_ids=None,
+                 early_exit=False):
     """Chain verify.  vlogits [B][N+1][V], dlogits [B][N][V], draft_tokens [B][N].
 
     With ``shared_rows`` the logits are a single [N+1][V] / [N][V] set used by
-    every sequence (for enumeration tests)."""
+    every sequence (for enumeration tests).  With ``early_exit`` only the rows
+    the walk reaches are checked and reported (T > 0): a bad row or token
+    after the first rejection does not fault the sequence, and q(d), p(d) and
+    the margin are NaN after the rejecting position."""
     draft_tokens = _i32(draft_tokens)
     B, N = draft_tokens.shape
     vl = _f32(vlogits)
@@ -298,7 +305,7 @@ def verify_chain(vlogits, dlogits, draft_tokens, T=1.0, seed=0, step=0,
     return _verify_core(vl, dl, V, T, None, 0, np.full(B, N, np.int32),
                         draft_tokens, N, seed, step, u_acc, u_samp,
                         v_bstride=vstride, d_bstride=dstride, B=B, maxpos=N,
-                        seq_ids=seq_ids)
+                        seq_ids=seq_ids, early_exit=early_exit)
 
 
 def verify_tree(vlogits, dlogits, parent, token, score, max_depth, T=1.0,

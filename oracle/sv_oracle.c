@@ -370,17 +370,33 @@ static int orc_verify_greedy(const float *vlog, int64_t v_bstride, int B, int V,
   return 0;
 }
 
-int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
-               int64_t d_bstride, int B, int V, float T,
-               const int32_t *path, int path_stride, const int32_t *npos_arr,
-               const int32_t *tok, int tok_stride, uint64_t seed,
-               uint64_t step, const uint32_t *u_acc, int u_acc_stride,
-               const uint32_t *u_samp, const int32_t *seq_ids,
-               int32_t *out_tokens, int out_stride,
-               int32_t *out_accept, double *out_q, double *out_p,
-               double *out_margin, int margin_stride, double *out_gap,
-               uint32_t *out_status) {
+/* The verify walk of every sequence.  Two readings of which rows a round
+ * touches:
+ *   early_exit = 0  every row and token of the round is checked before the
+ *                   walk (any bad row or token faults the sequence), and q(d),
+ *                   p(d) and the margin are reported for every position;
+ *   early_exit = 1  only the rows the walk reaches, in its order ([Lesson]
+ *                   Passo 3 and [Blog] section 4 spec_decode: the walk ends at
+ *                   the first rejection, so nothing after it is needed): at
+ *                   position i the verifier and draft rows of i and token i
+ *                   are checked first (a bad one faults the sequence with the
+ *                   bits found there), then judged; the bonus row is checked
+ *                   only when every position passes.  q(d), p(d) and the margin
+ *                   exist for positions up to the first rejection, NaN after.
+ * Accepted tokens, the correction / bonus token and the accept length are the
+ * same in both readings whenever neither faults. */
+int orc_verify_ex(const float *vlog, int64_t v_bstride, const float *dlog,
+                  int64_t d_bstride, int B, int V, float T,
+                  const int32_t *path, int path_stride, const int32_t *npos_arr,
+                  const int32_t *tok, int tok_stride, uint64_t seed,
+                  uint64_t step, const uint32_t *u_acc, int u_acc_stride,
+                  const uint32_t *u_samp, const int32_t *seq_ids,
+                  int32_t *out_tokens, int out_stride,
+                  int32_t *out_accept, double *out_q, double *out_p,
+                  double *out_margin, int margin_stride, double *out_gap,
+                  uint32_t *out_status, int early_exit) {
   if (B < 0 || V <= 0 || !(T >= 0.0f)) return -1;
+  if (early_exit && T == 0.0f) return -1;
   if (T == 0.0f)
     return orc_verify_greedy(vlog, v_bstride, B, V, path, path_stride, npos_arr, tok,
                              tok_stride, out_tokens, out_stride, out_accept, out_q, out_p,
@@ -395,6 +411,7 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
     const int32_t *pb = path ? path + (int64_t)b * path_stride : NULL;
     const int32_t *tb = tok + (int64_t)b * tok_stride;
     uint32_t status = 0;
+    int p_zero_seen = 0;
     int32_t *ot = out_tokens + (int64_t)b * out_stride;
     for (int i = 0; i < out_stride; ++i) ot[i] = -1;
     for (int i = 0; i < margin_stride; ++i) {
@@ -404,23 +421,23 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
     if (out_margin)
       for (int i = 0; i <= margin_stride; ++i)
         out_margin[(int64_t)b * (margin_stride + 1) + i] = NAN;
-    /* row and token checks over every row / token the round could touch */
-    for (int i = 0; i <= npos; ++i) {
+    /* full reading: every row / token the round could touch, before the walk */
+    for (int i = 0; i <= npos && !early_exit; ++i) {
       int r = pb ? pb[i] : i;
       if (orc_row_bad(vb + (int64_t)r * V, V)) status |= ORC_ROW_NAN;
       if (i < npos && orc_row_bad(db + (int64_t)r * V, V)) status |= ORC_ROW_NAN;
       if (i < npos && (tb[i] < 0 || tb[i] >= V)) status |= ORC_ROW_BAD_TOKEN;
     }
-    if (status) {
-      out_accept[b] = 0;
-      out_status[b] = status;
-      if (out_gap) out_gap[b] = NAN;
-      continue;
-    }
     int a = 0, stopped = 0;
-    for (int i = 0; i < npos; ++i) {
+    for (int i = 0; i < npos && !status && !(early_exit && stopped); ++i) {
       int r = pb ? pb[i] : i;
       const float *xq = vb + (int64_t)r * V, *xp = db + (int64_t)r * V;
+      if (early_exit) {
+        /* early exit: this position's rows and token, as the walk reaches them */
+        if (orc_row_bad(xq, V) || orc_row_bad(xp, V)) status |= ORC_ROW_NAN;
+        if (tb[i] < 0 || tb[i] >= V) status |= ORC_ROW_BAD_TOKEN;
+        if (status) break;
+      }
       int d = tb[i];
       double mq, sq, mp, sp;
       orc_row_stats(xq, V, Td, &mq, &sq);
@@ -444,7 +461,7 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
       if (out_margin) out_margin[(int64_t)b * (margin_stride + 1) + i] = rc - u;
       if (stopped) continue;
       int acc = p_zero ? 1 : (u < rc);
-      if (p_zero && !stopped) status |= ORC_ROW_P_ZERO;
+      if (p_zero) p_zero_seen = 1;
       if (acc) {
         ot[i] = d;
         a = i + 1;
@@ -452,6 +469,25 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
         stopped = 1;
       }
     }
+    if (early_exit && !status && a == npos &&
+        orc_row_bad(vb + (int64_t)(pb ? pb[npos] : npos) * V, V))
+      status |= ORC_ROW_NAN; /* early exit: the bonus row, reached */
+    if (status) {
+      /* a fault: nothing is emitted and no probability reported */
+      for (int i = 0; i < out_stride; ++i) ot[i] = -1;
+      for (int i = 0; i < margin_stride; ++i) {
+        if (out_q) out_q[(int64_t)b * margin_stride + i] = NAN;
+        if (out_p) out_p[(int64_t)b * margin_stride + i] = NAN;
+      }
+      if (out_margin)
+        for (int i = 0; i <= margin_stride; ++i)
+          out_margin[(int64_t)b * (margin_stride + 1) + i] = NAN;
+      out_accept[b] = 0;
+      out_status[b] = status;
+      if (out_gap) out_gap[b] = NAN;
+      continue;
+    }
+    if (p_zero_seen) status |= ORC_ROW_P_ZERO;
     /* correction (residual at position a) or bonus (verifier row path[npos]) */
     uint32_t us = u_samp ? u_samp[b]
                          : orc_u24(seed, step, sid, (uint32_t)a, ORC_DRAW_SAMPLE);
@@ -474,6 +510,22 @@ int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
       out_margin[(int64_t)b * (margin_stride + 1) + margin_stride] = gap;
   }
   return 0;
+}
+
+int orc_verify(const float *vlog, int64_t v_bstride, const float *dlog,
+               int64_t d_bstride, int B, int V, float T,
+               const int32_t *path, int path_stride, const int32_t *npos_arr,
+               const int32_t *tok, int tok_stride, uint64_t seed,
+               uint64_t step, const uint32_t *u_acc, int u_acc_stride,
+               const uint32_t *u_samp, const int32_t *seq_ids,
+               int32_t *out_tokens, int out_stride,
+               int32_t *out_accept, double *out_q, double *out_p,
+               double *out_margin, int margin_stride, double *out_gap,
+               uint32_t *out_status) {
+  return orc_verify_ex(vlog, v_bstride, dlog, d_bstride, B, V, T, path, path_stride,
+                       npos_arr, tok, tok_stride, seed, step, u_acc, u_acc_stride, u_samp,
+                       seq_ids, out_tokens, out_stride, out_accept, out_q, out_p,
+                       out_margin, margin_stride, out_gap, out_status, 0);
 }
 
 /* ------------------------------------------------------------------------
