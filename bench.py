@@ -67,6 +67,9 @@ def parse():
                     help="time the tree-masked verifier attention (one layer) instead")
     ap.add_argument("--greedy", action="store_true",
                     help="temperature 0: greedy verification (verifier rows only, no sampling)")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="chain configs: sv_verify_chain_early_exit (rows after a sequence's "
+                         "first rejection are not read once it is known)")
     ap.add_argument("--batch", type=int, default=0,
                     help="per-GPU batch override (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -207,6 +210,7 @@ def measured_peaks():
 # these files are unchanged)
 KERNEL_SOURCES = {
     "row_stats": ("common.cuh", "rowstat.cuh", "verify.cu"),
+    "row_stats_ee": ("common.cuh", "rowstat.cuh", "verify.cu"),
     "sampler_kv": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
     "launches": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
     "tree_attention": ("common.cuh", "tree_attn.cu"),
@@ -240,6 +244,7 @@ class Workload:
         from speculative_decoding_verification_vocab_gb300 import synth
         self.cfg = cfg
         self.greedy = False
+        self.early = False
         self.rounds = []
         self.tree = cfg.kind.startswith("tree")
         for r in range(pool):
@@ -269,11 +274,17 @@ class Workload:
     def rows_per_step(self):
         return self.B * self.T
 
-    def stats_bytes(self, r):
-        """Logit bytes the row pass reads: verifier and draft rows along the
-        path (2D+1 per sequence), or the verifier rows alone when greedy."""
+    def stats_bytes(self, r, acc=None):
+        """Logit bytes the row pass must read: verifier and draft rows along
+        the path (2D+1 per sequence), the verifier rows alone when greedy, or
+        with early exit the rows the walk reaches given the accept lengths
+        `acc`: 2(a+1) after a rejection at a < D, 2D+1 on full acceptance."""
         d = self.rounds[r]["depth"]
-        rows = d + 1 if self.greedy else 2 * d + 1
+        if self.early and acc is not None:
+            a = np.asarray(acc, np.int64)
+            rows = np.where(a < d, 2 * (a + 1), 2 * d + 1)
+        else:
+            rows = d + 1 if self.greedy else 2 * d + 1
         return int((rows * self.V * self.esize).sum())
 
 
@@ -296,9 +307,10 @@ def run_round(sv, wl, cfg, maxd, src, out, i, seed, step_no, ws, stream, side, e
         sv.sv_kv_compact(wl.kv, wl.kv, wl.kv_base, wl.kv_base, out["path"][i], out["acc"][i], 1,
                          out["kv"][i], side)
     else:
-        sv.sv_verify_chain(src["vq"], src["dp"], src["d"], cfg.temperature, seed, step_no,
-                           out["tok"][i], out["acc"][i], None, None, None, out["st"][i], ws,
-                           stream, accept_event=ev_acc)
+        verify = sv.sv_verify_chain_early_exit if wl.early else sv.sv_verify_chain
+        verify(src["vq"], src["dp"], src["d"], cfg.temperature, seed, step_no,
+               out["tok"][i], out["acc"][i], None, None, None, out["st"][i], ws,
+               stream, accept_event=ev_acc)
         side.wait_event(ev_acc)
         # chain rollback: the accepted drafts' rows are already in place;
         # only the logical length moves (rows NULL = identity)
@@ -328,6 +340,10 @@ def run_ours(args):
     if args.greedy:  # then verified at T = 0
         cfg = dataclasses.replace(cfg, temperature=0.0)
         wl.greedy = True
+    if args.early_exit:
+        if wl.tree or wl.greedy:
+            raise SystemExit("--early-exit applies to chain configs at T > 0")
+        wl.early = True
     K, W = args.steps, args.warmup
     T, V = wl.T, wl.V
     maxd = cfg.depth if wl.tree else cfg.N
@@ -395,7 +411,7 @@ def run_ours(args):
     depth_used = np.stack([wl.rounds[k % args.pool]["depth"] for k in range(K)])
     alpha_hat = float(acc.sum() / max(1, np.minimum(acc + 1, depth_used).sum()))
     # algorithmic bytes
-    stats_bytes = sum(wl.stats_bytes(k % args.pool) for k in range(K))
+    stats_bytes = sum(wl.stats_bytes(k % args.pool, acc[k]) for k in range(K))
     kv_moved = 0
     if wl.tree:
         for k in range(K):
@@ -410,7 +426,8 @@ def run_ours(args):
     total_tokens = sum_over_ranks(tokens, world)
 
     peak, peak_kind = measured_peaks()
-    rs_name = "row_argmax" if cfg.temperature == 0.0 else "row_stats"
+    rs_name = ("row_argmax" if cfg.temperature == 0.0 else
+               "row_stats_ee" if wl.early else "row_stats")
     rs_launches, rs_ms = trace.get(rs_name, (0, 0.0))
     rs_bytes_per_launch = stats_bytes / K
     rs_avg_ms = rs_ms / max(rs_launches, 1)
@@ -426,7 +443,8 @@ def run_ours(args):
         "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype.__repr__().endswith("bfloat16") else "f32",
         "data": "synthetic",
-        "config": {"workload": f"config {cfg.index}: {cfg.name}" + (" (greedy, T=0)" if wl.greedy else ""), "B_per_gpu": B, "T": T, "V": V,
+        "config": {"workload": f"config {cfg.index}: {cfg.name}" + (" (greedy, T=0)" if wl.greedy else "")
+                   + (" (early exit)" if wl.early else ""), "B_per_gpu": B, "T": T, "V": V,
                    "max_depth": maxd, "logits": str(cfg.dtype).replace("torch.", ""),
                    "kv": f"{kvb.L} layers x {kvb.H} kv heads x {kvb.D}, bf16",
                    "pool_rounds": args.pool,
@@ -517,7 +535,7 @@ def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):
     # host bytes the kernels read: the stats rows (copied to the device as
     # they are read; the accept walk and the sampler use the copies) and the
     # tree arrays
-    h2d = (wl.stats_bytes(0)
+    h2d = (wl.stats_bytes(0, hout["acc"].numpy() if wl.early else None)
            + sum(host[k].numel() * host[k].element_size() for k in names if k not in ("vq", "dp")))
     in_bytes = sum(h.numel() * h.element_size() for h in host.values())
 
@@ -559,7 +577,7 @@ def _rows_for_oracle(rd, ids, tree, maxd):
     return vq, dp
 
 
-def _oracle_round(cfg, rd, ids, step, kv=None):
+def _oracle_round(cfg, rd, ids, step, kv=None, early=False):
     """One round of the oracle on the sequences `ids` of a pooled round: the
     tree (or chain) verify and, for trees, the in-place KV compaction of the
     sampled sequences' window.  Returns (rows covered, seconds in the oracle)."""
@@ -585,7 +603,8 @@ def _oracle_round(cfg, rd, ids, step, kv=None):
     else:
         d = rd["d"][tid].cpu().numpy()
         t0 = time.perf_counter()
-        oracle.verify_chain(vq, dp, d, T=cfg.temperature, seed=1234, step=step, seq_ids=ids)
+        oracle.verify_chain(vq, dp, d, T=cfg.temperature, seed=1234, step=step, seq_ids=ids,
+                            early_exit=early)
     return len(ids) * vq.shape[1], time.perf_counter() - t0
 
 
@@ -607,7 +626,7 @@ def cpu_baseline(args, wl, cfg, budget_s=10.0, cap_s=30.0):
         rd = wl.rounds[groups % len(wl.rounds)]
         start = (groups // len(wl.rounds)) * k % wl.B
         ids = np.sort((start + np.arange(k)) % wl.B)
-        r, t = _oracle_round(cfg, rd, ids, groups, kv)
+        r, t = _oracle_round(cfg, rd, ids, groups, kv, early=wl.early)
         rows += r
         secs += t
         groups += 1

@@ -138,6 +138,38 @@ sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
                           void *stream, void *accept_event);
 
 /* ---------------------------------------------------------------------------
+ * sv_verify_chain_early_exit -- sv_verify_chain reading only the rows the walk
+ * reaches.  [Lesson] Passo 3 and [Blog] section 4 spec_decode: the walk ends
+ * at the first rejection, so the rows after it are never needed.
+ *
+ * Same arguments, workspace sizes, outputs and accepted / emitted tokens as
+ * sv_verify_chain, with these differences:
+ *   - temperature must be > 0 (SV_ERR_UNSUPPORTED otherwise: greedy
+ *     verification already reads only the verifier rows);
+ *   - rows are scheduled position by position; once a sequence's position i
+ *     has been judged a rejection (or a fault), the rows of its later
+ *     positions that have not been scheduled yet are not read.  How many rows
+ *     are skipped depends on scheduling, never the results;
+ *   - faults follow the walk: at the first position whose verifier or draft
+ *     row has no finite positive softmax sum, or whose token is outside
+ *     [0, V), the sequence faults with the bits found there (accept_len 0,
+ *     tokens -1); a bad row or token after the first rejection is not seen.
+ *     The bonus row faults the sequence only when every position passes;
+ *   - out_q_prob, out_p_prob and out_margin are NaN after the first
+ *     rejecting position.
+ * The workspace may be that of sv_verify_chain_workspace or
+ * sv_verify_chain_workspace_host for the same B, N, V.
+ * --------------------------------------------------------------------------- */
+sv_status sv_verify_chain_early_exit(const void *vlogits, const void *dlogits, sv_dtype dt,
+                                     const int32_t *draft_tokens, int B, int N, int V,
+                                     float temperature, uint64_t seed, uint64_t step,
+                                     int32_t *out_tokens, int32_t *out_accept_len,
+                                     float *out_q_prob, float *out_p_prob,
+                                     float *out_margin, uint32_t *out_status,
+                                     void *workspace, size_t workspace_bytes,
+                                     void *stream, void *accept_event);
+
+/* ---------------------------------------------------------------------------
  * sv_verify_tree -- verify a flattened draft tree per sequence.
  * [Blog] section 3 "为什么要树，以及树怎么一次验完" (flattened tree verified in
  * one pass), section 4 eagle_round (walk along best_child with the same

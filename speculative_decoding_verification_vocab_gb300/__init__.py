@@ -24,6 +24,7 @@ SV_ROW_BAD_BASE, SV_ROW_TIMEOUT = 32, 64
 SV_MAX_VOCAB, SV_MAX_POSITIONS, SV_MAX_TREE_NODES = 1 << 22, 1024, 1024
 
 EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_verify_chain",
+           "sv_verify_chain_early_exit",
            "sv_verify_chain_noalloc", "sv_verify_tree_workspace_host",
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
            "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_tree_attention", "sv_last_error",
@@ -59,6 +60,8 @@ def load_library(path: str = LIB_PATH):
     L.sv_verify_chain.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
                                   vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     L.sv_verify_chain.restype = i32
+    L.sv_verify_chain_early_exit.argtypes = L.sv_verify_chain.argtypes
+    L.sv_verify_chain_early_exit.restype = i32
     L.sv_verify_chain_noalloc_max_bytes.argtypes = []
     L.sv_verify_chain_noalloc_max_bytes.restype = sz
     L.sv_verify_chain_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, f32, u64, u64,
@@ -155,6 +158,19 @@ def sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out
     B, R, V = vlogits.shape
     N = R - 1
     return _check(load_library().sv_verify_chain(
+        _p(vlogits), _p(dlogits) if N > 0 else None, _dtype(vlogits),
+        _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
+        _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
+        _p(out_status), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), _event(accept_event)))
+
+
+def sv_verify_chain_early_exit(vlogits, dlogits, draft_tokens, temperature, seed, step,
+                               out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,
+                               out_status, workspace, stream=None, accept_event=None):
+    B, R, V = vlogits.shape
+    N = R - 1
+    return _check(load_library().sv_verify_chain_early_exit(
         _p(vlogits), _p(dlogits) if N > 0 else None, _dtype(vlogits),
         _p(draft_tokens) if N > 0 else None, B, N, V, float(temperature), int(seed), int(step),
         _p(out_tokens), _p(out_accept_len), _p(out_q_prob), _p(out_p_prob), _p(out_margin),
@@ -286,8 +302,9 @@ def _out_dev(t):
 
 
 def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0,
-                 workspace=None, stream=None, probs=True, accept_event=None):
-    """Allocate outputs and run sv_verify_chain.  Returns a dict of tensors."""
+                 workspace=None, stream=None, probs=True, accept_event=None, early_exit=False):
+    """Allocate outputs and run sv_verify_chain (sv_verify_chain_early_exit
+    with ``early_exit``).  Returns a dict of tensors."""
     B, R, V = vlogits.shape
     N = R - 1
     dev = _out_dev(vlogits)
@@ -301,9 +318,10 @@ def verify_chain(vlogits, dlogits, draft_tokens, temperature=1.0, seed=0, step=0
     if workspace is None:
         workspace = _ws(sv_verify_chain_workspace(B, N, V) if vlogits.is_cuda
                         else sv_verify_chain_workspace_host(B, N, V, vlogits.dtype), dev)
-    sv_verify_chain(vlogits, dlogits, draft_tokens, temperature, seed, step, out["tokens"],
-                    out["accept_len"], out["q_prob"], out["p_prob"], out["margin"],
-                    out["status"], workspace, stream, accept_event)
+    fn = sv_verify_chain_early_exit if early_exit else sv_verify_chain
+    fn(vlogits, dlogits, draft_tokens, temperature, seed, step, out["tokens"],
+       out["accept_len"], out["q_prob"], out["p_prob"], out["margin"],
+       out["status"], workspace, stream, accept_event)
     return out
 
 

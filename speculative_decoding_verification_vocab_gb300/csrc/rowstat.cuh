@@ -28,8 +28,8 @@ __device__ __forceinline__ float stat_ref(const StatState &st) {
 
 __device__ __forceinline__ void stat_raise(StatState &st, float cm, float k) {
   // cm > st.mx: move the reference up and rescale the sums
-  const float nk = cm * k;
-  const float f = (st.mx == -INFINITY) ? 0.0f : ex2_approx(st.mk - nk);
+  const float nk = __fmul_rn(cm, k);
+  const float f = (st.mx == -INFINITY) ? 0.0f : ex2_approx(__fsub_rn(st.mk, nk));
   const unsigned long long f2 = f2_pack(f, f);
   st.s01 = f2_mul(st.s01, f2);
   st.s23 = f2_mul(st.s23, f2);
@@ -127,7 +127,9 @@ __device__ __forceinline__ void stat_word<float>(uint4 v, StatState &st, float k
 }
 
 // Merge (mx2, mk2, s2) into (mx, mk, s): log2-domain references, -inf refs
-// contribute nothing, NaN sums stay NaN.
+// contribute nothing, NaN sums stay NaN.  The rescaled sum is one explicit
+// multiply and one fused multiply-add, so every kernel that inlines this
+// merge rounds it the same way (no contraction choice left to the compiler).
 __device__ __forceinline__ void st_combine(float &mx, float &mk, float &s, float mx2, float mk2,
                                            float s2) {
   const float a = (mx == -INFINITY) ? -INFINITY : mk;
@@ -136,7 +138,7 @@ __device__ __forceinline__ void st_combine(float &mx, float &mk, float &s, float
   if (M == -INFINITY) {
     s = s + s2;
   } else {
-    s = s * ex2_approx(a - M) + s2 * ex2_approx(b - M);
+    s = __fmaf_rn(s, ex2_approx(a - M), __fmul_rn(s2, ex2_approx(b - M)));
   }
   mx = fmaxf(mx, mx2);
   mk = M;
@@ -149,10 +151,10 @@ __device__ __forceinline__ void warp_stat_combine(float &mx, float &mk, float &s
   float M = a;
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (M != -INFINITY) s = s * ex2_approx(a - M);
+  if (M != -INFINITY) s = __fmul_rn(s, ex2_approx(a - M));
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    s += __shfl_xor_sync(0xffffffffu, s, o);
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   mk = M;

@@ -47,6 +47,7 @@ struct Task {
 struct Layout {
   int maxpos, P, G, CS;
   size_t ctr, rowlist, partial, task, norm, mass, run, done, inv, path, npos, tok, tstat;
+  size_t ee;     // early exit (chain): [B][maxpos] position counts, then [B] stop
   size_t end;    // end of the regions (256-aligned); an optional row copy follows
   size_t total;  // bytes to request: the regions plus base-pointer alignment
 };
@@ -158,11 +159,10 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
   return si;
 }
 
-// statistics of segment blockIdx.y of listed row row_i, by the whole CTA
+// statistics of segment seg of listed row row_i, by the whole CTA
 template <typename E, bool kCopy>
 __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_t *rowlist,
-                                             int row_i, float4 *partial) {
-  const int seg = blockIdx.y;
+                                             int row_i, int seg, float4 *partial) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg);
   const E *row = (const E *)si.row;
@@ -246,7 +246,7 @@ row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
   // slots and a CTA takes a second listed row when the paths are deep
   const int nrows = rowlist ? *rowcount : (int)gridDim.x;
   for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
-    stat_segment<E, kCopy>(r, G, rowlist, row_i, partial);
+    stat_segment<E, kCopy>(r, G, rowlist, row_i, blockIdx.y, partial);
 }
 
 Layout plan(int B, int maxpos, int V, bool tree) {
@@ -271,6 +271,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   L.run = take(sizeof(unsigned long long) * (size_t)B * L.CS * kSpThreads);
   L.done = take(sizeof(unsigned) * 2 * (size_t)B);
   L.inv = take(sizeof(float2) * (size_t)B);
+  L.ee = take(sizeof(int) * (size_t)B * (maxpos + 1));
   if (tree) {
     L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
     L.npos = take(sizeof(int32_t) * (size_t)B);
@@ -296,19 +297,75 @@ struct DecideOut {
 };
 
 // Merge the G segment partials of one row: raw max mx, log2 reference mk and
-// the sum s = sum_v exp2(fma(x_v, k, -mk)).
+// the sum s = sum_v exp2(fma(x_v, k, -mk)).  kCg: the partials were written by
+// other CTAs of the running kernel (read through L2).
+template <bool kCg = false>
 __device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx, float &mk,
                                            float &s) {
   mx = -INFINITY;
   mk = 0.0f;
   s = 0.0f;
   for (int g = 0; g < G; ++g) {
-    const float4 v = part[g];
+    const float4 v = kCg ? __ldcg(part + g) : part[g];
     st_combine(mx, mk, s, v.x, v.y, v.z);
   }
 }
 
-template <typename E>
+// One position of the walk from the merged statistics of its verifier and
+// draft rows ([Lesson] Passo 1: accept iff u < min(1, q(d)/p(d)), p(d) = 0
+// accepted outright): q(d), p(d), the clipped ratio, the uniform, and the
+// position's faults (a row without a finite positive sum, a token outside the
+// vocabulary).  The accept walk and the early-exit hint both call it on the
+// same partials, so they take the same decision.
+struct Judged {
+  float mxq, mxp;    // raw maxima of the verifier / draft row
+  float qd, pd, rc;  // q(d), p(d), min(1, q(d)/p(d))
+  uint32_t u24;      // the accept uniform
+  uint32_t bad;      // SV_ROW_NAN / SV_ROW_BAD_TOKEN found at this position
+  bool accept, p_zero;
+};
+template <typename E, bool kCg>
+__device__ __forceinline__ Judged judge_position(const Round &r, int G, const float4 *pb, int b,
+                                                 int i, int d, const E *vrow, const E *drow,
+                                                 uint64_t seed, uint64_t step) {
+  Judged J;
+  float mkq, sq, mkp, sp;
+  merge_slot<kCg>(pb + (size_t)i * G, G, J.mxq, mkq, sq);
+  merge_slot<kCg>(pb + (size_t)(r.maxpos + 1 + i) * G, G, J.mxp, mkp, sp);
+  J.bad = (!(sq > 0.0f) || !(sp > 0.0f)) ? SV_ROW_NAN : 0u;
+  J.qd = J.pd = J.rc = NAN;
+  J.u24 = 0u;
+  J.accept = J.p_zero = false;
+  if (d < 0 || d >= r.V) {
+    J.bad |= SV_ROW_BAD_TOKEN;
+    return J;
+  }
+  const float k = r.k;
+  const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
+  // log2 q(d) + log2 sq and log2 p(d) + log2 sp, against the row references
+  const float lq = fmaf(xq, k, -mkq), lp = fmaf(xp, k, -mkp);
+  J.qd = exp2f(lq) / sq;
+  J.pd = exp2f(lp) / sp;
+  J.p_zero = (xp == -INFINITY);
+  float ratio;
+  if (J.p_zero)
+    ratio = INFINITY;
+  else if (xq == -INFINITY)
+    ratio = 0.0f;
+  else
+    ratio = exp2f((lq - lp) + (log2f(sp) - log2f(sq)));
+  J.rc = fminf(ratio, 1.0f);
+  J.u24 = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawAccept);
+  const float u = (float)J.u24 * 0x1p-24f;
+  J.accept = J.p_zero || (u < J.rc);
+  return J;
+}
+
+// kEarly: the early-exit reading -- only the rows the walk reaches count: a
+// position's faults stop the walk there (and fault the sequence), the bonus
+// row faults only when every position passes, and q(d), p(d) and the margin
+// after the first rejection are NaN (those rows may never have been read).
+template <typename E, bool kEarly>
 __global__ void __launch_bounds__(kDecideWarps * 32)
 decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
               uint64_t step, DecideOut o, Task *__restrict__ tasks,
@@ -321,7 +378,6 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   const int npos = round_npos(r, b);
   const uint32_t tree_bad = r.tstat ? r.tstat[b] : 0u;
   const float4 *pb = partial + (size_t)b * r.P * G;
-  const float k = r.k;
   // per position: raw max of the verifier / draft row and the sample uniform,
   // kept for the task so that lane 0 needs no further global reads
   extern __shared__ float dsm[];
@@ -330,6 +386,8 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   uint32_t *usm = (uint32_t *)(mxd + (r.maxpos + 1));
 
   uint32_t bad = 0, pzero_bits = 0, acc_bits = 0;
+  // early exit: per chunk, this lane's position faults (row / token)
+  uint32_t nan_bits = 0, tokbad_bits = 0;
   // bonus row (verifier row of position npos) is checked by lane 0
   if (lane == 0 && !tree_bad) {
     float mx, mk, s;
@@ -338,50 +396,36 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     mxv[npos] = mx;
     usm[npos] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)npos, kDrawSample);
   }
+  const uint32_t bonus_bad = kEarly ? __shfl_sync(FULL, bad, 0) : 0u;
+  if (kEarly) bad = 0;
   const int nchunks = (npos + 31) / 32;
   for (int c = 0; c < nchunks && !tree_bad; ++c) {
     const int i = c * 32 + lane;
     if (i >= npos) break;
     const int d = r.tok[(size_t)b * r.tok_stride + i];  // issued first: x_d depends on it
-    float mxq, mkq, sq, mxp, mkp, sp;
-    merge_slot(pb + (size_t)i * G, G, mxq, mkq, sq);
-    merge_slot(pb + (size_t)(r.maxpos + 1 + i) * G, G, mxp, mkp, sp);
-    mxv[i] = mxq;
-    mxd[i] = mxp;
-    usm[i] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawSample);
-    if (!(sq > 0.0f) || !(sp > 0.0f)) bad |= SV_ROW_NAN;
-    if (d < 0 || d >= r.V) {
-      bad |= SV_ROW_BAD_TOKEN;
-      continue;
-    }
     const E *vrow = used_row<E>(r, b, i, src_row<E>(r, b, i));
     const E *drow = used_row<E>(r, b, r.maxpos + 1 + i, src_row<E>(r, b, r.maxpos + 1 + i));
-    const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
-    // log2 q(d) + log2 sq and log2 p(d) + log2 sp, against the row references
-    const float lq = fmaf(xq, k, -mkq), lp = fmaf(xp, k, -mkp);
-    const float qd = exp2f(lq) / sq, pd = exp2f(lp) / sp;
-    const bool p_zero = (xp == -INFINITY);
-    float ratio;
-    if (p_zero)
-      ratio = INFINITY;
-    else if (xq == -INFINITY)
-      ratio = 0.0f;
-    else
-      ratio = exp2f((lq - lp) + (log2f(sp) - log2f(sq)));
-    const float rc = fminf(ratio, 1.0f);
-    const uint32_t u24 = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawAccept);
-    const float u = (float)u24 * 0x1p-24f;
-    const bool accept = p_zero || (u < rc);
-    if (accept) acc_bits |= 1u << c;
-    if (p_zero) pzero_bits |= 1u << c;
-    if (o.q_prob) o.q_prob[(size_t)b * r.maxpos + i] = qd;
-    if (o.p_prob) o.p_prob[(size_t)b * r.maxpos + i] = pd;
-    if (o.margin) o.margin[(size_t)b * (r.maxpos + 1) + i] = rc - u;
+    const Judged J = judge_position<E, false>(r, G, pb, b, i, d, vrow, drow, seed, step);
+    mxv[i] = J.mxq;
+    mxd[i] = J.mxp;
+    usm[i] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)i, kDrawSample);
+    if (kEarly) {
+      if (J.bad & SV_ROW_NAN) nan_bits |= 1u << c;
+      if (J.bad & SV_ROW_BAD_TOKEN) tokbad_bits |= 1u << c;
+    } else {
+      bad |= J.bad;
+    }
+    if (J.bad & SV_ROW_BAD_TOKEN) continue;
+    if (J.accept && !(kEarly && J.bad)) acc_bits |= 1u << c;
+    if (J.p_zero) pzero_bits |= 1u << c;
+    if (o.q_prob) o.q_prob[(size_t)b * r.maxpos + i] = J.qd;
+    if (o.p_prob) o.p_prob[(size_t)b * r.maxpos + i] = J.pd;
+    if (o.margin) o.margin[(size_t)b * (r.maxpos + 1) + i] = J.rc - (float)J.u24 * 0x1p-24f;
   }
   bad = __reduce_or_sync(FULL, bad);
   if (tree_bad) bad = SV_ROW_BAD_TREE;
 
-  // first rejection
+  // first rejection (early exit: first rejection or fault)
   int a = npos;
   uint32_t pz = 0;
   for (int c = 0; c < nchunks; ++c) {
@@ -392,10 +436,17 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
       a = c * 32 + __ffs(rej) - 1;
       const unsigned below = (a - c * 32) >= 32 ? FULL : ((1u << (a - c * 32)) - 1u);
       pz |= pzc & below;
+      if (kEarly && !tree_bad) {
+        const int la = a - c * 32;
+        const uint32_t nb = __shfl_sync(FULL, nan_bits >> c, la) & 1u;
+        const uint32_t tb = __shfl_sync(FULL, tokbad_bits >> c, la) & 1u;
+        bad = (nb ? SV_ROW_NAN : 0u) | (tb ? SV_ROW_BAD_TOKEN : 0u);
+      }
       break;
     }
     pz |= pzc;
   }
+  if (kEarly && !tree_bad && a == npos) bad = bonus_bad;
   if (bad) a = 0;
 
   // outputs
@@ -405,7 +456,7 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     if (!bad && i < a) t = r.tok[(size_t)b * r.tok_stride + i];
     o.tokens[(size_t)b * W + i] = t;
     if (o.path_out) o.path_out[(size_t)b * W + i] = (i == 0) ? 0 : ((!bad && i <= a) ? round_node(r, b, i) : -1);
-    if (i >= npos || bad) {
+    if (i >= npos || bad || (kEarly && i > a)) {
       if (i < r.maxpos) {
         if (o.q_prob) o.q_prob[(size_t)b * r.maxpos + i] = NAN;
         if (o.p_prob) o.p_prob[(size_t)b * r.maxpos + i] = NAN;
@@ -432,6 +483,67 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     done[b] = 0u;        // the sampler's per-sequence completion counts:
     done[r.B + b] = 0u;  // slice CTAs of sample_mass, of sample_norm
   }
+}
+
+// ---------------------------------------------------------------------------
+// row_stats in early-exit order (chain, T > 0): the walk ends at the first
+// rejection ([Lesson] Passo 3; [Blog] section 4 spec_decode), so rows after it
+// need not be read.  One CTA per (position i, sequence b, row, segment), in
+// position-major order: the rows of position i of a sequence are scheduled a
+// whole position-wave (2 B G CTAs) after those of position i - 1, by which
+// time that position has usually been judged.  The CTA completing the 2G
+// segments of position i (a per-position count; nothing waits on it) judges
+// it with the accept walk's own function on the same partials and, on a
+// rejection or a fault, lowers stop[b] to i.  A CTA that finds stop[b] < i
+// reads nothing and writes a NaN partial, so a walk that ever reached such a
+// row would fault instead of using stale statistics.  The bonus row
+// (position N) is read unless the sequence stopped before it.
+constexpr unsigned kEeInit = 0x7F7F7F7Fu;  // counts and stop[] start here (byte fill)
+
+template <typename E, bool kCopy>
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+row_stats_ee_kernel(Round r, int G, float4 *__restrict__ partial, unsigned *__restrict__ count,
+                    int *__restrict__ stop, uint64_t seed, uint64_t step) {
+  grid_dep_sync();
+  const int N = r.maxpos;
+  const long long wave = 2LL * r.B * G;  // CTAs per drafted position
+  const long long x = blockIdx.x;
+  int i, b, j, seg;
+  if (x < wave * N) {
+    i = (int)(x / wave);
+    const int rem = (int)(x - (long long)i * wave);
+    b = rem / (2 * G);
+    const int k = rem - b * 2 * G;
+    seg = k < G ? k : k - G;
+    j = k < G ? i : N + 1 + i;
+  } else {
+    i = N;
+    const int rem = (int)(x - wave * N);
+    b = rem / G;
+    seg = rem - b * G;
+    j = N;
+  }
+  __shared__ int skip;
+  if (threadIdx.x == 0) skip = *(volatile int *)(stop + b) < i;
+  __syncthreads();
+  if (skip) {
+    if (threadIdx.x == 0)
+      partial[((size_t)b * r.P + j) * G + seg] = make_float4(NAN, NAN, NAN, NAN);
+    return;
+  }
+  stat_segment<E, kCopy>(r, G, nullptr, b * r.P + j, seg, partial);
+  // thread 0 wrote this segment's partial; the position's last CTA judges it
+  if (i == N || threadIdx.x != 0) return;
+  __threadfence();
+  if (atomicAdd(count + (size_t)b * N + i, 1u) != kEeInit + 2u * (unsigned)G - 1u) return;
+  __threadfence();
+  const int d = r.tok[(size_t)b * r.tok_stride + i];
+  // x_d from the source rows: a host-resident row's device copy is being
+  // written by this kernel and is not read through the read-only path here
+  const Judged J = judge_position<E, true>(r, G, partial + (size_t)b * r.P * G, b, i, d,
+                                           src_row<E>(r, b, i), src_row<E>(r, b, N + 1 + i),
+                                           seed, step);
+  if (J.bad || !J.accept) atomicMin(stop + b, i);
 }
 
 // ---------------------------------------------------------------------------
@@ -1188,13 +1300,28 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
 // ---------------------------------------------------------------------------
 template <typename E>
 sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, uint64_t step,
-                     const DecideOut &o, cudaStream_t st, cudaEvent_t accept_event) {
+                     const DecideOut &o, cudaStream_t st, cudaEvent_t accept_event,
+                     bool early = false) {
   float4 *partial = (float4 *)(ws + L.partial);
   Task *tasks = (Task *)(ws + L.task);
   sv_status s;
   // segments per row for this element type (the workspace holds L.G >= G)
   const int G = (r.V + seg_elems<E>() - 1) / seg_elems<E>();
-  {
+  if (early) {
+    // per-position counts [B][N] and stop [B], byte-filled to kEeInit
+    unsigned *count = (unsigned *)(ws + L.ee);
+    int *stop = (int *)(count + (size_t)r.B * r.maxpos);
+    if (cudaMemsetAsync(count, 0x7F, sizeof(int) * (size_t)r.B * (r.maxpos + 1), st) !=
+        cudaSuccess)
+      return set_error(SV_ERR_CUDA, "row_stats_ee: count reset");
+    const long long nblk = (long long)r.B * G * r.P;
+    LaunchScope ls("row_stats_ee", st);
+    s = check_launch("row_stats_ee", launch_pdl(r.copy ? row_stats_ee_kernel<E, true>
+                                                       : row_stats_ee_kernel<E, false>,
+                                                dim3((unsigned)nblk), dim3(kRsThreads), 0, st,
+                                                r, G, partial, count, stop, seed, step));
+    if (s != SV_OK) return s;
+  } else {
     // tree: B * P row slots bound the listed rows; half as many CTAs per
     // segment, each taking a second row when the paths are deep
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
@@ -1210,12 +1337,13 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   {
     // per warp: raw maxima of both rows and the sample uniform per position
     const size_t dsm = (size_t)kDecideWarps * 3 * (r.maxpos + 1) * sizeof(float);
+    auto kern = early ? decide_kernel<E, true> : decide_kernel<E, false>;
     if (dsm > 48 * 1024 &&
-        cudaFuncSetAttribute(decide_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)dsm) != cudaSuccess)
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm) !=
+            cudaSuccess)
       return set_error(SV_ERR_CUDA, "decide: shared memory attribute");
     LaunchScope ls("decide", st);
-    s = check_launch("decide", launch_pdl(decide_kernel<E>,
+    s = check_launch("decide", launch_pdl(kern,
                                           dim3((r.B + kDecideWarps - 1) / kDecideWarps),
                                           dim3(kDecideWarps * 32), dsm, st, r, G, partial, seed,
                                           step, o, tasks, (unsigned *)(ws + L.done)));
@@ -1355,23 +1483,30 @@ extern "C" size_t sv_verify_chain_workspace_host(int B, int N, int V, sv_dtype d
   return L.total + row_copy_bytes(B, L, V, dt);
 }
 
-extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
-                                     const int32_t *draft_tokens, int B, int N, int V,
-                                     float temperature, uint64_t seed, uint64_t step,
-                                     int32_t *out_tokens, int32_t *out_accept_len,
-                                     float *out_q_prob, float *out_p_prob, float *out_margin,
-                                     uint32_t *out_status, void *workspace,
-                                     size_t workspace_bytes, void *stream,
-                                     void *accept_event) {
+namespace sv {
+namespace {
+sv_status verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
+                       const int32_t *draft_tokens, int B, int N, int V, float temperature,
+                       uint64_t seed, uint64_t step, int32_t *out_tokens,
+                       int32_t *out_accept_len, float *out_q_prob, float *out_p_prob,
+                       float *out_margin, uint32_t *out_status, void *workspace,
+                       size_t workspace_bytes, void *stream, void *accept_event, bool early) {
   sv_status s = check_common(vlogits, dt, B, V, temperature, out_tokens, out_accept_len,
                              out_status, workspace);
-  if (s != SV_OK || B == 0) return s;
+  if (s != SV_OK) return s;
+  if (early && temperature == 0.0f)
+    return set_error(SV_ERR_UNSUPPORTED,
+                     "early exit needs temperature > 0 (greedy reads only verifier rows)");
+  if (B == 0) return s;
   if (N < 0) return set_error(SV_ERR_INVALID_ARG, "N must be >= 0 (got %d)", N);
   if (N > SV_MAX_POSITIONS) return set_error(SV_ERR_UNSUPPORTED, "N > %d", SV_MAX_POSITIONS);
   if (N > 0 && (!dlogits || !draft_tokens))
     return set_error(SV_ERR_INVALID_ARG, "dlogits and draft_tokens are required when N > 0");
   const Layout L = plan(B, N, V, false);
   if ((s = check_grid(B, L)) != SV_OK) return s;
+  if (early && (long long)B * L.P * ((V + seg_elems<float>() - 1) / seg_elems<float>()) >
+                   0x7fffffffLL)
+    return set_error(SV_ERR_UNSUPPORTED, "batch too large for early exit: B=%d", B);
   if (workspace_bytes < L.total)
     return set_error(SV_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                      L.total);
@@ -1406,8 +1541,35 @@ extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, s
     return dt == SV_BF16 ? run_verify_greedy<uint16_t>(r, L, ws, o, st, (cudaEvent_t)accept_event)
                          : run_verify_greedy<float>(r, L, ws, o, st, (cudaEvent_t)accept_event);
   }
-  return dt == SV_BF16 ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event)
-                       : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event);
+  return dt == SV_BF16
+             ? run_verify<uint16_t>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event, early)
+             : run_verify<float>(r, L, ws, seed, step, o, st, (cudaEvent_t)accept_event, early);
+}
+}  // namespace
+}  // namespace sv
+
+extern "C" sv_status sv_verify_chain(const void *vlogits, const void *dlogits, sv_dtype dt,
+                                     const int32_t *draft_tokens, int B, int N, int V,
+                                     float temperature, uint64_t seed, uint64_t step,
+                                     int32_t *out_tokens, int32_t *out_accept_len,
+                                     float *out_q_prob, float *out_p_prob, float *out_margin,
+                                     uint32_t *out_status, void *workspace,
+                                     size_t workspace_bytes, void *stream,
+                                     void *accept_event) {
+  return sv::verify_chain(vlogits, dlogits, dt, draft_tokens, B, N, V, temperature, seed, step,
+                          out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,
+                          out_status, workspace, workspace_bytes, stream, accept_event, false);
+}
+
+extern "C" sv_status sv_verify_chain_early_exit(
+    const void *vlogits, const void *dlogits, sv_dtype dt, const int32_t *draft_tokens, int B,
+    int N, int V, float temperature, uint64_t seed, uint64_t step, int32_t *out_tokens,
+    int32_t *out_accept_len, float *out_q_prob, float *out_p_prob, float *out_margin,
+    uint32_t *out_status, void *workspace, size_t workspace_bytes, void *stream,
+    void *accept_event) {
+  return sv::verify_chain(vlogits, dlogits, dt, draft_tokens, B, N, V, temperature, seed, step,
+                          out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,
+                          out_status, workspace, workspace_bytes, stream, accept_event, true);
 }
 
 extern "C" size_t sv_verify_tree_workspace(int B, int T, int max_depth, int V) {
