@@ -299,15 +299,23 @@ struct DecideOut {
 // Merge the G segment partials of one row: raw max mx, log2 reference mk and
 // the sum s = sum_v exp2(fma(x_v, k, -mk)).  kCg: the partials were written by
 // other CTAs of the running kernel (read through L2).
+// The loads of a group of 8 partials are issued together, then merged in
+// segment order (the same order for every G, so the result does not depend on
+// how the loads were grouped).
 template <bool kCg = false>
 __device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx, float &mk,
                                            float &s) {
   mx = -INFINITY;
   mk = 0.0f;
   s = 0.0f;
-  for (int g = 0; g < G; ++g) {
-    const float4 v = kCg ? __ldcg(part + g) : part[g];
-    st_combine(mx, mk, s, v.x, v.y, v.z);
+  for (int g0 = 0; g0 < G; g0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (g0 + g < G) v[g] = kCg ? __ldcg(part + g0 + g) : part[g0 + g];
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (g0 + g < G) st_combine(mx, mk, s, v[g].x, v[g].y, v[g].z);
   }
 }
 
@@ -329,6 +337,10 @@ __device__ __forceinline__ Judged judge_position(const Round &r, int G, const fl
                                                  int i, int d, const E *vrow, const E *drow,
                                                  uint64_t seed, uint64_t step) {
   Judged J;
+  // the two logits at the token first: their loads overlap the merges
+  const bool tok_ok = d >= 0 && d < r.V;
+  const float xq = tok_ok ? load_elem<E>(vrow + d) : 0.0f;
+  const float xp = tok_ok ? load_elem<E>(drow + d) : 0.0f;
   float mkq, sq, mkp, sp;
   merge_slot<kCg>(pb + (size_t)i * G, G, J.mxq, mkq, sq);
   merge_slot<kCg>(pb + (size_t)(r.maxpos + 1 + i) * G, G, J.mxp, mkp, sp);
@@ -336,12 +348,11 @@ __device__ __forceinline__ Judged judge_position(const Round &r, int G, const fl
   J.qd = J.pd = J.rc = NAN;
   J.u24 = 0u;
   J.accept = J.p_zero = false;
-  if (d < 0 || d >= r.V) {
+  if (!tok_ok) {
     J.bad |= SV_ROW_BAD_TOKEN;
     return J;
   }
   const float k = r.k;
-  const float xq = load_elem<E>(vrow + d), xp = load_elem<E>(drow + d);
   // log2 q(d) + log2 sq and log2 p(d) + log2 sp, against the row references
   const float lq = fmaf(xq, k, -mkq), lp = fmaf(xp, k, -mkp);
   J.qd = exp2f(lq) / sq;
@@ -1105,7 +1116,8 @@ __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, con
   const float iq = iv.x, ip = iv.y;
   const unsigned long long *mass = sw.mass + (size_t)b * sw.CS;
   unsigned long long Sw = 0;
-  for (int c = 0; c < sw.CS; ++c) Sw += __ldcg(mass + c);
+  for (int c0 = 0; c0 < sw.CS; c0 += 32)  // one load per lane, then a warp sum
+    Sw += warp_sum_u64(c0 + lane < sw.CS ? __ldcg(mass + c0 + lane) : 0ull);
   // residual mass 0 (q == p to the last bit): fall back to q; its masses are
   // recomputed here (a warp per slice / run), which only this case needs
   const bool use_q = !p.resid || Sw == 0ull;
@@ -1137,9 +1149,38 @@ __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, con
                            base_s);
   const unsigned long long *run = sw.run + ((size_t)b * sw.CS + cs) * kSpThreads;
   const unsigned long long tl = thr - base_s;
-  const int ri = warp_find(kSpThreads, tl,
-                           [&](int th) { return fallback ? run_mass(cs, th) : __ldcg(run + th); },
-                           base_r);
+  int ri;
+  if (fallback) {
+    ri = warp_find(kSpThreads, tl, [&](int th) { return run_mass(cs, th); }, base_r);
+  } else {
+    // the slice's run sums: lane l loads runs [8l, 8l + 8) at once, the warp
+    // finds the lane whose group crosses the threshold, that lane the run
+    constexpr int kPer = kSpThreads / 32;
+    unsigned long long rs[kPer], own = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      rs[k] = __ldcg(run + lane * kPer + k);
+      own += rs[k];
+    }
+    const unsigned long long inc = warp_incl_scan_u64(own);
+    const unsigned hit = __ballot_sync(0xffffffffu, inc > tl);
+    const int lh = hit ? __ffs(hit) - 1 : 31;  // tl < slice mass: some lane crosses
+    // this lane's group: the first run whose running sum crosses tl
+    unsigned long long run_acc = inc - own, base_k = run_acc;
+    int k_hit = kPer - 1;
+    bool found = false;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (!found && run_acc + rs[k] > tl) {
+        found = true;
+        k_hit = k;
+        base_k = run_acc;
+      }
+      run_acc += rs[k];
+    }
+    ri = __shfl_sync(0xffffffffu, lane * kPer + k_hit, lh);
+    base_r = __shfl_sync(0xffffffffu, base_k, lh);
+  }
   // the run's 32 elements, one per lane
   const int v = cs * kSpSlice + kSpRun * ri + lane;
   const unsigned long long w = w_elem<E>(r, p, v, iq, ip, use_q);
@@ -1224,9 +1265,12 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   const int b = blockIdx.x, lane = threadIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
   __shared__ float sc[SV_MAX_TREE_NODES];
+  __shared__ int32_t tk[SV_MAX_TREE_NODES];
+  __shared__ int32_t pn[SV_MAX_POSITIONS + 1];  // the path, written out at the end
   for (int c = lane; c < T; c += 32) {  // one coalesced pass over the tree
     pa[c] = parent[(size_t)b * T + c];
     sc[c] = score[(size_t)b * T + c];
+    tk[c] = token[(size_t)b * T + c];
   }
   __syncwarp();
   bool ok = true;
@@ -1252,7 +1296,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     return;
   }
   int cur = 0, D = 0;
-  if (lane == 0) pth[0] = 0;
+  if (lane == 0) pn[0] = 0;
   while (D < max_depth) {
     bool have = false;
     float bs = 0.0f;
@@ -1280,11 +1324,12 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     if (!have) break;
     ++D;
     cur = bi;
-    if (lane == 0) pth[D] = bi;
+    if (lane == 0) pn[D] = bi;
   }
   __syncwarp();
-  // tested tokens token[n_1..n_D], gathered in parallel
-  for (int i = lane; i < D; i += 32) tok[(size_t)b * tok_stride + i] = token[(size_t)b * T + pth[i + 1]];
+  // the path and its tested tokens token[n_1..n_D], written in parallel
+  for (int i = lane; i <= D; i += 32) pth[i] = pn[i];
+  for (int i = lane; i < D; i += 32) tok[(size_t)b * tok_stride + i] = tk[pn[i + 1]];
   int base = 0;
   if (lane == 0) {
     npos[b] = D;
