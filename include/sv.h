@@ -314,7 +314,8 @@ sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int
 
 /* sv_tree_finalize -- per sequence, the T-slot tree from C candidates
  * (cand_parent: index of the parent candidate, -1 for candidate 0 = the
- * root; cand_token; cand_score; cand_level, all [B][C]).  The kept nodes are
+ * root; cand_token; cand_score; cand_level, all [B][ldc], the first C
+ * columns used; ldc >= C, ldc = C for packed arrays).  The kept nodes are
  * the T first in (score descending, level ascending, index ascending) among
  * the root and the candidates with a token; slots number them in (level
  * ascending, score descending, index ascending).  out_parent [B][T] = slot of
@@ -324,8 +325,32 @@ sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int
  * T <= SV_MAX_TREE_NODES. */
 sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token,
                            const float *cand_score, const int32_t *cand_level, int B,
-                           int C, int T, int32_t *out_parent, int32_t *out_token,
+                           int C, int ldc, int T, int32_t *out_parent, int32_t *out_token,
                            float *out_score, void *stream);
+
+/* sv_tree_level -- one level of a build, with every step in the library's
+ * kernels: sv_tree_expand of the frontier's rows and sv_tree_select of their
+ * children, reading and writing a caller-owned candidate table
+ * cand_parent / cand_token / cand_score / cand_level, all [B][ldc]
+ * (ldc <= 2048), device memory.  Candidate 0 is the root; level l's children
+ * are appended at columns [n0, n0 + F*K).
+ *   level 1: expands the root (F = 1, n0 = 1, dlogits [B][1][V]) and also
+ *            writes candidate 0 (parent -1, token 0, score 1, level 0);
+ *            frontier is output only;
+ *   level l > 1: frontier [B][K] holds the candidate ids of the F <= K rows
+ *            of dlogits [B][F][V] (-1, or an id outside [0, n0): an empty
+ *            entry, which proposes nothing); a row's score is read from
+ *            cand_score.
+ * Each child gets parent = its row's candidate id (-1 for an empty entry),
+ * the token and score of sv_tree_expand, and level = l.  On return (in stream
+ * order) frontier [B][K] holds the ids of the next frontier, the K best
+ * children as sv_tree_select orders them (-1 where there are fewer).  The
+ * caller's next n0 is n0 + F*K; after the last level, sv_tree_finalize with
+ * C = that n0 and the same ldc builds the tree. */
+sv_status sv_tree_level(const void *dlogits, sv_dtype dt, int B, int F, int V,
+                        float temperature, int K, int level, int n0, int ldc,
+                        int32_t *frontier, int32_t *cand_parent, int32_t *cand_token,
+                        float *cand_score, int32_t *cand_level, void *stream);
 
 /* ---------------------------------------------------------------------------
  * sv_tree_attention -- tree-masked verifier attention, one layer.

@@ -29,7 +29,7 @@ EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_ve
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
            "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_tree_attention", "sv_last_error",
            "sv_launch_count", "sv_trace_enable", "sv_trace_collect", "sv_tree_expand",
-           "sv_tree_select", "sv_tree_finalize")
+           "sv_tree_select", "sv_tree_finalize", "sv_tree_level")
 
 
 class SvError(RuntimeError):
@@ -80,8 +80,11 @@ def load_library(path: str = LIB_PATH):
     L.sv_tree_expand.restype = i32
     L.sv_tree_select.argtypes = [vp, vp, i32, i32, i32, vp, vp]
     L.sv_tree_select.restype = i32
-    L.sv_tree_finalize.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
+    L.sv_tree_finalize.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
     L.sv_tree_finalize.restype = i32
+    L.sv_tree_level.argtypes = [vp, i32, i32, i32, i32, f32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                vp, vp]
+    L.sv_tree_level.restype = i32
     L.sv_tree_build_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     L.sv_tree_build_mask.restype = i32
     L.sv_kv_compact.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
@@ -264,10 +267,26 @@ def sv_tree_select(cand_score, cand_token, K, out_index, stream=None):
 
 def sv_tree_finalize(cand_parent, cand_token, cand_score, cand_level, T, out_parent, out_token,
                      out_score, stream=None):
+    """cand_* [B][C] with unit column stride and one common row stride (views
+    of a wider candidate table are passed as they are)."""
     B, Cn = cand_parent.shape
+    ld = cand_parent.stride(0) if B > 1 else Cn
+    for a in (cand_parent, cand_token, cand_score, cand_level):
+        if a.shape != (B, Cn) or (Cn > 1 and a.stride(1) != 1) or (B > 1 and a.stride(0) != ld):
+            raise ValueError("candidate arrays need unit column stride and one row stride")
     return _check(load_library().sv_tree_finalize(
-        _p(cand_parent), _p(cand_token), _p(cand_score), _p(cand_level), B, Cn, int(T),
+        _p(cand_parent), _p(cand_token), _p(cand_score), _p(cand_level), B, Cn, int(ld), int(T),
         _p(out_parent), _p(out_token), _p(out_score), _stream(stream)))
+
+
+def sv_tree_level(dlogits, K, level, n0, frontier, cand_parent, cand_token, cand_score,
+                  cand_level, temperature=1.0, stream=None):
+    """One build level through the candidate table [B][ldc] (see include/sv.h)."""
+    B, F, V = dlogits.shape
+    return _check(load_library().sv_tree_level(
+        _p(dlogits), _dtype(dlogits), B, F, V, float(temperature), int(K), int(level), int(n0),
+        int(cand_parent.shape[1]), _p(frontier), _p(cand_parent), _p(cand_token),
+        _p(cand_score), _p(cand_level), _stream(stream)))
 
 
 def sv_last_error():
@@ -373,44 +392,42 @@ def tree_finalize(cand_parent, cand_token, cand_score, cand_level, T, stream=Non
     return parent, token, score
 
 
+TREE_TABLE_COLUMNS = 2048  # candidate table width (the finalize step's limit)
+
+
 def build_tree(level_rows, K, T, temperature=1.0, stream=None, return_candidates=False):
     """EAGLE-2 dynamic tree from the draft rows of each level.  level_rows(l,
     frontier) -> [B][F][V] draft logits of the frontier's nodes (frontier:
-    [B][F] candidate ids; level 1's frontier is the root).  Every level's
-    expansion and frontier selection and the final pruning run in the
-    library's kernels; this loop only concatenates candidate lists.
-    Returns (parent, token, score) [B][T] for sv_verify_tree."""
+    int32 [B][K] candidate ids, -1 for an empty entry; None at level 1, whose
+    frontier is the root), or None to stop.  Every step -- each level's
+    expansion and frontier selection through one candidate table, and the
+    final pruning -- runs in the library's kernels; this loop allocates the
+    table and tracks where the next level's candidates start.
+    Returns (parent, token, score) [B][T] for sv_verify_tree (and the
+    candidate table's used columns with return_candidates)."""
     frontier = None
-    valid = None  # frontier entries that hold a node (a pick could come up empty)
-    cp, ct, cs, cl = [], [], [], []
-    depth = 0
+    table = None
+    n0, level = 1, 0
     while True:
-        rows = level_rows(depth + 1, frontier)
+        rows = level_rows(level + 1, None if level == 0 else frontier)
         if rows is None:
             break
         B, F, _ = rows.shape
-        dev = rows.device
-        if frontier is None:
-            frontier = torch.zeros(B, 1, dtype=torch.int64, device=dev)
-            cp.append(torch.full((B, 1), -1, dtype=torch.int32, device=dev))
-            ct.append(torch.zeros(B, 1, dtype=torch.int32, device=dev))
-            cs.append(torch.ones(B, 1, dtype=torch.float32, device=dev))
-            cl.append(torch.zeros(B, 1, dtype=torch.int32, device=dev))
-        depth += 1
-        n0 = sum(c.shape[1] for c in ct)
-        fscore = torch.gather(torch.cat(cs, 1), 1, frontier)
-        if valid is not None:  # an empty entry (NaN score) proposes nothing
-            fscore = fscore.masked_fill(~valid, float("nan"))
-        fscore = fscore.contiguous()
-        tok, sc = tree_expand(rows, fscore, K, temperature, stream)
-        cp.append(frontier.repeat_interleave(K, dim=1).to(torch.int32))
-        ct.append(tok.reshape(B, F * K))
-        cs.append(sc.reshape(B, F * K))
-        cl.append(torch.full((B, F * K), depth, dtype=torch.int32, device=dev))
-        sel = tree_select(cs[-1].contiguous(), ct[-1].contiguous(), K, stream).to(torch.int64)
-        valid = sel >= 0
-        frontier = torch.where(valid, sel + n0, torch.zeros_like(sel))
-    cands = tuple(torch.cat(a, 1).contiguous() for a in (cp, ct, cs, cl))
+        if table is None:
+            dev = _out_dev(rows)
+            C = TREE_TABLE_COLUMNS
+            table = (torch.empty(B, C, dtype=torch.int32, device=dev),
+                     torch.empty(B, C, dtype=torch.int32, device=dev),
+                     torch.empty(B, C, dtype=torch.float32, device=dev),
+                     torch.empty(B, C, dtype=torch.int32, device=dev))
+            frontier = torch.empty(B, K, dtype=torch.int32, device=dev)
+        level += 1
+        sv_tree_level(rows, K, level, n0, frontier, *table, temperature=temperature,
+                      stream=stream)
+        n0 += F * K
+    if table is None:
+        raise ValueError("level_rows gave no level")
+    cands = tuple(a[:, :n0] for a in table)
     tree = tree_finalize(*cands, T, stream=stream)
     return (tree, cands) if return_candidates else tree
 

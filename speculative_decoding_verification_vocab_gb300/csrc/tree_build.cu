@@ -14,7 +14,6 @@ namespace {
 
 constexpr int kExThreads = 256;
 constexpr int kExWarps = kExThreads / 32;
-constexpr int kExUnroll = 8;
 constexpr int kMaxK = 16;
 constexpr int kMaxCand = 2048;
 
@@ -172,11 +171,23 @@ __device__ __forceinline__ int warp_seed(WarpTopK &w, const uint4 (&buf)[kRsUnro
   return mine;
 }
 
+// The candidate table of a whole build ([B][ldc] parent / token / score /
+// level, candidate 0 = the root): with it, a level's expansion reads its
+// frontier scores from the table and appends its children at n0, and the
+// selection writes the next frontier's candidate ids -- no step between
+// levels runs outside these kernels.  token == null: the plain arrays.
+struct Table {
+  const int32_t *frontier;  // [B][K] candidate ids of the rows (-1: empty); null: the root
+  int32_t *parent, *token, *level;
+  float *score;
+  int ldc, n0, lvl, F;
+};
+
 template <typename E>
-__global__ void __launch_bounds__(kExThreads, 3)
+__global__ void __launch_bounds__(kExThreads, 4)
 tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
-                   const float *__restrict__ fscore, int K, int32_t *__restrict__ out_tok,
-                   float *__restrict__ out_score) {
+                   const float *__restrict__ fscore_in, int K, int32_t *__restrict__ out_tok,
+                   float *__restrict__ out_score, Table tb) {
   grid_dep_sync();
   const size_t rowi = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -191,7 +202,49 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   const uint4 *body = (const uint4 *)ab;
   const int nv = (int)((ae - ab) / 16);
   const int ntail = (int)((pe - ae) / sizeof(E));
-  // ragged head and tail elements (fewer than 8 each), by warp 0
+  int i = tid;
+  bool seeded = false;
+  constexpr int kStep = kRsUnroll * kExThreads;
+  // warp-uniform trip count (the warp's offers are warp-wide collectives):
+  // i - lane is the warp's first word of the batch.  The warp's last batch
+  // may run past the row's body: those words read as -inf (nothing added to
+  // the sums, never offered)
+  const uint32_t ninf = sizeof(E) == 2 ? 0xFF80FF80u : 0xFF800000u;
+  for (; i - lane < nv; i += kStep) {
+    uint4 buf[kRsUnroll];
+    unsigned inb = 0xffu;  // words of the batch inside the body
+    if ((i - lane) + 31 + (kRsUnroll - 1) * kExThreads < nv) {
+#pragma unroll
+      for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kExThreads);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRsUnroll; ++j) {
+        const bool in = i + j * kExThreads < nv;
+        buf[j] = in ? ld_stream_v4(body + i + j * kExThreads) : make_uint4(ninf, ninf, ninf, ninf);
+        if (!in) inb &= ~(1u << j);
+      }
+    }
+    stat_batch<E>(buf, st, k);
+    int skip = -1;
+    if (!seeded && w.ti == 0x7fffffff) {  // list still empty: seed it from this batch
+      skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
+      seeded = true;
+    }
+    // one gate per batch: the words are looked at only when some lane's
+    // batch maximum reaches the list's K-th value (after the first batches
+    // almost none does)
+    float bm = word_max<E>(buf[0]);
+#pragma unroll
+    for (int j = 1; j < kRsUnroll; ++j) bm = fmaxf(bm, word_max<E>(buf[j]));
+    if (__any_sync(0xffffffffu, bm >= w.tv))
+#pragma unroll
+      for (int j = 0; j < kRsUnroll; ++j)
+        warp_offer_words<E>(w, buf[j], nhead + (i + j * kExThreads) * kPer, (inb >> j) & 1u, K,
+                            skip);
+  }
+  // ragged head and tail elements (fewer than 8 each), by warp 0, offered
+  // after the body so that seeding (which replaces an empty list) cannot
+  // drop them
   if (warp == 0) {
     for (int j = 0; j < nhead + ntail; ++j) {
       const int v = j < nhead ? j : nhead + nv * kPer + (j - nhead);
@@ -200,32 +253,6 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
       if (x == x) warp_offer(w, x, v, K);
     }
   }
-  int i = tid;
-  bool seeded = false;
-  // warp-uniform trip count (the warp's offers are warp-wide collectives):
-  // a batch is taken only when every lane of the warp has its full batch
-  for (; (i - lane) + 31 + (kRsUnroll - 1) * kExThreads < nv; i += kRsUnroll * kExThreads) {
-    uint4 buf[kRsUnroll];
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kExThreads);
-    stat_batch<E>(buf, st, k);
-    int skip = -1;
-    if (!seeded && w.ti == 0x7fffffff) {  // list still empty: seed it from this batch
-      skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
-      seeded = true;
-    }
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j)
-      warp_offer_words<E>(w, buf[j], nhead + (i + j * kExThreads) * kPer, true, K, skip);
-  }
-  // the remainder: words are loaded warp-uniformly so every lane joins the ballots
-  for (int i0 = i - lane; i0 < nv; i0 += kExThreads) {
-    const int ii = i0 + lane;
-    const bool in = ii < nv;
-    const uint4 wd = in ? ld_stream_v4(body + ii) : make_uint4(0u, 0u, 0u, 0u);
-    if (in) stat_word<E>(wd, st, k);
-    warp_offer_words<E>(w, wd, nhead + ii * kPer, in, K);
-  }
   // the row's statistics, as the verify step's row pass combines them
   float a0, a1, a2, a3;
   f2_unpack(st.s01, a0, a1);
@@ -233,37 +260,80 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   float mx = st.mx, mk = st.mk, ssum = (a0 + a1) + (a2 + a3);
   warp_stat_combine(mx, mk, ssum);
   __shared__ float4 s_red[kExWarps];
-  __shared__ float s_tv[kExWarps][kMaxK];
-  __shared__ int s_ti[kExWarps][kMaxK];
+  __shared__ float s_tv[kExWarps * kMaxK];
+  __shared__ int s_ti[kExWarps * kMaxK];
+  __shared__ int s_pick[kMaxK];
   if (lane == 0) s_red[warp] = make_float4(mx, mk, ssum, 0.0f);
   if (lane < K) {
-    s_tv[warp][lane] = w.v;
-    s_ti[warp][lane] = w.i;
+    s_tv[warp * K + lane] = w.v;
+    s_ti[warp * K + lane] = w.i;
+  }
+  if (tid < K) s_pick[tid] = -1;
+  __syncthreads();
+  // merge: every listed entry's rank among the eight warp lists' entries
+  // (value descending, token ascending; the warps cover disjoint tokens);
+  // rank r < K is pick r
+  if (tid < kExWarps * K) {
+    const float x = s_tv[tid];
+    const int id = s_ti[tid];
+    if (x == x && id != 0x7fffffff) {
+      int rank = 0;
+      for (int e = 0; e < kExWarps * K; ++e) {
+        const float y = s_tv[e];
+        const int iy = s_ti[e];
+        rank += (y == y && iy != 0x7fffffff && tk_before(y, iy, x, id));
+      }
+      if (rank < K) s_pick[rank] = tid;
+    }
   }
   __syncthreads();
   if (warp != 0) return;
   float4 rs = lane < kExWarps ? s_red[lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
   warp_stat_combine(rs.x, rs.y, rs.z);
   const float MK = rs.y, S = rs.z;
+  // the row's node and its path score: from the arrays, or from the table
+  // (an id outside [0, n0) is an empty entry)
+  int node = 0;
+  float fs;
+  const int tb_b = tb.token ? (int)(rowi / tb.F) : 0, tb_f = tb.token ? (int)(rowi % tb.F) : 0;
+  if (!tb.token) {
+    fs = fscore_in[rowi];
+  } else if (!tb.frontier) {
+    fs = 1.0f;  // the root
+  } else {
+    node = tb.frontier[(size_t)tb_b * K + tb_f];
+    fs = (node >= 0 && node < tb.n0) ? tb.score[(size_t)tb_b * tb.ldc + node] : NAN;
+    if (!(node >= 0 && node < tb.n0)) node = -1;
+  }
   // a faulty row (NaN or +inf: the sum is NaN; all -inf: the sum is 0), or a
   // frontier entry with a NaN score (no node), proposes nothing
-  const bool bad = !(S > 0.0f) || fscore[rowi] != fscore[rowi];
-  // merge: the eight warp lists through warp 0's list
-  WarpTopK m{-INFINITY, 0x7fffffff, -INFINITY, 0x7fffffff};
-  for (int wi = 0; wi < kExWarps; ++wi)
-    for (int j = 0; j < K; ++j) {
-      const float x = s_tv[wi][j];
-      if (x == x && s_ti[wi][j] != 0x7fffffff) warp_offer(m, x, s_ti[wi][j], K);
-    }
+  const bool bad = !(S > 0.0f) || fs != fs;
   if (lane < K) {
-    const size_t o = rowi * (size_t)K + lane;
-    if (bad || m.i == 0x7fffffff) {
-      out_tok[o] = -1;
-      out_score[o] = -INFINITY;
+    const int e = s_pick[lane];
+    int32_t tok_o = -1;
+    float sc_o = -INFINITY;
+    if (!bad && e >= 0) {
+      const float p =
+          greedy ? (lane == 0 ? 1.0f : 0.0f) : ex2_approx(fmaf(s_tv[e], k, -MK)) / S;
+      tok_o = s_ti[e];
+      sc_o = fs * p;
+    }
+    if (!tb.token) {
+      out_tok[rowi * (size_t)K + lane] = tok_o;
+      out_score[rowi * (size_t)K + lane] = sc_o;
     } else {
-      const float p = greedy ? (lane == 0 ? 1.0f : 0.0f) : ex2_approx(fmaf(m.v, k, -MK)) / S;
-      out_tok[o] = m.i;
-      out_score[o] = fscore[rowi] * p;
+      const size_t c = (size_t)tb_b * tb.ldc + tb.n0 + (size_t)tb_f * K + lane;
+      tb.token[c] = tok_o;
+      tb.score[c] = sc_o;
+      tb.parent[c] = node;
+      tb.level[c] = tb.lvl;
+      if (!tb.frontier && lane == 0) {  // level 1 also writes the root, candidate 0
+        const size_t r = (size_t)tb_b * tb.ldc;
+        tb.token[r] = 0;
+        tb.score[r] = 1.0f;
+        tb.parent[r] = -1;
+        tb.level[r] = 0;
+      }
     }
   }
 }
@@ -274,10 +344,14 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
 // thread ranks its candidates against all others staged in shared memory,
 // and a candidate of rank r < K is pick r.
 __global__ void __launch_bounds__(kExThreads)
-tree_select_kernel(const float *__restrict__ score, const int32_t *__restrict__ token, int C,
-                   int K, int32_t *__restrict__ out) {
+tree_select_kernel(const float *__restrict__ score_base, const int32_t *__restrict__ token_base,
+                   int C, int ld, int off, int K, int32_t *__restrict__ out) {
   grid_dep_sync();
   const int b = blockIdx.x, tid = threadIdx.x;
+  // the C candidates of this sequence start at row b, column off (row stride
+  // ld); picks are written as off + their index
+  const float *score = score_base + (size_t)b * ld + off;
+  const int32_t *token = token_base + (size_t)b * ld + off;
   __shared__ float sv_[kMaxCand];
   __shared__ int ok_[kMaxCand];
   __shared__ int s_nvalid;
@@ -285,8 +359,8 @@ tree_select_kernel(const float *__restrict__ score, const int32_t *__restrict__ 
   __syncthreads();
   int nv = 0;
   for (int c = tid; c < C; c += kExThreads) {
-    sv_[c] = score[(size_t)b * C + c];
-    ok_[c] = token[(size_t)b * C + c] >= 0;
+    sv_[c] = score[c];
+    ok_[c] = token[c] >= 0;
     nv += ok_[c];
   }
   atomicAdd(&s_nvalid, nv);
@@ -297,7 +371,7 @@ tree_select_kernel(const float *__restrict__ score, const int32_t *__restrict__ 
     int rank = 0;
     for (int d = 0; d < C; ++d)
       rank += ok_[d] && (sv_[d] > v || (sv_[d] == v && d < c));
-    if (rank < K) out[(size_t)b * K + rank] = c;
+    if (rank < K) out[(size_t)b * K + rank] = off + c;
   }
   for (int r = s_nvalid + tid; r < K; r += kExThreads) out[(size_t)b * K + r] = -1;
 }
@@ -317,11 +391,11 @@ __device__ __forceinline__ bool keep_before(float sa, int la, int a, float sb, i
 __global__ void __launch_bounds__(kExThreads)
 tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restrict__ ctoken,
                      const float *__restrict__ cscore, const int32_t *__restrict__ clevel, int C,
-                     int Tn, int32_t *__restrict__ parent, int32_t *__restrict__ token,
+                     int ld, int Tn, int32_t *__restrict__ parent, int32_t *__restrict__ token,
                      float *__restrict__ score) {
   grid_dep_sync();
   const int b = blockIdx.x, tid = threadIdx.x;
-  const int32_t *cp = cparent + (size_t)b * C, *ct = ctoken + (size_t)b * C;
+  const int32_t *cp = cparent + (size_t)b * ld, *ct = ctoken + (size_t)b * ld;
   __shared__ float sc_[kMaxCand];
   __shared__ int lv_[kMaxCand];  // level, or -1: not a node
   __shared__ int slot_of[kMaxCand];
@@ -329,8 +403,8 @@ tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restr
   __shared__ int s_n;
   if (tid == 0) s_n = 0;
   for (int c = tid; c < C; c += kExThreads) {
-    sc_[c] = cscore[(size_t)b * C + c];
-    lv_[c] = (c == 0 || ct[c] >= 0) ? clevel[(size_t)b * C + c] : -1;
+    sc_[c] = cscore[(size_t)b * ld + c];
+    lv_[c] = (c == 0 || ct[c] >= 0) ? clevel[(size_t)b * ld + c] : -1;
     slot_of[c] = -1;
   }
   __syncthreads();
@@ -363,7 +437,8 @@ tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restr
   for (int i = tid; i < n; i += kExThreads) {
     const int c = keep[i], sl = slot_of[c];
     const int pc = cp[c];
-    parent[(size_t)b * Tn + sl] = pc < 0 ? -1 : (slot_of[pc] >= 0 ? slot_of[pc] : -2);
+    parent[(size_t)b * Tn + sl] =
+        pc < 0 ? -1 : (pc < C && slot_of[pc] >= 0 ? slot_of[pc] : -2);
     token[(size_t)b * Tn + sl] = ct[c];
     score[(size_t)b * Tn + sl] = sc_[c];
   }
@@ -410,10 +485,10 @@ extern "C" sv_status sv_tree_expand(const void *dlogits, sv_dtype dt, int B, int
                       dt == SV_BF16
                           ? launch_pdl(tree_expand_kernel<uint16_t>, grid, dim3(kExThreads), 0, st,
                                        (const uint16_t *)dlogits, V, k, greedy, frontier_score, K,
-                                       out_token, out_score)
+                                       out_token, out_score, Table{})
                           : launch_pdl(tree_expand_kernel<float>, grid, dim3(kExThreads), 0, st,
                                        (const float *)dlogits, V, k, greedy, frontier_score, K,
-                                       out_token, out_score));
+                                       out_token, out_score, Table{}));
 }
 
 extern "C" sv_status sv_tree_select(const float *cand_score, const int32_t *cand_token, int B,
@@ -430,14 +505,15 @@ extern "C" sv_status sv_tree_select(const float *cand_score, const int32_t *cand
   LaunchScope ls("tree_select", st);
   return check_launch("tree_select",
                       launch_pdl(tree_select_kernel, dim3(B), dim3(kExThreads), 0, st,
-                                 cand_score, cand_token, C, K, out_index));
+                                 cand_score, cand_token, C, C, 0, K, out_index));
 }
 
 extern "C" sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token,
                                       const float *cand_score, const int32_t *cand_level, int B,
-                                      int C, int T, int32_t *out_parent, int32_t *out_token,
-                                      float *out_score, void *stream) {
+                                      int C, int ldc, int T, int32_t *out_parent,
+                                      int32_t *out_token, float *out_score, void *stream) {
   if (B < 0 || C < 1 || T < 1) return set_error(SV_ERR_INVALID_ARG, "need B >= 0, C >= 1, T >= 1");
+  if (ldc < C) return set_error(SV_ERR_INVALID_ARG, "need ldc >= C (got ldc %d, C %d)", ldc, C);
   if (C > kMaxCand) return set_error(SV_ERR_UNSUPPORTED, "C > %d", kMaxCand);
   if (T > SV_MAX_TREE_NODES) return set_error(SV_ERR_UNSUPPORTED, "T > %d", SV_MAX_TREE_NODES);
   if (B == 0) return SV_OK;
@@ -456,6 +532,63 @@ extern "C" sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t 
   LaunchScope ls("tree_finalize", st);
   return check_launch("tree_finalize",
                       launch_pdl(tree_finalize_kernel, dim3(B), dim3(kExThreads), 0, st,
-                                 cand_parent, cand_token, cand_score, cand_level, C, T,
+                                 cand_parent, cand_token, cand_score, cand_level, C, ldc, T,
                                  out_parent, out_token, out_score));
+}
+
+extern "C" sv_status sv_tree_level(const void *dlogits, sv_dtype dt, int B, int F, int V,
+                                   float temperature, int K, int level, int n0, int ldc,
+                                   int32_t *frontier, int32_t *cand_parent, int32_t *cand_token,
+                                   float *cand_score, int32_t *cand_level, void *stream) {
+  if (B < 0 || F < 1 || V < 1) return set_error(SV_ERR_INVALID_ARG, "need B >= 0, F >= 1, V >= 1");
+  if (K < 1 || K > V) return set_error(SV_ERR_INVALID_ARG, "need 1 <= K <= V");
+  if (K > kMaxK) return set_error(SV_ERR_UNSUPPORTED, "K > %d", kMaxK);
+  if (V > SV_MAX_VOCAB) return set_error(SV_ERR_UNSUPPORTED, "V > %d", SV_MAX_VOCAB);
+  if (dt != SV_F32 && dt != SV_BF16) return set_error(SV_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!(temperature >= 0.0f) || !isfinite(temperature))
+    return set_error(SV_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+  if (level < 1) return set_error(SV_ERR_INVALID_ARG, "level must be >= 1");
+  if (level == 1 && (F != 1 || n0 != 1))
+    return set_error(SV_ERR_INVALID_ARG, "level 1 expands the root: F = 1, n0 = 1");
+  if (level > 1 && (F > K || n0 < 2))
+    return set_error(SV_ERR_INVALID_ARG, "level > 1: F <= K (the frontier) and n0 >= 2");
+  if ((long long)n0 + (long long)F * K > ldc)
+    return set_error(SV_ERR_INVALID_ARG, "candidate table full: n0 + F*K > ldc");
+  if (ldc > kMaxCand) return set_error(SV_ERR_UNSUPPORTED, "ldc > %d", kMaxCand);
+  if ((long long)B * F > 0x7fffffffLL) return set_error(SV_ERR_UNSUPPORTED, "B * F too large");
+  if (B == 0) return SV_OK;
+  if (!dlogits || !frontier || !cand_parent || !cand_token || !cand_score || !cand_level)
+    return set_error(SV_ERR_INVALID_ARG, "null pointer argument");
+  if ((uintptr_t)dlogits % (dt == SV_F32 ? 4 : 2)) return set_error(SV_ERR_INVALID_ARG, "dlogits misaligned");
+  sv_status s;
+  if ((s = map_arg(dlogits, "dlogits")) != SV_OK || (s = map_arg(frontier, "frontier")) != SV_OK ||
+      (s = map_arg(cand_parent, "cand_parent")) != SV_OK ||
+      (s = map_arg(cand_token, "cand_token")) != SV_OK ||
+      (s = map_arg(cand_score, "cand_score")) != SV_OK ||
+      (s = map_arg(cand_level, "cand_level")) != SV_OK)
+    return s;
+  const int greedy = temperature == 0.0f;
+  const float k = greedy ? kLog2eB : kLog2eB / temperature;
+  cudaStream_t st = (cudaStream_t)stream;
+  Table tb{level == 1 ? nullptr : frontier, cand_parent, cand_token, cand_level, cand_score,
+           ldc, n0, level, F};
+  {
+    LaunchScope ls("tree_expand", st);
+    const dim3 grid((unsigned)(B * F));
+    s = check_launch("tree_expand",
+                     dt == SV_BF16
+                         ? launch_pdl(tree_expand_kernel<uint16_t>, grid, dim3(kExThreads), 0, st,
+                                      (const uint16_t *)dlogits, V, k, greedy, nullptr, K, nullptr,
+                                      nullptr, tb)
+                         : launch_pdl(tree_expand_kernel<float>, grid, dim3(kExThreads), 0, st,
+                                      (const float *)dlogits, V, k, greedy, nullptr, K, nullptr,
+                                      nullptr, tb));
+    if (s != SV_OK) return s;
+  }
+  // the next frontier: the K best of this level's F*K children, as ids
+  LaunchScope ls("tree_select", st);
+  return check_launch("tree_select",
+                      launch_pdl(tree_select_kernel, dim3(B), dim3(kExThreads), 0, st,
+                                 (const float *)cand_score, (const int32_t *)cand_token, F * K, ldc,
+                                 n0, K, frontier));
 }

@@ -1,5 +1,7 @@
 """GPU parity of the dynamic draft-tree builder (sv_tree_expand,
-sv_tree_select, sv_tree_finalize) through the C ABI against the oracle.
+sv_tree_select, sv_tree_finalize, and sv_tree_level, which runs a level's
+expansion and selection through one candidate table) through the C ABI
+against the oracle.
 Tokens, picks and trees are compared exactly; child scores (fp32 softmax
 against double) within 2e-6 relative."""
 import numpy as np
@@ -122,3 +124,76 @@ def test_build_config5_shaped_tree_and_verify_it():
     out = sv.verify_tree(vq, dp, parent, token, score, depth)
     torch.cuda.synchronize()
     assert np.all(to_np(out["status"]) == 0)
+
+
+def _plain_build(level_rows, K, Tn, T=1.0):
+    """The same build from the plain primitives, with the bookkeeping between
+    levels done here in torch: the reference for the candidate-table mode."""
+    frontier, valid = None, None
+    cp, ct, cs, cl = [], [], [], []
+    depth = 0
+    while True:
+        rows = level_rows(depth + 1, frontier)
+        if rows is None:
+            break
+        B, F, _ = rows.shape
+        if frontier is None:
+            frontier = torch.zeros(B, 1, dtype=torch.int64, device=DEV)
+            cp.append(torch.full((B, 1), -1, dtype=torch.int32, device=DEV))
+            ct.append(torch.zeros(B, 1, dtype=torch.int32, device=DEV))
+            cs.append(torch.ones(B, 1, dtype=torch.float32, device=DEV))
+            cl.append(torch.zeros(B, 1, dtype=torch.int32, device=DEV))
+        depth += 1
+        n0 = sum(c.shape[1] for c in ct)
+        fs = torch.gather(torch.cat(cs, 1), 1, frontier)
+        if valid is not None:
+            fs = fs.masked_fill(~valid, float("nan"))
+        tok, sc = sv.tree_expand(rows, fs.contiguous(), K, temperature=T)
+        par = frontier.to(torch.int32)
+        if valid is not None:
+            par = torch.where(valid, par, torch.full_like(par, -1))
+        cp.append(par.repeat_interleave(K, dim=1))
+        ct.append(tok.reshape(B, F * K))
+        cs.append(sc.reshape(B, F * K))
+        cl.append(torch.full((B, F * K), depth, dtype=torch.int32, device=DEV))
+        sel = sv.tree_select(cs[-1].contiguous(), ct[-1].contiguous(), K).to(torch.int64)
+        valid = sel >= 0
+        frontier = torch.where(valid, sel + n0, torch.zeros_like(sel))
+    cands = tuple(torch.cat(a, 1).contiguous() for a in (cp, ct, cs, cl))
+    return sv.tree_finalize(*cands, Tn), cands
+
+
+@pytest.mark.parametrize("dtype,V,K,depth,Tn,T", [
+    (torch.bfloat16, 3001, 4, 4, 20, 1.0),     # ragged rows
+    (torch.float32, 4096, 10, 3, 60, 0.8),
+    (torch.bfloat16, 5000, 16, 3, 100, 0.0),   # greedy, the largest K
+])
+def test_level_table_equals_plain_build(dtype, V, K, depth, Tn, T):
+    """sv_tree_level (every step in the kernels) gives the candidate table
+    and the tree of the plain primitives with host bookkeeping, bit for bit;
+    a faulty level-1 row leaves its sequence with the root alone."""
+    B = 6
+    rows = {}
+
+    def level_rows(lvl, frontier):
+        if lvl > depth:
+            return None
+        F = 1 if lvl == 1 else K
+        if lvl not in rows:
+            g = torch.Generator(device=DEV).manual_seed(31 * lvl + V)
+            x = (torch.randn((B, F, V), generator=g, device=DEV) * 2.0).to(dtype)
+            if lvl == 1:
+                x[2, 0, 7] = float("nan")     # sequence 2 proposes nothing
+            rows[lvl] = x
+        return rows[lvl]
+
+    (p1, t1, s1), c1 = sv.build_tree(level_rows, K, Tn, temperature=T, return_candidates=True)
+    (p0, t0, s0), c0 = _plain_build(level_rows, K, Tn, T=T)
+    torch.cuda.synchronize()
+    for a, b in zip(c1[1:], c0[1:]):            # tokens, scores, levels
+        assert torch.equal(a, b)
+    tok = c0[1]
+    assert torch.equal(torch.where(tok >= 0, c1[0], 0), torch.where(tok >= 0, c0[0], 0))
+    assert torch.equal(p1, p0) and torch.equal(t1, t0) and torch.equal(s1, s0)
+    assert int((to_np(t1)[2] >= 0).sum()) == 1 and to_np(p1)[2, 0] == -1
+    assert np.all(to_np(c1[1])[2, 1:] == -1) and np.all(to_np(c1[0])[2, 1 + K:] == -1)

@@ -93,3 +93,28 @@ def test_tree_attention_host_checks_need_no_gpu(lib):
     assert f(null, null, null, null, 0, 4, 8, 2, 128, 16, 1.0, null, null, null, null) == 0
     assert f(null, null, null, null, 1, 4, 8, 2, 128, 16, 1.0, null, null, null, null) == 1
     assert b"null" in lib.sv_last_error()
+
+
+def test_tree_level_host_checks_need_no_gpu(lib):
+    """sv_tree_level refuses inconsistent levels and full tables before any
+    CUDA call."""
+    f = lib.sv_tree_level
+    null = None
+    # (dlogits, dt, B, F, V, T, K, level, n0, ldc, frontier, parent, token, score, level, stream)
+    def call(B=1, F=1, V=100, T=1.0, K=10, level=1, n0=1, ldc=2048):
+        return f(null, 1, B, F, V, T, K, level, n0, ldc, null, null, null, null, null, null)
+    assert call(F=2) == 1 and b"root" in lib.sv_last_error()       # level 1 expands the root
+    assert call(n0=3) == 1
+    assert call(level=2, F=11, n0=11) == 1                         # F > K
+    assert call(level=2, F=10, n0=1) == 1                          # n0 < 2 after level 1
+    assert call(level=2, F=10, n0=2000, ldc=2048) == 1             # table full
+    assert b"full" in lib.sv_last_error()
+    assert call(ldc=4096) == 2                                     # wider than finalize takes
+    assert call(K=17) == 2 and call(K=0) == 1 and call(T=-1.0) == 1
+    assert call(level=0) == 1
+    assert call(B=0) == 0                                          # no-op
+    assert call() == 1 and b"null" in lib.sv_last_error()
+    # finalize: the row stride must cover the columns used
+    g = lib.sv_tree_finalize
+    assert g(null, null, null, null, 1, 10, 9, 5, null, null, null, null) == 1
+    assert b"ldc" in lib.sv_last_error()
