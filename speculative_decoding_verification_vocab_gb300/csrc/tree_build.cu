@@ -399,29 +399,42 @@ tree_finalize_kernel(const int32_t *__restrict__ cparent, const int32_t *__restr
   __shared__ float sc_[kMaxCand];
   __shared__ int lv_[kMaxCand];  // level, or -1: not a node
   __shared__ int slot_of[kMaxCand];
-  __shared__ int keep[SV_MAX_TREE_NODES];
-  __shared__ int s_n;
-  if (tid == 0) s_n = 0;
-  for (int c = tid; c < C; c += kExThreads) {
-    sc_[c] = cscore[(size_t)b * ld + c];
-    lv_[c] = (c == 0 || ct[c] >= 0) ? clevel[(size_t)b * ld + c] : -1;
-    slot_of[c] = -1;
-  }
-  __syncthreads();
-  for (int c = tid; c < C; c += kExThreads) {
-    if (lv_[c] < 0) continue;
-    const float v = sc_[c];
-    const int l = lv_[c];
-    int rank = 0;
-    for (int d = 0; d < C && rank < Tn; ++d)
-      rank += lv_[d] >= 0 && keep_before(sc_[d], lv_[d], d, v, l, c);
-    if (rank < Tn) {
-      keep[rank] = c;
-      atomicAdd(&s_n, 1);
+  __shared__ int keep[kMaxCand];  // candidates in keep order, non-nodes (-1) last
+  __shared__ int s_nodes;
+  int P = 1;
+  while (P < C) P <<= 1;
+  if (tid == 0) s_nodes = 0;
+  for (int c = tid; c < P; c += kExThreads) {
+    const bool in = c < C;
+    if (in) {
+      sc_[c] = cscore[(size_t)b * ld + c];
+      lv_[c] = (c == 0 || ct[c] >= 0) ? clevel[(size_t)b * ld + c] : -1;
+      slot_of[c] = -1;
     }
+    keep[c] = (in && lv_[c] >= 0) ? c : -1;
   }
   __syncthreads();
-  const int n = s_n;
+  // keep order: a bitonic sort of the candidate ids in shared memory (the
+  // order is total: ids are unique), the first Tn nodes are kept
+  auto before = [&](int x, int y) {
+    return x >= 0 && (y < 0 || keep_before(sc_[x], lv_[x], x, sc_[y], lv_[y], y));
+  };
+  for (int size = 2; size <= P; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int q = tid; q < P / 2; q += kExThreads) {
+        const int lo = 2 * q - (q & (stride - 1)), hi = lo + stride;
+        const int x = keep[lo], y = keep[hi];
+        if (((lo & size) == 0) ? before(y, x) : before(x, y)) {
+          keep[lo] = y;
+          keep[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = tid; i < P; i += kExThreads)
+    if (keep[i] >= 0 && (i + 1 == P || keep[i + 1] < 0)) s_nodes = i + 1;
+  __syncthreads();
+  const int n = min(s_nodes, Tn);
   for (int i = tid; i < n; i += kExThreads) {
     const int c = keep[i];
     const int l = lv_[c];
