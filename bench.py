@@ -214,6 +214,7 @@ KERNEL_SOURCES = {
     "sampler_kv": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
     "launches": ("common.cuh", "rowstat.cuh", "tree_kv.cu", "verify.cu"),
     "tree_attention": ("common.cuh", "tree_attn.cu"),
+    "tree_expand": ("common.cuh", "rowstat.cuh", "tree_build.cu"),
 }
 
 
@@ -746,7 +747,8 @@ def run_tree_build(args):
         "roofline": {"kernel": "tree_expand", "bound": "hbm", "achieved": ach, "peak": peak,
                      "unit": "GB/s", "frac": ach / peak if ach else None,
                      "peak_kind": f"{peak_kind} copy bandwidth",
-                     "alg_bytes_per_launch": per_level_bytes, "traffic": None},
+                     "alg_bytes_per_launch": per_level_bytes,
+                     "traffic": recorded_traffic("tree_expand", cfg.name)},
         "clocks": clk.summary(),
     }
     print(json.dumps(line))

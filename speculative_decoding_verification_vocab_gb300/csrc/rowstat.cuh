@@ -45,13 +45,15 @@ __device__ __forceinline__ unsigned long long ex2_acc(unsigned long long acc,
   return f2_add(acc, f2_pack(ex2_approx(y0), ex2_approx(y1)));
 }
 
+// Returns the batch's maximum logit (NaN elements are skipped by the maxima),
+// which the tree expansion reuses as its top-K gate.
 template <typename E>
-__device__ __forceinline__ void stat_batch(const uint4 (&w)[kRsUnroll], StatState &st, float k);
+__device__ __forceinline__ float stat_batch(const uint4 (&w)[kRsUnroll], StatState &st, float k);
 
 // kRsUnroll words of 8 bf16 logits
 template <>
-__device__ __forceinline__ void stat_batch<uint16_t>(const uint4 (&w)[kRsUnroll], StatState &st,
-                                                     float k) {
+__device__ __forceinline__ float stat_batch<uint16_t>(const uint4 (&w)[kRsUnroll], StatState &st,
+                                                      float k) {
   uint32_t m[kRsUnroll];
 #pragma unroll
   for (int j = 0; j < kRsUnroll; ++j) m[j] = bf2_max(bf2_max(w[j].x, w[j].y), bf2_max(w[j].z, w[j].w));
@@ -75,12 +77,13 @@ __device__ __forceinline__ void stat_batch<uint16_t>(const uint4 (&w)[kRsUnroll]
         st.s01 = ex2_acc(st.s01, y2);
     }
   }
+  return cm;
 }
 
 // kRsUnroll words of 4 fp32 logits
 template <>
-__device__ __forceinline__ void stat_batch<float>(const uint4 (&w)[kRsUnroll], StatState &st,
-                                                  float k) {
+__device__ __forceinline__ float stat_batch<float>(const uint4 (&w)[kRsUnroll], StatState &st,
+                                                   float k) {
   float m[kRsUnroll];
 #pragma unroll
   for (int j = 0; j < kRsUnroll; ++j)
@@ -100,6 +103,7 @@ __device__ __forceinline__ void stat_batch<float>(const uint4 (&w)[kRsUnroll], S
     st.s23 = ex2_acc(st.s23, f2_fma(f2_pack(__uint_as_float(w[j].z), __uint_as_float(w[j].w)),
                                     k2, nr2));
   }
+  return m[0];
 }
 
 // one logit (ragged head / tail, and the short remainder of a segment)

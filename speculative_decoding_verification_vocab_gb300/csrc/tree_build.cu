@@ -224,18 +224,14 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
         if (!in) inb &= ~(1u << j);
       }
     }
-    stat_batch<E>(buf, st, k);
+    const float bm = stat_batch<E>(buf, st, k);  // the batch maximum
     int skip = -1;
     if (!seeded && w.ti == 0x7fffffff) {  // list still empty: seed it from this batch
       skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
       seeded = true;
     }
     // one gate per batch: the words are looked at only when some lane's
-    // batch maximum reaches the list's K-th value (after the first batches
-    // almost none does)
-    float bm = word_max<E>(buf[0]);
-#pragma unroll
-    for (int j = 1; j < kRsUnroll; ++j) bm = fmaxf(bm, word_max<E>(buf[j]));
+    // batch maximum reaches the list's K-th value
     if (__any_sync(0xffffffffu, bm >= w.tv))
 #pragma unroll
       for (int j = 0; j < kRsUnroll; ++j)
