@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=5, choices=[2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pool", type=int, default=4, help="distinct rounds rotated in the timed loop")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -377,18 +377,34 @@ def run_ours(args):
         torch.distributed.barrier()
     # timed region: K steps back to back (kernels chained by programmatic
     # dependent launch; no event between them)
+    # a pool of rounds smaller than twice L2 (the tiny chain) would be read
+    # from L2: then every step is timed alone, with a 256 MB write between
+    # steps outside its events
+    pool_bytes = sum(v.numel() * v.element_size() for rd in wl.rounds
+                     for v in (rd["vq"], rd["dp"]))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if pool_bytes < 2 * L2_BYTES \
+        else None
     n_launch0 = sv.sv_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         torch.cuda.synchronize()
         e0.record(stream)
+        step_ms = 0.0
         for k in range(K):
+            if flush is not None:
+                flush.fill_(k & 255)
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
             step(W + k, wl.rounds[k % args.pool], W + k)
+            if flush is not None:
+                s1.record(stream)
+                s1.synchronize()
+                step_ms += s0.elapsed_time(s1)
         e1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = e0.elapsed_time(e1)
+    ms = e0.elapsed_time(e1) if flush is None else step_ms
     launches = sv.sv_launch_count() - n_launch0
     # the same K steps again with an event pair around every launch: per-kernel
     # durations (the events serialise the launches, so this pass is slower and
@@ -403,6 +419,18 @@ def run_ours(args):
     sv.sv_trace_enable(False)
     trace = sv.sv_trace_collect()
     traced_ms = t0.elapsed_time(t1)
+    # the spread: 5 more repeats of the K-step loop, each bracketed alone
+    # (outside the measurement above)
+    rep_ms = []
+    for _ in range(5):
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        r0.record(stream)
+        for k in range(K):
+            step(W + k, wl.rounds[k % args.pool], W + k)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rep_ms.append(r0.elapsed_time(r1) / K)
 
     acc = o_acc[W:].cpu().numpy()
     st = o_st[W:].cpu().numpy()
@@ -449,11 +477,19 @@ def run_ours(args):
                    "max_depth": maxd, "logits": str(cfg.dtype).replace("torch.", ""),
                    "kv": f"{kvb.L} layers x {kvb.H} kv heads x {kvb.D}, bf16",
                    "pool_rounds": args.pool,
-                   "l2": f"inputs larger than L2: each step reads {stats_bytes / K / 1e6:.0f} MB of "
+                   "l2": (f"L2 flushed between steps (a 256 MB write outside each step's events; "
+                          f"the pool of rounds is {pool_bytes / 1e6:.2f} MB)") if flush is not None else
+                         f"inputs larger than L2: each step reads {stats_bytes / K / 1e6:.0f} MB of "
                          f"logit rows from a pool of {args.pool} distinct rounds "
                          f"({args.pool * wl.rounds[0]['vq'].numel() * wl.esize * 2 / 1e9:.1f} GB)"},
         "accepted_tokens_per_s": total_tokens / (ms_max / 1e3),
-        "mean_emitted_per_seq": tokens / (K * B), "alpha_hat": alpha_hat,
+        "mean_emitted_per_seq": tokens / (K * B), "mean_accept_len": float(acc.mean()),
+        "alpha_hat": alpha_hat,
+        "us_per_round": 1e3 * ms_max / K,
+        "repeats": {"n": len(rep_ms), "ms_per_step_median": float(np.median(rep_ms)),
+                    "p10": float(np.percentile(rep_ms, 10)),
+                    "p90": float(np.percentile(rep_ms, 90)),
+                    "note": "5 further repeats of the K-step loop after the measurement"},
         "hbm_gbs": alg_bytes / (ms_max / 1e3) / 1e9,
         "hbm_frac_measured": alg_bytes / (ms_max / 1e3) / 1e9 / peak,
         "hbm_frac_nominal_8tbs": alg_bytes / (ms_max / 1e3) / 1e9 / 8000.0,
@@ -578,10 +614,12 @@ def _rows_for_oracle(rd, ids, tree, maxd):
     return vq, dp
 
 
-def _oracle_round(cfg, rd, ids, step, kv=None, early=False):
-    """One round of the oracle on the sequences `ids` of a pooled round: the
-    tree (or chain) verify and, for trees, the in-place KV compaction of the
-    sampled sequences' window.  Returns (rows covered, seconds in the oracle)."""
+def _oracle_job(cfg, rd, ids, step, early=False):
+    """The oracle's inputs for the sequences `ids` of a pooled round, marshalled
+    up front, and a function that runs the round on them: the tree (or chain)
+    verify and, for trees, the in-place KV compaction of the sampled
+    sequences' window (a KV buffer is passed in, one per thread).  Returns
+    (rows covered, run)."""
     import oracle
     import torch
     tree = "parent" in rd
@@ -591,22 +629,33 @@ def _oracle_round(cfg, rd, ids, step, kv=None, early=False):
         par = rd["parent"][tid].cpu().numpy()
         tok = rd["token"][tid].cpu().numpy()
         sc = rd["score"][tid].cpu().numpy()
-        t0 = time.perf_counter()
-        o = oracle.verify_tree(vq, dp, par, tok, sc, cfg.depth, T=cfg.temperature, seed=1234,
-                               step=step, seq_ids=ids)
-        oracle.tree_mask(par)
-        if kv is not None:
-            L, H, D, S, buf = kv
-            nb = len(ids)
-            base = np.zeros(nb, np.int32)
-            oracle.kv_compact(buf, buf, L, nb, S, S, H, D, 2, base, base, o["path"],
-                              o["accept_len"] + 1)
+
+        def run(kv):
+            o = oracle.verify_tree(vq, dp, par, tok, sc, cfg.depth, T=cfg.temperature, seed=1234,
+                                   step=step, seq_ids=ids)
+            oracle.tree_mask(par)
+            if kv is not None:
+                L, H, D, S, buf = kv
+                nb = len(ids)
+                base = np.zeros(nb, np.int32)
+                oracle.kv_compact(buf, buf, L, nb, S, S, H, D, 2, base, base, o["path"],
+                                  o["accept_len"] + 1)
     else:
         d = rd["d"][tid].cpu().numpy()
-        t0 = time.perf_counter()
-        oracle.verify_chain(vq, dp, d, T=cfg.temperature, seed=1234, step=step, seq_ids=ids,
-                            early_exit=early)
-    return len(ids) * vq.shape[1], time.perf_counter() - t0
+
+        def run(kv):
+            oracle.verify_chain(vq, dp, d, T=cfg.temperature, seed=1234, step=step, seq_ids=ids,
+                                early_exit=early)
+    return len(ids) * vq.shape[1], run
+
+
+def _oracle_round(cfg, rd, ids, step, kv=None, early=False):
+    """One round of the oracle on the sequences `ids` (see _oracle_job).
+    Returns (rows covered, seconds in the oracle)."""
+    rows, run = _oracle_job(cfg, rd, ids, step, early)
+    t0 = time.perf_counter()
+    run(kv)
+    return rows, time.perf_counter() - t0
 
 
 def _kv_window(cfg, k, S):
@@ -616,25 +665,69 @@ def _kv_window(cfg, k, S):
     return (kvc.L, kvc.H, kvc.D, S, buf)
 
 
-def cpu_baseline(args, wl, cfg, budget_s=10.0, cap_s=30.0):
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args, wl, cfg, budget_s=10.0, cap_s=30.0, all_core_s=5.0):
     """The oracle on the host cores: groups of `--cpu-sample` sequences taken
     in turn from the pooled rounds (a new step number each group) until the
-    oracle has run for `budget_s` seconds (at most `cap_s`)."""
+    oracle has run for `budget_s` seconds (at most `cap_s`), single-threaded;
+    then the same kind of groups on every host core (one Python thread per
+    core; the C oracle keeps no global state and ctypes releases the GIL
+    during its calls) for about `all_core_s` seconds of wall time.
+    Marshalling is outside both timings."""
+    from concurrent.futures import ThreadPoolExecutor
     k = min(args.cpu_sample, wl.B)
     kv = _kv_window(cfg, k, wl.S) if wl.tree else None
     rows, secs, groups = 0, 0.0, 0
+
+    def group(g):
+        rd = wl.rounds[g % len(wl.rounds)]
+        start = (g // len(wl.rounds)) * k % wl.B
+        return rd, np.sort((start + np.arange(k)) % wl.B)
+
     while secs < budget_s and secs < cap_s:
-        rd = wl.rounds[groups % len(wl.rounds)]
-        start = (groups // len(wl.rounds)) * k % wl.B
-        ids = np.sort((start + np.arange(k)) % wl.B)
+        rd, ids = group(groups)
         r, t = _oracle_round(cfg, rd, ids, groups, kv, early=wl.early)
         rows += r
         secs += t
         groups += 1
-    return {"value": rows / secs, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{groups} groups of {k} sequences from {len(wl.rounds)} rounds of "
-                      f"config {cfg.index} ({cfg.name}); {rows} rows; single-threaded C "
-                      f"oracle in double precision, {secs:.1f} s in the oracle"}
+    out = {"value": rows / secs, "unit": "rows/s", "cores": 1, "kind": "oracle",
+           "sample": f"{groups} groups of {k} sequences from {len(wl.rounds)} rounds of "
+                     f"config {cfg.index} ({cfg.name}); {rows} rows; single-threaded C "
+                     f"oracle in double precision, {secs:.1f} s in the oracle"}
+    # every core: one marshalled group per thread (its own KV window), run
+    # over and over until the wall-clock budget is spent
+    n = host_cores()
+    jobs = [_oracle_job(cfg, *group(g), g, wl.early) for g in range(n)]
+    kvs = [None] * n
+    if wl.tree:
+        kvc = cfg.kv
+        kvs = [(kvc.L, kvc.H, kvc.D, wl.S,
+                np.full((kvc.L, 2, k, wl.S, kvc.H, kvc.D * 2), 1, np.uint8)) for _ in range(n)]
+    t0 = time.perf_counter()
+    deadline = t0 + all_core_s
+
+    def work(i):
+        r, run = jobs[i]
+        done = 0
+        while time.perf_counter() < deadline:
+            run(kvs[i])
+            done += r
+        return done
+
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        rows_all = sum(ex.map(work, range(n)))
+    wall = time.perf_counter() - t0
+    ng = n
+    out["all_cores"] = {"value": rows_all / wall, "unit": "rows/s", "cores": n,
+                        "sample": f"{ng} groups of {k} sequences, one per thread on {n} "
+                                  f"threads, each run repeatedly for {wall:.1f} s wall"}
+    return out
 
 
 def run_reference(args):
