@@ -67,6 +67,9 @@ def parse():
                     help="time the tree-masked verifier attention (one layer) instead")
     ap.add_argument("--greedy", action="store_true",
                     help="temperature 0: greedy verification (verifier rows only, no sampling)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture each pooled round's step in a CUDA graph and replay it in "
+                         "the timed loop (the latency-bound small configurations)")
     ap.add_argument("--early-exit", action="store_true",
                     help="chain configs: sv_verify_chain_early_exit (rows after a sequence's "
                          "first rejection are not read once it is known)")
@@ -366,9 +369,34 @@ def run_ours(args):
     ev_fork, ev_acc = torch.cuda.Event(), torch.cuda.Event()
     outs = dict(path=o_path, tok=o_tok, acc=o_acc, st=o_st, kv=o_kv, mask=o_mask, depth=o_depth)
 
-    def step(i, rd, seed_step):
-        run_round(sv, wl, cfg, maxd, rd, outs, i, rank_seed(1234, rank), seed_step, ws, stream,
-                  side, ev_fork, ev_acc)
+    def step(i, rd, seed_step, on=None):
+        run_round(sv, wl, cfg, maxd, rd, outs, i, rank_seed(1234, rank), seed_step, ws,
+                  stream if on is None else on, side, ev_fork, ev_acc)
+
+    graphs, graph_launches = None, 0
+    if args.graph:
+        # one graph per pooled round (its step number fixed at capture, its
+        # outputs in slice W + round), both streams of the step inside it;
+        # every replay re-runs every kernel
+        cap = torch.cuda.Stream(device=dev)
+        graphs = []
+        c0 = sv.sv_launch_count()
+        for r in range(args.pool):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                step(W + r, wl.rounds[r], W + r, on=cap)
+            graphs.append(g)
+        graph_launches = (sv.sv_launch_count() - c0) // args.pool
+        torch.cuda.synchronize()
+
+    def timed_step(k):
+        if graphs is not None:
+            graphs[k % args.pool].replay()
+        else:
+            step(W + k, wl.rounds[k % args.pool], W + k)
+
+    def out_slice(k):  # where timed step k left its outputs
+        return W + (k % args.pool) if graphs is not None else W + k
 
     for i in range(W):
         step(i, wl.rounds[i % args.pool], i)
@@ -384,9 +412,10 @@ def run_ours(args):
                      for v in (rd["vq"], rd["dp"]))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if pool_bytes < 2 * L2_BYTES \
         else None
-    n_launch0 = sv.sv_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    def time_loop():
+        """K timed steps: back to back under one event pair, or (flush mode)
+        each under its own pair with the L2 flush between them.  Returns ms."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
         step_ms = 0.0
@@ -395,17 +424,21 @@ def run_ours(args):
                 flush.fill_(k & 255)
                 s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 s0.record(stream)
-            step(W + k, wl.rounds[k % args.pool], W + k)
+            timed_step(k)
             if flush is not None:
                 s1.record(stream)
                 s1.synchronize()
                 step_ms += s0.elapsed_time(s1)
         e1.record(stream)
         torch.cuda.synchronize()
+        return e0.elapsed_time(e1) if flush is None else step_ms
+
+    n_launch0 = sv.sv_launch_count()
+    with Clocks(local) as clk:
+        ms = time_loop()
     if world > 1:
         torch.distributed.barrier()
-    ms = e0.elapsed_time(e1) if flush is None else step_ms
-    launches = sv.sv_launch_count() - n_launch0
+    launches = sv.sv_launch_count() - n_launch0 + K * graph_launches
     # the same K steps again with an event pair around every launch: per-kernel
     # durations (the events serialise the launches, so this pass is slower and
     # is not the step time)
@@ -419,18 +452,9 @@ def run_ours(args):
     sv.sv_trace_enable(False)
     trace = sv.sv_trace_collect()
     traced_ms = t0.elapsed_time(t1)
-    # the spread: 5 more repeats of the K-step loop, each bracketed alone
+    # the spread: 5 more repeats of the timed loop, each timed the same way
     # (outside the measurement above)
-    rep_ms = []
-    for _ in range(5):
-        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        r0.record(stream)
-        for k in range(K):
-            step(W + k, wl.rounds[k % args.pool], W + k)
-        r1.record(stream)
-        torch.cuda.synchronize()
-        rep_ms.append(r0.elapsed_time(r1) / K)
+    rep_ms = [time_loop() / K for _ in range(5)]
 
     acc = o_acc[W:].cpu().numpy()
     st = o_st[W:].cpu().numpy()
@@ -473,6 +497,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16" if cfg.dtype.__repr__().endswith("bfloat16") else "f32",
         "data": "synthetic",
         "config": {"workload": f"config {cfg.index}: {cfg.name}" + (" (greedy, T=0)" if wl.greedy else "")
+                   + (" (CUDA graph replay)" if graphs is not None else "")
                    + (" (early exit)" if wl.early else ""), "B_per_gpu": B, "T": T, "V": V,
                    "max_depth": maxd, "logits": str(cfg.dtype).replace("torch.", ""),
                    "kv": f"{kvb.L} layers x {kvb.H} kv heads x {kvb.D}, bf16",
