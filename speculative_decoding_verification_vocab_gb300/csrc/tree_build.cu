@@ -92,7 +92,7 @@ __device__ __forceinline__ void warp_offer_words(WarpTopK &w, uint4 word, int v,
   // the lane marks the elements of its word that can reach the list
   unsigned emask = 0u;
   if (in && m >= w.tv) {
-#pragma unroll 1
+#pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const float x = word_elem<E>(word, j);
       if (x >= w.tv && v + j != skip) emask |= 1u << j;  // NaN fails the compare
