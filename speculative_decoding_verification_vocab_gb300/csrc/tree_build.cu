@@ -129,14 +129,13 @@ __device__ __forceinline__ int warp_seed(WarpTopK &w, const uint4 (&buf)[kRsUnro
 #pragma unroll
   for (int j = 0; j < kRsUnroll; ++j) {
     const float m = word_max<E>(buf[j]);
+    int first = 0;  // the word's first element equal to its maximum
+#pragma unroll
+    for (int e = kPer - 1; e >= 0; --e)
+      if (word_elem<E>(buf[j], e) == m) first = e;
     if (m > bv) {  // words come in increasing id: strict keeps the lowest id
-#pragma unroll 1
-      for (int e = 0; e < kPer; ++e)
-        if (word_elem<E>(buf[j], e) == m) {
-          bv = m;
-          bi = v0 + j * stride_elems + e;
-          break;
-        }
+      bv = m;
+      bi = v0 + j * stride_elems + first;
     }
   }
   float sv = bv;
