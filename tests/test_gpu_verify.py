@@ -482,3 +482,42 @@ def test_accept_event_marks_final_accept_outputs():
     # random KV bytes hold NaN patterns: compare the bytes
     assert torch.equal(kl, kl_ref)
     assert torch.equal(kv.view(torch.int16), kv_ref.view(torch.int16))
+
+
+def _path_rows_f32(x, parent, score, depth):
+    """float32 copy of x [B][T][V] holding only each sequence's best-path rows
+    (zeros elsewhere: the oracle reads only those rows), without a dense
+    conversion of the whole tensor."""
+    B, T, V = x.shape
+    out = np.zeros((B, T, V), np.float32)
+    for b in range(B):
+        nodes = oracle.tree_best_path(parent[b], score[b], depth).astype(np.int64)
+        out[b, nodes] = x[b, torch.from_numpy(nodes).to(x.device)].float().cpu().numpy()
+    return out
+
+
+@pytest.mark.parametrize("idx,early", [(3, False), (3, True), (5, False)])
+def test_full_batch_parity_three_rounds(idx, early):
+    """Every sequence of three rounds of the large configurations (not a
+    sample): tokens, accept lengths, status and paths exact up to the near-tie
+    rule, probabilities within tolerance."""
+    cfg = synth.CONFIGS[idx]
+    for rnd in range(3):
+        if cfg.kind == "chain":
+            vq, dp, d = synth.chain_inputs(cfg, seed=100 + rnd, device=DEV)
+            g = sv.verify_chain(vq, dp, d, seed=idx, step=rnd, early_exit=early)
+            torch.cuda.synchronize()
+            o = oracle.verify_chain(_np32(vq), _np32(dp), d.cpu().numpy(), seed=idx, step=rnd,
+                                    early_exit=early)
+            compare_verify(g, o, rows_per_seq=cfg.N + 1, label=f"config {idx} round {rnd}")
+        else:
+            vq, dp, parent, token, score = synth.tree_inputs(cfg, seed=100 + rnd, device=DEV)
+            g = sv.verify_tree(vq, dp, parent, token, score, cfg.depth, seed=idx, step=rnd)
+            torch.cuda.synchronize()
+            par, sc = parent.cpu().numpy(), score.cpu().numpy()
+            o = oracle.verify_tree(_path_rows_f32(vq, par, sc, cfg.depth),
+                                   _path_rows_f32(dp, par, sc, cfg.depth), par,
+                                   token.cpu().numpy(), sc, cfg.depth, seed=idx, step=rnd)
+            npos = _npos_of(o, par, sc, cfg.depth)
+            compare_verify(g, o, rows_per_seq=parent.shape[1], npos=npos,
+                           label=f"config {idx} round {rnd}")
