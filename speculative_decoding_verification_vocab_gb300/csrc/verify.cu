@@ -109,12 +109,15 @@ __device__ __forceinline__ const E *used_row(const Round &r, int b, int j, const
 // segment.  Ragged head / tail elements (outside the 16-byte-aligned body)
 // are read one by one.  Row slot j of a sequence is the verifier row of
 // position j (j <= maxpos) or the draft row of position j - maxpos - 1.
-constexpr int kSegElems = 16384;  // smallest segment (fp32); sizes the workspace
-constexpr int kRsThreads = 256;
+constexpr int kSegElems = 8192;  // smallest segment (fp32); sizes the workspace
+constexpr int kRsThreads = 128;
 // A thread owns 2 * kRsUnroll 16-byte words of a segment: the first
 // kRsUnroll go to registers, the second are staged into shared memory by
-// asynchronous copies issued first, so a CTA keeps 64 KB of loads in flight
-// while holding only 32 words of registers per thread.
+// asynchronous copies issued first, so a CTA keeps 32 KB of loads in flight
+// while holding only 32 words of registers per thread.  Segments of 32 KB
+// (128 threads, 10 CTAs/SM) rather than 64 KB: twice the CTAs of half the
+// work even out the end of a launch (row pass 0.86 -> 0.95 of the copy
+// bandwidth on the large-vocabulary chain).
 template <typename E>
 __host__ __device__ constexpr int seg_elems() {
   return kRsThreads * 2 * kRsUnroll * 16 / (int)sizeof(E);
@@ -238,7 +241,7 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
 }
 
 template <typename E, bool kCopy>
-__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
   grid_dep_sync();
@@ -512,7 +515,7 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
 constexpr unsigned kEeInit = 0x7F7F7F7Fu;  // counts and stop[] start here (byte fill)
 
 template <typename E, bool kCopy>
-__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_stats_ee_kernel(Round r, int G, float4 *__restrict__ partial, unsigned *__restrict__ count,
                     int *__restrict__ stop, uint64_t seed, uint64_t step) {
   grid_dep_sync();
@@ -695,7 +698,7 @@ __device__ __forceinline__ void argmax_segment(const Round &r, int G, const int3
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 5 : 4)
+__global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_argmax_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
                   const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
   grid_dep_sync();
