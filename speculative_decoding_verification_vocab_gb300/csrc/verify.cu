@@ -26,12 +26,12 @@ namespace sv {
 namespace {
 
 constexpr int kDecideWarps = 4;
-// sampler geometry: a CTA owns an 8192-element slice of a row; each of its
+// sampler geometry: a CTA owns a 4096-element slice of a row; each of its
 // threads owns kSpRun consecutive elements of the slice
-constexpr int kSpThreads = 256;
+constexpr int kSpThreads = 128;
 constexpr int kSpWarps = kSpThreads / 32;
 constexpr int kSpRun = 32;
-constexpr int kSpSlice = kSpThreads * kSpRun;  // 8192 elements per CTA
+constexpr int kSpSlice = kSpThreads * kSpRun;  // 4096 elements per CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Task {
@@ -1020,7 +1020,7 @@ __device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, 
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 4 : 2)
+__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 8 : 4)
 sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
   grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
@@ -1204,7 +1204,7 @@ __device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, con
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 4 : 2)
+__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 8 : 4)
 sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
   grid_dep_sync();
   const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
