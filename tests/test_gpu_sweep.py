@@ -82,3 +82,59 @@ def test_tree_sweep(seed):
     npos = np.array([len(oracle.tree_best_path(par[b], sc[b], max_depth)) - 1 for b in range(B)])
     compare_verify(g, o, rows_per_seq=T, npos=npos,
                    label=f"tree sweep {seed} B{B} T{T} depth{depth} cap{max_depth} V{V}")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_greedy_sweep(seed):
+    from test_gpu_greedy import _greedy_drafts, _same
+    cfg, B, N, V, _ = _chain_case(1000 + seed)
+    vq, dp, _ = synth.chain_inputs(cfg, seed=seed, B=B, V=V, N=N)
+    d = _greedy_drafts(vq, N, 0.85, seed=seed)
+    g = sv.verify_chain(vq.to(DEV), dp.to(DEV), d.to(DEV), temperature=0.0)
+    torch.cuda.synchronize()
+    o = oracle.verify_chain(_np32(vq), _np32(dp), d.numpy(), T=0.0)
+    _same(g, o, f"greedy sweep {seed} B{B} N{N} V{V} {cfg.dtype}")
+
+
+def _bytes(t):
+    return t.detach().cpu().contiguous().view(torch.uint8).numpy().copy()
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_kv_compact_sweep(seed):
+    """Random cache shapes and accepted paths, in place and as a commit from
+    a separate buffer, byte for byte against the oracle."""
+    rng = np.random.default_rng(500 + seed)
+    L, B, H = int(rng.integers(1, 5)), int(rng.integers(1, 13)), int(rng.integers(1, 9))
+    D = int(rng.choice([1, 3, 5, 16, 64, 128]))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+    esz = torch.tensor([], dtype=dtype).element_size()
+    P = int(rng.integers(1, 12))
+    span = P + int(rng.integers(0, 20))           # tree slots a path can use
+    base = rng.integers(0, 16, B).astype(np.int32)
+    S = int(base.max()) + span + 1
+    rows = np.zeros((B, P), np.int32)
+    for b in range(B):                            # root, then strictly increasing slots
+        rows[b, 1:] = np.sort(rng.choice(np.arange(1, span), P - 1, replace=False))
+    n = rng.integers(0, P + 1, B).astype(np.int32)  # rows kept (root included)
+    kv = synth.kv_cache(L, B, S, H, D, device=DEV, seed=seed, dtype=dtype)
+    ref = _bytes(kv)
+    tb = torch.from_numpy(base).to(DEV)
+    kl = sv.kv_compact(kv, kv, tb, tb, torch.from_numpy(rows).to(DEV),
+                       torch.from_numpy(np.maximum(n - 1, 0)).to(DEV), 1)
+    torch.cuda.synchronize()
+    okl = oracle.kv_compact(ref, ref, L, B, S, S, H, D, esz, base, base, rows,
+                            np.maximum(n, 1))
+    assert np.array_equal(kl.cpu().numpy(), okl), seed
+    assert np.array_equal(_bytes(kv), ref), seed
+    # commit from a separate buffer of P rows to the cache at base
+    src = synth.kv_cache(L, B, P, H, D, device=DEV, seed=seed + 50, dtype=dtype)
+    dst = synth.kv_cache(L, B, S + P, H, D, device=DEV, seed=seed + 60, dtype=dtype)
+    sref, dref = _bytes(src), _bytes(dst)
+    zeros = torch.zeros(B, dtype=torch.int32, device=DEV)
+    kl = sv.kv_compact(src, dst, zeros, tb, None, torch.from_numpy(n).to(DEV), 0)
+    torch.cuda.synchronize()
+    okl = oracle.kv_compact(sref, dref, L, B, P, S + P, H, D, esz, np.zeros(B, np.int32), base,
+                            np.tile(np.arange(P, dtype=np.int32), (B, 1)), n)
+    assert np.array_equal(kl.cpu().numpy(), okl), seed
+    assert np.array_equal(_bytes(dst), dref), seed
