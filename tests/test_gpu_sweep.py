@@ -138,3 +138,28 @@ def test_kv_compact_sweep(seed):
                             np.tile(np.arange(P, dtype=np.int32), (B, 1)), n)
     assert np.array_equal(kl.cpu().numpy(), okl), seed
     assert np.array_equal(_bytes(dst), dref), seed
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_tree_expand_sweep(seed):
+    """Top-K expansion on random shapes: tokens exact, child scores within the
+    builder's tolerance (bf16 rows with many equal logits included)."""
+    from test_gpu_tree_build import SCORE_RTOL
+    rng = np.random.default_rng(900 + seed)
+    B, F = int(rng.integers(1, 9)), int(rng.integers(1, 11))
+    V = int(rng.choice([16, 33, 1000, 1001, 4096, 20481, 70000]))
+    K = int(rng.integers(1, min(16, V) + 1))
+    T = float(rng.choice([0.0, 0.6, 1.0]))
+    dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+    sigma = float(rng.choice([0.3, 1.0, 3.0]))     # small sigma in bf16: many ties
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((B, F, V), generator=g) * sigma).to(dtype)
+    fs = torch.rand((B, F), generator=g) * 0.9 + 0.05
+    tok, sc = sv.tree_expand(x.to(DEV), fs.to(DEV), K, temperature=T)
+    torch.cuda.synchronize()
+    otok, osc = oracle.tree_expand(x.float().numpy(), fs.numpy(), K, T=T)
+    assert np.array_equal(tok.cpu().numpy(), otok), seed
+    gs = sc.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(gs), np.isneginf(osc)), seed
+    fin = np.isfinite(osc)
+    assert np.allclose(gs[fin], osc[fin], rtol=SCORE_RTOL, atol=0.0), seed
