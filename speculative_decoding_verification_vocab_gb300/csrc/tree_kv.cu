@@ -76,7 +76,7 @@ tree_mask_kernel(const int32_t *__restrict__ parent, int T, int W, uint64_t *__r
 // strictly increasing mean a later batch never reads a slot an earlier one
 // wrote (a unit's moves go in increasing k), and a batch's reads precede its
 // writes; different threads touch different columns or slabs.
-constexpr int kKvSlabs = 8;
+constexpr int kKvSlabs = 16;
 constexpr int kKvMaxRows = 4096;
 constexpr int kKvBatch = 8;
 
