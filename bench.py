@@ -827,12 +827,12 @@ def run_tree_build(args):
         return sv.build_tree(lambda lvl, f: rows[lvl - 1] if lvl <= depth else None, K, Tn,
                              cfg.temperature, stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    n0 = sv.sv_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    with Clocks(local) as clk:  # warm-up inside: the timing starts on warm clocks
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        n0 = sv.sv_launch_count()
         e0.record(stream)
         for k in range(args.steps):
             step(k)
@@ -903,12 +903,12 @@ def run_attention(args):
     def step():
         sv.sv_tree_attention(q, kv, base, mask, scale, out, lse, status, stream)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    n0 = sv.sv_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    with Clocks(local) as clk:  # warm-up inside: the timing starts on warm clocks
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        n0 = sv.sv_launch_count()
         e0.record(stream)
         for _ in range(args.steps):
             step()
