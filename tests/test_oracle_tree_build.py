@@ -131,3 +131,26 @@ def test_built_scores_are_path_products():
                 prod *= _softmax(rows[(b, par)], T)[ct[b, node]]
                 node = par
             assert np.isclose(score[b, i], prod, rtol=1e-6)
+
+
+@pytest.mark.parametrize("seed", [5, 6, 7])
+def test_kept_tree_has_the_largest_total_score(seed):
+    """Brute force on tiny builds: over every ancestor-closed set of T nodes
+    holding the root, none has a larger total path score than the tree the
+    builder keeps.  Scores never grow along a path (each factor is a
+    probability), which is why keeping the T best candidates is optimal."""
+    import itertools
+    rng = np.random.default_rng(seed)
+    B, V, K, depth, Tn = 3, 6, 2, 3, 5
+    (cp, ct, cs, cl), rows, (parent, token, score) = _build_tree(rng, B, V, K, depth, Tn)
+    for b in range(B):
+        valid = [c for c in range(1, cp.shape[1]) if ct[b, c] >= 0]
+        best = -1.0
+        for sub in itertools.combinations(valid, Tn - 1):
+            s = set(sub) | {0}
+            if all(int(cp[b, c]) in s for c in sub):
+                best = max(best, sum(float(cs[b, c]) for c in s))
+        got = sum(float(v) for v in score[b])
+        assert np.isclose(got, best, rtol=1e-12, atol=0), (b, got, best)
+        # and the kept nodes form a tree with parents before children
+        assert parent[b, 0] == -1 and all(0 <= parent[b, i] < i for i in range(1, Tn))
