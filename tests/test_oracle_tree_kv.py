@@ -221,26 +221,3 @@ def test_expected_tokens_closed_forms():
     assert abs(oracle.expected_tokens(0.6, 5) - 2.38336) < 1e-12
     assert abs(oracle.expected_tokens(0.9, 5) - 4.68559) < 1e-12
     assert abs(oracle.speedup(0.8, 8, 0.05) - (1 - 0.8 ** 9) / 0.2 / 1.4) < 1e-12
-
-
-def test_pages_worked_numbers_against_the_formula():
-    """The lesson's worked numbers are looser than its own formula; record
-    where they agree and where they cannot be reproduced."""
-    def best(a, c, Nmax=60):
-        s = [oracle.speedup(a, N, c) for N in range(1, Nmax + 1)]
-        return int(np.argmax(s)) + 1, max(s), s
-    # alpha = 0.8, c = 0.05: the page says N ~ 5-7 and 3.2x
-    N_opt, s_opt, s = best(0.8, 0.05)
-    assert N_opt == 8 and abs(s_opt - 3.09208) < 1e-4
-    assert all(s[N - 1] >= 0.95 * s_opt for N in (5, 6, 7))      # N = 5..7 is within 5% of the optimum
-    assert abs(3.2 - s_opt) / s_opt < 0.04                         # 3.2x is within 4% of the optimum
-    # alpha = 0.95, c = 0.02: the page says N ~ 8-10 and ~5x; the formula's optimum is N = 31 (9.95x)
-    N_opt, s_opt, s = best(0.95, 0.02)
-    assert N_opt == 31 and abs(s_opt - 9.95) < 0.01
-    assert s[7] > 6.3 and s[9] > 7.1                               # N = 8..10 gives 6.4-7.2x, not ~5x
-    # N = 5, alpha 0.6 -> 0.9: the page says 2.2 -> 4.1 tokens per pass; the formula gives 2.38 -> 4.69
-    assert abs(oracle.expected_tokens(0.6, 5) - 2.2) > 0.15
-    assert abs(oracle.expected_tokens(0.9, 5) - 4.1) > 0.5
-    # exercise 2: N = 1..10 at alpha = 0.9, c = 0.04 -- time per token keeps falling to N = 10
-    t = [(N * 0.04 + 1) / oracle.expected_tokens(0.9, N) for N in range(1, 11)]
-    assert int(np.argmin(t)) + 1 == 10
