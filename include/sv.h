@@ -346,7 +346,13 @@ sv_status sv_tree_finalize(const int32_t *cand_parent, const int32_t *cand_token
  * order) frontier [B][K] holds the ids of the next frontier, the K best
  * children as sv_tree_select orders them (-1 where there are fewer).  The
  * caller's next n0 is n0 + F*K; after the last level, sv_tree_finalize with
- * C = that n0 and the same ldc builds the tree. */
+ * C = that n0 and the same ldc builds the tree.
+ * Errors, returned before anything is enqueued: SV_ERR_INVALID_ARG for
+ * B < 0, F < 1, V < 1, K outside [1, V], a negative or non-finite
+ * temperature, level < 1, level 1 with F != 1 or n0 != 1, level > 1 with
+ * F > K or n0 < 2, a full table (n0 + F*K > ldc), a null or misaligned
+ * pointer, or one the device cannot address; SV_ERR_UNSUPPORTED for K > 16,
+ * ldc > 2048 or V above SV_MAX_VOCAB.  B = 0 returns SV_OK with no launch. */
 sv_status sv_tree_level(const void *dlogits, sv_dtype dt, int B, int F, int V,
                         float temperature, int K, int level, int n0, int ldc,
                         int32_t *frontier, int32_t *cand_parent, int32_t *cand_token,
