@@ -1,6 +1,6 @@
 """Host logic of the benchmark that needs no GPU: the clock record (samples
 kept to the timed region, throttle reasons), the early-exit byte accounting,
-and the default step counts of the two arms."""
+the default step counts of the two arms, and the reference arm's line."""
 import datetime
 import os
 import sys
@@ -75,3 +75,29 @@ def test_default_steps_per_arm(monkeypatch):
     seen.pop("ours")
     bench.main()
     assert seen == {"ref": 20, "ours": 7}
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """The reference arm (the CPU oracle) on the small chain: one JSON line
+    with the keys of the benchmark contract, its own cpu_baseline and an e2e
+    with no host-device traffic."""
+    import json
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--config", "1",
+                                      "--steps", "2", "--warmup", "1", "--cpu-sample", "2"])
+    bench.main()
+    out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(out) == 1
+    line = json.loads(out[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["value"] > 0 and line["unit"] == "rows/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"].startswith("config 1")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
