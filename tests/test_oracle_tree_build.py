@@ -152,5 +152,9 @@ def test_kept_tree_has_the_largest_total_score(seed):
                 best = max(best, sum(float(cs[b, c]) for c in s))
         got = sum(float(v) for v in score[b])
         assert np.isclose(got, best, rtol=1e-12, atol=0), (b, got, best)
+        # a plausible wrong rule, keeping breadth-first (level, then score),
+        # is ancestor-closed too but falls short: the pin tells them apart
+        bfs = sorted([0] + valid, key=lambda c: (cl[b, c], -cs[b, c], c))[:Tn]
+        assert sum(float(cs[b, c]) for c in bfs) < best - 1e-9
         # and the kept nodes form a tree with parents before children
         assert parent[b, 0] == -1 and all(0 <= parent[b, i] < i for i in range(1, Tn))
