@@ -660,10 +660,10 @@ void orc_tree_mask(const int32_t *parent, int B, int T, uint64_t *mask,
  * [L][2][B][S][H][D] of elem_bytes each.  For every sequence, layer and K/V:
  * dst row dst_base+k <- src row src_base+rows[k], k < n_rows, all reads
  * before any write.  kv_len = dst_base + n_rows, or -1 (nothing moved) when a
- * row is out of range, n_rows is out of [0, P] or above 4096 (the library's
- * per-call row limit), or an in-place call (src ==
+ * row is out of range, n_rows is out of [0, P], or an in-place call (src ==
  * dst) has dst_base != src_base or rows not strictly increasing with
- * rows[k] >= k.
+ * rows[k] >= k.  The pages put no bound on the number of rows kept, and
+ * neither does this definition.
  * ---------------------------------------------------------------------- */
 void orc_kv_compact(const uint8_t *src, uint8_t *dst, int L, int B, int S_src,
                     int S_dst, int H, int D, int elem_bytes,
@@ -675,7 +675,7 @@ void orc_kv_compact(const uint8_t *src, uint8_t *dst, int L, int B, int S_src,
   uint8_t *tmp = (uint8_t *)malloc(rb * (size_t)(P > 0 ? P : 1));
   for (int b = 0; b < B; ++b) {
     int n = n_rows[b];
-    int ok = (n >= 0 && n <= P && n <= 4096 && src_base[b] >= 0 && dst_base[b] >= 0 &&
+    int ok = (n >= 0 && n <= P && src_base[b] >= 0 && dst_base[b] >= 0 &&
               dst_base[b] + n <= S_dst);
     if (inplace && src_base[b] != dst_base[b]) ok = 0;
     for (int k = 0; ok && k < n; ++k) {

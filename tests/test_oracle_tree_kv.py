@@ -177,6 +177,22 @@ def test_kv_compact_gather_matches_numpy():
         assert np.array_equal(work[:, :, b, :base[b]], kv[:, :, b, :base[b]])
 
 
+def test_kv_compact_has_no_row_limit():
+    # [Lesson] "Reversão de KV cache" / Passo 4 bound nothing but the buffer:
+    # a request for more rows than any kernel limit is still copied
+    rng = np.random.default_rng(8)
+    L, B, S, H, D, n = 1, 2, 5000, 1, 4, 4999
+    src = rng.integers(0, 256, (L, 2, B, S, H, D * 2), dtype=np.uint8)
+    dst = rng.integers(0, 256, (L, 2, B, S, H, D * 2), dtype=np.uint8)
+    rows = np.stack([np.sort(rng.choice(S, n, replace=False)).astype(np.int32) for _ in range(B)])
+    nn = np.array([n, 4097], np.int32)
+    z = np.zeros(B, np.int32)
+    want = _kv_numpy(src, dst, z, z, rows, nn)
+    kl = oracle.kv_compact(src, dst, L, B, S, S, H, D, 2, z, z, rows, nn)
+    assert kl.tolist() == [n, 4097]
+    assert np.array_equal(dst, want)
+
+
 def test_kv_exercise4_two_sequences_rollback_and_commit():
     # sequence A accepts every draft, sequence B rejects at position 2
     L, B, S, H, D, N, base = 2, 2, 64, 2, 64, 4, 32
