@@ -89,6 +89,9 @@ def _declare(L):
     L.orc_sample_repro.argtypes = [_f32p, C.c_void_p, C.c_int, C.c_float, C.c_uint32,
                                    C.POINTER(C.c_double), C.POINTER(C.c_int)]
     L.orc_sample_repro.restype = C.c_int
+    L.orc_sample_repro_many.argtypes = [_f32p, C.c_void_p, C.c_int, C.c_float, _u32p, C.c_int,
+                                        _i32p, _f64p, C.POINTER(C.c_int)]
+    L.orc_sample_repro_many.restype = C.c_int
     L.orc_verify.argtypes = [
         _f32p, C.c_int64, _f32p, C.c_int64, C.c_int, C.c_int, C.c_float,
         C.c_void_p, C.c_int, _i32p, _i32p, C.c_int, C.c_uint64, C.c_uint64,
@@ -230,6 +233,23 @@ def sample_repro(xq, xp, u24_, T=1.0):
         k = lib().orc_sample_repro(xq, None, xq.size, float(invT), u24_,
                                    C.byref(gap), C.byref(rz))
     return int(k), gap.value, bool(rz.value)
+
+
+def sample_repro_many(xq, xp, u24s, T=1.0):
+    """Many draws on one row (pair) in the kernel arithmetic: the weights are
+    formed once.  Returns (tokens [n], gaps [n], resid_zero)."""
+    xq = _f32(xq)
+    u = np.ascontiguousarray(u24s, np.uint32)
+    invT = np.float32(np.float32(1.0) / np.float32(T))
+    tok = np.empty(u.size, np.int32)
+    gaps = np.empty(u.size, np.float64)
+    rz = C.c_int()
+    keep = _f32(xp) if xp is not None else None  # holds the buffer during the call
+    xpp = keep.ctypes.data if keep is not None else None
+    rc = lib().orc_sample_repro_many(xq, xpp, xq.size, float(invT), u, u.size, tok, gaps,
+                                     C.byref(rz))
+    assert rc == 0
+    return tok, gaps, bool(rz.value)
 
 
 # ---------------------------------------------------------------- verify

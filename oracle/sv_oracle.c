@@ -175,13 +175,20 @@ int orc_invcdf_f64(const double *w, int V, double t) {
  *   z_v   = fl32(x_v * invT),     invT = fl32(1 / T)
  *   m     = max_v z_v             (exact)
  *   e_v   = exp32(z_v - m)        (fl32 subtraction, then exp32 below)
- *   S_e   = sum_v floor(e_v * 2^40)                     (exact uint64)
- *   inv_s = fl32( 2^40 / fl64(S_e) )                    (fl64 divide)
- *   q_v   = fl32(e_v * inv_s)
- *   w_v   = max(0, fl32(q_v - p_v))   residual   |   w_v = q_v   bonus
- *   W_v   = floor(w_v * 2^62);  S_W = sum_v W_v         (exact uint64)
- *   if S_W == 0 (residual with q == p): W_v = floor(q_v * 2^62)
- *   t     = floor(u24 * S_W / 2^24)                     (exact, 128-bit)
+ *   E_v   = floor(e_v * 2^40);  S_E = sum_v E_v         (exact uint64)
+ *
+ * A draw from q -- the bonus token from q_{N+1} ([Lesson] "O invariante"),
+ * or the correction when the residual mass is zero ([Lesson] Passo 2) --
+ * takes the weights W_v = E_v, S = S_E: q_v = e_v / sum e, and E_v is e_v
+ * on a 2^-40 grid, so these weights are q up to that truncation.
+ *
+ * A residual draw at a rejection ([Lesson] Passo 2) normalises both rows:
+ *   inv_s = fl32( 2^40 / fl64(S_E) )                    (per row, fl64 divide)
+ *   q_v   = fl32(e_v * inv_s),  p_v likewise from the draft row
+ *   w_v   = max(0, fl32(q_v - p_v));  W_v = floor(w_v * 2^62);  S = sum_v W_v
+ *   if S == 0 (q == p to the last bit): the draw from q above
+ *
+ *   t     = floor(u24 * S / 2^24)                       (exact, 128-bit)
  *   token = min { k : sum_{v<=k} W_v > t }
  *
  * exp32(a): 0 if a < -80; else n = rint(a*log2e) via the 1.5*2^23 shift,
@@ -224,64 +231,92 @@ static float orc_zmax32(const float *x, int V, float invT) {
   return m;
 }
 
-static float orc_inv_sum32(const float *x, int V, float invT, float m) {
+/* E_v = floor(exp32(fl32(x_v * invT) - m) * 2^40) of one row; returns S_E */
+static uint64_t orc_fixed_exp40(const float *x, int V, float invT, float m, uint64_t *E) {
   uint64_t se = 0;
   for (int v = 0; v < V; ++v) {
     float e = orc_exp32(x[v] * invT - m);
-    se += (uint64_t)(e * 0x1p40f);
+    E[v] = (uint64_t)(e * 0x1p40f);
+    se += E[v];
   }
-  return (float)(0x1p40 / (double)se);
+  return se;
 }
 
-/* Residual (xp != NULL) or bonus (xp == NULL) sample in the arithmetic
- * above.  Returns the token; *gap gets min(t - C_{k-1}, C_k - 1 - t) / S_W and
- * *resid_zero is set when the residual mass was zero and q was used. */
-int orc_sample_repro(const float *xq, const float *xp, int V, float invT,
-                     uint32_t u24, double *gap, int *resid_zero) {
-  float mq = orc_zmax32(xq, V, invT);
-  float iq = orc_inv_sum32(xq, V, invT, mq);
-  float mp = 0.0f, ip = 0.0f;
-  if (xp) {
-    mp = orc_zmax32(xp, V, invT);
-    ip = orc_inv_sum32(xp, V, invT, mp);
-  }
-  uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
-  uint64_t S = 0;
-  int use_q = (xp == NULL);
+static float orc_inv_sum(uint64_t se) { return (float)(0x1p40 / (double)se); }
+
+/* The weights W_v and their sum S of a residual (xp != NULL) or a draw from q
+ * (xp == NULL), as specified above.  *resid_zero is set when a residual had
+ * zero mass and q was used. */
+static uint64_t orc_sample_weights(const float *xq, const float *xp, int V, float invT,
+                                   uint64_t *W, int *resid_zero) {
   *resid_zero = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    S = 0;
-    for (int v = 0; v < V; ++v) {
-      float q = orc_exp32(xq[v] * invT - mq) * iq;
-      float w;
-      if (use_q) {
-        w = q;
-      } else {
-        float p = orc_exp32(xp[v] * invT - mp) * ip;
-        float d = q - p;
-        w = d > 0.0f ? d : 0.0f;
-      }
-      W[v] = (uint64_t)(w * 0x1p62f);
-      S += W[v];
-    }
-    if (S != 0 || use_q) break;
-    use_q = 1; /* residual mass zero: fall back to q ([Lesson] Passo 2) */
-    *resid_zero = 1;
-  }
-  uint64_t t = (uint64_t)(((unsigned __int128)u24 * (unsigned __int128)S) >> 24);
-  uint64_t c = 0;
-  int k = -1;
+  float mq = orc_zmax32(xq, V, invT);
+  uint64_t se_q = orc_fixed_exp40(xq, V, invT, mq, W);
+  if (!xp) return se_q;
+  float iq = orc_inv_sum(se_q);
+  float mp = orc_zmax32(xp, V, invT);
+  uint64_t *Ep = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)V);
+  float ip = orc_inv_sum(orc_fixed_exp40(xp, V, invT, mp, Ep));
+  free(Ep);
+  uint64_t *R = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)V);
+  uint64_t S = 0;
   for (int v = 0; v < V; ++v) {
-    uint64_t prev = c;
-    c += W[v];
-    if (c > t) {
-      uint64_t below = t - prev, above = c - 1 - t;
-      *gap = (double)(below < above ? below : above) / (double)S;
-      k = v;
-      break;
-    }
+    float q = orc_exp32(xq[v] * invT - mq) * iq;
+    float p = orc_exp32(xp[v] * invT - mp) * ip;
+    float d = q - p;
+    R[v] = (uint64_t)((d > 0.0f ? d : 0.0f) * 0x1p62f);
+    S += R[v];
+  }
+  if (S != 0) memcpy(W, R, sizeof(uint64_t) * (size_t)V);
+  free(R);
+  if (S == 0) { /* residual mass zero: fall back to q ([Lesson] Passo 2) */
+    *resid_zero = 1;
+    return se_q;
+  }
+  return S;
+}
+
+/* The token of uniform u24 over weights W (cumulative sums C, total S):
+ * the smallest k with C_k > t, t = floor(u24 S / 2^24); *gap gets
+ * min(t - C_{k-1}, C_k - 1 - t) / S, the distance to the nearer boundary. */
+static int orc_pick(const uint64_t *C, int V, uint64_t S, uint32_t u24, double *gap) {
+  uint64_t t = (uint64_t)(((unsigned __int128)u24 * (unsigned __int128)S) >> 24);
+  int lo = 0, hi = V - 1; /* C[V-1] = S > t, so the answer exists */
+  while (lo < hi) {
+    int mid = lo + (hi - lo) / 2;
+    if (C[mid] > t) hi = mid;
+    else lo = mid + 1;
+  }
+  uint64_t prev = lo ? C[lo - 1] : 0;
+  uint64_t below = t - prev, above = C[lo] - 1 - t;
+  *gap = (double)(below < above ? below : above) / (double)S;
+  return lo;
+}
+
+/* n draws on one row (pair): tokens[i] for uniform u24[i].  Returns 0, or -1
+ * when V < 1. */
+int orc_sample_repro_many(const float *xq, const float *xp, int V, float invT,
+                          const uint32_t *u24, int n, int32_t *tokens, double *gaps,
+                          int *resid_zero) {
+  if (V < 1) return -1;
+  uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)V);
+  uint64_t S = orc_sample_weights(xq, xp, V, invT, W, resid_zero);
+  for (int v = 1; v < V; ++v) W[v] += W[v - 1]; /* cumulative sums in place */
+  for (int i = 0; i < n; ++i) {
+    double g;
+    tokens[i] = orc_pick(W, V, S, u24[i], &g);
+    if (gaps) gaps[i] = g;
   }
   free(W);
+  return 0;
+}
+
+/* One draw: residual (xp != NULL) or from q (xp == NULL).  Returns the token;
+ * *gap and *resid_zero as above. */
+int orc_sample_repro(const float *xq, const float *xp, int V, float invT,
+                     uint32_t u24, double *gap, int *resid_zero) {
+  int32_t k = -1;
+  orc_sample_repro_many(xq, xp, V, invT, &u24, 1, &k, gap, resid_zero);
   return k;
 }
 
