@@ -73,7 +73,7 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_ROW_P_ZERO 8u     /* a tested draft token had p(d) = 0 (draft logit -inf) and was accepted */
 #define SV_ROW_BAD_TREE 16u  /* parent/score arrays do not describe a tree */
 #define SV_ROW_BAD_BASE 32u  /* sv_tree_attention: base < 0 or base + T > S */
-#define SV_ROW_TIMEOUT 64u   /* sv_tree_attention: a wait on the device ran out */
+#define SV_ROW_TIMEOUT 64u   /* a bounded wait on the device ran out (attention, sampling) */
 
 /* Build limits. */
 #define SV_MAX_VOCAB (1 << 22)  /* fixed-point sampling sums stay below 2^63 */
@@ -118,9 +118,15 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *                  nearest CDF boundary, as a fraction of the sampled mass.
  *   out_status     [B]       SV_ROW_* bits.  On NAN / BAD_TOKEN the sequence
  *                  emits nothing: accept_len 0, tokens all -1.
- * The correction/bonus choice uses exact 64-bit fixed-point prefix sums of an
- * fp32 distribution computed with a fixed sequence of IEEE operations, so the
- * chosen token does not depend on how the sum is split across threads.
+ * The correction/bonus choice uses exact 64-bit fixed-point prefix sums of
+ * weights computed with a fixed sequence of IEEE fp32 operations, so the
+ * chosen token does not depend on how the sum is split across threads: a
+ * draw from q (the bonus, or a zero residual) takes the weights
+ * floor(e_v 2^40), e_v = exp(x_v / T - max_v x_v / T) in that arithmetic; a
+ * residual takes floor(max(0, q_v - p_v) 2^62) with q, p normalised by those
+ * sums.  The sampler's device waits are bounded; one that runs out (which a
+ * working device never does) sets SV_ROW_TIMEOUT for the sequence and leaves
+ * its correction/bonus token at -1.
  * --------------------------------------------------------------------------- */
 size_t sv_verify_chain_workspace(int B, int N, int V);
 /* A larger workspace for logits in page-locked host memory: with it, every
@@ -260,10 +266,14 @@ sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int B,
  * synchronise the device.  Such callers still pass every input and output.
  *
  * Scratch comes from one file-scope static device array of
- * sv_verify_chain_noalloc_max_bytes() bytes (4 MiB), which every GPU that
- * loads this library keeps until the process exits.  A call whose
- * sv_verify_chain_workspace(B, N, V) exceeds it returns SV_ERR_UNSUPPORTED
- * with a message and enqueues nothing.  The first call on a device looks up
+ * sv_verify_chain_noalloc_max_bytes() bytes (16 MiB), which every GPU that
+ * loads this library keeps until the process exits.  It holds the workspace
+ * of any call with sv_verify_chain_workspace(B, N, V) <= 16 MiB: for example
+ * B = 256, N = 7, V = 128256 (about 9.6 MB), or up to B = 447 at that N and
+ * V.
+ * The argument checks of sv_verify_chain come first, in its order; then a
+ * call whose workspace exceeds the array returns SV_ERR_UNSUPPORTED with a
+ * message and enqueues nothing.  The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture.  Nothing here
  * calls cudaMalloc, cudaFree or any allocating routine.

@@ -134,6 +134,10 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
+// every group but the most recently committed one has completed
+__device__ __forceinline__ void cp_async_wait_1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
@@ -144,7 +148,11 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
 }
 
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic): two IEEE round-to-nearest
-// operations per instruction, bit-identical to the scalar ones.
+// operations per instruction, bit-identical to the scalar ones.  A packed
+// multiply feeding a packed add or subtract has been seen contracted into a
+// fused multiply-add despite the explicit rounding modifier; where each
+// rounding is part of a specification, the products go through the scalar
+// __fmul_rn intrinsic instead.
 __device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -230,9 +238,13 @@ __device__ __forceinline__ float exp32_repro(float a) {
   return (a >= -80.0f) ? e : 0.0f;
 }
 
-// exp32_repro of both lanes of a packed pair, bit for bit: the same fp32
-// operations as packed pair instructions (fused multiply-adds and one
-// subtraction; no multiply feeds an addition, so none can be contracted).
+// exp32_repro of both lanes of a packed pair: the same fp32 operations as
+// packed pair instructions (fused multiply-adds and one subtraction; no
+// multiply feeds an addition, so none can be contracted), bit for bit equal
+// to exp32_repro for a >= -80.  Below -80 the argument is clamped to -80, so
+// the result is exp32_repro(-80) (about 1.8e-35) instead of 0: both are 0
+// once floored onto the 2^-40 or 2^-62 grid of the sampling weights, and a
+// product or difference with a value of at least 2^-62 rounds the same way.
 __device__ __forceinline__ unsigned long long f2_add_rz(unsigned long long a,
                                                         unsigned long long b) {
   unsigned long long r;
@@ -241,6 +253,9 @@ __device__ __forceinline__ unsigned long long f2_add_rz(unsigned long long a,
 }
 __device__ __forceinline__ unsigned long long f2_splat(float a) { return f2_pack(a, a); }
 __device__ __forceinline__ unsigned long long exp32x2(unsigned long long a2) {
+  float a0, a1;
+  f2_unpack(a2, a0, a1);
+  a2 = f2_pack(fmaxf(a0, -80.0f), fmaxf(a1, -80.0f));
   const unsigned long long t2 = f2_fma(a2, f2_splat(0x1.715476p+0f), f2_splat(0x1.8p+23f));
   const unsigned long long n2 = f2_sub(t2, f2_splat(0x1.8p+23f));
   unsigned long long r2 = f2_fma(n2, f2_splat(-0x1.62e4p-1f), a2);
@@ -252,13 +267,14 @@ __device__ __forceinline__ unsigned long long exp32x2(unsigned long long a2) {
   p2 = f2_fma(p2, r2, f2_splat(0.5f));
   p2 = f2_fma(p2, r2, f2_splat(1.0f));
   p2 = f2_fma(p2, r2, f2_splat(1.0f));
-  float t0, t1, q0, q1, a0, a1;
+  float t0, t1, q0, q1;
   f2_unpack(t2, t0, t1);
   f2_unpack(p2, q0, q1);
-  f2_unpack(a2, a0, a1);
-  const float e0 = __int_as_float(__float_as_int(q0) + ((__float_as_int(t0) - 0x4B400000) << 23));
-  const float e1 = __int_as_float(__float_as_int(q1) + ((__float_as_int(t1) - 0x4B400000) << 23));
-  return f2_pack(a0 >= -80.0f ? e0 : 0.0f, a1 >= -80.0f ? e1 : 0.0f);
+  // t = 1.5 2^23 + n, whose bits are 0x4B400000 + n; shifted left by 23 the
+  // constant leaves the 32-bit word, so (t bits << 23) adds n to p's exponent
+  const float e0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  const float e1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
+  return f2_pack(e0, e1);
 }
 
 }  // namespace sv

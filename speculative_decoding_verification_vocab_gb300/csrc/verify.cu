@@ -7,16 +7,17 @@
 //                streams the whole input; HBM-bound
 //   decide       one warp per sequence: q(d)/p(d), Philox uniforms, the left-
 //                to-right accept walk, outputs, and the sampling task
-//   sample_norm  exact fixed-point normaliser partials of the 1-2 sampled rows;
-//                the last slice CTA of a sequence turns them into 1/S_e
-//   sample_mass  fixed-point residual / bonus masses per slice and per run;
-//                the last slice CTA of a sequence does the inverse-CDF pick
+//   sample       the correction / bonus draws: exact fixed-point weights of
+//                the sampled row(s) of every sequence and the inverse-CDF
+//                pick, one persistent kernel over (sequence, slice) items
 //
 // Pages: "Decodificação Especulativa e EAGLE-3" (lesson; "O invariante",
 // Passo 1-3) and "投机解码发展" (blog; section 2 steps, section 4 spec_decode /
 // eagle_round pseudocode).  p = draft, q = verifier.
 #include <math.h>
 #include <stdio.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "rowstat.cuh"
@@ -26,12 +27,7 @@ namespace sv {
 namespace {
 
 constexpr int kDecideWarps = 4;
-// sampler geometry: a CTA owns a 4096-element slice of a row; each of its
-// threads owns kSpRun consecutive elements of the slice
-constexpr int kSpThreads = 128;
-constexpr int kSpWarps = kSpThreads / 32;
-constexpr int kSpRun = 32;
-constexpr int kSpSlice = kSpThreads * kSpRun;  // 4096 elements per CTA
+constexpr int kSpSlice = 4096;  // sampler: elements of a row per work item
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Task {
@@ -45,8 +41,8 @@ struct Task {
 };
 
 struct Layout {
-  int maxpos, P, G, CS;
-  size_t ctr, rowlist, partial, task, norm, mass, run, done, inv, path, npos, tok, tstat;
+  int maxpos, P, G, NS;
+  size_t ctr, rowlist, partial, task, slice, runs, done, rlist, qc, path, npos, tok, tstat;
   size_t ee;     // early exit (chain): [B][maxpos] position counts, then [B] stop
   size_t end;    // end of the regions (256-aligned); an optional row copy follows
   size_t total;  // bytes to request: the regions plus base-pointer alignment
@@ -243,8 +239,11 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
 template <typename E, bool kCopy>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
-                 const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+                 const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
+                 unsigned *__restrict__ qc) {
   grid_dep_sync();
+  // the sampler's lists and item counter are rebuilt by the accept walk
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 3) qc[threadIdx.x] = 0u;
   // chain: one row per CTA (exact grid); tree: the grid covers half the row
   // slots and a CTA takes a second listed row when the paths are deep
   const int nrows = rowlist ? *rowcount : (int)gridDim.x;
@@ -268,12 +267,12 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   L.rowlist = tree ? take(sizeof(int32_t) * nslots) : 0;
   L.partial = take(sizeof(float4) * nslots * L.G);
   L.task = take(sizeof(Task) * (size_t)B);
-  L.CS = (V + kSpSlice - 1) / kSpSlice;
-  L.norm = take(sizeof(ulonglong2) * (size_t)B * L.CS);
-  L.mass = take(sizeof(unsigned long long) * (size_t)B * L.CS);
-  L.run = take(sizeof(unsigned long long) * (size_t)B * L.CS * kSpThreads);
+  L.NS = (V + kSpSlice - 1) / kSpSlice;
+  L.slice = take(sizeof(unsigned long long) * 3 * (size_t)B * L.NS);
+  L.runs = take(sizeof(unsigned long long) * (size_t)B * L.NS * 128);
   L.done = take(sizeof(unsigned) * 2 * (size_t)B);
-  L.inv = take(sizeof(float2) * (size_t)B);
+  L.rlist = take(sizeof(int) * 2 * (size_t)B);
+  L.qc = take(sizeof(unsigned) * 4);
   L.ee = take(sizeof(int) * (size_t)B * (maxpos + 1));
   if (tree) {
     L.path = take(sizeof(int32_t) * (size_t)B * (maxpos + 1));
@@ -382,8 +381,8 @@ __device__ __forceinline__ Judged judge_position(const Round &r, int G, const fl
 template <typename E, bool kEarly>
 __global__ void __launch_bounds__(kDecideWarps * 32)
 decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
-              uint64_t step, DecideOut o, Task *__restrict__ tasks,
-              unsigned *__restrict__ done) {
+              uint64_t step, DecideOut o, Task *__restrict__ tasks, int *__restrict__ lists,
+              unsigned *__restrict__ qc, unsigned *__restrict__ done) {
   grid_dep_sync();
   const int b = blockIdx.x * kDecideWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -494,8 +493,15 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     t.mp = (!bad && a < npos) ? mxd[a] : 0.0f;
     t.u24 = bad ? 0u : usm[vi];
     tasks[b] = t;
-    done[b] = 0u;        // the sampler's per-sequence completion counts:
-    done[r.B + b] = 0u;  // slice CTAs of sample_mass, of sample_norm
+    // the sampler's lists: residual draws, then bonus draws; its counts
+    if (t.active) {
+      if (a < npos)
+        lists[atomicAdd(qc, 1u)] = b;
+      else
+        lists[r.B + atomicAdd(qc + 1, 1u)] = b;
+    }
+    done[b] = 0u;
+    done[r.B + b] = 0u;
   }
 }
 
@@ -517,8 +523,11 @@ constexpr unsigned kEeInit = 0x7F7F7F7Fu;  // counts and stop[] start here (byte
 template <typename E, bool kCopy>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_stats_ee_kernel(Round r, int G, float4 *__restrict__ partial, unsigned *__restrict__ count,
-                    int *__restrict__ stop, uint64_t seed, uint64_t step) {
+                    int *__restrict__ stop, uint64_t seed, uint64_t step,
+                    unsigned *__restrict__ qc) {
   grid_dep_sync();
+  // the sampler's lists and item counter are rebuilt by the accept walk
+  if (blockIdx.x == 0 && threadIdx.x < 3) qc[threadIdx.x] = 0u;
   const int N = r.maxpos;
   const long long wave = 2LL * r.B * G;  // CTAs per drafted position
   const long long x = blockIdx.x;
@@ -786,114 +795,126 @@ decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideO
 // ---------------------------------------------------------------------------
 // The sampling arithmetic (fixed sequence of IEEE fp32 operations + exact
 // 64-bit fixed point), shared by specification with the CPU oracle:
-//   z = fl(x * invT); e = exp32_repro(fl(z - max z)); S_e = sum floor(e 2^40)
-//   inv_s = fl32(2^40 / fl64(S_e)); q = fl(e * inv_s)
-//   w = max(0, fl(q - p)) (residual) or q (bonus); W = floor(w 2^62)
-//   t = floor(u24 * sum W / 2^24); token = min{k : sum_{v<=k} W_v > t}
-// Only scalar _rn intrinsics are used where a product feeds a sum, so no
-// multiply can be fused into a later add.
+//   z = fl(x * invT); e = exp32_repro(fl(z - max z)); E = floor(e 2^40)
+//   a draw from q (bonus; zero residual): weights E, S = sum E
+//   a residual draw: inv_s = fl32(2^40 / fl64(sum E)) per row, q = fl(e inv_s),
+//     p likewise, w = max(0, fl(q - p)), weights W = floor(w 2^62), S = sum W
+//   t = floor(u24 * S / 2^24); token = min{k : sum_{v<=k} weight_v > t}
+// Only scalar or packed _rn operations are used where a product feeds a sum,
+// so no multiply can be fused into a later add.
 //
-// Exact sums without 64-bit conversions (slow on this GPU): a value v in
-// [0, 1] splits exactly into parts on fixed grids -- a = v truncated to a
-// multiple of 2^-16 (an add rounding toward zero onto 2^7, minus 2^7), then
-// the remainder truncated to 2^-32, and so on.  Parts of up to 128 values sum
-// exactly in fp32 (each part fits 17 bits, 7 more bits of headroom); the
-// per-thread part sums become integers once and meet in uint64.  The result is
-// sum floor(v 2^40) (three parts) or sum floor(v 2^62) (four parts) exactly.
+// Exact sums without 64-bit conversions: a value v in [0, 1] splits exactly
+// into parts on fixed grids, each part truncated by one add rounding toward
+// zero onto a power of two and one subtraction of it:
+//   E (2^-40 grid): a on 2^-20 (21 bits), then the remainder on 2^-40
+//                   (20 bits); up to 16 values per part sum exactly in fp32;
+//   W (2^-62 grid): parts on 2^-21, 2^-42 and 2^-62; up to 8 values per part.
+// The part sums become integers once per 16 (8) values and meet in uint64, so
+// sum floor(v 2^40) and sum floor(v 2^62) are exact whatever the order.  The
+// sums stay below 2^63: sum E <= V 2^40 with V <= 2^22, and sum W <= 2^62
+// (1 + 2^-20) because the normalised q row sums to 1 up to rounding.
 //
-// Two kernels per round.  A CTA owns one kSpSlice-element slice of one
-// sequence's q row (and p row for a residual); thread t owns the kSpRun
-// consecutive elements [t * kSpRun, (t + 1) * kSpRun) of the slice:
-//   sample_norm  partial sums of floor(e 2^40) of the slice; the CTA that
-//                completes a sequence's slices last (a per-sequence count)
-//                computes 1/S_e of the q and p rows once
-//   sample_mass  W of every element; the sum of each thread's run is stored
-//                (the prefix search's blocks)
-// Both evaluate the exponentials and the splits on packed fp32 pairs: the q
-// and p element of one position (residual), or two neighbouring q elements
-// (bonus), one per lane.
-//   (pick)       in the CTA that finishes a sequence's masses last, one warp:
-//                the threshold, the slice, the run, then a warp scan of the
-//                run's 32 elements
+// One persistent kernel.  Its work items are (sequence, slice) pairs, a slice
+// being kSpSlice consecutive elements of the sampled row(s); consumer thread t
+// owns the run of 32 consecutive elements [32 t, 32 t + 32) of a slice.  A CTA
+// is one producer warp and four consumer warps around a two-stage ring in
+// shared memory:
+//   producer   claims the next item from a counter, reads its sequence's
+//              task, issues asynchronous 16-byte copies of the slice of each
+//              row into the free stage (word k of consumer thread t at slot
+//              k * 128 + t, so consumer reads are conflict-free), and signals
+//              the stage's "full" barrier when the copies land
+//   consumers  wait for a full stage, compute the item, release the stage
+//              ("empty" barrier), store the sums, and pick a token when the
+//              item completed its sequence
+// Items are claimed in this order:
+//   pass 1, residual draws  exact sums of E over the slice of the q and the p
+//                           row (the accept walk lists these sequences)
+//   pass 1, bonus draws     the run sums of E of the q row, stored
+//   pass 2, residual draws  the run sums of W, stored, with both rows' 1/S
+//                           formed by the producer from the pass-1 sums
+// Each item ends with its slice sums and a per-sequence completion count; the
+// CTA that completes a sequence's last pass picks its token: the slice holding
+// the threshold (slice sums), the run (stored run sums), then one lane per
+// element of the run.  A pass-2 item needs its sequence's pass 1 complete;
+// every pass-1 item is claimed before any pass-2 item and pass-1 items never
+// wait, so that wait always ends.  Every wait (barriers, the pass-1 count) is
+// bounded by a wall-clock limit; one that runs out sets SV_ROW_TIMEOUT for
+// the sequence concerned and the CTA stops taking items.
 
-struct Parts40 {
-  float a, b, c;  // multiples of 2^-16, 2^-32, 2^-40
-};
-struct Parts62 {
-  float a, b, c, d;  // multiples of 2^-16, 2^-32, 2^-48, 2^-62
-};
-__device__ __forceinline__ unsigned long long fix_of(const Parts40 &P) {
-  return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 24) +
-         (unsigned long long)__float2uint_rn(__fmul_rn(P.b, 0x1p32f)) * (1ull << 8) +
-         (unsigned long long)__float2uint_rn(__fmul_rn(P.c, 0x1p40f));
-}
-__device__ __forceinline__ unsigned long long fix_of(const Parts62 &P) {
-  return (unsigned long long)__float2uint_rn(__fmul_rn(P.a, 0x1p16f)) * (1ull << 46) +
-         (unsigned long long)__float2uint_rn(__fmul_rn(P.b, 0x1p32f)) * (1ull << 30) +
-         (unsigned long long)__float2uint_rn(__fmul_rn(P.c, 0x1p48f)) * (1ull << 14) +
-         (unsigned long long)__float2uint_rn(__fmul_rn(P.d, 0x1p62f));
-}
-// single values (the final scan only)
-__device__ __forceinline__ unsigned long long fix62(float w) {
-  return __float2ull_rz(__fmul_rn(w, 0x1p62f));
-}
+constexpr int kSpThreads = 128;  // consumer threads (the producer warp is extra)
+constexpr int kSpWarps = kSpThreads / 32;
+template <typename E>
+__host__ __device__ constexpr int sp_per() { return 16 / (int)sizeof(E); }  // elements per word
+template <typename E>
+__host__ __device__ constexpr int sp_words() { return kSpSlice / sp_per<E>(); }  // words per slice
+template <typename E>
+__host__ __device__ constexpr int sp_wpt() { return sp_words<E>() / kSpThreads; }  // words per thread
+// shared memory of one stage: q and p words of the slice
+template <typename E>
+__host__ __device__ constexpr size_t sp_stage_bytes() { return 2 * (size_t)sp_words<E>() * 16; }
+
 __device__ __forceinline__ float inv_sum(unsigned long long se) {
   return __double2float_rn(__ddiv_rn(0x1p40, __ull2double_rn(se)));
 }
+__device__ __forceinline__ unsigned long long fix62(float w) {
+  return __float2ull_rz(__fmul_rn(w, 0x1p62f));
+}
+__device__ __forceinline__ unsigned long long fix40(float e) {
+  return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+}
 
-// A thread's run of kSpRun consecutive logits of one row, kept as the raw
-// 16-byte words (bf16 pairs or fp32) and converted element by element when
-// used.  Elements past the row's end read as -inf, whose exponential is 0.
-template <typename E>
-struct Run;
-template <>
-struct Run<uint16_t> {
-  uint4 w[kSpRun / 8];
-  __device__ __forceinline__ float operator[](int j) const {
-    const uint4 &q = w[j >> 3];
-    const int c = (j >> 1) & 3;
-    const uint32_t x = c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
-    return (j & 1) ? bf16_hi(x) : bf16_lo(x);
-  }
+__device__ __forceinline__ unsigned long long trunc2(unsigned long long v, float grid_top) {
+  const unsigned long long g = f2_splat(grid_top);
+  return f2_sub(f2_add_rz(v, g), g);
+}
+// E parts of a packed pair (<= 16 values per lane between conversions)
+struct Acc40 {
+  unsigned long long a, b;
 };
-template <>
-struct Run<float> {
-  uint4 w[kSpRun / 4];
-  __device__ __forceinline__ float operator[](int j) const {
-    const uint4 &q = w[j >> 2];
-    const int c = j & 3;
-    return __uint_as_float(c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w);
-  }
+__device__ __forceinline__ void acc40(Acc40 &P, unsigned long long e) {
+  const unsigned long long a = trunc2(e, 0x1p3f);     // 2^-20 grid
+  const unsigned long long b = trunc2(f2_sub(e, a), 0x1p-17f);  // 2^-40 grid
+  P.a = f2_add(P.a, a);
+  P.b = f2_add(P.b, b);
+}
+// adds both lanes' exact sums to s0 / s1 and clears the parts
+__device__ __forceinline__ void drain40(Acc40 &P, unsigned long long &s0, unsigned long long &s1) {
+  float a0, a1, b0, b1;
+  f2_unpack(P.a, a0, a1);
+  f2_unpack(P.b, b0, b1);
+  s0 += ((unsigned long long)__float2uint_rn(__fmul_rn(a0, 0x1p20f)) << 20) +
+        __float2uint_rn(__fmul_rn(b0, 0x1p40f));
+  s1 += ((unsigned long long)__float2uint_rn(__fmul_rn(a1, 0x1p20f)) << 20) +
+        __float2uint_rn(__fmul_rn(b1, 0x1p40f));
+  P.a = P.b = 0ull;
+}
+// W parts of a packed pair (<= 8 values per lane between conversions)
+struct Acc62 {
+  unsigned long long a, b, c;
 };
-
-template <typename E>
-__device__ __forceinline__ void load_run(Run<E> &run, const E *row, int v, int V, bool vec) {
-  constexpr int kPer = 16 / sizeof(E);  // elements per word
-  if (vec && v + kSpRun <= V) {
-    const uint4 *p = (const uint4 *)(row + v);
+__device__ __forceinline__ void acc62(Acc62 &P, unsigned long long w) {
+  const unsigned long long a = trunc2(w, 0x1p2f);     // 2^-21 grid
+  const unsigned long long r1 = f2_sub(w, a);
+  const unsigned long long b = trunc2(r1, 0x1p-19f);  // 2^-42 grid
+  const unsigned long long c = trunc2(f2_sub(r1, b), 0x1p-39f);  // 2^-62 grid
+  P.a = f2_add(P.a, a);
+  P.b = f2_add(P.b, b);
+  P.c = f2_add(P.c, c);
+}
+__device__ __forceinline__ unsigned long long drain62(Acc62 &P) {
+  float a[2], b[2], c[2];
+  f2_unpack(P.a, a[0], a[1]);
+  f2_unpack(P.b, b[0], b[1]);
+  f2_unpack(P.c, c[0], c[1]);
+  unsigned long long s = 0;
 #pragma unroll
-    for (int k = 0; k < kSpRun / kPer; ++k) run.w[k] = __ldg(p + k);
-    return;
-  }
-  // ragged or unaligned run: element by element
-  uint32_t bits[kSpRun];
-#pragma unroll
-  for (int j = 0; j < kSpRun; ++j) {
-    const bool in = v + j < V;
-    if (sizeof(E) == 2)
-      bits[j] = in ? (uint32_t)__ldg((const unsigned short *)row + v + j) : 0xff80u;
-    else
-      bits[j] = in ? __float_as_uint(__ldg((const float *)row + v + j)) : 0xff800000u;
-  }
-#pragma unroll
-  for (int k = 0; k < kSpRun / kPer; ++k) {
-    uint32_t q[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      q[c] = sizeof(E) == 2 ? (bits[8 * k + 2 * c] | (bits[8 * k + 2 * c + 1] << 16))
-                            : bits[4 * k + c];
-    run.w[k] = make_uint4(q[0], q[1], q[2], q[3]);
-  }
+  for (int l = 0; l < 2; ++l)
+    s += ((unsigned long long)__float2uint_rn(__fmul_rn(a[l], 0x1p21f)) << 41) +
+         ((unsigned long long)__float2uint_rn(__fmul_rn(b[l], 0x1p42f)) << 20) +
+         __float2uint_rn(__fmul_rn(c[l], 0x1p62f));
+  P.a = P.b = P.c = 0ull;
+  return s;
 }
 
 // packed exponent arguments fl(fl(x * invT) - mz) of two elements (the
@@ -903,84 +924,72 @@ __device__ __forceinline__ unsigned long long arg2(float x0, float x1, float m0,
   if (unit_t) return f2_sub(f2_pack(x0, x1), f2_pack(m0, m1));
   return f2_pack(__fsub_rn(__fmul_rn(x0, invT), m0), __fsub_rn(__fmul_rn(x1, invT), m1));
 }
-
-// split-part accumulation of a packed pair (each lane as add40 / add62)
-struct Parts40x2 {
-  unsigned long long a, b, c;
-};
-struct Parts62x2 {
-  unsigned long long a, b, c, d;
-};
-__device__ __forceinline__ unsigned long long trunc2(unsigned long long v, float grid_top) {
-  const unsigned long long g = f2_splat(grid_top);
-  return f2_sub(f2_add_rz(v, g), g);
-}
-__device__ __forceinline__ void add40x2(Parts40x2 &P, unsigned long long e) {
-  const unsigned long long a = trunc2(e, 0x1p7f);
-  const unsigned long long r1 = f2_sub(e, a);
-  const unsigned long long b = trunc2(r1, 0x1p-9f);
-  const unsigned long long r2 = f2_sub(r1, b);
-  const unsigned long long c = trunc2(r2, 0x1p-17f);
-  P.a = f2_add(P.a, a);
-  P.b = f2_add(P.b, b);
-  P.c = f2_add(P.c, c);
-}
-__device__ __forceinline__ void add62x2(Parts62x2 &P, unsigned long long w) {
-  const unsigned long long a = trunc2(w, 0x1p7f);
-  const unsigned long long r1 = f2_sub(w, a);
-  const unsigned long long b = trunc2(r1, 0x1p-9f);
-  const unsigned long long r2 = f2_sub(r1, b);
-  const unsigned long long c = trunc2(r2, 0x1p-25f);
-  const unsigned long long r3 = f2_sub(r2, c);
-  const unsigned long long d = trunc2(r3, 0x1p-39f);
-  P.a = f2_add(P.a, a);
-  P.b = f2_add(P.b, b);
-  P.c = f2_add(P.c, c);
-  P.d = f2_add(P.d, d);
-}
-// the two lanes' exact sums
-__device__ __forceinline__ void fix_lanes(const Parts40x2 &P, unsigned long long &s0,
-                                          unsigned long long &s1) {
-  Parts40 l0, l1;
-  f2_unpack(P.a, l0.a, l1.a);
-  f2_unpack(P.b, l0.b, l1.b);
-  f2_unpack(P.c, l0.c, l1.c);
-  s0 = fix_of(l0);
-  s1 = fix_of(l1);
-}
-__device__ __forceinline__ unsigned long long fix_sum(const Parts62x2 &P) {
-  Parts62 l0, l1;
-  f2_unpack(P.a, l0.a, l1.a);
-  f2_unpack(P.b, l0.b, l1.b);
-  f2_unpack(P.c, l0.c, l1.c);
-  f2_unpack(P.d, l0.d, l1.d);
-  return fix_of(l0) + fix_of(l1);
-}
-
 __device__ __forceinline__ float e1(float x, float invT, float mz, bool unit_t) {
   const float z = unit_t ? x : __fmul_rn(x, invT);
   return exp32_repro(__fsub_rn(z, mz));
 }
 
-struct SampleWs {
-  ulonglong2 *norm;          // [B][CS] partial (sum floor(e_q 2^40), sum floor(e_p 2^40))
-  unsigned long long *mass;  // [B][CS] slice sum W
-  unsigned long long *run;   // [B][CS][kSpThreads] run sums of W
-  unsigned *done;            // [2][B] slice CTAs of sample_mass / sample_norm finished
-                             // (zeroed by decide)
-  float2 *inv;               // [B] (1/S_e of q, of p) from the last sample_norm CTA
-  int CS;                    // slices per row
-  int B;
-};
+// element j of a 16-byte word of logits
+template <typename E>
+__device__ __forceinline__ float word_elem(const uint4 &q, int j);
+template <>
+__device__ __forceinline__ float word_elem<uint16_t>(const uint4 &q, int j) {
+  const int c = j >> 1;
+  const uint32_t x = c == 0 ? q.x : c == 1 ? q.y : c == 2 ? q.z : q.w;
+  return (j & 1) ? bf16_hi(x) : bf16_lo(x);
+}
+template <>
+__device__ __forceinline__ float word_elem<float>(const uint4 &q, int j) {
+  return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
+}
+
+// The residual weights of two elements from their exponentials (q and p
+// lanes packed): max(0, fl(fl(e_q iq) - fl(e_p ip))).  Scalar _rn intrinsics:
+// the packed multiply and subtract were observed to be contracted into a
+// fused multiply-add by the compiler, which changes the last bit of q - p.
+__device__ __forceinline__ unsigned long long resid_pair(unsigned long long eq,
+                                                         unsigned long long ep, float iq,
+                                                         float ip) {
+  float q0, q1, p0, p1;
+  f2_unpack(eq, q0, q1);
+  f2_unpack(ep, p0, p1);
+  const float d0 = __fsub_rn(__fmul_rn(q0, iq), __fmul_rn(p0, ip));
+  const float d1 = __fsub_rn(__fmul_rn(q1, iq), __fmul_rn(p1, ip));
+  return f2_pack(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f));
+}
+
+// A word of a row read element by element (ragged or unaligned rows);
+// elements at or past V read as -inf, whose exponential is 0.
+template <typename E>
+__device__ __forceinline__ uint4 load_word_slow(const E *row, int v0, int V) {
+  uint32_t q[4];
+  if (sizeof(E) == 2) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t lo = v0 + 2 * c < V ? (uint32_t)__ldg((const unsigned short *)row + v0 + 2 * c) : 0xff80u;
+      const uint32_t hi = v0 + 2 * c + 1 < V ? (uint32_t)__ldg((const unsigned short *)row + v0 + 2 * c + 1) : 0xff80u;
+      q[c] = lo | (hi << 16);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      q[c] = v0 + c < V ? __float_as_uint(__ldg((const float *)row + v0 + c)) : 0xff800000u;
+  }
+  return make_uint4(q[0], q[1], q[2], q[3]);
+}
+template <typename E>
+__device__ __forceinline__ uint4 load_word(const E *row, int v0, int V, bool vec) {
+  if (vec && v0 + sp_per<E>() <= V) return __ldg((const uint4 *)(row + v0));
+  return load_word_slow<E>(row, v0, V);
+}
 
 struct RowPair {
   const void *rq, *rp;
   float mzq, mzp;
   bool resid, vec, unit_t;
 };
-
-template <typename E>
-__device__ __forceinline__ RowPair row_pair(const Round &r, const Task &t) {
+template <typename E, typename TaskLike>
+__device__ __forceinline__ RowPair row_pair(const Round &r, const TaskLike &t) {
   RowPair p;
   p.resid = t.rp != nullptr;
   const E *rq = (const E *)t.rq;
@@ -994,76 +1003,18 @@ __device__ __forceinline__ RowPair row_pair(const Round &r, const Task &t) {
   return p;
 }
 
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v,
-                                                            unsigned long long *red) {
-  v = warp_sum_u64(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  unsigned long long tot = 0;
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kSpWarps; ++i) tot += red[i];
-  __syncthreads();
-  return tot;  // valid on thread 0
-}
-
-// S_e of the q and p rows of sequence b -> 1 / sum, by one thread
-__device__ __forceinline__ void inv_sums(const SampleWs &sw, int b, bool resid, float &iq,
-                                         float &ip) {
-  unsigned long long Sq = 0, Sp = 0;
-  for (int c = 0; c < sw.CS; ++c) {
-    const ulonglong2 n = __ldcg(sw.norm + (size_t)b * sw.CS + c);  // other CTAs' sums
-    Sq += n.x;
-    Sp += n.y;
-  }
-  iq = inv_sum(Sq);
-  ip = resid ? inv_sum(Sp) : 0.0f;
-}
-
+// the weight of one element: E (a draw from q) or W (residual)
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 8 : 4)
-sample_norm_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw) {
-  grid_dep_sync();
-  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
-  const Task t = tasks[b];
-  if (!t.active) return;
-  const RowPair p = row_pair<E>(r, t);
-  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
-  Run<E> rq;
-  load_run<E>(rq, (const E *)p.rq, v, r.V, p.vec);
-  Parts40x2 P{0ull, 0ull, 0ull};
-  unsigned long long fq, fp;
-  if (p.resid) {  // lanes (q row, p row) of the same element
-    Run<E> rp;
-    load_run<E>(rp, (const E *)p.rp, v, r.V, p.vec);
-#pragma unroll
-    for (int j = 0; j < kSpRun; ++j)
-      add40x2(P, exp32x2(arg2(rq[j], rp[j], p.mzq, p.mzp, r.invT, p.unit_t)));
-    fix_lanes(P, fq, fp);
-  } else {  // lanes (element j, element j + 1) of the q row
-#pragma unroll
-    for (int j = 0; j < kSpRun; j += 2)
-      add40x2(P, exp32x2(arg2(rq[j], rq[j + 1], p.mzq, p.mzq, r.invT, p.unit_t)));
-    unsigned long long f1;
-    fix_lanes(P, fq, f1);
-    fq += f1;
-    fp = 0ull;
-  }
-  __shared__ unsigned long long red[kSpWarps];
-  const unsigned long long sq = block_sum_u64(fq, red);
-  const unsigned long long sp = block_sum_u64(fp, red);
-  if (threadIdx.x == 0) {
-    // the last slice CTA of the sequence turns the slice sums into 1/S_e
-    sw.norm[blockIdx.x] = make_ulonglong2(sq, sp);
-    __threadfence();
-    if (atomicAdd(sw.done + sw.B + b, 1u) == (unsigned)(sw.CS - 1)) {
-      __threadfence();
-      float iq, ip;
-      inv_sums(sw, b, p.resid, iq, ip);
-      sw.inv[b] = make_float2(iq, ip);
-    }
-  }
+__device__ __forceinline__ unsigned long long weight_elem(const Round &r, const RowPair &p, int v,
+                                                          float iq, float ip, bool use_q) {
+  if (v >= r.V) return 0ull;
+  const float eq = e1(load_elem<E>((const E *)p.rq + v), r.invT, p.mzq, p.unit_t);
+  if (use_q) return fix40(eq);
+  const float d = __fsub_rn(
+      __fmul_rn(eq, iq),
+      __fmul_rn(e1(load_elem<E>((const E *)p.rp + v), r.invT, p.mzp, p.unit_t), ip));
+  return fix62(d > 0.0f ? d : 0.0f);
 }
-
 
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
@@ -1075,14 +1026,14 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return v;
 }
 
-// first index i in [0, n) where the running sum of get(i) exceeds thr;
-// `base` gets the sum before it.  One warp, uniform result.
+// First index i in [0, n) whose running sum of vals exceeds thr, by one warp
+// (uniform result); base gets the sum before it.
 template <typename F>
 __device__ __forceinline__ int warp_find(int n, unsigned long long thr, F get,
                                          unsigned long long &base) {
   base = 0;
   for (int c0 = 0; c0 < n; c0 += 32) {
-    const int c = c0 + (threadIdx.x & 31);
+    const int c = c0 + (int)(threadIdx.x & 31);
     const unsigned long long v = c < n ? get(c) : 0ull;
     const unsigned long long inc = warp_incl_scan_u64(v) + base;
     const unsigned hit = __ballot_sync(0xffffffffu, c < n && inc > thr);
@@ -1093,166 +1044,499 @@ __device__ __forceinline__ int warp_find(int n, unsigned long long thr, F get,
     }
     base = __shfl_sync(0xffffffffu, inc, 31);
   }
-  return n - 1;  // not reached when thr < total
-}
-
-// W (or the q mass) of one element
-template <typename E>
-__device__ __forceinline__ unsigned long long w_elem(const Round &r, const RowPair &p, int v,
-                                                     float iq, float ip, bool use_q) {
-  if (v >= r.V) return 0ull;
-  const float q = __fmul_rn(e1(load_elem<E>((const E *)p.rq + v), r.invT, p.mzq, p.unit_t), iq);
-  if (use_q) return fix62(q);
-  const float d = __fsub_rn(
-      q, __fmul_rn(e1(load_elem<E>((const E *)p.rp + v), r.invT, p.mzp, p.unit_t), ip));
-  return fix62(d > 0.0f ? d : 0.0f);
+  return n - 1;  // not reached when thr < the total
 }
 
 
-// The inverse-CDF pick of sequence b, by one warp (the last sample_mass CTA
-// of the sequence; the other CTAs' masses are read through L2).
+
+// A consumer thread's 32 elements of one row's slice: words
+// [t wpt, (t + 1) wpt) of the slice.  The bulk copy staged the slice's first
+// nbulk words in order; the rest (a ragged row end, or every word of a row
+// that is not 16-byte aligned) is read from global memory, -inf past V.  The
+// words are fetched in an order rotated by the thread index, which keeps the
+// 16-byte shared-memory reads of a quarter warp on distinct banks; the sums
+// below do not depend on the order.
 template <typename E>
-__device__ __forceinline__ void pick_sequence(const Round &r, const Task &t, const RowPair &p,
-                                              const SampleWs &sw, const DecideOut &o, int b) {
-  const int lane = threadIdx.x & 31;
-  const float2 iv = sw.inv[b];
-  const float iq = iv.x, ip = iv.y;
-  const unsigned long long *mass = sw.mass + (size_t)b * sw.CS;
-  unsigned long long Sw = 0;
-  for (int c0 = 0; c0 < sw.CS; c0 += 32)  // one load per lane, then a warp sum
-    Sw += warp_sum_u64(c0 + lane < sw.CS ? __ldcg(mass + c0 + lane) : 0ull);
-  // residual mass 0 (q == p to the last bit): fall back to q; its masses are
-  // recomputed here (a warp per slice / run), which only this case needs
-  const bool use_q = !p.resid || Sw == 0ull;
-  const bool fallback = p.resid && use_q;
-  auto run_mass = [&](int c, int th) -> unsigned long long {  // one lane, one run
-    unsigned long long m = 0;
-    const int v0 = c * kSpSlice + kSpRun * th;
-    for (int j = 0; j < kSpRun; ++j) m += w_elem<E>(r, p, v0 + j, iq, ip, true);
-    return m;
-  };
-  auto slice_mass = [&](int c) -> unsigned long long {  // one lane, one slice
-    unsigned long long m = 0;
-    for (int th = 0; th < kSpThreads; ++th) m += run_mass(c, th);
-    return m;
-  };
-  unsigned long long S = Sw;
-  if (fallback) {
-    S = 0;
-    for (int c0 = 0; c0 < sw.CS; c0 += 32) {
-      const unsigned long long m = (c0 + lane < sw.CS) ? slice_mass(c0 + lane) : 0ull;
-      S += warp_sum_u64(m);
+__device__ __forceinline__ void fetch_run(uint4 (&w)[sp_wpt<E>()], const uint4 *stage,
+                                          const E *row, int V, int s, int nbulk) {
+  constexpr int kWpt = sp_wpt<E>();
+  constexpr int kSh = kWpt == 4 ? 1 : 0;  // threads per 128-byte line: 2 (bf16), 1 (fp32)
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int k = 0; k < kWpt; ++k) {
+    const int wi = t * kWpt + ((k + (t >> kSh)) & (kWpt - 1));
+    w[k] = wi < nbulk ? stage[wi]
+                      : load_word_slow<E>(row, s * kSpSlice + wi * sp_per<E>(), V);
+  }
+}
+
+// The run sums of a thread.
+// E of the q row; lanes (element j, element j + 1), 16 values per lane.
+template <typename E>
+__device__ __forceinline__ unsigned long long run_e40(const Round &r, const RowPair &p,
+                                                      const uint4 (&wq)[sp_wpt<E>()]) {
+  Acc40 P{0ull, 0ull};
+#pragma unroll
+  for (int k = 0; k < sp_wpt<E>(); ++k)
+#pragma unroll
+    for (int j = 0; j < sp_per<E>(); j += 2)
+      acc40(P, exp32x2(arg2(word_elem<E>(wq[k], j), word_elem<E>(wq[k], j + 1), p.mzq, p.mzq,
+                            r.invT, p.unit_t)));
+  unsigned long long s0 = 0, s1 = 0;
+  drain40(P, s0, s1);
+  return s0 + s1;
+}
+// E of the q row and of the p row; lanes (q element, p element), drained
+// every 16 values.
+template <typename E>
+__device__ __forceinline__ void run_e40_pair(const Round &r, const RowPair &p,
+                                             const uint4 (&wq)[sp_wpt<E>()],
+                                             const uint4 (&wp)[sp_wpt<E>()],
+                                             unsigned long long &fq, unsigned long long &fp) {
+  Acc40 P{0ull, 0ull};
+  fq = fp = 0;
+#pragma unroll
+  for (int k = 0; k < sp_wpt<E>(); ++k)
+#pragma unroll
+    for (int j = 0; j < sp_per<E>(); ++j) {
+      acc40(P, exp32x2(arg2(word_elem<E>(wq[k], j), word_elem<E>(wp[k], j), p.mzq, p.mzp, r.invT,
+                            p.unit_t)));
+      if ((k * sp_per<E>() + j) % 16 == 15) drain40(P, fq, fp);
+    }
+}
+// W; lanes (element j, element j + 1), drained every 8 values.
+template <typename E>
+__device__ __forceinline__ unsigned long long run_w62(const Round &r, const RowPair &p,
+                                                      const uint4 (&wq)[sp_wpt<E>()],
+                                                      const uint4 (&wp)[sp_wpt<E>()], float iq,
+                                                      float ip) {
+  Acc62 P{0ull, 0ull, 0ull};
+  unsigned long long fw = 0;
+#pragma unroll
+  for (int k = 0; k < sp_wpt<E>(); ++k)
+#pragma unroll
+    for (int j = 0; j < sp_per<E>(); j += 2) {
+      const unsigned long long eq = exp32x2(arg2(word_elem<E>(wq[k], j), word_elem<E>(wq[k], j + 1),
+                                                 p.mzq, p.mzq, r.invT, p.unit_t));
+      const unsigned long long ep = exp32x2(arg2(word_elem<E>(wp[k], j), word_elem<E>(wp[k], j + 1),
+                                                 p.mzp, p.mzp, r.invT, p.unit_t));
+      acc62(P, resid_pair(eq, ep, iq, ip));
+      if (((k * sp_per<E>() + j) / 2) % 8 == 7) fw += drain62(P);
+    }
+  return fw;
+}
+
+struct SampleWs {
+  unsigned long long *slice;  // [3][B][NS] slice sums: E of q, E of p, W
+  unsigned long long *runs;   // [B][NS][kSpThreads] run sums in use (E or W)
+  unsigned *done;             // [2][B] completed slices of pass 1 / 2 (zeroed by decide)
+  const int *rlist, *blist;   // residual / bonus draws, listed by the accept walk
+  unsigned *qc;               // [0] residual count, [1] bonus count, [2] next item
+                              // (zeroed by the row pass)
+  int NS, B;
+};
+
+// 1 / S of the q and p rows of residual draw b from its pass-1 slice sums,
+// by one warp (uniform result)
+__device__ __forceinline__ float2 resid_inv(const SampleWs &sw, int b) {
+  const unsigned long long *slq = sw.slice + (size_t)b * sw.NS;
+  const unsigned long long *slp = sw.slice + ((size_t)sw.B + b) * sw.NS;
+  unsigned long long Sq = 0, Sp = 0;
+  for (int c = (int)(threadIdx.x & 31); c < sw.NS; c += 32) {
+    Sq += __ldcg(slq + c);
+    Sp += __ldcg(slp + c);
+  }
+  Sq = warp_sum_u64(Sq);
+  Sp = warp_sum_u64(Sp);
+  return make_float2(inv_sum(Sq), inv_sum(Sp));
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Named barrier of the four consumer warps (the producer warp never joins).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// mbarrier primitives of the ring, every wait bounded by kSpWaitNs
+constexpr unsigned long long kSpWaitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ unsigned long long sp_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t sp_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void sp_mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void sp_mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// an arrival that also expects `bytes` of bulk copies to complete on the barrier
+__device__ __forceinline__ void sp_mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// TMA bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global into this CTA's shared memory, completing on `bar`
+__device__ __forceinline__ void sp_bulk_copy(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool sp_mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity`; false (and *abort set) when it runs
+// out or another warp of the CTA has given up.
+__device__ __noinline__ bool sp_mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                               volatile int *abort) {
+  const unsigned long long t0 = sp_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (sp_mbar_try(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (sp_ns() - t0 > kSpWaitNs) {
+        *abort = 1;
+        return false;
+      }
     }
   }
+}
+__device__ __forceinline__ bool sp_mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return sp_mbar_try(bar, parity) || sp_mbar_wait_slow(bar, parity, abort);
+}
+
+// What the producer tells the consumers about the item in a stage
+struct ItemMeta {
+  const void *rq, *rp;  // the sampled rows (rp null for a bonus draw)
+  float mq, mp;         // their raw maxima
+  float iq, ip;         // 1/S of both rows (pass 2)
+  uint32_t u24;
+  int a, b, s, kind;    // kind: 0 pass 1 residual, 1 pass 1 bonus, 2 pass 2, -1 none left
+  int ok;               // pass 2: the sequence's pass 1 was complete
+  int nbulk;            // leading words of the slice staged by the bulk copy
+};
+
+struct SampleSmem {
+  unsigned long long full[2], empty[2];  // the ring's barriers
+  ItemMeta meta[2];
+  unsigned long long red[2][2][kSpWarps];  // per stage, per sum: the warps' partial sums
+  int abort;
+};
+
+// The inverse-CDF pick of sequence b by one warp (the producer warp of the
+// CTA that completed the sequence): the slice (slice sums), the run (stored
+// run sums, or the q row's run sums recomputed for the zero-residual
+// fallback), then one lane per element of the run.
+template <typename E>
+__device__ __forceinline__ void pick_token_warp(const Round &r, const ItemMeta &t, int b,
+                                                const SampleWs &sw,
+                                                const unsigned long long *slices, bool use_q,
+                                                bool recompute, const DecideOut &o) {
+  const int lane = threadIdx.x & 31;
+  const int NS = sw.NS;
+  const RowPair p = row_pair<E>(r, t);
+  unsigned long long S = 0;
+  for (int c = lane; c < NS; c += 32) S += __ldcg(slices + c);
+  S = warp_sum_u64(S);
   const unsigned long long thr =
       (__umul64hi((unsigned long long)t.u24, S) << 40) | (((unsigned long long)t.u24 * S) >> 24);
-  unsigned long long base_s, base_r;
-  const int cs = warp_find(sw.CS, thr,
-                           [&](int c) { return fallback ? slice_mass(c) : __ldcg(mass + c); },
-                           base_s);
-  const unsigned long long *run = sw.run + ((size_t)b * sw.CS + cs) * kSpThreads;
-  const unsigned long long tl = thr - base_s;
-  int ri;
-  if (fallback) {
-    ri = warp_find(kSpThreads, tl, [&](int th) { return run_mass(cs, th); }, base_r);
-  } else {
-    // the slice's run sums: lane l loads runs [8l, 8l + 8) at once, the warp
-    // finds the lane whose group crosses the threshold, that lane the run
-    constexpr int kPer = kSpThreads / 32;
-    unsigned long long rs[kPer], own = 0;
+  unsigned long long base;
+  const int s = warp_find(NS, thr, [&](int c) { return __ldcg(slices + c); }, base);
+  const unsigned long long tl = thr - base;
+  // the run: lane l holds runs [4l, 4l + 4)
+  constexpr int kPer = kSpThreads / 32;
+  const unsigned long long *runs = sw.runs + ((size_t)b * NS + s) * kSpThreads;
+  unsigned long long rs[kPer], own = 0;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      rs[k] = __ldcg(run + lane * kPer + k);
-      own += rs[k];
-    }
-    const unsigned long long inc = warp_incl_scan_u64(own);
-    const unsigned hit = __ballot_sync(0xffffffffu, inc > tl);
-    const int lh = hit ? __ffs(hit) - 1 : 31;  // tl < slice mass: some lane crosses
-    // this lane's group: the first run whose running sum crosses tl
-    unsigned long long run_acc = inc - own, base_k = run_acc;
-    int k_hit = kPer - 1;
-    bool found = false;
+  for (int k = 0; k < kPer; ++k) {
+    const int ri = lane * kPer + k;
+    if (recompute) {  // E of the q row over run ri of slice s
+      Acc40 P{0ull, 0ull};
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      if (!found && run_acc + rs[k] > tl) {
-        found = true;
-        k_hit = k;
-        base_k = run_acc;
+      for (int w = 0; w < sp_wpt<E>(); ++w) {
+        const uint4 q = load_word<E>((const E *)p.rq,
+                                     s * kSpSlice + (ri * sp_wpt<E>() + w) * sp_per<E>(), r.V,
+                                     p.vec);
+#pragma unroll
+        for (int j = 0; j < sp_per<E>(); j += 2)
+          acc40(P, exp32x2(arg2(word_elem<E>(q, j), word_elem<E>(q, j + 1), p.mzq, p.mzq, r.invT,
+                                p.unit_t)));
       }
-      run_acc += rs[k];
+      unsigned long long s0 = 0, s1 = 0;
+      drain40(P, s0, s1);
+      rs[k] = s0 + s1;
+    } else {
+      rs[k] = __ldcg(runs + ri);
     }
-    ri = __shfl_sync(0xffffffffu, lane * kPer + k_hit, lh);
-    base_r = __shfl_sync(0xffffffffu, base_k, lh);
+    own += rs[k];
   }
+  const unsigned long long inc = warp_incl_scan_u64(own);
+  const unsigned hit_g = __ballot_sync(0xffffffffu, inc > tl);
+  const int lh = hit_g ? __ffs(hit_g) - 1 : 31;  // tl < the slice sum: some lane crosses
+  unsigned long long run_acc = inc - own, base_k = run_acc;
+  int k_hit = kPer - 1;
+  bool found = false;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    if (!found && run_acc + rs[k] > tl) {
+      found = true;
+      k_hit = k;
+      base_k = run_acc;
+    }
+    run_acc += rs[k];
+  }
+  const int ri = __shfl_sync(0xffffffffu, lane * kPer + k_hit, lh);
+  const unsigned long long tb = tl - __shfl_sync(0xffffffffu, base_k, lh);
   // the run's 32 elements, one per lane
-  const int v = cs * kSpSlice + kSpRun * ri + lane;
-  const unsigned long long w = w_elem<E>(r, p, v, iq, ip, use_q);
-  const unsigned long long tb = tl - base_r;
-  const unsigned long long inc = warp_incl_scan_u64(w);
-  const unsigned hit = __ballot_sync(0xffffffffu, inc > tb);
+  const int v = s * kSpSlice + 32 * ri + lane;
+  const unsigned long long wt = weight_elem<E>(r, p, v, t.iq, t.ip, use_q);
+  const unsigned long long incw = warp_incl_scan_u64(wt);
+  const unsigned hit = __ballot_sync(0xffffffffu, incw > tb);
   const int l = __ffs(hit) - 1;
   if (lane == l) {
-    const unsigned long long c = inc - w;
-    const unsigned long long b_lo = tb - c, b_hi = c + w - 1ull - tb;
+    const unsigned long long c = incw - wt;
+    const unsigned long long b_lo = tb - c, b_hi = c + wt - 1ull - tb;
     const int Wd = r.maxpos + 1;
     o.tokens[(size_t)b * Wd + t.a] = v;
     if (o.margin)
       o.margin[(size_t)b * Wd + r.maxpos] =
           (float)((double)(b_lo < b_hi ? b_lo : b_hi) / (double)S);
-    if (fallback) o.status[b] |= SV_ROW_RESID_ZERO;
+    if (p.resid && use_q) o.status[b] |= SV_ROW_RESID_ZERO;
   }
 }
 
+// The producer warp finishes an item whose results the consumers have stored
+// (their arrivals on the stage's "empty" barrier precede this): the item is
+// counted for its sequence, and the warp that completes a sequence's bonus
+// pass or residual pass 2 picks its token.
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads, sizeof(E) == 2 ? 8 : 4)
-sample_mass_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
-  grid_dep_sync();
-  const int b = blockIdx.x / sw.CS, cs = blockIdx.x - b * sw.CS;
-  const Task t = tasks[b];
-  if (!t.active) return;
-  const RowPair p = row_pair<E>(r, t);
-  const int v = cs * kSpSlice + kSpRun * threadIdx.x;
-  Run<E> rq, rp;
-  load_run<E>(rq, (const E *)p.rq, v, r.V, p.vec);
-  if (p.resid) load_run<E>(rp, (const E *)p.rp, v, r.V, p.vec);
-  const float2 iv = sw.inv[b];  // written by sample_norm
-  const float iq = iv.x, ip = iv.y;
-  Parts62x2 P{0ull, 0ull, 0ull, 0ull};
-  if (p.resid) {
-#pragma unroll
-    for (int j = 0; j < kSpRun; j += 2) {
-      float q0, p0, q1, p1;
-      f2_unpack(exp32x2(arg2(rq[j], rp[j], p.mzq, p.mzp, r.invT, p.unit_t)), q0, p0);
-      f2_unpack(exp32x2(arg2(rq[j + 1], rp[j + 1], p.mzq, p.mzp, r.invT, p.unit_t)), q1, p1);
-      const float d0 = __fsub_rn(__fmul_rn(q0, iq), __fmul_rn(p0, ip));
-      const float d1 = __fsub_rn(__fmul_rn(q1, iq), __fmul_rn(p1, ip));
-      add62x2(P, f2_pack(fmaxf(d0, 0.0f), fmaxf(d1, 0.0f)));
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kSpRun; j += 2) {
-      float e0, e1;
-      f2_unpack(exp32x2(arg2(rq[j], rq[j + 1], p.mzq, p.mzq, r.invT, p.unit_t)), e0, e1);
-      // q >= 0; the max keeps the product out of the split's addition
-      add62x2(P, f2_pack(fmaxf(__fmul_rn(e0, iq), 0.0f), fmaxf(__fmul_rn(e1, iq), 0.0f)));
-    }
+__device__ __forceinline__ void finish_item(const Round &r, const ItemMeta &m, const SampleWs &sw,
+                                            const DecideOut &o) {
+  if (m.kind < 0 || (m.kind == 2 && !m.ok)) return;
+  const int lane = threadIdx.x & 31;
+  unsigned old = 0;
+  if (lane == 0) {
+    __threadfence();  // the consumers' sums (seen through the barrier) before the count
+    old = atomicAdd(sw.done + (m.kind == 2 ? sw.B + m.b : m.b), 1u);
   }
-  const unsigned long long mine = fix_sum(P);
-  sw.run[(size_t)blockIdx.x * kSpThreads + threadIdx.x] = mine;
-  __shared__ unsigned long long red[kSpWarps];
-  const unsigned long long tot = block_sum_u64(mine, red);  // also a CTA barrier
-  __shared__ int s_last;
-  if (threadIdx.x == 0) {
-    // the barrier above orders every thread's run store before this
-    // thread's device-scope fence, which orders them (cumulatively) before
-    // the count that the last CTA of the sequence observes
-    sw.mass[blockIdx.x] = tot;
-    __threadfence();
-    s_last = atomicAdd(sw.done + b, 1u) == (unsigned)(sw.CS - 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old != (unsigned)(sw.NS - 1) || m.kind == 0) return;
+  __threadfence();  // the other CTAs' sums of this sequence, after the count
+  if (m.kind == 1) {
+    pick_token_warp<E>(r, m, m.b, sw, sw.slice + (size_t)m.b * sw.NS, true, false, o);
+    return;
+  }
+  const unsigned long long *slw = sw.slice + ((size_t)2 * sw.B + m.b) * sw.NS;
+  unsigned long long Sw = 0;
+  for (int c = lane; c < sw.NS; c += 32) Sw += __ldcg(slw + c);
+  if (warp_sum_u64(Sw) != 0ull)
+    pick_token_warp<E>(r, m, m.b, sw, slw, false, false, o);
+  else  // residual mass 0 (q == p to the last bit): the draw from q
+    pick_token_warp<E>(r, m, m.b, sw, sw.slice + (size_t)m.b * sw.NS, true, true, o);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kSpThreads + 32)
+sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
+  grid_dep_sync();
+  extern __shared__ __align__(128) uint4 stage_sm[];  // [2 stages][q, p][words]
+  __shared__ SampleSmem sm;
+  constexpr int kW = sp_words<E>();
+  const int tid = threadIdx.x, NS = sw.NS;
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      sp_mbar_init(sp_addr(&sm.full[i]), 1);            // the producer's arrival (+ bytes)
+      sp_mbar_init(sp_addr(&sm.empty[i]), kSpThreads);  // every consumer, results stored
+      sm.meta[i].kind = -1;
+    }
+    sm.abort = 0;
   }
   __syncthreads();
-  // the last slice CTA of the sequence picks the token
-  if (s_last && threadIdx.x < 32) pick_sequence<E>(r, t, p, sw, o, b);
+  volatile int *abort = &sm.abort;
+  if (tid >= kSpThreads) {
+    // ------------------------------------------------------ producer / finisher
+    const int lane = tid - kSpThreads;
+    const int R = (int)__ldcg(sw.qc), Bn = (int)__ldcg(sw.qc + 1);
+    const int n1r = R * NS, n1 = n1r + Bn * NS, total = n1 + R * NS;
+    ItemMeta held[2];  // the item each stage holds, finished once it is released
+    held[0].kind = held[1].kind = -1;
+    int n = 0;
+    for (;; ++n) {
+      const int slot = n & 1;
+      if (n >= 2) {
+        if (!sp_mbar_wait(sp_addr(&sm.empty[slot]), ((n >> 1) - 1) & 1, abort)) break;
+        finish_item<E>(r, held[slot], sw, o);
+        held[slot].kind = -1;
+      }
+      int i = 0;
+      if (lane == 0) i = *abort ? total : (int)atomicAdd(sw.qc + 2, 1u);
+      i = __shfl_sync(0xffffffffu, i, 0);
+      ItemMeta m;
+      m.kind = -1;
+      m.nbulk = 0;
+      if (i < total) {
+        int b, s;
+        if (i < n1r) {
+          m.kind = 0;
+          b = sw.rlist[i / NS];
+          s = i % NS;
+        } else if (i < n1) {
+          m.kind = 1;
+          b = sw.blist[(i - n1r) / NS];
+          s = (i - n1r) % NS;
+        } else {
+          m.kind = 2;
+          b = sw.rlist[(i - n1) / NS];
+          s = (i - n1) % NS;
+        }
+        const Task t = tasks[b];
+        m.rq = t.rq;
+        m.rp = t.rp;
+        m.mq = t.mq;
+        m.mp = t.mp;
+        m.u24 = t.u24;
+        m.a = t.a;
+        m.b = b;
+        m.s = s;
+        m.ok = 1;
+        m.iq = m.ip = 0.0f;
+        if (m.kind == 2) {
+          // The sequence's pass 1 must be complete (bounded wait).  The item
+          // in flight in the other stage may be one of those pass-1 items: it
+          // is counted here as soon as its consumers are done, or this wait
+          // could never end.
+          const int other = (n + 1) & 1;
+          const unsigned long long t0 = sp_ns();
+          for (;;) {
+            unsigned done = 0;
+            if (lane == 0) done = ld_acquire(sw.done + b);
+            done = __shfl_sync(0xffffffffu, done, 0);
+            if (done >= (unsigned)NS) break;
+            if (held[other].kind >= 0 && n >= 1 &&
+                sp_mbar_try(sp_addr(&sm.empty[other]), ((n - 1) >> 1) & 1)) {
+              finish_item<E>(r, held[other], sw, o);
+              held[other].kind = -1;
+              continue;
+            }
+            if (sp_ns() - t0 > kSpWaitNs) {
+              m.ok = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+          const float2 iv = resid_inv(sw, b);
+          m.iq = iv.x;
+          m.ip = iv.y;
+          if (!m.ok && lane == 0) atomicOr(o.status + b, SV_ROW_TIMEOUT);
+        }
+        // the words of the slice that lie inside an aligned row: one bulk copy
+        // per row (the consumers read the rest themselves)
+        const RowPair p = row_pair<E>(r, t);
+        const int left = r.V - s * kSpSlice;
+        m.nbulk = p.vec ? (left < kSpSlice ? left : kSpSlice) / sp_per<E>() : 0;
+      }
+      const uint32_t bytes = (uint32_t)m.nbulk * 16u * (m.kind == 1 ? 1u : 2u);
+      if (lane == 0) {
+        sm.meta[slot] = m;
+        sp_mbar_expect_tx(sp_addr(&sm.full[slot]), bytes);  // arrival (release) + expected bytes
+        if (bytes) {
+          const uint32_t dst = sp_addr(stage_sm + (size_t)(2 * slot) * kW);
+          const size_t off = (size_t)m.s * kSpSlice * sizeof(E);
+          sp_bulk_copy(dst, (const char *)m.rq + off, (uint32_t)m.nbulk * 16u,
+                       sp_addr(&sm.full[slot]));
+          if (m.kind != 1)
+            sp_bulk_copy(dst + (uint32_t)kW * 16u, (const char *)m.rp + off,
+                         (uint32_t)m.nbulk * 16u, sp_addr(&sm.full[slot]));
+        }
+      }
+      __syncwarp();
+      held[slot] = m;
+      if (m.kind < 0) break;
+    }
+    // the item still held by the other stage: released once the consumers are done
+    const int other = (n + 1) & 1;
+    if (!*abort && held[other].kind >= 0 && n >= 1 &&
+        sp_mbar_wait(sp_addr(&sm.empty[other]), ((n - 1) >> 1) & 1, abort))
+      finish_item<E>(r, held[other], sw, o);
+    // after an abort, let this CTA's bulk copies in flight land before it exits
+    if (*abort && lane == 0) {
+      for (int k = n - 1; k <= n; ++k) {
+        if (k < 0) continue;
+        const unsigned long long t0 = sp_ns();
+        while (!sp_mbar_try(sp_addr(&sm.full[k & 1]), (k >> 1) & 1) && sp_ns() - t0 < kSpWaitNs) {
+        }
+      }
+    }
+    return;
+  }
+  // ---------------------------------------------------------------- consumers
+  for (int n = 0;; ++n) {
+    const int slot = n & 1;
+    if (!sp_mbar_wait(sp_addr(&sm.full[slot]), (n >> 1) & 1, abort)) {
+      if (tid == 0 && sm.meta[slot].kind >= 0) atomicOr(o.status + sm.meta[slot].b, SV_ROW_TIMEOUT);
+      break;
+    }
+    const ItemMeta m = sm.meta[slot];
+    if (m.kind < 0) break;
+    const int b = m.b, s = m.s;
+    if (m.kind == 2 && !m.ok) {
+      sp_mbar_arrive(sp_addr(&sm.empty[slot]));
+      continue;
+    }
+    const RowPair p = row_pair<E>(r, m);
+    const uint4 *sq = stage_sm + (size_t)(2 * slot) * kW;
+    uint4 wq[sp_wpt<E>()], wp[sp_wpt<E>()];
+    fetch_run<E>(wq, sq, (const E *)p.rq, r.V, s, m.nbulk);
+    if (m.kind != 1) fetch_run<E>(wp, sq + kW, (const E *)p.rp, r.V, s, m.nbulk);
+    unsigned long long f0, f1 = 0;
+    if (m.kind == 0) {
+      run_e40_pair<E>(r, p, wq, wp, f0, f1);
+    } else if (m.kind == 1) {
+      f0 = run_e40<E>(r, p, wq);
+    } else {
+      f0 = run_w62<E>(r, p, wq, wp, m.iq, m.ip);
+    }
+    // run sums (bonus E, residual W) and the slice sums
+    if (m.kind != 0) sw.runs[((size_t)b * NS + s) * kSpThreads + tid] = f0;
+    // (per-stage buffers: a warp can be one item ahead of thread 0's reads,
+    // never two, since the stage is refilled only after thread 0 releases it)
+    f0 = warp_sum_u64(f0);
+    f1 = warp_sum_u64(f1);
+    if ((tid & 31) == 0) {
+      sm.red[slot][0][tid >> 5] = f0;
+      sm.red[slot][1][tid >> 5] = f1;
+    }
+    csync();
+    if (tid == 0) {
+      unsigned long long a0 = 0, a1 = 0;
+      for (int w = 0; w < kSpWarps; ++w) {
+        a0 += sm.red[slot][0][w];
+        a1 += sm.red[slot][1][w];
+      }
+      const int which = m.kind == 2 ? 2 : 0;
+      sw.slice[((size_t)which * sw.B + b) * NS + s] = a0;
+      if (m.kind == 0) sw.slice[((size_t)sw.B + b) * NS + s] = a1;
+    }
+    // every consumer's stores precede its arrival: the producer then counts
+    // the item (and may pick) and reuses the stage
+    sp_mbar_arrive(sp_addr(&sm.empty[slot]));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1346,6 +1630,54 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
 }
 
 // ---------------------------------------------------------------------------
+// The sampler's persistent grids: every SM filled with as many CTAs as fit,
+// looked up once per device and kernel.
+template <typename E, typename K>
+int persistent_grid(K k, int which, size_t smem) {
+  static std::mutex mu;
+  static int cache[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev][which]) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+      return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kSpThreads + 32, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      return 0;
+    cache[dev][which] = per_sm * num_sms();
+  }
+  return cache[dev][which];
+}
+
+template <typename E>
+sv_status launch_sampler(const Round &r, const Layout &L, char *ws, const Task *tasks,
+                         const DecideOut &o, cudaStream_t st) {
+  SampleWs sw;
+  sw.slice = (unsigned long long *)(ws + L.slice);
+  sw.runs = (unsigned long long *)(ws + L.runs);
+  sw.done = (unsigned *)(ws + L.done);
+  sw.rlist = (const int *)(ws + L.rlist);
+  sw.blist = sw.rlist + r.B;
+  sw.qc = (unsigned *)(ws + L.qc);
+  sw.NS = L.NS;
+  sw.B = r.B;
+  const size_t smem = 2 * sp_stage_bytes<E>();
+  // at most 2 B NS items: never more CTAs than that
+  const long long items = 2LL * r.B * L.NS;
+  const int g = persistent_grid<E>(sample_kernel<E>, 0, smem);
+  if (!g) return set_error(SV_ERR_CUDA, "sample: occupancy query");
+  LaunchScope ls("sample", st);
+  return check_launch("sample",
+                      launch_pdl(sample_kernel<E>, dim3((unsigned)(items < g ? items : g)),
+                                 dim3(kSpThreads + 32), smem, st, r, tasks, sw, o));
+}
+
+// ---------------------------------------------------------------------------
 template <typename E>
 sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, uint64_t step,
                      const DecideOut &o, cudaStream_t st, cudaEvent_t accept_event,
@@ -1367,7 +1699,8 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     s = check_launch("row_stats_ee", launch_pdl(r.copy ? row_stats_ee_kernel<E, true>
                                                        : row_stats_ee_kernel<E, false>,
                                                 dim3((unsigned)nblk), dim3(kRsThreads), 0, st,
-                                                r, G, partial, count, stop, seed, step));
+                                                r, G, partial, count, stop, seed, step,
+                                                (unsigned *)(ws + L.qc)));
     if (s != SV_OK) return s;
   } else {
     // tree: B * P row slots bound the listed rows; half as many CTAs per
@@ -1379,7 +1712,8 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
                                                     : row_stats_kernel<E, false>,
                                              dim3(gx, (unsigned)G),
                                              dim3(kRsThreads), 0, st, r, G, rowlist,
-                                             (const int *)(ws + L.ctr), partial));
+                                             (const int *)(ws + L.ctr), partial,
+                                             (unsigned *)(ws + L.qc)));
     if (s != SV_OK) return s;
   }
   {
@@ -1394,34 +1728,15 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     s = check_launch("decide", launch_pdl(kern,
                                           dim3((r.B + kDecideWarps - 1) / kDecideWarps),
                                           dim3(kDecideWarps * 32), dsm, st, r, G, partial, seed,
-                                          step, o, tasks, (unsigned *)(ws + L.done)));
+                                          step, o, tasks, (int *)(ws + L.rlist),
+                                          (unsigned *)(ws + L.qc), (unsigned *)(ws + L.done)));
     if (s != SV_OK) return s;
   }
   if (accept_event) {
     const cudaError_t e = cudaEventRecord(accept_event, st);
     if (e != cudaSuccess) return set_error(SV_ERR_CUDA, "accept_event: %s", cudaGetErrorString(e));
   }
-  SampleWs sw;
-  sw.norm = (ulonglong2 *)(ws + L.norm);
-  sw.mass = (unsigned long long *)(ws + L.mass);
-  sw.run = (unsigned long long *)(ws + L.run);
-  sw.done = (unsigned *)(ws + L.done);
-  sw.inv = (float2 *)(ws + L.inv);
-  sw.CS = L.CS;
-  sw.B = r.B;
-  const unsigned grid = (unsigned)((long)r.B * L.CS);
-  {
-    LaunchScope ls("sample_norm", st);
-    s = check_launch("sample_norm", launch_pdl(sample_norm_kernel<E>, dim3(grid),
-                                               dim3(kSpThreads), 0, st, r, tasks, sw));
-    if (s != SV_OK) return s;
-  }
-  {
-    LaunchScope ls("sample_mass", st);
-    s = check_launch("sample_mass", launch_pdl(sample_mass_kernel<E>, dim3(grid),
-                                               dim3(kSpThreads), 0, st, r, tasks, sw, o));
-    if (s != SV_OK) return s;
-  }
+  if ((s = launch_sampler<E>(r, L, ws, tasks, o, st)) != SV_OK) return s;
   return SV_OK;
 }
 
@@ -1474,7 +1789,7 @@ sv_status check_common(const void *vlogits, sv_dtype dt, int B, int V, float tem
 
 // grid sizes of the round's kernels must fit a 32-bit grid dimension
 sv_status check_grid(int B, const Layout &L) {
-  if ((long long)B * L.P > 0x7fffffffLL || (long long)B * L.CS > 0x7fffffffLL)
+  if ((long long)B * L.P > 0x7fffffffLL || (long long)B * L.NS > 0x7fffffffLL)
     return set_error(SV_ERR_UNSUPPORTED, "batch too large: B=%d", B);
   return SV_OK;
 }
@@ -1716,11 +2031,9 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
 // stand-in, not device memory), so the device address is looked up once per
 // device with cudaGetSymbolAddress, with that device current, on the first
 // call made on it.
-#include <mutex>
-
 namespace sv {
 namespace {
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void *g_static_ptr[kMaxDevices] = {};
@@ -1731,6 +2044,10 @@ static __device__ __align__(256) unsigned char g_static_scratch[sv::kStaticScrat
 
 namespace sv {
 namespace {
+// a non-null stand-in for the argument checks, which want a workspace pointer;
+// the host-side name of the array is never dereferenced or passed to a kernel
+const void *g_static_scratch_host_name() { return (const void *)&g_static_scratch; }
+
 sv_status static_scratch_address(void **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1762,9 +2079,15 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dl
                                              float *out_p_prob, float *out_margin,
                                              uint32_t *out_status, void *stream,
                                              void *accept_event) {
-  if (B < 0 || N < 0 || V < 1)
-    return set_error(SV_ERR_INVALID_ARG, "need B >= 0, N >= 0, V >= 1");
-  if (B == 0) return SV_OK;
+  // the argument checks of sv_verify_chain, in its order, before the
+  // capacity check (the scratch itself is never null)
+  sv_status s = check_common(vlogits, dt, B, V, temperature, out_tokens, out_accept_len,
+                             out_status, g_static_scratch_host_name());
+  if (s != SV_OK || B == 0) return s;
+  if (N < 0) return set_error(SV_ERR_INVALID_ARG, "N must be >= 0 (got %d)", N);
+  if (N > SV_MAX_POSITIONS) return set_error(SV_ERR_UNSUPPORTED, "N > %d", SV_MAX_POSITIONS);
+  if (N > 0 && (!dlogits || !draft_tokens))
+    return set_error(SV_ERR_INVALID_ARG, "dlogits and draft_tokens are required when N > 0");
   const size_t need = sv_verify_chain_workspace(B, N, V);
   if (need > kStaticScratchBytes)
     return set_error(SV_ERR_UNSUPPORTED,
@@ -1773,7 +2096,7 @@ extern "C" sv_status sv_verify_chain_noalloc(const void *vlogits, const void *dl
                      "caller-owned workspace",
                      B, N, V, need, kStaticScratchBytes);
   void *ws = nullptr;
-  sv_status s = static_scratch_address(&ws);
+  s = static_scratch_address(&ws);
   if (s != SV_OK) return s;
   return sv_verify_chain(vlogits, dlogits, dt, draft_tokens, B, N, V, temperature, seed, step,
                          out_tokens, out_accept_len, out_q_prob, out_p_prob, out_margin,

@@ -371,8 +371,8 @@ def test_trace_and_launch_count():
     sv.verify_chain(vq.to(DEV), dp.to(DEV), d.to(DEV))
     sv.sv_trace_enable(False)
     tr = sv.sv_trace_collect()
-    assert sv.sv_launch_count() - n0 == 4
-    assert set(tr) == {"row_stats", "decide", "sample_norm", "sample_mass"}
+    assert sv.sv_launch_count() - n0 == 3
+    assert set(tr) == {"row_stats", "decide", "sample"}
     assert all(v[0] == 1 and v[1] > 0 for v in tr.values())
 
 

@@ -118,3 +118,25 @@ def test_tree_level_host_checks_need_no_gpu(lib):
     g = lib.sv_tree_finalize
     assert g(null, null, null, null, 1, 10, 9, 5, null, null, null, null) == 1
     assert b"ldc" in lib.sv_last_error()
+
+
+def test_noalloc_capacity_and_argument_order(lib):
+    """The allocation-free chain verify: the shape its documentation quotes
+    (the large-vocabulary chain, B=256, N=7, V=128256) fits the static
+    scratch, and bad arguments get sv_verify_chain's statuses before the
+    capacity check (host-side only, no GPU)."""
+    cap = lib.sv_verify_chain_noalloc_max_bytes()
+    assert cap == 16 << 20
+    assert lib.sv_verify_chain_workspace(256, 7, 128256) <= cap
+    null = None
+    args = lambda B, N, V, dt=1, T=1.0: (null, null, dt, null, B, N, V, T, 0, 0, null, null, null,
+                                         null, null, null, null, null)
+    # an oversize request with a bad dtype / temperature / null outputs: the
+    # argument error wins, exactly as sv_verify_chain reports it
+    assert lib.sv_verify_chain_noalloc(*args(1 << 20, 7, 128256, dt=7)) == 1
+    assert lib.sv_verify_chain_noalloc(*args(1 << 20, 7, 128256, T=-1.0)) == 1
+    assert lib.sv_verify_chain_noalloc(*args(1 << 20, 7, 128256)) == 1      # null pointers
+    assert b"null" in lib.sv_last_error()
+    assert lib.sv_verify_chain_noalloc(*args(-1, 7, 128256)) == 1
+    assert lib.sv_verify_chain_noalloc(*args(0, 7, 128256)) == 0            # B = 0: no-op
+    assert lib.sv_verify_chain_noalloc(*args(4, 7, (1 << 22) + 1)) == 2     # V above the maximum
