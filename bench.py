@@ -340,14 +340,53 @@ def run_round(sv, wl, cfg, maxd, src, out, i, seed, step_no, ws, stream, side, e
 
 def run_ours(args):
     import torch
-    import speculative_decoding_verification_vocab_gb300 as sv
-    from speculative_decoding_verification_vocab_gb300 import synth
 
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
+    line = measure(args, rank, world, local)
+    if args.config == 5 and not (args.greedy or args.early_exit or args.graph or args.batch):
+        line["secondary"] = secondary(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+SECONDARY_STEPS = 50
+
+
+def secondary(args, rank, world, local):
+    """The large-vocabulary chain (B=256, N=7, V=128256), the workload the
+    bandwidth target names, measured in the same run as the headline line:
+    the full reading and the early-exit reading, each over SECONDARY_STEPS
+    timed steps (at least K) with its own row-pass roofline.  Device-resident
+    inputs only (no end-to-end or CPU legs)."""
+    import argparse as ap
+    out = {}
+    for name, early in (("config 3: large_vocab_chain", False),
+                        ("config 3: large_vocab_chain (early exit)", True)):
+        a = ap.Namespace(**vars(args))
+        a.config, a.early_exit, a.greedy, a.graph, a.batch = 3, early, False, False, 0
+        a.steps = max(args.steps, SECONDARY_STEPS)
+        a.no_e2e = a.no_cpu_baseline = True
+        m = measure(a, rank, world, local)
+        out[name] = {k: m[k] for k in ("value", "unit", "steps", "ms_per_step",
+                                       "accepted_tokens_per_s", "mean_accept_len",
+                                       "rows_read_per_s", "hbm_gbs", "hbm_frac_measured",
+                                       "roofline", "kernels", "repeats", "clocks",
+                                       "alg_bytes_per_step", "config")}
+    return out
+
+
+def measure(args, rank, world, local):
+    """One workload measured as the JSON line reports it (returns the dict)."""
+    import torch
+    import speculative_decoding_verification_vocab_gb300 as sv
+    from speculative_decoding_verification_vocab_gb300 import synth
+
     dev = torch.device("cuda", local)
     sv.load_library()
     cfg = synth.CONFIGS[args.config]
@@ -528,6 +567,9 @@ def run_ours(args):
                          f"logit rows from a pool of {args.pool} distinct rounds "
                          f"({args.pool * wl.rounds[0]['vq'].numel() * wl.esize * 2 / 1e9:.1f} GB)"},
         "accepted_tokens_per_s": total_tokens / (ms_max / 1e3),
+        # logit rows the row pass actually reads (verifier and draft rows on
+        # the path; `value` counts B*T tree slots, most of which are never read)
+        "rows_read_per_s": sum_over_ranks(stats_bytes / (V * wl.esize), world) / (ms_max / 1e3),
         "mean_emitted_per_seq": tokens / (K * B), "mean_accept_len": float(acc.mean()),
         "alpha_hat": alpha_hat,
         "us_per_round": 1e3 * ms_max / K,
@@ -547,14 +589,21 @@ def run_ours(args):
         "roofline": roofline,
         "clocks": clk.summary(),
     }
+    kv_launches, kv_ms = trace.get("kv_compact", (0, 0.0))
+    if wl.tree and kv_launches:
+        # the compaction runs on the side stream beside the sampling: its
+        # bandwidth inside the step (event pair on that stream, traced pass)
+        kv_gbs = (kv_bytes / K) / (kv_ms / kv_launches / 1e3) / 1e9
+        line["kv_compact_in_step"] = {"alg_bytes_per_launch": kv_bytes / K,
+                                      "avg_launch_ms": kv_ms / kv_launches, "achieved": kv_gbs,
+                                      "unit": "GB/s", "frac": kv_gbs / peak}
     if not args.no_e2e:
         line["e2e"] = e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, wl, cfg)
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    del wl
+    torch.cuda.empty_cache()
+    return line
 
 
 def e2e_ours(args, wl, cfg, sv, dev, stream, maxd, B, world):

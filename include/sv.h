@@ -403,6 +403,16 @@ sv_status sv_tree_attention(const void *q, const void *kv, const int32_t *base,
                             const uint64_t *mask, int B, int T, int Hq, int Hkv,
                             int D, int S, float scale, void *out, float *out_lse,
                             uint32_t *out_status, void *stream);
+/* sv_tree_attention with the limit of each pipeline wait given: wait_ns
+ * nanoseconds (0: the default 2 s).  The pages have no counterpart; it makes
+ * the timeout path reachable.  After a wait runs out, the kernel still lets
+ * every copy and product it has issued complete (each of those waits bounded
+ * by 2 s) before it releases tensor memory and exits, so the context stays
+ * usable; the affected sequences get SV_ROW_TIMEOUT. */
+sv_status sv_tree_attention_ex(const void *q, const void *kv, const int32_t *base,
+                               const uint64_t *mask, int B, int T, int Hq, int Hkv,
+                               int D, int S, float scale, void *out, float *out_lse,
+                               uint32_t *out_status, uint64_t wait_ns, void *stream);
 
 /* Thread-local message for the last non-OK status returned on this thread. */
 const char *sv_last_error(void);

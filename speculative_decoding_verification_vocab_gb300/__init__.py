@@ -27,7 +27,7 @@ EXPORTS = ("sv_verify_chain_workspace", "sv_verify_chain_workspace_host", "sv_ve
            "sv_verify_chain_early_exit",
            "sv_verify_chain_noalloc", "sv_verify_tree_workspace_host",
            "sv_verify_chain_noalloc_max_bytes", "sv_verify_tree_workspace",
-           "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_tree_attention", "sv_last_error",
+           "sv_verify_tree", "sv_tree_build_mask", "sv_kv_compact", "sv_tree_attention", "sv_tree_attention_ex", "sv_last_error",
            "sv_launch_count", "sv_trace_enable", "sv_trace_collect", "sv_tree_expand",
            "sv_tree_select", "sv_tree_finalize", "sv_tree_level")
 
@@ -93,6 +93,9 @@ def load_library(path: str = LIB_PATH):
     L.sv_tree_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp,
                                     vp, vp]
     L.sv_tree_attention.restype = i32
+    L.sv_tree_attention_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp,
+                                       vp, u64, vp]
+    L.sv_tree_attention_ex.restype = i32
     L.sv_last_error.argtypes = []
     L.sv_last_error.restype = C.c_char_p
     L.sv_launch_count.argtypes = []
@@ -248,6 +251,17 @@ def sv_tree_attention(q, kv, base, mask, scale, out, out_lse=None, out_status=No
     return _check(load_library().sv_tree_attention(
         _p(q), _p(kv), _p(base), _p(mask), B, T, Hq, Hkv, D, S, float(scale), _p(out),
         _p(out_lse), _p(out_status), _stream(stream)))
+
+
+def sv_tree_attention_ex(q, kv, base, mask, scale, out, out_lse=None, out_status=None,
+                         wait_ns=0, stream=None):
+    """sv_tree_attention with the limit of each device wait in nanoseconds
+    (0: the default 2 s)."""
+    B, T, Hq, D = q.shape
+    S, Hkv = kv.shape[2], kv.shape[3]
+    return _check(load_library().sv_tree_attention_ex(
+        _p(q), _p(kv), _p(base), _p(mask), B, T, Hq, Hkv, D, S, float(scale), _p(out),
+        _p(out_lse), _p(out_status), int(wait_ns), _stream(stream)))
 
 
 def sv_tree_expand(dlogits, frontier_score, K, out_token, out_score, temperature=1.0,
@@ -441,9 +455,10 @@ def tree_build_mask(parent, stream=None):
     return mask, depth
 
 
-def tree_attention(q, kv, base, mask, scale=None, return_lse=False, stream=None):
+def tree_attention(q, kv, base, mask, scale=None, return_lse=False, stream=None, wait_ns=0):
     """Tree-masked attention of one layer: returns out (like q), and with
-    return_lse the log-sum-exp [B][T][Hq] and the status words [B]."""
+    return_lse the log-sum-exp [B][T][Hq] and the status words [B].
+    wait_ns: limit of each device wait (0: the default 2 s)."""
     B, T, Hq, D = q.shape
     if scale is None:
         scale = D ** -0.5
@@ -451,7 +466,7 @@ def tree_attention(q, kv, base, mask, scale=None, return_lse=False, stream=None)
     out = torch.empty_like(q, device=dev)
     lse = torch.empty(B, T, Hq, dtype=torch.float32, device=dev) if return_lse else None
     status = torch.zeros(B, dtype=torch.int32, device=dev) if return_lse else None
-    sv_tree_attention(q, kv, base, mask, scale, out, lse, status, stream)
+    sv_tree_attention_ex(q, kv, base, mask, scale, out, lse, status, wait_ns, stream)
     return (out, lse, status) if return_lse else out
 
 

@@ -63,7 +63,7 @@ constexpr int kBarQ = 0, kBarK = 1, kBarV = kBarK + kStages, kBarKF = kBarV + kS
 constexpr uint32_t kColS = 0, kColO = 128, kColQ = 256, kColP = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;   // lazy rescale threshold (log2 units)
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s: default wait limit, and every drain's
 
 struct AttnArgs {
   const uint16_t *q;
@@ -75,6 +75,7 @@ struct AttnArgs {
   int B, T, Hq, Hkv, S, G, W, npt;  // npt = tree nodes per item = 128 / G
   int mtiles, n_items;              // query tiles per (sequence, KV head); items
   float scale_log2;                 // softmax scale * log2(e)
+  unsigned long long wait_ns;       // limit of each wait of the pipeline (drains: kWaitNs)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -98,15 +99,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase of `parity` to complete.  Gives up after kWaitNs
-// or as soon as another role of the CTA has given up (*abort != 0).
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
+// Bounded wait for the phase of `parity` to complete.  Gives up after
+// `limit` ns or as soon as another role of the CTA has given up (*abort != 0).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            unsigned long long limit) {
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (global_ns() - t0 > limit) {
         *abort = 1;
         return false;
       }
@@ -114,8 +116,16 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
   }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
+// Short limits (below 1 ms) poll with the non-blocking test and read the
+// clock every time: a blocking try_wait may itself suspend the thread longer
+// than such a limit.
+constexpr unsigned long long kShortWaitNs = 1000000ull;
+__device__ __noinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             unsigned long long limit);
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned long long limit = kWaitNs) {
+  if (limit < kShortWaitNs) return mbar_wait_short(bar, parity, abort, limit);
+  return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort, limit);
 }
 
 // Non-blocking test of the phase of `parity`.
@@ -128,6 +138,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_short(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             unsigned long long limit) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > limit) {
+      *abort = 1;
+      return false;
+    }
+  }
 }
 
 // One lane of the (converged) warp: true there, false elsewhere.
@@ -420,7 +443,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (x.n_tiles > 0) {
           // the item's query tile, once the softmax warps have read the last
           // one (the previous phase of kBarQF, already seen by this thread)
-          if (nq > 0 && !mbar_wait(bar(kBarQF), (nq - 1) & 1, abort)) {
+          if (nq > 0 && !mbar_wait(bar(kBarQF), (nq - 1) & 1, abort, a.wait_ns)) {
             atomicMin(const_cast<int *>(abort_item), it);
             break;
           }
@@ -461,7 +484,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             t_last = global_ns();
             continue;
           }
-          if (*abort || global_ns() - t_last > kWaitNs) {
+          if (*abort || global_ns() - t_last > a.wait_ns) {
             *abort = 1;
             atomicMin(const_cast<int *>(abort_item), it);
             stop = true;
@@ -505,14 +528,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mma_commit(bar(kBarKF + g % kStages));
     };
     auto wait_s_ready = [&](int g) -> bool {  // K_g landed, S_{g-1} read out
-      return (g < 1 || mbar_wait(bar(kBarSF), (g - 1) & 1, abort)) &&
-             mbar_wait(bar(kBarK + g % kStages), (g / kStages) & 1, abort);
+      return (g < 1 || mbar_wait(bar(kBarSF), (g - 1) & 1, abort, a.wait_ns)) &&
+             mbar_wait(bar(kBarK + g % kStages), (g / kStages) & 1, abort, a.wait_ns);
     };
     int it = blockIdx.x;
     for (; ok && it < a.n_items; it += gridDim.x) {
       const Item x = decode_item(a, it);
       if (x.n_tiles == 0) continue;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQ), nq & 1, abort));  // this item's Q
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQ), nq & 1, abort, a.wait_ns));  // this item's Q
       ++nq;
       if (!ok) break;
       tc_fence_after();
@@ -532,8 +555,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ++gS;
         }
         ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar(kBarP + (gP & 1)), (gP >> 1) & 1, abort) &&
-                            mbar_wait(bar(kBarV + gP % kStages), (gP / kStages) & 1, abort));
+                        mbar_wait(bar(kBarP + (gP & 1)), (gP >> 1) & 1, abort, a.wait_ns) &&
+                            mbar_wait(bar(kBarV + gP % kStages), (gP / kStages) & 1, abort, a.wait_ns));
         if (!ok) break;
         // the last tile's PV runs only the K16 steps holding keys below
         // n_keys; value rows past the last key inside the last step may hold
@@ -617,7 +640,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // swizzled: row r32, chunk c at (c ^ (r32 & 7)) * 16; rows past T are
         // the copy's zero fill), into tensor memory as bf16 pairs (32x32b:
         // lane = row); the item's S products wait for all eight warps
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQS), nq & 1, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQS), nq & 1, abort, a.wait_ns));
         ++nq;
         if (!ok) break;
         uint32_t qv[32];
@@ -662,7 +685,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float l[2] = {0.0f, 0.0f};            // partial sums over this thread's columns
       for (int j = 0; j < x.n_tiles; ++j) {
         const int g = gT + j, pb = g & 1;
-        ok = mbar_wait(bar(kBarS), g & 1, abort);
+        ok = mbar_wait(bar(kBarS), g & 1, abort, a.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -748,7 +771,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // PV_{g-2} has retired: P buffer pb is free (this warp has seen
           // every earlier phase of its barrier)
           const int i = g - 2;
-          ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+          ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort, a.wait_ns);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
@@ -757,7 +780,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // these rows of it to the new reference
           if (j >= 1) {
             const int i = g - 1;
-            ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+            ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort, a.wait_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
           }
@@ -780,7 +803,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (ok) {
         const int i = gT + x.n_tiles - 1;
-        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort);
+        ok = mbar_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort, a.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (ok) {
@@ -876,10 +899,10 @@ sv_status encode4(CUtensorMap *m, const void *base, const cuuint64_t dims[4],
 
 using namespace sv;
 
-extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int32_t *base,
-                                       const uint64_t *mask, int B, int T, int Hq, int Hkv, int D,
-                                       int S, float scale, void *out, float *out_lse,
-                                       uint32_t *out_status, void *stream) {
+extern "C" sv_status sv_tree_attention_ex(const void *q, const void *kv, const int32_t *base,
+                                          const uint64_t *mask, int B, int T, int Hq, int Hkv,
+                                          int D, int S, float scale, void *out, float *out_lse,
+                                          uint32_t *out_status, uint64_t wait_ns, void *stream) {
   if (B < 0 || T < 1 || Hq < 1 || Hkv < 1 || S < 1)
     return set_error(SV_ERR_INVALID_ARG, "need B >= 0, T >= 1, Hq >= 1, Hkv >= 1, S >= 1");
   if (T > SV_MAX_TREE_NODES) return set_error(SV_ERR_UNSUPPORTED, "T > %d", SV_MAX_TREE_NODES);
@@ -942,6 +965,7 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
   a.W = (T + 63) / 64;
   a.npt = npt;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = wait_ns ? wait_ns : kWaitNs;
   const int mtiles = (T + npt - 1) / npt;
   const long long n_items = (long long)mtiles * Hkv * B;
   if (n_items > 0x7fffffffLL) return set_error(SV_ERR_UNSUPPORTED, "too many query tiles");
@@ -953,4 +977,12 @@ extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int3
   return check_launch("tree_attention",
                       launch_pdl(tree_attn_kernel, dim3(grid), dim3(kAttnThreads),
                                  kAttnSmem, st, tq, tkv, a));
+}
+
+extern "C" sv_status sv_tree_attention(const void *q, const void *kv, const int32_t *base,
+                                       const uint64_t *mask, int B, int T, int Hq, int Hkv, int D,
+                                       int S, float scale, void *out, float *out_lse,
+                                       uint32_t *out_status, void *stream) {
+  return sv_tree_attention_ex(q, kv, base, mask, B, T, Hq, Hkv, D, S, scale, out, out_lse,
+                              out_status, 0, stream);
 }

@@ -212,3 +212,24 @@ def test_attention_full_size_sampled_rows():
         qk = (np.abs(kf[i, :nk, kh]) @ np.abs(qf[i, n, h])).max()
         bound = gamma * D ** -0.5 * qk + (nk + 2) * U32 + 2.0 ** -21 + 1e-6
         assert abs(l[i, n, h] - rlse[k]) <= bound
+
+
+def test_attention_wait_limit_runs_out_and_the_context_survives():
+    """The timeout path, reached in the allowed way: every pipeline wait is
+    given a limit of 1 ns (sv_tree_attention_ex), so the first wait that is
+    not already satisfied gives up.  The call returns, the sequence carries
+    SV_ROW_TIMEOUT, the copies and products already issued still complete
+    (the kernel's drains keep their 2 s bound), and a normal call straight
+    after it on the same context matches the oracle."""
+    B, T, Hq, Hkv, S = 1, 4, 8, 2, 256
+    q, kv, base = synth.attention_inputs(B, T, Hq, Hkv, 128, S, [200], seed=11)
+    parent = torch.tensor([[-1, 0, 0, 1]], dtype=torch.int32)
+    mask, _ = sv.tree_build_mask(parent.to(DEV))
+    out, lse, st = sv.tree_attention(q.to(DEV), kv.to(DEV), base.to(DEV), mask, 128 ** -0.5,
+                                     return_lse=True, wait_ns=1)
+    torch.cuda.synchronize()
+    assert int(st[0]) & sv.SV_ROW_TIMEOUT
+    # the context is usable: a normal call on the same inputs is exact
+    out, lse, st, ref, rlse, _ = _run(q, kv, base, parent, 128 ** -0.5)
+    assert int(st.count_nonzero()) == 0
+    _check(q, kv, base, out, lse, ref, rlse, 128 ** -0.5, T)
