@@ -132,20 +132,36 @@ struct SegInfo {
   size_t out;        // partial index
 };
 
+// Tree rows known before the best path is: each sequence's root rows (the
+// verifier row of node 0, and its draft row when a path can go deeper), which
+// are row slots 0 and maxpos + 1 of every path.
+__device__ __forceinline__ int root_rows(const Round &r, bool greedy) {
+  return (greedy || r.maxpos == 0) ? 1 : 2;
+}
+
+// Row index space of a row pass: a chain's rows b * P + j; a tree's root rows
+// first (R0 per sequence, row_i < R0 B), then the rows tree_path listed.
 template <typename E>
 __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t *rowlist,
-                                            int row_i, int seg) {
+                                            int row_i, int seg, int R0 = 0) {
   int b, j;
-  if (rowlist) {
-    const int e = rowlist[row_i];
+  const E *row;
+  if (rowlist && row_i < R0 * r.B) {
+    b = row_i / R0;
+    const bool is_v = row_i - b * R0 == 0;
+    j = is_v ? 0 : r.maxpos + 1;
+    row = (const E *)(is_v ? r.vlog : r.dlog) + (size_t)b * (is_v ? r.v_rows : r.d_rows) * r.V;
+  } else if (rowlist) {
+    const int e = rowlist[row_i - R0 * r.B];
     b = e >> 12;
     j = slot_of_active(e & 0xfff, round_npos(r, b), r.maxpos);
+    row = src_row<E>(r, b, j);
   } else {
     b = row_i / r.P;
     j = row_i - b * r.P;
+    row = src_row<E>(r, b, j);
   }
   SegInfo si;
-  const E *row = src_row<E>(r, b, j);
   si.row = (const char *)row;
   si.copy = r.copy ? (char *)used_row<E>(r, b, j, row) : nullptr;
   si.v0 = seg * seg_elems<E>();
@@ -161,9 +177,9 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
 // statistics of segment seg of listed row row_i, by the whole CTA
 template <typename E, bool kCopy>
 __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_t *rowlist,
-                                             int row_i, int seg, float4 *partial) {
+                                             int row_i, int seg, float4 *partial, int R0 = 0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg);
+  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg, R0);
   const E *row = (const E *)si.row;
   const float k = r.k;
   StatState st{-INFINITY, 0.0f, 0ull, 0ull};
@@ -240,15 +256,34 @@ template <typename E, bool kCopy>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
-                 unsigned *__restrict__ qc) {
+                 unsigned *__restrict__ qc, int nroot) {
+  // Tree: the root-row CTAs need nothing from tree_path, the grid before this
+  // one, so they start streaming without waiting for it (this grid can only
+  // launch once tree_path's CTAs have passed their own wait for the grids
+  // before it, so the workspace is free).  The listed-row CTAs wait.
+  if (!rowlist) {
+    // chain: one CTA per (row = x, segment = y)
+    grid_dep_sync();
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 3) qc[threadIdx.x] = 0u;
+    stat_segment<E, kCopy>(r, G, nullptr, blockIdx.x, blockIdx.y, partial);
+    return;
+  }
+  // tree: segment = x, row CTA = y, so that CTAs are dispatched root rows
+  // first (x runs fastest); gridDim.y = nroot root CTAs + the listed-row CTAs
+  const int R0 = root_rows(r, false), nroot_rows = R0 * r.B;
+  if ((int)blockIdx.y < nroot) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the sampler's lists and item counter are rebuilt by the accept walk
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 3) qc[threadIdx.x] = 0u;
+    for (int row_i = blockIdx.y; row_i < nroot_rows; row_i += nroot)
+      stat_segment<E, kCopy>(r, G, rowlist, row_i, blockIdx.x, partial, R0);
+    return;
+  }
   grid_dep_sync();
-  // the sampler's lists and item counter are rebuilt by the accept walk
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 3) qc[threadIdx.x] = 0u;
-  // chain: one row per CTA (exact grid); tree: the grid covers half the row
-  // slots and a CTA takes a second listed row when the paths are deep
-  const int nrows = rowlist ? *rowcount : (int)gridDim.x;
-  for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
-    stat_segment<E, kCopy>(r, G, rowlist, row_i, blockIdx.y, partial);
+  // the listed rows, a CTA taking further rows when the paths are deep
+  const int ncta = (int)gridDim.y - nroot, nrows = *rowcount;
+  for (int li = (int)blockIdx.y - nroot; li < nrows; li += ncta)
+    stat_segment<E, kCopy>(r, G, rowlist, nroot_rows + li, blockIdx.x, partial, R0);
 }
 
 Layout plan(int B, int maxpos, int V, bool tree) {
@@ -636,10 +671,9 @@ __device__ __forceinline__ void arg_word<float>(ArgState &a, uint4 w, int v) {
 
 template <typename E>
 __device__ __forceinline__ void argmax_segment(const Round &r, int G, const int32_t *rowlist,
-                                               int row_i, float4 *partial) {
-  const int seg = blockIdx.y;
+                                               int row_i, int seg, float4 *partial, int R0 = 0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg);
+  const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg, R0);
   const E *row = (const E *)si.row;
   ArgState a{-INFINITY, 0x7fffffff, 0u};
   const int nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
@@ -709,11 +743,26 @@ __device__ __forceinline__ void argmax_segment(const Round &r, int G, const int3
 template <typename E>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
 row_argmax_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
-                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial) {
+                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
+                  int nroot) {
+  if (!rowlist) {  // chain: one CTA per (row = x, segment = y)
+    grid_dep_sync();
+    argmax_segment<E>(r, G, nullptr, blockIdx.x, blockIdx.y, partial);
+    return;
+  }
+  // tree, as row_stats: segment = x, row CTA = y, the root rows (which need
+  // nothing from tree_path) first
+  const int nroot_rows = root_rows(r, true) * r.B;
+  if ((int)blockIdx.y < nroot) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int row_i = blockIdx.y; row_i < nroot_rows; row_i += nroot)
+      argmax_segment<E>(r, G, rowlist, row_i, blockIdx.x, partial, 1);
+    return;
+  }
   grid_dep_sync();
-  const int nrows = rowlist ? *rowcount : (int)gridDim.x;
-  for (int row_i = blockIdx.x; row_i < nrows; row_i += gridDim.x)
-    argmax_segment<E>(r, G, rowlist, row_i, partial);
+  const int ncta = (int)gridDim.y - nroot, nrows = *rowcount;
+  for (int li = (int)blockIdx.y - nroot; li < nrows; li += ncta)
+    argmax_segment<E>(r, G, rowlist, nroot_rows + li, blockIdx.x, partial, 1);
 }
 
 // arg max of verifier row slot j of sequence b from its G segment partials
@@ -1577,8 +1626,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     if (lane == 0) {
       pth[0] = 0;
       npos[b] = 0;
-      tstat[b] = SV_ROW_BAD_TREE;
-      rowlist[atomicAdd(rowcount, 1)] = b << 12;  // the root row only
+      tstat[b] = SV_ROW_BAD_TREE;  // (its root rows are read by their own CTAs)
     }
     return;
   }
@@ -1617,16 +1665,29 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   // the path and its tested tokens token[n_1..n_D], written in parallel
   for (int i = lane; i <= D; i += 32) pth[i] = pn[i];
   for (int i = lane; i < D; i += 32) tok[(size_t)b * tok_stride + i] = tk[pn[i + 1]];
+  // the path's rows other than the root's (those have their own CTAs): the
+  // verifier rows n_1..n_D, then (stochastic rule) the draft rows n_1..n_{D-1}
+  const int nrow = D == 0 ? 0 : (greedy ? D : 2 * D - 1);
   int base = 0;
   if (lane == 0) {
     npos[b] = D;
     tstat[b] = 0u;
-    base = atomicAdd(rowcount, greedy ? D + 1 : 2 * D + 1);
+    if (nrow) base = atomicAdd(rowcount, nrow);
   }
   base = __shfl_sync(0xffffffffu, base, 0);
-  // the verifier rows n_0..n_D, then (stochastic rule) the draft rows
-  const int nrow = greedy ? D + 1 : 2 * D + 1;
-  for (int a = lane; a < nrow; a += 32) rowlist[base + a] = (b << 12) | a;
+  for (int k = lane; k < nrow; k += 32)
+    rowlist[base + k] = (b << 12) | (k < D ? k + 1 : D + 2 + (k - D));
+}
+
+// ---------------------------------------------------------------------------
+// Tree row-pass grids: gridDim.y holds the root-row CTAs then the listed-row
+// CTAs (at most 65535 in all); either kind loops when there are more rows.
+int tree_root_ctas(int root_rows) { return root_rows < 32768 ? root_rows : 32768; }
+int tree_list_ctas(int list_slots, int nroot) {
+  // half as many CTAs as listed-row slots: one takes a second row when the
+  // paths are deep
+  const int want = (list_slots + 1) / 2 > 0 ? (list_slots + 1) / 2 : 1;
+  return want < 65535 - nroot ? want : 65535 - nroot;
 }
 
 // ---------------------------------------------------------------------------
@@ -1706,14 +1767,19 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
     // tree: B * P row slots bound the listed rows; half as many CTAs per
     // segment, each taking a second row when the paths are deep
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
-    const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
+    dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
+    int nroot = 0;
+    if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
+      const int R0 = r.maxpos == 0 ? 1 : 2;  // root rows per sequence (root_rows)
+      nroot = tree_root_ctas(R0 * r.B);
+      grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - R0), nroot)));
+    }
     LaunchScope ls("row_stats", st);
     s = check_launch("row_stats", launch_pdl(r.copy ? row_stats_kernel<E, true>
                                                     : row_stats_kernel<E, false>,
-                                             dim3(gx, (unsigned)G),
-                                             dim3(kRsThreads), 0, st, r, G, rowlist,
+                                             grid, dim3(kRsThreads), 0, st, r, G, rowlist,
                                              (const int *)(ws + L.ctr), partial,
-                                             (unsigned *)(ws + L.qc)));
+                                             (unsigned *)(ws + L.qc), nroot));
     if (s != SV_OK) return s;
   }
   {
@@ -1748,11 +1814,16 @@ sv_status run_verify_greedy(const Round &r, const Layout &L, char *ws, const Dec
   sv_status s;
   {
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
-    const unsigned gx = rowlist ? (unsigned)((r.B * r.P + 1) / 2) : (unsigned)(r.B * r.P);
+    dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
+    int nroot = 0;
+    if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
+      nroot = tree_root_ctas(r.B);
+      grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - 1), nroot)));
+    }
     LaunchScope ls("row_argmax", st);
-    s = check_launch("row_argmax", launch_pdl(row_argmax_kernel<E>, dim3(gx, (unsigned)G),
-                                              dim3(kRsThreads), 0, st, r, G, rowlist,
-                                              (const int *)(ws + L.ctr), partial));
+    s = check_launch("row_argmax", launch_pdl(row_argmax_kernel<E>, grid, dim3(kRsThreads), 0,
+                                              st, r, G, rowlist, (const int *)(ws + L.ctr),
+                                              partial, nroot));
     if (s != SV_OK) return s;
   }
   {
