@@ -91,6 +91,7 @@ struct KvArgs {
   int inplace, vec, copy;
   int ncol;             // units per row: 16-byte words (vec) or bytes
   int step_sl, step_c;  // kKvThreads units = step_sl rows + step_c units
+  int mcap;             // room for moves in shared memory: min(P, kKvMaxRows), >= 1
 };
 
 struct KvCursor {
@@ -116,7 +117,9 @@ __global__ void __launch_bounds__(kKvThreads) kv_compact_kernel(KvArgs a) {
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
   __shared__ int s_ok, s_nm;
-  __shared__ int s_src[kKvMaxRows], s_dst[kKvMaxRows];
+  // the moves (at most min(P, kKvMaxRows) per sequence): sources, then targets
+  extern __shared__ int s_moves[];
+  int *s_src = s_moves, *s_dst = s_moves + a.mcap;
   if (threadIdx.x < 32) {
     const int n = a.n_rows[b] + a.n_add;
     const int sb = a.src_base[b], db = a.dst_base[b];
@@ -276,8 +279,11 @@ extern "C" sv_status sv_kv_compact(const void *src_kv, void *dst_kv, int L, int 
   a.step_sl = kKvThreads / a.ncol;
   a.step_c = kKvThreads % a.ncol;
   const unsigned gy = a.copy ? (unsigned)((2 * L + kKvSlabs - 1) / kKvSlabs) : 1u;
+  // shared memory for the move lists sized by P (a few rows for a tree path),
+  // so that the copy CTAs fit beside other kernels' CTAs on an SM
+  a.mcap = P < kKvMaxRows ? (P > 0 ? P : 1) : kKvMaxRows;
   cudaStream_t st = (cudaStream_t)stream;
   LaunchScope ls("kv_compact", st);
-  return check_launch("kv_compact",
-                      launch_pdl(kv_compact_kernel, dim3(B, gy), dim3(kKvThreads), 0, st, a));
+  return check_launch("kv_compact", launch_pdl(kv_compact_kernel, dim3(B, gy), dim3(kKvThreads),
+                                               2 * (size_t)a.mcap * sizeof(int), st, a));
 }

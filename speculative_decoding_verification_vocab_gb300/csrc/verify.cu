@@ -1590,24 +1590,38 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
 
 // ---------------------------------------------------------------------------
 // tree_path: one warp per sequence.  Validates the tree, walks best children
-// (highest score; ties to the lower slot) at most max_depth steps.
+// (highest score; ties to the lower slot) at most max_depth steps.  Every
+// node's best child comes from one parallel pass (a 64-bit shared-memory
+// maximum per parent of the key (score in a monotone integer order, ~slot)),
+// so the walk itself is a chain of max_depth shared-memory loads.
+__device__ __forceinline__ unsigned long long child_key(float s, int c) {
+  const unsigned u = __float_as_uint(__fadd_rn(s, 0.0f));  // -0 joins +0: they compare equal
+  const unsigned o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (0xffffffffu - (unsigned)c);
+}
+
 __global__ void __launch_bounds__(32)
 tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__ token,
                  const float *__restrict__ score, int B, int T, int max_depth,
                  int32_t *__restrict__ path, int32_t *__restrict__ npos,
                  int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
                  int32_t *__restrict__ rowlist, int *__restrict__ rowcount, int greedy) {
-  grid_dep_sync();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x, lane = threadIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
   __shared__ float sc[SV_MAX_TREE_NODES];
   __shared__ int32_t tk[SV_MAX_TREE_NODES];
+  __shared__ unsigned long long best[SV_MAX_TREE_NODES];  // 0: no child
   __shared__ int32_t pn[SV_MAX_POSITIONS + 1];  // the path, written out at the end
   for (int c = lane; c < T; c += 32) {  // one coalesced pass over the tree
     pa[c] = parent[(size_t)b * T + c];
     sc[c] = score[(size_t)b * T + c];
     tk[c] = token[(size_t)b * T + c];
+    best[c] = 0ull;
   }
+  // the next grid (the row pass) starts streaming its root rows once this
+  // grid's few loads have returned, not while they are in flight
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncwarp();
   bool ok = true;
   for (int c = lane; c < T; c += 32) {
@@ -1630,37 +1644,25 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     }
     return;
   }
-  int cur = 0, D = 0;
-  if (lane == 0) pn[0] = 0;
-  while (D < max_depth) {
-    bool have = false;
-    float bs = 0.0f;
-    int bi = 0x7fffffff;
-    for (int c = 1 + lane; c < T; c += 32) {
-      if (pa[c] != cur) continue;
-      const float sv = sc[c];
-      if (!have || sv > bs || (sv == bs && c < bi)) {
-        have = true;
-        bs = sv;
-        bi = c;
-      }
-    }
-#pragma unroll
-    for (int o2 = 16; o2; o2 >>= 1) {
-      const int oh = __shfl_xor_sync(0xffffffffu, (int)have, o2);
-      const float os = __shfl_xor_sync(0xffffffffu, bs, o2);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o2);
-      if (oh && (!have || os > bs || (os == bs && oi < bi))) {
-        have = true;
-        bs = os;
-        bi = oi;
-      }
-    }
-    if (!have) break;
-    ++D;
-    cur = bi;
-    if (lane == 0) pn[D] = bi;
+  // valid tree: every live node c > 0 has a live parent p < c and a score
+  // that is not NaN, so the keys order exactly as the scores do
+  for (int c = 1 + lane; c < T; c += 32) {
+    const int p = pa[c];
+    if (p >= 0) atomicMax(&best[p], child_key(sc[c], c));
   }
+  __syncwarp();
+  int D = 0;
+  if (lane == 0) {
+    int cur = 0;
+    pn[0] = 0;
+    while (D < max_depth) {
+      const unsigned long long k = best[cur];
+      if (k == 0ull) break;
+      cur = (int)(0xffffffffu - (unsigned)k);
+      pn[++D] = cur;
+    }
+  }
+  D = __shfl_sync(0xffffffffu, D, 0);
   __syncwarp();
   // the path and its tested tokens token[n_1..n_D], written in parallel
   for (int i = lane; i <= D; i += 32) pth[i] = pn[i];
