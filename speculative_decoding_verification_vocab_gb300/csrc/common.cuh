@@ -277,4 +277,67 @@ __device__ __forceinline__ unsigned long long exp32x2(unsigned long long a2) {
   return f2_pack(e0, e1);
 }
 
+// ---------------------------------------------------------------- bulk ring
+// mbarrier primitives of a shared-memory ring filled by TMA bulk copies, every
+// wait bounded by kRingWaitNs
+constexpr unsigned long long kRingWaitNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ unsigned long long ring_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t ring_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ring_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void ring_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// an arrival that also expects `bytes` of bulk copies to complete on the barrier
+__device__ __forceinline__ void ring_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// TMA bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global into this CTA's shared memory, completing on `bar`
+__device__ __forceinline__ void ring_bulk(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool ring_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity`; false (and *abort set) when it runs
+// out or another warp of the CTA has given up.
+static __device__ __noinline__ bool ring_wait_slow(uint32_t bar, uint32_t parity,
+                                               volatile int *abort) {
+  const unsigned long long t0 = ring_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ring_try(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort) return false;
+      if (ring_ns() - t0 > kRingWaitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return ring_try(bar, parity) || ring_wait_slow(bar, parity, abort);
+}
+
 }  // namespace sv

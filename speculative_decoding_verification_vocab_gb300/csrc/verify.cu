@@ -94,9 +94,11 @@ __device__ __forceinline__ const E *used_row(const Round &r, int b, int j, const
 }
 
 // ---------------------------------------------------------------------------
-// row_stats: online softmax statistics of every used logit row.
-// One CTA per (row, kSegElems-element segment); grid x = row (tree: the rows
-// on the best paths, listed by tree_path), y = segment.  Each thread loads
+// row_stats: online softmax statistics of every used logit row, per
+// (row, segment) unit.  Logits in device memory go through the persistent
+// bulk-ring kernel further below; host-resident logits (read in place over
+// the host link) through one CTA per unit: grid x = row (tree: the rows on
+// the best paths, listed by tree_path), y = segment.  Each thread loads
 // kRsUnroll 16-byte words at once, takes the batch maximum on packed pairs,
 // moves its log2-domain reference only when that maximum exceeds the running
 // one, and folds the batch into a sum of exp2(fma(x, k, -ref)) with packed
@@ -107,13 +109,9 @@ __device__ __forceinline__ const E *used_row(const Round &r, int b, int j, const
 // position j (j <= maxpos) or the draft row of position j - maxpos - 1.
 constexpr int kSegElems = 8192;  // smallest segment (fp32); sizes the workspace
 constexpr int kRsThreads = 128;
-// A thread owns 2 * kRsUnroll 16-byte words of a segment: the first
-// kRsUnroll go to registers, the second are staged into shared memory by
-// asynchronous copies issued first, so a CTA keeps 32 KB of loads in flight
-// while holding only 32 words of registers per thread.  Segments of 32 KB
-// (128 threads, 10 CTAs/SM) rather than 64 KB: twice the CTAs of half the
-// work even out the end of a launch (row pass 0.86 -> 0.95 of the copy
-// bandwidth on the large-vocabulary chain).
+// A segment is 32 KB: 2 * kRsUnroll 16-byte words for each of 128 threads.
+// (The early-exit and arg-max passes still take one segment per CTA, half of
+// each thread's words staged into shared memory by cp.async.)
 template <typename E>
 __host__ __device__ constexpr int seg_elems() {
   return kRsThreads * 2 * kRsUnroll * 16 / (int)sizeof(E);
@@ -203,24 +201,6 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
   const uint4 *body = (const uint4 *)si.ab;
   const int nv = (int)((si.ae - si.ab) / 16);
   int i = tid;
-  if (!kCopy && r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
-    // full pattern: the second half through shared memory (each thread reads
-    // back only the slots it copied, so its own wait is the only sync needed)
-    __shared__ uint4 sbuf[kRsUnroll][kRsThreads];
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j)
-      cp_async16(&sbuf[j][tid], body + i + (kRsUnroll + j) * kRsThreads);
-    cp_async_commit();
-    uint4 buf[kRsUnroll];
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
-    stat_batch<E>(buf, st, k);
-    cp_async_wait_all();
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) buf[j] = sbuf[j][tid];
-    stat_batch<E>(buf, st, k);
-    i += 2 * kRsUnroll * kRsThreads;
-  }
   for (; i + (kRsUnroll - 1) * kRsThreads < nv; i += kRsUnroll * kRsThreads) {
     uint4 buf[kRsUnroll];
 #pragma unroll
@@ -286,6 +266,228 @@ row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
     stat_segment<E, kCopy>(r, G, rowlist, nroot_rows + li, blockIdx.x, partial, R0);
 }
 
+// ---------------------------------------------------------------------------
+// row_stats over logits in device memory: a persistent grid, one TMA bulk
+// ring per CTA.  The units are the same (row, segment) pairs as above, in the
+// same index space (tree: root rows, then the rows tree_path listed), taken by
+// CTA c in the order c, c + gridDim.x, ...; every segment's body is one
+// 16-byte-aligned run of at most 32 KB.
+//   producer (one thread of warp 4)  claims the CTA's next unit, waits until
+//              its stage is released, writes the unit's description and
+//              starts bulk copies of the body into the stage (arrival with
+//              the byte count on the stage's "full" barrier)
+//   consumers (warps 0-3)  wait for a full stage, fold its words into their
+//              statistics exactly as the CTA-per-segment kernel does (thread
+//              t takes words t + 128 j), release the stage, read any ragged
+//              head / tail elements directly, and combine the CTA's triples
+//              into the segment's partial
+// So every SM keeps the next stages' bytes in flight while it computes the
+// current one, and no CTA waits for a whole segment before starting the next.
+// Tree: the root units need nothing from tree_path; the producer waits for
+// it (griddepcontrol.wait) only when it first reaches a listed unit.  A wait
+// that runs out (kRingWaitNs) stops the CTA; the partials of its remaining
+// units are written as NaN sums with .w = 1, which the accept walk reports as
+// SV_ROW_TIMEOUT.
+constexpr int kRbStages = 4;
+constexpr int kRbChunk = 16384;  // bytes per stage: half a 32 KB segment
+constexpr int kRbConsumers = 128;              // 4 consumer warps
+constexpr int kRbThreads = kRbConsumers + 32;  // + the producer warp
+static_assert(kRbChunk % (16 * kRbConsumers) == 0, "a chunk is whole words of every consumer");
+
+struct RbMeta {
+  const char *row;   // row base
+  int v0, v1;        // element range of the segment
+  int nhead, ntail;  // ragged elements before / after the staged body
+  int w0, w1;        // the body words of this chunk (segment-relative)
+  int first, last;   // the chunk opens / closes its segment
+  int end;           // 1: no further unit (consumers stop)
+  size_t out;        // partial index
+};
+struct RbSmem {
+  unsigned long long full[kRbStages], empty[kRbStages], reduced[kRbStages];
+  RbMeta meta[kRbStages];
+  float4 red[kRbStages][kRbConsumers / 32];
+  int abort;
+};
+
+// unit u of a row pass: its row / segment and where its partial goes
+template <typename E>
+__device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const int32_t *rowlist, int R0,
+                                           long long u) {
+  const int row_i = (int)(u / G), seg = (int)(u - (long long)row_i * G);
+  return rowlist ? seg_info<E>(r, G, rowlist, row_i, seg, R0)
+                 : seg_info<E>(r, G, nullptr, row_i, seg);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kRbThreads)
+row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+                      const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
+                      unsigned *__restrict__ qc) {
+  extern __shared__ __align__(128) uint4 rb_stage[];  // [kRbStages][kRbChunk]
+  __shared__ RbSmem sm;
+  constexpr int kCW = kRbChunk / 16;  // words per stage
+  const int tid = threadIdx.x;
+  const bool tree = rowlist != nullptr;
+  const int R0 = tree ? root_rows(r, false) : 0;
+  if (!tree)
+    grid_dep_sync();  // chain: the workspace is free once the previous step's grids are done
+  else
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0 && tid < 3) qc[tid] = 0u;  // the sampler's counters, rebuilt by the walk
+  if (tid == 0) {
+    for (int i = 0; i < kRbStages; ++i) {
+      ring_init(ring_addr(&sm.full[i]), 1);
+      ring_init(ring_addr(&sm.empty[i]), kRbConsumers);
+      ring_init(ring_addr(&sm.reduced[i]), kRbConsumers / 32);
+    }
+    sm.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  volatile int *abort = &sm.abort;
+  long long n_units = tree ? (long long)R0 * r.B * G : (long long)r.B * r.P * G;
+  bool waited = !tree;
+  if (tid >= kRbConsumers) {
+    // ---------------------------------------------------------------- producer
+    if (tid != kRbConsumers) return;
+    long long k = 0;  // stages filled so far
+    bool done = false;
+    for (long long j = 0; !done; ++j) {  // the CTA's j-th unit
+      const long long u = blockIdx.x + j * (long long)gridDim.x;
+      if (u >= n_units && !waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+        n_units += (long long)__ldcg(rowcount) * G;
+      }
+      RbMeta m;
+      m.end = u >= n_units;
+      int nc = 1, nw = 0;
+      SegInfo si;
+      if (!m.end) {
+        si = rb_unit<E>(r, G, rowlist, R0, u);
+        const E *row = (const E *)si.row;
+        m.row = si.row;
+        m.v0 = si.v0;
+        m.v1 = si.v1;
+        m.nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
+        m.ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
+        m.out = si.out;
+        nw = (int)((si.ae - si.ab) / 16);
+        nc = nw > kCW ? (nw + kCW - 1) / kCW : 1;
+      }
+      for (int c = 0; c < nc; ++c, ++k) {
+        const int stage = (int)(k % kRbStages);
+        const long long use = k / kRbStages;
+        if (use > 0 &&
+            !ring_wait(ring_addr(&sm.empty[stage]), (uint32_t)((use - 1) & 1), abort)) {
+          done = true;
+          break;
+        }
+        const uint32_t full = ring_addr(&sm.full[stage]);
+        if (m.end) {
+          sm.meta[stage] = m;
+          ring_arrive(full);
+          ++k;
+          done = true;
+          break;
+        }
+        m.w0 = c * kCW;
+        m.w1 = min(nw, m.w0 + kCW);
+        m.first = c == 0;
+        m.last = c == nc - 1;
+        sm.meta[stage] = m;
+        const uint32_t bytes = (uint32_t)(m.w1 - m.w0) * 16u;
+        if (bytes) {
+          ring_expect_tx(full, bytes);
+          ring_bulk(ring_addr(rb_stage + (size_t)stage * kCW), (const uint4 *)si.ab + m.w0, bytes,
+                    full);
+        } else {
+          ring_arrive(full);
+        }
+      }
+    }
+    // copies issued for the last kRbStages stages land before the CTA's
+    // shared memory is released (at once unless a wait ran out)
+    for (long long kk = k - 1; kk >= 0 && kk >= k - kRbStages; --kk) {
+      const uint32_t bar = ring_addr(&sm.full[kk % kRbStages]);
+      const unsigned long long t0 = ring_ns();
+      while (!ring_try(bar, (uint32_t)((kk / kRbStages) & 1)) && ring_ns() - t0 < kRingWaitNs) {
+      }
+    }
+    return;
+  }
+  // ------------------------------------------------------------------ consumers
+  const int warp = tid >> 5, lane = tid & 31;
+  const float k2 = r.k;
+  long long j = 0;  // units finished (their partials written)
+  // a stage's reduction barrier completes once per unit that ends in it, not
+  // once per use: bit s is the parity of stage s's next reduction
+  unsigned rpar = 0u;
+  StatState st{-INFINITY, 0.0f, 0ull, 0ull};
+  for (long long k = 0;; ++k) {
+    const int stage = (int)(k % kRbStages);
+    const uint32_t ph = (uint32_t)((k / kRbStages) & 1);
+    if (!ring_wait(ring_addr(&sm.full[stage]), ph, abort)) break;
+    const RbMeta m = sm.meta[stage];
+    if (m.end) break;
+    if (m.first) {
+      st = StatState{-INFINITY, 0.0f, 0ull, 0ull};
+      const E *row = (const E *)m.row;
+      if (tid < m.nhead) stat1(elem_to_f32(__ldg(row + m.v0 + tid)), st, k2);
+      if (tid < m.ntail) stat1(elem_to_f32(__ldg(row + m.v1 - m.ntail + tid)), st, k2);
+    }
+    // thread t takes words t + 128 i of the segment, kRsUnroll at a time
+    const uint4 *sb = rb_stage + (size_t)stage * kCW;
+    const int nw = m.w1 - m.w0;
+    int i = tid;
+    for (; i + (kRsUnroll - 1) * kRbConsumers < nw; i += kRsUnroll * kRbConsumers) {
+      uint4 buf[kRsUnroll];
+#pragma unroll
+      for (int q = 0; q < kRsUnroll; ++q) buf[q] = sb[i + q * kRbConsumers];
+      stat_batch<E>(buf, st, k2);
+    }
+    for (; i < nw; i += kRbConsumers) stat_word<E>(sb[i], st, k2);
+    if (!m.last) {
+      ring_arrive(ring_addr(&sm.empty[stage]));
+      continue;
+    }
+    // last chunk: warps 1-3 release the stage now; warp 0 once it has read
+    // the stage's reduction slots, so that no warp writes them for a later
+    // unit first
+    if (warp) ring_arrive(ring_addr(&sm.empty[stage]));
+    float a0, a1, a2, a3;
+    f2_unpack(st.s01, a0, a1);
+    f2_unpack(st.s23, a2, a3);
+    float mx = st.mx, mk = st.mk, s = (a0 + a1) + (a2 + a3);
+    warp_stat_combine(mx, mk, s);
+    if (lane == 0) {
+      sm.red[stage][warp] = make_float4(mx, mk, s, 0.0f);
+      ring_arrive(ring_addr(&sm.reduced[stage]));
+    }
+    const uint32_t rph = (rpar >> stage) & 1u;
+    rpar ^= 1u << stage;
+    if (warp == 0) {
+      if (!ring_wait(ring_addr(&sm.reduced[stage]), rph, abort)) break;
+      float4 v = lane < kRbConsumers / 32 ? sm.red[stage][lane]
+                                          : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+      ring_arrive(ring_addr(&sm.empty[stage]));
+      warp_stat_combine(v.x, v.y, v.z);
+      if (lane == 0) partial[m.out] = v;
+    }
+    ++j;
+  }
+  if (*abort && tid == 0) {
+    // a wait ran out: thread 0 wrote the partials of units < j; mark the rest
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      n_units += (long long)__ldcg(rowcount) * G;
+    }
+    for (long long u = blockIdx.x + j * (long long)gridDim.x; u < n_units; u += gridDim.x)
+      partial[rb_unit<E>(r, G, rowlist, R0, u).out] = make_float4(NAN, NAN, NAN, 1.0f);
+  }
+}
+
 Layout plan(int B, int maxpos, int V, bool tree) {
   Layout L;
   L.maxpos = maxpos;
@@ -339,12 +541,15 @@ struct DecideOut {
 // The loads of a group of 8 partials are issued together, then merged in
 // segment order (the same order for every G, so the result does not depend on
 // how the loads were grouped).
+// Returns true when a segment's partial is marked as never computed (.w != 0:
+// the row pass gave up on a bounded wait).
 template <bool kCg = false>
-__device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx, float &mk,
+__device__ __forceinline__ bool merge_slot(const float4 *part, int G, float &mx, float &mk,
                                            float &s) {
   mx = -INFINITY;
   mk = 0.0f;
   s = 0.0f;
+  bool lost = false;
   for (int g0 = 0; g0 < G; g0 += 8) {
     float4 v[8];
 #pragma unroll
@@ -352,8 +557,12 @@ __device__ __forceinline__ void merge_slot(const float4 *part, int G, float &mx,
       if (g0 + g < G) v[g] = kCg ? __ldcg(part + g0 + g) : part[g0 + g];
 #pragma unroll
     for (int g = 0; g < 8; ++g)
-      if (g0 + g < G) st_combine(mx, mk, s, v[g].x, v[g].y, v[g].z);
+      if (g0 + g < G) {
+        st_combine(mx, mk, s, v[g].x, v[g].y, v[g].z);
+        lost |= v[g].w != 0.0f;
+      }
   }
+  return lost;
 }
 
 // One position of the walk from the merged statistics of its verifier and
@@ -379,9 +588,10 @@ __device__ __forceinline__ Judged judge_position(const Round &r, int G, const fl
   const float xq = tok_ok ? load_elem<E>(vrow + d) : 0.0f;
   const float xp = tok_ok ? load_elem<E>(drow + d) : 0.0f;
   float mkq, sq, mkp, sp;
-  merge_slot<kCg>(pb + (size_t)i * G, G, J.mxq, mkq, sq);
-  merge_slot<kCg>(pb + (size_t)(r.maxpos + 1 + i) * G, G, J.mxp, mkp, sp);
+  const bool lq_ = merge_slot<kCg>(pb + (size_t)i * G, G, J.mxq, mkq, sq);
+  const bool lp_ = merge_slot<kCg>(pb + (size_t)(r.maxpos + 1 + i) * G, G, J.mxp, mkp, sp);
   J.bad = (!(sq > 0.0f) || !(sp > 0.0f)) ? SV_ROW_NAN : 0u;
+  if (lq_ || lp_) J.bad |= SV_ROW_TIMEOUT;
   J.qd = J.pd = J.rc = NAN;
   J.u24 = 0u;
   J.accept = J.p_zero = false;
@@ -439,7 +649,7 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   // bonus row (verifier row of position npos) is checked by lane 0
   if (lane == 0 && !tree_bad) {
     float mx, mk, s;
-    merge_slot(pb + (size_t)npos * G, G, mx, mk, s);
+    if (merge_slot(pb + (size_t)npos * G, G, mx, mk, s)) bad |= SV_ROW_TIMEOUT;
     if (!(s > 0.0f)) bad |= SV_ROW_NAN;
     mxv[npos] = mx;
     usm[npos] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)npos, kDrawSample);
@@ -1209,67 +1419,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 // Named barrier of the four consumer warps (the producer warp never joins).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// mbarrier primitives of the ring, every wait bounded by kSpWaitNs
-constexpr unsigned long long kSpWaitNs = 2000000000ull;  // 2 s
-__device__ __forceinline__ unsigned long long sp_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ uint32_t sp_addr(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void sp_mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void sp_mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// an arrival that also expects `bytes` of bulk copies to complete on the barrier
-__device__ __forceinline__ void sp_mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-// TMA bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from global into this CTA's shared memory, completing on `bar`
-__device__ __forceinline__ void sp_bulk_copy(uint32_t dst, const void *src, uint32_t bytes,
-                                             uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ bool sp_mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of `parity`; false (and *abort set) when it runs
-// out or another warp of the CTA has given up.
-__device__ __noinline__ bool sp_mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                               volatile int *abort) {
-  const unsigned long long t0 = sp_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (sp_mbar_try(bar, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*abort) return false;
-      if (sp_ns() - t0 > kSpWaitNs) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-__device__ __forceinline__ bool sp_mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
-  return sp_mbar_try(bar, parity) || sp_mbar_wait_slow(bar, parity, abort);
-}
-
 // What the producer tells the consumers about the item in a stage
 struct ItemMeta {
   const void *rq, *rp;  // the sampled rows (rp null for a bonus draw)
@@ -1410,8 +1559,8 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
   const int tid = threadIdx.x, NS = sw.NS;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      sp_mbar_init(sp_addr(&sm.full[i]), 1);            // the producer's arrival (+ bytes)
-      sp_mbar_init(sp_addr(&sm.empty[i]), kSpThreads);  // every consumer, results stored
+      ring_init(ring_addr(&sm.full[i]), 1);            // the producer's arrival (+ bytes)
+      ring_init(ring_addr(&sm.empty[i]), kSpThreads);  // every consumer, results stored
       sm.meta[i].kind = -1;
     }
     sm.abort = 0;
@@ -1429,7 +1578,7 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     for (;; ++n) {
       const int slot = n & 1;
       if (n >= 2) {
-        if (!sp_mbar_wait(sp_addr(&sm.empty[slot]), ((n >> 1) - 1) & 1, abort)) break;
+        if (!ring_wait(ring_addr(&sm.empty[slot]), ((n >> 1) - 1) & 1, abort)) break;
         finish_item<E>(r, held[slot], sw, o);
         held[slot].kind = -1;
       }
@@ -1471,19 +1620,19 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
           // is counted here as soon as its consumers are done, or this wait
           // could never end.
           const int other = (n + 1) & 1;
-          const unsigned long long t0 = sp_ns();
+          const unsigned long long t0 = ring_ns();
           for (;;) {
             unsigned done = 0;
             if (lane == 0) done = ld_acquire(sw.done + b);
             done = __shfl_sync(0xffffffffu, done, 0);
             if (done >= (unsigned)NS) break;
             if (held[other].kind >= 0 && n >= 1 &&
-                sp_mbar_try(sp_addr(&sm.empty[other]), ((n - 1) >> 1) & 1)) {
+                ring_try(ring_addr(&sm.empty[other]), ((n - 1) >> 1) & 1)) {
               finish_item<E>(r, held[other], sw, o);
               held[other].kind = -1;
               continue;
             }
-            if (sp_ns() - t0 > kSpWaitNs) {
+            if (ring_ns() - t0 > kRingWaitNs) {
               m.ok = 0;
               break;
             }
@@ -1503,15 +1652,15 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
       const uint32_t bytes = (uint32_t)m.nbulk * 16u * (m.kind == 1 ? 1u : 2u);
       if (lane == 0) {
         sm.meta[slot] = m;
-        sp_mbar_expect_tx(sp_addr(&sm.full[slot]), bytes);  // arrival (release) + expected bytes
+        ring_expect_tx(ring_addr(&sm.full[slot]), bytes);  // arrival (release) + expected bytes
         if (bytes) {
-          const uint32_t dst = sp_addr(stage_sm + (size_t)(2 * slot) * kW);
+          const uint32_t dst = ring_addr(stage_sm + (size_t)(2 * slot) * kW);
           const size_t off = (size_t)m.s * kSpSlice * sizeof(E);
-          sp_bulk_copy(dst, (const char *)m.rq + off, (uint32_t)m.nbulk * 16u,
-                       sp_addr(&sm.full[slot]));
+          ring_bulk(dst, (const char *)m.rq + off, (uint32_t)m.nbulk * 16u,
+                       ring_addr(&sm.full[slot]));
           if (m.kind != 1)
-            sp_bulk_copy(dst + (uint32_t)kW * 16u, (const char *)m.rp + off,
-                         (uint32_t)m.nbulk * 16u, sp_addr(&sm.full[slot]));
+            ring_bulk(dst + (uint32_t)kW * 16u, (const char *)m.rp + off,
+                         (uint32_t)m.nbulk * 16u, ring_addr(&sm.full[slot]));
         }
       }
       __syncwarp();
@@ -1521,14 +1670,14 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     // the item still held by the other stage: released once the consumers are done
     const int other = (n + 1) & 1;
     if (!*abort && held[other].kind >= 0 && n >= 1 &&
-        sp_mbar_wait(sp_addr(&sm.empty[other]), ((n - 1) >> 1) & 1, abort))
+        ring_wait(ring_addr(&sm.empty[other]), ((n - 1) >> 1) & 1, abort))
       finish_item<E>(r, held[other], sw, o);
     // after an abort, let this CTA's bulk copies in flight land before it exits
     if (*abort && lane == 0) {
       for (int k = n - 1; k <= n; ++k) {
         if (k < 0) continue;
-        const unsigned long long t0 = sp_ns();
-        while (!sp_mbar_try(sp_addr(&sm.full[k & 1]), (k >> 1) & 1) && sp_ns() - t0 < kSpWaitNs) {
+        const unsigned long long t0 = ring_ns();
+        while (!ring_try(ring_addr(&sm.full[k & 1]), (k >> 1) & 1) && ring_ns() - t0 < kRingWaitNs) {
         }
       }
     }
@@ -1537,7 +1686,7 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
   // ---------------------------------------------------------------- consumers
   for (int n = 0;; ++n) {
     const int slot = n & 1;
-    if (!sp_mbar_wait(sp_addr(&sm.full[slot]), (n >> 1) & 1, abort)) {
+    if (!ring_wait(ring_addr(&sm.full[slot]), (n >> 1) & 1, abort)) {
       if (tid == 0 && sm.meta[slot].kind >= 0) atomicOr(o.status + sm.meta[slot].b, SV_ROW_TIMEOUT);
       break;
     }
@@ -1545,7 +1694,7 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     if (m.kind < 0) break;
     const int b = m.b, s = m.s;
     if (m.kind == 2 && !m.ok) {
-      sp_mbar_arrive(sp_addr(&sm.empty[slot]));
+      ring_arrive(ring_addr(&sm.empty[slot]));
       continue;
     }
     const RowPair p = row_pair<E>(r, m);
@@ -1584,7 +1733,7 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     }
     // every consumer's stores precede its arrival: the producer then counts
     // the item (and may pick) and reuses the stage
-    sp_mbar_arrive(sp_addr(&sm.empty[slot]));
+    ring_arrive(ring_addr(&sm.empty[slot]));
   }
 }
 
@@ -1696,19 +1845,19 @@ int tree_list_ctas(int list_slots, int nroot) {
 // The sampler's persistent grids: every SM filled with as many CTAs as fit,
 // looked up once per device and kernel.
 template <typename E, typename K>
-int persistent_grid(K k, int which, size_t smem) {
+int persistent_grid(K k, int which, size_t smem, int threads) {
   static std::mutex mu;
   static int cache[64][2] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (!cache[dev][which]) {
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
+    // (dynamic plus static shared memory may pass 48 KB below 48 KB dynamic)
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
       return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kSpThreads + 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) !=
             cudaSuccess ||
         per_sm < 1)
       return 0;
@@ -1732,12 +1881,29 @@ sv_status launch_sampler(const Round &r, const Layout &L, char *ws, const Task *
   const size_t smem = 2 * sp_stage_bytes<E>();
   // at most 2 B NS items: never more CTAs than that
   const long long items = 2LL * r.B * L.NS;
-  const int g = persistent_grid<E>(sample_kernel<E>, 0, smem);
+  const int g = persistent_grid<E>(sample_kernel<E>, 0, smem, kSpThreads + 32);
   if (!g) return set_error(SV_ERR_CUDA, "sample: occupancy query");
   LaunchScope ls("sample", st);
   return check_launch("sample",
                       launch_pdl(sample_kernel<E>, dim3((unsigned)(items < g ? items : g)),
                                  dim3(kSpThreads + 32), smem, st, r, tasks, sw, o));
+}
+
+// The row pass over device-resident logits: the persistent bulk-ring grid,
+// never more CTAs than units (tree: root units and every listed-row slot).
+template <typename E>
+sv_status launch_row_stats_bulk(const Round &r, int G, const int32_t *rowlist,
+                                const int *rowcount, float4 *partial, unsigned *qc,
+                                cudaStream_t st) {
+  const size_t smem = (size_t)kRbStages * kRbChunk;
+  const int g = persistent_grid<E>(row_stats_bulk_kernel<E>, 1, smem, kRbThreads);
+  if (!g) return set_error(SV_ERR_CUDA, "row_stats: occupancy query");
+  const long long units = (long long)r.B * r.P * G;
+  LaunchScope ls("row_stats", st);
+  return check_launch("row_stats",
+                      launch_pdl(row_stats_bulk_kernel<E>, dim3((unsigned)(units < g ? units : g)),
+                                 dim3(kRbThreads), smem, st, r, G, rowlist, rowcount, partial,
+                                 qc));
 }
 
 // ---------------------------------------------------------------------------
@@ -1766,22 +1932,28 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
                                                 (unsigned *)(ws + L.qc)));
     if (s != SV_OK) return s;
   } else {
-    // tree: B * P row slots bound the listed rows; half as many CTAs per
-    // segment, each taking a second row when the paths are deep
     const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
-    dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
-    int nroot = 0;
-    if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
-      const int R0 = r.maxpos == 0 ? 1 : 2;  // root rows per sequence (root_rows)
-      nroot = tree_root_ctas(R0 * r.B);
-      grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - R0), nroot)));
+    if (r.stage && !r.copy) {
+      s = launch_row_stats_bulk<E>(r, G, rowlist, (const int *)(ws + L.ctr), partial,
+                                   (unsigned *)(ws + L.qc), st);
+    } else {
+      // host-resident logits: one CTA per (row, segment); tree: B * P row
+      // slots bound the listed rows, half as many CTAs per segment, each
+      // taking a second row when the paths are deep
+      dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
+      int nroot = 0;
+      if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
+        const int R0 = r.maxpos == 0 ? 1 : 2;  // root rows per sequence (root_rows)
+        nroot = tree_root_ctas(R0 * r.B);
+        grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - R0), nroot)));
+      }
+      LaunchScope ls("row_stats", st);
+      s = check_launch("row_stats", launch_pdl(r.copy ? row_stats_kernel<E, true>
+                                                      : row_stats_kernel<E, false>,
+                                               grid, dim3(kRsThreads), 0, st, r, G, rowlist,
+                                               (const int *)(ws + L.ctr), partial,
+                                               (unsigned *)(ws + L.qc), nroot));
     }
-    LaunchScope ls("row_stats", st);
-    s = check_launch("row_stats", launch_pdl(r.copy ? row_stats_kernel<E, true>
-                                                    : row_stats_kernel<E, false>,
-                                             grid, dim3(kRsThreads), 0, st, r, G, rowlist,
-                                             (const int *)(ws + L.ctr), partial,
-                                             (unsigned *)(ws + L.qc), nroot));
     if (s != SV_OK) return s;
   }
   {
