@@ -269,26 +269,25 @@ row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
 // ---------------------------------------------------------------------------
 // row_stats over logits in device memory: a persistent grid, one TMA bulk
 // ring per CTA.  The units are the same (row, segment) pairs as above, in the
-// same index space (tree: root rows, then the rows tree_path listed), taken by
-// CTA c in the order c, c + gridDim.x, ...; every segment's body is one
-// 16-byte-aligned run of at most 32 KB.
+// same index space (tree: root rows, then the rows tree_path listed), claimed
+// one at a time from a counter shared by the grid, so that SMs that stream
+// faster take more of them; a segment's 16-byte-aligned body is staged as
+// kRbChunk-byte chunks, one per ring stage.
 //   producer (one thread of warp 4)  claims the CTA's next unit, waits until
-//              its stage is released, writes the unit's description and
-//              starts bulk copies of the body into the stage (arrival with
-//              the byte count on the stage's "full" barrier)
+//              a stage is released, writes the chunk's description and starts
+//              a bulk copy of it into the stage (arrival with the byte count
+//              on the stage's "full" barrier)
 //   consumers (warps 0-3)  wait for a full stage, fold its words into their
-//              statistics exactly as the CTA-per-segment kernel does (thread
-//              t takes words t + 128 j), release the stage, read any ragged
-//              head / tail elements directly, and combine the CTA's triples
-//              into the segment's partial
-// So every SM keeps the next stages' bytes in flight while it computes the
-// current one, and no CTA waits for a whole segment before starting the next.
+//              statistics (thread t takes words t + 128 j of the segment),
+//              release the stage, read any ragged head / tail elements
+//              directly, and after a segment's last chunk combine the CTA's
+//              triples into the segment's partial
 // Tree: the root units need nothing from tree_path; the producer waits for
-// it (griddepcontrol.wait) only when it first reaches a listed unit.  A wait
-// that runs out (kRingWaitNs) stops the CTA; the partials of its remaining
-// units are written as NaN sums with .w = 1, which the accept walk reports as
-// SV_ROW_TIMEOUT.
-constexpr int kRbStages = 4;
+// it (griddepcontrol.wait) only when it first claims a listed unit.  A wait
+// that runs out (kRingWaitNs) stops the CTA; the partials of the units it may
+// not have finished are written as NaN sums with .w = 1, which the accept
+// walk reports as SV_ROW_TIMEOUT.
+constexpr int kRbStages = 3;
 constexpr int kRbChunk = 16384;  // bytes per stage: half a 32 KB segment
 constexpr int kRbConsumers = 128;              // 4 consumer warps
 constexpr int kRbThreads = kRbConsumers + 32;  // + the producer warp
@@ -306,6 +305,7 @@ struct RbMeta {
 struct RbSmem {
   unsigned long long full[kRbStages], empty[kRbStages], reduced[kRbStages];
   RbMeta meta[kRbStages];
+  long long unit[kRbStages];  // the unit each stage was last filled for
   float4 red[kRbStages][kRbConsumers / 32];
   int abort;
 };
@@ -322,7 +322,8 @@ __device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const int32_t 
 template <typename E>
 __global__ void __launch_bounds__(kRbThreads)
 row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
-                      const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
+                      const int32_t *__restrict__ rowcount,
+                      unsigned long long *__restrict__ next_unit, float4 *__restrict__ partial,
                       unsigned *__restrict__ qc) {
   extern __shared__ __align__(128) uint4 rb_stage[];  // [kRbStages][kRbChunk]
   __shared__ RbSmem sm;
@@ -352,9 +353,12 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
     // ---------------------------------------------------------------- producer
     if (tid != kRbConsumers) return;
     long long k = 0;  // stages filled so far
-    bool done = false;
-    for (long long j = 0; !done; ++j) {  // the CTA's j-th unit
-      const long long u = blockIdx.x + j * (long long)gridDim.x;
+    bool lost = false;
+    // units are claimed from a counter shared by the grid (zeroed before the
+    // launch), so SMs that stream faster take more of them; the next claim
+    // is issued before the current unit's copies
+    long long u = (long long)atomicAdd(next_unit, 1ull), nxt = -1;
+    for (;;) {
       if (u >= n_units && !waited) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         waited = true;
@@ -362,6 +366,7 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
       }
       RbMeta m;
       m.end = u >= n_units;
+      nxt = m.end ? -1 : (long long)atomicAdd(next_unit, 1ull);
       int nc = 1, nw = 0;
       SegInfo si;
       if (!m.end) {
@@ -381,16 +386,15 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
         const long long use = k / kRbStages;
         if (use > 0 &&
             !ring_wait(ring_addr(&sm.empty[stage]), (uint32_t)((use - 1) & 1), abort)) {
-          done = true;
+          lost = true;
           break;
         }
+        sm.unit[stage] = m.end ? -1 : u;
         const uint32_t full = ring_addr(&sm.full[stage]);
         if (m.end) {
           sm.meta[stage] = m;
           ring_arrive(full);
-          ++k;
-          done = true;
-          break;
+          continue;
         }
         m.w0 = c * kCW;
         m.w1 = min(nw, m.w0 + kCW);
@@ -406,6 +410,8 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
           ring_arrive(full);
         }
       }
+      if (lost || m.end) break;
+      u = nxt;
     }
     // copies issued for the last kRbStages stages land before the CTA's
     // shared memory is released (at once unless a wait ran out)
@@ -415,12 +421,28 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
       while (!ring_try(bar, (uint32_t)((kk / kRbStages) & 1)) && ring_ns() - t0 < kRingWaitNs) {
       }
     }
+    if (lost || *abort) {
+      // a wait ran out: the units this CTA may not have finished -- those of
+      // the stages in use, the one being filled and the next one claimed --
+      // get partials marked as never computed (a finished one among them
+      // only widens the report)
+      if (!waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        n_units += (long long)__ldcg(rowcount) * G;
+      }
+      auto mark = [&](long long v) {
+        if (v >= 0 && v < n_units)
+          partial[rb_unit<E>(r, G, rowlist, R0, v).out] = make_float4(NAN, NAN, NAN, 1.0f);
+      };
+      for (int i = 0; i < kRbStages && i < k; ++i) mark(sm.unit[i]);
+      mark(u);
+      mark(nxt);
+    }
     return;
   }
   // ------------------------------------------------------------------ consumers
   const int warp = tid >> 5, lane = tid & 31;
   const float k2 = r.k;
-  long long j = 0;  // units finished (their partials written)
   // a stage's reduction barrier completes once per unit that ends in it, not
   // once per use: bit s is the parity of stage s's next reduction
   unsigned rpar = 0u;
@@ -475,16 +497,6 @@ row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
       warp_stat_combine(v.x, v.y, v.z);
       if (lane == 0) partial[m.out] = v;
     }
-    ++j;
-  }
-  if (*abort && tid == 0) {
-    // a wait ran out: thread 0 wrote the partials of units < j; mark the rest
-    if (!waited) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      n_units += (long long)__ldcg(rowcount) * G;
-    }
-    for (long long u = blockIdx.x + j * (long long)gridDim.x; u < n_units; u += gridDim.x)
-      partial[rb_unit<E>(r, G, rowlist, R0, u).out] = make_float4(NAN, NAN, NAN, 1.0f);
   }
 }
 
@@ -500,7 +512,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  L.ctr = take(sizeof(int));  // active row count (tree)
+  L.ctr = take(16);  // [0] active row count (tree); [8] the row pass's next unit (u64)
   L.rowlist = tree ? take(sizeof(int32_t) * nslots) : 0;
   L.partial = take(sizeof(float4) * nslots * L.G);
   L.task = take(sizeof(Task) * (size_t)B);
@@ -1899,11 +1911,16 @@ sv_status launch_row_stats_bulk(const Round &r, int G, const int32_t *rowlist,
   const int g = persistent_grid<E>(row_stats_bulk_kernel<E>, 1, smem, kRbThreads);
   if (!g) return set_error(SV_ERR_CUDA, "row_stats: occupancy query");
   const long long units = (long long)r.B * r.P * G;
+  // the unit counter sits after the row count; a tree call zeroed both before
+  // its path walk, a chain zeroes it here
+  unsigned long long *next_unit = (unsigned long long *)((char *)rowcount + 8);
+  if (!rowlist && cudaMemsetAsync(next_unit, 0, 8, st) != cudaSuccess)
+    return set_error(SV_ERR_CUDA, "row_stats: unit counter reset");
   LaunchScope ls("row_stats", st);
   return check_launch("row_stats",
                       launch_pdl(row_stats_bulk_kernel<E>, dim3((unsigned)(units < g ? units : g)),
-                                 dim3(kRbThreads), smem, st, r, G, rowlist, rowcount, partial,
-                                 qc));
+                                 dim3(kRbThreads), smem, st, r, G, rowlist, rowcount, next_unit,
+                                 partial, qc));
 }
 
 // ---------------------------------------------------------------------------
@@ -2228,7 +2245,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
   int32_t *tok = (int32_t *)(ws + L.tok);
   uint32_t *tstat = (uint32_t *)(ws + L.tstat);
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(ws + L.ctr, 0, sizeof(int), st) != cudaSuccess)
+  if (cudaMemsetAsync(ws + L.ctr, 0, 16, st) != cudaSuccess)
     return check_launch("row counter reset");
   {
     LaunchScope ls("tree_path", st);
