@@ -117,11 +117,6 @@ __host__ __device__ constexpr int seg_elems() {
   return kRsThreads * 2 * kRsUnroll * 16 / (int)sizeof(E);
 }
 
-// Row slot of active row `a` of sequence b (tree: a <= npos verifier, then draft)
-__device__ __forceinline__ int slot_of_active(int a, int npos, int maxpos) {
-  return a <= npos ? a : maxpos + 1 + (a - npos - 1);
-}
-
 struct SegInfo {
   const char *row;   // row base
   char *copy;        // its device copy (host-resident logits), or null
@@ -140,7 +135,7 @@ __device__ __forceinline__ int root_rows(const Round &r, bool greedy) {
 // Row index space of a row pass: a chain's rows b * P + j; a tree's root rows
 // first (R0 per sequence, row_i < R0 B), then the rows tree_path listed.
 template <typename E>
-__device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t *rowlist,
+__device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const uint64_t *rowlist,
                                             int row_i, int seg, int R0 = 0) {
   int b, j;
   const E *row;
@@ -150,10 +145,11 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
     j = is_v ? 0 : r.maxpos + 1;
     row = (const E *)(is_v ? r.vlog : r.dlog) + (size_t)b * (is_v ? r.v_rows : r.d_rows) * r.V;
   } else if (rowlist) {
-    const int e = rowlist[row_i - R0 * r.B];
-    b = e >> 12;
-    j = slot_of_active(e & 0xfff, round_npos(r, b), r.maxpos);
-    row = src_row<E>(r, b, j);
+    // one load: tree_path stored the row slot and the row itself
+    const uint64_t e = rowlist[row_i - R0 * r.B];
+    b = (int)(e >> 44);
+    j = (int)((e >> 32) & 0xfffu);
+    row = (const E *)((e >> 30) & 1u ? r.dlog : r.vlog) + (size_t)(e & 0x3fffffffu) * r.V;
   } else {
     b = row_i / r.P;
     j = row_i - b * r.P;
@@ -174,7 +170,7 @@ __device__ __forceinline__ SegInfo seg_info(const Round &r, int G, const int32_t
 
 // statistics of segment seg of listed row row_i, by the whole CTA
 template <typename E, bool kCopy>
-__device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_t *rowlist,
+__device__ __forceinline__ void stat_segment(const Round &r, int G, const uint64_t *rowlist,
                                              int row_i, int seg, float4 *partial, int R0 = 0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg, R0);
@@ -234,7 +230,7 @@ __device__ __forceinline__ void stat_segment(const Round &r, int G, const int32_
 
 template <typename E, bool kCopy>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
-row_stats_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+row_stats_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
                  const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
                  unsigned *__restrict__ qc, int nroot) {
   // Tree: the root-row CTAs need nothing from tree_path, the grid before this
@@ -312,7 +308,7 @@ struct RbSmem {
 
 // unit u of a row pass: its row / segment and where its partial goes
 template <typename E>
-__device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const int32_t *rowlist, int R0,
+__device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const uint64_t *rowlist, int R0,
                                            long long u) {
   const int row_i = (int)(u / G), seg = (int)(u - (long long)row_i * G);
   return rowlist ? seg_info<E>(r, G, rowlist, row_i, seg, R0)
@@ -321,7 +317,7 @@ __device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const int32_t 
 
 template <typename E>
 __global__ void __launch_bounds__(kRbThreads)
-row_stats_bulk_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+row_stats_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
                       const int32_t *__restrict__ rowcount,
                       unsigned long long *__restrict__ next_unit, float4 *__restrict__ partial,
                       unsigned *__restrict__ qc) {
@@ -513,7 +509,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
     return o;
   };
   L.ctr = take(16);  // [0] active row count (tree); [8] the row pass's next unit (u64)
-  L.rowlist = tree ? take(sizeof(int32_t) * nslots) : 0;
+  L.rowlist = tree ? take(sizeof(uint64_t) * nslots) : 0;
   L.partial = take(sizeof(float4) * nslots * L.G);
   L.task = take(sizeof(Task) * (size_t)B);
   L.NS = (V + kSpSlice - 1) / kSpSlice;
@@ -892,7 +888,7 @@ __device__ __forceinline__ void arg_word<float>(ArgState &a, uint4 w, int v) {
 }
 
 template <typename E>
-__device__ __forceinline__ void argmax_segment(const Round &r, int G, const int32_t *rowlist,
+__device__ __forceinline__ void argmax_segment(const Round &r, int G, const uint64_t *rowlist,
                                                int row_i, int seg, float4 *partial, int R0 = 0) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SegInfo si = seg_info<E>(r, G, rowlist, row_i, seg, R0);
@@ -964,7 +960,7 @@ __device__ __forceinline__ void argmax_segment(const Round &r, int G, const int3
 
 template <typename E>
 __global__ void __launch_bounds__(kRsThreads, sizeof(E) == 2 ? 10 : 8)
-row_argmax_kernel(Round r, int G, const int32_t *__restrict__ rowlist,
+row_argmax_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
                   const int32_t *__restrict__ rowcount, float4 *__restrict__ partial,
                   int nroot) {
   if (!rowlist) {  // chain: one CTA per (row = x, segment = y)
@@ -1755,6 +1751,12 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
 // node's best child comes from one parallel pass (a 64-bit shared-memory
 // maximum per parent of the key (score in a monotone integer order, ~slot)),
 // so the walk itself is a chain of max_depth shared-memory loads.
+// A listed row: bits 0-29 its row in the verifier / draft logits
+// (b T + node), bit 30 draft, bits 32-43 its row slot, bits 44-63 b.
+__device__ __forceinline__ uint64_t list_entry(int b, int slot, bool draft, long long row) {
+  return (uint64_t)row | ((uint64_t)draft << 30) | ((uint64_t)slot << 32) | ((uint64_t)b << 44);
+}
+
 __device__ __forceinline__ unsigned long long child_key(float s, int c) {
   const unsigned u = __float_as_uint(__fadd_rn(s, 0.0f));  // -0 joins +0: they compare equal
   const unsigned o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -1766,7 +1768,7 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
                  const float *__restrict__ score, int B, int T, int max_depth,
                  int32_t *__restrict__ path, int32_t *__restrict__ npos,
                  int32_t *__restrict__ tok, int tok_stride, uint32_t *__restrict__ tstat,
-                 int32_t *__restrict__ rowlist, int *__restrict__ rowcount, int greedy) {
+                 uint64_t *__restrict__ rowlist, int *__restrict__ rowcount, int greedy) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x, lane = threadIdx.x;
   __shared__ int32_t pa[SV_MAX_TREE_NODES];
@@ -1828,8 +1830,9 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
   // the path and its tested tokens token[n_1..n_D], written in parallel
   for (int i = lane; i <= D; i += 32) pth[i] = pn[i];
   for (int i = lane; i < D; i += 32) tok[(size_t)b * tok_stride + i] = tk[pn[i + 1]];
-  // the path's rows other than the root's (those have their own CTAs): the
-  // verifier rows n_1..n_D, then (stochastic rule) the draft rows n_1..n_{D-1}
+  // the path's rows other than the root's (the row pass reads those without
+  // waiting for this grid): the verifier rows n_1..n_D, then (stochastic
+  // rule) the draft rows n_1..n_{D-1}
   const int nrow = D == 0 ? 0 : (greedy ? D : 2 * D - 1);
   int base = 0;
   if (lane == 0) {
@@ -1838,8 +1841,13 @@ tree_path_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__
     if (nrow) base = atomicAdd(rowcount, nrow);
   }
   base = __shfl_sync(0xffffffffu, base, 0);
-  for (int k = lane; k < nrow; k += 32)
-    rowlist[base + k] = (b << 12) | (k < D ? k + 1 : D + 2 + (k - D));
+  for (int k = lane; k < nrow; k += 32) {
+    // verifier row of path position k + 1, or draft row of position k - D + 1
+    const bool draft = k >= D;
+    const int i = draft ? k - D + 1 : k + 1;
+    rowlist[base + k] =
+        list_entry(b, draft ? max_depth + 1 + i : i, draft, (long long)b * T + pn[i]);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1904,7 +1912,7 @@ sv_status launch_sampler(const Round &r, const Layout &L, char *ws, const Task *
 // The row pass over device-resident logits: the persistent bulk-ring grid,
 // never more CTAs than units (tree: root units and every listed-row slot).
 template <typename E>
-sv_status launch_row_stats_bulk(const Round &r, int G, const int32_t *rowlist,
+sv_status launch_row_stats_bulk(const Round &r, int G, const uint64_t *rowlist,
                                 const int *rowcount, float4 *partial, unsigned *qc,
                                 cudaStream_t st) {
   const size_t smem = (size_t)kRbStages * kRbChunk;
@@ -1949,7 +1957,7 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
                                                 (unsigned *)(ws + L.qc)));
     if (s != SV_OK) return s;
   } else {
-    const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
+    const uint64_t *rowlist = r.path ? (const uint64_t *)(ws + L.rowlist) : nullptr;
     if (r.stage && !r.copy) {
       s = launch_row_stats_bulk<E>(r, G, rowlist, (const int *)(ws + L.ctr), partial,
                                    (unsigned *)(ws + L.qc), st);
@@ -2004,7 +2012,7 @@ sv_status run_verify_greedy(const Round &r, const Layout &L, char *ws, const Dec
   const int G = (r.V + seg_elems<E>() - 1) / seg_elems<E>();
   sv_status s;
   {
-    const int32_t *rowlist = r.path ? (const int32_t *)(ws + L.rowlist) : nullptr;
+    const uint64_t *rowlist = r.path ? (const uint64_t *)(ws + L.rowlist) : nullptr;
     dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
     int nroot = 0;
     if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
@@ -2252,7 +2260,7 @@ extern "C" sv_status sv_verify_tree(const void *vlogits, const void *dlogits, sv
     s = check_launch("tree_path",
                      launch_pdl(tree_path_kernel, dim3(B), dim3(32), 0, st, parent, token, score,
                                 B, T, max_depth, path, npos, tok, max_depth > 0 ? max_depth : 1,
-                                tstat, (int32_t *)(ws + L.rowlist), (int *)(ws + L.ctr),
+                                tstat, (uint64_t *)(ws + L.rowlist), (int *)(ws + L.ctr),
                                 temperature == 0.0f ? 1 : 0));
     if (s != SV_OK) return s;
   }
