@@ -123,22 +123,6 @@ template <> __device__ __forceinline__ float load_elem<uint16_t>(const uint16_t 
   return __uint_as_float((uint32_t)__ldg(p) << 16);
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only), and its completion
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-// every group but the most recently committed one has completed
-__device__ __forceinline__ void cp_async_wait_1() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

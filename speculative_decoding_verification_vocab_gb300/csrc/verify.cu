@@ -315,23 +315,109 @@ __device__ __forceinline__ SegInfo rb_unit(const Round &r, int G, const uint64_t
                  : seg_info<E>(r, G, nullptr, row_i, seg);
 }
 
+// Arg-max primitives (the greedy row pass): per thread the largest logit and
+// its lowest index, with fault flags.
+constexpr uint32_t kArgNan = 1u;   // a NaN or +inf logit
+constexpr uint32_t kArgSeen = 2u;  // a logit above -inf
+constexpr uint32_t kArgLost = 4u;  // the row pass gave up on a bounded wait
+
+struct ArgState {
+  float best;  // running maximum (NaN ignored)
+  int idx;     // lowest index holding it
+  uint32_t flags;
+};
+
+__device__ __forceinline__ void arg1(ArgState &a, float x, int v) {
+  if (x > a.best) {
+    a.best = x;
+    a.idx = v;
+  }
+  if (x != x || x == INFINITY) a.flags |= kArgNan;
+  if (x > -INFINITY) a.flags |= kArgSeen;
+}
+// (best, idx) pairs: larger value wins, equal values go to the lower index
+__device__ __forceinline__ void arg_merge(ArgState &a, float best, int idx, uint32_t flags) {
+  if (best > a.best || (best == a.best && idx < a.idx)) {
+    a.best = best;
+    a.idx = idx;
+  }
+  a.flags |= flags;
+}
+
+// one 16-byte word of logits starting at element v; the word's maximum is
+// taken on packed pairs first and the elements are scanned only when it
+// beats the running maximum (in index order, so the lowest index is kept)
 template <typename E>
+__device__ __forceinline__ void arg_word(ArgState &a, uint4 w, int v);
+template <>
+__device__ __forceinline__ void arg_word<uint16_t>(ArgState &a, uint4 w, int v) {
+  const uint32_t m = bf2_max(bf2_max(w.x, w.y), bf2_max(w.z, w.w));
+  const uint32_t mn = bf2_max_nan(bf2_max_nan(w.x, w.y), bf2_max_nan(w.z, w.w));
+  const float wm = fmaxf(bf16_lo(m), bf16_hi(m));
+  const float n0 = bf16_lo(mn), n1 = bf16_hi(mn);  // NaN in either half: a NaN element
+  if (n0 != n0 || n1 != n1 || wm == INFINITY) a.flags |= kArgNan;
+  if (wm > -INFINITY) a.flags |= kArgSeen;
+  if (wm > a.best) {
+    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+    int k = 7;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      const float x = (j & 1) ? bf16_hi(q[j >> 1]) : bf16_lo(q[j >> 1]);
+      if (x == wm) k = j;
+    }
+    a.best = wm;
+    a.idx = v + k;
+  }
+}
+template <>
+__device__ __forceinline__ void arg_word<float>(ArgState &a, uint4 w, int v) {
+  const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                      __uint_as_float(w.w)};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) arg1(a, x[j], v + j);
+}
+
+// The consumers' per-thread state: online statistics, or (kArg) the arg max.
+template <bool kArg>
+struct RbState;
+template <>
+struct RbState<false> {
+  StatState st;
+  __device__ __forceinline__ void reset() { st = StatState{-INFINITY, 0.0f, 0ull, 0ull}; }
+};
+template <>
+struct RbState<true> {
+  ArgState a;
+  __device__ __forceinline__ void reset() { a = ArgState{-INFINITY, 0x7fffffff, 0u}; }
+};
+
+// A segment's partial that the row pass never computed (a wait ran out):
+// statistics: NaN sums with .w = 1; arg max: the fault and "lost" flags.
+template <bool kArg>
+__device__ __forceinline__ float4 rb_lost() {
+  return kArg ? make_float4(-INFINITY, __int_as_float(0x7fffffff),
+                            __uint_as_float(kArgNan | kArgLost), 0.0f)
+              : make_float4(NAN, NAN, NAN, 1.0f);
+}
+
+template <typename E, bool kArg>
 __global__ void __launch_bounds__(kRbThreads)
-row_stats_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
-                      const int32_t *__restrict__ rowcount,
-                      unsigned long long *__restrict__ next_unit, float4 *__restrict__ partial,
-                      unsigned *__restrict__ qc) {
+row_pass_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
+                     const int32_t *__restrict__ rowcount,
+                     unsigned long long *__restrict__ next_unit, float4 *__restrict__ partial,
+                     unsigned *__restrict__ qc) {
   extern __shared__ __align__(128) uint4 rb_stage[];  // [kRbStages][kRbChunk]
   __shared__ RbSmem sm;
   constexpr int kCW = kRbChunk / 16;  // words per stage
+  constexpr int kPer = 16 / (int)sizeof(E);
   const int tid = threadIdx.x;
   const bool tree = rowlist != nullptr;
-  const int R0 = tree ? root_rows(r, false) : 0;
+  const int R0 = tree ? root_rows(r, kArg) : 0;
   if (!tree)
     grid_dep_sync();  // chain: the workspace is free once the previous step's grids are done
   else
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == 0 && tid < 3) qc[tid] = 0u;  // the sampler's counters, rebuilt by the walk
+  if (qc && blockIdx.x == 0 && tid < 3) qc[tid] = 0u;  // the sampler's counters, rebuilt by the walk
   if (tid == 0) {
     for (int i = 0; i < kRbStages; ++i) {
       ring_init(ring_addr(&sm.full[i]), 1);
@@ -428,7 +514,7 @@ row_stats_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
       }
       auto mark = [&](long long v) {
         if (v >= 0 && v < n_units)
-          partial[rb_unit<E>(r, G, rowlist, R0, v).out] = make_float4(NAN, NAN, NAN, 1.0f);
+          partial[rb_unit<E>(r, G, rowlist, R0, v).out] = rb_lost<kArg>();
       };
       for (int i = 0; i < kRbStages && i < k; ++i) mark(sm.unit[i]);
       mark(u);
@@ -442,55 +528,110 @@ row_stats_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
   // a stage's reduction barrier completes once per unit that ends in it, not
   // once per use: bit s is the parity of stage s's next reduction
   unsigned rpar = 0u;
-  StatState st{-INFINITY, 0.0f, 0ull, 0ull};
+  RbState<kArg> ps;
+  ps.reset();
   for (long long k = 0;; ++k) {
     const int stage = (int)(k % kRbStages);
     const uint32_t ph = (uint32_t)((k / kRbStages) & 1);
     if (!ring_wait(ring_addr(&sm.full[stage]), ph, abort)) break;
     const RbMeta m = sm.meta[stage];
     if (m.end) break;
+    const E *row = (const E *)m.row;
+    // ragged elements.  Arg max: the head before the first chunk's words,
+    // the tail after the last chunk's (increasing index order within a
+    // thread keeps the lowest index).  Statistics: head and tail first, the
+    // order of every other row-statistics kernel, so that all of them round
+    // a segment's sum alike.
     if (m.first) {
-      st = StatState{-INFINITY, 0.0f, 0ull, 0ull};
-      const E *row = (const E *)m.row;
-      if (tid < m.nhead) stat1(elem_to_f32(__ldg(row + m.v0 + tid)), st, k2);
-      if (tid < m.ntail) stat1(elem_to_f32(__ldg(row + m.v1 - m.ntail + tid)), st, k2);
+      ps.reset();
+      if (tid < m.nhead) {
+        if constexpr (kArg)
+          arg1(ps.a, load_elem<E>(row + m.v0 + tid), m.v0 + tid);
+        else
+          stat1(elem_to_f32(__ldg(row + m.v0 + tid)), ps.st, k2);
+      }
+      if constexpr (!kArg) {
+        if (tid < m.ntail) stat1(elem_to_f32(__ldg(row + m.v1 - m.ntail + tid)), ps.st, k2);
+      }
     }
     // thread t takes words t + 128 i of the segment, kRsUnroll at a time
     const uint4 *sb = rb_stage + (size_t)stage * kCW;
     const int nw = m.w1 - m.w0;
+    const int vw = m.v0 + m.nhead + m.w0 * kPer;  // element index of the chunk's first word
     int i = tid;
     for (; i + (kRsUnroll - 1) * kRbConsumers < nw; i += kRsUnroll * kRbConsumers) {
       uint4 buf[kRsUnroll];
 #pragma unroll
       for (int q = 0; q < kRsUnroll; ++q) buf[q] = sb[i + q * kRbConsumers];
-      stat_batch<E>(buf, st, k2);
+      if constexpr (kArg) {
+#pragma unroll
+        for (int q = 0; q < kRsUnroll; ++q)
+          arg_word<E>(ps.a, buf[q], vw + (i + q * kRbConsumers) * kPer);
+      } else {
+        stat_batch<E>(buf, ps.st, k2);
+      }
     }
-    for (; i < nw; i += kRbConsumers) stat_word<E>(sb[i], st, k2);
+    for (; i < nw; i += kRbConsumers) {
+      if constexpr (kArg)
+        arg_word<E>(ps.a, sb[i], vw + i * kPer);
+      else
+        stat_word<E>(sb[i], ps.st, k2);
+    }
     if (!m.last) {
       ring_arrive(ring_addr(&sm.empty[stage]));
       continue;
+    }
+    if constexpr (kArg) {
+      if (tid < m.ntail) arg1(ps.a, load_elem<E>(row + m.v1 - m.ntail + tid), m.v1 - m.ntail + tid);
     }
     // last chunk: warps 1-3 release the stage now; warp 0 once it has read
     // the stage's reduction slots, so that no warp writes them for a later
     // unit first
     if (warp) ring_arrive(ring_addr(&sm.empty[stage]));
-    float a0, a1, a2, a3;
-    f2_unpack(st.s01, a0, a1);
-    f2_unpack(st.s23, a2, a3);
-    float mx = st.mx, mk = st.mk, s = (a0 + a1) + (a2 + a3);
-    warp_stat_combine(mx, mk, s);
+    float4 mine;
+    if constexpr (kArg) {
+      ArgState c = ps.a;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, c.best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, c.idx, o);
+        const uint32_t of = __shfl_xor_sync(0xffffffffu, c.flags, o);
+        arg_merge(c, ob, oi, of);
+      }
+      mine = make_float4(c.best, __int_as_float(c.idx), __uint_as_float(c.flags), 0.0f);
+    } else {
+      float a0, a1, a2, a3;
+      f2_unpack(ps.st.s01, a0, a1);
+      f2_unpack(ps.st.s23, a2, a3);
+      float mx = ps.st.mx, mk = ps.st.mk, sum = (a0 + a1) + (a2 + a3);
+      warp_stat_combine(mx, mk, sum);
+      mine = make_float4(mx, mk, sum, 0.0f);
+    }
     if (lane == 0) {
-      sm.red[stage][warp] = make_float4(mx, mk, s, 0.0f);
+      sm.red[stage][warp] = mine;
       ring_arrive(ring_addr(&sm.reduced[stage]));
     }
     const uint32_t rph = (rpar >> stage) & 1u;
     rpar ^= 1u << stage;
     if (warp == 0) {
       if (!ring_wait(ring_addr(&sm.reduced[stage]), rph, abort)) break;
-      float4 v = lane < kRbConsumers / 32 ? sm.red[stage][lane]
-                                          : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+      const float4 none = kArg ? make_float4(-INFINITY, __int_as_float(0x7fffffff), 0.0f, 0.0f)
+                               : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+      float4 v = lane < kRbConsumers / 32 ? sm.red[stage][lane] : none;
       ring_arrive(ring_addr(&sm.empty[stage]));
-      warp_stat_combine(v.x, v.y, v.z);
+      if constexpr (kArg) {
+        ArgState c{v.x, __float_as_int(v.y), __float_as_uint(v.z)};
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ob = __shfl_xor_sync(0xffffffffu, c.best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, c.idx, o);
+          const uint32_t of = __shfl_xor_sync(0xffffffffu, c.flags, o);
+          arg_merge(c, ob, oi, of);
+        }
+        v = make_float4(c.best, __int_as_float(c.idx), __uint_as_float(c.flags), 0.0f);
+      } else {
+        warp_stat_combine(v.x, v.y, v.z);
+      }
       if (lane == 0) partial[m.out] = v;
     }
   }
@@ -828,65 +969,6 @@ row_stats_ee_kernel(Round r, int G, float4 *__restrict__ partial, unsigned *__re
 // fault flags; decide_greedy: one warp per sequence accepts while the draft
 // token is the row's arg max and emits the arg max where the walk stops.
 // Only verifier rows are read; nothing is sampled.
-constexpr uint32_t kArgNan = 1u;   // a NaN or +inf logit
-constexpr uint32_t kArgSeen = 2u;  // a logit above -inf
-
-struct ArgState {
-  float best;  // running maximum (NaN ignored)
-  int idx;     // lowest index holding it
-  uint32_t flags;
-};
-
-__device__ __forceinline__ void arg1(ArgState &a, float x, int v) {
-  if (x > a.best) {
-    a.best = x;
-    a.idx = v;
-  }
-  if (x != x || x == INFINITY) a.flags |= kArgNan;
-  if (x > -INFINITY) a.flags |= kArgSeen;
-}
-// (best, idx) pairs: larger value wins, equal values go to the lower index
-__device__ __forceinline__ void arg_merge(ArgState &a, float best, int idx, uint32_t flags) {
-  if (best > a.best || (best == a.best && idx < a.idx)) {
-    a.best = best;
-    a.idx = idx;
-  }
-  a.flags |= flags;
-}
-
-// one 16-byte word of logits starting at element v; the word's maximum is
-// taken on packed pairs first and the elements are scanned only when it
-// beats the running maximum (in index order, so the lowest index is kept)
-template <typename E>
-__device__ __forceinline__ void arg_word(ArgState &a, uint4 w, int v);
-template <>
-__device__ __forceinline__ void arg_word<uint16_t>(ArgState &a, uint4 w, int v) {
-  const uint32_t m = bf2_max(bf2_max(w.x, w.y), bf2_max(w.z, w.w));
-  const uint32_t mn = bf2_max_nan(bf2_max_nan(w.x, w.y), bf2_max_nan(w.z, w.w));
-  const float wm = fmaxf(bf16_lo(m), bf16_hi(m));
-  const float n0 = bf16_lo(mn), n1 = bf16_hi(mn);  // NaN in either half: a NaN element
-  if (n0 != n0 || n1 != n1 || wm == INFINITY) a.flags |= kArgNan;
-  if (wm > -INFINITY) a.flags |= kArgSeen;
-  if (wm > a.best) {
-    const uint32_t q[4] = {w.x, w.y, w.z, w.w};
-    int k = 7;
-#pragma unroll
-    for (int j = 7; j >= 0; --j) {
-      const float x = (j & 1) ? bf16_hi(q[j >> 1]) : bf16_lo(q[j >> 1]);
-      if (x == wm) k = j;
-    }
-    a.best = wm;
-    a.idx = v + k;
-  }
-}
-template <>
-__device__ __forceinline__ void arg_word<float>(ArgState &a, uint4 w, int v) {
-  const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
-                      __uint_as_float(w.w)};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) arg1(a, x[j], v + j);
-}
-
 template <typename E>
 __device__ __forceinline__ void argmax_segment(const Round &r, int G, const uint64_t *rowlist,
                                                int row_i, int seg, float4 *partial, int R0 = 0) {
@@ -902,25 +984,6 @@ __device__ __forceinline__ void argmax_segment(const Round &r, int G, const uint
   const int nv = (int)((si.ae - si.ab) / 16);
   constexpr int kPer = 16 / (int)sizeof(E);
   int i = tid;
-  if (r.stage && i + (2 * kRsUnroll - 1) * kRsThreads < nv) {
-    // as row_stats: the second half of the thread's words through shared
-    // memory; words are still taken in increasing index order
-    __shared__ uint4 sbuf[kRsUnroll][kRsThreads];
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j)
-      cp_async16(&sbuf[j][tid], body + i + (kRsUnroll + j) * kRsThreads);
-    cp_async_commit();
-    uint4 buf[kRsUnroll];
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kRsThreads);
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j) arg_word<E>(a, buf[j], vbody + (i + j * kRsThreads) * kPer);
-    cp_async_wait_all();
-#pragma unroll
-    for (int j = 0; j < kRsUnroll; ++j)
-      arg_word<E>(a, sbuf[j][tid], vbody + (i + (kRsUnroll + j) * kRsThreads) * kPer);
-    i += 2 * kRsUnroll * kRsThreads;
-  }
   for (; i + (kRsUnroll - 1) * kRsThreads < nv; i += kRsUnroll * kRsThreads) {
     uint4 buf[kRsUnroll];
 #pragma unroll
@@ -1012,6 +1075,7 @@ decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideO
   if (lane == 0 && !tree_bad) {
     const ArgState a = merge_arg(pb + (size_t)npos * G, G);
     if (arg_bad(a)) bad |= SV_ROW_NAN;
+    if (a.flags & kArgLost) bad |= SV_ROW_TIMEOUT;
     am[npos] = a.idx;
   }
   const int nchunks = (npos + 31) / 32;
@@ -1022,6 +1086,7 @@ decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideO
     const ArgState a = merge_arg(pb + (size_t)i * G, G);
     am[i] = a.idx;
     if (arg_bad(a)) bad |= SV_ROW_NAN;
+    if (a.flags & kArgLost) bad |= SV_ROW_TIMEOUT;
     if (d < 0 || d >= r.V) bad |= SV_ROW_BAD_TOKEN;
     if (d != a.idx) rej_bits |= 1u << c;
     if (o.q_prob) o.q_prob[(size_t)b * r.maxpos + i] = (d == a.idx) ? 1.0f : 0.0f;
@@ -1862,12 +1927,13 @@ int tree_list_ctas(int list_slots, int nroot) {
 }
 
 // ---------------------------------------------------------------------------
-// The sampler's persistent grids: every SM filled with as many CTAs as fit,
-// looked up once per device and kernel.
+// Persistent grids (the row passes' bulk rings, the sampler): every SM filled
+// with as many CTAs as fit, looked up once per device and kernel (`which`
+// tells apart kernels of one signature: 0 sampler, 1 statistics, 2 arg max).
 template <typename E, typename K>
 int persistent_grid(K k, int which, size_t smem, int threads) {
   static std::mutex mu;
-  static int cache[64][2] = {};
+  static int cache[64][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
@@ -1909,26 +1975,26 @@ sv_status launch_sampler(const Round &r, const Layout &L, char *ws, const Task *
                                  dim3(kSpThreads + 32), smem, st, r, tasks, sw, o));
 }
 
-// The row pass over device-resident logits: the persistent bulk-ring grid,
+// A row pass over device-resident logits: the persistent bulk-ring grid,
 // never more CTAs than units (tree: root units and every listed-row slot).
-template <typename E>
-sv_status launch_row_stats_bulk(const Round &r, int G, const uint64_t *rowlist,
-                                const int *rowcount, float4 *partial, unsigned *qc,
-                                cudaStream_t st) {
+// qc: the sampler's counters to zero (statistics pass), or null.
+template <typename E, bool kArg>
+sv_status launch_row_pass_bulk(const char *name, const Round &r, int G, const uint64_t *rowlist,
+                               const int *rowcount, float4 *partial, unsigned *qc,
+                               cudaStream_t st) {
   const size_t smem = (size_t)kRbStages * kRbChunk;
-  const int g = persistent_grid<E>(row_stats_bulk_kernel<E>, 1, smem, kRbThreads);
-  if (!g) return set_error(SV_ERR_CUDA, "row_stats: occupancy query");
+  const int g = persistent_grid<E>(row_pass_bulk_kernel<E, kArg>, kArg ? 2 : 1, smem, kRbThreads);
+  if (!g) return set_error(SV_ERR_CUDA, "%s: occupancy query", name);
   const long long units = (long long)r.B * r.P * G;
   // the unit counter sits after the row count; a tree call zeroed both before
   // its path walk, a chain zeroes it here
   unsigned long long *next_unit = (unsigned long long *)((char *)rowcount + 8);
   if (!rowlist && cudaMemsetAsync(next_unit, 0, 8, st) != cudaSuccess)
-    return set_error(SV_ERR_CUDA, "row_stats: unit counter reset");
-  LaunchScope ls("row_stats", st);
-  return check_launch("row_stats",
-                      launch_pdl(row_stats_bulk_kernel<E>, dim3((unsigned)(units < g ? units : g)),
-                                 dim3(kRbThreads), smem, st, r, G, rowlist, rowcount, next_unit,
-                                 partial, qc));
+    return set_error(SV_ERR_CUDA, "%s: unit counter reset", name);
+  LaunchScope ls(name, st);
+  return check_launch(name, launch_pdl(row_pass_bulk_kernel<E, kArg>,
+                                       dim3((unsigned)(units < g ? units : g)), dim3(kRbThreads),
+                                       smem, st, r, G, rowlist, rowcount, next_unit, partial, qc));
 }
 
 // ---------------------------------------------------------------------------
@@ -1959,8 +2025,8 @@ sv_status run_verify(const Round &r, const Layout &L, char *ws, uint64_t seed, u
   } else {
     const uint64_t *rowlist = r.path ? (const uint64_t *)(ws + L.rowlist) : nullptr;
     if (r.stage && !r.copy) {
-      s = launch_row_stats_bulk<E>(r, G, rowlist, (const int *)(ws + L.ctr), partial,
-                                   (unsigned *)(ws + L.qc), st);
+      s = launch_row_pass_bulk<E, false>("row_stats", r, G, rowlist, (const int *)(ws + L.ctr),
+                                         partial, (unsigned *)(ws + L.qc), st);
     } else {
       // host-resident logits: one CTA per (row, segment); tree: B * P row
       // slots bound the listed rows, half as many CTAs per segment, each
@@ -2013,16 +2079,22 @@ sv_status run_verify_greedy(const Round &r, const Layout &L, char *ws, const Dec
   sv_status s;
   {
     const uint64_t *rowlist = r.path ? (const uint64_t *)(ws + L.rowlist) : nullptr;
-    dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
-    int nroot = 0;
-    if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
-      nroot = tree_root_ctas(r.B);
-      grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - 1), nroot)));
+    if (r.stage) {
+      s = launch_row_pass_bulk<E, true>("row_argmax", r, G, rowlist, (const int *)(ws + L.ctr),
+                                        partial, nullptr, st);
+    } else {
+      // host-resident logits: one CTA per (row, segment)
+      dim3 grid((unsigned)(r.B * r.P), (unsigned)G);
+      int nroot = 0;
+      if (rowlist) {  // tree: (segment, root CTAs + listed-row CTAs)
+        nroot = tree_root_ctas(r.B);
+        grid = dim3((unsigned)G, (unsigned)(nroot + tree_list_ctas(r.B * (r.P - 1), nroot)));
+      }
+      LaunchScope ls("row_argmax", st);
+      s = check_launch("row_argmax", launch_pdl(row_argmax_kernel<E>, grid, dim3(kRsThreads), 0,
+                                                st, r, G, rowlist, (const int *)(ws + L.ctr),
+                                                partial, nroot));
     }
-    LaunchScope ls("row_argmax", st);
-    s = check_launch("row_argmax", launch_pdl(row_argmax_kernel<E>, grid, dim3(kRsThreads), 0,
-                                              st, r, G, rowlist, (const int *)(ws + L.ctr),
-                                              partial, nroot));
     if (s != SV_OK) return s;
   }
   {
