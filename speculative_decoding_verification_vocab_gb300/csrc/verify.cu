@@ -436,34 +436,46 @@ row_pass_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
     if (tid != kRbConsumers) return;
     long long k = 0;  // stages filled so far
     bool lost = false;
-    // units are claimed from a counter shared by the grid (zeroed before the
-    // launch), so SMs that stream faster take more of them; the next claim
-    // is issued before the current unit's copies
-    long long u = (long long)atomicAdd(next_unit, 1ull), nxt = -1;
-    for (;;) {
-      if (u >= n_units && !waited) {
+    // A unit's description: its chunks' metadata, body and chunk count.
+    struct Prep {
+      RbMeta m;
+      const uint4 *ab;
+      int nw, nc;
+    };
+    auto prepare = [&](long long v, Prep &p) {
+      if (v >= n_units && !waited) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         waited = true;
         n_units += (long long)__ldcg(rowcount) * G;
       }
-      RbMeta m;
-      m.end = u >= n_units;
-      nxt = m.end ? -1 : (long long)atomicAdd(next_unit, 1ull);
-      int nc = 1, nw = 0;
-      SegInfo si;
-      if (!m.end) {
-        si = rb_unit<E>(r, G, rowlist, R0, u);
-        const E *row = (const E *)si.row;
-        m.row = si.row;
-        m.v0 = si.v0;
-        m.v1 = si.v1;
-        m.nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
-        m.ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
-        m.out = si.out;
-        nw = (int)((si.ae - si.ab) / 16);
-        nc = nw > kCW ? (nw + kCW - 1) / kCW : 1;
-      }
-      for (int c = 0; c < nc; ++c, ++k) {
+      p.m.end = v >= n_units;
+      p.nc = 1;
+      p.nw = 0;
+      p.ab = nullptr;
+      if (p.m.end) return;
+      const SegInfo si = rb_unit<E>(r, G, rowlist, R0, v);
+      const E *row = (const E *)si.row;
+      p.m.row = si.row;
+      p.m.v0 = si.v0;
+      p.m.v1 = si.v1;
+      p.m.nhead = (int)((si.ab - (uintptr_t)(row + si.v0)) / sizeof(E));
+      p.m.ntail = (int)(((uintptr_t)(row + si.v1) - si.ae) / sizeof(E));
+      p.m.out = si.out;
+      p.ab = (const uint4 *)si.ab;
+      p.nw = (int)((si.ae - si.ab) / 16);
+      p.nc = p.nw > kCW ? (p.nw + kCW - 1) / kCW : 1;
+    };
+    // Units are claimed from a counter shared by the grid (zeroed before the
+    // launch), so SMs that stream faster take more of them.  The next claim
+    // is kept one unit ahead, and a unit is described (for a listed tree row
+    // that takes a load of its list entry) while the previous unit's copies
+    // are in flight, so a released stage is refilled at once.
+    long long cu = (long long)atomicAdd(next_unit, 1ull);
+    long long na = (long long)atomicAdd(next_unit, 1ull);
+    Prep p;
+    prepare(cu, p);
+    for (;;) {
+      for (int c = 0; c < p.nc; ++c, ++k) {
         const int stage = (int)(k % kRbStages);
         const long long use = k / kRbStages;
         if (use > 0 &&
@@ -471,29 +483,31 @@ row_pass_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
           lost = true;
           break;
         }
-        sm.unit[stage] = m.end ? -1 : u;
+        sm.unit[stage] = p.m.end ? -1 : cu;
         const uint32_t full = ring_addr(&sm.full[stage]);
+        RbMeta m = p.m;
         if (m.end) {
           sm.meta[stage] = m;
           ring_arrive(full);
           continue;
         }
         m.w0 = c * kCW;
-        m.w1 = min(nw, m.w0 + kCW);
+        m.w1 = min(p.nw, m.w0 + kCW);
         m.first = c == 0;
-        m.last = c == nc - 1;
+        m.last = c == p.nc - 1;
         sm.meta[stage] = m;
         const uint32_t bytes = (uint32_t)(m.w1 - m.w0) * 16u;
         if (bytes) {
           ring_expect_tx(full, bytes);
-          ring_bulk(ring_addr(rb_stage + (size_t)stage * kCW), (const uint4 *)si.ab + m.w0, bytes,
-                    full);
+          ring_bulk(ring_addr(rb_stage + (size_t)stage * kCW), p.ab + m.w0, bytes, full);
         } else {
           ring_arrive(full);
         }
       }
-      if (lost || m.end) break;
-      u = nxt;
+      if (lost || p.m.end) break;
+      cu = na;
+      prepare(cu, p);
+      na = p.m.end ? -1 : (long long)atomicAdd(next_unit, 1ull);
     }
     // copies issued for the last kRbStages stages land before the CTA's
     // shared memory is released (at once unless a wait ran out)
@@ -505,7 +519,7 @@ row_pass_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
     }
     if (lost || *abort) {
       // a wait ran out: the units this CTA may not have finished -- those of
-      // the stages in use, the one being filled and the next one claimed --
+      // the stages in use, the one being filled and the one claimed ahead --
       // get partials marked as never computed (a finished one among them
       // only widens the report)
       if (!waited) {
@@ -517,8 +531,8 @@ row_pass_bulk_kernel(Round r, int G, const uint64_t *__restrict__ rowlist,
           partial[rb_unit<E>(r, G, rowlist, R0, v).out] = rb_lost<kArg>();
       };
       for (int i = 0; i < kRbStages && i < k; ++i) mark(sm.unit[i]);
-      mark(u);
-      mark(nxt);
+      mark(cu);
+      mark(na);
     }
     return;
   }
@@ -1151,14 +1165,14 @@ decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideO
 // owns the run of 32 consecutive elements [32 t, 32 t + 32) of a slice.  A CTA
 // is one producer warp and four consumer warps around a two-stage ring in
 // shared memory:
-//   producer   claims the next item from a counter, reads its sequence's
-//              task, issues asynchronous 16-byte copies of the slice of each
-//              row into the free stage (word k of consumer thread t at slot
-//              k * 128 + t, so consumer reads are conflict-free), and signals
-//              the stage's "full" barrier when the copies land
-//   consumers  wait for a full stage, compute the item, release the stage
-//              ("empty" barrier), store the sums, and pick a token when the
-//              item completed its sequence
+//   producer   counts the item a released stage held for its sequence (and,
+//              if that completed the sequence's pass, picks the token),
+//              claims the next item from a grid-wide counter, reads its
+//              sequence's task and starts TMA bulk copies of the slice of
+//              each row into the stage ("full" barrier, with the byte count)
+//   consumers  wait for a full stage, compute the item, store the run sums,
+//              combine the warps' slice sums (a bounded "reduced" barrier;
+//              thread 0 stores them) and release the stage ("empty" barrier)
 // Items are claimed in this order:
 //   pass 1, residual draws  exact sums of E over the slice of the q and the p
 //                           row (the accept walk lists these sequences)
@@ -1489,8 +1503,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   return v;
 }
 
-// Named barrier of the four consumer warps (the producer warp never joins).
-__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // What the producer tells the consumers about the item in a stage
 struct ItemMeta {
@@ -1505,6 +1517,7 @@ struct ItemMeta {
 
 struct SampleSmem {
   unsigned long long full[2], empty[2];  // the ring's barriers
+  unsigned long long reduced[2];         // the consumer warps' slice sums are in
   ItemMeta meta[2];
   unsigned long long red[2][2][kSpWarps];  // per stage, per sum: the warps' partial sums
   int abort;
@@ -1634,6 +1647,7 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     for (int i = 0; i < 2; ++i) {
       ring_init(ring_addr(&sm.full[i]), 1);            // the producer's arrival (+ bytes)
       ring_init(ring_addr(&sm.empty[i]), kSpThreads);  // every consumer, results stored
+      ring_init(ring_addr(&sm.reduced[i]), kSpWarps);   // lane 0 of every consumer warp
       sm.meta[i].kind = -1;
     }
     sm.abort = 0;
@@ -1767,6 +1781,8 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     if (m.kind < 0) break;
     const int b = m.b, s = m.s;
     if (m.kind == 2 && !m.ok) {
+      // nothing computed; both barriers still complete their phase for it
+      if ((tid & 31) == 0) ring_arrive(ring_addr(&sm.reduced[slot]));
       ring_arrive(ring_addr(&sm.empty[slot]));
       continue;
     }
@@ -1792,8 +1808,20 @@ sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o)
     if ((tid & 31) == 0) {
       sm.red[slot][0][tid >> 5] = f0;
       sm.red[slot][1][tid >> 5] = f1;
+      ring_arrive(ring_addr(&sm.reduced[slot]));
     }
-    csync();
+    // warps 1-3 release the stage now (their stores precede the arrival);
+    // warp 0 once thread 0 has combined the warps' sums (a bounded wait on
+    // the stage's "reduced" barrier), so that no warp writes them for a
+    // later item first
+    if (tid >= 32) {
+      ring_arrive(ring_addr(&sm.empty[slot]));
+      continue;
+    }
+    if (!ring_wait(ring_addr(&sm.reduced[slot]), (n >> 1) & 1, abort)) {
+      if (tid == 0) atomicOr(o.status + b, SV_ROW_TIMEOUT);
+      break;
+    }
     if (tid == 0) {
       unsigned long long a0 = 0, a1 = 0;
       for (int w = 0; w < kSpWarps; ++w) {
