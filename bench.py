@@ -74,6 +74,8 @@ def parse():
     ap.add_argument("--early-exit", action="store_true",
                     help="chain configs: sv_verify_chain_early_exit (rows after a sequence's "
                          "first rejection are not read once it is known)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="config 5 only: leave out the large-vocabulary chain lines")
     ap.add_argument("--batch", type=int, default=0,
                     help="per-GPU batch override (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -347,7 +349,8 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     line = measure(args, rank, world, local)
-    if args.config == 5 and not (args.greedy or args.early_exit or args.graph or args.batch):
+    if args.config == 5 and not (args.greedy or args.early_exit or args.graph or args.batch or
+                                 args.no_secondary):
         line["secondary"] = secondary(args, rank, world, local)
     if rank == 0:
         print(json.dumps(line))
