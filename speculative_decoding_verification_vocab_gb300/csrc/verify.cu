@@ -27,7 +27,8 @@ namespace sv {
 namespace {
 
 constexpr int kDecideWarps = 4;
-constexpr int kSpSlice = 4096;  // sampler: elements of a row per work item
+constexpr int kSpSlice = 4096;   // sampler: elements of a row per work item
+constexpr int kSpThreads = 128;  // sampler: consumer threads (the producer warp is extra)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Task {
@@ -669,7 +670,7 @@ Layout plan(int B, int maxpos, int V, bool tree) {
   L.task = take(sizeof(Task) * (size_t)B);
   L.NS = (V + kSpSlice - 1) / kSpSlice;
   L.slice = take(sizeof(unsigned long long) * 3 * (size_t)B * L.NS);
-  L.runs = take(sizeof(unsigned long long) * (size_t)B * L.NS * 128);
+  L.runs = take(sizeof(unsigned long long) * (size_t)B * L.NS * kSpThreads);
   L.done = take(sizeof(unsigned) * 2 * (size_t)B);
   L.rlist = take(sizeof(int) * 2 * (size_t)B);
   L.qc = take(sizeof(unsigned) * 4);
@@ -1188,7 +1189,6 @@ decide_greedy_kernel(Round r, int G, const float4 *__restrict__ partial, DecideO
 // bounded by a wall-clock limit; one that runs out sets SV_ROW_TIMEOUT for
 // the sequence concerned and the CTA stops taking items.
 
-constexpr int kSpThreads = 128;  // consumer threads (the producer warp is extra)
 constexpr int kSpWarps = kSpThreads / 32;
 template <typename E>
 __host__ __device__ constexpr int sp_per() { return 16 / (int)sizeof(E); }  // elements per word
