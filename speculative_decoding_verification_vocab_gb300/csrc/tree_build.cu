@@ -202,16 +202,14 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   const int nv = (int)((ae - ab) / 16);
   const int ntail = (int)((pe - ae) / sizeof(E));
   int i = tid;
-  bool seeded = false;
   constexpr int kStep = kRsUnroll * kExThreads;
   // warp-uniform trip count (the warp's offers are warp-wide collectives):
   // i - lane is the warp's first word of the batch.  The warp's last batch
   // may run past the row's body: those words read as -inf (nothing added to
   // the sums, never offered)
   const uint32_t ninf = sizeof(E) == 2 ? 0xFF80FF80u : 0xFF800000u;
-  for (; i - lane < nv; i += kStep) {
-    uint4 buf[kRsUnroll];
-    unsigned inb = 0xffu;  // words of the batch inside the body
+  auto load = [&](uint4 (&buf)[kRsUnroll], unsigned &inb) {
+    inb = 0xffu;  // words of the batch inside the body
     if ((i - lane) + 31 + (kRsUnroll - 1) * kExThreads < nv) {
 #pragma unroll
       for (int j = 0; j < kRsUnroll; ++j) buf[j] = ld_stream_v4(body + i + j * kExThreads);
@@ -223,19 +221,32 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
         if (!in) inb &= ~(1u << j);
       }
     }
-    const float bm = stat_batch<E>(buf, st, k);  // the batch maximum
-    int skip = -1;
-    if (!seeded && w.ti == 0x7fffffff) {  // list still empty: seed it from this batch
-      skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
-      seeded = true;
-    }
-    // one gate per batch: the words are looked at only when some lane's
-    // batch maximum reaches the list's K-th value
+  };
+  // one gate per batch: the words are looked at only when some lane's batch
+  // maximum reaches the list's K-th value
+  auto offer = [&](const uint4 (&buf)[kRsUnroll], unsigned inb, float bm, int skip) {
     if (__any_sync(0xffffffffu, bm >= w.tv))
 #pragma unroll
       for (int j = 0; j < kRsUnroll; ++j)
         warp_offer_words<E>(w, buf[j], nhead + (i + j * kExThreads) * kPer, (inb >> j) & 1u, K,
                             skip);
+  };
+  // the first batch seeds the empty list (peeled off, so that the seeding
+  // code stays out of the streaming loop)
+  if (i - lane < nv) {
+    uint4 buf[kRsUnroll];
+    unsigned inb;
+    load(buf, inb);
+    const float bm = stat_batch<E>(buf, st, k);  // the batch maximum
+    const int skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
+    offer(buf, inb, bm, skip);
+    i += kStep;
+  }
+  for (; i - lane < nv; i += kStep) {
+    uint4 buf[kRsUnroll];
+    unsigned inb;
+    load(buf, inb);
+    offer(buf, inb, stat_batch<E>(buf, st, k), -1);
   }
   // ragged head and tail elements (fewer than 8 each), by warp 0, offered
   // after the body so that seeding (which replaces an empty list) cannot
