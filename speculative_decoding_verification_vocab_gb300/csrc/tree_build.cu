@@ -85,17 +85,18 @@ __device__ __forceinline__ float word_elem(uint4 w, int j) {
 // of the lane already in the list (-1: none)
 template <typename E>
 __device__ __forceinline__ void warp_offer_words(WarpTopK &w, uint4 word, int v, bool in, int K,
-                                                 int skip = -1) {
+                                                 int skip, float floor_v) {
   constexpr int kPer = 16 / (int)sizeof(E);
   const unsigned FULL = 0xffffffffu;
   const float m = in ? word_max<E>(word) : -INFINITY;
   // the lane marks the elements of its word that can reach the list
   unsigned emask = 0u;
-  if (in && m >= w.tv) {
+  const float gate = fmaxf(w.tv, floor_v);
+  if (in && m >= gate) {
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const float x = word_elem<E>(word, j);
-      if (x >= w.tv && v + j != skip) emask |= 1u << j;  // NaN fails the compare
+      if (x >= gate && v + j != skip) emask |= 1u << j;  // NaN fails the compare
     }
   }
   unsigned cand = __ballot_sync(FULL, emask != 0u);
@@ -201,6 +202,25 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   const uint4 *body = (const uint4 *)ab;
   const int nv = (int)((ae - ab) / 16);
   const int ntail = (int)((pe - ae) / sizeof(E));
+  // The largest K-th value of any warp's list bounds the row's final K-th
+  // value from below, so every warp may drop elements under it: kept in
+  // shared memory as an order-preserving integer key, raised by each warp's
+  // lane 0 whenever its full list's K-th value rises.
+  __shared__ unsigned s_floor;
+  if (tid == 0) s_floor = 0u;  // below every float's key
+  __syncthreads();
+  auto fkey = [](float x) {
+    const unsigned u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  };
+  auto raise_floor = [&]() {
+    if (lane == 0 && w.ti != 0x7fffffff) atomicMax(&s_floor, fkey(w.tv));
+  };
+  auto floor_v = [&]() {
+    const unsigned kk = *(volatile unsigned *)&s_floor;
+    if (kk == 0u) return -INFINITY;
+    return __uint_as_float((kk & 0x80000000u) ? (kk & 0x7fffffffu) : ~kk);
+  };
   int i = tid;
   constexpr int kStep = kRsUnroll * kExThreads;
   // warp-uniform trip count (the warp's offers are warp-wide collectives):
@@ -225,11 +245,15 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
   // one gate per batch: the words are looked at only when some lane's batch
   // maximum reaches the list's K-th value
   auto offer = [&](const uint4 (&buf)[kRsUnroll], unsigned inb, float bm, int skip) {
-    if (__any_sync(0xffffffffu, bm >= w.tv))
+    const float fl = __shfl_sync(0xffffffffu, floor_v(), 0);  // one read per warp and batch
+    if (__any_sync(0xffffffffu, bm >= fmaxf(w.tv, fl))) {
+      const float tv0 = w.tv;
 #pragma unroll
       for (int j = 0; j < kRsUnroll; ++j)
         warp_offer_words<E>(w, buf[j], nhead + (i + j * kExThreads) * kPer, (inb >> j) & 1u, K,
-                            skip);
+                            skip, fl);
+      if (w.tv != tv0) raise_floor();
+    }
   };
   // the first batch seeds the empty list (peeled off, so that the seeding
   // code stays out of the streaming loop)
@@ -239,6 +263,7 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
     load(buf, inb);
     const float bm = stat_batch<E>(buf, st, k);  // the batch maximum
     const int skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
+    raise_floor();
     offer(buf, inb, bm, skip);
     i += kStep;
   }
