@@ -128,6 +128,9 @@ def test_noalloc_capacity_and_argument_order(lib):
     cap = lib.sv_verify_chain_noalloc_max_bytes()
     assert cap == 16 << 20
     assert lib.sv_verify_chain_workspace(256, 7, 128256) <= cap
+    # the limit the documentation states: up to B = 447 at N = 7, V = 128256
+    assert lib.sv_verify_chain_workspace(447, 7, 128256) <= cap
+    assert lib.sv_verify_chain_workspace(448, 7, 128256) > cap
     null = None
     args = lambda B, N, V, dt=1, T=1.0: (null, null, dt, null, B, N, V, T, 0, 0, null, null, null,
                                          null, null, null, null, null)
