@@ -255,9 +255,35 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
       if (w.tv != tv0) raise_floor();
     }
   };
+  // After the seeding round the CTA ranks the union of the warps' lists (the
+  // entries are distinct elements of the row, so their K-th is a lower bound
+  // on the row's final K-th value) and raises the floor to it: a much
+  // tighter bound than any one warp's K-th.  Every thread takes part, so the
+  // rounds are counted for the whole CTA (a warp past the row's body reads
+  // -inf words).  Once is enough: ranking again after later rounds costs
+  // more (two barriers each) than the tighter floor saves.
+  __shared__ float s_lv[kExWarps * kMaxK];
+  __shared__ int s_li[kExWarps * kMaxK];
+  auto cta_floor = [&]() {
+    if (lane < K) {
+      s_lv[warp * K + lane] = w.v;
+      s_li[warp * K + lane] = w.i;
+    }
+    __syncthreads();
+    if (tid < kExWarps * K && s_li[tid] != 0x7fffffff) {
+      const float x = s_lv[tid];
+      const int id = s_li[tid];
+      int rank = 0;
+      for (int e = 0; e < kExWarps * K; ++e)
+        rank += (s_li[e] != 0x7fffffff && tk_before(s_lv[e], s_li[e], x, id));
+      if (rank == K - 1) atomicMax(&s_floor, fkey(x));
+    }
+    __syncthreads();  // the lists are rewritten only after every rank is taken
+  };
+  const int rounds = (nv + kStep - 1) / kStep;  // batch rounds of the whole CTA
   // the first batch seeds the empty list (peeled off, so that the seeding
   // code stays out of the streaming loop)
-  if (i - lane < nv) {
+  if (rounds > 0) {
     uint4 buf[kRsUnroll];
     unsigned inb;
     load(buf, inb);
@@ -265,9 +291,10 @@ tree_expand_kernel(const E *__restrict__ dlog, int V, float k, int greedy,
     const int skip = warp_seed<E>(w, buf, nhead + i * kPer, kExThreads * kPer, K);
     raise_floor();
     offer(buf, inb, bm, skip);
+    if (rounds > 1) cta_floor();
     i += kStep;
   }
-  for (; i - lane < nv; i += kStep) {
+  for (int r = 1; r < rounds; ++r, i += kStep) {
     uint4 buf[kRsUnroll];
     unsigned inb;
     load(buf, inb);
