@@ -797,6 +797,13 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   const int lane = threadIdx.x & 31;
   if (b >= r.B) return;
   const unsigned FULL = 0xffffffffu;
+  // the first chunk's draft token and path node, loaded beside the path
+  // length instead of after it (in bounds whatever the length)
+  int d_pf = 0, n_pf = lane;
+  if (lane < r.maxpos) {
+    d_pf = r.tok[(size_t)b * r.tok_stride + lane];
+    if (r.path) n_pf = r.path[(size_t)b * (r.maxpos + 1) + lane];
+  }
   const int npos = round_npos(r, b);
   const uint32_t tree_bad = r.tstat ? r.tstat[b] : 0u;
   const float4 *pb = partial + (size_t)b * r.P * G;
@@ -810,23 +817,16 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
   uint32_t bad = 0, pzero_bits = 0, acc_bits = 0;
   // early exit: per chunk, this lane's position faults (row / token)
   uint32_t nan_bits = 0, tokbad_bits = 0;
-  // bonus row (verifier row of position npos) is checked by lane 0
-  if (lane == 0 && !tree_bad) {
-    float mx, mk, s;
-    if (merge_slot(pb + (size_t)npos * G, G, mx, mk, s)) bad |= SV_ROW_TIMEOUT;
-    if (!(s > 0.0f)) bad |= SV_ROW_NAN;
-    mxv[npos] = mx;
-    usm[npos] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)npos, kDrawSample);
-  }
-  const uint32_t bonus_bad = kEarly ? __shfl_sync(FULL, bad, 0) : 0u;
-  if (kEarly) bad = 0;
   const int nchunks = (npos + 31) / 32;
   for (int c = 0; c < nchunks && !tree_bad; ++c) {
     const int i = c * 32 + lane;
     if (i >= npos) break;
-    const int d = r.tok[(size_t)b * r.tok_stride + i];  // issued first: x_d depends on it
-    const E *vrow = used_row<E>(r, b, i, src_row<E>(r, b, i));
-    const E *drow = used_row<E>(r, b, r.maxpos + 1 + i, src_row<E>(r, b, r.maxpos + 1 + i));
+    // issued first: x_d depends on them
+    const int d = c == 0 ? d_pf : r.tok[(size_t)b * r.tok_stride + i];
+    const int node = c == 0 ? n_pf : round_node(r, b, i);
+    const E *vrow = used_row<E>(r, b, i, (const E *)r.vlog + ((size_t)b * r.v_rows + node) * r.V);
+    const E *drow = used_row<E>(r, b, r.maxpos + 1 + i,
+                                (const E *)r.dlog + ((size_t)b * r.d_rows + node) * r.V);
     const Judged J = judge_position<E, false>(r, G, pb, b, i, d, vrow, drow, seed, step);
     mxv[i] = J.mxq;
     mxd[i] = J.mxp;
@@ -844,6 +844,18 @@ decide_kernel(Round r, int G, const float4 *__restrict__ partial, uint64_t seed,
     if (o.p_prob) o.p_prob[(size_t)b * r.maxpos + i] = J.pd;
     if (o.margin) o.margin[(size_t)b * (r.maxpos + 1) + i] = J.rc - (float)J.u24 * 0x1p-24f;
   }
+  // bonus row (verifier row of position npos), checked by lane 0 after the
+  // positions (its results are needed only from here on)
+  uint32_t bonus_bits = 0;
+  if (lane == 0 && !tree_bad) {
+    float mx, mk, s;
+    if (merge_slot(pb + (size_t)npos * G, G, mx, mk, s)) bonus_bits |= SV_ROW_TIMEOUT;
+    if (!(s > 0.0f)) bonus_bits |= SV_ROW_NAN;
+    mxv[npos] = mx;
+    usm[npos] = uniform_u24(seed, step, (uint32_t)b, (uint32_t)npos, kDrawSample);
+  }
+  const uint32_t bonus_bad = kEarly ? __shfl_sync(FULL, bonus_bits, 0) : 0u;
+  if (!kEarly) bad |= bonus_bits;
   bad = __reduce_or_sync(FULL, bad);
   if (tree_bad) bad = SV_ROW_BAD_TREE;
 
