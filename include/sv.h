@@ -73,7 +73,7 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_ROW_P_ZERO 8u     /* a tested draft token had p(d) = 0 (draft logit -inf) and was accepted */
 #define SV_ROW_BAD_TREE 16u  /* parent/score arrays do not describe a tree */
 #define SV_ROW_BAD_BASE 32u  /* sv_tree_attention: base < 0 or base + T > S */
-#define SV_ROW_TIMEOUT 64u   /* a bounded wait on the device ran out (attention, sampling) */
+#define SV_ROW_TIMEOUT 64u   /* a bounded wait on the device ran out (row pass, sampling, attention) */
 
 /* Build limits. */
 #define SV_MAX_VOCAB (1 << 22)  /* fixed-point sampling sums stay below 2^63 */
@@ -124,9 +124,11 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  * draw from q (the bonus, or a zero residual) takes the weights
  * floor(e_v 2^40), e_v = exp(x_v / T - max_v x_v / T) in that arithmetic; a
  * residual takes floor(max(0, q_v - p_v) 2^62) with q, p normalised by those
- * sums.  The sampler's device waits are bounded; one that runs out (which a
- * working device never does) sets SV_ROW_TIMEOUT for the sequence and leaves
- * its correction/bonus token at -1.
+ * sums.  The row pass's and the sampler's device waits are bounded; one that
+ * runs out (which a working device never does) sets SV_ROW_TIMEOUT for the
+ * sequences concerned: a row-pass segment it left unread also faults the
+ * sequence as SV_ROW_NAN (accept_len 0, tokens -1); a sampler wait leaves
+ * the correction/bonus token at -1.
  * --------------------------------------------------------------------------- */
 size_t sv_verify_chain_workspace(int B, int N, int V);
 /* A larger workspace for logits in page-locked host memory: with it, every
