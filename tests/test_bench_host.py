@@ -101,3 +101,40 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+_SECONDARY_KEYS = ("value", "unit", "steps", "ms_per_step", "accepted_tokens_per_s",
+                   "mean_accept_len", "rows_read_per_s", "hbm_gbs", "hbm_frac_measured",
+                   "roofline", "kernels", "repeats", "clocks", "alg_bytes_per_step", "config")
+
+
+def test_secondary_lines_only_on_the_default_run(monkeypatch, capsys):
+    """The default run (config 5) adds the large-vocabulary chain's full and
+    early-exit lines, each over at least SECONDARY_STEPS device-resident
+    steps; a flag that changes the workload, or --no-secondary, leaves them
+    out."""
+    import json
+    import torch
+    calls = []
+
+    def fake_measure(a, rank, world, local):
+        calls.append((a.config, a.early_exit, a.steps, a.no_e2e, a.no_cpu_baseline))
+        return {k: a.config for k in _SECONDARY_KEYS}
+
+    monkeypatch.setattr(bench, "measure", fake_measure)
+    monkeypatch.setattr(torch.cuda, "set_device", lambda *a, **k: None)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "7"])
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert calls == [(5, False, 7, False, False),
+                     (3, False, bench.SECONDARY_STEPS, True, True),
+                     (3, True, bench.SECONDARY_STEPS, True, True)]
+    assert sorted(line["secondary"]) == ["config 3: large_vocab_chain",
+                                         "config 3: large_vocab_chain (early exit)"]
+    assert all(set(v) == set(_SECONDARY_KEYS) for v in line["secondary"].values())
+    for extra in (["--no-secondary"], ["--greedy"], ["--config", "3"]):
+        calls.clear()
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--steps", "7", *extra])
+        bench.main()
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert len(calls) == 1 and "secondary" not in line, extra
