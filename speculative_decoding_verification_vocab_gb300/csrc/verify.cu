@@ -1647,8 +1647,10 @@ __device__ __forceinline__ void finish_item(const Round &r, const ItemMeta &m, c
     pick_token_warp<E>(r, m, m.b, sw, sw.slice + (size_t)m.b * sw.NS, true, true, o);
 }
 
+// bf16: five CTAs per SM (at most 72 registers, no spills) keep more
+// consumer warps resident than four; fp32 would spill at that cap
 template <typename E>
-__global__ void __launch_bounds__(kSpThreads + 32)
+__global__ void __launch_bounds__(kSpThreads + 32, sizeof(E) == 2 ? 5 : 4)
 sample_kernel(Round r, const Task *__restrict__ tasks, SampleWs sw, DecideOut o) {
   grid_dep_sync();
   extern __shared__ __align__(128) uint4 stage_sm[];  // [2 stages][q, p][words]
