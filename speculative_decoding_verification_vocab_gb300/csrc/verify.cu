@@ -111,8 +111,8 @@ __device__ __forceinline__ const E *used_row(const Round &r, int b, int j, const
 constexpr int kSegElems = 8192;  // smallest segment (fp32); sizes the workspace
 constexpr int kRsThreads = 128;
 // A segment is 32 KB: 2 * kRsUnroll 16-byte words for each of 128 threads.
-// (The early-exit and arg-max passes still take one segment per CTA, half of
-// each thread's words staged into shared memory by cp.async.)
+// (The early-exit pass, and every pass over host-resident logits, take one
+// segment per CTA with plain 16-byte loads.)
 template <typename E>
 __host__ __device__ constexpr int seg_elems() {
   return kRsThreads * 2 * kRsUnroll * 16 / (int)sizeof(E);
